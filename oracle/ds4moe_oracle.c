@@ -1,0 +1,358 @@
+/*
+ * CPU oracle for the routed mixture-of-experts FFN layer.
+ *
+ * TEST INFRASTRUCTURE ONLY. Nothing on the product path may call, link or
+ * execute this file; only the test suite, the smoke check and the benchmark's
+ * CPU-baseline leg use it. It shares no code with the CUDA library.
+ *
+ * It is a plain, slow, obviously correct restatement of what the layer
+ * computes, in IEEE binary64 throughout:
+ *
+ *   logits   L[t,e] = sum_h x[t,h] * Wr[e,h]
+ *   scores   s = sigmoid(L),  selection score sel = s + b_e  (b = 0 without a bias)
+ *   routing  the top_k experts by sel (descending; equal scores -> lower index),
+ *            weights w_k = s_{e_k} / sum_j s_{e_j}
+ *   experts  g = Wg[e] x,  u = Wu[e] x,  h = silu(g) * u,  ye = Wd[e] h
+ *   shared   ysh = Wd_sh (silu(Wg_sh x) * (Wu_sh x))
+ *   output   y[t] = sum_k w_k * ye_k + ysh
+ *
+ * Sources. The block sum "y = sum_k rw_k (s_e * ye_k) + ysh" with an unweighted
+ * shared expert is the engine's MoE sum in "YoungAi - DeepSeek V4.1 Flash on
+ * one DGX Spark", section 4.2 ("The objective"); without a sidecar s_e = 1.
+ * The bias enters the selection score only and leaves the mixing weights
+ * untouched (same page, section 3 and section 4.2, "The router bias").
+ * 384 experts with 6 chosen per token: same page, section 2.2. Only routed
+ * experts are 2-bit; the shared expert stays 8-bit ("Running DeepSeek V4
+ * Flash on an RTX 5080 ...", model list: "up/gate at IQ2_XXS, down at Q2_K",
+ * shared experts left untouched; the quant recipe "...-SExpQ8-..." on the
+ * txtmix.com ds4 teardown, section 3). Sigmoid scoring with renormalised
+ * weights, SwiGLU experts and the exact block formats are part of the layer's
+ * workload definition; the pages do not spell them out.
+ *
+ * Precision of decisions: the expert choice is an integer decided by floating
+ * point, so it is taken on the fp32 rounding of the exact selection score, the
+ * precision the CUDA kernels decide in. The gap between the k-th and (k+1)-th
+ * fp32 selection score is reported so callers can flag near-ties.
+ *
+ * Storage formats (little-endian):
+ *   2-bit block, 84 bytes per 256 consecutive weights of one row:
+ *     scales[16] (low nibble = scale sc_j, high nibble = min m_j of sub-block j
+ *     of 16 weights), qs[64] (code q_i of weight i at byte i/4, bits 2*(i%4)),
+ *     d (binary16), dmin (binary16);   w_i = d * sc_j * q_i - dmin * m_j.
+ *   8-bit block, 34 bytes per 32 consecutive weights: d (binary16), 32 int8
+ *     codes;   w_i = d * q_i.
+ *   Routed gate/up [E][I][H/256] blocks, down [E][H][I/256]; shared gate/up
+ *   [I_sh][H/32], shared down [H][I_sh/32]; router fp32 [E][H]; x bf16 [T][H].
+ */
+#include <math.h>
+#include <omp.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+typedef struct {
+    int32_t hidden;       /* H */
+    int32_t inter;        /* I, routed intermediate */
+    int32_t n_experts;    /* E */
+    int32_t top_k;        /* K */
+    int32_t shared_inter; /* I_sh, 0 = no shared expert */
+} oracle_shape;
+
+enum { Q2_BYTES = 84, Q8_BYTES = 34 };
+
+/* IEEE binary16 -> double: sign, 5-bit exponent (bias 15), 10-bit fraction. */
+double oracle_f16(uint16_t h)
+{
+    int sign = (h >> 15) & 1;
+    int e = (h >> 10) & 31;
+    int m = h & 1023;
+    double v;
+    if (e == 0)
+        v = ldexp((double)m, -24); /* subnormal: m * 2^-24 */
+    else if (e == 31)
+        v = m ? NAN : INFINITY;
+    else
+        v = ldexp((double)(1024 + m), e - 25); /* (1 + m/1024) * 2^(e-15) */
+    return sign ? -v : v;
+}
+
+/* bfloat16 -> double: sign, 8-bit exponent (bias 127), 7-bit fraction. */
+double oracle_bf16(uint16_t b)
+{
+    int sign = (b >> 15) & 1;
+    int e = (b >> 7) & 255;
+    int m = b & 127;
+    double v;
+    if (e == 0)
+        v = ldexp((double)m, -133); /* subnormal: m * 2^-133 */
+    else if (e == 255)
+        v = m ? NAN : INFINITY;
+    else
+        v = ldexp((double)(128 + m), e - 134); /* (1 + m/128) * 2^(e-127) */
+    return sign ? -v : v;
+}
+
+static uint16_t le16(const uint8_t *p) { return (uint16_t)(p[0] | (p[1] << 8)); }
+
+/* One 2-bit block -> 256 weights. */
+void oracle_dequant_q2(const uint8_t *blk, double *w)
+{
+    const uint8_t *scales = blk;
+    const uint8_t *qs = blk + 16;
+    double d = oracle_f16(le16(blk + 80));
+    double dmin = oracle_f16(le16(blk + 82));
+    for (int i = 0; i < 256; i++) {
+        int j = i / 16;
+        int sc = scales[j] & 15;
+        int m = scales[j] >> 4;
+        int q = (qs[i / 4] >> (2 * (i % 4))) & 3;
+        w[i] = d * sc * q - dmin * m;
+    }
+}
+
+/* One 8-bit block -> 32 weights. */
+void oracle_dequant_q8(const uint8_t *blk, double *w)
+{
+    double d = oracle_f16(le16(blk));
+    for (int i = 0; i < 32; i++)
+        w[i] = d * (double)(int8_t)blk[2 + i];
+}
+
+/* A row of k weights stored as k/256 2-bit blocks (or k/32 8-bit blocks). */
+void oracle_dequant_q2_row(const uint8_t *row, int64_t k, double *w)
+{
+    for (int64_t b = 0; b < k / 256; b++)
+        oracle_dequant_q2(row + b * Q2_BYTES, w + b * 256);
+}
+
+void oracle_dequant_q8_row(const uint8_t *row, int64_t k, double *w)
+{
+    for (int64_t b = 0; b < k / 32; b++)
+        oracle_dequant_q8(row + b * Q8_BYTES, w + b * 32);
+}
+
+static double dot(const double *a, const double *b, int64_t n)
+{
+    double acc = 0.0;
+    for (int64_t i = 0; i < n; i++)
+        acc += a[i] * b[i];
+    return acc;
+}
+
+/* Threads the oracle uses when not told otherwise. */
+int32_t oracle_max_threads(void) { return omp_get_max_threads(); }
+
+double oracle_silu(double z) { return z / (1.0 + exp(-z)); }
+
+double oracle_sigmoid(double z) { return 1.0 / (1.0 + exp(-z)); }
+
+/* ---- routing ------------------------------------------------------------ */
+
+typedef struct {
+    float sel;
+    int32_t e;
+} scored;
+
+static int by_score_then_index(const void *pa, const void *pb)
+{
+    const scored *a = (const scored *)pa, *b = (const scored *)pb;
+    if (a->sel > b->sel) return -1;
+    if (a->sel < b->sel) return 1;
+    return (a->e > b->e) - (a->e < b->e);
+}
+
+/* Exact logits L[T][E] = x Wr^T (bf16 x, fp32 Wr, binary64 sums). */
+int oracle_logits(const oracle_shape *s, const float *router_w, const uint16_t *x, int32_t T, double *logits)
+{
+    const int H = s->hidden, E = s->n_experts;
+    if (H <= 0 || E <= 0 || T < 0)
+        return -1;
+#pragma omp parallel for schedule(static)
+    for (int32_t t = 0; t < T; t++) {
+        double *xt = (double *)malloc(sizeof(double) * H);
+        for (int h = 0; h < H; h++)
+            xt[h] = oracle_bf16(x[(int64_t)t * H + h]);
+        for (int e = 0; e < E; e++) {
+            double L = 0.0;
+            for (int h = 0; h < H; h++)
+                L += xt[h] * (double)router_w[(int64_t)e * H + h];
+            logits[(int64_t)t * E + e] = L;
+        }
+        free(xt);
+    }
+    return 0;
+}
+
+/*
+ * Selection from exact logits. Outputs (any may be NULL except idx):
+ *   idx[T][K]     chosen experts in descending selection score
+ *   weights[T][K] renormalised sigmoid scores of the chosen experts
+ *   gap[T]        fp32 score of the K-th minus the (K+1)-th choice (+inf if K == E)
+ *   sel[T][E]     fp32 selection scores the decision was taken on
+ */
+int oracle_select(const oracle_shape *s, const double *logits, const float *router_bias, int32_t T,
+                  int32_t *idx, double *weights, double *gap, float *sel_out)
+{
+    const int E = s->n_experts, K = s->top_k;
+    if (E <= 0 || K <= 0 || K > E || T < 0)
+        return -1;
+#pragma omp parallel for schedule(static)
+    for (int32_t t = 0; t < T; t++) {
+        double *score = (double *)malloc(sizeof(double) * E);
+        scored *order = (scored *)malloc(sizeof(scored) * E);
+        for (int e = 0; e < E; e++) {
+            score[e] = oracle_sigmoid(logits[(int64_t)t * E + e]);
+            double selection = score[e] + (router_bias ? (double)router_bias[e] : 0.0);
+            order[e].sel = (float)selection;
+            order[e].e = e;
+            if (sel_out)
+                sel_out[(int64_t)t * E + e] = order[e].sel;
+        }
+        qsort(order, (size_t)E, sizeof(scored), by_score_then_index);
+        double total = 0.0;
+        for (int k = 0; k < K; k++)
+            total += score[order[k].e];
+        for (int k = 0; k < K; k++) {
+            idx[(int64_t)t * K + k] = order[k].e;
+            if (weights)
+                weights[(int64_t)t * K + k] = total > 0.0 ? score[order[k].e] / total : 1.0 / K;
+        }
+        if (gap)
+            gap[t] = (K < E) ? (double)order[K - 1].sel - (double)order[K].sel : INFINITY;
+        free(score);
+        free(order);
+    }
+    return 0;
+}
+
+/* Route T tokens: logits, then selection. logits_out may be NULL. */
+int oracle_route(const oracle_shape *s, const float *router_w, const float *router_bias,
+                 const uint16_t *x, int32_t T, int32_t *idx, double *weights, double *gap,
+                 double *logits_out, float *sel_out)
+{
+    const int E = s->n_experts, K = s->top_k;
+    if (s->hidden <= 0 || E <= 0 || K <= 0 || K > E || T < 0)
+        return -1;
+    double *logits = logits_out ? logits_out : (double *)malloc(sizeof(double) * ((size_t)T * E + 1));
+    int rc = oracle_logits(s, router_w, x, T, logits);
+    if (rc == 0)
+        rc = oracle_select(s, logits, router_bias, T, idx, weights, gap, sel_out);
+    if (!logits_out)
+        free(logits);
+    return rc;
+}
+
+/* ---- experts ------------------------------------------------------------ */
+
+/* One routed expert on one token: ye[H] = Wd (silu(Wg x) * (Wu x)). */
+void oracle_expert_q2(const oracle_shape *s, const uint8_t *gate_e, const uint8_t *up_e,
+                      const uint8_t *down_e, const double *xt, double *ye)
+{
+    const int H = s->hidden, I = s->inter;
+    const int64_t gate_row = (int64_t)(H / 256) * Q2_BYTES, down_row = (int64_t)(I / 256) * Q2_BYTES;
+    double *w = (double *)malloc(sizeof(double) * (H > I ? H : I));
+    double *h = (double *)malloc(sizeof(double) * I);
+    for (int i = 0; i < I; i++) {
+        oracle_dequant_q2_row(gate_e + i * gate_row, H, w);
+        double g = dot(w, xt, H);
+        oracle_dequant_q2_row(up_e + i * gate_row, H, w);
+        double u = dot(w, xt, H);
+        h[i] = oracle_silu(g) * u;
+    }
+    for (int j = 0; j < H; j++) {
+        oracle_dequant_q2_row(down_e + j * down_row, I, w);
+        ye[j] = dot(w, h, I);
+    }
+    free(w);
+    free(h);
+}
+
+/* The shared expert on one token: ysh[H]. */
+void oracle_shared_q8(const oracle_shape *s, const uint8_t *sh_gate, const uint8_t *sh_up,
+                      const uint8_t *sh_down, const double *xt, double *ysh)
+{
+    const int H = s->hidden, I = s->shared_inter;
+    const int64_t gate_row = (int64_t)(H / 32) * Q8_BYTES, down_row = (int64_t)(I / 32) * Q8_BYTES;
+    double *w = (double *)malloc(sizeof(double) * (H > I ? H : I));
+    double *h = (double *)malloc(sizeof(double) * I);
+    for (int i = 0; i < I; i++) {
+        oracle_dequant_q8_row(sh_gate + i * gate_row, H, w);
+        double g = dot(w, xt, H);
+        oracle_dequant_q8_row(sh_up + i * gate_row, H, w);
+        double u = dot(w, xt, H);
+        h[i] = oracle_silu(g) * u;
+    }
+    for (int j = 0; j < H; j++) {
+        oracle_dequant_q8_row(sh_down + j * down_row, I, w);
+        ysh[j] = dot(w, h, I);
+    }
+    free(w);
+    free(h);
+}
+
+/*
+ * The layer output for given routing: y[T][H] = sum_k weights[t,k] ye_{idx[t,k]} + ysh.
+ * ysh is skipped when shared_inter == 0 or the shared pointers are NULL.
+ * Tokens are independent and each row is computed by one thread in a fixed
+ * order, so the result does not depend on nthreads (<= 0: library default).
+ */
+int oracle_forward_routed(const oracle_shape *s, const uint8_t *gate, const uint8_t *up,
+                          const uint8_t *down, const uint8_t *sh_gate, const uint8_t *sh_up,
+                          const uint8_t *sh_down, const uint16_t *x, int32_t T, const int32_t *idx,
+                          const double *weights, double *y, int32_t nthreads)
+{
+    const int H = s->hidden, I = s->inter, E = s->n_experts, K = s->top_k;
+    if (H <= 0 || I <= 0 || H % 256 || I % 256 || K <= 0 || K > E || T < 0)
+        return -1;
+    const int has_shared = s->shared_inter > 0 && sh_gate && sh_up && sh_down;
+    if (has_shared && s->shared_inter % 32)
+        return -1;
+    for (int64_t p = 0; p < (int64_t)T * K; p++)
+        if (idx[p] < 0 || idx[p] >= E)
+            return -1;
+    const int64_t expert_gate = (int64_t)I * (H / 256) * Q2_BYTES;
+    const int64_t expert_down = (int64_t)H * (I / 256) * Q2_BYTES;
+    const int nt = nthreads > 0 ? nthreads : omp_get_max_threads();
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nt)
+    for (int32_t t = 0; t < T; t++) {
+        double *xt = (double *)malloc(sizeof(double) * H);
+        double *ye = (double *)malloc(sizeof(double) * H);
+        double *acc = (double *)calloc((size_t)H, sizeof(double));
+        for (int h = 0; h < H; h++)
+            xt[h] = oracle_bf16(x[(int64_t)t * H + h]);
+        for (int k = 0; k < K; k++) {
+            int e = idx[(int64_t)t * K + k];
+            oracle_expert_q2(s, gate + e * expert_gate, up + e * expert_gate, down + e * expert_down, xt, ye);
+            double wk = weights[(int64_t)t * K + k];
+            for (int j = 0; j < H; j++)
+                acc[j] += wk * ye[j];
+        }
+        if (has_shared) {
+            oracle_shared_q8(s, sh_gate, sh_up, sh_down, xt, ye);
+            for (int j = 0; j < H; j++)
+                acc[j] += ye[j];
+        }
+        memcpy(y + (int64_t)t * H, acc, sizeof(double) * H);
+        free(xt);
+        free(ye);
+        free(acc);
+    }
+    return 0;
+}
+
+/* Route, then compute the layer. idx/weights/gap may be NULL. */
+int oracle_forward(const oracle_shape *s, const float *router_w, const float *router_bias,
+                   const uint8_t *gate, const uint8_t *up, const uint8_t *down, const uint8_t *sh_gate,
+                   const uint8_t *sh_up, const uint8_t *sh_down, const uint16_t *x, int32_t T, double *y,
+                   int32_t *idx_out, double *weights_out, double *gap_out, int32_t nthreads)
+{
+    const int K = s->top_k;
+    int32_t *idx = idx_out ? idx_out : (int32_t *)malloc(sizeof(int32_t) * (size_t)T * K + 1);
+    double *w = weights_out ? weights_out : (double *)malloc(sizeof(double) * (size_t)T * K + 1);
+    int rc = oracle_route(s, router_w, router_bias, x, T, idx, w, gap_out, NULL, NULL);
+    if (rc == 0)
+        rc = oracle_forward_routed(s, gate, up, down, sh_gate, sh_up, sh_down, x, T, idx, w, y, nthreads);
+    if (!idx_out) free(idx);
+    if (!weights_out) free(w);
+    return rc;
+}

@@ -1,0 +1,234 @@
+"""Seeded synthetic workloads for the routed-MoE layer.
+
+This module draws inputs only; it contains none of the layer's arithmetic and
+is shared by the CPU oracle tests, the GPU parity tests and the benchmark.
+The C side (``ds4moe_synth.c``) does the drawing and the storage encodings.
+
+Workloads (hidden H, routed intermediate I, experts E, top-k K, shared
+intermediate I_sh, tokens T):
+
+* ``tiny``          H=512,  I=256,  E=32,  K=6, I_sh=256,  T=4
+* ``decode_t1``     H=4096, I=2048, E=384, K=6, I_sh=2048, T=1
+* ``decode_t8``     the decode_t1 layer, T=8 tokens with independent seeds
+* ``prefill_t1024`` the decode_t1 layer, T=1024 tokens, no router bias
+* ``prefill_t4096_zipf4`` four independent layers shaped like decode_t1, each
+  with a Zipf(s=1.1) rank profile added to the router's selection score,
+  applied to the same T=4096 tokens.
+
+Distributions: router ~ N(0, 0.02^2) fp32; 2-bit codes uniform 0..3, 4-bit
+scales and mins uniform 0..15, d and dmin ~ |N(0, 0.01^2)| in binary16; 8-bit
+codes uniform in [-127, 127] with d ~ |N(0, 0.001^2)|; x ~ N(0, 1) in bf16.
+"""
+from __future__ import annotations
+
+import ctypes
+import json
+import os
+import subprocess
+from dataclasses import dataclass
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "ds4moe_synth.c")
+_LIB = os.path.join(_HERE, "libds4moe_synth.so")
+
+SEED_BASE = 0xD54E0000
+
+# stream ids of the counter-based generator
+S_ROUTER, S_GATE, S_UP, S_DOWN, S_SH_GATE, S_SH_UP, S_SH_DOWN, S_BIAS_RANK = range(1, 9)
+S_X = 16
+
+Q2_BLOCK_BYTES = 84
+Q8_BLOCK_BYTES = 34
+
+ZIPF_S = 1.1
+ZIPF_BETA_FILE = os.path.join(_HERE, "zipf_beta.json")
+
+
+def build(force: bool = False) -> str:
+    """Compile the generator into a shared library next to its source."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + ".tmp%d" % os.getpid()
+        subprocess.check_call(["gcc", "-O2", "-fopenmp", "-ffp-contract=off", "-fPIC", "-shared", "-std=c11",
+                               "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+_lib = None
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        lib = ctypes.CDLL(build())
+        u8p = ctypes.POINTER(ctypes.c_uint8)
+        lib.synth_fill_q2.argtypes = [u8p, ctypes.c_int64, ctypes.c_uint64, ctypes.c_uint64, ctypes.c_double]
+        lib.synth_fill_q8.argtypes = [u8p, ctypes.c_int64, ctypes.c_uint64, ctypes.c_uint64, ctypes.c_double]
+        lib.synth_fill_normal_f32.argtypes = [ctypes.POINTER(ctypes.c_float), ctypes.c_int64,
+                                              ctypes.c_uint64, ctypes.c_uint64, ctypes.c_double]
+        lib.synth_fill_normal_bf16.argtypes = [ctypes.POINTER(ctypes.c_uint16), ctypes.c_int64,
+                                               ctypes.c_uint64, ctypes.c_uint64, ctypes.c_double]
+        lib.synth_rank_permutation.argtypes = [ctypes.POINTER(ctypes.c_int32), ctypes.c_int32,
+                                               ctypes.c_uint64, ctypes.c_uint64]
+        lib.synth_to_f16.argtypes = [ctypes.c_float]
+        lib.synth_to_f16.restype = ctypes.c_uint16
+        lib.synth_to_bf16.argtypes = [ctypes.c_float]
+        lib.synth_to_bf16.restype = ctypes.c_uint16
+        _lib = lib
+    return _lib
+
+
+def _ptr(a: np.ndarray, ct):
+    assert a.flags["C_CONTIGUOUS"]
+    return a.ctypes.data_as(ctypes.POINTER(ct))
+
+
+@dataclass(frozen=True)
+class Shape:
+    hidden: int
+    inter: int
+    n_experts: int
+    top_k: int
+    shared_inter: int
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    shape: Shape
+    tokens: int
+    n_layers: int
+    zipf: bool
+    layer_seeds: tuple
+    description: str
+
+
+TINY_SHAPE = Shape(512, 256, 32, 6, 256)
+V4F_SHAPE = Shape(4096, 2048, 384, 6, 2048)
+
+WORKLOADS = {
+    "tiny": Workload("tiny", TINY_SHAPE, 4, 1, False, (SEED_BASE + 0,),
+                     "tiny layer H=512 I=256 E=32 top-6 I_sh=256, T=4"),
+    "decode_t1": Workload("decode_t1", V4F_SHAPE, 1, 1, False, (SEED_BASE + 1,),
+                          "decode batch 1: H=4096 I=2048 E=384 top-6 I_sh=2048, T=1"),
+    "decode_t8": Workload("decode_t8", V4F_SHAPE, 8, 1, False, (SEED_BASE + 1,),
+                          "decode multi-session: the H=4096 E=384 layer, T=8 independent tokens"),
+    "prefill_t1024": Workload("prefill_t1024", V4F_SHAPE, 1024, 1, False, (SEED_BASE + 1,),
+                              "prefill chunk: the H=4096 E=384 layer, T=1024 tokens, near-uniform load"),
+    "prefill_t4096_zipf4": Workload("prefill_t4096_zipf4", V4F_SHAPE, 4096, 4, True,
+                                    tuple(SEED_BASE + 4 + 0x100 * l for l in range(4)),
+                                    "long prefill with skew: 4 independent H=4096 E=384 layers, "
+                                    "T=4096, Zipf(1.1) router bias (hottest ~20x mean load)"),
+}
+
+
+def q2_matrix(rows: int, k: int, seed: int, stream: int, sigma: float = 0.01) -> np.ndarray:
+    assert k % 256 == 0
+    out = np.empty((rows, k // 256, Q2_BLOCK_BYTES), dtype=np.uint8)
+    _load().synth_fill_q2(_ptr(out, ctypes.c_uint8), out.shape[0] * out.shape[1], seed, stream, sigma)
+    return out
+
+
+def q8_matrix(rows: int, k: int, seed: int, stream: int, sigma: float = 0.001) -> np.ndarray:
+    assert k % 32 == 0
+    out = np.empty((rows, k // 32, Q8_BLOCK_BYTES), dtype=np.uint8)
+    _load().synth_fill_q8(_ptr(out, ctypes.c_uint8), out.shape[0] * out.shape[1], seed, stream, sigma)
+    return out
+
+
+def normal_f32(n: int, seed: int, stream: int, sigma: float) -> np.ndarray:
+    out = np.empty(n, dtype=np.float32)
+    _load().synth_fill_normal_f32(_ptr(out, ctypes.c_float), n, seed, stream, sigma)
+    return out
+
+
+def normal_bf16(n: int, seed: int, stream: int, sigma: float = 1.0) -> np.ndarray:
+    """Raw bfloat16 bits (uint16)."""
+    out = np.empty(n, dtype=np.uint16)
+    _load().synth_fill_normal_bf16(_ptr(out, ctypes.c_uint16), n, seed, stream, sigma)
+    return out
+
+
+def rank_permutation(n: int, seed: int, stream: int = S_BIAS_RANK) -> np.ndarray:
+    out = np.empty(n, dtype=np.int32)
+    _load().synth_rank_permutation(_ptr(out, ctypes.c_int32), n, seed, stream)
+    return out
+
+
+def f32_to_f16_bits(v: float) -> int:
+    return int(_load().synth_to_f16(v))
+
+
+def f32_to_bf16_bits(v: float) -> int:
+    return int(_load().synth_to_bf16(v))
+
+
+def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
+    """Decode raw bfloat16 bits (a plain bit shift; used to hand activations to tests)."""
+    return (bits.astype(np.uint32) << 16).view(np.float32)
+
+
+def zipf_profile(n_experts: int, layer_seed: int) -> np.ndarray:
+    """r_e^-s for a seeded rank permutation r (rank 1 = hottest expert)."""
+    ranks = rank_permutation(n_experts, layer_seed).astype(np.float64)
+    return ranks ** (-ZIPF_S)
+
+
+def zipf_beta(layer_seed: int) -> float:
+    """Bias magnitude for one skewed layer, read from the committed calibration file."""
+    with open(ZIPF_BETA_FILE) as f:
+        table = json.load(f)
+    return float(table["beta"][str(layer_seed)])
+
+
+def make_layer(shape: Shape, seed: int, zipf: bool = False, zipf_beta_value: float | None = None) -> dict:
+    """All weights of one layer in canonical layout (host numpy arrays)."""
+    H, I, E, Ish = shape.hidden, shape.inter, shape.n_experts, shape.shared_inter
+    layer = {
+        "router_w": normal_f32(E * H, seed, S_ROUTER, 0.02).reshape(E, H),
+        "gate": q2_matrix(E * I, H, seed, S_GATE).reshape(E, I, H // 256, Q2_BLOCK_BYTES),
+        "up": q2_matrix(E * I, H, seed, S_UP).reshape(E, I, H // 256, Q2_BLOCK_BYTES),
+        "down": q2_matrix(E * H, I, seed, S_DOWN).reshape(E, H, I // 256, Q2_BLOCK_BYTES),
+        "router_bias": None,
+    }
+    if Ish > 0:
+        layer["sh_gate"] = q8_matrix(Ish, H, seed, S_SH_GATE)
+        layer["sh_up"] = q8_matrix(Ish, H, seed, S_SH_UP)
+        layer["sh_down"] = q8_matrix(H, Ish, seed, S_SH_DOWN)
+    else:
+        layer["sh_gate"] = layer["sh_up"] = layer["sh_down"] = None
+    if zipf:
+        beta = zipf_beta(seed) if zipf_beta_value is None else zipf_beta_value
+        layer["router_bias"] = (beta * zipf_profile(E, seed)).astype(np.float32)
+    return layer
+
+
+def token_seed(workload: str, t: int) -> int:
+    """Seed of token t for the decode workloads (one seed per token)."""
+    if workload == "decode_t1":
+        return SEED_BASE + 1 + 0x20000 + t
+    if workload == "decode_t8":
+        return SEED_BASE + 2 + 0x10000 + t
+    raise KeyError(workload)
+
+
+def make_tokens(workload: str, T: int | None = None, first: int = 0) -> np.ndarray:
+    """bf16 activations [T, H] (raw bits) of a workload.
+
+    Decode workloads draw each token from its own seed; ``first`` offsets the
+    token index, which gives the rotating token pool used for timing.
+    """
+    wl = WORKLOADS[workload]
+    H = wl.shape.hidden
+    T = wl.tokens if T is None else T
+    if workload in ("decode_t1", "decode_t8"):
+        return np.stack([normal_bf16(H, token_seed(workload, first + t), S_X) for t in range(T)])
+    if workload == "tiny":
+        return normal_bf16(T * H, SEED_BASE + 0 + 0x10000, S_X).reshape(T, H)
+    if workload == "prefill_t1024":
+        return normal_bf16(T * H, SEED_BASE + 3, S_X).reshape(T, H)
+    if workload == "prefill_t4096_zipf4":
+        return normal_bf16(T * H, SEED_BASE + 4 + 0x10000, S_X).reshape(T, H)
+    raise KeyError(workload)

@@ -1,0 +1,115 @@
+"""The oracle's pins catch plausible mistakes.
+
+Each case plants one slip in a copy of the oracle's C source (on the CPU,
+never in the CUDA library), builds it, and runs the pin suite against it. At
+least one pin must fail for every mutant; an uncaught mutant means the pins
+leave that part of the oracle unchecked. Every mutant keeps all memory
+accesses in bounds.
+"""
+import os
+import subprocess
+import tempfile
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+import test_oracle_pins as pins
+
+SRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "oracle", "ds4moe_oracle.c")
+
+MUTANTS = {
+    "scale_min_nibbles_swapped": [("int sc = scales[j] & 15;", "int sc = scales[j] >> 4;"),
+                                  ("int m = scales[j] >> 4;", "int m = scales[j] & 15;")],
+    "codes_msb_first": [("(qs[i / 4] >> (2 * (i % 4))) & 3", "(qs[i / 4] >> (6 - 2 * (i % 4))) & 3")],
+    "d_dmin_swapped": [("oracle_f16(le16(blk + 80))", "oracle_f16(le16(blk + 82x))"),
+                       ("oracle_f16(le16(blk + 82))", "oracle_f16(le16(blk + 80))"),
+                       ("blk + 82x", "blk + 82")],
+    "min_added": [("w[i] = d * sc * q - dmin * m;", "w[i] = d * sc * q + dmin * m;")],
+    "min_dropped": [("w[i] = d * sc * q - dmin * m;", "w[i] = d * sc * q;")],
+    "block_order_reversed": [("oracle_dequant_q2(row + b * Q2_BYTES, w + b * 256);",
+                              "oracle_dequant_q2(row + b * Q2_BYTES, w + (k / 256 - 1 - b) * 256);")],
+    "q8_unsigned": [("w[i] = d * (double)(int8_t)blk[2 + i];", "w[i] = d * (double)blk[2 + i];")],
+    "f16_exponent_bias": [("v = ldexp((double)(1024 + m), e - 25);", "v = ldexp((double)(1024 + m), e - 24);")],
+    "bf16_no_hidden_bit": [("v = ldexp((double)(128 + m), e - 134);", "v = ldexp((double)m, e - 134);")],
+    "silu_sign": [("return z / (1.0 + exp(-z));", "return z / (1.0 + exp(z));")],
+    "sigmoid_is_exp": [("return 1.0 / (1.0 + exp(-z));", "return exp(z);")],
+    "router_transposed": [("L += xt[h] * (double)router_w[(int64_t)e * H + h];",
+                           "L += xt[h] * (double)router_w[(int64_t)h * E + e];")],
+    "ties_prefer_higher_index": [("return (a->e > b->e) - (a->e < b->e);", "return (a->e < b->e) - (a->e > b->e);")],
+    "ascending_selection": [("if (a->sel > b->sel) return -1;", "if (a->sel > b->sel) return 1;"),
+                            ("if (a->sel < b->sel) return 1;", "if (a->sel < b->sel) return -1;")],
+    "bias_in_weights": [("total += score[order[k].e];", "total += (double)order[k].sel;"),
+                        ("weights[(int64_t)t * K + k] = total > 0.0 ? score[order[k].e] / total : 1.0 / K;",
+                         "weights[(int64_t)t * K + k] = total > 0.0 ? (double)order[k].sel / total : 1.0 / K;")],
+    "no_renormalisation": [("score[order[k].e] / total : 1.0 / K;", "score[order[k].e] : 1.0 / K;")],
+    "gate_up_exchanged": [("h[i] = oracle_silu(g) * u;\n    }\n    for (int j = 0; j < H; j++) {\n        oracle_dequant_q2_row",
+                           "h[i] = oracle_silu(u) * g;\n    }\n    for (int j = 0; j < H; j++) {\n        oracle_dequant_q2_row")],
+    "routing_weight_dropped": [("acc[j] += wk * ye[j];", "acc[j] += ye[j];")],
+    "shared_dropped": [("acc[j] += ye[j];\n        }", "acc[j] += 0.0 * ye[j];\n        }")],
+    "shared_weighted": [("acc[j] += ye[j];\n        }", "acc[j] += weights[(int64_t)t * K] * ye[j];\n        }")],
+    "down_uses_gate_activation": [("ye[j] = dot(w, h, I);", "ye[j] = dot(w, xt, I);")],
+}
+
+
+def _pin_functions(tiny):
+    """(name, callable) for every pin in the pin suite."""
+    out = []
+    for name in dir(pins):
+        if not name.startswith("test_"):
+            continue
+        fn = getattr(pins, name)
+        if name in ("test_q2_golden_blocks",):
+            out += [(f"{name}[{c}]", (lambda c=c, fn=fn: fn(c))) for c in pins.Q2_CLOSED]
+        elif name in ("test_q8_golden_blocks",):
+            out += [(f"{name}[{c}]", (lambda c=c, fn=fn: fn(c))) for c in pins.Q8_CLOSED]
+        elif fn.__code__.co_argcount == 1:
+            out.append((name, (lambda fn=fn: fn(tiny))))
+        else:
+            out.append((name, fn))
+    return out
+
+
+@pytest.fixture(scope="module")
+def tiny():
+    wl = synth.WORKLOADS["tiny"]
+    return wl.shape, synth.make_layer(wl.shape, wl.layer_seeds[0]), synth.make_tokens("tiny")
+
+
+@pytest.fixture(scope="module")
+def workdir():
+    with tempfile.TemporaryDirectory() as d:
+        yield d
+
+
+def _build_mutant(src, subs, path):
+    for old, new in subs:
+        assert old in src, f"mutation anchor not found: {old!r}"
+        src = src.replace(old, new, 1)
+    cpath = path + ".c"
+    with open(cpath, "w") as f:
+        f.write(src)
+    subprocess.check_call(["gcc", "-O1", "-fopenmp", "-ffp-contract=off", "-fPIC", "-shared", "-std=c11",
+                           "-o", path, cpath, "-lm"])
+
+
+def test_unmutated_oracle_passes_every_pin(tiny):
+    for name, fn in _pin_functions(tiny):
+        fn()
+
+
+@pytest.mark.parametrize("mutant", sorted(MUTANTS))
+def test_mutant_is_caught(mutant, tiny, workdir):
+    src = open(SRC).read()
+    lib = os.path.join(workdir, f"lib_{mutant}.so")
+    _build_mutant(src, MUTANTS[mutant], lib)
+    failed = []
+    with oracle.using_library(lib), np.errstate(all="ignore"):
+        for name, fn in _pin_functions(tiny):
+            try:
+                fn()
+            except (AssertionError, ValueError):
+                failed.append(name)
+                break
+    assert failed, f"no pin catches mutant {mutant}"

@@ -1,0 +1,432 @@
+"""Pins of the CPU oracle against facts independent of it.
+
+Each test fixes a value the format definition, a closed form, a library
+routine or brute force determines, chosen so that a plausible slip in the
+oracle (a swapped nibble or field, a transposed matrix, gate and up
+exchanged, bias leaking into the weights, a dropped shared term, wrong block
+order) fails at least one of them.
+"""
+import itertools
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from handmade import as_u8, bf16_bits, f16_bits, q2_block, q8_block
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "blocks.json")
+
+Q2_CLOSED = {
+    "unit_scale_ramp": lambda i: i % 4,
+    "scale_min_ramp": lambda i: 1.75 * (i // 16) - 3.75,
+    "zero": lambda i: 0.0,
+    "subnormal_d": lambda i: 45 * 2.0 ** -24,
+    "negative_d": lambda i: -(i % 4),
+    "byte_position": lambda i: ((i // 4) % 4) - ((i // 16) % 2),
+}
+Q8_CLOSED = {
+    "half_scale_ramp": lambda i: 0.5 * (i if i < 16 else 15 - i),
+    "neg_two_extremes": lambda i: -2 * (-127 if i % 2 == 0 else 127),
+}
+
+
+def _golden():
+    with open(GOLDEN) as f:
+        return json.load(f)
+
+
+# ---- number formats ---------------------------------------------------------
+
+def test_f16_decode_exhaustive_matches_numpy():
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ref = bits.view(np.float16).astype(np.float64)
+    got = np.array([oracle.f16(int(b)) for b in bits])
+    nan = np.isnan(ref)
+    assert (np.isnan(got) == nan).all()
+    assert (got[~nan] == ref[~nan]).all()
+    # signed zeros keep their sign
+    assert math.copysign(1.0, oracle.f16(0x8000)) == -1.0
+
+
+def test_bf16_decode_exhaustive_matches_bit_shift():
+    bits = np.arange(65536, dtype=np.uint32)
+    with np.errstate(invalid="ignore"):
+        ref = (bits << 16).astype(np.uint32).view(np.float32).astype(np.float64)
+    got = np.array([oracle.bf16(int(b)) for b in bits])
+    nan = np.isnan(ref)
+    assert (np.isnan(got) == nan).all()
+    assert (got[~nan] == ref[~nan]).all()
+
+
+def test_sigmoid_silu_closed_forms():
+    assert oracle.sigmoid(0.0) == 0.5
+    assert oracle.silu(0.0) == 0.0
+    assert abs(oracle.sigmoid(math.log(3.0)) - 0.75) < 1e-15
+    assert abs(oracle.silu(math.log(3.0)) - 0.75 * math.log(3.0)) < 1e-15
+    assert oracle.silu(-800.0) == 0.0
+    assert oracle.silu(50.0) == pytest.approx(50.0, rel=1e-20)
+
+
+# ---- block dequantisation ---------------------------------------------------
+
+@pytest.mark.parametrize("case", [c["name"] for c in json.load(open(GOLDEN))["q2"]])
+def test_q2_golden_blocks(case):
+    c = next(c for c in _golden()["q2"] if c["name"] == case)
+    blk = (bytes.fromhex(c["scales"][0]) * c["scales"][1] + bytes.fromhex(c["qs"][0]) * c["qs"][1]
+           + int(c["d"], 16).to_bytes(2, "little") + int(c["dmin"], 16).to_bytes(2, "little"))
+    assert len(blk) == 84
+    got = oracle.dequant_q2(np.frombuffer(blk, dtype=np.uint8))
+    want = np.array([Q2_CLOSED[case](i) for i in range(256)], dtype=np.float64)
+    assert (got == want).all()
+
+
+@pytest.mark.parametrize("case", [c["name"] for c in json.load(open(GOLDEN))["q8"]])
+def test_q8_golden_blocks(case):
+    c = next(c for c in _golden()["q8"] if c["name"] == case)
+    blk = int(c["d"], 16).to_bytes(2, "little") + bytes.fromhex(c["qs"][0]) * c["qs"][1]
+    assert len(blk) == 34
+    got = oracle.dequant_q8(np.frombuffer(blk, dtype=np.uint8))
+    want = np.array([Q8_CLOSED[case](i) for i in range(32)], dtype=np.float64)
+    assert (got == want).all()
+
+
+def test_q2_round_trip_from_fields():
+    """Random fields -> bytes (independent encoder) -> oracle decode == field formula."""
+    rng = np.random.default_rng(1)
+    for _ in range(50):
+        d = float(np.float16(rng.normal(0, 0.02)))
+        dmin = float(np.float16(abs(rng.normal(0, 0.02))))
+        sc = rng.integers(0, 16, 16)
+        m = rng.integers(0, 16, 16)
+        q = rng.integers(0, 4, 256)
+        got = oracle.dequant_q2(np.frombuffer(q2_block(d, dmin, sc, m, q), dtype=np.uint8))
+        j = np.arange(256) // 16
+        want = d * sc[j] * q - dmin * m[j]
+        assert (got == want).all()
+
+
+def test_q8_round_trip_from_fields():
+    rng = np.random.default_rng(2)
+    for _ in range(50):
+        d = float(np.float16(rng.normal(0, 0.01)))
+        q = rng.integers(-127, 128, 32)
+        got = oracle.dequant_q8(np.frombuffer(q8_block(d, q), dtype=np.uint8))
+        assert (got == d * q).all()
+
+
+def test_row_dequant_block_order():
+    """Block b of a row covers weights 256b..256b+255."""
+    blocks = [q2_block(float(b + 1), 0.0, 1, 0, 1) for b in range(4)]
+    row = np.frombuffer(b"".join(blocks), dtype=np.uint8)
+    w = oracle.dequant_q2_matrix(row.reshape(1, 4, 84))[0]
+    assert (w == np.repeat(np.arange(1, 5, dtype=np.float64), 256)).all()
+
+
+# ---- routing ----------------------------------------------------------------
+
+def _identity_router(E, H):
+    w = np.zeros((E, H), dtype=np.float32)
+    w[np.arange(E), np.arange(E)] = 1.0
+    return w
+
+
+def _route_logits(logits_rows, K, bias=None, H=None):
+    """Route tokens whose logits are given exactly (identity router, x = logits)."""
+    logits_rows = np.asarray(logits_rows, dtype=np.float32)
+    T, E = logits_rows.shape
+    H = H or max(E, 8)
+    x = np.zeros((T, H), dtype=np.float32)
+    x[:, :E] = logits_rows
+    shape = synth.Shape(H, 256, E, K, 0)
+    return oracle.route(shape, _identity_router(E, H), bias, bf16_bits(x), want_logits=True)
+
+
+def _expected_topk(sel32, K):
+    order = np.lexsort((np.arange(sel32.size), -sel32.astype(np.float64)))
+    return order[:K]
+
+
+def test_route_logits_are_exact_dot_products():
+    rng = np.random.default_rng(3)
+    H, E = 64, 5
+    x = rng.normal(size=(3, H)).astype(np.float32)
+    x = (bf16_bits(np.float32(np.round(x * 8) / 8)))  # small dyadic values, exact in bf16
+    W = (np.round(rng.normal(size=(E, H)) * 16) / 16).astype(np.float32)
+    r = oracle.route(synth.Shape(H, 256, E, 2, 0), W, None, x, want_logits=True)
+    xf = synth.bf16_bits_to_f32(x).astype(np.float64)
+    assert (r["logits"] == xf @ W.astype(np.float64).T).all()  # dyadic -> every sum exact
+
+
+def test_topk_matches_sort_and_brute_force():
+    rng = np.random.default_rng(4)
+    E, K = 9, 3
+    for _ in range(200):
+        logits = np.clip(rng.normal(size=(1, E)) * 2, -7.5, 7.5)
+        logits = np.float32(np.round(logits * 16) / 16)  # <= 7 significant bits: exact in bf16
+        r = _route_logits(logits, K)
+        sel = r["sel"][0]
+        assert list(r["idx"][0]) == list(_expected_topk(sel, K))
+        # brute force: the chosen set is the unique K-subset that beats every outsider
+        best = [S for S in itertools.combinations(range(E), K)
+                if all((sel[a], -a) > (sel[b], -b) for a in S for b in range(E) if b not in S)]
+        assert len(best) == 1 and set(best[0]) == set(r["idx"][0])
+
+
+def test_topk_large_random_vs_sort():
+    rng = np.random.default_rng(5)
+    E, K = 384, 6
+    logits = np.float32(np.round(np.clip(rng.normal(size=(64, E)), -7.5, 7.5) * 16) / 16)
+    r = _route_logits(logits, K, H=512)
+    for t in range(64):
+        assert list(r["idx"][t]) == list(_expected_topk(r["sel"][t], K))
+        s = np.sort(r["sel"][t].astype(np.float64))[::-1]
+        assert r["gap"][t] == s[K - 1] - s[K]
+
+
+def test_topk_ties_prefer_lower_index():
+    r = _route_logits([[1.0, 2.0, 2.0, 2.0, 0.5, 2.0]], 3)
+    assert list(r["idx"][0]) == [1, 2, 3]
+    assert r["gap"][0] == 0.0
+    r = _route_logits([[0.25] * 8], 4)
+    assert list(r["idx"][0]) == [0, 1, 2, 3]
+    assert np.allclose(r["weights"][0], 0.25, rtol=0, atol=1e-15)
+
+
+def test_topk_degenerate_k_equals_e_and_single_expert():
+    r = _route_logits([[0.5, -1.0, 3.0]], 3)
+    assert list(r["idx"][0]) == [2, 0, 1]
+    assert r["gap"][0] == math.inf
+    r = _route_logits([[-4.0]], 1)
+    assert list(r["idx"][0]) == [0] and r["weights"][0, 0] == 1.0
+
+
+def test_weights_renormalised_sigmoid():
+    logits = [0.0, math.log(3.0), -1.5, 0.75]
+    r = _route_logits([np.float32(np.round(np.array(logits) * 128) / 128)], 2)
+    L = r["logits"][0]
+    s = 1.0 / (1.0 + np.exp(-L))
+    sel = [int(i) for i in r["idx"][0]]
+    assert sel == [1, 3]
+    want = s[sel] / s[sel].sum()
+    assert np.allclose(r["weights"][0], want, rtol=1e-15, atol=0)
+    assert abs(r["weights"][0].sum() - 1.0) < 1e-15
+
+
+def test_bias_changes_selection_only():
+    logits = np.float32([[0.0, 1.0, 2.0, 3.0]])
+    bias = np.float32([10.0, 0.0, 0.0, 0.0])
+    r = _route_logits(logits, 2, bias=bias)
+    assert list(r["idx"][0]) == [0, 3]
+    s0, s3 = 0.5, 1.0 / (1.0 + math.exp(-3.0))
+    assert np.allclose(r["weights"][0], [s0 / (s0 + s3), s3 / (s0 + s3)], rtol=1e-15, atol=0)
+    assert r["sel"][0, 0] == np.float32(0.5 + 10.0)
+
+
+# ---- expert FFN closed forms ------------------------------------------------
+
+def _one_expert_layer(H=512, I=256):
+    """E=K=1, no shared expert, x = 1 on the first 256 dims and 2 on the rest.
+
+    gate row i: block b has all codes 1, sc=1, m=0, d = a[i, b]  -> g_i = 256 sum_b a[i,b] x_b
+    up row i:   d = bb[i, b]                                      -> u_i likewise
+    down row j: codes 1, sc=1, m=1, d=c[j], dmin=e[j]            -> y_j = (c_j - e_j) sum_i h_i
+    """
+    nb = H // 256
+    a = np.array([[2.0 ** -10 * (1 + (i + 3 * b) % 4) for b in range(nb)] for i in range(I)])
+    bb = np.array([[2.0 ** -11 * (1 + (i + b) % 8) for b in range(nb)] for i in range(I)])
+    c = np.array([2.0 ** -6 * (1 + j % 3) for j in range(H)])
+    e = np.array([2.0 ** -8 * (j % 2) for j in range(H)])
+    gate = as_u8([[q2_block(a[i, b], 0.0, 1, 0, 1) for b in range(nb)] for i in range(I)])
+    up = as_u8([[q2_block(bb[i, b], 0.0, 1, 0, 1) for b in range(nb)] for i in range(I)])
+    down = as_u8([[q2_block(c[j], e[j], 1, 1, 1) for _ in range(I // 256)] for j in range(H)])
+    xval = np.where(np.arange(H) < 256, 1.0, 2.0)
+    xb = np.array([256.0 * (1.0 if b == 0 else 2.0) for b in range(nb)])
+    g = a @ xb
+    u = bb @ xb
+    h = g / (1 + np.exp(-g)) * u
+    y = (c - e) * h.sum()
+    return gate, up, down, xval, y
+
+
+def test_single_expert_closed_form():
+    H, I = 512, 256
+    gate, up, down, xval, y_want = _one_expert_layer(H, I)
+    shape = synth.Shape(H, I, 1, 1, 0)
+    layer = {"gate": gate.reshape(1, I, H // 256, 84), "up": up.reshape(1, I, H // 256, 84),
+             "down": down.reshape(1, H, I // 256, 84), "router_w": np.zeros((1, H), np.float32),
+             "router_bias": None, "sh_gate": None, "sh_up": None, "sh_down": None}
+    x = bf16_bits(np.float32(xval)[None, :])
+    y, r = oracle.forward(shape, layer, x)
+    assert r["idx"][0, 0] == 0 and r["weights"][0, 0] == 1.0
+    assert np.allclose(y[0], y_want, rtol=1e-13, atol=0)
+    # the expert entry point agrees with the layer on this case
+    ye = oracle.expert(shape, layer["gate"][0], layer["up"][0], layer["down"][0], xval)
+    assert np.allclose(ye, y_want, rtol=1e-13, atol=0)
+
+
+def test_shared_expert_closed_form():
+    """Shared gate row i = alpha_i, up row i = beta_i, down row j = gamma_j * (+1/-1 by block)."""
+    H, Ish = 256, 64
+    alpha = np.array([2.0 ** -9 * (1 + i % 4) for i in range(Ish)])
+    beta = np.array([2.0 ** -10 * (1 + i % 5) for i in range(Ish)])
+    gamma = np.array([2.0 ** -7 * (1 + j % 7) for j in range(H)])
+    sg = as_u8([[q8_block(alpha[i], 1) for _ in range(H // 32)] for i in range(Ish)])
+    su = as_u8([[q8_block(beta[i], 1) for _ in range(H // 32)] for i in range(Ish)])
+    # down row j: block 0 codes +1, block 1 codes -1 (Ish = 64 -> 2 blocks)
+    sd = as_u8([[q8_block(gamma[j], 1), q8_block(gamma[j], -1)] for j in range(H)])
+    x = np.ones(H)
+    g = alpha * H
+    u = beta * H
+    h = g / (1 + np.exp(-g)) * u
+    want = gamma * (h[:32].sum() - h[32:].sum())
+    got = oracle.shared(synth.Shape(H, 256, 1, 1, Ish), sg, su, sd, x)
+    assert np.allclose(got, want, rtol=1e-13, atol=0)
+
+
+def test_combine_two_experts_closed_form():
+    """E=2, K=2, one-hot router: y = w0 ye0 + w1 ye1 + ysh with w from the sigmoid scores.
+
+    Every gate/up row of expert e is constant (a_e, b_e), so g = a_e sum(x) and
+    u = b_e sum(x); down row j of expert e is the constant c_ej, so
+    ye_j = c_ej * I * silu(g) * u. The shared expert is the same with 8-bit rows.
+    """
+    H, I, Ish = 256, 256, 32
+    a = [2.0 ** -10 * (1 + e) for e in range(2)]
+    b = [2.0 ** -11 * (2 + e) for e in range(2)]
+    c = [[2.0 ** -6 * (1 + j % 2 + 2 * e) for j in range(H)] for e in range(2)]
+    gates = [as_u8([[q2_block(a[e], 0.0, 1, 0, 1)] for _ in range(I)]) for e in range(2)]
+    ups = [as_u8([[q2_block(b[e], 0.0, 1, 0, 1)] for _ in range(I)]) for e in range(2)]
+    downs = [as_u8([[q2_block(c[e][j], 0.0, 1, 0, 1)] for j in range(H)]) for e in range(2)]
+    sg = as_u8([[q8_block(2.0 ** -8, 1) for _ in range(H // 32)] for _ in range(Ish)])
+    su = as_u8([[q8_block(2.0 ** -8, 2) for _ in range(H // 32)] for _ in range(Ish)])
+    sd = as_u8([[q8_block(2.0 ** -5, -1)] for _ in range(H)])
+    router = np.zeros((2, H), np.float32)
+    router[0, 0] = 1.0
+    router[1, 1] = 1.0
+    x = np.ones(H, np.float32)
+    x[0], x[1] = 0.5, -1.25
+    layer = {"gate": np.stack(gates), "up": np.stack(ups), "down": np.stack(downs), "router_w": router,
+             "router_bias": None, "sh_gate": sg, "sh_up": su, "sh_down": sd}
+    y, r = oracle.forward(synth.Shape(H, I, 2, 2, Ish), layer, bf16_bits(x[None, :]))
+    xs = float(x.astype(np.float64).sum())
+    s = np.array([1 / (1 + math.exp(-0.5)), 1 / (1 + math.exp(1.25))])
+    w = s / s.sum()
+    ye = []
+    for e in range(2):
+        g, u = a[e] * xs, b[e] * xs
+        ye.append(np.array(c[e]) * I * (g / (1 + math.exp(-g)) * u))
+    gsh, ush = 2.0 ** -8 * xs, 2.0 ** -8 * 2 * xs
+    ysh = -(2.0 ** -5) * Ish * (gsh / (1 + math.exp(-gsh)) * ush)
+    want = w[0] * ye[0] + w[1] * ye[1] + ysh
+    assert list(r["idx"][0]) == [0, 1]
+    assert np.allclose(r["weights"][0], w, rtol=1e-15, atol=0)
+    assert np.allclose(y[0], want, rtol=1e-13, atol=0)
+
+
+# ---- invariants on random layers --------------------------------------------
+
+@pytest.fixture(scope="module")
+def tiny():
+    wl = synth.WORKLOADS["tiny"]
+    layer = synth.make_layer(wl.shape, wl.layer_seeds[0])
+    x = synth.make_tokens("tiny")
+    return wl.shape, layer, x
+
+
+def test_identical_experts_equal_single_expert(tiny):
+    shape, layer, x = tiny
+    L = dict(layer)
+    for k in ("gate", "up", "down"):
+        L[k] = np.ascontiguousarray(np.broadcast_to(layer[k][:1], layer[k].shape))
+    y, r = oracle.forward(shape, L, x)
+    xf = synth.bf16_bits_to_f32(x).astype(np.float64)
+    for t in range(x.shape[0]):
+        single = oracle.expert(shape, L["gate"][0], L["up"][0], L["down"][0], xf[t])
+        ysh = oracle.shared(shape, L["sh_gate"], L["sh_up"], L["sh_down"], xf[t])
+        ref = single + ysh
+        assert np.linalg.norm(y[t] - ref) <= 1e-12 * np.linalg.norm(ref)
+
+
+def test_token_independence_and_thread_count(tiny):
+    shape, layer, x = tiny
+    y_all, _ = oracle.forward(shape, layer, x, nthreads=4)
+    y_one, _ = oracle.forward(shape, layer, x, nthreads=1)
+    assert (y_all == y_one).all()
+    for t in range(x.shape[0]):
+        yt, _ = oracle.forward(shape, layer, x[t:t + 1])
+        assert (yt[0] == y_all[t]).all()
+
+
+def test_expert_permutation_invariance(tiny):
+    shape, layer, x = tiny
+    y, r = oracle.forward(shape, layer, x)
+    assert (r["gap"] > 0).all()
+    perm = np.random.default_rng(7).permutation(shape.n_experts)  # new expert p holds old perm[p]
+    L = dict(layer)
+    for k in ("gate", "up", "down", "router_w"):
+        L[k] = np.ascontiguousarray(layer[k][perm])
+    y2, r2 = oracle.forward(shape, L, x)
+    assert (perm[r2["idx"]] == r["idx"]).all()
+    assert (y2 == y).all()
+
+
+def test_shared_term_is_added_unweighted(tiny):
+    shape, layer, x = tiny
+    y, r = oracle.forward(shape, layer, x)
+    no_sh = dict(layer, sh_gate=None, sh_up=None, sh_down=None)
+    y0 = oracle.forward_routed(shape, no_sh, x, r["idx"], r["weights"])
+    xf = synth.bf16_bits_to_f32(x).astype(np.float64)
+    for t in range(x.shape[0]):
+        ysh = oracle.shared(shape, layer["sh_gate"], layer["sh_up"], layer["sh_down"], xf[t])
+        assert np.allclose(y[t] - y0[t], ysh, rtol=1e-9, atol=1e-9 * np.abs(ysh).max())
+
+
+def _np_dequant_q2(m):
+    """Vectorised decoder written from the layout (cross-check, not a pin)."""
+    m = m.reshape(-1, 84)
+    scales = m[:, :16].astype(np.int64)
+    qs = m[:, 16:80].astype(np.int64)
+    d = m[:, 80:82].copy().view(np.float16).astype(np.float64)[:, 0]
+    dmin = m[:, 82:84].copy().view(np.float16).astype(np.float64)[:, 0]
+    q = np.stack([(qs >> (2 * s)) & 3 for s in range(4)], axis=-1).reshape(-1, 256)
+    sc = np.repeat(scales & 15, 16, axis=1)
+    mn = np.repeat(scales >> 4, 16, axis=1)
+    return d[:, None] * sc * q - dmin[:, None] * mn
+
+
+def _np_dequant_q8(m):
+    m = m.reshape(-1, 34)
+    d = m[:, :2].copy().view(np.float16).astype(np.float64)[:, 0]
+    return d[:, None] * m[:, 2:].view(np.int8).astype(np.float64)
+
+
+def test_dense_cross_check(tiny):
+    """All experts evaluated densely with numpy matmuls, masked by the routing."""
+    shape, layer, x = tiny
+    H, I, E = shape.hidden, shape.inter, shape.n_experts
+    y, r = oracle.forward(shape, layer, x)
+    xf = synth.bf16_bits_to_f32(x).astype(np.float64)
+    Wg = _np_dequant_q2(layer["gate"]).reshape(E, I, H)
+    Wu = _np_dequant_q2(layer["up"]).reshape(E, I, H)
+    Wd = _np_dequant_q2(layer["down"]).reshape(E, H, I)
+    g = np.einsum("eih,th->tei", Wg, xf)
+    u = np.einsum("eih,th->tei", Wu, xf)
+    h = g / (1 + np.exp(-g)) * u
+    ye = np.einsum("ehi,tei->teh", Wd, h)
+    gate_w = np.zeros((x.shape[0], E))
+    for t in range(x.shape[0]):
+        gate_w[t, r["idx"][t]] = r["weights"][t]
+    Sg = _np_dequant_q8(layer["sh_gate"]).reshape(shape.shared_inter, H)
+    Su = _np_dequant_q8(layer["sh_up"]).reshape(shape.shared_inter, H)
+    Sd = _np_dequant_q8(layer["sh_down"]).reshape(H, shape.shared_inter)
+    gs, us = xf @ Sg.T, xf @ Su.T
+    ysh = (gs / (1 + np.exp(-gs)) * us) @ Sd.T
+    dense = np.einsum("te,teh->th", gate_w, ye) + ysh
+    assert np.linalg.norm(dense - y) <= 1e-12 * np.linalg.norm(dense)
+    # routing by numpy over the oracle's own fp32 selection scores
+    for t in range(x.shape[0]):
+        assert list(r["idx"][t]) == list(_expected_topk(r["sel"][t], shape.top_k))
