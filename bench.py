@@ -1,0 +1,406 @@
+#!/usr/bin/env python
+"""Benchmark of the routed-MoE layer (ds4moe) on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+A step is one ds4moe_forward over one batch of the workload's synthetic tokens
+(all of router, grouping, experts, shared expert and combine). The default
+workload is decode batch 1 on the H=4096, E=384, top-6 layer; a rotating pool
+of 64 tokens makes consecutive steps pick different experts, and L2 is flushed
+(a 2x-L2 device write) between steps, outside the timed events.
+
+Prints one JSON line. ``value`` is whole-job tokens/s with inputs resident in
+HBM; ``e2e`` is the same metric through ds4moe_forward_host with pinned host
+buffers (host->device copy of x and device->host copy of y inside each step).
+``roofline`` is for the dominant kernel, timed live with CUDA events recorded
+by the library on its stream. ``cpu_baseline`` times the CPU oracle on a
+bounded sample of the same workload. ``--impl reference`` times that oracle
+alone as the reference arm.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "MoE-layer tokens/sec (decode T=1..8, prefill T=1024); % HBM / tensor roofline"
+UNIT = "tokens/s"
+POOL = 64
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="decode_t1",
+                    choices=["decode_t1", "decode_t8", "prefill_t1024", "prefill_t4096_zipf4", "tiny"])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile-steps", type=int, default=20)
+    return ap.parse_args()
+
+
+# ---- algorithmic work --------------------------------------------------------
+
+Q2_BPW = 84 / 256  # bytes per 2-bit weight
+Q8_BPW = 34 / 32
+
+
+def layer_bytes(shape, T, U):
+    """Bytes the layer must move per call: selected experts, shared expert, router, x in, y out."""
+    H, I, E, Ish = shape.hidden, shape.inter, shape.n_experts, shape.shared_inter
+    return (U * 3 * H * I * Q2_BPW + 3 * H * Ish * Q8_BPW + 4 * E * H + 2 * T * H + 4 * T * H)
+
+
+def layer_flops(shape, T):
+    H, I, K, Ish, E = shape.hidden, shape.inter, shape.top_k, shape.shared_inter, shape.n_experts
+    return T * (2 * K * 3 * H * I + 2 * 3 * H * Ish + 2 * E * H)
+
+
+def kernel_bytes(name, shape, T, U):
+    """Algorithmic bytes of one launch of a library kernel (weights it must read plus its activations)."""
+    H, I, E, K, Ish = shape.hidden, shape.inter, shape.n_experts, shape.top_k, shape.shared_inter
+    P = T * K
+    table = {
+        "router_logits": 4 * E * H + 4 * T * H + 4 * T * E,
+        "simple_gateup_q2": U * 2 * I * H * Q2_BPW + 4 * T * H + 4 * P * I,
+        "simple_down_q2": U * H * I * Q2_BPW + 4 * P * I + 4 * P * H,
+        "simple_gateup_q8": 2 * Ish * H * Q8_BPW + 4 * T * H + 4 * T * Ish,
+        "simple_down_q8": H * Ish * Q8_BPW + 4 * T * Ish + 4 * T * H,
+        "combine": 4 * P * H + 4 * T * H + 4 * T * H,
+    }
+    return table.get(name)
+
+
+# ---- clocks --------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.sw_power_cap",
+              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown"]
+
+    def __init__(self, gpu_id):
+        self.gpu_id = gpu_id
+        self.lines = []
+        self.proc = None
+
+    def __enter__(self):
+        cmd = ["nvidia-smi", "--query-gpu=" + ",".join(self.FIELDS), "--format=csv,noheader,nounits", "-lms", "100"]
+        if self.gpu_id:
+            cmd += ["-i", self.gpu_id]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["sw_power_cap", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) != len(self.FIELDS):
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---- the workload ----------------------------------------------------------------
+
+def workload_layers(name):
+    import synth
+    wl = synth.WORKLOADS[name]
+    return wl, [synth.make_layer(wl.shape, s, zipf=wl.zipf) for s in wl.layer_seeds]
+
+
+def workload_batches(name):
+    """List of bf16 token batches (host uint16 [T, H]) cycled through by the steps."""
+    import synth
+    wl = synth.WORKLOADS[name]
+    if name == "decode_t1":
+        pool = synth.make_tokens(name, T=POOL)
+        return [pool[i:i + 1] for i in range(POOL)]
+    if name == "decode_t8":
+        import synth as s
+        H = wl.shape.hidden
+        batches = []
+        for b in range(POOL // 8):
+            batches.append(np.stack([s.normal_bf16(H, s.token_seed("decode_t8", 8 * b + t), s.S_X)
+                                     for t in range(8)]))
+        return batches
+    return [synth.make_tokens(name)]
+
+
+def cpu_oracle_rate(name, layers, batches, budget_tokens=None):
+    """Time the oracle on a bounded sample; returns (tokens/s, threads used, sample text, seconds)."""
+    import oracle
+    import synth
+    wl = synth.WORKLOADS[name]
+    cores = oracle.max_threads()
+    if wl.tokens <= 8:
+        n = budget_tokens or min(16, POOL if name == "decode_t1" else 16)
+        flat = np.concatenate(batches)[:n]
+        sample = f"{len(flat)} tokens of the {name} pool through all {len(layers)} layer(s), oracle.forward"
+    else:
+        n = budget_tokens or 16
+        flat = batches[0][:n]
+        sample = f"first {len(flat)} of the {wl.tokens} tokens through all {len(layers)} layer(s), oracle.forward"
+    t0 = time.perf_counter()
+    for layer in layers:
+        oracle.forward(wl.shape, layer, np.ascontiguousarray(flat))
+    dt = time.perf_counter() - t0
+    return len(flat) / dt, min(cores, len(flat)), sample, dt
+
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        backend = "nccl" if torch.cuda.is_available() and args.impl == "ours" else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def run_reference(args, world, rank):
+    import synth
+    if rank != 0:
+        return
+    wl, layers = workload_layers(args.workload)
+    batches = workload_batches(args.workload)
+    times = []
+    n_tok = None
+    for i in range(args.warmup + args.steps):
+        rate, cores, sample, dt = cpu_oracle_rate(args.workload, layers, batches)
+        n_tok = rate * dt
+        if i >= args.warmup:
+            times.append(dt)
+    total = sum(times)
+    value = n_tok * len(times) / total
+    out = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * total / len(times),
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+           "config": workload_config(wl, args.workload, None),
+           "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+           "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(out))
+
+
+def workload_config(wl, name, l2_note):
+    s = wl.shape
+    cfg = {"workload": name, "description": wl.description, "hidden": s.hidden, "inter": s.inter,
+           "n_experts": s.n_experts, "top_k": s.top_k, "shared_inter": s.shared_inter,
+           "tokens_per_step": wl.tokens, "layers_per_step": wl.n_layers,
+           "weights": "routed 2-bit 84B/256 blocks, shared 8-bit 34B/32 blocks, router fp32"}
+    if l2_note:
+        cfg["l2"] = l2_note
+    return cfg
+
+
+def main():
+    args = parse()
+    world, rank, local = dist_setup(args)
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+        return
+
+    import torch
+
+    import quantized_moe_expert_gb300 as ds4
+    import synth
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    wl, layers = workload_layers(args.workload)
+    shape = wl.shape
+    batches = workload_batches(args.workload)
+    T = wl.tokens
+    handles = []
+    for layer in layers:
+        w = {k: (None if v is None else torch.from_numpy(np.ascontiguousarray(v)).to(dev)) for k, v in layer.items()}
+        handles.append(ds4.MoELayer(shape, w, max_tokens=max(T, 8)))
+        del w
+    torch.cuda.empty_cache()
+    stream = torch.cuda.current_stream(dev)
+    for m in handles:
+        m.set_stream(stream)
+    xs = [torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).to(dev) for b in batches]
+    y = torch.empty((T, shape.hidden), dtype=torch.float32, device=dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
+    l2_note = f"flushed between steps: {2 * l2 // (1 << 20)} MiB device write outside the timed events"
+
+    def step(i):
+        x = xs[i % len(xs)]
+        for m in handles:
+            ds4.ds4moe_forward(m.handle, x, T, y)
+
+    # unique experts per batch, from the library's own routing
+    uniq = []
+    for x in xs[:min(len(xs), 64)]:
+        per_layer = []
+        for m in handles:
+            idx, _, _, _ = m.route(x)
+            per_layer.append(len(torch.unique(idx)))
+        uniq.append(per_layer)
+    U_mean = float(np.mean(uniq))
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    for i in range(args.warmup):
+        flush.zero_()
+        step(i)
+    torch.cuda.synchronize()
+    launches_per_step = handles[0].stats().kernel_count * len(handles)
+
+    gpu_id = getattr(torch.cuda.get_device_properties(dev), "uuid", None)
+    gpu_id = ("GPU-" + str(gpu_id)) if gpu_id is not None and not str(gpu_id).startswith("GPU-") else gpu_id
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(gpu_id) as clk:
+        for i in range(args.steps):
+            flush.zero_()
+            evs[i][0].record(stream)
+            step(args.warmup + i)
+            evs[i][1].record(stream)
+        torch.cuda.synchronize()
+    barrier()
+    step_ms = [a.elapsed_time(b) for a, b in evs]
+    total_ms = sum(step_ms)
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    value = world * T * args.steps / (total_ms / 1000.0)
+    ms_per_step = total_ms / args.steps
+
+    # per-kernel device times, recorded by the library around each launch
+    for m in handles:
+        ds4.ds4moe_profile(m.handle, True)
+    for i in range(args.profile_steps):
+        flush.zero_()
+        step(i)
+    ktimes = {}
+    for m in handles:
+        for name, (n, ms) in ds4.ds4moe_profile_read(m.handle).items():
+            a = ktimes.setdefault(name, [0, 0.0])
+            a[0] += n
+            a[1] += ms
+        ds4.ds4moe_profile(m.handle, False)
+    dom = max(ktimes, key=lambda k: ktimes[k][1])
+    dom_avg_ms = ktimes[dom][1] / ktimes[dom][0]
+    dom_bytes = kernel_bytes(dom, shape, T, U_mean)
+    peaks = {}
+    pk_path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(pk_path):
+        with open(pk_path) as f:
+            peaks = json.load(f)
+    hbm_peak = peaks.get("hbm_gbs", 6800.0)
+    peak_src = "measured" if "hbm_gbs" in peaks else "fallback"
+    roofline = None
+    if dom_bytes is not None:
+        ach = dom_bytes / (dom_avg_ms / 1000.0) / 1e9
+        roofline = {"bound": "hbm", "kernel": dom, "achieved": ach, "peak": hbm_peak, "unit": "GB/s",
+                    "frac": ach / hbm_peak, "traffic": None, "peak_source": peak_src,
+                    "bytes_per_launch": dom_bytes, "avg_launch_us": 1000 * dom_avg_ms}
+    lay_bytes = layer_bytes(shape, T, U_mean) * len(handles)
+    layer_gbs = lay_bytes / (ms_per_step / 1000.0) / 1e9
+
+    # end to end through host memory
+    xh = [torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).pin_memory() for b in batches]
+    yh = torch.empty((T, shape.hidden), dtype=torch.float32).pin_memory()
+    e2e_ms = []
+    for i in range(args.warmup + args.steps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for m in handles:
+            ds4.ds4moe_forward_host(m.handle, xh[i % len(xh)].data_ptr(), T, yh.data_ptr())
+        b.record(stream)
+        b.synchronize()
+        if i >= args.warmup:
+            e2e_ms.append(a.elapsed_time(b))
+    e2e_total = sum(e2e_ms)
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([e2e_total], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_total = float(t.item())
+    e2e = {"value": world * T * args.steps / (e2e_total / 1000.0), "unit": UNIT,
+           "h2d_bytes_per_step": 2 * T * shape.hidden * len(handles),
+           "d2h_bytes_per_step": 4 * T * shape.hidden * len(handles)}
+    for m in handles:
+        if m.status() != 0:
+            raise RuntimeError("device error reported by the library")
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rate, cores, sample, dt = cpu_oracle_rate(args.workload, layers, batches)
+        cpu = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample,
+               "seconds": dt}
+
+    if rank == 0:
+        out = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+               "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+               "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+               "config": workload_config(wl, args.workload, l2_note),
+               "roofline": roofline,
+               "layer_roofline": {"bound": "hbm" if args.workload != "prefill_t4096_zipf4" else "tensor",
+                                  "bytes_per_step": lay_bytes, "achieved_gbs": layer_gbs,
+                                  "frac_hbm": layer_gbs / hbm_peak,
+                                  "tflops": layer_flops(shape, T) * len(handles) / (ms_per_step / 1000) / 1e12,
+                                  "unique_experts_mean": U_mean},
+               "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
+               "clocks": clk.summary(),
+               "kernels_us": {k: round(1000 * v[1] / v[0], 2) for k, v in ktimes.items()}}
+        print(json.dumps(out))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

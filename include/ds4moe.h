@@ -1,0 +1,206 @@
+/*
+ * ds4moe: the routed mixture-of-experts FFN layer of a DeepSeek-V4-Flash-shaped
+ * model on one NVIDIA GB300 (sm_103a), as a C ABI.
+ *
+ * What one call computes, for T tokens x[T][H] (bf16):
+ *
+ *   L[t,e]   = sum_h x[t,h] Wr[e,h]                         router logits (fp32)
+ *   s[t,e]   = sigmoid(L[t,e]);  sel = s + b_e              selection score (b optional)
+ *   idx[t,:] = the K experts of largest sel, in descending order, equal scores
+ *              resolved towards the lower expert index
+ *   w[t,k]   = s[t,idx[t,k]] / sum_j s[t,idx[t,j]]          mixing weights (bias-free)
+ *   ye       = Wd[e] (silu(Wg[e] x_t) * (Wu[e] x_t))        SwiGLU expert, 2-bit weights
+ *   ysh      = same with the 8-bit shared expert
+ *   y[t]     = sum_k w[t,k] ye_{idx[t,k]}(x_t) + ysh(x_t)
+ *
+ * The block sum with an unweighted shared expert is the engine's MoE sum of
+ * "YoungAi - DeepSeek V4.1 Flash on one DGX Spark", section 4.2 ("The
+ * objective", with every sidecar gain s_e = 1). The router bias is added to the
+ * selection score only, mixing weights untouched (same page, section 3 and
+ * section 4.2, "The router bias"). 384 experts, 6 per token: same page,
+ * section 2.2. Only the routed experts are 2-bit; the shared expert stays
+ * 8-bit ("Running DeepSeek V4 Flash on an RTX 5080 ...": routed up/gate and
+ * down are 2-bit, shared experts are left untouched; the ds4 teardown on
+ * txtmix.com, section 3, names the shared-expert recipe SExpQ8).
+ *
+ * Storage formats the caller hands to ds4moe_create (little-endian, rows of
+ * consecutive weights along the reduction dimension K):
+ *   2-bit block, 84 bytes per 256 weights:
+ *     [0,16)  scales[j], j = 0..15: low nibble sc_j, high nibble m_j of the
+ *             sub-block of weights 16j..16j+15
+ *     [16,80) qs: code q_i of weight i at byte 16 + i/4, bits 2*(i%4)..+1
+ *     [80,82) d (binary16)   [82,84) dmin (binary16)
+ *     weight i = d * sc_{i/16} * q_i - dmin * m_{i/16}
+ *   8-bit block, 34 bytes per 32 weights: [0,2) d (binary16), [2,34) int8 q_i;
+ *     weight i = d * q_i
+ *   router_w   fp32 [E][H];  router_bias fp32 [E] or NULL
+ *   gate, up   2-bit [E][I][H/256] blocks;  down 2-bit [E][H][I/256] blocks
+ *   sh_gate, sh_up 8-bit [I_sh][H/32];  sh_down 8-bit [H][I_sh/32]
+ *
+ * Conventions of every entry point:
+ *   - Return 0 (DS4MOE_OK) or a negative DS4MOE_E* code; nothing is launched
+ *     when an argument is rejected. ds4moe_strerror names each code.
+ *   - "device" pointers must be CUDA device (or managed) memory of the handle's
+ *     device; host pointers are rejected with DS4MOE_EINVAL.
+ *   - Compute calls are asynchronous on the handle's stream (ds4moe_set_stream;
+ *     default: the legacy default stream). Caller buffers must stay valid until
+ *     the stream reaches the call. A handle may not be used by two host threads
+ *     at once; calls on one handle are serialised by its stream.
+ *   - Errors found by kernels (a wait that timed out) are sticky in the handle
+ *     and reported by ds4moe_status.
+ *   - NaN or Inf inputs are not checked and propagate.
+ */
+#ifndef DS4MOE_H
+#define DS4MOE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define DS4MOE_MAGIC 0x454D3444u /* "D4ME" */
+#define DS4MOE_VERSION 1u
+
+enum {
+    DS4MOE_OK = 0,
+    DS4MOE_EINVAL = -1,       /* bad argument: pointer, shape, token count, magic/version */
+    DS4MOE_ENOMEM = -2,       /* device allocation failed */
+    DS4MOE_ECUDA = -3,        /* a CUDA call or launch failed */
+    DS4MOE_EUNSUPPORTED = -4, /* device is not compute capability 10.3 (GB300) */
+    DS4MOE_ETIMEOUT = -5,     /* a bounded device-side wait gave up */
+    DS4MOE_EDEVICE = -6       /* a kernel reported an internal inconsistency */
+};
+
+/* Execution paths for ds4moe_forward_path. */
+enum {
+    DS4MOE_PATH_AUTO = 0,    /* decode for T <= 8, prefill above */
+    DS4MOE_PATH_DECODE = 1,  /* fused dequant-GEMV (memory-bound regime) */
+    DS4MOE_PATH_PREFILL = 2  /* grouped GEMM on tcgen05 tensor cores */
+};
+
+typedef struct ds4moe ds4moe_t; /* opaque handle */
+
+/* Layer description. All sizes are element counts. */
+typedef struct {
+    uint32_t magic;       /* DS4MOE_MAGIC */
+    uint32_t version;     /* DS4MOE_VERSION */
+    int32_t hidden;       /* H, multiple of 256 */
+    int32_t inter;        /* I (routed intermediate), multiple of 256 */
+    int32_t n_experts;    /* E, 1..1024 */
+    int32_t top_k;        /* K, 1..min(E, 8) */
+    int32_t shared_inter; /* I_sh, multiple of 256, or 0 for no shared expert */
+    int32_t max_tokens;   /* largest T any call will pass, 1..65536 */
+    uint32_t flags;       /* reserved, must be 0 */
+} ds4moe_layer_desc;
+
+/* Device pointers to the weights in the storage formats above. */
+typedef struct {
+    const float *router_w;    /* [E][H] */
+    const float *router_bias; /* [E] or NULL */
+    const void *gate;         /* 2-bit [E][I][H/256] */
+    const void *up;           /* 2-bit [E][I][H/256] */
+    const void *down;         /* 2-bit [E][H][I/256] */
+    const void *sh_gate;      /* 8-bit [I_sh][H/32], NULL iff I_sh == 0 */
+    const void *sh_up;        /* 8-bit [I_sh][H/32], NULL iff I_sh == 0 */
+    const void *sh_down;      /* 8-bit [H][I_sh/32], NULL iff I_sh == 0 */
+} ds4moe_weights;
+
+/*
+ * Validate the description, copy every weight into library-owned device
+ * memory in the kernels' layout, size the scratch for max_tokens, and
+ * synchronise. The caller's weight buffers may be freed once this returns.
+ * Runs on the current device, which must be a GB300 (sm_103).
+ * Errors: EINVAL (desc, NULL or host pointer), EUNSUPPORTED, ENOMEM, ECUDA.
+ */
+int ds4moe_create(const ds4moe_layer_desc *desc, const ds4moe_weights *weights, ds4moe_t **out);
+
+/* Free everything the handle owns (synchronises its stream first). NULL is OK. */
+int ds4moe_destroy(ds4moe_t *h);
+
+/* Issue later calls on this cudaStream_t (NULL = legacy default stream). */
+int ds4moe_set_stream(ds4moe_t *h, void *cuda_stream);
+
+/*
+ * Routing only. x_bf16: device [T][H] bf16. Writes idx_out device int32 [T][K]
+ * and w_out device fp32 [T][K]. 0 <= T <= max_tokens; T == 0 does nothing.
+ */
+int ds4moe_route(ds4moe_t *h, const void *x_bf16, int32_t T, int32_t *idx_out, float *w_out);
+
+/*
+ * The layer. x_bf16: device [T][H] bf16; y: device fp32 [T][H].
+ * 0 <= T <= max_tokens; T == 0 does nothing. Picks the decode path for T <= 8
+ * and the prefill path otherwise.
+ */
+int ds4moe_forward(ds4moe_t *h, const void *x_bf16, int32_t T, float *y);
+
+/*
+ * The layer from and to HOST memory: copies x_host (bf16 [T][H]) to the device,
+ * runs ds4moe_forward, copies y back to y_host (fp32 [T][H]) and waits for the
+ * copy. Pinned host buffers give the fastest copies; pageable ones work.
+ */
+int ds4moe_forward_host(ds4moe_t *h, const void *x_host, int32_t T, float *y_host);
+
+/* ds4moe_forward with an explicit path (DS4MOE_PATH_*). Both paths accept any T. */
+int ds4moe_forward_path(ds4moe_t *h, const void *x_bf16, int32_t T, int32_t path, float *y);
+
+/*
+ * The layer for a caller-given routing (no router): idx device int32 [T][K]
+ * with 0 <= idx < E, w device fp32 [T][K]. Used to compare the expert and
+ * combine stages on tokens whose routing is a near-tie. Indices out of range
+ * are clamped by the kernels and reported as DS4MOE_EDEVICE by ds4moe_status.
+ */
+int ds4moe_forward_routed(ds4moe_t *h, const void *x_bf16, int32_t T, const int32_t *idx,
+                          const float *w, int32_t path, float *y);
+
+/*
+ * Routing with diagnostics: like ds4moe_route, and also gap_out device fp32 [T]
+ * = the K-th minus the (K+1)-th largest fp32 selection score (+inf when K == E),
+ * and, if sel_out is not NULL, the fp32 selection scores [T][E].
+ */
+int ds4moe_route_detail(ds4moe_t *h, const void *x_bf16, int32_t T, int32_t *idx_out, float *w_out,
+                        float *gap_out, float *sel_out);
+
+/* Synchronise the handle's stream; return and clear the sticky device error. */
+int ds4moe_status(ds4moe_t *h);
+
+/* Statistics of the last forward call (read after ds4moe_status). */
+typedef struct {
+    int32_t tokens;        /* T of the last call */
+    int32_t path;          /* DS4MOE_PATH_DECODE or DS4MOE_PATH_PREFILL */
+    int32_t n_unique;      /* distinct routed experts touched */
+    int32_t max_load;      /* most (token, k) pairs on one expert */
+    int32_t kernel_count;  /* kernels the call launched */
+} ds4moe_stats;
+
+int ds4moe_get_stats(ds4moe_t *h, ds4moe_stats *out);
+
+/* Device bytes the handle owns: repacked weights and scratch. */
+int ds4moe_memory(ds4moe_t *h, uint64_t *weight_bytes, uint64_t *scratch_bytes);
+
+/*
+ * Per-kernel timing with CUDA events recorded on the handle's stream around
+ * every kernel the library launches. ds4moe_profile(h, 1) clears the records
+ * and starts recording; ds4moe_profile(h, 0) stops. ds4moe_profile_read
+ * synchronises the stream and writes up to max entries (one per kernel name,
+ * in first-launch order) with the number of launches and their summed device
+ * time; *n_out gets the number of entries. Recording adds one event pair per
+ * launch; leave it off when timing whole calls.
+ */
+typedef struct {
+    char name[48];
+    int32_t launches;
+    double total_ms;
+} ds4moe_kernel_time;
+
+int ds4moe_profile(ds4moe_t *h, int32_t enable);
+int ds4moe_profile_read(ds4moe_t *h, ds4moe_kernel_time *out, int32_t max, int32_t *n_out);
+
+/* Static string for a return code. */
+const char *ds4moe_strerror(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DS4MOE_H */

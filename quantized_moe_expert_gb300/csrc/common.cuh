@@ -1,0 +1,99 @@
+// Shared device-side definitions of the ds4moe library: the repacked weight
+// layout, the handle's scratch, error bits and small helpers.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/ds4moe.h"
+
+namespace ds4 {
+
+constexpr int kQ2Block = 256;      // weights per 2-bit super-block
+constexpr int kQ2Sub = 16;         // weights per sub-block (one scale/min nibble pair)
+constexpr int kQ2Bytes = 84;       // canonical bytes per 2-bit block
+constexpr int kQ8Block = 32;       // weights per 8-bit block
+constexpr int kQ8Bytes = 34;       // canonical bytes per 8-bit block
+constexpr int kMaxTopK = 8;
+
+// Sticky device error bits (OR-ed into the handle's status word).
+constexpr unsigned kErrIndex = 1u << 0;    // a routed index was out of range and was clamped
+constexpr unsigned kErrTimeout = 1u << 1;  // a bounded wait gave up
+constexpr unsigned kErrInternal = 1u << 2; // an internal consistency check failed
+
+// 2-bit matrix in the kernels' layout: three separately aligned streams, each
+// row-major over (row, block). Row r, block b:
+//   codes  qs + (r * nb + b) * 64     64 bytes, code i at byte i/4, bits 2*(i%4)
+//   scales sc + (r * nb + b) * 16     16 bytes, low nibble scale, high nibble min
+//   dm[r * nb + b]                    binary16 d in the low half, dmin in the high half
+// A row's codes are contiguous (nb * 64 bytes), so a warp reads them with
+// fully coalesced 16-byte loads and a row range is one contiguous bulk copy.
+struct Q2Mat {
+    const uint8_t *qs;
+    const uint8_t *sc;
+    const uint32_t *dm;
+    int64_t rows;
+    int32_t nb; // blocks per row = K / 256
+};
+
+// 8-bit matrix: int8 codes [rows][K] and binary16 scales [rows][K/32].
+struct Q8Mat {
+    const int8_t *qs;
+    const uint16_t *d;
+    int64_t rows;
+    int32_t k;
+};
+
+__device__ __forceinline__ float f16_to_f32(uint32_t bits) {
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(bits & 0xFFFFu)));
+}
+
+__device__ __forceinline__ float bf16_to_f32(uint32_t bits) {
+    return __uint_as_float((bits & 0xFFFFu) << 16);
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    return v;
+}
+
+__device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
+
+__device__ __forceinline__ float sigmoid(float z) { return 1.0f / (1.0f + expf(-z)); }
+
+// Scratch owned by a handle, sized for max_tokens at create time.
+// Pair index p = t * K + k names the k-th routed choice of token t.
+struct Scratch {
+    float *x32;        // [Tmax][H] activations widened to fp32
+    float *xsum;       // [Tmax][H/16] sums of x over each 16-wide sub-block
+    float *logits;     // [Tmax][E]
+    int32_t *idx;      // [Tmax][K] routed experts
+    float *w;          // [Tmax][K] mixing weights
+    float *gap;        // [Tmax]
+    int32_t *counts;   // [E] pairs per expert
+    int32_t *offsets;  // [E+1] exclusive scan of counts
+    int32_t *uexp;     // [min(E, Tmax*K)] distinct experts in ascending order
+    int32_t *uoff;     // [min(E, Tmax*K) + 1] first pair position of each distinct expert
+    int32_t *nuniq;    // [1] number of distinct experts
+    int32_t *perm;     // [Tmax*K] pair index at each expert-grouped position
+    int32_t *inv;      // [Tmax*K] expert-grouped position of each pair
+    float *h;          // [Tmax*K][I] routed SwiGLU activations, expert-grouped order
+    float *ye;         // [Tmax*K][H] routed expert outputs, expert-grouped order
+    float *hsh;        // [Tmax][I_sh]
+    float *ysh;        // [Tmax][H]
+    uint16_t *xstage;  // [Tmax][H] bf16 staging for host-memory calls
+    float *ystage;     // [Tmax][H]
+};
+
+struct LayerDev {
+    int H, I, E, K, Ish, Tmax;
+    const float *router_w;
+    const float *router_bias;
+    Q2Mat gate, up, down; // rows: gate/up E*I (K = H), down E*H (K = I)
+    Q8Mat sh_gate, sh_up, sh_down;
+};
+
+} // namespace ds4

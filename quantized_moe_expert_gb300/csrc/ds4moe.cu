@@ -1,0 +1,680 @@
+// ds4moe C ABI: handle lifetime, argument checks, weight repacking and the
+// launch sequence of the layer. Kernels live in the headers included below.
+#include <cuda_runtime.h>
+
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+#include <string>
+#include <vector>
+
+#include "../../include/ds4moe.h"
+#include "common.cuh"
+#include "decode_simple.cuh"
+#include "dispatch.cuh"
+#include "router.cuh"
+
+using namespace ds4;
+
+// Per-kernel CUDA-event timing (ds4moe_profile).
+struct Profiler {
+    bool on = false;
+    struct Rec {
+        int name;
+        cudaEvent_t a, b;
+    };
+    std::vector<std::string> names;
+    std::vector<int32_t> launches;
+    std::vector<double> total_ms;
+    std::vector<Rec> pending;
+    std::vector<cudaEvent_t> pool;
+
+    cudaEvent_t take() {
+        if (pool.empty()) {
+            cudaEvent_t e;
+            cudaEventCreate(&e);
+            return e;
+        }
+        cudaEvent_t e = pool.back();
+        pool.pop_back();
+        return e;
+    }
+    int name_id(const char *n) {
+        for (size_t i = 0; i < names.size(); i++)
+            if (names[i] == n)
+                return (int)i;
+        names.emplace_back(n);
+        launches.push_back(0);
+        total_ms.push_back(0.0);
+        return (int)names.size() - 1;
+    }
+    void drain() { // caller has synchronised the stream
+        for (const Rec &r : pending) {
+            float ms = 0.f;
+            cudaEventElapsedTime(&ms, r.a, r.b);
+            launches[r.name] += 1;
+            total_ms[r.name] += ms;
+            pool.push_back(r.a);
+            pool.push_back(r.b);
+        }
+        pending.clear();
+    }
+    void clear() {
+        drain();
+        names.clear();
+        launches.clear();
+        total_ms.clear();
+    }
+    ~Profiler() {
+        for (const Rec &r : pending) {
+            cudaEventDestroy(r.a);
+            cudaEventDestroy(r.b);
+        }
+        for (cudaEvent_t e : pool)
+            cudaEventDestroy(e);
+    }
+};
+
+struct ds4moe {
+    Profiler prof;
+    LayerDev L;
+    Scratch S;
+    int device = 0;
+    cudaStream_t stream = nullptr;
+    unsigned *status = nullptr; // device word of kErr* bits
+    void *weight_mem = nullptr;
+    uint64_t weight_bytes = 0;
+    void *scratch_mem = nullptr;
+    uint64_t scratch_bytes = 0;
+    ds4moe_stats stats{};
+};
+
+namespace {
+
+// ---- argument checks -------------------------------------------------------
+
+bool is_device_ptr(const void *p) {
+    if (!p)
+        return false;
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged;
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int check_desc(const ds4moe_layer_desc *d) {
+    if (!d || d->magic != DS4MOE_MAGIC || d->version != DS4MOE_VERSION || d->flags != 0)
+        return DS4MOE_EINVAL;
+    if (d->hidden <= 0 || d->hidden % 256 || d->inter <= 0 || d->inter % 256)
+        return DS4MOE_EINVAL;
+    if (d->n_experts < 1 || d->n_experts > 1024 || d->top_k < 1 || d->top_k > kMaxTopK ||
+        d->top_k > d->n_experts)
+        return DS4MOE_EINVAL;
+    if (d->shared_inter < 0 || d->shared_inter % 256)
+        return DS4MOE_EINVAL;
+    if (d->max_tokens < 1 || d->max_tokens > 65536)
+        return DS4MOE_EINVAL;
+    if ((int64_t)d->hidden * d->inter > (int64_t)1 << 30)
+        return DS4MOE_EINVAL;
+    return DS4MOE_OK;
+}
+
+// ---- repacking: canonical 84/34-byte blocks -> per-field streams -----------
+
+__global__ void repack_q2_kernel(const uint32_t *__restrict__ src, int64_t nblocks, uint8_t *__restrict__ qs,
+                                 uint8_t *__restrict__ sc, uint32_t *__restrict__ dm) {
+    const int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (b >= nblocks)
+        return;
+    const uint32_t *s = src + b * (kQ2Bytes / 4);
+    uint32_t w[21];
+#pragma unroll
+    for (int i = 0; i < 21; i++)
+        w[i] = s[i];
+    reinterpret_cast<uint4 *>(sc)[b] = make_uint4(w[0], w[1], w[2], w[3]);
+    uint4 *q = reinterpret_cast<uint4 *>(qs + b * 64);
+#pragma unroll
+    for (int i = 0; i < 4; i++)
+        q[i] = make_uint4(w[4 + 4 * i], w[5 + 4 * i], w[6 + 4 * i], w[7 + 4 * i]);
+    dm[b] = w[20]; // d in the low half, dmin in the high half
+}
+
+__global__ void repack_q8_kernel(const uint16_t *__restrict__ src, int64_t nblocks, int8_t *__restrict__ qs,
+                                 uint16_t *__restrict__ d) {
+    const int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (b >= nblocks)
+        return;
+    const uint16_t *s = src + b * (kQ8Bytes / 2);
+    d[b] = s[0];
+    uint32_t w[8];
+#pragma unroll
+    for (int i = 0; i < 8; i++)
+        w[i] = (uint32_t)s[1 + 2 * i] | ((uint32_t)s[2 + 2 * i] << 16);
+    uint4 *q = reinterpret_cast<uint4 *>(qs + b * 32);
+    q[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    q[1] = make_uint4(w[4], w[5], w[6], w[7]);
+}
+
+// Bump allocator over one device allocation, 256-byte aligned pieces.
+struct Carver {
+    char *base;
+    uint64_t used = 0;
+    template <class T> T *take(uint64_t count) {
+        T *p = reinterpret_cast<T *>(base ? base + used : nullptr);
+        used += (count * sizeof(T) + 255) & ~uint64_t(255);
+        return p;
+    }
+};
+
+void layout_weights(ds4moe *h, Carver &c) {
+    LayerDev &L = h->L;
+    auto q2 = [&](Q2Mat &m, int64_t rows, int k) {
+        m.rows = rows;
+        m.nb = k / 256;
+        const uint64_t nblk = (uint64_t)rows * m.nb;
+        m.qs = c.take<uint8_t>(nblk * 64);
+        m.sc = c.take<uint8_t>(nblk * 16);
+        m.dm = c.take<uint32_t>(nblk);
+    };
+    auto q8 = [&](Q8Mat &m, int64_t rows, int k) {
+        m.rows = rows;
+        m.k = k;
+        m.qs = c.take<int8_t>((uint64_t)rows * k);
+        m.d = c.take<uint16_t>((uint64_t)rows * (k / 32));
+    };
+    L.router_w = c.take<float>((uint64_t)L.E * L.H);
+    L.router_bias = c.take<float>(L.E);
+    q2(L.gate, (int64_t)L.E * L.I, L.H);
+    q2(L.up, (int64_t)L.E * L.I, L.H);
+    q2(L.down, (int64_t)L.E * L.H, L.I);
+    if (L.Ish > 0) {
+        q8(L.sh_gate, L.Ish, L.H);
+        q8(L.sh_up, L.Ish, L.H);
+        q8(L.sh_down, L.H, L.Ish);
+    }
+}
+
+void layout_scratch(ds4moe *h, Carver &c) {
+    const LayerDev &L = h->L;
+    Scratch &S = h->S;
+    const int64_t T = L.Tmax, P = (int64_t)L.Tmax * L.K;
+    const int64_t U = P < L.E ? P : L.E;
+    S.x32 = c.take<float>(T * L.H);
+    S.xsum = c.take<float>(T * (L.H / 16));
+    S.logits = c.take<float>(T * L.E);
+    S.idx = c.take<int32_t>(P);
+    S.w = c.take<float>(P);
+    S.gap = c.take<float>(T);
+    S.counts = c.take<int32_t>(L.E);
+    S.offsets = c.take<int32_t>(L.E + 1);
+    S.uexp = c.take<int32_t>(U);
+    S.uoff = c.take<int32_t>(U + 1);
+    S.nuniq = c.take<int32_t>(1);
+    S.perm = c.take<int32_t>(P);
+    S.inv = c.take<int32_t>(P);
+    S.h = c.take<float>(P * L.I);
+    S.ye = c.take<float>(P * L.H);
+    S.hsh = c.take<float>(T * (L.Ish > 0 ? L.Ish : 1));
+    S.ysh = c.take<float>(T * L.H);
+    S.xstage = c.take<uint16_t>(T * L.H);
+    S.ystage = c.take<float>(T * L.H);
+}
+
+int cuda_rc(cudaError_t e) {
+    if (e == cudaSuccess)
+        return DS4MOE_OK;
+    cudaGetLastError();
+    return e == cudaErrorMemoryAllocation ? DS4MOE_ENOMEM : DS4MOE_ECUDA;
+}
+
+int launch_rc() { return cuda_rc(cudaGetLastError()); }
+
+unsigned blocks_for(int64_t n, int per) { return (unsigned)((n + per - 1) / per); }
+
+// Launch `body` (a kernel launch on h->stream), bracketed by timing events when
+// profiling is on, and count it.
+template <class F> void launch(ds4moe *h, const char *name, F &&body) {
+    if (h->prof.on) {
+        Profiler::Rec r{h->prof.name_id(name), h->prof.take(), h->prof.take()};
+        cudaEventRecord(r.a, h->stream);
+        body();
+        cudaEventRecord(r.b, h->stream);
+        h->prof.pending.push_back(r);
+    } else {
+        body();
+    }
+    h->stats.kernel_count += 1;
+}
+
+// ---- the launch sequence ----------------------------------------------------
+
+int run_prep(ds4moe *h, const void *x, int T) {
+    const LayerDev &L = h->L;
+    Scratch &S = h->S;
+    cudaStream_t st = h->stream;
+    launch(h, "prep_x", [&] {
+        prep_x_kernel<<<blocks_for((int64_t)T * (L.H / 16), 256), 256, 0, st>>>(
+            static_cast<const uint16_t *>(x), T, L.H, S.x32, S.xsum);
+    });
+    return launch_rc();
+}
+
+int run_router(ds4moe *h, const void *x, int T, float *sel_out) {
+    const LayerDev &L = h->L;
+    Scratch &S = h->S;
+    cudaStream_t st = h->stream;
+    int rc = run_prep(h, x, T);
+    if (rc)
+        return rc;
+    launch(h, "router_logits", [&] {
+        dim3 lg(blocks_for(L.E, 8), blocks_for(T, kRouterTok));
+        router_logits_kernel<<<lg, 256, 0, st>>>(S.x32, T, L.H, L.router_w, L.E, S.logits);
+    });
+    launch(h, "router_select", [&] {
+        const size_t smem = (size_t)kSelectWarps * 2 * L.E * sizeof(float);
+        router_select_kernel<<<blocks_for(T, kSelectWarps), 32 * kSelectWarps, smem, st>>>(
+            S.logits, L.router_bias, T, L.E, L.K, S.idx, S.w, S.gap, sel_out);
+    });
+    return launch_rc();
+}
+
+// Expert grouping for the routing in S.idx.
+int run_dispatch(ds4moe *h, int T) {
+    const LayerDev &L = h->L;
+    Scratch &S = h->S;
+    cudaStream_t st = h->stream;
+    const int P = T * L.K;
+    cudaMemsetAsync(S.counts, 0, sizeof(int32_t) * L.E, st);
+    launch(h, "dispatch_count", [&] {
+        dispatch_count_kernel<<<blocks_for(P, 256), 256, 0, st>>>(S.idx, P, L.E, S.counts, h->status);
+    });
+    launch(h, "dispatch_scan", [&] {
+        dispatch_scan_kernel<<<1, 1024, 0, st>>>(S.counts, L.E, P, S.offsets, S.uexp, S.uoff, S.nuniq);
+    });
+    launch(h, "dispatch_place", [&] {
+        dispatch_place_kernel<<<L.E, 256, 0, st>>>(S.idx, P, S.counts, S.offsets, S.perm, S.inv);
+    });
+    return launch_rc();
+}
+
+// Experts and combine for the routing already in S.idx / S.w (x already prepped).
+int run_experts_simple(ds4moe *h, int T, float *y) {
+    const LayerDev &L = h->L;
+    Scratch &S = h->S;
+    cudaStream_t st = h->stream;
+    const int P = T * L.K;
+    const int U = P < L.E ? P : L.E;
+    int rc = run_dispatch(h, T);
+    if (rc)
+        return rc;
+    launch(h, "simple_gateup_q2", [&] {
+        simple_gateup_q2_kernel<<<dim3(blocks_for(L.I, kRowsPerCta), U), 32 * kRowsPerCta, 0, st>>>(L, S);
+    });
+    launch(h, "simple_down_q2", [&] {
+        simple_down_q2_kernel<<<dim3(blocks_for(L.H, kRowsPerCta), U), 32 * kRowsPerCta, 0, st>>>(L, S);
+    });
+    if (L.Ish > 0) {
+        launch(h, "simple_gateup_q8", [&] {
+            simple_gateup_q8_kernel<<<blocks_for(L.Ish, kRowsPerCta), 32 * kRowsPerCta, 0, st>>>(L, S, T);
+        });
+        launch(h, "simple_down_q8", [&] {
+            simple_down_q8_kernel<<<blocks_for(L.H, kRowsPerCta), 32 * kRowsPerCta, 0, st>>>(L, S, T);
+        });
+    }
+    launch(h, "combine", [&] {
+        combine_kernel<<<blocks_for((int64_t)T * L.H / 4, 256), 256, 0, st>>>(
+            S.ye, L.Ish > 0 ? S.ysh : nullptr, S.w, S.inv, T, L.H, L.K, y);
+    });
+    return launch_rc();
+}
+
+int check_call(ds4moe *h, const void *x, int T) {
+    if (!h)
+        return DS4MOE_EINVAL;
+    if (T < 0 || T > h->L.Tmax)
+        return DS4MOE_EINVAL;
+    if (T > 0 && !is_device_ptr(x))
+        return DS4MOE_EINVAL;
+    if (T > 0 && !aligned(x, 16))
+        return DS4MOE_EINVAL;
+    return DS4MOE_OK;
+}
+
+int forward_impl(ds4moe *h, const void *x, int T, int path, float *y) {
+    h->stats = ds4moe_stats{};
+    h->stats.tokens = T;
+    if (path == DS4MOE_PATH_AUTO)
+        path = T <= 8 ? DS4MOE_PATH_DECODE : DS4MOE_PATH_PREFILL;
+    h->stats.path = path;
+    int rc = run_router(h, x, T, nullptr);
+    if (rc)
+        return rc;
+    return run_experts_simple(h, T, y);
+}
+
+} // namespace
+
+extern "C" {
+
+const char *ds4moe_strerror(int code) {
+    switch (code) {
+    case DS4MOE_OK: return "ok";
+    case DS4MOE_EINVAL: return "invalid argument";
+    case DS4MOE_ENOMEM: return "device allocation failed";
+    case DS4MOE_ECUDA: return "CUDA call or launch failed";
+    case DS4MOE_EUNSUPPORTED: return "device is not a GB300 (compute capability 10.3)";
+    case DS4MOE_ETIMEOUT: return "a bounded device-side wait timed out";
+    case DS4MOE_EDEVICE: return "a kernel reported an inconsistency (e.g. an out-of-range expert index)";
+    default: return "unknown ds4moe error";
+    }
+}
+
+int ds4moe_create(const ds4moe_layer_desc *desc, const ds4moe_weights *w, ds4moe_t **out) {
+    if (!out)
+        return DS4MOE_EINVAL;
+    *out = nullptr;
+    int rc = check_desc(desc);
+    if (rc)
+        return rc;
+    if (!w || !is_device_ptr(w->router_w) || !is_device_ptr(w->gate) || !is_device_ptr(w->up) ||
+        !is_device_ptr(w->down))
+        return DS4MOE_EINVAL;
+    if (w->router_bias && !is_device_ptr(w->router_bias))
+        return DS4MOE_EINVAL;
+    const bool has_shared = desc->shared_inter > 0;
+    if (has_shared != (w->sh_gate != nullptr) || has_shared != (w->sh_up != nullptr) ||
+        has_shared != (w->sh_down != nullptr))
+        return DS4MOE_EINVAL;
+    if (has_shared && (!is_device_ptr(w->sh_gate) || !is_device_ptr(w->sh_up) || !is_device_ptr(w->sh_down)))
+        return DS4MOE_EINVAL;
+    if (!aligned(w->router_w, 16) || !aligned(w->gate, 4) || !aligned(w->up, 4) || !aligned(w->down, 4) ||
+        (has_shared && (!aligned(w->sh_gate, 2) || !aligned(w->sh_up, 2) || !aligned(w->sh_down, 2))) ||
+        (w->router_bias && !aligned(w->router_bias, 4)))
+        return DS4MOE_EINVAL;
+
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return DS4MOE_ECUDA;
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess)
+        return DS4MOE_ECUDA;
+    if (prop.major != 10 || prop.minor != 3)
+        return DS4MOE_EUNSUPPORTED;
+
+    ds4moe *h = new (std::nothrow) ds4moe();
+    if (!h)
+        return DS4MOE_ENOMEM;
+    h->device = dev;
+    LayerDev &L = h->L;
+    L.H = desc->hidden;
+    L.I = desc->inter;
+    L.E = desc->n_experts;
+    L.K = desc->top_k;
+    L.Ish = desc->shared_inter;
+    L.Tmax = desc->max_tokens;
+
+    Carver probe{nullptr};
+    layout_weights(h, probe);
+    h->weight_bytes = probe.used;
+    Carver sprobe{nullptr};
+    layout_scratch(h, sprobe);
+    h->scratch_bytes = sprobe.used;
+
+    rc = cuda_rc(cudaMalloc(&h->weight_mem, h->weight_bytes));
+    if (!rc)
+        rc = cuda_rc(cudaMalloc(&h->scratch_mem, h->scratch_bytes));
+    if (!rc)
+        rc = cuda_rc(cudaMalloc(reinterpret_cast<void **>(&h->status), sizeof(unsigned)));
+    if (rc) {
+        ds4moe_destroy(h);
+        return rc;
+    }
+    Carver wc{static_cast<char *>(h->weight_mem)};
+    layout_weights(h, wc);
+    Carver sc{static_cast<char *>(h->scratch_mem)};
+    layout_scratch(h, sc);
+
+    cudaStream_t st = nullptr; // create-time work runs on the legacy stream and is waited for
+    cudaMemsetAsync(h->status, 0, sizeof(unsigned), st);
+    cudaMemcpyAsync(const_cast<float *>(L.router_w), w->router_w, sizeof(float) * L.E * L.H,
+                    cudaMemcpyDeviceToDevice, st);
+    if (w->router_bias)
+        cudaMemcpyAsync(const_cast<float *>(L.router_bias), w->router_bias, sizeof(float) * L.E,
+                        cudaMemcpyDeviceToDevice, st);
+    else
+        L.router_bias = nullptr;
+    auto rq2 = [&](const void *src, Q2Mat &m) {
+        const int64_t nblk = m.rows * m.nb;
+        repack_q2_kernel<<<blocks_for(nblk, 256), 256, 0, st>>>(
+            static_cast<const uint32_t *>(src), nblk, const_cast<uint8_t *>(m.qs), const_cast<uint8_t *>(m.sc),
+            const_cast<uint32_t *>(m.dm));
+    };
+    auto rq8 = [&](const void *src, Q8Mat &m) {
+        const int64_t nblk = m.rows * (m.k / 32);
+        repack_q8_kernel<<<blocks_for(nblk, 256), 256, 0, st>>>(
+            static_cast<const uint16_t *>(src), nblk, const_cast<int8_t *>(m.qs), const_cast<uint16_t *>(m.d));
+    };
+    rq2(w->gate, L.gate);
+    rq2(w->up, L.up);
+    rq2(w->down, L.down);
+    if (has_shared) {
+        rq8(w->sh_gate, L.sh_gate);
+        rq8(w->sh_up, L.sh_up);
+        rq8(w->sh_down, L.sh_down);
+    }
+    rc = launch_rc();
+    if (!rc)
+        rc = cuda_rc(cudaStreamSynchronize(st));
+    if (rc) {
+        ds4moe_destroy(h);
+        return rc;
+    }
+    *out = h;
+    return DS4MOE_OK;
+}
+
+int ds4moe_destroy(ds4moe_t *h) {
+    if (!h)
+        return DS4MOE_OK;
+    if (h->stream)
+        cudaStreamSynchronize(h->stream);
+    else
+        cudaDeviceSynchronize();
+    cudaFree(h->weight_mem);
+    cudaFree(h->scratch_mem);
+    cudaFree(h->status);
+    delete h;
+    return DS4MOE_OK;
+}
+
+int ds4moe_set_stream(ds4moe_t *h, void *stream) {
+    if (!h)
+        return DS4MOE_EINVAL;
+    h->stream = static_cast<cudaStream_t>(stream);
+    return DS4MOE_OK;
+}
+
+int ds4moe_route_detail(ds4moe_t *h, const void *x, int32_t T, int32_t *idx_out, float *w_out, float *gap_out,
+                        float *sel_out) {
+    int rc = check_call(h, x, T);
+    if (rc)
+        return rc;
+    if (T == 0)
+        return DS4MOE_OK;
+    if (!is_device_ptr(idx_out) || !is_device_ptr(w_out) || (gap_out && !is_device_ptr(gap_out)) ||
+        (sel_out && !is_device_ptr(sel_out)))
+        return DS4MOE_EINVAL;
+    h->stats = ds4moe_stats{};
+    rc = run_router(h, x, T, sel_out);
+    if (rc)
+        return rc;
+    const LayerDev &L = h->L;
+    cudaStream_t st = h->stream;
+    cudaMemcpyAsync(idx_out, h->S.idx, sizeof(int32_t) * T * L.K, cudaMemcpyDeviceToDevice, st);
+    cudaMemcpyAsync(w_out, h->S.w, sizeof(float) * T * L.K, cudaMemcpyDeviceToDevice, st);
+    if (gap_out)
+        cudaMemcpyAsync(gap_out, h->S.gap, sizeof(float) * T, cudaMemcpyDeviceToDevice, st);
+    return launch_rc();
+}
+
+int ds4moe_route(ds4moe_t *h, const void *x, int32_t T, int32_t *idx_out, float *w_out) {
+    return ds4moe_route_detail(h, x, T, idx_out, w_out, nullptr, nullptr);
+}
+
+int ds4moe_forward_path(ds4moe_t *h, const void *x, int32_t T, int32_t path, float *y) {
+    int rc = check_call(h, x, T);
+    if (rc)
+        return rc;
+    if (path < DS4MOE_PATH_AUTO || path > DS4MOE_PATH_PREFILL)
+        return DS4MOE_EINVAL;
+    if (T == 0)
+        return DS4MOE_OK;
+    if (!is_device_ptr(y) || !aligned(y, 16))
+        return DS4MOE_EINVAL;
+    return forward_impl(h, x, T, path, y);
+}
+
+int ds4moe_forward(ds4moe_t *h, const void *x, int32_t T, float *y) {
+    return ds4moe_forward_path(h, x, T, DS4MOE_PATH_AUTO, y);
+}
+
+int ds4moe_forward_routed(ds4moe_t *h, const void *x, int32_t T, const int32_t *idx, const float *w,
+                          int32_t path, float *y) {
+    int rc = check_call(h, x, T);
+    if (rc)
+        return rc;
+    if (path < DS4MOE_PATH_AUTO || path > DS4MOE_PATH_PREFILL)
+        return DS4MOE_EINVAL;
+    if (T == 0)
+        return DS4MOE_OK;
+    if (!is_device_ptr(idx) || !is_device_ptr(w) || !is_device_ptr(y) || !aligned(y, 16))
+        return DS4MOE_EINVAL;
+    const LayerDev &L = h->L;
+    Scratch &S = h->S;
+    cudaStream_t st = h->stream;
+    h->stats = ds4moe_stats{};
+    h->stats.tokens = T;
+    h->stats.path = path == DS4MOE_PATH_AUTO ? (T <= 8 ? DS4MOE_PATH_DECODE : DS4MOE_PATH_PREFILL) : path;
+    rc = run_prep(h, x, T);
+    if (rc)
+        return rc;
+    cudaMemcpyAsync(S.idx, idx, sizeof(int32_t) * T * L.K, cudaMemcpyDeviceToDevice, st);
+    cudaMemcpyAsync(S.w, w, sizeof(float) * T * L.K, cudaMemcpyDeviceToDevice, st);
+    rc = launch_rc();
+    if (rc)
+        return rc;
+    return run_experts_simple(h, T, y);
+}
+
+int ds4moe_forward_host(ds4moe_t *h, const void *x_host, int32_t T, float *y_host) {
+    if (!h || T < 0 || T > h->L.Tmax)
+        return DS4MOE_EINVAL;
+    if (T == 0)
+        return DS4MOE_OK;
+    if (!x_host || !y_host)
+        return DS4MOE_EINVAL;
+    const LayerDev &L = h->L;
+    cudaStream_t st = h->stream;
+    int rc = cuda_rc(cudaMemcpyAsync(h->S.xstage, x_host, sizeof(uint16_t) * T * L.H, cudaMemcpyHostToDevice, st));
+    if (rc)
+        return rc;
+    rc = forward_impl(h, h->S.xstage, T, DS4MOE_PATH_AUTO, h->S.ystage);
+    if (rc)
+        return rc;
+    rc = cuda_rc(cudaMemcpyAsync(y_host, h->S.ystage, sizeof(float) * T * L.H, cudaMemcpyDeviceToHost, st));
+    if (rc)
+        return rc;
+    return cuda_rc(cudaStreamSynchronize(st));
+}
+
+int ds4moe_status(ds4moe_t *h) {
+    if (!h)
+        return DS4MOE_EINVAL;
+    int rc = cuda_rc(cudaStreamSynchronize(h->stream));
+    if (rc)
+        return rc;
+    unsigned bits = 0;
+    rc = cuda_rc(cudaMemcpy(&bits, h->status, sizeof(unsigned), cudaMemcpyDeviceToHost));
+    if (rc)
+        return rc;
+    if (bits)
+        cudaMemset(h->status, 0, sizeof(unsigned));
+    if (bits & kErrTimeout)
+        return DS4MOE_ETIMEOUT;
+    if (bits)
+        return DS4MOE_EDEVICE;
+    return DS4MOE_OK;
+}
+
+int ds4moe_get_stats(ds4moe_t *h, ds4moe_stats *out) {
+    if (!h || !out)
+        return DS4MOE_EINVAL;
+    int rc = cuda_rc(cudaStreamSynchronize(h->stream));
+    if (rc)
+        return rc;
+    *out = h->stats;
+    if (h->stats.tokens > 0) {
+        int32_t n = 0;
+        cudaMemcpy(&n, h->S.nuniq, sizeof(int32_t), cudaMemcpyDeviceToHost);
+        out->n_unique = n;
+        int32_t *counts = static_cast<int32_t *>(malloc(sizeof(int32_t) * h->L.E));
+        if (counts && cudaMemcpy(counts, h->S.counts, sizeof(int32_t) * h->L.E, cudaMemcpyDeviceToHost) ==
+                          cudaSuccess) {
+            int mx = 0;
+            for (int e = 0; e < h->L.E; e++)
+                mx = counts[e] > mx ? counts[e] : mx;
+            out->max_load = mx;
+        }
+        free(counts);
+    }
+    return cuda_rc(cudaGetLastError());
+}
+
+int ds4moe_profile(ds4moe_t *h, int32_t enable) {
+    if (!h)
+        return DS4MOE_EINVAL;
+    int rc = cuda_rc(cudaStreamSynchronize(h->stream));
+    if (rc)
+        return rc;
+    if (enable)
+        h->prof.clear();
+    else
+        h->prof.drain();
+    h->prof.on = enable != 0;
+    return DS4MOE_OK;
+}
+
+int ds4moe_profile_read(ds4moe_t *h, ds4moe_kernel_time *out, int32_t max, int32_t *n_out) {
+    if (!h || !n_out || max < 0 || (max > 0 && !out))
+        return DS4MOE_EINVAL;
+    int rc = cuda_rc(cudaStreamSynchronize(h->stream));
+    if (rc)
+        return rc;
+    h->prof.drain();
+    const int n = (int)h->prof.names.size();
+    for (int i = 0; i < n && i < max; i++) {
+        memset(out[i].name, 0, sizeof(out[i].name));
+        strncpy(out[i].name, h->prof.names[i].c_str(), sizeof(out[i].name) - 1);
+        out[i].launches = h->prof.launches[i];
+        out[i].total_ms = h->prof.total_ms[i];
+    }
+    *n_out = n;
+    return DS4MOE_OK;
+}
+
+int ds4moe_memory(ds4moe_t *h, uint64_t *weight_bytes, uint64_t *scratch_bytes) {
+    if (!h)
+        return DS4MOE_EINVAL;
+    if (weight_bytes)
+        *weight_bytes = h->weight_bytes;
+    if (scratch_bytes)
+        *scratch_bytes = h->scratch_bytes;
+    return DS4MOE_OK;
+}
+
+} // extern "C"

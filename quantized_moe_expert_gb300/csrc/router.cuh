@@ -1,0 +1,156 @@
+// Router: fp32 logits, sigmoid scores, exact top-k and renormalised weights.
+//
+// Scores are sigmoids of the logits; a per-expert bias, when present, is added
+// to the selection score only ("YoungAi - DeepSeek V4.1 Flash on one DGX
+// Spark", section 3: "selection score += delta-b", mixing weights untouched).
+// The top-k is exact on the fp32 selection score with equal scores resolved
+// towards the lower expert index, and the weights are the chosen sigmoid
+// scores divided by their sum.
+#pragma once
+
+#include "common.cuh"
+
+namespace ds4 {
+
+// x bf16 [T][H] -> x32 fp32 [T][H] and xsum [T][H/16]. One thread per
+// 16-element sub-block: two 16-byte loads, four 16-byte stores, one sum.
+__global__ void prep_x_kernel(const uint16_t *__restrict__ x, int T, int H, float *__restrict__ x32,
+                              float *__restrict__ xsum) {
+    const int64_t nsub = (int64_t)T * (H / 16);
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= nsub)
+        return;
+    const uint4 *src = reinterpret_cast<const uint4 *>(x + i * 16);
+    uint4 a = src[0], b = src[1];
+    uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    float v[16];
+    float s = 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; j++) {
+        v[2 * j] = __uint_as_float(w[j] << 16);
+        v[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+    }
+#pragma unroll
+    for (int j = 0; j < 16; j++)
+        s += v[j];
+    float4 *dst = reinterpret_cast<float4 *>(x32 + i * 16);
+#pragma unroll
+    for (int j = 0; j < 4; j++)
+        dst[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+    xsum[i] = s;
+}
+
+// logits[t][e] = sum_h x32[t][h] * Wr[e][h]. One warp per (expert, tile of up
+// to 8 tokens); each lane strides the row with 16-byte loads and keeps one
+// partial per token, then the warp reduces.
+constexpr int kRouterTok = 8;
+
+__global__ void router_logits_kernel(const float *__restrict__ x32, int T, int H, const float *__restrict__ wr,
+                                     int E, float *__restrict__ logits) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int e = blockIdx.x * (blockDim.x >> 5) + warp;
+    const int t0 = blockIdx.y * kRouterTok;
+    if (e >= E)
+        return;
+    const int nt = min(kRouterTok, T - t0);
+    float acc[kRouterTok];
+#pragma unroll
+    for (int t = 0; t < kRouterTok; t++)
+        acc[t] = 0.f;
+    const float4 *row = reinterpret_cast<const float4 *>(wr + (int64_t)e * H);
+    for (int c = lane; c < H / 4; c += 32) {
+        float4 wv = __ldg(row + c);
+#pragma unroll
+        for (int t = 0; t < kRouterTok; t++) {
+            if (t < nt) {
+                float4 xv = __ldg(reinterpret_cast<const float4 *>(x32 + (int64_t)(t0 + t) * H) + c);
+                acc[t] = fmaf(wv.x, xv.x, acc[t]);
+                acc[t] = fmaf(wv.y, xv.y, acc[t]);
+                acc[t] = fmaf(wv.z, xv.z, acc[t]);
+                acc[t] = fmaf(wv.w, xv.w, acc[t]);
+            }
+        }
+    }
+#pragma unroll
+    for (int t = 0; t < kRouterTok; t++) {
+        float v = warp_sum(acc[t]);
+        if (lane == 0 && t < nt)
+            logits[(int64_t)(t0 + t) * E + e] = v;
+    }
+}
+
+// One warp per token: selection scores into shared memory, then K+1 rounds of
+// a warp-wide arg-max ordered by (score desc, index asc). Round K+1 only
+// yields the runner-up score for the near-tie gap.
+constexpr int kSelectWarps = 4;
+
+__global__ void router_select_kernel(const float *__restrict__ logits, const float *__restrict__ bias, int T,
+                                     int E, int K, int32_t *__restrict__ idx, float *__restrict__ w,
+                                     float *__restrict__ gap, float *__restrict__ sel_out) {
+    extern __shared__ float smem[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int t = blockIdx.x * kSelectWarps + warp;
+    if (t >= T)
+        return;
+    float *sel = smem + warp * 2 * E;
+    float *score = sel + E;
+    for (int e = lane; e < E; e += 32) {
+        float s = sigmoid(logits[(int64_t)t * E + e]);
+        float v = bias ? s + bias[e] : s;
+        score[e] = s;
+        sel[e] = v;
+        if (sel_out)
+            sel_out[(int64_t)t * E + e] = v;
+    }
+    __syncwarp();
+    float chosen_s[kMaxTopK];
+    int chosen_e[kMaxTopK];
+    float kth = 0.f, next = -INFINITY;
+    const int rounds = K < E ? K + 1 : K;
+    for (int r = 0; r < rounds; r++) {
+        float bv = -INFINITY;
+        int be = 0x7FFFFFFF;
+        for (int e = lane; e < E; e += 32) {
+            float v = sel[e];
+            if (v > bv || (v == bv && e < be)) {
+                bv = v;
+                be = e;
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, o);
+            int oe = __shfl_xor_sync(0xFFFFFFFFu, be, o);
+            if (ov > bv || (ov == bv && oe < be)) {
+                bv = ov;
+                be = oe;
+            }
+        }
+        if (be >= E) // every remaining score was NaN: keep the index in range
+            be = 0;
+        if (r < K) {
+            chosen_e[r] = be;
+            chosen_s[r] = score[be];
+            if (r == K - 1)
+                kth = bv;
+            if (lane == (be & 31))
+                sel[be] = -INFINITY;
+            __syncwarp();
+        } else {
+            next = bv;
+        }
+    }
+    if (lane == 0) {
+        float total = 0.f;
+        for (int k = 0; k < K; k++)
+            total += chosen_s[k];
+        for (int k = 0; k < K; k++) {
+            idx[(int64_t)t * K + k] = chosen_e[k];
+            w[(int64_t)t * K + k] = total > 0.f ? chosen_s[k] / total : 1.0f / K;
+        }
+        if (gap)
+            gap[t] = K < E ? kth - next : INFINITY;
+    }
+}
+
+} // namespace ds4
