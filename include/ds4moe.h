@@ -69,7 +69,8 @@ enum {
     DS4MOE_ECUDA = -3,        /* a CUDA call or launch failed */
     DS4MOE_EUNSUPPORTED = -4, /* device is not compute capability 10.3 (GB300) */
     DS4MOE_ETIMEOUT = -5,     /* a bounded device-side wait gave up */
-    DS4MOE_EDEVICE = -6       /* a kernel reported an internal inconsistency */
+    DS4MOE_EDEVICE = -6,      /* a kernel reported an internal inconsistency */
+    DS4MOE_ESCRATCH = -7      /* request needs more than the fixed scratch of ds4moe_route_noalloc */
 };
 
 /* Execution paths for ds4moe_forward_path. */
@@ -195,6 +196,44 @@ typedef struct {
 
 int ds4moe_profile(ds4moe_t *h, int32_t enable);
 int ds4moe_profile_read(ds4moe_t *h, ds4moe_kernel_time *out, int32_t max, int32_t *n_out);
+
+/*
+ * Routing that allocates nothing. The pages have no counterpart; this entry
+ * point exists for callers that cannot allocate device memory at call time:
+ * an engine that reserves all of HBM for its own pools at start-up, or a
+ * latency-critical caller for whom cudaMalloc's implicit device-wide
+ * synchronisation is not acceptable. It also routes without building a handle
+ * (ds4moe_create copies the whole layer).
+ *
+ * Computes what ds4moe_route computes, from the caller's router weights:
+ *   router_w    device fp32 [E][H], 16-byte aligned
+ *   router_bias device fp32 [E] or NULL (added to the selection score only)
+ *   x_bf16      device bf16 [T][H], 16-byte aligned
+ *   idx_out     device int32 [T][K];  w_out device fp32 [T][K]
+ *   stream      cudaStream_t the kernels run on (NULL = legacy default stream)
+ * with H a multiple of 256, 1 <= E <= 1024, 1 <= K <= min(E, 8), T >= 0.
+ *
+ * The scratch (activations widened to fp32, their 16-element sums and the
+ * logits) is one statically allocated device array of DS4MOE_NOALLOC_SCRATCH
+ * bytes, which every GPU that loads the library keeps until the process
+ * exits. A call needs 4*T*(H + H/16 + E) bytes plus up to 768 bytes of
+ * alignment; larger requests return DS4MOE_ESCRATCH and launch nothing (with
+ * H=4096 and E=384 that is T <= 221). The call never calls cudaMalloc or
+ * cudaFree and launches three kernels on `stream`.
+ *
+ * The first call on each device, with that device current, resolves the
+ * array's device address (cudaGetSymbolAddress) and caches it; make that
+ * first call before any stream capture. All calls share the one array, which
+ * keeps the last call's contents (nothing in it needs to start at zero):
+ * calls whose kernels can overlap on the GPU, such as calls on different
+ * streams that are not ordered, race on it and must be serialised by the
+ * caller.
+ * Errors: EINVAL, ESCRATCH, EUNSUPPORTED (device not sm_103), ECUDA.
+ */
+#define DS4MOE_NOALLOC_SCRATCH (4u << 20)
+
+int ds4moe_route_noalloc(const float *router_w, const float *router_bias, const void *x_bf16, int32_t T,
+                         int32_t H, int32_t E, int32_t K, int32_t *idx_out, float *w_out, void *stream);
 
 /* Static string for a return code. */
 const char *ds4moe_strerror(int code);

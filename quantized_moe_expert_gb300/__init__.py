@@ -19,6 +19,8 @@ DS4MOE_MAGIC = 0x454D3444
 DS4MOE_VERSION = 1
 DS4MOE_OK, DS4MOE_EINVAL, DS4MOE_ENOMEM, DS4MOE_ECUDA, DS4MOE_EUNSUPPORTED, DS4MOE_ETIMEOUT, DS4MOE_EDEVICE = (
     0, -1, -2, -3, -4, -5, -6)
+DS4MOE_ESCRATCH = -7
+DS4MOE_NOALLOC_SCRATCH = 4 << 20
 PATH_AUTO, PATH_DECODE, PATH_PREFILL = 0, 1, 2
 
 
@@ -60,6 +62,7 @@ SIGNATURES = {
     "ds4moe_memory": (ctypes.c_int, [_vp, ctypes.POINTER(ctypes.c_uint64), ctypes.POINTER(ctypes.c_uint64)]),
     "ds4moe_profile": (ctypes.c_int, [_vp, _i32]),
     "ds4moe_profile_read": (ctypes.c_int, [_vp, ctypes.POINTER(KernelTime), _i32, ctypes.POINTER(_i32)]),
+    "ds4moe_route_noalloc": (ctypes.c_int, [_vp, _vp, _vp, _i32, _i32, _i32, _i32, _vp, _vp, _vp]),
     "ds4moe_strerror": (ctypes.c_char_p, [ctypes.c_int]),
 }
 
@@ -166,6 +169,13 @@ def ds4moe_profile_read(h: int) -> dict:
     n = _i32()
     _check(_lib.ds4moe_profile_read(h, buf, 64, ctypes.byref(n)), "ds4moe_profile_read")
     return {buf[i].name.decode(): (buf[i].launches, buf[i].total_ms) for i in range(min(n.value, 64))}
+
+
+def ds4moe_route_noalloc(router_w, router_bias, x, T: int, H: int, E: int, K: int, idx_out, w_out,
+                         stream=None):
+    """Routing from the caller's router weights with no device allocation (fixed static scratch)."""
+    _check(_lib.ds4moe_route_noalloc(_addr(router_w), _addr(router_bias), _addr(x), T, H, E, K, _addr(idx_out),
+                                     _addr(w_out), stream or None), "ds4moe_route_noalloc")
 
 
 def ds4moe_strerror(code: int) -> str:

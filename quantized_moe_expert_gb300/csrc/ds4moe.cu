@@ -5,6 +5,7 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
 #include <new>
 #include <string>
 #include <vector>
@@ -370,6 +371,8 @@ const char *ds4moe_strerror(int code) {
     case DS4MOE_EUNSUPPORTED: return "device is not a GB300 (compute capability 10.3)";
     case DS4MOE_ETIMEOUT: return "a bounded device-side wait timed out";
     case DS4MOE_EDEVICE: return "a kernel reported an inconsistency (e.g. an out-of-range expert index)";
+    case DS4MOE_ESCRATCH:
+        return "request needs more than the fixed DS4MOE_NOALLOC_SCRATCH bytes of ds4moe_route_noalloc";
     default: return "unknown ds4moe error";
     }
 }
@@ -678,3 +681,80 @@ int ds4moe_memory(ds4moe_t *h, uint64_t *weight_bytes, uint64_t *scratch_bytes) 
 }
 
 } // extern "C"
+
+// ---- routing without allocation ------------------------------------------------
+//
+// The scratch of ds4moe_route_noalloc lives in this file-scope device array.
+// Host code may not use the symbol as a pointer: its device address is
+// resolved once per device with cudaGetSymbolAddress and cached.
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[DS4MOE_NOALLOC_SCRATCH];
+
+namespace {
+
+constexpr int kNoAllocMaxDevices = 64;
+std::mutex g_noalloc_mutex;
+void *g_noalloc_ptr[kNoAllocMaxDevices] = {};
+
+// Device address of the scratch array on the current device.
+int noalloc_scratch(void **out) {
+    int dev = 0;
+    int rc = cuda_rc(cudaGetDevice(&dev));
+    if (rc)
+        return rc;
+    if (dev < 0 || dev >= kNoAllocMaxDevices)
+        return DS4MOE_EUNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (!g_noalloc_ptr[dev]) {
+        cudaDeviceProp prop;
+        rc = cuda_rc(cudaGetDeviceProperties(&prop, dev));
+        if (rc)
+            return rc;
+        if (prop.major != 10 || prop.minor != 3)
+            return DS4MOE_EUNSUPPORTED;
+        void *p = nullptr;
+        rc = cuda_rc(cudaGetSymbolAddress(&p, g_noalloc_scratch));
+        if (rc)
+            return rc;
+        g_noalloc_ptr[dev] = p;
+    }
+    *out = g_noalloc_ptr[dev];
+    return DS4MOE_OK;
+}
+
+uint64_t round256(uint64_t n) { return (n + 255) & ~uint64_t(255); }
+
+} // namespace
+
+extern "C" int ds4moe_route_noalloc(const float *router_w, const float *router_bias, const void *x_bf16,
+                                    int32_t T, int32_t H, int32_t E, int32_t K, int32_t *idx_out, float *w_out,
+                                    void *stream) {
+    if (T < 0 || H <= 0 || H % 256 || E < 1 || E > 1024 || K < 1 || K > kMaxTopK || K > E)
+        return DS4MOE_EINVAL;
+    if (T == 0)
+        return DS4MOE_OK;
+    if (!is_device_ptr(router_w) || !aligned(router_w, 16) || !is_device_ptr(x_bf16) || !aligned(x_bf16, 16) ||
+        !is_device_ptr(idx_out) || !is_device_ptr(w_out) || (router_bias && !is_device_ptr(router_bias)))
+        return DS4MOE_EINVAL;
+    const uint64_t x32_bytes = round256(4ull * T * H);
+    const uint64_t xsum_bytes = round256(4ull * T * (H / 16));
+    const uint64_t logit_bytes = round256(4ull * T * E);
+    if (x32_bytes + xsum_bytes + logit_bytes > DS4MOE_NOALLOC_SCRATCH)
+        return DS4MOE_ESCRATCH;
+    void *base = nullptr;
+    int rc = noalloc_scratch(&base);
+    if (rc)
+        return rc;
+    float *x32 = static_cast<float *>(base);
+    float *xsum = reinterpret_cast<float *>(static_cast<char *>(base) + x32_bytes);
+    float *logits = reinterpret_cast<float *>(static_cast<char *>(base) + x32_bytes + xsum_bytes);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    prep_x_kernel<<<blocks_for((int64_t)T * (H / 16), 256), 256, 0, st>>>(static_cast<const uint16_t *>(x_bf16), T,
+                                                                         H, x32, xsum);
+    router_logits_kernel<<<dim3(blocks_for(E, 8), blocks_for(T, kRouterTok)), 256, 0, st>>>(x32, T, H, router_w, E,
+                                                                                          logits);
+    const size_t smem = (size_t)kSelectWarps * 2 * E * sizeof(float);
+    router_select_kernel<<<blocks_for(T, kSelectWarps), 32 * kSelectWarps, smem, st>>>(
+        logits, router_bias, T, E, K, idx_out, w_out, nullptr, nullptr);
+    return launch_rc();
+}

@@ -29,7 +29,7 @@ def test_library_exports_every_declared_symbol():
 
 
 def test_strerror_names_every_code():
-    for code in (0, -1, -2, -3, -4, -5, -6):
+    for code in (0, -1, -2, -3, -4, -5, -6, -7):
         assert ds4.ds4moe_strerror(code) not in ("", "unknown ds4moe error")
     assert ds4.ds4moe_strerror(-99) == "unknown ds4moe error"
 
