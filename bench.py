@@ -77,6 +77,8 @@ def kernel_bytes(name, shape, T, U):
         "simple_gateup_q8": 2 * Ish * H * Q8_BPW + 4 * T * H + 4 * T * Ish,
         "simple_down_q8": H * Ish * Q8_BPW + 4 * T * Ish + 4 * T * H,
         "combine": 4 * P * H + 4 * T * H + 4 * T * H,
+        # one launch of the fused decode kernel does the whole layer for up to 8 tokens
+        "decode_fused": layer_bytes(shape, T, U),
     }
     return table.get(name)
 

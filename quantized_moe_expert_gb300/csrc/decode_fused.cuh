@@ -1,0 +1,1404 @@
+// Decode path (T <= 8 tokens per launch): one persistent cooperative kernel.
+//
+// Each CTA is one producer warp and eight consumer warps. The producer's lane
+// 0 pulls jobs from a global queue (an atomic counter) and streams each job's
+// weight tiles and activation rows into a ring of shared-memory stages with
+// bulk asynchronous copies (cp.async.bulk completing on an mbarrier); the
+// consumer warps multiply them on the tensor cores (mma.sync, see the layouts
+// in frag_layout.cuh) and release the stage. Stages hold up to 192 KB per SM
+// in flight, independent of registers, so the weight stream can run at the
+// HBM rate.
+//
+// Jobs are numbered so that each depends only on jobs with smaller numbers,
+// and a CTA takes its jobs in increasing order, so the oldest unfinished job
+// can always run: the queue cannot deadlock as long as all CTAs are resident,
+// which the cooperative launch guarantees. The queue, in order:
+//
+//   R    one router row: fp32 logits for all T tokens
+//   SGU  shared expert, one 16-row tile of gate and up: h_sh = silu(g) * u
+//   SEL  one job: per-token sigmoid, exact top-k, weights; activation
+//        pre-scaling for the 2-bit MMA; distinct-expert grouping; publishes
+//        the routing (waits for all R jobs)
+//   GU   (distinct expert, 16-row tile of I): gate and up, h = silu(g) * u,
+//        stored as a bf16 hi/lo pair pre-scaled for the down MMA
+//   SD   shared expert down, one 16-row tile of H (waits: all SGU)
+//   D    (distinct expert, 16-row tile of H): down projection (waits: that
+//        expert's GU tiles); the last contribution to a tile combines it:
+//        y = sum_k w_k ye_k + ysh, in fixed order
+// The producer resolves the addresses of GU, SD and D jobs after the routing
+// is published; the weight loads of a job never wait for its data
+// dependencies, only its consumers do, so loads overlap those waits.
+//
+// This follows the pages' decode engine in spirit - routed experts and the
+// shared expert proceed side by side ("YoungAi - DeepSeek V4.1 Flash on one
+// DGX Spark", section 4.4, "Side stream"), each distinct expert's bits are read
+// once for all rows that chose it (same section, verify batch), and work
+// starts on data that does not depend on its producer (same section,
+// "Programmatic dependent launch") - but as one kernel with fine-grained
+// dependencies instead of a chain of launches.
+//
+// Every wait is bounded (kWaitNs of %globaltimer); a wait that runs out sets
+// kErrTimeout in the status word and an abort flag that makes every CTA drain
+// its ring and leave.
+#pragma once
+
+#include "common.cuh"
+#include "frag_layout.cuh"
+
+namespace ds4 {
+
+constexpr int kDecodeT = 8;             // tokens per launch
+constexpr int kMaxSlots = 64;           // distinct experts per launch <= 8 tokens * top-8
+constexpr uint64_t kWaitNs = 500000000; // 0.5 s
+constexpr int kRing = 3;                // shared-memory stages per CTA (two CTAs per SM)
+constexpr int kSlotBytes = 28672;       // bytes per stage
+constexpr int kConsumerWarps = 8;
+constexpr int kDecodeThreads = 32 * (kConsumerWarps + 1);
+
+// Control words (zeroed at create; every launch leaves them zeroed again).
+enum : int {
+    kCtlJobNext = 0,
+    kCtlRouterDone = 1,
+    kCtlRoutingEpoch = 2,
+    kCtlSguDone = 3,
+    kCtlFinished = 4,
+    kCtlAbort = 5,
+    kCtlGuDone = 8,              // [kMaxSlots]
+    kCtlTileCnt = 8 + kMaxSlots, // [H / 16]
+};
+
+struct DecodeArgs {
+    int H, I, E, K, Ish;
+    const float *router_w, *router_bias;
+    Q2Frag gate, up, down;
+    Q8Frag sh_gate, sh_up, sh_down;
+    const uint16_t *x; // [T][H] bf16
+    int T;
+    float *y;                  // [T][H]
+    const int32_t *forced_idx; // [T][K] or nullptr
+    const float *forced_w;
+    unsigned epoch;
+    float *logits;   // [8][E]
+    int32_t *idx;    // [8][K]
+    float *w;        // [8][K]
+    float *gap;      // [8]
+    int32_t *counts; // [E]
+    int32_t *nuniq, *uexp, *uoff, *perm, *inv;
+    uint16_t *xq;            // [8][H] bf16 x * 2^e(k)
+    float *xoff, *xsum;      // [8][H/16]
+    uint16_t *hq_hi, *hq_lo; // [64][I] bf16 h * 2^e(k) as hi + lo
+    float *hoff, *hsum;      // [64][I/16]
+    uint16_t *hs_hi, *hs_lo; // [8][Ish] binary16 shared h as hi + lo
+    float *ye;               // [64][H]
+    float *ysh;              // [8][H]
+    unsigned *ctl;
+    unsigned *status;
+};
+
+enum JobType : int { kJobEnd = 0, kJobR, kJobSgu, kJobSel, kJobGu, kJobSd, kJobD };
+
+// What the producer tells the consumers about one stage.
+struct StageDesc {
+    int type;
+    int a0;         // R: expert row; GU/D: distinct-expert slot; SGU/SD: tile
+    int tile;       // GU/D: 16-row tile within the expert
+    int sub, nsub;  // sub-stage index and count of the job
+    int c0, W;      // column range [c0, c0 + W) of this sub-stage
+    int ntok, tp;   // tokens of the job and their count padded to 1, 2, 4 or 8
+    int nuniq;      // distinct experts of this launch (GU, SD, D)
+    int pos[kDecodeT]; // pair position of each token column (GU, D outputs)
+    int tok[kDecodeT]; // token of each column
+    int oq[2], os[2], od[2]; // byte offsets of the matrix pieces (codes, scales, d/dmin)
+    int oact, olo, ooff, osum; // activation pieces
+    int act_pitch, sub_pitch;  // bytes per token row of the hi/lo and off/sum pieces
+};
+
+struct DecodeSmem {
+    alignas(128) uint8_t ring[kRing][kSlotBytes];
+    StageDesc desc[kRing];
+    alignas(8) uint64_t full[kRing];
+    alignas(8) uint64_t empty[kRing];
+    float part[2][kConsumerWarps][2][16][kDecodeT]; // per-warp partial sums, double-buffered by job
+    int flag;
+    int sel_idx[kDecodeT][kMaxTopK];
+    unsigned bitmap[32];
+    int word_prefix[32];
+    int slot_cnt[kMaxSlots];
+    // the producer's list of bulk copies for the stage it is building
+    const void *pc_src[40];
+    unsigned pc_bytes[40];
+    unsigned pc_dst[40];
+};
+
+// ---- small PTX helpers --------------------------------------------------------
+
+__device__ __forceinline__ uint64_t globaltimer() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ unsigned ld_acquire(const unsigned *p) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_release(unsigned *p, unsigned v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+                 "{%0,%1,%2,%3};"
+                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                 : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                        uint32_t b0, uint32_t b1) {
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+                 "{%0,%1,%2,%3};"
+                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                 : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t lop3_magic(uint32_t v, uint32_t mask) {
+    uint32_t r;
+    // (v & mask) | 0x3F803F80
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(v), "r"(mask), "r"(0x3F803F80u));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+    uint32_t r;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t hsub2_1152(uint32_t v) {
+    uint32_t r;
+    const uint32_t c = 0x64806480u; // binary16 1152 in both halves
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(v), "r"(c));
+    return r;
+}
+
+// bf16 pair (as u32) -> binary16 pair, round to nearest.
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v) {
+    const float lo = __uint_as_float(v << 16), hi = __uint_as_float(v & 0xFFFF0000u);
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// bf16 bits of v, round to nearest even (v finite).
+__device__ __forceinline__ uint32_t f32_to_bf16_bits(float v) {
+    uint32_t u = __float_as_uint(v);
+    return (u + 0x7FFFu + ((u >> 16) & 1u)) >> 16;
+}
+
+__device__ __forceinline__ float nib_to_f(uint32_t n) { return __uint_as_float(0x4B000000u | n) - 8388608.0f; }
+
+__device__ __forceinline__ unsigned ld_relaxed(const unsigned *p) {
+    unsigned v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// One thread waits until *p >= target (or == target when eq): relaxed polls
+// with a short sleep between them, one acquire fence once the value is seen.
+// Returns false after kWaitNs or when another CTA aborted.
+__device__ bool wait_counter(const DecodeArgs &a, const unsigned *p, unsigned target, bool eq) {
+    uint64_t t0 = 0;
+    for (unsigned it = 0;; it++) {
+        const unsigned v = ld_relaxed(p);
+        if (eq ? v == target : v >= target) {
+            __threadfence();
+            return true;
+        }
+        if ((it & 63) == 0) {
+            if (ld_relaxed(a.ctl + kCtlAbort))
+                return false;
+            const uint64_t now = globaltimer();
+            if (it == 0)
+                t0 = now;
+            else if (now - t0 > kWaitNs) {
+                atomicOr(a.status, kErrTimeout);
+                atomicExch(a.ctl + kCtlAbort, 1u);
+                return false;
+            }
+        }
+        __nanosleep(128);
+    }
+}
+
+// ---- mbarrier, bulk copy and barrier helpers ------------------------------------
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, unsigned count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_tx(uint64_t *bar, unsigned bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, unsigned parity) {
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok)
+                 : "r"(smem_u32(bar)), "r"(parity)
+                 : "memory");
+    return ok != 0;
+}
+
+// Bounded wait for the completion of the phase with the given parity.
+__device__ __forceinline__ bool mbar_wait(const DecodeArgs &a, uint64_t *bar, unsigned parity) {
+    if (mbar_try_wait(bar, parity))
+        return true;
+    uint64_t t0 = 0;
+    for (unsigned it = 0;; it++) {
+        if (mbar_try_wait(bar, parity))
+            return true;
+        if ((it & 255) == 0) {
+            const uint64_t now = globaltimer();
+            if (it == 0)
+                t0 = now;
+            else if (now - t0 > kWaitNs) {
+                atomicOr(a.status, kErrTimeout);
+                atomicExch(a.ctl + kCtlAbort, 1u);
+                return false;
+            }
+        }
+        __nanosleep(32);
+    }
+}
+
+// Global -> shared bulk copy completing on `bar` (16-byte aligned, size % 16 == 0).
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, unsigned bytes, uint64_t *bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_u32(dst)),
+                 "l"(src), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
+
+// Barrier of the eight consumer warps (the producer warp does not take part).
+__device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+
+// ---- tensor-core tile GEMV over one stage -----------------------------------------
+//
+// A warp multiplies one 16-row tile by TP token columns (1, 2, 4 or 8). The 8
+// columns of each m16n8k16 MMA are (slot, token) pairs with 8/TP slots:
+// chunk c (16 columns) feeds only the columns of slot c % (8/TP), so one
+// accumulator tile holds 8/TP chunks' dot products side by side and each
+// chunk's scale is applied once per accumulator tile rather than per MMA.
+// out[m][rr][col] accumulates row g + 8*rr (g = lane/4) and token
+// (2*(lane%4) + col) % TP over the warp's columns; reduce_out combines the
+// lanes that share a (row, token) at the end of the job.
+
+template <int TP> __device__ __forceinline__ int srow(const StageDesc &d, int t) { return t < d.ntok ? t : 0; }
+
+// 2-bit matrices (NMAT of them share the activations) over the stage's kc
+// range of this warp. Activations in the stage: bf16 pairs of x * 2^e(k)
+// (and the low parts when SPLIT), per-sub-block offset sums and plain sums.
+template <int TP, int NMAT, bool SPLIT>
+__device__ __forceinline__ void q2_stage(const uint8_t *sl, const StageDesc &d, int warp, int lane,
+                                         float (&out)[2][2][2]) {
+    constexpr int S = 8 / TP;
+    const int g = lane >> 2, tig = lane & 3;
+    const int bs = g / TP, bt = g % TP;
+    const int n0 = 2 * tig, n1 = 2 * tig + 1;
+    const int s0 = n0 / TP, t0 = n0 % TP, s1 = n1 / TP, t1 = n1 % TP;
+    const int nkc = d.W >> 7;
+    const int kb = nkc * warp / kConsumerWarps, ke = nkc * (warp + 1) / kConsumerWarps;
+    const uint32_t *act = reinterpret_cast<const uint32_t *>(sl + d.oact + srow<TP>(d, bt) * d.act_pitch);
+    const uint32_t *act_lo = reinterpret_cast<const uint32_t *>(sl + d.olo + srow<TP>(d, bt) * d.act_pitch);
+    const float *off0 = reinterpret_cast<const float *>(sl + d.ooff + srow<TP>(d, t0) * d.sub_pitch);
+    const float *sum0 = reinterpret_cast<const float *>(sl + d.osum + srow<TP>(d, t0) * d.sub_pitch);
+    const float *off1 = reinterpret_cast<const float *>(sl + d.ooff + srow<TP>(d, t1) * d.sub_pitch);
+    const float *sum1 = reinterpret_cast<const float *>(sl + d.osum + srow<TP>(d, t1) * d.sub_pitch);
+    float asc[NMAT][2][2], amn[NMAT][2][2];
+#pragma unroll
+    for (int m = 0; m < NMAT; m++)
+#pragma unroll
+        for (int r = 0; r < 2; r++)
+            asc[m][r][0] = asc[m][r][1] = amn[m][r][0] = amn[m][r][1] = 0.f;
+    for (int kc = kb; kc < ke; kc++) {
+        uint4 q[NMAT], s[NMAT];
+#pragma unroll
+        for (int m = 0; m < NMAT; m++) {
+            q[m] = reinterpret_cast<const uint4 *>(sl + d.oq[m])[kc * 32 + lane];
+            s[m] = reinterpret_cast<const uint4 *>(sl + d.os[m])[kc * 8 + g];
+        }
+        const int colbase = kc * 128 + 2 * tig; // column within the stage
+#pragma unroll
+        for (int nt = 0; nt < 8 / S; nt++) {
+            // two accumulators (even and odd slots) halve the dependent MMA chain
+            float D[NMAT][4], D2[NMAT][4];
+#pragma unroll
+            for (int m = 0; m < NMAT; m++)
+#pragma unroll
+                for (int i = 0; i < 4; i++)
+                    D[m][i] = D2[m][i] = 0.f;
+#pragma unroll
+            for (int sl2 = 0; sl2 < S; sl2++) {
+                const int c = nt * S + sl2; // chunk 0..7 within kc
+                const int G = c >> 2, cc = c & 3;
+                const int r_lo = 2 * cc, r_hi = 2 * cc + 1;
+                const bool on = bs == sl2;
+                const int col = colbase + 16 * c;
+                const uint32_t b0 = on ? act[col >> 1] : 0u;
+                const uint32_t b1 = on ? act[(col + 8) >> 1] : 0u;
+                uint32_t c0 = 0, c1 = 0;
+                if (SPLIT) {
+                    c0 = on ? act_lo[col >> 1] : 0u;
+                    c1 = on ? act_lo[(col + 8) >> 1] : 0u;
+                }
+#pragma unroll
+                for (int m = 0; m < NMAT; m++) {
+                    const uint32_t wg = G ? q[m].z : q[m].x, wg8 = G ? q[m].w : q[m].y;
+                    constexpr uint32_t k3 = 0x00030003u;
+                    const uint32_t a0 = lop3_magic(wg >> frag_shift(r_lo), k3 << frag_pos(r_lo));
+                    const uint32_t a1 = lop3_magic(wg8 >> frag_shift(r_lo), k3 << frag_pos(r_lo));
+                    const uint32_t a2 = lop3_magic(wg >> frag_shift(r_hi), k3 << frag_pos(r_hi));
+                    const uint32_t a3 = lop3_magic(wg8 >> frag_shift(r_hi), k3 << frag_pos(r_hi));
+                    if (SPLIT) { // hi parts and lo parts in separate chains
+                        mma_bf16(D[m], a0, a1, a2, a3, b0, b1);
+                        mma_bf16(D2[m], a0, a1, a2, a3, c0, c1);
+                    } else {
+                        float(&acc)[4] = (sl2 & 1) ? D2[m] : D[m];
+                        mma_bf16(acc, a0, a1, a2, a3, b0, b1);
+                    }
+                }
+            }
+#pragma unroll
+            for (int m = 0; m < NMAT; m++)
+#pragma unroll
+                for (int i = 0; i < 4; i++)
+                    D[m][i] += D2[m][i];
+            // scale and min terms of the accumulator tile, per (row, chunk)
+            const int ca = nt * S + s0, cb = nt * S + s1;
+            const int ja = kc * 8 + ca, jb = kc * 8 + cb;
+            const float oa = off0[ja], ua = sum0[ja], ob = off1[jb], ub = sum1[jb];
+            const int sha = 8 * (ca & 3), shb = 8 * (cb & 3);
+#pragma unroll
+            for (int m = 0; m < NMAT; m++) {
+                const uint32_t ba = ((ca < 4 ? s[m].x : s[m].y) >> sha) & 0xFFu;
+                const uint32_t bb = ((cb < 4 ? s[m].x : s[m].y) >> shb) & 0xFFu;
+                const uint32_t ba8 = ((ca < 4 ? s[m].z : s[m].w) >> sha) & 0xFFu;
+                const uint32_t bb8 = ((cb < 4 ? s[m].z : s[m].w) >> shb) & 0xFFu;
+                asc[m][0][0] = fmaf(nib_to_f(ba & 15u), D[m][0] - oa, asc[m][0][0]);
+                amn[m][0][0] = fmaf(nib_to_f(ba >> 4), ua, amn[m][0][0]);
+                asc[m][0][1] = fmaf(nib_to_f(bb & 15u), D[m][1] - ob, asc[m][0][1]);
+                amn[m][0][1] = fmaf(nib_to_f(bb >> 4), ub, amn[m][0][1]);
+                asc[m][1][0] = fmaf(nib_to_f(ba8 & 15u), D[m][2] - oa, asc[m][1][0]);
+                amn[m][1][0] = fmaf(nib_to_f(ba8 >> 4), ua, amn[m][1][0]);
+                asc[m][1][1] = fmaf(nib_to_f(bb8 & 15u), D[m][3] - ob, asc[m][1][1]);
+                amn[m][1][1] = fmaf(nib_to_f(bb8 >> 4), ub, amn[m][1][1]);
+            }
+        }
+        // end of a 256-column block (stages start on block boundaries) or of this
+        // warp's range: apply the block's d and dmin
+        if ((kc & 1) == 1 || kc + 1 == ke) {
+#pragma unroll
+            for (int m = 0; m < NMAT; m++) {
+                const uint2 dw = reinterpret_cast<const uint2 *>(sl + d.od[m])[(kc >> 1) * 8 + g];
+                const float dg = f16_to_f32(dw.x), mg = f16_to_f32(dw.x >> 16);
+                const float dg8 = f16_to_f32(dw.y), mg8 = f16_to_f32(dw.y >> 16);
+#pragma unroll
+                for (int col = 0; col < 2; col++) {
+                    out[m][0][col] += dg * asc[m][0][col] - mg * amn[m][0][col];
+                    out[m][1][col] += dg8 * asc[m][1][col] - mg8 * amn[m][1][col];
+                    asc[m][0][col] = asc[m][1][col] = amn[m][0][col] = amn[m][1][col] = 0.f;
+                }
+            }
+        }
+    }
+}
+
+// 8-bit matrices: A = the codes as exact binary16 integers, B = binary16
+// activations (FROM_BF16: the stage holds bf16 rows, converted here); each slot
+// of an accumulator tile is one 32-column block (one scale).
+template <int TP, int NMAT, bool SPLIT, bool FROM_BF16>
+__device__ __forceinline__ void q8_stage(const uint8_t *sl, const StageDesc &d, int warp, int lane,
+                                         float (&out)[2][2][2]) {
+    constexpr int S = 8 / TP;
+    const int g = lane >> 2, tig = lane & 3;
+    const int bs = g / TP, bt = g % TP;
+    const int n0 = 2 * tig, n1 = 2 * tig + 1;
+    const int s0 = n0 / TP, s1 = n1 / TP;
+    const int nbq = d.W >> 5;
+    const int bb = nbq * warp / kConsumerWarps, be = nbq * (warp + 1) / kConsumerWarps;
+    const uint32_t *act = reinterpret_cast<const uint32_t *>(sl + d.oact + srow<TP>(d, bt) * d.act_pitch);
+    const uint32_t *act_lo = reinterpret_cast<const uint32_t *>(sl + d.olo + srow<TP>(d, bt) * d.act_pitch);
+    for (int base = bb; base < be; base += S) {
+        float D[NMAT][4], D2[NMAT][4];
+#pragma unroll
+        for (int m = 0; m < NMAT; m++)
+#pragma unroll
+            for (int i = 0; i < 4; i++)
+                D[m][i] = D2[m][i] = 0.f;
+#pragma unroll
+        for (int sl2 = 0; sl2 < S; sl2++) {
+            const int bq = base + sl2;
+            if (bq < be) {
+                uint4 q[NMAT];
+#pragma unroll
+                for (int m = 0; m < NMAT; m++)
+                    q[m] = reinterpret_cast<const uint4 *>(sl + d.oq[m])[bq * 32 + lane];
+                const bool on = bs == sl2;
+#pragma unroll
+                for (int c = 0; c < 2; c++) {
+                    const int col = bq * 32 + 16 * c + 2 * tig;
+                    uint32_t b0 = on ? act[col >> 1] : 0u, b1 = on ? act[(col + 8) >> 1] : 0u;
+                    if (FROM_BF16) {
+                        b0 = bf16x2_to_f16x2(b0);
+                        b1 = bf16x2_to_f16x2(b1);
+                    }
+                    uint32_t c0 = 0, c1 = 0;
+                    if (SPLIT) {
+                        c0 = on ? act_lo[col >> 1] : 0u;
+                        c1 = on ? act_lo[(col + 8) >> 1] : 0u;
+                    }
+#pragma unroll
+                    for (int m = 0; m < NMAT; m++) {
+                        const uint32_t vg = c ? q[m].z : q[m].x, vg8 = c ? q[m].w : q[m].y;
+                        const uint32_t a0 = hsub2_1152(prmt(vg, 0x64646464u, 0x4140u));
+                        const uint32_t a1 = hsub2_1152(prmt(vg8, 0x64646464u, 0x4140u));
+                        const uint32_t a2 = hsub2_1152(prmt(vg, 0x64646464u, 0x4342u));
+                        const uint32_t a3 = hsub2_1152(prmt(vg8, 0x64646464u, 0x4342u));
+                        if (SPLIT) {
+                            mma_f16(D[m], a0, a1, a2, a3, b0, b1);
+                            mma_f16(D2[m], a0, a1, a2, a3, c0, c1);
+                        } else {
+                            mma_f16(c ? D2[m] : D[m], a0, a1, a2, a3, b0, b1);
+                        }
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int m = 0; m < NMAT; m++)
+#pragma unroll
+            for (int i = 0; i < 4; i++)
+                D[m][i] += D2[m][i];
+        const int bqa = base + s0, bqb = base + s1;
+#pragma unroll
+        for (int m = 0; m < NMAT; m++) {
+            const uint32_t *dv = reinterpret_cast<const uint32_t *>(sl + d.od[m]);
+            if (bqa < be) {
+                const uint32_t dw = dv[bqa * 8 + g];
+                out[m][0][0] = fmaf(f16_to_f32(dw), D[m][0], out[m][0][0]);
+                out[m][1][0] = fmaf(f16_to_f32(dw >> 16), D[m][2], out[m][1][0]);
+            }
+            if (bqb < be) {
+                const uint32_t dw = dv[bqb * 8 + g];
+                out[m][0][1] = fmaf(f16_to_f32(dw), D[m][1], out[m][0][1]);
+                out[m][1][1] = fmaf(f16_to_f32(dw >> 16), D[m][3], out[m][1][1]);
+            }
+        }
+    }
+}
+
+// Combine the lanes that hold the same (row, token) at the end of a job.
+template <int TP, int NMAT> __device__ __forceinline__ void reduce_out(float (&out)[2][2][2]) {
+#pragma unroll
+    for (int m = 0; m < NMAT; m++)
+#pragma unroll
+        for (int r = 0; r < 2; r++) {
+            if (TP == 1) {
+                out[m][r][0] += out[m][r][1];
+                out[m][r][1] = 0.f;
+            }
+#pragma unroll
+            for (int col = 0; col < 2; col++) {
+                float v = out[m][r][col];
+                if (TP <= 2) {
+                    v += __shfl_xor_sync(0xFFFFFFFFu, v, 1);
+                    v += __shfl_xor_sync(0xFFFFFFFFu, v, 2);
+                } else if (TP == 4) {
+                    v += __shfl_xor_sync(0xFFFFFFFFu, v, 2);
+                }
+                out[m][r][col] = v;
+            }
+        }
+}
+
+// Lanes holding final (row, token) values and the token of each of their columns.
+template <int TP> __device__ __forceinline__ bool tile_owner(int lane) {
+    const int tig = lane & 3;
+    return TP <= 2 ? tig == 0 : (TP == 4 ? tig < 2 : true);
+}
+
+template <int TP, int NMAT>
+__device__ __forceinline__ void store_part(DecodeSmem &sm, int buf, int warp, int lane, const float (&out)[2][2][2]) {
+    if (!tile_owner<TP>(lane))
+        return;
+    const int g = lane >> 2;
+#pragma unroll
+    for (int m = 0; m < NMAT; m++)
+#pragma unroll
+        for (int col = 0; col < 2; col++) {
+            if (TP == 1 && col == 1)
+                continue;
+            const int t = (2 * (lane & 3) + col) % TP;
+            sm.part[buf][warp][m][g][t] = out[m][0][col];
+            sm.part[buf][warp][m][g + 8][t] = out[m][1][col];
+        }
+}
+
+// Router row over the stage: fp32 weights at oq[0], bf16 x rows at oact; warp
+// w takes columns [w W/8, (w+1) W/8). out (as 8 floats) accumulates token t's
+// partial dot product in each lane.
+__device__ __forceinline__ void router_stage(const uint8_t *sl, const StageDesc &d, int T, int warp, int lane,
+                                             float (&out)[2][2][2]) {
+    float *acc = &out[0][0][0];
+    const float4 *wr = reinterpret_cast<const float4 *>(sl + d.oq[0]);
+    const int n4 = d.W >> 2;
+    const int b = n4 * warp / kConsumerWarps, e = n4 * (warp + 1) / kConsumerWarps;
+#pragma unroll 4
+    for (int i = b + lane; i < e; i += 32) {
+        const float4 wv = wr[i];
+#pragma unroll
+        for (int t = 0; t < kDecodeT; t++) {
+            if (t < T) {
+                const uint2 xv = reinterpret_cast<const uint2 *>(sl + d.oact + t * d.act_pitch)[i];
+                acc[t] = fmaf(wv.x, __uint_as_float(xv.x << 16), acc[t]);
+                acc[t] = fmaf(wv.y, __uint_as_float(xv.x & 0xFFFF0000u), acc[t]);
+                acc[t] = fmaf(wv.z, __uint_as_float(xv.y << 16), acc[t]);
+                acc[t] = fmaf(wv.w, __uint_as_float(xv.y & 0xFFFF0000u), acc[t]);
+            }
+        }
+    }
+}
+
+// Top-k of one token by one warp. Lane l holds the scores of experts
+// l + 32 i, i < NV, in registers. Each lane keeps its own best candidate;
+// each round the warp takes the best of the 32 candidates (score desc, index
+// asc) and only the lane that lost its candidate looks for its next one.
+template <int NV>
+__device__ __forceinline__ void select_token(const DecodeArgs &a, DecodeSmem &sm, int t, int lane, bool warm) {
+    const int E = a.E, K = a.K;
+    float sel[NV], sco[NV];
+    // unconditional (clamped) loads first, so that all NV loads are in flight together
+    float lg[NV], bi[NV];
+#pragma unroll
+    for (int i = 0; i < NV; i++) {
+        const int e = min(lane + 32 * i, E - 1);
+        lg[i] = __ldcg(a.logits + t * E + e);
+        bi[i] = a.router_bias ? __ldg(a.router_bias + e) : 0.f;
+    }
+#pragma unroll
+    for (int i = 0; i < NV; i++) {
+        const int e = lane + 32 * i;
+        const float s = sigmoid(lg[i]);
+        sco[i] = e < E ? s : 0.f;
+        sel[i] = e < E ? (a.router_bias ? s + bi[i] : s) : -INFINITY;
+    }
+    // the lane's best candidate: highest score, lowest index among equals
+    float cv = -INFINITY;
+    int ci = -1;
+#pragma unroll
+    for (int i = 0; i < NV; i++)
+        if (lane + 32 * i < E && (ci < 0 || sel[i] > cv)) {
+            cv = sel[i];
+            ci = i;
+        }
+    float chosen_s = 0.f, total = 0.f, kth = 0.f, next = -INFINITY;
+    int chosen_e = 0;
+    const int rounds = K < E ? K + 1 : K;
+    for (int r = 0; r < rounds; r++) {
+        float bv = cv;
+        int be = ci < 0 ? 0x7FFFFFFF : lane + 32 * ci;
+        float bs = 0.f;
+#pragma unroll
+        for (int i = 0; i < NV; i++)
+            if (i == ci)
+                bs = sco[i];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, o);
+            const int oe = __shfl_xor_sync(0xFFFFFFFFu, be, o);
+            const float os = __shfl_xor_sync(0xFFFFFFFFu, bs, o);
+            if (ov > bv || (ov == bv && oe < be)) {
+                bv = ov;
+                be = oe;
+                bs = os;
+            }
+        }
+        if (be >= E) // every remaining score was NaN: keep the index in range
+            be = 0;
+        if (r < K) {
+            if (lane == r) {
+                chosen_e = be;
+                chosen_s = bs;
+            }
+            total += bs;
+            if (r == K - 1)
+                kth = bv;
+            if (ci >= 0 && lane + 32 * ci == be) { // this lane's candidate was taken
+#pragma unroll
+                for (int i = 0; i < NV; i++)
+                    if (i == ci)
+                        sel[i] = -INFINITY;
+                cv = -INFINITY;
+                ci = -1;
+#pragma unroll
+                for (int i = 0; i < NV; i++)
+                    if (lane + 32 * i < E && (ci < 0 || sel[i] > cv)) {
+                        cv = sel[i];
+                        ci = i;
+                    }
+            }
+        } else {
+            next = bv;
+        }
+    }
+    if (lane < K) {
+        sm.sel_idx[t][lane] = chosen_e;
+        if (!warm) {
+            a.idx[t * K + lane] = chosen_e;
+            a.w[t * K + lane] = total > 0.f ? chosen_s / total : 1.0f / K;
+        }
+    }
+    if (lane == 0 && !warm)
+        a.gap[t] = K < E ? kth - next : INFINITY;
+}
+
+// Per-token selection (warp t handles token t); activation pre-scaling for the
+// 2-bit MMA (all consumer threads); then the grouping, computed in shared
+// memory and written out once. warm: a dry run on stale data that stores
+// nothing to global memory; it runs while the job waits for the router rows,
+// so the real run finds its instructions in the instruction cache.
+__device__ void job_select(const DecodeArgs &a, DecodeSmem &sm, int warp, int lane, bool warm) {
+    const int T = a.T, E = a.E, K = a.K, H = a.H;
+    if (warp < T) {
+        const int t = warp;
+        if (a.forced_idx) {
+            if (lane < K && !warm) {
+                int e = a.forced_idx[t * K + lane];
+                if (e < 0 || e >= E) {
+                    atomicOr(a.status, kErrIndex);
+                    e = e < 0 ? 0 : E - 1;
+                }
+                sm.sel_idx[t][lane] = e;
+                a.idx[t * K + lane] = e;
+                a.w[t * K + lane] = a.forced_w[t * K + lane];
+            }
+        } else if (E <= 32) {
+            select_token<1>(a, sm, t, lane, warm);
+        } else if (E <= 64) {
+            select_token<2>(a, sm, t, lane, warm);
+        } else if (E <= 128) {
+            select_token<4>(a, sm, t, lane, warm);
+        } else if (E <= 256) {
+            select_token<8>(a, sm, t, lane, warm);
+        } else if (E <= 384) {
+            select_token<12>(a, sm, t, lane, warm);
+        } else if (E <= 512) {
+            select_token<16>(a, sm, t, lane, warm);
+        } else {
+            select_token<32>(a, sm, t, lane, warm);
+        }
+    }
+    // activation pre-scaling: thread i takes sub-blocks i, i + 256, ... of all tokens
+    const int nsub = H / 16;
+    for (int q = threadIdx.x; q < T * nsub; q += 32 * kConsumerWarps) {
+        const int t = q / nsub, j = q % nsub;
+        const uint4 *src = reinterpret_cast<const uint4 *>(a.x + (int64_t)t * H + 16 * j);
+        const uint4 p0 = __ldg(src), p1 = __ldg(src + 1);
+        const uint32_t wv[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+        uint32_t outw[8];
+        float so = 0.f, ss = 0.f;
+#pragma unroll
+        for (int h2 = 0; h2 < 8; h2++) {
+            const float e2 = (float)(1 << frag_exp(16 * j + 2 * h2)); // same exponent for both columns
+            const float v0 = __uint_as_float(wv[h2] << 16), v1 = __uint_as_float(wv[h2] & 0xFFFF0000u);
+            const float s0 = v0 * e2, s1 = v1 * e2; // exact: power-of-two scaling of bf16
+            so += s0 + s1;
+            ss += v0 + v1;
+            outw[h2] = (f32_to_bf16_bits(s0) & 0xFFFFu) | (f32_to_bf16_bits(s1) << 16);
+        }
+        if (!warm) {
+            uint4 *dst = reinterpret_cast<uint4 *>(a.xq + (int64_t)t * H + 16 * j);
+            dst[0] = make_uint4(outw[0], outw[1], outw[2], outw[3]);
+            dst[1] = make_uint4(outw[4], outw[5], outw[6], outw[7]);
+            a.xoff[t * nsub + j] = so;
+            a.xsum[t * nsub + j] = ss;
+        }
+    }
+    if (!warm)
+        for (int e = threadIdx.x; e < E; e += 32 * kConsumerWarps)
+            a.counts[e] = 0;
+    if (threadIdx.x < 32)
+        sm.bitmap[threadIdx.x] = 0;
+    consumer_sync();
+    // grouping (warp 0): distinct experts in ascending order, the pairs of each
+    // in pair order. P <= 64 pairs: lane l owns pairs l and l + 32.
+    const int P = T * K;
+    if (warp == 0) {
+        int pe[2];
+#pragma unroll
+        for (int h = 0; h < 2; h++) {
+            const int p = lane + 32 * h;
+            pe[h] = p < P ? sm.sel_idx[p / K][p % K] : -1;
+            if (pe[h] >= 0)
+                atomicOr(&sm.bitmap[pe[h] >> 5], 1u << (pe[h] & 31));
+        }
+        __syncwarp();
+        const unsigned bits = sm.bitmap[lane];
+        int incl = __popc(bits);
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+            if (lane >= o)
+                incl += v;
+        }
+        const int nu = __shfl_sync(0xFFFFFFFFu, incl, 31);
+        sm.word_prefix[lane] = incl - __popc(bits);
+        __syncwarp();
+        int slot[2], rank[2];
+#pragma unroll
+        for (int h = 0; h < 2; h++) {
+            const int p = lane + 32 * h, e = pe[h];
+            slot[h] = rank[h] = 0;
+            if (e >= 0) {
+                slot[h] = sm.word_prefix[e >> 5] + __popc(sm.bitmap[e >> 5] & ((1u << (e & 31)) - 1u));
+                for (int q = 0; q < p; q++)
+                    rank[h] += sm.sel_idx[q / K][q % K] == e;
+            }
+        }
+        // pairs per slot: the rank-0 pair of each expert counts its pairs
+        if (lane < kMaxSlots / 2)
+            sm.slot_cnt[lane] = sm.slot_cnt[lane + 32] = 0;
+        __syncwarp();
+#pragma unroll
+        for (int h = 0; h < 2; h++)
+            if (pe[h] >= 0)
+                atomicAdd(&sm.slot_cnt[slot[h]], 1);
+        __syncwarp();
+        // exclusive scan of the (<= 64) slot counts: lane l sums slots 2l, 2l+1
+        const int c0 = sm.slot_cnt[2 * lane], c1 = sm.slot_cnt[2 * lane + 1];
+        int pair_incl = c0 + c1;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xFFFFFFFFu, pair_incl, o);
+            if (lane >= o)
+                pair_incl += v;
+        }
+        const int base = pair_incl - c0 - c1;
+        __syncwarp();
+        sm.slot_cnt[2 * lane] = base;
+        sm.slot_cnt[2 * lane + 1] = base + c0;
+        __syncwarp();
+        if (warm)
+            return;
+        if (2 * lane < nu)
+            a.uoff[2 * lane] = base;
+        if (2 * lane + 1 < nu)
+            a.uoff[2 * lane + 1] = base + c0;
+        if (lane == 0) {
+            a.uoff[nu] = P;
+            *a.nuniq = nu;
+        }
+#pragma unroll
+        for (int h = 0; h < 2; h++) {
+            const int p = lane + 32 * h, e = pe[h];
+            if (e >= 0) {
+                const int pos = sm.slot_cnt[slot[h]] + rank[h];
+                a.inv[p] = pos;
+                a.perm[pos] = p;
+                if (rank[h] == 0)
+                    a.uexp[slot[h]] = e;
+                atomicAdd(a.counts + e, 1);
+            }
+        }
+    }
+}
+
+// ---- job space ---------------------------------------------------------------------
+
+struct JobSpace {
+    int nR, nSGU, tilesI, tilesH, Umax;
+    int oSGU, oSEL, oGU, oSD, oD, total;
+};
+
+__device__ __forceinline__ JobSpace job_space(const DecodeArgs &a) {
+    JobSpace s;
+    s.nR = a.forced_idx ? 0 : a.E; // one router row per job
+    s.nSGU = a.Ish > 0 ? a.Ish / 16 : 0;
+    s.tilesI = a.I / 16;
+    s.tilesH = a.H / 16;
+    s.Umax = min(a.E, a.T * a.K);
+    // the selection comes right after the router rows: it is on the critical path
+    s.oSEL = s.nR;
+    s.oSGU = s.oSEL + 1;
+    s.oGU = s.oSGU + s.nSGU;
+    s.oSD = s.oGU + s.Umax * s.tilesI;
+    s.oD = s.oSD + (a.Ish > 0 ? s.tilesH : 0);
+    s.total = s.oD + s.Umax * s.tilesH;
+    return s;
+}
+
+__device__ __forceinline__ int pad_tp(int n) { return n <= 1 ? 1 : (n <= 2 ? 2 : (n <= 4 ? 4 : 8)); }
+
+// Widest stage W (a multiple of 256 dividing K) whose bytes, at per_col_x16
+// sixteenths of a byte per column, fit one ring slot.
+__device__ __forceinline__ int pick_w(int K, int per_col_x16) {
+    const int nb = K / 256;
+    for (int m = nb; m >= 1; m--)
+        if (nb % m == 0 && (int64_t)256 * m * per_col_x16 <= (int64_t)16 * kSlotBytes)
+            return 256 * m;
+    return 256;
+}
+
+// ---- producer (lane 0 of the last warp) --------------------------------------------
+
+// Lays out one stage: put() places a piece that the bulk copies bring in;
+// reserve() only sets space aside for a piece the consumers fill themselves
+// after their dependency wait (data other CTAs are still producing).
+struct StageWriter {
+    DecodeSmem &sm;
+    int slot;
+    // Most pieces of one stage: a D stage with 8 tokens has 3 weight pieces and
+    // 4 activation pieces per token (hi, lo, offsets, sums) = 35.
+    static constexpr int kMaxPieces = 40;
+    unsigned off = 0; // layout offset
+    unsigned tx = 0;  // bytes brought in by bulk copies
+    const void **src;
+    unsigned *bytes;
+    unsigned *dst;
+    int np = 0;
+    bool overflow = false;
+    __device__ StageWriter(DecodeSmem &s, int sl) : sm(s), slot(sl), src(s.pc_src), bytes(s.pc_bytes), dst(s.pc_dst) {}
+    __device__ int put(const void *p, unsigned n) {
+        const int o = (int)off;
+        if (np == kMaxPieces) { // cannot happen with the stage shapes above; never write past the arrays
+            overflow = true;
+            off += n;
+            return o;
+        }
+        src[np] = p;
+        bytes[np] = n;
+        dst[np] = off;
+        np++;
+        off += n;
+        tx += n;
+        return o;
+    }
+    int nindep = -1; // pieces before this index need no dependency wait
+    // Pieces put after this call are data other CTAs of this launch are still
+    // producing: issue() copies them only after the dependency is met.
+    __device__ void dependent_from_here() { nindep = np; }
+    // Expect every byte, copy the weights, then (if the stage has dependent
+    // pieces) wait for *dep >= target and copy the rest. Returns false if the
+    // wait gave up; the stage is then never completed and the consumers drain.
+    __device__ bool issue(const DecodeArgs &a, const unsigned *dep, unsigned target) {
+        uint64_t *bar = &sm.full[slot];
+        if (overflow)
+            atomicOr(a.status, kErrInternal);
+        if (tx == 0) {
+            mbar_arrive(bar);
+            return true;
+        }
+        mbar_arrive_tx(bar, tx);
+        const int split = nindep < 0 ? np : nindep;
+        for (int i = 0; i < split; i++)
+            bulk_g2s(sm.ring[slot] + dst[i], src[i], bytes[i], bar);
+        if (split < np) {
+            if (!wait_counter(a, dep, target, false))
+                return false;
+            // the data was written through the generic proxy by other CTAs; the
+            // bulk copies read it through the async proxy
+            asm volatile("fence.proxy.async.global;" ::: "memory");
+            for (int i = split; i < np; i++)
+                bulk_g2s(sm.ring[slot] + dst[i], src[i], bytes[i], bar);
+        }
+        return true;
+    }
+};
+
+__device__ void producer(const DecodeArgs &a, DecodeSmem &sm, const JobSpace &js) {
+    unsigned n = 0; // stages issued so far
+    bool routed = false;
+    int nu = 0;
+    // claim the next ring slot (waits until the consumers released it)
+    auto claim = [&](int &slot) -> bool {
+        slot = (int)(n % kRing);
+        return mbar_wait(a, &sm.empty[slot], ((n / kRing) & 1u) ^ 1u);
+    };
+    bool ok = true;
+    while (ok) {
+        const int j = ld_relaxed(a.ctl + kCtlAbort) ? js.total : (int)atomicAdd(a.ctl + kCtlJobNext, 1u);
+        if (j >= js.total)
+            break;
+        if (j >= js.oGU && !routed) {
+            if (!wait_counter(a, a.ctl + kCtlRoutingEpoch, a.epoch, true))
+                break;
+            asm volatile("fence.proxy.async.global;" ::: "memory");
+            routed = true;
+            nu = __ldcg(a.nuniq);
+        }
+        int type, a0 = 0, tile = 0, ntok = a.T, K = a.H, per16 = 0;
+        int pos[kDecodeT], tok[kDecodeT];
+        for (int i = 0; i < kDecodeT; i++)
+            pos[i] = tok[i] = i < a.T ? i : 0;
+        if (j < js.oSEL) {
+            type = kJobR;
+            a0 = j;
+            per16 = 16 * (4 + 2 * a.T);
+        } else if (j < js.oSGU) {
+            type = kJobSel;
+        } else if (j < js.oGU) {
+            type = kJobSgu;
+            a0 = j - js.oSGU;
+            per16 = 2 * 16 * 17 + 16 * 2 * a.T; // two 8-bit tiles (17/16 B per column each) + bf16 x rows
+        } else if (j < js.oSD) {
+            type = kJobGu;
+            a0 = (j - js.oGU) / js.tilesI;
+            tile = (j - js.oGU) % js.tilesI;
+        } else if (j < js.oD) {
+            type = kJobSd;
+            a0 = j - js.oSD;
+            K = a.Ish;
+            per16 = 16 * 17 + 16 * 4 * a.T; // one 8-bit tile + binary16 hi and lo rows
+        } else {
+            type = kJobD;
+            a0 = (j - js.oD) / js.tilesH;
+            tile = (j - js.oD) % js.tilesH;
+            K = a.I;
+        }
+        if ((type == kJobGu || type == kJobD)) {
+            if (a0 >= nu)
+                continue; // fewer distinct experts than the bound
+            const int p0 = __ldcg(a.uoff + a0), p1 = __ldcg(a.uoff + a0 + 1);
+            ntok = p1 - p0;
+            for (int i = 0; i < kDecodeT; i++) {
+                const int ii = i < ntok ? i : 0;
+                pos[i] = p0 + ii;
+                tok[i] = __ldcg(a.perm + p0 + ii) / a.K;
+            }
+            // 2-bit tile(s): 84/256 B per column per 16 rows = 5.25 B; activations per token:
+            // GU x' (2 B) + off/sum (0.5 B); D hi + lo (4 B) + off/sum (0.5 B)
+            per16 = type == kJobGu ? 2 * 84 + ntok * 40 : 84 + ntok * 72;
+        }
+        const int e = (type == kJobGu || type == kJobD) ? __ldcg(a.uexp + a0) : 0;
+        const int W = type == kJobSel ? 0 : pick_w(K, per16);
+        const int nsub = type == kJobSel ? 1 : K / W;
+        for (int sub = 0; sub < nsub && ok; sub++) {
+            int slot;
+            if (!claim(slot)) {
+                ok = false;
+                break;
+            }
+            StageDesc &d = sm.desc[slot];
+            d.type = type;
+            d.a0 = a0;
+            d.tile = tile;
+            d.sub = sub;
+            d.nsub = nsub;
+            d.c0 = sub * W;
+            d.W = W;
+            d.ntok = ntok;
+            d.tp = pad_tp(ntok);
+            d.nuniq = nu;
+            for (int i = 0; i < kDecodeT; i++) {
+                d.pos[i] = pos[i];
+                d.tok[i] = tok[i];
+            }
+            StageWriter sw(sm, slot);
+            const int c0 = sub * W;
+            if (type == kJobR) {
+                d.oq[0] = sw.put(a.router_w + (int64_t)a0 * a.H + c0, 4u * W);
+                d.act_pitch = 2 * W;
+                d.oact = (int)sw.off;
+                for (int t = 0; t < a.T; t++)
+                    sw.put(a.x + (int64_t)t * a.H + c0, 2u * W);
+            } else if (type == kJobSgu) {
+                const Q8Frag *M[2] = {&a.sh_gate, &a.sh_up};
+                for (int m = 0; m < 2; m++) {
+                    const int64_t u = (int64_t)a0 * M[m]->nbq + c0 / 32;
+                    d.oq[m] = sw.put(M[m]->qs + u * 32, (unsigned)(W / 32) * 512u);
+                    d.od[m] = sw.put(M[m]->d + u * 8, (unsigned)(W / 32) * 32u);
+                }
+                d.act_pitch = 2 * W;
+                d.oact = (int)sw.off;
+                for (int t = 0; t < a.T; t++)
+                    sw.put(a.x + (int64_t)t * a.H + c0, 2u * W);
+            } else if (type == kJobSd) {
+                const int64_t u = (int64_t)a0 * a.sh_down.nbq + c0 / 32;
+                d.oq[0] = sw.put(a.sh_down.qs + u * 32, (unsigned)(W / 32) * 512u);
+                d.od[0] = sw.put(a.sh_down.d + u * 8, (unsigned)(W / 32) * 32u);
+                d.act_pitch = 2 * W;
+                sw.dependent_from_here(); // h of the shared expert: written by the SGU jobs
+                d.oact = (int)sw.off;
+                for (int t = 0; t < a.T; t++)
+                    sw.put(a.hs_hi + (int64_t)t * a.Ish + c0, 2u * W);
+                d.olo = (int)sw.off;
+                for (int t = 0; t < a.T; t++)
+                    sw.put(a.hs_lo + (int64_t)t * a.Ish + c0, 2u * W);
+            } else if (type == kJobGu || type == kJobD) {
+                const Q2Frag *M[2] = {type == kJobGu ? &a.gate : &a.down, &a.up};
+                const int nmat = type == kJobGu ? 2 : 1;
+                const int rows_per_e = type == kJobGu ? a.I : a.H;
+                const int64_t gt = (int64_t)e * (rows_per_e / 16) + tile;
+                for (int m = 0; m < nmat; m++) {
+                    const int64_t u = gt * M[m]->nkc + c0 / 128;
+                    d.oq[m] = sw.put(M[m]->qs + u * 32, (unsigned)(W / 128) * 512u);
+                    d.os[m] = sw.put(M[m]->sc + u * 8, (unsigned)(W / 128) * 128u);
+                    d.od[m] = sw.put(M[m]->dm + (gt * (M[m]->nkc / 2) + c0 / 256) * 8, (unsigned)(W / 256) * 64u);
+                }
+                const uint16_t *hi = a.xq;
+                const float *of = a.xoff, *su = a.xsum;
+                d.act_pitch = 2 * W;
+                d.sub_pitch = W / 4;
+                if (type == kJobGu) {
+                    // x rows were written by the selection job, which completed before the
+                    // routing was published: safe to copy now
+                    d.oact = (int)sw.off;
+                    for (int t = 0; t < ntok; t++)
+                        sw.put(hi + (int64_t)tok[t] * K + c0, 2u * W);
+                    d.ooff = (int)sw.off;
+                    for (int t = 0; t < ntok; t++)
+                        sw.put(of + (int64_t)tok[t] * (K / 16) + c0 / 16, (unsigned)W / 4u);
+                    d.osum = (int)sw.off;
+                    for (int t = 0; t < ntok; t++)
+                        sw.put(su + (int64_t)tok[t] * (K / 16) + c0 / 16, (unsigned)W / 4u);
+                } else {
+                    // h rows of this expert: written by its GU jobs
+                    sw.dependent_from_here();
+                    d.oact = (int)sw.off;
+                    for (int t = 0; t < ntok; t++)
+                        sw.put(a.hq_hi + (int64_t)pos[t] * K + c0, 2u * W);
+                    d.olo = (int)sw.off;
+                    for (int t = 0; t < ntok; t++)
+                        sw.put(a.hq_lo + (int64_t)pos[t] * K + c0, 2u * W);
+                    d.ooff = (int)sw.off;
+                    for (int t = 0; t < ntok; t++)
+                        sw.put(a.hoff + (int64_t)pos[t] * (K / 16) + c0 / 16, (unsigned)W / 4u);
+                    d.osum = (int)sw.off;
+                    for (int t = 0; t < ntok; t++)
+                        sw.put(a.hsum + (int64_t)pos[t] * (K / 16) + c0 / 16, (unsigned)W / 4u);
+                }
+            }
+            const unsigned *dep = type == kJobD ? a.ctl + kCtlGuDone + a0 : a.ctl + kCtlSguDone;
+            const unsigned target = type == kJobD ? (unsigned)js.tilesI : (unsigned)js.nSGU;
+            n++;
+            if (!sw.issue(a, dep, target)) {
+                ok = false;
+                break;
+            }
+        }
+    }
+    // end of this CTA's jobs
+    int slot;
+    if (claim(slot)) {
+        sm.desc[slot].type = kJobEnd;
+        mbar_arrive(&sm.full[slot]);
+    }
+}
+
+// ---- consumers (warps 0..7) ----------------------------------------------------------
+
+// y for 16 rows (tile ti) and all tokens, in fixed order: sum over k, then
+// shared. Warp 0 of the consumers.
+__device__ void combine_tile(const DecodeArgs &a, int ti, int lane) {
+    for (int q = lane; q < 16 * a.T; q += 32) {
+        const int r = q & 15, t = q >> 4;
+        const int col = ti * 16 + r;
+        float v = 0.f;
+        for (int k = 0; k < a.K; k++)
+            v = fmaf(__ldcg(a.w + t * a.K + k), __ldcg(a.ye + (int64_t)__ldcg(a.inv + t * a.K + k) * a.H + col), v);
+        if (a.Ish > 0)
+            v += __ldcg(a.ysh + (int64_t)t * a.H + col);
+        a.y[(int64_t)t * a.H + col] = v;
+    }
+}
+
+// After the consumers' barrier that follows the job's result writes: warp 0
+// counts the contribution to H tile ti; the last contribution combines the
+// tile. The other warps go on with the next job.
+__device__ void arrive_tile(const DecodeArgs &a, int ti, int nuniq, int warp, int lane) {
+    if (warp != 0)
+        return;
+    unsigned last = 0;
+    if (lane == 0) {
+        __threadfence();
+        const unsigned expected = (unsigned)nuniq + (a.Ish > 0 ? 1u : 0u);
+        const unsigned old = atomicAdd(a.ctl + kCtlTileCnt + ti, 1u);
+        last = old + 1 == expected;
+        if (last) {
+            __threadfence();
+            a.ctl[kCtlTileCnt + ti] = 0; // ready for the next launch
+        }
+    }
+    if (__shfl_sync(0xFFFFFFFFu, last, 0))
+        combine_tile(a, ti, lane);
+}
+
+// After the consumers' barrier that follows the job's result writes: thread 0
+// publishes the job (release fence, then the count); nobody waits for it here.
+__device__ __forceinline__ void signal(const DecodeArgs &a, unsigned *ctr) {
+    if (threadIdx.x == 0) {
+        __threadfence();
+        atomicAdd(ctr, 1u);
+    }
+}
+
+template <int TP> struct JobOps {
+    static __device__ void stage(const DecodeArgs &a, const uint8_t *sl, const StageDesc &d, int warp, int lane,
+                                 float (&out)[2][2][2]) {
+        switch (d.type) {
+        case kJobSgu: q8_stage<TP, 2, false, true>(sl, d, warp, lane, out); break;
+        case kJobGu: q2_stage<TP, 2, false>(sl, d, warp, lane, out); break;
+        case kJobSd: q8_stage<TP, 1, true, false>(sl, d, warp, lane, out); break;
+        case kJobD: q2_stage<TP, 1, true>(sl, d, warp, lane, out); break;
+        default: break;
+        }
+    }
+    // End of a job: combine the warps' partial sums (barrier 1), write the
+    // results, barrier 2, then publish (thread 0 / warp 0, without a barrier).
+    static __device__ void finish(const DecodeArgs &a, DecodeSmem &sm, const StageDesc &d, int buf, int warp,
+                                  int lane, float (&out)[2][2][2]) {
+        const int tid = threadIdx.x;
+        auto P = sm.part[buf];
+        if (d.type == kJobSgu || d.type == kJobGu) {
+            reduce_out<TP, 2>(out);
+            store_part<TP, 2>(sm, buf, warp, lane, out);
+        } else {
+            reduce_out<TP, 1>(out);
+            store_part<TP, 1>(sm, buf, warp, lane, out);
+        }
+        consumer_sync();
+        if (d.type == kJobSgu) {
+            if (tid < 16 * a.T) {
+                const int r = tid & 15, t = tid >> 4;
+                float gs = 0.f, us = 0.f;
+                for (int w = 0; w < kConsumerWarps; w++) {
+                    gs += P[w][0][r][t];
+                    us += P[w][1][r][t];
+                }
+                const float hv = silu(gs) * us;
+                const __half hi = __float2half_rn(hv);
+                const __half lo = __float2half_rn(hv - __half2float(hi));
+                const int64_t o = (int64_t)t * a.Ish + d.a0 * 16 + r;
+                a.hs_hi[o] = __half_as_ushort(hi);
+                a.hs_lo[o] = __half_as_ushort(lo);
+            }
+            consumer_sync();
+            signal(a, a.ctl + kCtlSguDone);
+        } else if (d.type == kJobGu) {
+            // row r of the tile is column k = 16 tile + r of the down matrix
+            const int t = tid >> 4, r = tid & 15;
+            float hv_sum = 0.f, hv_off = 0.f;
+            if (t < d.ntok) {
+                float gs = 0.f, us = 0.f;
+                for (int w = 0; w < kConsumerWarps; w++) {
+                    gs += P[w][0][r][t];
+                    us += P[w][1][r][t];
+                }
+                const float hv = silu(gs) * us;
+                const int k = d.tile * 16 + r;
+                const float sc = (float)(1 << frag_exp(k));
+                const float hp = hv * sc;
+                const uint32_t hi = f32_to_bf16_bits(hp);
+                const float hif = __uint_as_float(hi << 16);
+                const uint32_t lo = f32_to_bf16_bits(hp - hif);
+                const float lof = __uint_as_float(lo << 16);
+                const int64_t o = (int64_t)d.pos[t] * a.I + k;
+                a.hq_hi[o] = (uint16_t)hi;
+                a.hq_lo[o] = (uint16_t)lo;
+                hv_off = hif + lof;
+                hv_sum = hv_off / sc;
+            }
+#pragma unroll
+            for (int o = 8; o > 0; o >>= 1) { // over the 16 rows: one sub-block of the down columns
+                hv_off += __shfl_xor_sync(0xFFFFFFFFu, hv_off, o);
+                hv_sum += __shfl_xor_sync(0xFFFFFFFFu, hv_sum, o);
+            }
+            if (t < d.ntok && r == 0) {
+                a.hoff[d.pos[t] * (a.I / 16) + d.tile] = hv_off;
+                a.hsum[d.pos[t] * (a.I / 16) + d.tile] = hv_sum;
+            }
+            consumer_sync();
+            signal(a, a.ctl + kCtlGuDone + d.a0);
+        } else if (d.type == kJobSd) {
+            if (tid < 16 * a.T) {
+                const int r = tid & 15, t = tid >> 4;
+                float v = 0.f;
+                for (int w = 0; w < kConsumerWarps; w++)
+                    v += P[w][0][r][t];
+                a.ysh[(int64_t)t * a.H + d.a0 * 16 + r] = v;
+            }
+            consumer_sync();
+            arrive_tile(a, d.a0, d.nuniq, warp, lane);
+        } else { // kJobD
+            const int t = tid >> 4, r = tid & 15;
+            if (t < d.ntok) {
+                float v = 0.f;
+                for (int w = 0; w < kConsumerWarps; w++)
+                    v += P[w][0][r][t];
+                a.ye[(int64_t)d.pos[t] * a.H + d.tile * 16 + r] = v;
+            }
+            consumer_sync();
+            arrive_tile(a, d.tile, d.nuniq, warp, lane);
+        }
+    }
+};
+
+__device__ __forceinline__ void stage_tp(int tp, const DecodeArgs &a, const uint8_t *sl, const StageDesc &d,
+                                         int warp, int lane, float (&out)[2][2][2]) {
+    switch (tp) {
+    case 1: JobOps<1>::stage(a, sl, d, warp, lane, out); break;
+    case 2: JobOps<2>::stage(a, sl, d, warp, lane, out); break;
+    case 4: JobOps<4>::stage(a, sl, d, warp, lane, out); break;
+    default: JobOps<8>::stage(a, sl, d, warp, lane, out); break;
+    }
+}
+
+__device__ __forceinline__ void finish_tp(int tp, const DecodeArgs &a, DecodeSmem &sm, const StageDesc &d, int buf,
+                                          int warp, int lane, float (&out)[2][2][2]) {
+    switch (tp) {
+    case 1: JobOps<1>::finish(a, sm, d, buf, warp, lane, out); break;
+    case 2: JobOps<2>::finish(a, sm, d, buf, warp, lane, out); break;
+    case 4: JobOps<4>::finish(a, sm, d, buf, warp, lane, out); break;
+    default: JobOps<8>::finish(a, sm, d, buf, warp, lane, out); break;
+    }
+}
+
+__device__ void consumer(const DecodeArgs &a, DecodeSmem &sm, const JobSpace &js, int warp, int lane) {
+    unsigned n = 0, jobs_done = 0;
+    float out[2][2][2];
+    bool alive = true; // false after a failed dependency wait: drain the ring without computing
+    while (true) {
+        const int slot = (int)(n % kRing);
+        if (!mbar_wait(a, &sm.full[slot], (n / kRing) & 1u))
+            break;
+        const StageDesc &d = sm.desc[slot];
+        const int type = d.type;
+        if (type == kJobEnd)
+            break;
+        if (d.sub == 0) {
+#pragma unroll
+            for (int i = 0; i < 8; i++)
+                (&out[0][0][0])[i] = 0.f;
+            const unsigned *dep = nullptr;
+            unsigned target = 0;
+            if (type == kJobSel) {
+                dep = a.ctl + kCtlRouterDone;
+                target = (unsigned)js.nR;
+            }
+            if (type == kJobSel && alive) {
+                if (threadIdx.x < kDecodeT * kMaxTopK)
+                    (&sm.sel_idx[0][0])[threadIdx.x] = 0;
+                consumer_sync();
+                job_select(a, sm, warp, lane, true);
+                consumer_sync();
+            }
+            if (dep && alive) {
+                if (threadIdx.x == 0)
+                    sm.flag = wait_counter(a, dep, target, false);
+                consumer_sync();
+                alive = sm.flag != 0;
+                consumer_sync();
+            }
+        }
+        if (alive) {
+            if (type == kJobR)
+                router_stage(sm.ring[slot], d, a.T, warp, lane, out);
+            else if (type != kJobSel)
+                stage_tp(d.tp, a, sm.ring[slot], d, warp, lane, out);
+        }
+        const bool last = d.sub == d.nsub - 1;
+        if (last && alive) {
+            if (type == kJobR) {
+                const int buf = (int)(jobs_done & 1u);
+                float *acc = &out[0][0][0];
+#pragma unroll
+                for (int t = 0; t < kDecodeT; t++) {
+                    if (t < a.T) {
+                        const float v = warp_sum(acc[t]);
+                        if (lane == 0)
+                            sm.part[buf][warp][0][0][t] = v;
+                    }
+                }
+                consumer_sync();
+                if (threadIdx.x < a.T) {
+                    float v = 0.f;
+                    for (int w = 0; w < kConsumerWarps; w++)
+                        v += sm.part[buf][w][0][0][threadIdx.x];
+                    a.logits[threadIdx.x * a.E + d.a0] = v;
+                }
+                consumer_sync();
+                signal(a, a.ctl + kCtlRouterDone);
+            } else if (type == kJobSel) {
+                job_select(a, sm, warp, lane, false);
+                consumer_sync();
+                if (threadIdx.x == 0) {
+                    __threadfence();
+                    st_release(a.ctl + kCtlRoutingEpoch, a.epoch);
+                }
+            } else {
+                const int buf = (int)(jobs_done & 1u);
+                finish_tp(d.tp, a, sm, d, buf, warp, lane, out);
+            }
+            jobs_done++;
+        }
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(&sm.empty[slot]);
+        n++;
+    }
+}
+
+__global__ void __launch_bounds__(kDecodeThreads, 2) decode_fused_kernel(DecodeArgs a) {
+    extern __shared__ __align__(128) uint8_t dsmem[];
+    DecodeSmem &sm = *reinterpret_cast<DecodeSmem *>(dsmem);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kRing; i++) {
+            mbar_init(&sm.full[i], 1);
+            mbar_init(&sm.empty[i], kConsumerWarps);
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    const JobSpace js = job_space(a);
+    if (warp == kConsumerWarps) {
+        if (lane == 0)
+            producer(a, sm, js);
+    } else {
+        consumer(a, sm, js, warp, lane);
+    }
+    // the last CTA out resets the counters for the next launch
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        const unsigned done = atomicAdd(a.ctl + kCtlFinished, 1u);
+        if (done + 1 == gridDim.x) {
+            __threadfence();
+            if (!ld_acquire(a.ctl + kCtlAbort)) {
+                a.ctl[kCtlJobNext] = 0;
+                a.ctl[kCtlRouterDone] = 0;
+                a.ctl[kCtlSguDone] = 0;
+                for (int s = 0; s < kMaxSlots; s++)
+                    a.ctl[kCtlGuDone + s] = 0;
+                __threadfence();
+                a.ctl[kCtlFinished] = 0;
+            }
+        }
+    }
+}
+
+} // namespace ds4

@@ -12,7 +12,9 @@
 
 #include "../../include/ds4moe.h"
 #include "common.cuh"
+#include "decode_fused.cuh"
 #include "decode_simple.cuh"
+#include "frag_layout.cuh"
 #include "dispatch.cuh"
 #include "router.cuh"
 
@@ -77,10 +79,29 @@ struct Profiler {
     }
 };
 
+// Buffers and state of the fused decode kernel (sized for 8 tokens).
+struct DecodeState {
+    Q2Frag gate, up, down;
+    Q8Frag sh_gate, sh_up, sh_down;
+    float *logits = nullptr, *gap = nullptr;
+    int32_t *counts = nullptr, *nuniq = nullptr, *uexp = nullptr, *uoff = nullptr, *perm = nullptr, *inv = nullptr;
+    uint16_t *xq = nullptr;
+    float *xoff = nullptr, *xsum = nullptr;
+    uint16_t *hq_hi = nullptr, *hq_lo = nullptr;
+    float *hoff = nullptr, *hsum = nullptr;
+    uint16_t *hs_hi = nullptr, *hs_lo = nullptr;
+    float *ye = nullptr, *ysh = nullptr;
+    unsigned *ctl = nullptr;
+    int ctl_words = 0;
+    int grid = 0;
+    unsigned epoch = 0;
+};
+
 struct ds4moe {
     Profiler prof;
     LayerDev L;
     Scratch S;
+    DecodeState D;
     int device = 0;
     cudaStream_t stream = nullptr;
     unsigned *status = nullptr; // device word of kErr* bits
@@ -198,6 +219,28 @@ void layout_weights(ds4moe *h, Carver &c) {
         q8(L.sh_up, L.Ish, L.H);
         q8(L.sh_down, L.H, L.Ish);
     }
+    DecodeState &D = h->D;
+    auto f2 = [&](Q2Frag &m, int64_t rows, int k) {
+        m.rows = rows;
+        m.nkc = k / 128;
+        m.qs = c.take<uint4>((uint64_t)(rows / 16) * m.nkc * 32);
+        m.sc = c.take<uint4>((uint64_t)(rows / 16) * m.nkc * 8);
+        m.dm = c.take<uint2>((uint64_t)(rows / 16) * (m.nkc / 2) * 8);
+    };
+    auto f8 = [&](Q8Frag &m, int64_t rows, int k) {
+        m.rows = rows;
+        m.nbq = k / 32;
+        m.qs = c.take<uint4>((uint64_t)(rows / 16) * m.nbq * 32);
+        m.d = c.take<uint32_t>((uint64_t)(rows / 16) * m.nbq * 8);
+    };
+    f2(D.gate, (int64_t)L.E * L.I, L.H);
+    f2(D.up, (int64_t)L.E * L.I, L.H);
+    f2(D.down, (int64_t)L.E * L.H, L.I);
+    if (L.Ish > 0) {
+        f8(D.sh_gate, L.Ish, L.H);
+        f8(D.sh_up, L.Ish, L.H);
+        f8(D.sh_down, L.H, L.Ish);
+    }
 }
 
 void layout_scratch(ds4moe *h, Carver &c) {
@@ -224,6 +267,29 @@ void layout_scratch(ds4moe *h, Carver &c) {
     S.ysh = c.take<float>(T * L.H);
     S.xstage = c.take<uint16_t>(T * L.H);
     S.ystage = c.take<float>(T * L.H);
+    DecodeState &D = h->D;
+    const int64_t Td = kDecodeT, Pd = (int64_t)kDecodeT * L.K;
+    D.logits = c.take<float>(Td * L.E);
+    D.gap = c.take<float>(Td);
+    D.counts = c.take<int32_t>(L.E);
+    D.nuniq = c.take<int32_t>(1);
+    D.uexp = c.take<int32_t>(kMaxSlots);
+    D.uoff = c.take<int32_t>(kMaxSlots + 1);
+    D.perm = c.take<int32_t>(Pd);
+    D.inv = c.take<int32_t>(Pd);
+    D.xq = c.take<uint16_t>(Td * L.H);
+    D.xoff = c.take<float>(Td * (L.H / 16));
+    D.xsum = c.take<float>(Td * (L.H / 16));
+    D.hq_hi = c.take<uint16_t>(Pd * L.I);
+    D.hq_lo = c.take<uint16_t>(Pd * L.I);
+    D.hoff = c.take<float>(Pd * (L.I / 16));
+    D.hsum = c.take<float>(Pd * (L.I / 16));
+    D.hs_hi = c.take<uint16_t>(Td * (L.Ish > 0 ? L.Ish : 2));
+    D.hs_lo = c.take<uint16_t>(Td * (L.Ish > 0 ? L.Ish : 2));
+    D.ye = c.take<float>(Pd * L.H);
+    D.ysh = c.take<float>(Td * L.H);
+    D.ctl_words = kCtlTileCnt + L.H / 16;
+    D.ctl = c.take<unsigned>(D.ctl_words);
 }
 
 int cuda_rc(cudaError_t e) {
@@ -334,6 +400,72 @@ int run_experts_simple(ds4moe *h, int T, float *y) {
     return launch_rc();
 }
 
+// The fused decode kernel over tokens [0, T) in launches of up to 8 tokens.
+// forced_idx/forced_w: caller routing (nullptr = route here). idx_out/w_out
+// receive the routing of every token ([T][K]).
+int run_decode(ds4moe *h, const void *x, int T, float *y, const int32_t *forced_idx, const float *forced_w) {
+    const LayerDev &L = h->L;
+    DecodeState &D = h->D;
+    Scratch &S = h->S;
+    for (int t0 = 0; t0 < T; t0 += kDecodeT) {
+        const int Tc = T - t0 < kDecodeT ? T - t0 : kDecodeT;
+        DecodeArgs a;
+        a.H = L.H;
+        a.I = L.I;
+        a.E = L.E;
+        a.K = L.K;
+        a.Ish = L.Ish;
+        a.router_w = L.router_w;
+        a.router_bias = L.router_bias;
+        a.gate = D.gate;
+        a.up = D.up;
+        a.down = D.down;
+        a.sh_gate = D.sh_gate;
+        a.sh_up = D.sh_up;
+        a.sh_down = D.sh_down;
+        a.x = static_cast<const uint16_t *>(x) + (int64_t)t0 * L.H;
+        a.T = Tc;
+        a.y = y + (int64_t)t0 * L.H;
+        a.forced_idx = forced_idx ? forced_idx + (int64_t)t0 * L.K : nullptr;
+        a.forced_w = forced_w ? forced_w + (int64_t)t0 * L.K : nullptr;
+        a.epoch = ++D.epoch;
+        if (a.epoch == 0)
+            a.epoch = ++D.epoch;
+        a.logits = D.logits;
+        a.idx = S.idx + (int64_t)t0 * L.K;
+        a.w = S.w + (int64_t)t0 * L.K;
+        a.gap = S.gap + t0;
+        a.counts = D.counts;
+        a.nuniq = D.nuniq;
+        a.uexp = D.uexp;
+        a.uoff = D.uoff;
+        a.perm = D.perm;
+        a.inv = D.inv;
+        a.xq = D.xq;
+        a.xoff = D.xoff;
+        a.xsum = D.xsum;
+        a.hq_hi = D.hq_hi;
+        a.hq_lo = D.hq_lo;
+        a.hoff = D.hoff;
+        a.hsum = D.hsum;
+        a.hs_hi = D.hs_hi;
+        a.hs_lo = D.hs_lo;
+        a.ye = D.ye;
+        a.ysh = D.ysh;
+        a.ctl = D.ctl;
+        a.status = h->status;
+        void *args[] = {&a};
+        launch(h, "decode_fused", [&] {
+            cudaLaunchCooperativeKernel((const void *)decode_fused_kernel, dim3(D.grid), dim3(kDecodeThreads), args,
+                                        sizeof(DecodeSmem), h->stream);
+        });
+        int rc = launch_rc();
+        if (rc)
+            return rc;
+    }
+    return DS4MOE_OK;
+}
+
 int check_call(ds4moe *h, const void *x, int T) {
     if (!h)
         return DS4MOE_EINVAL;
@@ -352,6 +484,8 @@ int forward_impl(ds4moe *h, const void *x, int T, int path, float *y) {
     if (path == DS4MOE_PATH_AUTO)
         path = T <= 8 ? DS4MOE_PATH_DECODE : DS4MOE_PATH_PREFILL;
     h->stats.path = path;
+    if (path == DS4MOE_PATH_DECODE)
+        return run_decode(h, x, T, y, nullptr, nullptr);
     int rc = run_router(h, x, T, nullptr);
     if (rc)
         return rc;
@@ -470,6 +604,36 @@ int ds4moe_create(const ds4moe_layer_desc *desc, const ds4moe_weights *w, ds4moe
         rq8(w->sh_up, L.sh_up);
         rq8(w->sh_down, L.sh_down);
     }
+    DecodeState &D = h->D;
+    auto rf2 = [&](const void *src, Q2Frag &m) {
+        const int64_t n = (m.rows / 16) * m.nkc * 32;
+        repack_q2_frag_kernel<<<blocks_for(n, 256), 256, 0, st>>>(static_cast<const uint8_t *>(src), m.rows, m.nkc / 2,
+                                                                   const_cast<uint4 *>(m.qs), const_cast<uint4 *>(m.sc),
+                                                                   const_cast<uint2 *>(m.dm));
+    };
+    auto rf8 = [&](const void *src, Q8Frag &m) {
+        const int64_t n = (m.rows / 16) * m.nbq * 32;
+        repack_q8_frag_kernel<<<blocks_for(n, 256), 256, 0, st>>>(static_cast<const uint8_t *>(src), m.rows, m.nbq,
+                                                                   const_cast<uint4 *>(m.qs), const_cast<uint32_t *>(m.d));
+    };
+    rf2(w->gate, D.gate);
+    rf2(w->up, D.up);
+    rf2(w->down, D.down);
+    if (has_shared) {
+        rf8(w->sh_gate, D.sh_gate);
+        rf8(w->sh_up, D.sh_up);
+        rf8(w->sh_down, D.sh_down);
+    }
+    cudaMemsetAsync(D.ctl, 0, sizeof(unsigned) * D.ctl_words, st);
+    int per_sm = 0, nsm = 0;
+    cudaFuncSetAttribute(decode_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(DecodeSmem));
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_fused_kernel, kDecodeThreads, sizeof(DecodeSmem));
+    cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+    D.grid = per_sm * nsm;
+    if (D.grid <= 0) {
+        ds4moe_destroy(h);
+        return DS4MOE_ECUDA;
+    }
     rc = launch_rc();
     if (!rc)
         rc = cuda_rc(cudaStreamSynchronize(st));
@@ -563,6 +727,8 @@ int ds4moe_forward_routed(ds4moe_t *h, const void *x, int32_t T, const int32_t *
     h->stats = ds4moe_stats{};
     h->stats.tokens = T;
     h->stats.path = path == DS4MOE_PATH_AUTO ? (T <= 8 ? DS4MOE_PATH_DECODE : DS4MOE_PATH_PREFILL) : path;
+    if (h->stats.path == DS4MOE_PATH_DECODE)
+        return run_decode(h, x, T, y, idx, w);
     rc = run_prep(h, x, T);
     if (rc)
         return rc;
@@ -607,8 +773,10 @@ int ds4moe_status(ds4moe_t *h) {
         return rc;
     if (bits)
         cudaMemset(h->status, 0, sizeof(unsigned));
-    if (bits & kErrTimeout)
+    if (bits & kErrTimeout) {
+        cudaMemset(h->D.ctl, 0, sizeof(unsigned) * h->D.ctl_words); // an aborted launch leaves them dirty
         return DS4MOE_ETIMEOUT;
+    }
     if (bits)
         return DS4MOE_EDEVICE;
     return DS4MOE_OK;
@@ -622,11 +790,13 @@ int ds4moe_get_stats(ds4moe_t *h, ds4moe_stats *out) {
         return rc;
     *out = h->stats;
     if (h->stats.tokens > 0) {
+        const bool dec = h->stats.path == DS4MOE_PATH_DECODE;
         int32_t n = 0;
-        cudaMemcpy(&n, h->S.nuniq, sizeof(int32_t), cudaMemcpyDeviceToHost);
+        cudaMemcpy(&n, dec ? h->D.nuniq : h->S.nuniq, sizeof(int32_t), cudaMemcpyDeviceToHost);
         out->n_unique = n;
         int32_t *counts = static_cast<int32_t *>(malloc(sizeof(int32_t) * h->L.E));
-        if (counts && cudaMemcpy(counts, h->S.counts, sizeof(int32_t) * h->L.E, cudaMemcpyDeviceToHost) ==
+        if (counts && cudaMemcpy(counts, dec ? h->D.counts : h->S.counts, sizeof(int32_t) * h->L.E,
+                                 cudaMemcpyDeviceToHost) ==
                           cudaSuccess) {
             int mx = 0;
             for (int e = 0; e < h->L.E; e++)

@@ -95,8 +95,10 @@ def test_token_independence_and_determinism(tiny):
     y8b = moe.forward(xd, path=ds4.PATH_DECODE).cpu().numpy()
     assert (y8 == y8b).all()
     for t in range(8):
+        # a token's output does not depend on the other tokens of the batch (up to
+        # the summation order of the tensor-core packing, which depends on T)
         y1 = moe.forward(xd[t:t + 1].contiguous(), path=ds4.PATH_DECODE).cpu().numpy()
-        assert (y1[0] == y8[t]).all()
+        assert rel_l2(y1[0], y8[t]) <= 1e-5
 
 
 def test_forward_host_matches_device(tiny):
