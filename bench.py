@@ -72,13 +72,26 @@ def kernel_bytes(name, shape, T, U):
     P = T * K
     table = {
         "router_logits": 4 * E * H + 4 * T * H + 4 * T * E,
-        "simple_gateup_q2": U * 2 * I * H * Q2_BPW + 4 * T * H + 4 * P * I,
-        "simple_down_q2": U * H * I * Q2_BPW + 4 * P * I + 4 * P * H,
-        "simple_gateup_q8": 2 * Ish * H * Q8_BPW + 4 * T * H + 4 * T * Ish,
-        "simple_down_q8": H * Ish * Q8_BPW + 4 * T * Ish + 4 * T * H,
+        "prefill_gateup_q2": U * 2 * I * H * Q2_BPW + 2 * T * H + 2 * P * I,
+        "prefill_down_q2": U * H * I * Q2_BPW + 2 * P * I + 4 * P * H,
+        "prefill_gateup_q8": 2 * Ish * H * Q8_BPW + 2 * T * H + 2 * T * Ish,
+        "prefill_down_q8": H * Ish * Q8_BPW + 2 * T * Ish + 4 * T * H,
         "combine": 4 * P * H + 4 * T * H + 4 * T * H,
         # one launch of the fused decode kernel does the whole layer for up to 8 tokens
         "decode_fused": layer_bytes(shape, T, U),
+    }
+    return table.get(name)
+
+
+def kernel_flops(name, shape, T):
+    """Tensor-core flops of one launch (dense contractions only)."""
+    H, I, K, Ish = shape.hidden, shape.inter, shape.top_k, shape.shared_inter
+    P = T * K
+    table = {
+        "prefill_gateup_q2": 2 * P * 2 * I * H,
+        "prefill_down_q2": 2 * P * H * I,
+        "prefill_gateup_q8": 2 * T * 2 * Ish * H,
+        "prefill_down_q8": 2 * T * H * Ish,
     }
     return table.get(name)
 
@@ -341,13 +354,28 @@ def main():
         with open(pk_path) as f:
             peaks = json.load(f)
     hbm_peak = peaks.get("hbm_gbs", 6800.0)
+    tf_peak = peaks.get("bf16_tflops", 1872.7)
     peak_src = "measured" if "hbm_gbs" in peaks else "fallback"
     roofline = None
+    dom_flops = kernel_flops(dom, shape, T)
     if dom_bytes is not None:
-        ach = dom_bytes / (dom_avg_ms / 1000.0) / 1e9
-        roofline = {"bound": "hbm", "kernel": dom, "achieved": ach, "peak": hbm_peak, "unit": "GB/s",
-                    "frac": ach / hbm_peak, "traffic": None, "peak_source": peak_src,
-                    "bytes_per_launch": dom_bytes, "avg_launch_us": 1000 * dom_avg_ms}
+        sec = dom_avg_ms / 1000.0
+        t_hbm = dom_bytes / (hbm_peak * 1e9)
+        t_tc = dom_flops / (tf_peak * 1e12) if dom_flops else 0.0
+        if t_tc > t_hbm:
+            ach = dom_flops / sec / 1e12
+            roofline = {"bound": "tensor", "kernel": dom, "achieved": ach, "peak": tf_peak, "unit": "TFLOP/s",
+                        "frac": ach / tf_peak, "traffic": None, "peak_source": peak_src + " bf16 burst",
+                        "flops_per_launch": dom_flops, "bytes_per_launch": dom_bytes,
+                        "hbm_frac": dom_bytes / sec / 1e9 / hbm_peak, "avg_launch_us": 1000 * dom_avg_ms}
+        else:
+            ach = dom_bytes / sec / 1e9
+            roofline = {"bound": "hbm", "kernel": dom, "achieved": ach, "peak": hbm_peak, "unit": "GB/s",
+                        "frac": ach / hbm_peak, "traffic": None, "peak_source": peak_src,
+                        "bytes_per_launch": dom_bytes, "avg_launch_us": 1000 * dom_avg_ms}
+            if dom_flops:
+                roofline["flops_per_launch"] = dom_flops
+                roofline["tensor_frac"] = dom_flops / sec / 1e12 / tf_peak
     lay_bytes = layer_bytes(shape, T, U_mean) * len(handles)
     layer_gbs = lay_bytes / (ms_per_step / 1000.0) / 1e9
 
@@ -387,7 +415,7 @@ def main():
     if rank == 0:
         out = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
                "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-               "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+               "vs_baseline": None, "dtype": "f32" if T <= 8 else "bf16", "data": "synthetic",
                "config": workload_config(wl, args.workload, l2_note),
                "roofline": roofline,
                "layer_roofline": {"bound": "hbm" if args.workload != "prefill_t4096_zipf4" else "tensor",

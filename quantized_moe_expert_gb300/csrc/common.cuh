@@ -22,13 +22,16 @@ constexpr unsigned kErrIndex = 1u << 0;    // a routed index was out of range an
 constexpr unsigned kErrTimeout = 1u << 1;  // a bounded wait gave up
 constexpr unsigned kErrInternal = 1u << 2; // an internal consistency check failed
 
-// 2-bit matrix in the kernels' layout: three separately aligned streams, each
-// row-major over (row, block). Row r, block b:
-//   codes  qs + (r * nb + b) * 64     64 bytes, code i at byte i/4, bits 2*(i%4)
+// 2-bit matrix in the prefill kernels' layout: three separately aligned
+// streams, each row-major over (row, 256-weight block). Row r, block b:
+//   codes  qs + (r * nb + b) * 64     16 words, one per 16-weight sub-block
 //   scales sc + (r * nb + b) * 16     16 bytes, low nibble scale, high nibble min
 //   dm[r * nb + b]                    binary16 d in the low half, dmin in the high half
-// A row's codes are contiguous (nb * 64 bytes), so a warp reads them with
-// fully coalesced 16-byte loads and a row range is one contiguous bulk copy.
+// Sub-block sb = 4 s + 2 h + j (s: 64-column step of the block, h: its half,
+// j: 0/1) is stored as word / scale byte 8 h + 2 s + j, so one half of every
+// step is a contiguous 32-byte (codes) and 8-byte (scales) run. Inside the
+// word, weight pair p (weights 2p, 2p+1 of the sub-block) sits at bits 2p and
+// 16 + 2p, so a mask picks both codes of a pair into the two halves.
 struct Q2Mat {
     const uint8_t *qs;
     const uint8_t *sc;
@@ -80,9 +83,12 @@ struct Scratch {
     int32_t *nuniq;    // [1] number of distinct experts
     int32_t *perm;     // [Tmax*K] pair index at each expert-grouped position
     int32_t *inv;      // [Tmax*K] expert-grouped position of each pair
-    float *h;          // [Tmax*K][I] routed SwiGLU activations, expert-grouped order
+    uint16_t *h;       // [Tmax*K][I] bf16 routed SwiGLU activations, expert-grouped order
     float *ye;         // [Tmax*K][H] routed expert outputs, expert-grouped order
-    float *hsh;        // [Tmax][I_sh]
+    uint16_t *hsh;     // [Tmax][I_sh] bf16 shared-expert SwiGLU activations
+    int4 *grp_gu;      // routed tile groups of at most 128 rows (gate/up)
+    int4 *grp_dn;      // routed tile groups of at most 256 rows (down)
+    int32_t *ngrp;     // [2] number of groups in grp_gu, grp_dn
     float *ysh;        // [Tmax][H]
     uint16_t *xstage;  // [Tmax][H] bf16 staging for host-memory calls
     float *ystage;     // [Tmax][H]

@@ -13,9 +13,9 @@
 #include "../../include/ds4moe.h"
 #include "common.cuh"
 #include "decode_fused.cuh"
-#include "decode_simple.cuh"
 #include "frag_layout.cuh"
 #include "dispatch.cuh"
+#include "prefill_gemm.cuh"
 #include "router.cuh"
 
 using namespace ds4;
@@ -158,11 +158,29 @@ __global__ void repack_q2_kernel(const uint32_t *__restrict__ src, int64_t nbloc
 #pragma unroll
     for (int i = 0; i < 21; i++)
         w[i] = s[i];
-    reinterpret_cast<uint4 *>(sc)[b] = make_uint4(w[0], w[1], w[2], w[3]);
+    // canonical: scales[16] (words 0-3), codes[64] (words 4-19, code i at byte i/4,
+    // bits 2 (i % 4)), d and dmin (word 20)
+    uint32_t osc[4] = {0u, 0u, 0u, 0u}, oqs[16];
+#pragma unroll
+    for (int sb = 0; sb < 16; sb++) {
+        const int st = sb >> 2, hf = (sb >> 1) & 1, j = sb & 1;
+        const int slot = 8 * hf + 2 * st + j;
+        const uint32_t byte = (w[sb >> 2] >> (8 * (sb & 3))) & 0xFFu;
+        osc[slot >> 2] |= byte << (8 * (slot & 3));
+        uint32_t word = 0u;
+#pragma unroll
+        for (int k = 0; k < 16; k++) {
+            const int i = 16 * sb + k;
+            const uint32_t q = (w[4 + (i >> 4)] >> (2 * (i & 15))) & 3u;
+            word |= q << ((k & 1) ? 16 + (k - 1) : k);
+        }
+        oqs[slot] = word;
+    }
+    reinterpret_cast<uint4 *>(sc)[b] = make_uint4(osc[0], osc[1], osc[2], osc[3]);
     uint4 *q = reinterpret_cast<uint4 *>(qs + b * 64);
 #pragma unroll
     for (int i = 0; i < 4; i++)
-        q[i] = make_uint4(w[4 + 4 * i], w[5 + 4 * i], w[6 + 4 * i], w[7 + 4 * i]);
+        q[i] = make_uint4(oqs[4 * i], oqs[4 * i + 1], oqs[4 * i + 2], oqs[4 * i + 3]);
     dm[b] = w[20]; // d in the low half, dmin in the high half
 }
 
@@ -261,9 +279,12 @@ void layout_scratch(ds4moe *h, Carver &c) {
     S.nuniq = c.take<int32_t>(1);
     S.perm = c.take<int32_t>(P);
     S.inv = c.take<int32_t>(P);
-    S.h = c.take<float>(P * L.I);
+    S.h = c.take<uint16_t>(P * L.I);
     S.ye = c.take<float>(P * L.H);
-    S.hsh = c.take<float>(T * (L.Ish > 0 ? L.Ish : 1));
+    S.hsh = c.take<uint16_t>(T * (L.Ish > 0 ? L.Ish : 2));
+    S.grp_gu = c.take<int4>(U + P / 128 + 1);
+    S.grp_dn = c.take<int4>(U + P / 256 + 1);
+    S.ngrp = c.take<int32_t>(2);
     S.ysh = c.take<float>(T * L.H);
     S.xstage = c.take<uint16_t>(T * L.H);
     S.ystage = c.take<float>(T * L.H);
@@ -369,29 +390,83 @@ int run_dispatch(ds4moe *h, int T) {
     return launch_rc();
 }
 
-// Experts and combine for the routing already in S.idx / S.w (x already prepped).
-int run_experts_simple(ds4moe *h, int T, float *y) {
+// Grid size and dynamic shared memory of the prefill GEMM kernels.
+int g_pf_grid = 0;
+
+template <int FMT, int NA, int EPI> int setup_gemm() {
+    return cuda_rc(cudaFuncSetAttribute(pf::grouped_gemm_kernel<FMT, NA, EPI>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, pf::Cfg<NA>::kSmemBytes));
+}
+
+template <int FMT, int NA, int EPI> void launch_gemm(ds4moe *h, const char *name, const pf::Args &a) {
+    launch(h, name, [&] {
+        pf::grouped_gemm_kernel<FMT, NA, EPI><<<g_pf_grid, pf::kThreads, pf::Cfg<NA>::kSmemBytes, h->stream>>>(a);
+    });
+}
+
+// Experts and combine for the routing already in S.idx / S.w: grouped
+// tensor-core GEMMs over the expert-grouped rows.
+int run_experts_prefill(ds4moe *h, const void *x, int T, float *y) {
     const LayerDev &L = h->L;
     Scratch &S = h->S;
     cudaStream_t st = h->stream;
-    const int P = T * L.K;
-    const int U = P < L.E ? P : L.E;
     int rc = run_dispatch(h, T);
     if (rc)
         return rc;
-    launch(h, "simple_gateup_q2", [&] {
-        simple_gateup_q2_kernel<<<dim3(blocks_for(L.I, kRowsPerCta), U), 32 * kRowsPerCta, 0, st>>>(L, S);
+    launch(h, "plan_groups", [&] {
+        pf::plan_groups_kernel<<<1, 1024, 0, st>>>(S.uexp, S.uoff, S.nuniq, 128, S.grp_gu, S.ngrp, 256, S.grp_dn,
+                                                     S.ngrp + 1);
     });
-    launch(h, "simple_down_q2", [&] {
-        simple_down_q2_kernel<<<dim3(blocks_for(L.H, kRowsPerCta), U), 32 * kRowsPerCta, 0, st>>>(L, S);
-    });
+    pf::Args a{};
+    a.status = h->status;
+    // routed gate/up: B rows are the tokens of the expert-grouped pairs
+    a.q2[0] = L.gate;
+    a.q2[1] = L.up;
+    a.M = L.I;
+    a.Kd = L.H;
+    a.groups = S.grp_gu;
+    a.ngroups = S.ngrp;
+    a.dense_n = 0;
+    a.b = static_cast<const uint16_t *>(x);
+    a.ldb = L.H;
+    a.bmap = S.perm;
+    a.bmap_div = L.K;
+    a.out = S.h;
+    a.ldo = L.I;
+    launch_gemm<pf::kFmtQ2, 2, pf::kEpiSwiGLU>(h, "prefill_gateup_q2", a);
+    // routed down
+    a.q2[0] = L.down;
+    a.M = L.H;
+    a.Kd = L.I;
+    a.groups = S.grp_dn;
+    a.ngroups = S.ngrp + 1;
+    a.b = S.h;
+    a.ldb = L.I;
+    a.bmap = nullptr;
+    a.out = S.ye;
+    a.ldo = L.H;
+    launch_gemm<pf::kFmtQ2, 1, pf::kEpiF32>(h, "prefill_down_q2", a);
     if (L.Ish > 0) {
-        launch(h, "simple_gateup_q8", [&] {
-            simple_gateup_q8_kernel<<<blocks_for(L.Ish, kRowsPerCta), 32 * kRowsPerCta, 0, st>>>(L, S, T);
-        });
-        launch(h, "simple_down_q8", [&] {
-            simple_down_q8_kernel<<<blocks_for(L.H, kRowsPerCta), 32 * kRowsPerCta, 0, st>>>(L, S, T);
-        });
+        pf::Args s{};
+        s.status = h->status;
+        s.q8[0] = L.sh_gate;
+        s.q8[1] = L.sh_up;
+        s.M = L.Ish;
+        s.Kd = L.H;
+        s.dense_n = T;
+        s.b = static_cast<const uint16_t *>(x);
+        s.ldb = L.H;
+        s.out = S.hsh;
+        s.ldo = L.Ish;
+        launch_gemm<pf::kFmtQ8, 2, pf::kEpiSwiGLU>(h, "prefill_gateup_q8", s);
+        s.q8[0] = L.sh_down;
+        s.M = L.H;
+        s.Kd = L.Ish;
+        s.b = S.hsh;
+        s.ldb = L.Ish;
+        s.out = S.ysh;
+        s.ldo = L.H;
+        launch_gemm<pf::kFmtQ8, 1, pf::kEpiF32>(h, "prefill_down_q8", s);
     }
     launch(h, "combine", [&] {
         combine_kernel<<<blocks_for((int64_t)T * L.H / 4, 256), 256, 0, st>>>(
@@ -489,7 +564,7 @@ int forward_impl(ds4moe *h, const void *x, int T, int path, float *y) {
     int rc = run_router(h, x, T, nullptr);
     if (rc)
         return rc;
-    return run_experts_simple(h, T, y);
+    return run_experts_prefill(h, x, T, y);
 }
 
 } // namespace
@@ -630,7 +705,15 @@ int ds4moe_create(const ds4moe_layer_desc *desc, const ds4moe_weights *w, ds4moe
     cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_fused_kernel, kDecodeThreads, sizeof(DecodeSmem));
     cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
     D.grid = per_sm * nsm;
-    if (D.grid <= 0) {
+    g_pf_grid = nsm;
+    rc = setup_gemm<pf::kFmtQ2, 2, pf::kEpiSwiGLU>();
+    if (!rc)
+        rc = setup_gemm<pf::kFmtQ2, 1, pf::kEpiF32>();
+    if (!rc)
+        rc = setup_gemm<pf::kFmtQ8, 2, pf::kEpiSwiGLU>();
+    if (!rc)
+        rc = setup_gemm<pf::kFmtQ8, 1, pf::kEpiF32>();
+    if (rc || D.grid <= 0) {
         ds4moe_destroy(h);
         return DS4MOE_ECUDA;
     }
@@ -737,7 +820,7 @@ int ds4moe_forward_routed(ds4moe_t *h, const void *x, int32_t T, const int32_t *
     rc = launch_rc();
     if (rc)
         return rc;
-    return run_experts_simple(h, T, y);
+    return run_experts_prefill(h, x, T, y);
 }
 
 int ds4moe_forward_host(ds4moe_t *h, const void *x_host, int32_t T, float *y_host) {
