@@ -27,9 +27,10 @@ constexpr unsigned kErrInternal = 1u << 2; // an internal consistency check fail
 //   codes  qs + (r * nb + b) * 64     16 words, one per 16-weight sub-block
 //   scales sc + (r * nb + b) * 16     16 bytes, low nibble scale, high nibble min
 //   dm[r * nb + b]                    binary16 d in the low half, dmin in the high half
-// Sub-block sb = 4 s + 2 h + j (s: 64-column step of the block, h: its half,
-// j: 0/1) is stored as word / scale byte 8 h + 2 s + j, so one half of every
-// step is a contiguous 32-byte (codes) and 8-byte (scales) run. Inside the
+// Sub-block sb = 4 s + v (s: 64-column step of the block, v: its 16-column
+// quarter of the step) is stored as word / scale byte 4 v + s, so the four
+// steps of one quarter are one 16-byte (codes) and 4-byte (scales) run and a
+// half (quarters 2h, 2h+1) is one 32-byte and 8-byte run. Inside the
 // word, weight pair p (weights 2p, 2p+1 of the sub-block) sits at bits 2p and
 // 16 + 2p, so a mask picks both codes of a pair into the two halves.
 struct Q2Mat {

@@ -163,8 +163,7 @@ __global__ void repack_q2_kernel(const uint32_t *__restrict__ src, int64_t nbloc
     uint32_t osc[4] = {0u, 0u, 0u, 0u}, oqs[16];
 #pragma unroll
     for (int sb = 0; sb < 16; sb++) {
-        const int st = sb >> 2, hf = (sb >> 1) & 1, j = sb & 1;
-        const int slot = 8 * hf + 2 * st + j;
+        const int slot = 4 * (sb & 3) + (sb >> 2); // position in the step major, step minor
         const uint32_t byte = (w[sb >> 2] >> (8 * (sb & 3))) & 0xFFu;
         osc[slot >> 2] |= byte << (8 * (slot & 3));
         uint32_t word = 0u;
@@ -400,7 +399,7 @@ template <int FMT, int NA, int EPI> int setup_gemm() {
 
 template <int FMT, int NA, int EPI> void launch_gemm(ds4moe *h, const char *name, const pf::Args &a) {
     launch(h, name, [&] {
-        pf::grouped_gemm_kernel<FMT, NA, EPI><<<g_pf_grid, pf::kThreads, pf::Cfg<NA>::kSmemBytes, h->stream>>>(a);
+        pf::grouped_gemm_kernel<FMT, NA, EPI><<<g_pf_grid, pf::Cfg<NA>::kThreads, pf::Cfg<NA>::kSmemBytes, h->stream>>>(a);
     });
 }
 

@@ -18,19 +18,25 @@
 // n <= 128 tokens (two accumulators, gate and up) or n <= 256 (one). The
 // kernel is persistent (one CTA per SM, tiles dealt round robin) and warp
 // specialised:
-//   warps 0-7   producers: load the quantised rows of the tile (one 256-weight
-//               block ahead in registers), expand 128 x 64 bf16 A tiles into
-//               a 4-stage ring in the 128-byte-swizzled K-major layout, and
-//               copy the B rows of the stage with cp.async;
-//   warp 8      allocates TMEM (512 columns = two accumulator sets) and one
-//               lane issues tcgen05.mma (M=128, N=n rounded up to 16, K=16)
-//               and commits stage releases and finished accumulators to
-//               mbarriers;
-//   warps 9-12  epilogue: tcgen05.ld the finished accumulator (warp w reads
+//   warps 0-15  producers: load the quantised rows of the tile (one block
+//               ahead in registers), expand them to bf16 and write them
+//               straight into TMEM with tcgen05.st (A operand stages: row r
+//               of the tile is TMEM lane r, bf16 pairs along the columns),
+//               and copy the B rows of each K step into a 128-byte-swizzled
+//               shared-memory ring with cp.async, a few steps ahead;
+//   warp 16     allocates TMEM (all 512 columns) and one lane issues
+//               tcgen05.mma (A from TMEM, B from shared memory, M=128,
+//               N = n rounded up to 16, K=16) and commits stage releases and
+//               finished accumulators to mbarriers;
+//   warps 17-20 epilogue: tcgen05.ld the finished accumulator (warp w reads
 //               TMEM lanes 32 (w % 4) ..), apply SwiGLU or nothing, store.
-// With two accumulator sets the epilogue of one tile overlaps the MMAs of
-// the next. Every mbarrier wait is bounded; a wait that runs out sets the
-// timeout bit of the status word and every role of the CTA stops.
+// The expanded weights never pass through shared memory, whose bandwidth
+// would otherwise bound the small-n tiles. TMEM columns [0, 256) hold the
+// accumulators as two 128-column slots: a tile whose n fits one slot uses one
+// (so its epilogue overlaps the next tile's MMAs), a wider tile uses both.
+// Columns [256, 512) hold the A stages. Every mbarrier wait is bounded; a
+// wait that runs out sets the timeout bit of the status word and every role
+// of the CTA stops.
 //
 // 2-bit expansion. For a 16-weight sub-block with scale sc, min m and the
 // block's d, dmin: w = (d sc) q - (dmin m). S = d sc and C = dmin m are exact
@@ -46,12 +52,9 @@
 namespace ds4 {
 namespace pf {
 
-constexpr int kStages = 4;
-constexpr int kProdWarps = 8;
-constexpr int kProdThreads = 32 * kProdWarps;
-constexpr int kMmaWarp = kProdWarps;
-constexpr int kEpiWarp0 = kProdWarps + 1;
-constexpr int kThreads = 32 * (kProdWarps + 1 + 4);
+#ifndef DS4_PF_PROD_WARPS
+#define DS4_PF_PROD_WARPS 8
+#endif
 constexpr int kTileM = 128;
 constexpr int kTileK = 64;
 constexpr uint32_t kTmemCols = 512;
@@ -79,15 +82,25 @@ struct Args {
 };
 
 template <int NA> struct Cfg {
-    static constexpr int kNMax = NA == 2 ? 128 : 256;
-    static constexpr int kABytes = kTileM * kTileK * 2;
-    static constexpr int kBBytes = kNMax * kTileK * 2;
-    static constexpr int kStageBytes = NA * kABytes + kBBytes;
-    static constexpr int kBarOffset = kStages * kStageBytes;
+    static constexpr int kProdWarps = DS4_PF_PROD_WARPS;   // producer warps (8 or 16)
+    static constexpr int kProdThreads = 32 * kProdWarps;
+    static constexpr int kMmaWarp = kProdWarps;
+    static constexpr int kEpiWarp0 = kProdWarps + 1;
+    static constexpr int kThreads = 32 * (kProdWarps + 1 + 4);
+    static constexpr int kNMax = NA == 2 ? 128 : 256;      // tokens per tile
+    static constexpr int kPart = NA * 128 * 64 / kProdThreads; // weights per producer thread per K step
+    static constexpr int kPartsPerMat = 64 / kPart;
+    static constexpr int kBPass = kProdThreads / 8;        // B rows per pass
+    static constexpr int kBRows = kNMax / kBPass;          // B rows per thread per stage
+    static constexpr int kStages = NA == 2 ? 4 : 6;        // ring depth (TMEM- / smem-limited)
+    static constexpr int kLookB = NA == 2 ? 2 : 3;         // B copies run this many steps ahead
+    static constexpr int kACols = NA * kTileK / 2;         // TMEM columns of one A stage
+    static constexpr int kAcc1 = 128 / NA;                 // accumulator width in one slot
+    static constexpr int kBBytes = kNMax * kTileK * 2;     // one B stage
+    static constexpr int kBarOffset = kStages * kBBytes;
     static constexpr int kSmemBytes = kBarOffset + 256 + 1024; // + barriers + alignment slack
-    static constexpr int kAccStride = 256;                     // TMEM columns per accumulator set
+    static_assert(256 + kStages * kACols <= (int)kTmemCols, "TMEM budget");
 };
-
 // ---- PTX helpers --------------------------------------------------------------
 
 __device__ __forceinline__ uint64_t globaltimer() {
@@ -147,11 +160,6 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
 
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
-__device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
-                 : "memory");
-}
-
 __device__ __forceinline__ uint32_t lop3_or(uint32_t v, uint32_t mask, uint32_t magic) {
     uint32_t r; // (v & mask) | magic
     asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(v), "r"(mask), "r"(magic));
@@ -164,6 +172,33 @@ __device__ __forceinline__ uint32_t hfma2(uint32_t a, uint32_t b, uint32_t c) {
     return r;
 }
 
+// Warp-wide: 32 lanes x 16 columns of TMEM from registers.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+                     taddr),
+                 "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+                 "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(r[0]),
+                 "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// One thread: D[tmem] (+)= A[tmem] * B[smem]^T for one K=16 step.
+__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                       bool accumulate) {
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "setp.ne.b32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+                 "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"((uint32_t)accumulate)
+                 : "memory");
+}
+
 // {lo, hi} rounded to bf16, lo in the low half.
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     uint32_t r;
@@ -173,51 +208,76 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 
 // ---- quantised row data of one producer thread ----------------------------------
 //
-// Producer thread tid owns row (tid >> 1) of the m-tile and half (tid & 1) of
-// every 64-column K step, in each of the NA matrices.
+// Producer warp w writes TMEM lanes 32 (w % 4) .. + 31, so thread (w, lane)
+// owns tile row 32 (w % 4) + lane. Unit u = w / 4 picks the part of every
+// 64-column K step the thread expands: with two matrices (gate/up) the
+// 32-column half u % 2 of matrix u / 2, with one matrix the 16-column
+// quarter u.
 
-struct RawQ2 { // one 256-weight block, this thread's half: 8 sub-blocks
-    uint4 c0, c1;
-    uint2 sc;
+template <int P> struct RawQ2 { // one 256-weight block, P/16 quarters of 4 sub-blocks each
+    uint4 c[P / 16];
+    uint32_t sc[P / 16];
     uint32_t dm;
 };
 
-struct RawQ8 { // one 64-column K step, this thread's half: one 32-weight block
-    uint4 c0, c1;
-    uint32_t d;
+template <int P> struct RawQ8 { // one 64-column K step, P weights (one or two 32-weight blocks)
+    uint4 c[P / 16];
+    uint32_t d[P > 32 ? P / 32 : 1];
 };
 
-__device__ __forceinline__ void load_raw(const Q2Mat &m, int64_t row, int kb, int half, RawQ2 &r) {
+// part: quarter index of the first quarter owned (P = 16: u, P = 32: 2 * half)
+template <int P> __device__ __forceinline__ void load_raw(const Q2Mat &m, int64_t row, int kb, int part, RawQ2<P> &r) {
     const int64_t blk = row * m.nb + kb;
-    const uint4 *q = reinterpret_cast<const uint4 *>(m.qs + blk * 64 + half * 32);
-    r.c0 = __ldg(q);
-    r.c1 = __ldg(q + 1);
-    r.sc = __ldg(reinterpret_cast<const uint2 *>(m.sc + blk * 16 + half * 8));
+    const uint4 *q = reinterpret_cast<const uint4 *>(m.qs + blk * 64) + part;
+#pragma unroll
+    for (int i = 0; i < P / 16; i++)
+        r.c[i] = __ldg(q + i);
+    if (P == 64) {
+        const uint4 v = __ldg(reinterpret_cast<const uint4 *>(m.sc + blk * 16));
+        r.sc[0] = v.x;
+        r.sc[1] = v.y;
+        r.sc[P / 16 - 2] = v.z;
+        r.sc[P / 16 - 1] = v.w;
+    } else if (P == 32) {
+        const uint2 v = __ldg(reinterpret_cast<const uint2 *>(m.sc + blk * 16) + part / 2);
+        r.sc[0] = v.x;
+        r.sc[P / 16 - 1] = v.y;
+    } else {
+        r.sc[0] = __ldg(reinterpret_cast<const uint32_t *>(m.sc + blk * 16) + part);
+    }
     r.dm = __ldg(m.dm + blk);
 }
 
-__device__ __forceinline__ void load_raw(const Q8Mat &m, int64_t row, int ks, int half, RawQ8 &r) {
-    const int blk = 2 * ks + half;
-    const uint4 *q = reinterpret_cast<const uint4 *>(m.qs + row * m.k + blk * 32);
-    r.c0 = __ldg(q);
-    r.c1 = __ldg(q + 1);
-    r.d = __ldg(m.d + row * (m.k / 32) + blk);
+template <int P> __device__ __forceinline__ void load_raw(const Q8Mat &m, int64_t row, int ks, int part, RawQ8<P> &r) {
+    const int blk = 2 * ks + (part >> 1); // the 32-weight block holding quarter `part`
+    const uint4 *q = reinterpret_cast<const uint4 *>(m.qs + row * m.k + blk * 32) + (part & 1);
+#pragma unroll
+    for (int i = 0; i < P / 16; i++)
+        r.c[i] = __ldg(q + i);
+    const uint16_t *d = m.d + row * (m.k / 32) + blk;
+    if (P == 64) {
+        const uint32_t v = __ldg(reinterpret_cast<const uint32_t *>(d));
+        r.d[0] = v & 0xFFFFu;
+        r.d[P > 32 ? 1 : 0] = v >> 16;
+    } else {
+        r.d[0] = __ldg(d);
+    }
 }
 
 // Expand one sub-block word (16 weights, pair p of codes at bits 2p and
 // 16 + 2p) into 8 bf16 pairs.
-__device__ __forceinline__ void expand_q2_word(uint32_t W, uint32_t S2, uint32_t N2, uint32_t (&o)[8]) {
+__device__ __forceinline__ void expand_q2_word(uint32_t W, uint32_t S2, uint32_t N2, uint32_t *o) {
     constexpr uint32_t kMagic = 0x43004300u; // bf16 128 in both halves
     const uint32_t W6 = W >> 6, W12 = W >> 12;
     // 128 + q * 4^j  ->  q, exactly
-    uint32_t q0 = hfma2(lop3_or(W, 0x00030003u, kMagic), 0x3F803F80u, 0xC300C300u);
-    uint32_t q1 = hfma2(lop3_or(W, 0x000C000Cu, kMagic), 0x3E803E80u, 0xC200C200u);
-    uint32_t q2 = hfma2(lop3_or(W, 0x00300030u, kMagic), 0x3D803D80u, 0xC100C100u);
-    uint32_t q3 = hfma2(lop3_or(W6, 0x00030003u, kMagic), 0x3F803F80u, 0xC300C300u);
-    uint32_t q4 = hfma2(lop3_or(W6, 0x000C000Cu, kMagic), 0x3E803E80u, 0xC200C200u);
-    uint32_t q5 = hfma2(lop3_or(W6, 0x00300030u, kMagic), 0x3D803D80u, 0xC100C100u);
-    uint32_t q6 = hfma2(lop3_or(W12, 0x00030003u, kMagic), 0x3F803F80u, 0xC300C300u);
-    uint32_t q7 = hfma2(lop3_or(W12, 0x000C000Cu, kMagic), 0x3E803E80u, 0xC200C200u);
+    const uint32_t q0 = hfma2(lop3_or(W, 0x00030003u, kMagic), 0x3F803F80u, 0xC300C300u);
+    const uint32_t q1 = hfma2(lop3_or(W, 0x000C000Cu, kMagic), 0x3E803E80u, 0xC200C200u);
+    const uint32_t q2 = hfma2(lop3_or(W, 0x00300030u, kMagic), 0x3D803D80u, 0xC100C100u);
+    const uint32_t q3 = hfma2(lop3_or(W6, 0x00030003u, kMagic), 0x3F803F80u, 0xC300C300u);
+    const uint32_t q4 = hfma2(lop3_or(W6, 0x000C000Cu, kMagic), 0x3E803E80u, 0xC200C200u);
+    const uint32_t q5 = hfma2(lop3_or(W6, 0x00300030u, kMagic), 0x3D803D80u, 0xC100C100u);
+    const uint32_t q6 = hfma2(lop3_or(W12, 0x00030003u, kMagic), 0x3F803F80u, 0xC300C300u);
+    const uint32_t q7 = hfma2(lop3_or(W12, 0x000C000Cu, kMagic), 0x3E803E80u, 0xC200C200u);
     o[0] = hfma2(q0, S2, N2);
     o[1] = hfma2(q1, S2, N2);
     o[2] = hfma2(q2, S2, N2);
@@ -228,21 +288,17 @@ __device__ __forceinline__ void expand_q2_word(uint32_t W, uint32_t S2, uint32_t
     o[7] = hfma2(q7, S2, N2);
 }
 
-// K step s (0..3) of the block in r -> chunks 4 half .. 4 half + 3 of row `row`.
-__device__ __forceinline__ void expand_step(const RawQ2 &r, int s, int row, int half, uint32_t a_tile) {
+__device__ __forceinline__ float nib_to_f(uint32_t n) { return __uint_as_float(0x4B000000u | n) - 8388608.0f; }
+
+// K step s (0..3) of the block -> P/2 bf16 pairs.
+template <int P> __device__ __forceinline__ void expand_step(const RawQ2<P> &r, int s, uint32_t (&o)[P / 2]) {
     const float d = f16_to_f32(r.dm), dmin = f16_to_f32(r.dm >> 16);
-    const uint32_t words[8] = {r.c0.x, r.c0.y, r.c0.z, r.c0.w, r.c1.x, r.c1.y, r.c1.z, r.c1.w};
-    const uint32_t scw = s < 2 ? r.sc.x : r.sc.y;
 #pragma unroll
-    for (int j = 0; j < 2; j++) {
-        const uint32_t b = (scw >> (16 * (s & 1) + 8 * j)) & 0xFFu;
-        const float S = d * (float)(b & 15u), C = dmin * (float)(b >> 4);
-        const uint32_t S2 = pack_bf16x2(S, S), N2 = pack_bf16x2(-C, -C);
-        uint32_t o[8];
-        expand_q2_word(words[2 * s + j], S2, N2, o);
-        const int c = 4 * half + 2 * j;
-        sts128(a_tile + umma::sw128_offset(row, c), o[0], o[1], o[2], o[3]);
-        sts128(a_tile + umma::sw128_offset(row, c + 1), o[4], o[5], o[6], o[7]);
+    for (int v = 0; v < P / 16; v++) {
+        const uint32_t words[4] = {r.c[v].x, r.c[v].y, r.c[v].z, r.c[v].w};
+        const uint32_t b = (r.sc[v] >> (8 * s)) & 0xFFu;
+        const float S = d * nib_to_f(b & 15u), C = dmin * nib_to_f(b >> 4);
+        expand_q2_word(words[s], pack_bf16x2(S, S), pack_bf16x2(-C, -C), o + 8 * v);
     }
 }
 
@@ -255,25 +311,27 @@ __device__ __forceinline__ uint32_t q8_pair(uint32_t w, int j, float d) {
     return pack_bf16x2(d * s8_to_f(w >> (16 * j)), d * s8_to_f(w >> (16 * j + 8)));
 }
 
-__device__ __forceinline__ void expand_step(const RawQ8 &r, int /*s*/, int row, int half, uint32_t a_tile) {
-    const float d = f16_to_f32(r.d);
-    const uint32_t w[8] = {r.c0.x, r.c0.y, r.c0.z, r.c0.w, r.c1.x, r.c1.y, r.c1.z, r.c1.w};
+template <int P> __device__ __forceinline__ void expand_step(const RawQ8<P> &r, int /*s*/, uint32_t (&o)[P / 2]) {
 #pragma unroll
-    for (int i = 0; i < 4; i++) {
-        const uint32_t a = w[2 * i], b = w[2 * i + 1];
-        sts128(a_tile + umma::sw128_offset(row, 4 * half + i), q8_pair(a, 0, d), q8_pair(a, 1, d), q8_pair(b, 0, d),
-               q8_pair(b, 1, d));
+    for (int v = 0; v < P / 16; v++) {
+        const float d = f16_to_f32(r.d[P > 32 ? v >> 1 : 0]);
+        const uint32_t w[4] = {r.c[v].x, r.c[v].y, r.c[v].z, r.c[v].w};
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            o[8 * v + 2 * i] = q8_pair(w[i], 0, d);
+            o[8 * v + 2 * i + 1] = q8_pair(w[i], 1, d);
+        }
     }
 }
 
 template <int FMT> struct FmtTraits;
 template <> struct FmtTraits<kFmtQ2> {
-    using Raw = RawQ2;
+    template <int P> using Raw = RawQ2<P>;
     static constexpr int kStepsPerBlk = 4;
     __device__ static const Q2Mat &mat(const Args &a, int i) { return a.q2[i]; }
 };
 template <> struct FmtTraits<kFmtQ8> {
-    using Raw = RawQ8;
+    template <int P> using Raw = RawQ8<P>;
     static constexpr int kStepsPerBlk = 1;
     __device__ static const Q8Mat &mat(const Args &a, int i) { return a.q8[i]; }
 };
@@ -290,15 +348,40 @@ __device__ __forceinline__ int4 group_at(const Args &a, int g, int nmax) {
     return a.groups[g];
 }
 
+// Accumulator placement of a tile with n_mma columns: a narrow tile
+// (n_mma <= 128 / NA) takes one 128-column slot (the next one in turn), a
+// wide tile both.
+struct AccPlace {
+    uint32_t col;     // first column
+    uint32_t mstride; // columns between the matrices' accumulators
+    int slot;         // first slot
+    bool wide;
+};
+
+template <int NA> __device__ __forceinline__ AccPlace acc_place(int n_mma, int next1) {
+    AccPlace p;
+    p.wide = n_mma > 128 / NA;
+    p.slot = p.wide ? 0 : next1;
+    p.col = p.wide ? 0u : (uint32_t)(next1 * 128);
+    p.mstride = p.wide ? 256u / NA : 128u / NA;
+    return p;
+}
+
 // ---- the kernel -------------------------------------------------------------------
 
 template <int FMT, int NA, int EPI>
-__global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const Args a) {
+__global__ void __launch_bounds__(Cfg<NA>::kThreads, 1) grouped_gemm_kernel(const Args a) {
     using C = Cfg<NA>;
     using Tr = FmtTraits<FMT>;
-    using Raw = typename Tr::Raw;
+    constexpr int kPart = C::kPart;
+    using Raw = typename Tr::template Raw<kPart>;
     constexpr int kNMax = C::kNMax;
     constexpr int kSPB = Tr::kStepsPerBlk;
+    constexpr int kStages = C::kStages;
+    constexpr int kLookB = C::kLookB;
+    constexpr int kProdWarps = C::kProdWarps;
+    constexpr int kProdThreads = C::kProdThreads;
+    constexpr int kMmaWarp = C::kMmaWarp;
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -339,82 +422,108 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const Args a)
 
     if (warp < kProdWarps) {
         // ---------------- producers ----------------
-        const int row = tid >> 1, half = tid & 1;
-        const int bc = tid & 7;                 // B chunk column of this thread
-        constexpr int kBRows = kNMax / 32;      // B rows per thread per stage
-        int stage = 0;
-        unsigned eph = 1;
-        int t = blockIdx.x, kb = 0;
-        int4 gcur = make_int4(0, 0, 0, 0);
-        Raw nxt[NA];
-        if (t < ntiles) {
-            gcur = group_at(a, t / MT, kNMax);
-            const int64_t grow = (int64_t)gcur.x * a.M + (t % MT) * kTileM + row;
+        // Step j = (tile, K step) in order uses ring slot j % kStages (a TMEM A
+        // stage and a shared-memory B stage). The B rows of step j + kLookB are
+        // copied while step j is expanded.
+        constexpr int kBRows = C::kBRows;
+        const int q = warp & 3, u = warp >> 2;
+        const int row = 32 * q + lane;
+        const int mat = u / C::kPartsPerMat;
+        const int part = (u % C::kPartsPerMat) * (kPart / 16); // first quarter of the step owned
+        const int bc = tid & 7;                       // B chunk column of this thread
+        const uint32_t a_lane = tmem + ((uint32_t)(32 * q) << 16) + 256 + mat * (kTileK / 2) + part * 8;
+        const int my_tiles = (int)blockIdx.x < ntiles ? (ntiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+        const int nsteps = my_tiles * nk;
+        auto tile_of = [&](int tl) { return (int)blockIdx.x + tl * (int)gridDim.x; };
+        // B cursor: step jb = (tile ordinal b_tl, K step b_ks); row sources in bsrc
+        const uint16_t *bsrc[kBRows];
+        int b_tl = 0, b_ks = 0;
+        auto b_rows = [&]() {
+            const int4 g = group_at(a, tile_of(b_tl) / MT, kNMax);
 #pragma unroll
-            for (int m = 0; m < NA; m++)
-                load_raw(Tr::mat(a, m), grow, 0, half, nxt[m]);
-        }
-        int brow[kBRows];
-        bool ok = true;
-        while (t < ntiles && ok) {
-            Raw cur[NA];
+            for (int i = 0; i < kBRows; i++) {
+                const int n = (tid >> 3) + C::kBPass * i;
+                const uint16_t *src = nullptr;
+                if (n < g.z) {
+                    const int p = g.y + n;
+                    const int r = a.bmap ? __ldg(a.bmap + p) / a.bmap_div : p;
+                    src = a.b + (int64_t)r * a.ldb + bc * 8;
+                }
+                bsrc[i] = src;
+            }
+        };
+        auto issue_b = [&](int jb) {
+            if (jb < nsteps) {
+                const int slot = jb % kStages;
+                if (mbar_wait(empty + slot, ((jb / kStages) & 1) ^ 1, abort, a.status)) {
+                    const uint32_t b_tile = smem_base + slot * C::kBBytes;
 #pragma unroll
-            for (int m = 0; m < NA; m++)
-                cur[m] = nxt[m];
-            const int4 g = gcur;
-            if (kb == 0) { // B row sources of this tile
-#pragma unroll
-                for (int i = 0; i < kBRows; i++) {
-                    const int n = (tid >> 3) + 32 * i;
-                    int r = -1;
-                    if (n < g.z) {
-                        const int p = g.y + n;
-                        r = a.bmap ? __ldg(a.bmap + p) / a.bmap_div : p;
-                    }
-                    brow[i] = r;
+                    for (int i = 0; i < kBRows; i++)
+                        if (bsrc[i])
+                            cp_async16(b_tile + umma::sw128_offset((tid >> 3) + C::kBPass * i, bc),
+                                       bsrc[i] + b_ks * kTileK);
+                }
+                if (++b_ks == nk) {
+                    b_ks = 0;
+                    if (++b_tl < my_tiles)
+                        b_rows();
                 }
             }
-            // prefetch the next block (possibly of the next tile)
-            int t2 = t, kb2 = kb + 1;
-            if (kb2 == nblk) {
-                kb2 = 0;
-                t2 += gridDim.x;
-                if (t2 < ntiles)
-                    gcur = group_at(a, t2 / MT, kNMax);
+            asm volatile("cp.async.commit_group;" ::: "memory");
+        };
+        // A cursor: quantised rows one block ahead in registers; the tile's
+        // group record is read once per tile
+        Raw nxt;
+        int a_tl = 0, a_kb = 0;
+        int64_t a_row = 0;
+        auto a_tile = [&]() {
+            const int t = tile_of(a_tl);
+            const int4 g = group_at(a, t / MT, kNMax);
+            a_row = (int64_t)g.x * a.M + (t % MT) * kTileM + row;
+        };
+        auto load_next = [&]() {
+            load_raw<kPart>(Tr::mat(a, mat), a_row, a_kb, part, nxt);
+            if (++a_kb == nblk) {
+                a_kb = 0;
+                if (++a_tl < my_tiles)
+                    a_tile();
             }
-            if (t2 < ntiles) {
-                const int64_t grow = (int64_t)gcur.x * a.M + (t2 % MT) * kTileM + row;
+        };
+        if (nsteps > 0) {
+            a_tile();
+            load_next();
+            b_rows();
+        }
 #pragma unroll
-                for (int m = 0; m < NA; m++)
-                    load_raw(Tr::mat(a, m), grow, kb2, half, nxt[m]);
-            }
+        for (int jb = 0; jb < kLookB; jb++)
+            issue_b(jb);
+        const int nblocks = nsteps / kSPB;
+        for (int bi = 0; bi < nblocks && !*abort; bi++) {
+            const Raw cur = nxt;
+            if (bi + 1 < nblocks)
+                load_next();
 #pragma unroll
             for (int s = 0; s < kSPB; s++) {
-                const int ks = kb * kSPB + s;
-                if (!mbar_wait(empty + stage, eph, abort, a.status)) {
-                    ok = false;
-                    break;
+                const int j = bi * kSPB + s;
+                issue_b(j + kLookB);
+                const int slot = j % kStages;
+                umma::fence_after_sync(); // the stage's empty wait came before
+                uint32_t o[kPart / 2];
+                expand_step(cur, s, o);
+                if (kPart == 64) {
+                    tmem_st16(a_lane + slot * C::kACols, *reinterpret_cast<uint32_t(*)[16]>(o));
+                    tmem_st16(a_lane + slot * C::kACols + 16, *reinterpret_cast<uint32_t(*)[16]>(o + 16));
+                } else if (kPart == 32) {
+                    tmem_st16(a_lane + slot * C::kACols, *reinterpret_cast<uint32_t(*)[16]>(o));
+                } else {
+                    tmem_st8(a_lane + slot * C::kACols, *reinterpret_cast<uint32_t(*)[8]>(o));
                 }
-                const uint32_t st_base = smem_base + stage * C::kStageBytes;
-                const uint32_t b_tile = st_base + NA * C::kABytes;
-#pragma unroll
-                for (int i = 0; i < kBRows; i++)
-                    if (brow[i] >= 0)
-                        cp_async16(b_tile + umma::sw128_offset((tid >> 3) + 32 * i, bc),
-                                   a.b + (int64_t)brow[i] * a.ldb + ks * kTileK + bc * 8);
-#pragma unroll
-                for (int m = 0; m < NA; m++)
-                    expand_step(cur[m], s, row, half, st_base + m * C::kABytes);
-                cp_async_wait_all();
+                tmem_st_wait();
+                asm volatile("cp.async.wait_group %0;" ::"n"(kLookB) : "memory");
                 umma::fence_smem_to_async();
-                mbar_arrive(full + stage);
-                if (++stage == kStages) {
-                    stage = 0;
-                    eph ^= 1u;
-                }
+                umma::fence_before_sync();
+                mbar_arrive(full + slot);
             }
-            t = t2;
-            kb = kb2;
         }
         cp_async_wait_all();
     } else if (warp == kMmaWarp) {
@@ -422,32 +531,37 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const Args a)
         if (lane == 0) {
             int stage = 0;
             unsigned fph = 0;
-            unsigned use = 0u; // bit b: parity of the next use of accumulator set b
+            unsigned use = 0u; // bit b: parity of the next use of accumulator slot b
+            int next1 = 0;     // slot of the next narrow tile
             bool ok = true;
-            int it = 0;
-            for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x, it++) {
-                const int b = it & 1;
-                if (!mbar_wait(acce + b, ((use >> b) & 1u) ^ 1u, abort, a.status))
-                    break;
-                umma::fence_after_sync();
+            const uint64_t bdesc0 = umma::desc_sw128(smem_base);
+            for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
                 const int4 g = group_at(a, t / MT, kNMax);
                 const int n_mma = max(16, (g.z + 15) & ~15);
+                const AccPlace pl = acc_place<NA>(n_mma, next1);
+                const bool wide = pl.wide;
+                const int s0 = pl.slot;
+                if (!mbar_wait(acce + s0, ((use >> s0) & 1u) ^ 1u, abort, a.status))
+                    break;
+                if (wide && !mbar_wait(acce + 1, ((use >> 1) & 1u) ^ 1u, abort, a.status))
+                    break;
+                umma::fence_after_sync();
                 const uint32_t idesc = umma::idesc_bf16_f32(kTileM, n_mma);
+                const uint32_t d0 = tmem + pl.col, d1 = d0 + pl.mstride;
                 for (int ks = 0; ks < nk; ks++) {
                     if (!mbar_wait(full + stage, fph, abort, a.status)) {
                         ok = false;
                         break;
                     }
                     umma::fence_after_sync();
-                    const uint32_t st_base = smem_base + stage * C::kStageBytes;
-                    const uint64_t bdesc = umma::desc_sw128(st_base + NA * C::kABytes);
+                    const uint64_t bdesc = bdesc0 + (uint64_t)(stage * (C::kBBytes >> 4));
+                    const uint32_t acol = tmem + 256 + stage * C::kACols;
+                    const bool acc = ks > 0;
 #pragma unroll
-                    for (int m = 0; m < NA; m++) {
-                        const uint64_t adesc = umma::desc_sw128(st_base + m * C::kABytes);
-                        const uint32_t d_tmem = tmem + b * C::kAccStride + m * 128;
-#pragma unroll
-                        for (int kk = 0; kk < kTileK / 16; kk++)
-                            umma::mma_bf16(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc, ks > 0 || kk > 0);
+                    for (int kk = 0; kk < kTileK / 16; kk++) {
+                        mma_ts(d0, acol + kk * 8, bdesc + 2 * kk, idesc, acc || kk > 0);
+                        if (NA == 2)
+                            mma_ts(d1, acol + kTileK / 2 + kk * 8, bdesc + 2 * kk, idesc, acc || kk > 0);
                     }
                     umma::commit(empty + stage);
                     if (++stage == kStages) {
@@ -457,12 +571,18 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const Args a)
                 }
                 if (!ok)
                     break;
-                umma::commit(accf + b);
-                use ^= 1u << b;
+                umma::commit(accf + s0);
+                use ^= 1u << s0;
+                if (wide) {
+                    umma::commit(accf + 1);
+                    use ^= 2u;
+                } else {
+                    next1 ^= 1;
+                }
             }
             // all issued MMAs have completed before TMEM is released
             umma::commit(fin);
-            uint64_t t0 = globaltimer();
+            const uint64_t t0 = globaltimer();
             while (!mbar_try_wait(fin, 0)) {
                 if (globaltimer() - t0 > kWaitNs) {
                     atomicOr(a.status, kErrTimeout);
@@ -476,43 +596,58 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const Args a)
         // ---------------- epilogue ----------------
         const int q = warp & 3;
         unsigned use = 0u;
-        int it = 0;
-        for (int t = blockIdx.x; t < ntiles; t += gridDim.x, it++) {
-            const int b = it & 1;
-            if (!mbar_wait(accf + b, (use >> b) & 1u, abort, a.status))
-                break;
-            use ^= 1u << b;
-            umma::fence_after_sync();
+        int next1 = 0;
+        for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
             const int4 g = group_at(a, t / MT, kNMax);
+            const int n_mma = max(16, (g.z + 15) & ~15);
+            const AccPlace pl = acc_place<NA>(n_mma, next1);
+            const bool wide = pl.wide;
+            const int s0 = pl.slot;
+            if (!mbar_wait(accf + s0, (use >> s0) & 1u, abort, a.status))
+                break;
+            if (wide && !mbar_wait(accf + 1, (use >> 1) & 1u, abort, a.status))
+                break;
+            umma::fence_after_sync();
             const int mrow = (t % MT) * kTileM + 32 * q + lane;
-            const uint32_t tbase = tmem + ((uint32_t)(32 * q) << 16) + b * C::kAccStride;
-            for (int c0 = 0; c0 < g.z; c0 += 16) {
-                uint32_t r0[16];
-                umma::tmem_ld16(tbase + c0, r0);
-                if (EPI == kEpiSwiGLU) {
-                    uint32_t r1[16];
-                    umma::tmem_ld16(tbase + 128 + c0, r1);
+            const uint32_t tbase = tmem + ((uint32_t)(32 * q) << 16) + pl.col;
+            for (int c0 = 0; c0 < g.z; c0 += 8) {
+                float v[NA][8];
+#pragma unroll
+                for (int m = 0; m < NA; m++) {
+                    uint32_t r[8];
+                    umma::tmem_ld8(tbase + m * pl.mstride + c0, r);
                     umma::tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 8; j++)
+                        v[m][j] = __uint_as_float(r[j]);
+                }
+                if (EPI == kEpiSwiGLU) {
                     uint16_t *out = static_cast<uint16_t *>(a.out);
 #pragma unroll
-                    for (int j = 0; j < 16; j++) {
+                    for (int j = 0; j < 8; j++) {
                         if (c0 + j < g.z) {
-                            const float h = silu(__uint_as_float(r0[j])) * __uint_as_float(r1[j]);
+                            const float h = silu(v[0][j]) * v[NA - 1][j];
                             out[(int64_t)(g.y + c0 + j) * a.ldo + mrow] =
                                 (uint16_t)(pack_bf16x2(h, 0.f) & 0xFFFFu);
                         }
                     }
                 } else {
-                    umma::tmem_ld_wait();
                     float *out = static_cast<float *>(a.out);
 #pragma unroll
-                    for (int j = 0; j < 16; j++)
+                    for (int j = 0; j < 8; j++)
                         if (c0 + j < g.z)
-                            out[(int64_t)(g.y + c0 + j) * a.ldo + mrow] = __uint_as_float(r0[j]);
+                            out[(int64_t)(g.y + c0 + j) * a.ldo + mrow] = v[0][j];
                 }
             }
             umma::fence_before_sync();
-            mbar_arrive(acce + b);
+            mbar_arrive(acce + s0);
+            use ^= 1u << s0;
+            if (wide) {
+                mbar_arrive(acce + 1);
+                use ^= 2u;
+            } else {
+                next1 ^= 1;
+            }
         }
     }
 
