@@ -23,19 +23,21 @@ constexpr unsigned kErrTimeout = 1u << 1;  // a bounded wait gave up
 constexpr unsigned kErrInternal = 1u << 2; // an internal consistency check failed
 
 // 2-bit matrix in the prefill kernels' layout: three separately aligned
-// streams, each row-major over (row, 256-weight block). Row r, block b:
-//   codes  qs + (r * nb + b) * 64     16 words, one per 16-weight sub-block
-//   scales sc + (r * nb + b) * 16     16 bytes, low nibble scale, high nibble min
-//   dm[r * nb + b]                    binary16 d in the low half, dmin in the high half
-// Sub-block sb = 4 s + v (s: 64-column step of the block, v: its 16-column
-// quarter of the step) is stored as word / scale byte 4 v + s, so the four
-// steps of one quarter are one 16-byte (codes) and 4-byte (scales) run and a
-// half (quarters 2h, 2h+1) is one 32-byte and 8-byte run. Inside the
+// streams over (128-row tile rt, 256-weight block b, row r of the tile), so
+// that 32 consecutive rows' pieces of one block are adjacent in memory and a
+// warp (one lane per row) reads them with 512-byte coalesced loads.
+//   codes  16-byte quarter i of (rt, b, r): ((rt * nb + b) * 4 + i) * 128 + r
+//   scales 16 bytes of (rt, b, r):           (rt * nb + b) * 128 + r
+//   dm     one word of (rt, b, r):           (rt * nb + b) * 128 + r,
+//          binary16 d in the low half, dmin in the high half
+// Rows are a multiple of 128. Sub-block sb = 4 s + v of a block (s: its
+// 64-column step, v: the step's 16-column quarter) is the word s of quarter
+// v and scale byte 4 v + s (low nibble scale, high nibble min). Inside the
 // word, weight pair p (weights 2p, 2p+1 of the sub-block) sits at bits 2p and
 // 16 + 2p, so a mask picks both codes of a pair into the two halves.
 struct Q2Mat {
-    const uint8_t *qs;
-    const uint8_t *sc;
+    const uint4 *qs;
+    const uint4 *sc;
     const uint32_t *dm;
     int64_t rows;
     int32_t nb; // blocks per row = K / 256

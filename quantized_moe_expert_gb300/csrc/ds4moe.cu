@@ -148,12 +148,16 @@ int check_desc(const ds4moe_layer_desc *d) {
 
 // ---- repacking: canonical 84/34-byte blocks -> per-field streams -----------
 
-__global__ void repack_q2_kernel(const uint32_t *__restrict__ src, int64_t nblocks, uint8_t *__restrict__ qs,
-                                 uint8_t *__restrict__ sc, uint32_t *__restrict__ dm) {
-    const int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (b >= nblocks)
+__global__ void repack_q2_kernel(const uint32_t *__restrict__ src, int64_t nblocks, int nb, uint4 *__restrict__ qs,
+                                 uint4 *__restrict__ sc, uint32_t *__restrict__ dm) {
+    const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; // canonical block: row * nb + b
+    if (idx >= nblocks)
         return;
-    const uint32_t *s = src + b * (kQ2Bytes / 4);
+    const int64_t row = idx / nb;
+    const int b = (int)(idx - row * nb);
+    const int64_t tb = (row >> 7) * nb + b; // (tile, block)
+    const int r = (int)(row & 127);
+    const uint32_t *s = src + idx * (kQ2Bytes / 4);
     uint32_t w[21];
 #pragma unroll
     for (int i = 0; i < 21; i++)
@@ -163,7 +167,7 @@ __global__ void repack_q2_kernel(const uint32_t *__restrict__ src, int64_t nbloc
     uint32_t osc[4] = {0u, 0u, 0u, 0u}, oqs[16];
 #pragma unroll
     for (int sb = 0; sb < 16; sb++) {
-        const int slot = 4 * (sb & 3) + (sb >> 2); // position in the step major, step minor
+        const int slot = 4 * (sb & 3) + (sb >> 2); // quarter major, step minor
         const uint32_t byte = (w[sb >> 2] >> (8 * (sb & 3))) & 0xFFu;
         osc[slot >> 2] |= byte << (8 * (slot & 3));
         uint32_t word = 0u;
@@ -175,12 +179,11 @@ __global__ void repack_q2_kernel(const uint32_t *__restrict__ src, int64_t nbloc
         }
         oqs[slot] = word;
     }
-    reinterpret_cast<uint4 *>(sc)[b] = make_uint4(osc[0], osc[1], osc[2], osc[3]);
-    uint4 *q = reinterpret_cast<uint4 *>(qs + b * 64);
+    sc[tb * 128 + r] = make_uint4(osc[0], osc[1], osc[2], osc[3]);
 #pragma unroll
     for (int i = 0; i < 4; i++)
-        q[i] = make_uint4(oqs[4 * i], oqs[4 * i + 1], oqs[4 * i + 2], oqs[4 * i + 3]);
-    dm[b] = w[20]; // d in the low half, dmin in the high half
+        qs[(tb * 4 + i) * 128 + r] = make_uint4(oqs[4 * i], oqs[4 * i + 1], oqs[4 * i + 2], oqs[4 * i + 3]);
+    dm[tb * 128 + r] = w[20]; // d in the low half, dmin in the high half
 }
 
 __global__ void repack_q8_kernel(const uint16_t *__restrict__ src, int64_t nblocks, int8_t *__restrict__ qs,
@@ -216,8 +219,8 @@ void layout_weights(ds4moe *h, Carver &c) {
         m.rows = rows;
         m.nb = k / 256;
         const uint64_t nblk = (uint64_t)rows * m.nb;
-        m.qs = c.take<uint8_t>(nblk * 64);
-        m.sc = c.take<uint8_t>(nblk * 16);
+        m.qs = c.take<uint4>(nblk * 4);
+        m.sc = c.take<uint4>(nblk);
         m.dm = c.take<uint32_t>(nblk);
     };
     auto q8 = [&](Q8Mat &m, int64_t rows, int k) {
@@ -282,7 +285,7 @@ void layout_scratch(ds4moe *h, Carver &c) {
     S.ye = c.take<float>(P * L.H);
     S.hsh = c.take<uint16_t>(T * (L.Ish > 0 ? L.Ish : 2));
     S.grp_gu = c.take<int4>(U + P / 128 + 1);
-    S.grp_dn = c.take<int4>(U + P / 256 + 1);
+    S.grp_dn = c.take<int4>(U + P / 128 + 1);
     S.ngrp = c.take<int32_t>(2);
     S.ysh = c.take<float>(T * L.H);
     S.xstage = c.take<uint16_t>(T * L.H);
@@ -413,8 +416,8 @@ int run_experts_prefill(ds4moe *h, const void *x, int T, float *y) {
     if (rc)
         return rc;
     launch(h, "plan_groups", [&] {
-        pf::plan_groups_kernel<<<1, 1024, 0, st>>>(S.uexp, S.uoff, S.nuniq, 128, S.grp_gu, S.ngrp, 256, S.grp_dn,
-                                                     S.ngrp + 1);
+        pf::plan_groups_kernel<<<1, 1024, 0, st>>>(S.uexp, S.uoff, S.nuniq, pf::Cfg<2>::kNMax, S.grp_gu, S.ngrp,
+                                                     pf::Cfg<1>::kNMax, S.grp_dn, S.ngrp + 1);
     });
     pf::Args a{};
     a.status = h->status;
@@ -662,7 +665,7 @@ int ds4moe_create(const ds4moe_layer_desc *desc, const ds4moe_weights *w, ds4moe
     auto rq2 = [&](const void *src, Q2Mat &m) {
         const int64_t nblk = m.rows * m.nb;
         repack_q2_kernel<<<blocks_for(nblk, 256), 256, 0, st>>>(
-            static_cast<const uint32_t *>(src), nblk, const_cast<uint8_t *>(m.qs), const_cast<uint8_t *>(m.sc),
+            static_cast<const uint32_t *>(src), nblk, m.nb, const_cast<uint4 *>(m.qs), const_cast<uint4 *>(m.sc),
             const_cast<uint32_t *>(m.dm));
     };
     auto rq8 = [&](const void *src, Q8Mat &m) {

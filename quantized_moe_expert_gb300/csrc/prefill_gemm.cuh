@@ -15,24 +15,27 @@
 //   shared down      A = 8-bit shared down,            B = the shared SwiGLU rows
 //
 // A tile is (group, 128-row m-tile): D[128 x n] = A[128 x K] * B[n x K]^T with
-// n <= 128 tokens (two accumulators, gate and up) or n <= 256 (one). The
+// n <= 128 tokens. The
 // kernel is persistent (one CTA per SM, tiles dealt round robin) and warp
 // specialised:
-//   warps 0-15  producers: load the quantised rows of the tile (one block
+//   8 warps     producers: load the quantised rows of the tile (one block
 //               ahead in registers), expand them to bf16 and write them
 //               straight into TMEM with tcgen05.st (A operand stages: row r
 //               of the tile is TMEM lane r, bf16 pairs along the columns),
 //               and copy the B rows of each K step into a 128-byte-swizzled
 //               shared-memory ring with cp.async, a few steps ahead;
-//   warp 16     allocates TMEM (all 512 columns) and one lane issues
-//               tcgen05.mma (A from TMEM, B from shared memory, M=128,
-//               N = n rounded up to 16, K=16) and commits stage releases and
-//               finished accumulators to mbarriers;
-//   warps 17-20 epilogue: tcgen05.ld the finished accumulator (warp w reads
+//   2 warps     one lane each issues tcgen05.mma (A from TMEM, B from shared
+//               memory, M=128, N = n rounded up to 16, K=16) into its own
+//               accumulator - gate and up, or, with one matrix, the partial
+//               sums of even and odd K steps - and commits stage releases and
+//               finished accumulators to mbarriers (the first also owns the
+//               TMEM allocation, all 512 columns). Two issuers keep the
+//               tensor core busy where one thread's issue rate would not;
+//   4 warps     epilogue: tcgen05.ld the finished accumulator (warp w reads
 //               TMEM lanes 32 (w % 4) ..), apply SwiGLU or nothing, store.
 // The expanded weights never pass through shared memory, whose bandwidth
 // would otherwise bound the small-n tiles. TMEM columns [0, 256) hold the
-// accumulators as two 128-column slots: a tile whose n fits one slot uses one
+// two accumulators as two 128-column slots: a tile with n <= 64 uses one
 // (so its epilogue overlaps the next tile's MMAs), a wider tile uses both.
 // Columns [256, 512) hold the A stages. Every mbarrier wait is bounded; a
 // wait that runs out sets the timeout bit of the status word and every role
@@ -84,18 +87,17 @@ struct Args {
 template <int NA> struct Cfg {
     static constexpr int kProdWarps = DS4_PF_PROD_WARPS;   // producer warps (8 or 16)
     static constexpr int kProdThreads = 32 * kProdWarps;
-    static constexpr int kMmaWarp = kProdWarps;
-    static constexpr int kEpiWarp0 = kProdWarps + 1;
-    static constexpr int kThreads = 32 * (kProdWarps + 1 + 4);
-    static constexpr int kNMax = NA == 2 ? 128 : 256;      // tokens per tile
+    static constexpr int kMmaWarp = kProdWarps;            // two issuer warps: kMmaWarp, kMmaWarp + 1
+    static constexpr int kEpiWarp0 = kProdWarps + 2;
+    static constexpr int kThreads = 32 * (kProdWarps + 2 + 4);
+    static constexpr int kNMax = 128;                      // tokens per tile
     static constexpr int kPart = NA * 128 * 64 / kProdThreads; // weights per producer thread per K step
     static constexpr int kPartsPerMat = 64 / kPart;
     static constexpr int kBPass = kProdThreads / 8;        // B rows per pass
     static constexpr int kBRows = kNMax / kBPass;          // B rows per thread per stage
-    static constexpr int kStages = NA == 2 ? 4 : 6;        // ring depth (TMEM- / smem-limited)
-    static constexpr int kLookB = NA == 2 ? 2 : 3;         // B copies run this many steps ahead
+    static constexpr int kStages = NA == 2 ? 4 : 8;        // ring depth (TMEM-limited)
+    static constexpr int kLookB = NA == 2 ? 2 : 4;         // B copies run this many steps ahead
     static constexpr int kACols = NA * kTileK / 2;         // TMEM columns of one A stage
-    static constexpr int kAcc1 = 128 / NA;                 // accumulator width in one slot
     static constexpr int kBBytes = kNMax * kTileK * 2;     // one B stage
     static constexpr int kBarOffset = kStages * kBBytes;
     static constexpr int kSmemBytes = kBarOffset + 256 + 1024; // + barriers + alignment slack
@@ -225,27 +227,28 @@ template <int P> struct RawQ8 { // one 64-column K step, P weights (one or two 3
     uint32_t d[P > 32 ? P / 32 : 1];
 };
 
-// part: quarter index of the first quarter owned (P = 16: u, P = 32: 2 * half)
+// part: first quarter owned (P = 64: 0, P = 32: 2 * half, P = 16: u).
 template <int P> __device__ __forceinline__ void load_raw(const Q2Mat &m, int64_t row, int kb, int part, RawQ2<P> &r) {
-    const int64_t blk = row * m.nb + kb;
-    const uint4 *q = reinterpret_cast<const uint4 *>(m.qs + blk * 64) + part;
+    const int64_t tb = (row >> 7) * m.nb + kb;
+    const int rr = (int)(row & 127);
 #pragma unroll
     for (int i = 0; i < P / 16; i++)
-        r.c[i] = __ldg(q + i);
+        r.c[i] = __ldg(m.qs + (tb * 4 + part + i) * 128 + rr);
+    const uint4 *scp = m.sc + tb * 128 + rr;
     if (P == 64) {
-        const uint4 v = __ldg(reinterpret_cast<const uint4 *>(m.sc + blk * 16));
+        const uint4 v = __ldg(scp);
         r.sc[0] = v.x;
         r.sc[1] = v.y;
         r.sc[P / 16 - 2] = v.z;
         r.sc[P / 16 - 1] = v.w;
     } else if (P == 32) {
-        const uint2 v = __ldg(reinterpret_cast<const uint2 *>(m.sc + blk * 16) + part / 2);
+        const uint2 v = __ldg(reinterpret_cast<const uint2 *>(scp) + part / 2);
         r.sc[0] = v.x;
         r.sc[P / 16 - 1] = v.y;
     } else {
-        r.sc[0] = __ldg(reinterpret_cast<const uint32_t *>(m.sc + blk * 16) + part);
+        r.sc[0] = __ldg(reinterpret_cast<const uint32_t *>(scp) + part);
     }
-    r.dm = __ldg(m.dm + blk);
+    r.dm = __ldg(m.dm + tb * 128 + rr);
 }
 
 template <int P> __device__ __forceinline__ void load_raw(const Q8Mat &m, int64_t row, int ks, int part, RawQ8<P> &r) {
@@ -349,21 +352,21 @@ __device__ __forceinline__ int4 group_at(const Args &a, int g, int nmax) {
 }
 
 // Accumulator placement of a tile with n_mma columns: a narrow tile
-// (n_mma <= 128 / NA) takes one 128-column slot (the next one in turn), a
-// wide tile both.
+// (n_mma <= 64) takes one 128-column slot (the next one in turn) for its two
+// accumulators, a wide tile both slots.
 struct AccPlace {
-    uint32_t col;     // first column
-    uint32_t mstride; // columns between the matrices' accumulators
-    int slot;         // first slot
+    uint32_t col;    // first accumulator
+    uint32_t stride; // columns to the second accumulator
+    int slot;        // first slot
     bool wide;
 };
 
-template <int NA> __device__ __forceinline__ AccPlace acc_place(int n_mma, int next1) {
+__device__ __forceinline__ AccPlace acc_place(int n_mma, int next1) {
     AccPlace p;
-    p.wide = n_mma > 128 / NA;
+    p.wide = n_mma > 64;
     p.slot = p.wide ? 0 : next1;
     p.col = p.wide ? 0u : (uint32_t)(next1 * 128);
-    p.mstride = p.wide ? 256u / NA : 128u / NA;
+    p.stride = p.wide ? 128u : 64u;
     return p;
 }
 
@@ -397,13 +400,13 @@ __global__ void __launch_bounds__(Cfg<NA>::kThreads, 1) grouped_gemm_kernel(cons
     if (tid == 0) {
         for (int s = 0; s < kStages; s++) {
             mbar_init(full + s, kProdThreads);
-            mbar_init(empty + s, 1);
+            mbar_init(empty + s, NA == 2 ? 2 : 1);
         }
         for (int b = 0; b < 2; b++) {
-            mbar_init(accf + b, 1);
+            mbar_init(accf + b, 2);
             mbar_init(acce + b, 128);
         }
-        mbar_init(fin, 1);
+        mbar_init(fin, 2);
         *abort = 0u;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -526,8 +529,9 @@ __global__ void __launch_bounds__(Cfg<NA>::kThreads, 1) grouped_gemm_kernel(cons
             }
         }
         cp_async_wait_all();
-    } else if (warp == kMmaWarp) {
-        // ---------------- MMA issuer ----------------
+    } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
+        // ---------------- MMA issuers ----------------
+        const int iss = warp - kMmaWarp;
         if (lane == 0) {
             int stage = 0;
             unsigned fph = 0;
@@ -538,7 +542,7 @@ __global__ void __launch_bounds__(Cfg<NA>::kThreads, 1) grouped_gemm_kernel(cons
             for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
                 const int4 g = group_at(a, t / MT, kNMax);
                 const int n_mma = max(16, (g.z + 15) & ~15);
-                const AccPlace pl = acc_place<NA>(n_mma, next1);
+                const AccPlace pl = acc_place(n_mma, next1);
                 const bool wide = pl.wide;
                 const int s0 = pl.slot;
                 if (!mbar_wait(acce + s0, ((use >> s0) & 1u) ^ 1u, abort, a.status))
@@ -547,23 +551,23 @@ __global__ void __launch_bounds__(Cfg<NA>::kThreads, 1) grouped_gemm_kernel(cons
                     break;
                 umma::fence_after_sync();
                 const uint32_t idesc = umma::idesc_bf16_f32(kTileM, n_mma);
-                const uint32_t d0 = tmem + pl.col, d1 = d0 + pl.mstride;
+                const uint32_t dacc = tmem + pl.col + iss * pl.stride;
+                const uint32_t a_off = NA == 2 ? iss * (kTileK / 2) : 0;
                 for (int ks = 0; ks < nk; ks++) {
-                    if (!mbar_wait(full + stage, fph, abort, a.status)) {
-                        ok = false;
-                        break;
-                    }
-                    umma::fence_after_sync();
-                    const uint64_t bdesc = bdesc0 + (uint64_t)(stage * (C::kBBytes >> 4));
-                    const uint32_t acol = tmem + 256 + stage * C::kACols;
-                    const bool acc = ks > 0;
+                    if (NA == 2 || (ks & 1) == iss) {
+                        if (!mbar_wait(full + stage, fph, abort, a.status)) {
+                            ok = false;
+                            break;
+                        }
+                        umma::fence_after_sync();
+                        const uint64_t bdesc = bdesc0 + (uint64_t)(stage * (C::kBBytes >> 4));
+                        const uint32_t acol = tmem + 256 + stage * C::kACols + a_off;
+                        const bool acc = NA == 2 ? ks > 0 : ks > 1;
 #pragma unroll
-                    for (int kk = 0; kk < kTileK / 16; kk++) {
-                        mma_ts(d0, acol + kk * 8, bdesc + 2 * kk, idesc, acc || kk > 0);
-                        if (NA == 2)
-                            mma_ts(d1, acol + kTileK / 2 + kk * 8, bdesc + 2 * kk, idesc, acc || kk > 0);
+                        for (int kk = 0; kk < kTileK / 16; kk++)
+                            mma_ts(dacc, acol + kk * 8, bdesc + 2 * kk, idesc, acc || kk > 0);
+                        umma::commit(empty + stage);
                     }
-                    umma::commit(empty + stage);
                     if (++stage == kStages) {
                         stage = 0;
                         fph ^= 1u;
@@ -600,7 +604,7 @@ __global__ void __launch_bounds__(Cfg<NA>::kThreads, 1) grouped_gemm_kernel(cons
         for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
             const int4 g = group_at(a, t / MT, kNMax);
             const int n_mma = max(16, (g.z + 15) & ~15);
-            const AccPlace pl = acc_place<NA>(n_mma, next1);
+            const AccPlace pl = acc_place(n_mma, next1);
             const bool wide = pl.wide;
             const int s0 = pl.slot;
             if (!mbar_wait(accf + s0, (use >> s0) & 1u, abort, a.status))
@@ -611,22 +615,28 @@ __global__ void __launch_bounds__(Cfg<NA>::kThreads, 1) grouped_gemm_kernel(cons
             const int mrow = (t % MT) * kTileM + 32 * q + lane;
             const uint32_t tbase = tmem + ((uint32_t)(32 * q) << 16) + pl.col;
             for (int c0 = 0; c0 < g.z; c0 += 8) {
-                float v[NA][8];
+                // NA == 2: v[0] gate, v[1] up; NA == 1: the two partial sums, added
+                float v[2][8];
 #pragma unroll
-                for (int m = 0; m < NA; m++) {
+                for (int m = 0; m < 2; m++) {
                     uint32_t r[8];
-                    umma::tmem_ld8(tbase + m * pl.mstride + c0, r);
+                    umma::tmem_ld8(tbase + m * pl.stride + c0, r);
                     umma::tmem_ld_wait();
 #pragma unroll
                     for (int j = 0; j < 8; j++)
                         v[m][j] = __uint_as_float(r[j]);
+                }
+                if (NA == 1) {
+#pragma unroll
+                    for (int j = 0; j < 8; j++)
+                        v[0][j] += v[1][j];
                 }
                 if (EPI == kEpiSwiGLU) {
                     uint16_t *out = static_cast<uint16_t *>(a.out);
 #pragma unroll
                     for (int j = 0; j < 8; j++) {
                         if (c0 + j < g.z) {
-                            const float h = silu(v[0][j]) * v[NA - 1][j];
+                            const float h = silu(v[0][j]) * v[1][j];
                             out[(int64_t)(g.y + c0 + j) * a.ldo + mrow] =
                                 (uint16_t)(pack_bf16x2(h, 0.f) & 0xFFFFu);
                         }
