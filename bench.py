@@ -72,6 +72,7 @@ def kernel_bytes(name, shape, T, U):
     P = T * K
     table = {
         "router_logits": 4 * E * H + 4 * T * H + 4 * T * E,
+        "router_logits_tc": 2 * 3 * E * H + 2 * T * H + 4 * T * E,
         "prefill_gateup_q2": U * 2 * I * H * Q2_BPW + 2 * T * H + 2 * P * I,
         "prefill_down_q2": U * H * I * Q2_BPW + 2 * P * I + 4 * P * H,
         "prefill_gateup_q8": 2 * Ish * H * Q8_BPW + 2 * T * H + 2 * T * Ish,
@@ -85,9 +86,10 @@ def kernel_bytes(name, shape, T, U):
 
 def kernel_flops(name, shape, T):
     """Tensor-core flops of one launch (dense contractions only)."""
-    H, I, K, Ish = shape.hidden, shape.inter, shape.top_k, shape.shared_inter
+    H, I, K, Ish, E = shape.hidden, shape.inter, shape.top_k, shape.shared_inter, shape.n_experts
     P = T * K
     table = {
+        "router_logits_tc": 2 * T * E * 3 * H,
         "prefill_gateup_q2": 2 * P * 2 * I * H,
         "prefill_down_q2": 2 * P * H * I,
         "prefill_gateup_q8": 2 * T * 2 * Ish * H,

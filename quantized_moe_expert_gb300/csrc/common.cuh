@@ -100,6 +100,7 @@ struct Scratch {
 struct LayerDev {
     int H, I, E, K, Ish, Tmax;
     const float *router_w;
+    const uint16_t *router_w3; // [E][3H] bf16: hi, mid and lo parts of router_w, which sum to it exactly
     const float *router_bias;
     Q2Mat gate, up, down; // rows: gate/up E*I (K = H), down E*H (K = I)
     Q8Mat sh_gate, sh_up, sh_down;

@@ -1,5 +1,6 @@
 // ds4moe C ABI: handle lifetime, argument checks, weight repacking and the
 // launch sequence of the layer. Kernels live in the headers included below.
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include <cstdio>
@@ -202,6 +203,24 @@ __global__ void repack_q8_kernel(const uint16_t *__restrict__ src, int64_t nbloc
     q[1] = make_uint4(w[4], w[5], w[6], w[7]);
 }
 
+// fp32 router rows -> three bf16 parts (round to nearest each), stored side by
+// side per row: w = hi + mid + lo exactly, since each remainder is exact in fp32
+// and three 8-bit significands cover fp32's 24.
+__global__ void split_router_kernel(const float *__restrict__ w, int E, int H, uint16_t *__restrict__ w3) {
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= (int64_t)E * H)
+        return;
+    const int64_t e = i / H, h = i - e * H;
+    float v = w[i];
+    uint16_t *row = w3 + e * 3 * H;
+#pragma unroll
+    for (int part = 0; part < 3; part++) {
+        const __nv_bfloat16 b = __float2bfloat16_rn(v);
+        row[part * H + h] = __bfloat16_as_ushort(b);
+        v -= __bfloat162float(b);
+    }
+}
+
 // Bump allocator over one device allocation, 256-byte aligned pieces.
 struct Carver {
     char *base;
@@ -230,6 +249,7 @@ void layout_weights(ds4moe *h, Carver &c) {
         m.d = c.take<uint16_t>((uint64_t)rows * (k / 32));
     };
     L.router_w = c.take<float>((uint64_t)L.E * L.H);
+    L.router_w3 = c.take<uint16_t>((uint64_t)L.E * 3 * L.H);
     L.router_bias = c.take<float>(L.E);
     q2(L.gate, (int64_t)L.E * L.I, L.H);
     q2(L.up, (int64_t)L.E * L.I, L.H);
@@ -341,6 +361,20 @@ template <class F> void launch(ds4moe *h, const char *name, F &&body) {
     h->stats.kernel_count += 1;
 }
 
+// Grid size and dynamic shared memory of the prefill GEMM kernels.
+int g_pf_grid = 0;
+
+template <int FMT, int NA, int EPI> int setup_gemm() {
+    return cuda_rc(cudaFuncSetAttribute(pf::grouped_gemm_kernel<FMT, NA, EPI>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, pf::Cfg<NA>::kSmemBytes));
+}
+
+template <int FMT, int NA, int EPI> void launch_gemm(ds4moe *h, const char *name, const pf::Args &a) {
+    launch(h, name, [&] {
+        pf::grouped_gemm_kernel<FMT, NA, EPI><<<g_pf_grid, pf::Cfg<NA>::kThreads, pf::Cfg<NA>::kSmemBytes, h->stream>>>(a);
+    });
+}
+
 // ---- the launch sequence ----------------------------------------------------
 
 int run_prep(ds4moe *h, const void *x, int T) {
@@ -354,17 +388,39 @@ int run_prep(ds4moe *h, const void *x, int T) {
     return launch_rc();
 }
 
+// From this many tokens on, the router logits are a tensor-core GEMM over the
+// three bf16 parts of the router rows (K = 3 H, x repeated per part);
+// below it, a warp-per-expert fp32 dot product.
+constexpr int kRouterGemmMinT = 16;
+
 int run_router(ds4moe *h, const void *x, int T, float *sel_out) {
     const LayerDev &L = h->L;
     Scratch &S = h->S;
     cudaStream_t st = h->stream;
-    int rc = run_prep(h, x, T);
-    if (rc)
-        return rc;
-    launch(h, "router_logits", [&] {
-        dim3 lg(blocks_for(L.E, 8), blocks_for(T, kRouterTok));
-        router_logits_kernel<<<lg, 256, 0, st>>>(S.x32, T, L.H, L.router_w, L.E, S.logits);
-    });
+    if (T >= kRouterGemmMinT) {
+        pf::Args a{};
+        a.status = h->status;
+        a.bf[0].p = L.router_w3;
+        a.bf[0].rows = L.E;
+        a.bf[0].ld = 3 * L.H;
+        a.M = L.E;
+        a.Kd = 3 * L.H;
+        a.dense_n = T;
+        a.b = static_cast<const uint16_t *>(x);
+        a.ldb = L.H;
+        a.b_kwrap = L.H;
+        a.out = S.logits;
+        a.ldo = L.E;
+        launch_gemm<pf::kFmtBF16, 1, pf::kEpiF32>(h, "router_logits_tc", a);
+    } else {
+        int rc = run_prep(h, x, T);
+        if (rc)
+            return rc;
+        launch(h, "router_logits", [&] {
+            dim3 lg(blocks_for(L.E, 8), blocks_for(T, kRouterTok));
+            router_logits_kernel<<<lg, 256, 0, st>>>(S.x32, T, L.H, L.router_w, L.E, S.logits);
+        });
+    }
     launch(h, "router_select", [&] {
         const size_t smem = (size_t)kSelectWarps * 2 * L.E * sizeof(float);
         router_select_kernel<<<blocks_for(T, kSelectWarps), 32 * kSelectWarps, smem, st>>>(
@@ -390,20 +446,6 @@ int run_dispatch(ds4moe *h, int T) {
         dispatch_place_kernel<<<L.E, 256, 0, st>>>(S.idx, P, S.counts, S.offsets, S.perm, S.inv);
     });
     return launch_rc();
-}
-
-// Grid size and dynamic shared memory of the prefill GEMM kernels.
-int g_pf_grid = 0;
-
-template <int FMT, int NA, int EPI> int setup_gemm() {
-    return cuda_rc(cudaFuncSetAttribute(pf::grouped_gemm_kernel<FMT, NA, EPI>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize, pf::Cfg<NA>::kSmemBytes));
-}
-
-template <int FMT, int NA, int EPI> void launch_gemm(ds4moe *h, const char *name, const pf::Args &a) {
-    launch(h, name, [&] {
-        pf::grouped_gemm_kernel<FMT, NA, EPI><<<g_pf_grid, pf::Cfg<NA>::kThreads, pf::Cfg<NA>::kSmemBytes, h->stream>>>(a);
-    });
 }
 
 // Experts and combine for the routing already in S.idx / S.w: grouped
@@ -657,6 +699,8 @@ int ds4moe_create(const ds4moe_layer_desc *desc, const ds4moe_weights *w, ds4moe
     cudaMemsetAsync(h->status, 0, sizeof(unsigned), st);
     cudaMemcpyAsync(const_cast<float *>(L.router_w), w->router_w, sizeof(float) * L.E * L.H,
                     cudaMemcpyDeviceToDevice, st);
+    split_router_kernel<<<blocks_for((int64_t)L.E * L.H, 256), 256, 0, st>>>(L.router_w, L.E, L.H,
+                                                                             const_cast<uint16_t *>(L.router_w3));
     if (w->router_bias)
         cudaMemcpyAsync(const_cast<float *>(L.router_bias), w->router_bias, sizeof(float) * L.E,
                         cudaMemcpyDeviceToDevice, st);
@@ -715,6 +759,8 @@ int ds4moe_create(const ds4moe_layer_desc *desc, const ds4moe_weights *w, ds4moe
         rc = setup_gemm<pf::kFmtQ8, 2, pf::kEpiSwiGLU>();
     if (!rc)
         rc = setup_gemm<pf::kFmtQ8, 1, pf::kEpiF32>();
+    if (!rc)
+        rc = setup_gemm<pf::kFmtBF16, 1, pf::kEpiF32>();
     if (rc || D.grid <= 0) {
         ds4moe_destroy(h);
         return DS4MOE_ECUDA;
@@ -814,9 +860,6 @@ int ds4moe_forward_routed(ds4moe_t *h, const void *x, int32_t T, const int32_t *
     h->stats.path = path == DS4MOE_PATH_AUTO ? (T <= 8 ? DS4MOE_PATH_DECODE : DS4MOE_PATH_PREFILL) : path;
     if (h->stats.path == DS4MOE_PATH_DECODE)
         return run_decode(h, x, T, y, idx, w);
-    rc = run_prep(h, x, T);
-    if (rc)
-        return rc;
     cudaMemcpyAsync(S.idx, idx, sizeof(int32_t) * T * L.K, cudaMemcpyDeviceToDevice, st);
     cudaMemcpyAsync(S.w, w, sizeof(float) * T * L.K, cudaMemcpyDeviceToDevice, st);
     rc = launch_rc();

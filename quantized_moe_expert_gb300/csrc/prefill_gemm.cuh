@@ -63,13 +63,21 @@ constexpr int kTileK = 64;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kWaitNs = 1000000000ull; // 1 s: far beyond any legitimate wait
 
-enum { kFmtQ2 = 0, kFmtQ8 = 1 };
+enum { kFmtQ2 = 0, kFmtQ8 = 1, kFmtBF16 = 2 };
 enum { kEpiSwiGLU = 0, kEpiF32 = 1 };
+
+// Plain bf16 rows [rows][ld].
+struct BfMat {
+    const uint16_t *p;
+    int64_t rows;
+    int ld;
+};
 
 // Routed tile groups: {expert, first expert-grouped position, rows, 0}.
 struct Args {
     Q2Mat q2[2];
     Q8Mat q8[2];
+    BfMat bf[1];
     int M;                 // rows of one expert's matrix (output features)
     int Kd;                // reduction length
     const int4 *groups;    // routed groups (ignored when dense_n > 0)
@@ -79,6 +87,7 @@ struct Args {
     int ldb;
     const int32_t *bmap;   // nullable: B row of position p is bmap[p] / bmap_div
     int bmap_div;
+    int b_kwrap;           // > 0: B column of reduction index k is k % b_kwrap
     void *out;             // bf16 (SwiGLU) or fp32 rows [position][ldo]
     int ldo;
     unsigned *status;
@@ -327,7 +336,39 @@ template <int P> __device__ __forceinline__ void expand_step(const RawQ8<P> &r, 
     }
 }
 
+template <int P> struct RawBF { // one 64-column K step: P bf16 of the row
+    uint4 c[P / 8];
+};
+
+template <int P> __device__ __forceinline__ void load_raw(const BfMat &m, int64_t row, int ks, int part, RawBF<P> &r) {
+    if (row < m.rows) {
+        const uint4 *q = reinterpret_cast<const uint4 *>(m.p + row * m.ld + ks * 64 + part * 16);
+#pragma unroll
+        for (int i = 0; i < P / 8; i++)
+            r.c[i] = __ldg(q + i);
+    } else {
+#pragma unroll
+        for (int i = 0; i < P / 8; i++)
+            r.c[i] = make_uint4(0u, 0u, 0u, 0u);
+    }
+}
+
+template <int P> __device__ __forceinline__ void expand_step(const RawBF<P> &r, int /*s*/, uint32_t (&o)[P / 2]) {
+#pragma unroll
+    for (int i = 0; i < P / 8; i++) {
+        o[4 * i] = r.c[i].x;
+        o[4 * i + 1] = r.c[i].y;
+        o[4 * i + 2] = r.c[i].z;
+        o[4 * i + 3] = r.c[i].w;
+    }
+}
+
 template <int FMT> struct FmtTraits;
+template <> struct FmtTraits<kFmtBF16> {
+    template <int P> using Raw = RawBF<P>;
+    static constexpr int kStepsPerBlk = 1;
+    __device__ static const BfMat &mat(const Args &a, int i) { return a.bf[0]; }
+};
 template <> struct FmtTraits<kFmtQ2> {
     template <int P> using Raw = RawQ2<P>;
     static constexpr int kStepsPerBlk = 4;
@@ -417,7 +458,7 @@ __global__ void __launch_bounds__(Cfg<NA>::kThreads, 1) grouped_gemm_kernel(cons
     umma::fence_after_sync();
     const uint32_t tmem = *tmem_slot;
 
-    const int MT = a.M / kTileM;
+    const int MT = (a.M + kTileM - 1) / kTileM; // a partial last m-tile only for plain bf16 rows
     const int nk = a.Kd / kTileK;
     const int nblk = nk / kSPB;
     const int ntiles = num_groups(a, kNMax) * MT;
@@ -440,7 +481,7 @@ __global__ void __launch_bounds__(Cfg<NA>::kThreads, 1) grouped_gemm_kernel(cons
         auto tile_of = [&](int tl) { return (int)blockIdx.x + tl * (int)gridDim.x; };
         // B cursor: step jb = (tile ordinal b_tl, K step b_ks); row sources in bsrc
         const uint16_t *bsrc[kBRows];
-        int b_tl = 0, b_ks = 0;
+        int b_tl = 0, b_ks = 0, b_col = 0;
         auto b_rows = [&]() {
             const int4 g = group_at(a, tile_of(b_tl) / MT, kNMax);
 #pragma unroll
@@ -463,11 +504,14 @@ __global__ void __launch_bounds__(Cfg<NA>::kThreads, 1) grouped_gemm_kernel(cons
 #pragma unroll
                     for (int i = 0; i < kBRows; i++)
                         if (bsrc[i])
-                            cp_async16(b_tile + umma::sw128_offset((tid >> 3) + C::kBPass * i, bc),
-                                       bsrc[i] + b_ks * kTileK);
+                            cp_async16(b_tile + umma::sw128_offset((tid >> 3) + C::kBPass * i, bc), bsrc[i] + b_col);
                 }
+                b_col += kTileK;
+                if (b_col == a.b_kwrap)
+                    b_col = 0;
                 if (++b_ks == nk) {
                     b_ks = 0;
+                    b_col = 0;
                     if (++b_tl < my_tiles)
                         b_rows();
                 }
@@ -631,7 +675,9 @@ __global__ void __launch_bounds__(Cfg<NA>::kThreads, 1) grouped_gemm_kernel(cons
                     for (int j = 0; j < 8; j++)
                         v[0][j] += v[1][j];
                 }
-                if (EPI == kEpiSwiGLU) {
+                if (mrow >= a.M) {
+                    // rows past a partial last m-tile
+                } else if (EPI == kEpiSwiGLU) {
                     uint16_t *out = static_cast<uint16_t *>(a.out);
 #pragma unroll
                     for (int j = 0; j < 8; j++) {
