@@ -42,7 +42,7 @@ def parse():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="decode_t1",
-                    choices=["decode_t1", "decode_t8", "prefill_t1024", "prefill_t4096_zipf4", "tiny"])
+                    choices=["decode_t1", "decode_t8", "prefill_t1024", "prefill_t4096_zipf4", "tiny", "prefill_profile"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile-steps", type=int, default=20)
@@ -84,6 +84,31 @@ def kernel_bytes(name, shape, T, U):
     return table.get(name)
 
 
+# dram__bytes_read.sum + dram__bytes_write.sum per launch of the dominant
+# kernel, from one ncu capture of this workload (summaries under profiles/),
+# with the SHA-1 of the kernel's source file at capture time: the figure is
+# reported only while that source is unchanged.
+TRAFFIC = {
+    ("prefill_gateup_q2", "prefill_t1024"): (2179168768, "prefill_gemm.cuh", "9a24454cb3e8befff631275e94c6d351f4aced23"),
+    ("prefill_down_q2", "prefill_t1024"): (1175128576, "prefill_gemm.cuh", "9a24454cb3e8befff631275e94c6d351f4aced23"),
+    ("decode_fused", "decode_t1"): (84275712, "decode_fused.cuh", "e855ef65301a6db281c7cc2da0f106b1344dea1c"),
+}
+
+
+def kernel_traffic(name, workload):
+    import hashlib
+    rec = TRAFFIC.get((name, workload))
+    if rec is None:
+        return None
+    path = os.path.join(ROOT, "quantized_moe_expert_gb300", "csrc", rec[1])
+    try:
+        with open(path, "rb") as f:
+            digest = hashlib.sha1(f.read()).hexdigest()
+    except OSError:
+        return None
+    return rec[0] if digest == rec[2] else None
+
+
 def kernel_flops(name, shape, T):
     """Tensor-core flops of one launch (dense contractions only)."""
     H, I, K, Ish, E = shape.hidden, shape.inter, shape.top_k, shape.shared_inter, shape.n_experts
@@ -101,16 +126,62 @@ def kernel_flops(name, shape, T):
 # ---- clocks --------------------------------------------------------------------
 
 class ClockSampler:
+    """SM clock and throttle reasons sampled during the timed region.
+
+    Reads NVML through ctypes every 2 ms (read-only queries); falls back to
+    `nvidia-smi -lms 100` when the NVML library cannot be loaded.
+    """
+    # clock event reason bits (nvml.h)
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+               0x80: "hw_power_brake_slowdown"}
     FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.sw_power_cap",
               "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
               "clocks_event_reasons.sw_thermal_slowdown"]
 
     def __init__(self, gpu_id):
         self.gpu_id = gpu_id
+        self.sm, self.mx, self.reasons = [], [], set()
         self.lines = []
         self.proc = None
+        self.stop = threading.Event()
+        self.thread = None
+        self.nvml = self._nvml_handle()
+
+    def _nvml_handle(self):
+        import ctypes
+        try:
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if lib.nvmlInit_v2() != 0:
+                return None
+            h = ctypes.c_void_p()
+            if not self.gpu_id or lib.nvmlDeviceGetHandleByUUID(self.gpu_id.encode(), ctypes.byref(h)) != 0:
+                return None
+            get_reasons = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                lib.nvmlDeviceGetCurrentClocksThrottleReasons
+            return lib, h, get_reasons
+        except (OSError, AttributeError):
+            return None
+
+    def _poll_nvml(self):
+        import ctypes
+        lib, h, get_reasons = self.nvml
+        clk, mx, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        while not self.stop.is_set():
+            if lib.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk)) == 0 and \
+                    lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:
+                self.sm.append(float(clk.value))
+                self.mx.append(float(mx.value))
+            if get_reasons(h, ctypes.byref(rs)) == 0:
+                for bit, name in self.REASONS.items():
+                    if rs.value & bit:
+                        self.reasons.add(name)
+            self.stop.wait(0.002)
 
     def __enter__(self):
+        if self.nvml:
+            self.thread = threading.Thread(target=self._poll_nvml, daemon=True)
+            self.thread.start()
+            return self
         cmd = ["nvidia-smi", "--query-gpu=" + ",".join(self.FIELDS), "--format=csv,noheader,nounits", "-lms", "100"]
         if self.gpu_id:
             cmd += ["-i", self.gpu_id]
@@ -127,15 +198,18 @@ class ClockSampler:
             self.lines.append(line.strip())
 
     def __exit__(self, *a):
+        self.stop.set()
         if self.proc:
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=5)
 
     def summary(self):
-        sm, mx, reasons = [], [], set()
+        sm, mx, reasons = list(self.sm), list(self.mx), set(self.reasons)
         names = ["sw_power_cap", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown"]
         for ln in self.lines:
             parts = [p.strip() for p in ln.split(",")]
@@ -152,7 +226,7 @@ class ClockSampler:
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "source": "nvml" if self.nvml else "nvidia-smi"}
 
 
 # ---- the workload ----------------------------------------------------------------
@@ -215,6 +289,22 @@ def dist_setup(args):
             torch.cuda.set_device(local)
         dist.init_process_group(backend)
     return world, rank, local
+
+
+def max_over_ranks(value, world, device=None):
+    """The maximum of a per-rank float over all ranks (the slowest rank's time)."""
+    if world <= 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(world, tokens_per_rank_step, steps, total_ms):
+    """Whole-job tokens/s: every rank processes its own batches (weak scaling)."""
+    return world * tokens_per_rank_step * steps / (total_ms / 1000.0)
 
 
 def run_reference(args, world, rank):
@@ -325,13 +415,8 @@ def main():
         torch.cuda.synchronize()
     barrier()
     step_ms = [a.elapsed_time(b) for a, b in evs]
-    total_ms = sum(step_ms)
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
-    value = world * T * args.steps / (total_ms / 1000.0)
+    total_ms = max_over_ranks(sum(step_ms), world, dev)
+    value = job_rate(world, T, args.steps, total_ms)
     ms_per_step = total_ms / args.steps
 
     # per-kernel device times, recorded by the library around each launch
@@ -367,13 +452,14 @@ def main():
         if t_tc > t_hbm:
             ach = dom_flops / sec / 1e12
             roofline = {"bound": "tensor", "kernel": dom, "achieved": ach, "peak": tf_peak, "unit": "TFLOP/s",
-                        "frac": ach / tf_peak, "traffic": None, "peak_source": peak_src + " bf16 burst",
+                        "frac": ach / tf_peak, "traffic": kernel_traffic(dom, args.workload),
+                        "peak_source": peak_src + " bf16 burst",
                         "flops_per_launch": dom_flops, "bytes_per_launch": dom_bytes,
                         "hbm_frac": dom_bytes / sec / 1e9 / hbm_peak, "avg_launch_us": 1000 * dom_avg_ms}
         else:
             ach = dom_bytes / sec / 1e9
             roofline = {"bound": "hbm", "kernel": dom, "achieved": ach, "peak": hbm_peak, "unit": "GB/s",
-                        "frac": ach / hbm_peak, "traffic": None, "peak_source": peak_src,
+                        "frac": ach / hbm_peak, "traffic": kernel_traffic(dom, args.workload), "peak_source": peak_src,
                         "bytes_per_launch": dom_bytes, "avg_launch_us": 1000 * dom_avg_ms}
             if dom_flops:
                 roofline["flops_per_launch"] = dom_flops
@@ -395,13 +481,8 @@ def main():
         b.synchronize()
         if i >= args.warmup:
             e2e_ms.append(a.elapsed_time(b))
-    e2e_total = sum(e2e_ms)
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([e2e_total], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_total = float(t.item())
-    e2e = {"value": world * T * args.steps / (e2e_total / 1000.0), "unit": UNIT,
+    e2e_total = max_over_ranks(sum(e2e_ms), world, dev)
+    e2e = {"value": job_rate(world, T, args.steps, e2e_total), "unit": UNIT,
            "h2d_bytes_per_step": 2 * T * shape.hidden * len(handles),
            "d2h_bytes_per_step": 4 * T * shape.hidden * len(handles)}
     for m in handles:

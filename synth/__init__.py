@@ -121,6 +121,12 @@ WORKLOADS = {
                                     tuple(SEED_BASE + 4 + 0x100 * l for l in range(4)),
                                     "long prefill with skew: 4 independent H=4096 E=384 layers, "
                                     "T=4096, Zipf(1.1) router bias (hottest ~20x mean load)"),
+    # A reduced copy of the prefill layer for profiler captures: the same expert
+    # matrices (H=4096, I=2048) but 48 experts (~400 MB of 2-bit rows, above the
+    # L2 size) and 128 tokens, so one launch is short.
+    "prefill_profile": Workload("prefill_profile", Shape(4096, 2048, 48, 6, 2048), 128, 1, False,
+                                (SEED_BASE + 5,),
+                                "profiling case: H=4096 I=2048 E=48 top-6 I_sh=2048, T=128"),
 }
 
 
@@ -231,4 +237,6 @@ def make_tokens(workload: str, T: int | None = None, first: int = 0) -> np.ndarr
         return normal_bf16(T * H, SEED_BASE + 3, S_X).reshape(T, H)
     if workload == "prefill_t4096_zipf4":
         return normal_bf16(T * H, SEED_BASE + 4 + 0x10000, S_X).reshape(T, H)
+    if workload == "prefill_profile":
+        return normal_bf16(T * H, SEED_BASE + 5 + 0x10000, S_X).reshape(T, H)
     raise KeyError(workload)
