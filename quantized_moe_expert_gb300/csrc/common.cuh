@@ -43,12 +43,26 @@ struct Q2Mat {
     int32_t nb; // blocks per row = K / 256
 };
 
-// 8-bit matrix: int8 codes [rows][K] and binary16 scales [rows][K/32].
+// 8-bit matrix in the prefill kernels' layout, per 128-row tile rt and
+// 64-column step ks (two 32-weight blocks), consecutive rows adjacent:
+//   codes  16-byte quarter i of (rt, ks, r): ((rt * nks + ks) * 4 + i) * 128 + r
+//   d      one word of (rt, ks, r):          (rt * nks + ks) * 128 + r,
+//          binary16 scale of the first block low, of the second block high
 struct Q8Mat {
-    const int8_t *qs;
-    const uint16_t *d;
+    const uint4 *qs;
+    const uint32_t *d;
     int64_t rows;
-    int32_t k;
+    int32_t nks; // K / 64
+};
+
+// bf16 matrix in the prefill kernels' layout, per 128-row tile rt and 64-column
+// step ks: 16-byte chunk c (columns 8c .. 8c+7) of row r at
+// ((rt * nks + ks) * 8 + c) * 128 + r. Rows are padded with zeros to a
+// multiple of 128.
+struct BfMat {
+    const uint4 *p;
+    int64_t rows;
+    int32_t nks;
 };
 
 __device__ __forceinline__ float f16_to_f32(uint32_t bits) {
@@ -89,6 +103,7 @@ struct Scratch {
     uint16_t *h;       // [Tmax*K][I] bf16 routed SwiGLU activations, expert-grouped order
     float *ye;         // [Tmax*K][H] routed expert outputs, expert-grouped order
     uint16_t *hsh;     // [Tmax][I_sh] bf16 shared-expert SwiGLU activations
+    uint16_t *xp;      // [Tmax*K][H] bf16 token rows in expert-grouped order (routed gate/up B)
     int4 *grp_gu;      // routed tile groups of at most 128 rows (gate/up)
     int4 *grp_dn;      // routed tile groups of at most 256 rows (down)
     int32_t *ngrp;     // [2] number of groups in grp_gu, grp_dn
@@ -100,7 +115,7 @@ struct Scratch {
 struct LayerDev {
     int H, I, E, K, Ish, Tmax;
     const float *router_w;
-    const uint16_t *router_w3; // [E][3H] bf16: hi, mid and lo parts of router_w, which sum to it exactly
+    BfMat router_w3; // [E][3H] bf16 (tile layout): hi, mid and lo parts of router_w, which sum to it exactly
     const float *router_bias;
     Q2Mat gate, up, down; // rows: gate/up E*I (K = H), down E*H (K = I)
     Q8Mat sh_gate, sh_up, sh_down;

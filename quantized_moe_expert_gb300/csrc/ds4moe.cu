@@ -1,5 +1,7 @@
 // ds4moe C ABI: handle lifetime, argument checks, weight repacking and the
 // launch sequence of the layer. Kernels live in the headers included below.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -100,6 +102,10 @@ struct DecodeState {
 
 struct ds4moe {
     Profiler prof;
+    pf::BMaps map_xp, map_h, map_hsh; // B tensor maps over scratch (fixed addresses)
+    pf::BMaps map_x;                  // over the caller's x of the last call
+    const void *map_x_ptr = nullptr;
+    int map_x_rows = -1;
     LayerDev L;
     Scratch S;
     DecodeState D;
@@ -187,20 +193,24 @@ __global__ void repack_q2_kernel(const uint32_t *__restrict__ src, int64_t nbloc
     dm[tb * 128 + r] = w[20]; // d in the low half, dmin in the high half
 }
 
-__global__ void repack_q8_kernel(const uint16_t *__restrict__ src, int64_t nblocks, int8_t *__restrict__ qs,
+__global__ void repack_q8_kernel(const uint16_t *__restrict__ src, int64_t nblocks, int nblk32, uint4 *__restrict__ qs,
                                  uint16_t *__restrict__ d) {
-    const int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (b >= nblocks)
+    const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; // canonical block: row * nblk32 + blk
+    if (idx >= nblocks)
         return;
-    const uint16_t *s = src + b * (kQ8Bytes / 2);
-    d[b] = s[0];
+    const int64_t row = idx / nblk32;
+    const int blk = (int)(idx - row * nblk32);
+    const int nks = nblk32 / 2, ks = blk >> 1, hb = blk & 1;
+    const int64_t ts = (row >> 7) * nks + ks;
+    const int r = (int)(row & 127);
+    const uint16_t *s = src + idx * (kQ8Bytes / 2);
     uint32_t w[8];
 #pragma unroll
     for (int i = 0; i < 8; i++)
         w[i] = (uint32_t)s[1 + 2 * i] | ((uint32_t)s[2 + 2 * i] << 16);
-    uint4 *q = reinterpret_cast<uint4 *>(qs + b * 32);
-    q[0] = make_uint4(w[0], w[1], w[2], w[3]);
-    q[1] = make_uint4(w[4], w[5], w[6], w[7]);
+    qs[(ts * 4 + 2 * hb) * 128 + r] = make_uint4(w[0], w[1], w[2], w[3]);
+    qs[(ts * 4 + 2 * hb + 1) * 128 + r] = make_uint4(w[4], w[5], w[6], w[7]);
+    d[(ts * 128 + r) * 2 + hb] = s[0];
 }
 
 // fp32 router rows -> three bf16 parts (round to nearest each), stored side by
@@ -210,13 +220,16 @@ __global__ void split_router_kernel(const float *__restrict__ w, int E, int H, u
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= (int64_t)E * H)
         return;
-    const int64_t e = i / H, h = i - e * H;
+    const int64_t e = i / H;
+    const int h = (int)(i - e * H);
+    const int nks = 3 * H / 64;
     float v = w[i];
-    uint16_t *row = w3 + e * 3 * H;
 #pragma unroll
     for (int part = 0; part < 3; part++) {
         const __nv_bfloat16 b = __float2bfloat16_rn(v);
-        row[part * H + h] = __bfloat16_as_ushort(b);
+        const int k = part * H + h; // column of the [E][3H] matrix
+        const int64_t chunk = (((e >> 7) * nks + k / 64) * 8 + (k % 64) / 8) * 128 + (e & 127);
+        w3[chunk * 8 + k % 8] = __bfloat16_as_ushort(b);
         v -= __bfloat162float(b);
     }
 }
@@ -244,12 +257,14 @@ void layout_weights(ds4moe *h, Carver &c) {
     };
     auto q8 = [&](Q8Mat &m, int64_t rows, int k) {
         m.rows = rows;
-        m.k = k;
-        m.qs = c.take<int8_t>((uint64_t)rows * k);
-        m.d = c.take<uint16_t>((uint64_t)rows * (k / 32));
+        m.nks = k / 64;
+        m.qs = c.take<uint4>((uint64_t)rows * k / 16);
+        m.d = c.take<uint32_t>((uint64_t)rows * (k / 64));
     };
     L.router_w = c.take<float>((uint64_t)L.E * L.H);
-    L.router_w3 = c.take<uint16_t>((uint64_t)L.E * 3 * L.H);
+    L.router_w3.rows = L.E;
+    L.router_w3.nks = 3 * L.H / 64;
+    L.router_w3.p = c.take<uint4>((uint64_t)((L.E + 127) / 128) * 128 * 3 * L.H / 8);
     L.router_bias = c.take<float>(L.E);
     q2(L.gate, (int64_t)L.E * L.I, L.H);
     q2(L.up, (int64_t)L.E * L.I, L.H);
@@ -304,6 +319,7 @@ void layout_scratch(ds4moe *h, Carver &c) {
     S.h = c.take<uint16_t>(P * L.I);
     S.ye = c.take<float>(P * L.H);
     S.hsh = c.take<uint16_t>(T * (L.Ish > 0 ? L.Ish : 2));
+    S.xp = c.take<uint16_t>(P * L.H);
     S.grp_gu = c.take<int4>(U + P / 128 + 1);
     S.grp_dn = c.take<int4>(U + P / 128 + 1);
     S.ngrp = c.take<int32_t>(2);
@@ -366,13 +382,52 @@ int g_pf_grid = 0;
 
 template <int FMT, int NA, int EPI> int setup_gemm() {
     return cuda_rc(cudaFuncSetAttribute(pf::grouped_gemm_kernel<FMT, NA, EPI>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize, pf::Cfg<NA>::kSmemBytes));
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, pf::Cfg<FMT, NA>::kSmemBytes));
 }
 
-template <int FMT, int NA, int EPI> void launch_gemm(ds4moe *h, const char *name, const pf::Args &a) {
+template <int FMT, int NA, int EPI>
+void launch_gemm(ds4moe *h, const char *name, const pf::BMaps &bm, const pf::Args &a) {
     launch(h, name, [&] {
-        pf::grouped_gemm_kernel<FMT, NA, EPI><<<g_pf_grid, pf::Cfg<NA>::kThreads, pf::Cfg<NA>::kSmemBytes, h->stream>>>(a);
+        pf::grouped_gemm_kernel<FMT, NA, EPI>
+            <<<g_pf_grid, pf::Cfg<FMT, NA>::kThreads, pf::Cfg<FMT, NA>::kSmemBytes, h->stream>>>(bm, a);
     });
+}
+
+// Tensor maps of a bf16 matrix [rows][cols] for the GEMM's B operand: 64-column
+// boxes of 16, 32, 64 and 128 rows, 128-byte swizzle, zero fill past the end.
+int make_bmaps(const void *base, int64_t rows, int cols, pf::BMaps *out) {
+    static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+    if (!encode) {
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", reinterpret_cast<void **>(&encode), 12000,
+                                             cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || !encode) {
+            cudaGetLastError();
+            encode = nullptr;
+            return DS4MOE_ECUDA;
+        }
+    }
+    for (int i = 0; i < pf::kBoxes; i++) {
+        const cuuint64_t gdim[2] = {(cuuint64_t)cols, (cuuint64_t)(rows > 0 ? rows : 1)};
+        const cuuint64_t gstride[1] = {(cuuint64_t)cols * 2};
+        const cuuint32_t box[2] = {64u, 16u << i};
+        const cuuint32_t estride[2] = {1u, 1u};
+        if (encode(&out->m[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), gdim, gstride, box,
+                   estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return DS4MOE_ECUDA;
+    }
+    return DS4MOE_OK;
+}
+
+// Tensor maps over the caller's x [T][H] (re-encoded when x or T changes).
+int x_maps(ds4moe *h, const void *x, int T) {
+    if (x == h->map_x_ptr && T == h->map_x_rows)
+        return DS4MOE_OK;
+    const int rc = make_bmaps(x, T, h->L.H, &h->map_x);
+    h->map_x_ptr = rc ? nullptr : x;
+    h->map_x_rows = rc ? -1 : T;
+    return rc;
 }
 
 // ---- the launch sequence ----------------------------------------------------
@@ -398,20 +453,19 @@ int run_router(ds4moe *h, const void *x, int T, float *sel_out) {
     Scratch &S = h->S;
     cudaStream_t st = h->stream;
     if (T >= kRouterGemmMinT) {
+        int rc = x_maps(h, x, T);
+        if (rc)
+            return rc;
         pf::Args a{};
         a.status = h->status;
-        a.bf[0].p = L.router_w3;
-        a.bf[0].rows = L.E;
-        a.bf[0].ld = 3 * L.H;
+        a.bf[0] = L.router_w3;
         a.M = L.E;
         a.Kd = 3 * L.H;
         a.dense_n = T;
-        a.b = static_cast<const uint16_t *>(x);
-        a.ldb = L.H;
         a.b_kwrap = L.H;
         a.out = S.logits;
         a.ldo = L.E;
-        launch_gemm<pf::kFmtBF16, 1, pf::kEpiF32>(h, "router_logits_tc", a);
+        launch_gemm<pf::kFmtBF16, 1, pf::kEpiF32>(h, "router_logits_tc", h->map_x, a);
     } else {
         int rc = run_prep(h, x, T);
         if (rc)
@@ -458,12 +512,15 @@ int run_experts_prefill(ds4moe *h, const void *x, int T, float *y) {
     if (rc)
         return rc;
     launch(h, "plan_groups", [&] {
-        pf::plan_groups_kernel<<<1, 1024, 0, st>>>(S.uexp, S.uoff, S.nuniq, pf::Cfg<2>::kNMax, S.grp_gu, S.ngrp,
-                                                     pf::Cfg<1>::kNMax, S.grp_dn, S.ngrp + 1);
+        pf::plan_groups_kernel<<<1, 1024, 0, st>>>(S.uexp, S.uoff, S.nuniq, pf::Cfg<pf::kFmtQ2, 2>::kNMax, S.grp_gu, S.ngrp,
+                                                     pf::Cfg<pf::kFmtQ2, 1>::kNMax, S.grp_dn, S.ngrp + 1);
+    });
+    launch(h, "gather_rows", [&] {
+        pf::gather_rows_kernel<<<T * L.K, 256, 0, st>>>(static_cast<const uint16_t *>(x), S.perm, L.K, L.H, S.xp);
     });
     pf::Args a{};
     a.status = h->status;
-    // routed gate/up: B rows are the tokens of the expert-grouped pairs
+    // routed gate/up: B rows are the gathered token rows, in expert-grouped order
     a.q2[0] = L.gate;
     a.q2[1] = L.up;
     a.M = L.I;
@@ -471,26 +528,22 @@ int run_experts_prefill(ds4moe *h, const void *x, int T, float *y) {
     a.groups = S.grp_gu;
     a.ngroups = S.ngrp;
     a.dense_n = 0;
-    a.b = static_cast<const uint16_t *>(x);
-    a.ldb = L.H;
-    a.bmap = S.perm;
-    a.bmap_div = L.K;
     a.out = S.h;
     a.ldo = L.I;
-    launch_gemm<pf::kFmtQ2, 2, pf::kEpiSwiGLU>(h, "prefill_gateup_q2", a);
+    launch_gemm<pf::kFmtQ2, 2, pf::kEpiSwiGLU>(h, "prefill_gateup_q2", h->map_xp, a);
     // routed down
     a.q2[0] = L.down;
     a.M = L.H;
     a.Kd = L.I;
     a.groups = S.grp_dn;
     a.ngroups = S.ngrp + 1;
-    a.b = S.h;
-    a.ldb = L.I;
-    a.bmap = nullptr;
     a.out = S.ye;
     a.ldo = L.H;
-    launch_gemm<pf::kFmtQ2, 1, pf::kEpiF32>(h, "prefill_down_q2", a);
+    launch_gemm<pf::kFmtQ2, 1, pf::kEpiF32>(h, "prefill_down_q2", h->map_h, a);
     if (L.Ish > 0) {
+        rc = x_maps(h, x, T);
+        if (rc)
+            return rc;
         pf::Args s{};
         s.status = h->status;
         s.q8[0] = L.sh_gate;
@@ -498,19 +551,15 @@ int run_experts_prefill(ds4moe *h, const void *x, int T, float *y) {
         s.M = L.Ish;
         s.Kd = L.H;
         s.dense_n = T;
-        s.b = static_cast<const uint16_t *>(x);
-        s.ldb = L.H;
         s.out = S.hsh;
         s.ldo = L.Ish;
-        launch_gemm<pf::kFmtQ8, 2, pf::kEpiSwiGLU>(h, "prefill_gateup_q8", s);
+        launch_gemm<pf::kFmtQ8, 2, pf::kEpiSwiGLU>(h, "prefill_gateup_q8", h->map_x, s);
         s.q8[0] = L.sh_down;
         s.M = L.H;
         s.Kd = L.Ish;
-        s.b = S.hsh;
-        s.ldb = L.Ish;
         s.out = S.ysh;
         s.ldo = L.H;
-        launch_gemm<pf::kFmtQ8, 1, pf::kEpiF32>(h, "prefill_down_q8", s);
+        launch_gemm<pf::kFmtQ8, 1, pf::kEpiF32>(h, "prefill_down_q8", h->map_hsh, s);
     }
     launch(h, "combine", [&] {
         combine_kernel<<<blocks_for((int64_t)T * L.H / 4, 256), 256, 0, st>>>(
@@ -694,13 +743,27 @@ int ds4moe_create(const ds4moe_layer_desc *desc, const ds4moe_weights *w, ds4moe
     layout_weights(h, wc);
     Carver sc{static_cast<char *>(h->scratch_mem)};
     layout_scratch(h, sc);
+    {
+        const int64_t P = (int64_t)L.Tmax * L.K;
+        rc = make_bmaps(h->S.xp, P, L.H, &h->map_xp);
+        if (!rc)
+            rc = make_bmaps(h->S.h, P, L.I, &h->map_h);
+        if (!rc && L.Ish > 0)
+            rc = make_bmaps(h->S.hsh, L.Tmax, L.Ish, &h->map_hsh);
+        if (rc) {
+            ds4moe_destroy(h);
+            return rc;
+        }
+    }
 
     cudaStream_t st = nullptr; // create-time work runs on the legacy stream and is waited for
     cudaMemsetAsync(h->status, 0, sizeof(unsigned), st);
     cudaMemcpyAsync(const_cast<float *>(L.router_w), w->router_w, sizeof(float) * L.E * L.H,
                     cudaMemcpyDeviceToDevice, st);
-    split_router_kernel<<<blocks_for((int64_t)L.E * L.H, 256), 256, 0, st>>>(L.router_w, L.E, L.H,
-                                                                             const_cast<uint16_t *>(L.router_w3));
+    cudaMemsetAsync(const_cast<uint4 *>(L.router_w3.p), 0,
+                    (size_t)((L.E + 127) / 128) * 128 * 3 * L.H * sizeof(uint16_t), st);
+    split_router_kernel<<<blocks_for((int64_t)L.E * L.H, 256), 256, 0, st>>>(
+        L.router_w, L.E, L.H, reinterpret_cast<uint16_t *>(const_cast<uint4 *>(L.router_w3.p)));
     if (w->router_bias)
         cudaMemcpyAsync(const_cast<float *>(L.router_bias), w->router_bias, sizeof(float) * L.E,
                         cudaMemcpyDeviceToDevice, st);
@@ -713,9 +776,10 @@ int ds4moe_create(const ds4moe_layer_desc *desc, const ds4moe_weights *w, ds4moe
             const_cast<uint32_t *>(m.dm));
     };
     auto rq8 = [&](const void *src, Q8Mat &m) {
-        const int64_t nblk = m.rows * (m.k / 32);
+        const int64_t nblk = m.rows * (m.nks * 2);
         repack_q8_kernel<<<blocks_for(nblk, 256), 256, 0, st>>>(
-            static_cast<const uint16_t *>(src), nblk, const_cast<int8_t *>(m.qs), const_cast<uint16_t *>(m.d));
+            static_cast<const uint16_t *>(src), nblk, m.nks * 2, const_cast<uint4 *>(m.qs),
+            reinterpret_cast<uint16_t *>(const_cast<uint32_t *>(m.d)));
     };
     rq2(w->gate, L.gate);
     rq2(w->up, L.up);

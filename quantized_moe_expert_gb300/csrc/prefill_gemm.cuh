@@ -1,29 +1,34 @@
 // Prefill expert stage: grouped GEMMs on the 5th-generation tensor cores with
-// the quantised weights expanded to bf16 in shared memory on the fly.
+// the quantised weights expanded to bf16 on the fly.
 //
 // For a batch of many tokens the routed layer is a dense contraction per
 // expert ("a grouped GEMM that dequantizes tiles into shared memory as bf16",
 // the prefill design of the routed-MoE layer): expert e's gate/up rows times
 // the activations of the tokens routed to e, SwiGLU, then the down rows times
-// those SwiGLU rows. One kernel template serves the four GEMMs of the layer:
+// those SwiGLU rows. One kernel template serves the GEMMs of the layer:
 //
-//   routed gate/up   A = 2-bit gate and up rows of e,  B = x rows of e's tokens,
+//   routed gate/up   A = 2-bit gate and up rows of e,  B = e's token rows (x,
+//                    gathered into expert-grouped order beforehand),
 //                    out = bf16 silu(g) * u in expert-grouped order
 //   routed down      A = 2-bit down rows of e,         B = those bf16 rows,
 //                    out = fp32 expert outputs in expert-grouped order
 //   shared gate/up   A = 8-bit shared gate and up,     B = every x row
 //   shared down      A = 8-bit shared down,            B = the shared SwiGLU rows
+//   router logits    A = bf16 parts of the router,     B = every x row (K = 3H)
 //
-// A tile is (group, 128-row m-tile): D[128 x n] = A[128 x K] * B[n x K]^T with
-// n <= 128 tokens. The
-// kernel is persistent (one CTA per SM, tiles dealt round robin) and warp
+// A tile is (group of <= 128 B rows, 128-row m-tile of the expert's matrix):
+// D[128 x n] = A[128 x K] * B[n x K]^T, the weights on the M side. The kernel
+// is persistent (one CTA per SM, tiles dealt round robin) and warp
 // specialised:
-//   8 warps     producers: load the quantised rows of the tile (one block
-//               ahead in registers), expand them to bf16 and write them
-//               straight into TMEM with tcgen05.st (A operand stages: row r
-//               of the tile is TMEM lane r, bf16 pairs along the columns),
-//               and copy the B rows of each K step into a 128-byte-swizzled
-//               shared-memory ring with cp.async, a few steps ahead;
+//   1 warp      loader: one lane streams each tile's quantised rows, one
+//               256-weight block (2-bit) or 64-column step (8-bit, bf16) at
+//               a time, into a shared-memory raw ring with bulk copies, and
+//               each K step's B rows with a 2D tensor copy (128-byte swizzle,
+//               box height 16..128 rows by the tile's n) into the B ring;
+//   8 warps     producers: read their row of the raw block from shared
+//               memory, expand it to bf16 and write it straight into TMEM
+//               with tcgen05.st (A operand stages: row r of the tile is TMEM
+//               lane r, bf16 pairs along the columns);
 //   2 warps     one lane each issues tcgen05.mma (A from TMEM, B from shared
 //               memory, M=128, N = n rounded up to 16, K=16) into its own
 //               accumulator - gate and up, or, with one matrix, the partial
@@ -31,8 +36,9 @@
 //               finished accumulators to mbarriers (the first also owns the
 //               TMEM allocation, all 512 columns). Two issuers keep the
 //               tensor core busy where one thread's issue rate would not;
-//   4 warps     epilogue: tcgen05.ld the finished accumulator (warp w reads
-//               TMEM lanes 32 (w % 4) ..), apply SwiGLU or nothing, store.
+//   4 warps     epilogue: tcgen05.ld the finished accumulators (warp w reads
+//               TMEM lanes 32 (w % 4) ..), apply SwiGLU or add the partial
+//               sums, store.
 // The expanded weights never pass through shared memory, whose bandwidth
 // would otherwise bound the small-n tiles. TMEM columns [0, 256) hold the
 // two accumulators as two 128-column slots: a tile with n <= 64 uses one
@@ -49,31 +55,30 @@
 // exact in fp32.
 #pragma once
 
+#include <cuda.h>
+
 #include "common.cuh"
 #include "umma.cuh"
 
 namespace ds4 {
 namespace pf {
 
-#ifndef DS4_PF_PROD_WARPS
-#define DS4_PF_PROD_WARPS 8
-#endif
 constexpr int kTileM = 128;
 constexpr int kTileK = 64;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kWaitNs = 1000000000ull; // 1 s: far beyond any legitimate wait
+constexpr int kBoxes = 4;                   // B box heights 16, 32, 64, 128 rows
 
 enum { kFmtQ2 = 0, kFmtQ8 = 1, kFmtBF16 = 2 };
 enum { kEpiSwiGLU = 0, kEpiF32 = 1 };
 
-// Plain bf16 rows [rows][ld].
-struct BfMat {
-    const uint16_t *p;
-    int64_t rows;
-    int ld;
+// Tensor maps of one B matrix (bf16 rows, 128-byte swizzle, box 64 columns x
+// 16 << i rows); passed by value as a grid constant.
+struct BMaps {
+    CUtensorMap m[kBoxes];
 };
 
-// Routed tile groups: {expert, first expert-grouped position, rows, 0}.
+// Routed tile groups: {expert, first row of the group in B and out, rows, 0}.
 struct Args {
     Q2Mat q2[2];
     Q8Mat q8[2];
@@ -83,35 +88,35 @@ struct Args {
     const int4 *groups;    // routed groups (ignored when dense_n > 0)
     const int32_t *ngroups;
     int dense_n;           // > 0: one dense group of dense_n rows, in n-tiles
-    const uint16_t *b;     // bf16 B rows [..][ldb]
-    int ldb;
-    const int32_t *bmap;   // nullable: B row of position p is bmap[p] / bmap_div
-    int bmap_div;
     int b_kwrap;           // > 0: B column of reduction index k is k % b_kwrap
-    void *out;             // bf16 (SwiGLU) or fp32 rows [position][ldo]
+    void *out;             // bf16 (SwiGLU) or fp32 rows [group row][ldo]
     int ldo;
     unsigned *status;
 };
 
-template <int NA> struct Cfg {
-    static constexpr int kProdWarps = DS4_PF_PROD_WARPS;   // producer warps (8 or 16)
+template <int FMT, int NA> struct Cfg {
+    static constexpr int kProdWarps = 8;
     static constexpr int kProdThreads = 32 * kProdWarps;
-    static constexpr int kMmaWarp = kProdWarps;            // two issuer warps: kMmaWarp, kMmaWarp + 1
-    static constexpr int kEpiWarp0 = kProdWarps + 2;
-    static constexpr int kThreads = 32 * (kProdWarps + 2 + 4);
-    static constexpr int kNMax = 128;                      // tokens per tile
+    static constexpr int kLoadWarp = kProdWarps;           // one loader warp
+    static constexpr int kMmaWarp = kProdWarps + 1;        // two issuer warps
+    static constexpr int kEpiWarp0 = kProdWarps + 3;       // four epilogue warps
+    static constexpr int kThreads = 32 * (kProdWarps + 1 + 2 + 4);
+    static constexpr int kNMax = 128;                      // B rows per tile
     static constexpr int kPart = NA * 128 * 64 / kProdThreads; // weights per producer thread per K step
     static constexpr int kPartsPerMat = 64 / kPart;
-    static constexpr int kBPass = kProdThreads / 8;        // B rows per pass
-    static constexpr int kBRows = kNMax / kBPass;          // B rows per thread per stage
-    static constexpr int kStages = NA == 2 ? 4 : 8;        // ring depth (TMEM-limited)
-    static constexpr int kLookB = NA == 2 ? 2 : 4;         // B copies run this many steps ahead
+    static constexpr int kStages = NA == 2 ? 4 : 8;        // A (TMEM) and B (smem) ring depth
     static constexpr int kACols = NA * kTileK / 2;         // TMEM columns of one A stage
+    static constexpr int kSPB = FMT == kFmtQ2 ? 4 : 1;     // K steps per raw block
+    static constexpr int kRawMat = FMT == kFmtQ2 ? 8192 + 2048 + 512 : (FMT == kFmtQ8 ? 8192 + 512 : 16384);
+    static constexpr int kRaw = 4;                         // raw ring depth (blocks)
     static constexpr int kBBytes = kNMax * kTileK * 2;     // one B stage
-    static constexpr int kBarOffset = kStages * kBBytes;
-    static constexpr int kSmemBytes = kBarOffset + 256 + 1024; // + barriers + alignment slack
+    static constexpr int kRawOffset = kStages * kBBytes;
+    static constexpr int kBarOffset = kRawOffset + kRaw * NA * kRawMat;
+    static constexpr int kSmemBytes = kBarOffset + 512 + 1024; // + barriers + alignment slack
     static_assert(256 + kStages * kACols <= (int)kTmemCols, "TMEM budget");
+    static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 };
+
 // ---- PTX helpers --------------------------------------------------------------
 
 __device__ __forceinline__ uint64_t globaltimer() {
@@ -165,11 +170,43 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, unsigned parity, volati
     }
 }
 
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+__device__ __forceinline__ void mbar_arrive_tx(uint64_t *bar, unsigned bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(umma::smem_addr(bar)), "r"(bytes)
+                 : "memory");
 }
 
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+// Global -> shared bulk copy completing on `bar` (16-byte aligned, size % 16 == 0).
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, unsigned bytes, uint64_t *bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(src), "r"(bytes), "r"(umma::smem_addr(bar))
+                 : "memory");
+}
+
+// 2D tensor copy of the box at (x, y) (x = column, a multiple of 8) into shared memory.
+__device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap *map, int x, int y, uint64_t *bar) {
+    asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
+                 "%3}], [%4];" ::"r"(dst),
+                 "l"(map), "r"(x), "r"(y), "r"(umma::smem_addr(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ uint2 lds64(uint32_t addr) {
+    uint2 v;
+    asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
+    return v;
+}
 
 __device__ __forceinline__ uint32_t lop3_or(uint32_t v, uint32_t mask, uint32_t magic) {
     uint32_t r; // (v & mask) | magic
@@ -220,10 +257,12 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 // ---- quantised row data of one producer thread ----------------------------------
 //
 // Producer warp w writes TMEM lanes 32 (w % 4) .. + 31, so thread (w, lane)
-// owns tile row 32 (w % 4) + lane. Unit u = w / 4 picks the part of every
-// 64-column K step the thread expands: with two matrices (gate/up) the
-// 32-column half u % 2 of matrix u / 2, with one matrix the 16-column
-// quarter u.
+// owns tile row r = 32 (w % 4) + lane. Unit u = w / 4 picks the part of every
+// 64-column K step the thread expands: with two matrices (gate/up) all of
+// matrix u, with one matrix the 32-column half u. The thread reads its row's
+// share of a raw block from shared memory, where the loader put the block's
+// tile-layout pieces (consecutive rows adjacent, so a warp's reads are
+// conflict-free).
 
 template <int P> struct RawQ2 { // one 256-weight block, P/16 quarters of 4 sub-blocks each
     uint4 c[P / 16];
@@ -233,47 +272,49 @@ template <int P> struct RawQ2 { // one 256-weight block, P/16 quarters of 4 sub-
 
 template <int P> struct RawQ8 { // one 64-column K step, P weights (one or two 32-weight blocks)
     uint4 c[P / 16];
-    uint32_t d[P > 32 ? P / 32 : 1];
+    uint32_t d[P > 32 ? 2 : 1];
 };
 
-// part: first quarter owned (P = 64: 0, P = 32: 2 * half, P = 16: u).
-template <int P> __device__ __forceinline__ void load_raw(const Q2Mat &m, int64_t row, int kb, int part, RawQ2<P> &r) {
-    const int64_t tb = (row >> 7) * m.nb + kb;
-    const int rr = (int)(row & 127);
+template <int P> struct RawBF { // one 64-column K step: P bf16 of the row
+    uint4 c[P / 8];
+};
+
+// part: first 16-column quarter of the step owned (P = 64: 0, P = 32: 2 * half).
+template <int P> __device__ __forceinline__ void read_raw(uint32_t slot, int r, int part, RawQ2<P> &x) {
 #pragma unroll
     for (int i = 0; i < P / 16; i++)
-        r.c[i] = __ldg(m.qs + (tb * 4 + part + i) * 128 + rr);
-    const uint4 *scp = m.sc + tb * 128 + rr;
+        x.c[i] = lds128(slot + ((part + i) * 128 + r) * 16);
     if (P == 64) {
-        const uint4 v = __ldg(scp);
-        r.sc[0] = v.x;
-        r.sc[1] = v.y;
-        r.sc[P / 16 - 2] = v.z;
-        r.sc[P / 16 - 1] = v.w;
-    } else if (P == 32) {
-        const uint2 v = __ldg(reinterpret_cast<const uint2 *>(scp) + part / 2);
-        r.sc[0] = v.x;
-        r.sc[P / 16 - 1] = v.y;
+        const uint4 v = lds128(slot + 8192 + r * 16);
+        x.sc[0] = v.x;
+        x.sc[1] = v.y;
+        x.sc[P / 16 - 2] = v.z;
+        x.sc[P / 16 - 1] = v.w;
     } else {
-        r.sc[0] = __ldg(reinterpret_cast<const uint32_t *>(scp) + part);
+        const uint2 v = lds64(slot + 8192 + r * 16 + (part / 2) * 8);
+        x.sc[0] = v.x;
+        x.sc[P / 16 - 1] = v.y;
     }
-    r.dm = __ldg(m.dm + tb * 128 + rr);
+    x.dm = lds32(slot + 10240 + r * 4);
 }
 
-template <int P> __device__ __forceinline__ void load_raw(const Q8Mat &m, int64_t row, int ks, int part, RawQ8<P> &r) {
-    const int blk = 2 * ks + (part >> 1); // the 32-weight block holding quarter `part`
-    const uint4 *q = reinterpret_cast<const uint4 *>(m.qs + row * m.k + blk * 32) + (part & 1);
+template <int P> __device__ __forceinline__ void read_raw(uint32_t slot, int r, int part, RawQ8<P> &x) {
 #pragma unroll
     for (int i = 0; i < P / 16; i++)
-        r.c[i] = __ldg(q + i);
-    const uint16_t *d = m.d + row * (m.k / 32) + blk;
-    if (P == 64) {
-        const uint32_t v = __ldg(reinterpret_cast<const uint32_t *>(d));
-        r.d[0] = v & 0xFFFFu;
-        r.d[P > 32 ? 1 : 0] = v >> 16;
+        x.c[i] = lds128(slot + ((part + i) * 128 + r) * 16);
+    const uint32_t d = lds32(slot + 8192 + r * 4);
+    if (P > 32) {
+        x.d[0] = d & 0xFFFFu;
+        x.d[P > 32 ? 1 : 0] = d >> 16;
     } else {
-        r.d[0] = __ldg(d);
+        x.d[0] = (d >> (16 * (part / 2))) & 0xFFFFu;
     }
+}
+
+template <int P> __device__ __forceinline__ void read_raw(uint32_t slot, int r, int part, RawBF<P> &x) {
+#pragma unroll
+    for (int i = 0; i < P / 8; i++)
+        x.c[i] = lds128(slot + ((2 * part + i) * 128 + r) * 16);
 }
 
 // Expand one sub-block word (16 weights, pair p of codes at bits 2p and
@@ -336,23 +377,6 @@ template <int P> __device__ __forceinline__ void expand_step(const RawQ8<P> &r, 
     }
 }
 
-template <int P> struct RawBF { // one 64-column K step: P bf16 of the row
-    uint4 c[P / 8];
-};
-
-template <int P> __device__ __forceinline__ void load_raw(const BfMat &m, int64_t row, int ks, int part, RawBF<P> &r) {
-    if (row < m.rows) {
-        const uint4 *q = reinterpret_cast<const uint4 *>(m.p + row * m.ld + ks * 64 + part * 16);
-#pragma unroll
-        for (int i = 0; i < P / 8; i++)
-            r.c[i] = __ldg(q + i);
-    } else {
-#pragma unroll
-        for (int i = 0; i < P / 8; i++)
-            r.c[i] = make_uint4(0u, 0u, 0u, 0u);
-    }
-}
-
 template <int P> __device__ __forceinline__ void expand_step(const RawBF<P> &r, int /*s*/, uint32_t (&o)[P / 2]) {
 #pragma unroll
     for (int i = 0; i < P / 8; i++) {
@@ -364,20 +388,47 @@ template <int P> __device__ __forceinline__ void expand_step(const RawBF<P> &r, 
 }
 
 template <int FMT> struct FmtTraits;
-template <> struct FmtTraits<kFmtBF16> {
-    template <int P> using Raw = RawBF<P>;
-    static constexpr int kStepsPerBlk = 1;
-    __device__ static const BfMat &mat(const Args &a, int i) { return a.bf[0]; }
-};
 template <> struct FmtTraits<kFmtQ2> {
     template <int P> using Raw = RawQ2<P>;
-    static constexpr int kStepsPerBlk = 4;
-    __device__ static const Q2Mat &mat(const Args &a, int i) { return a.q2[i]; }
 };
 template <> struct FmtTraits<kFmtQ8> {
     template <int P> using Raw = RawQ8<P>;
-    static constexpr int kStepsPerBlk = 1;
-    __device__ static const Q8Mat &mat(const Args &a, int i) { return a.q8[i]; }
+};
+template <> struct FmtTraits<kFmtBF16> {
+    template <int P> using Raw = RawBF<P>;
+};
+
+// The loader's bulk copies of raw block kb of 128-row tile rt of matrix m
+// into `dst` (kRawMat bytes); returns the bytes.
+__device__ __forceinline__ unsigned copy_raw(const Q2Mat &m, int64_t rt, int kb, uint32_t dst, uint64_t *bar) {
+    const int64_t tb = rt * m.nb + kb;
+    bulk_g2s(dst, m.qs + tb * 512, 8192, bar);
+    bulk_g2s(dst + 8192, m.sc + tb * 128, 2048, bar);
+    bulk_g2s(dst + 10240, m.dm + tb * 128, 512, bar);
+    return 8192 + 2048 + 512;
+}
+
+__device__ __forceinline__ unsigned copy_raw(const Q8Mat &m, int64_t rt, int ks, uint32_t dst, uint64_t *bar) {
+    const int64_t ts = rt * m.nks + ks;
+    bulk_g2s(dst, m.qs + ts * 512, 8192, bar);
+    bulk_g2s(dst + 8192, m.d + ts * 128, 512, bar);
+    return 8192 + 512;
+}
+
+__device__ __forceinline__ unsigned copy_raw(const BfMat &m, int64_t rt, int ks, uint32_t dst, uint64_t *bar) {
+    bulk_g2s(dst, m.p + (rt * m.nks + ks) * 1024, 16384, bar);
+    return 16384;
+}
+
+template <int FMT> struct MatOf;
+template <> struct MatOf<kFmtQ2> {
+    __device__ static const Q2Mat &get(const Args &a, int i) { return a.q2[i]; }
+};
+template <> struct MatOf<kFmtQ8> {
+    __device__ static const Q8Mat &get(const Args &a, int i) { return a.q8[i]; }
+};
+template <> struct MatOf<kFmtBF16> {
+    __device__ static const BfMat &get(const Args &a, int i) { return a.bf[0]; }
 };
 
 // ---- tiles ------------------------------------------------------------------------
@@ -414,24 +465,24 @@ __device__ __forceinline__ AccPlace acc_place(int n_mma, int next1) {
 // ---- the kernel -------------------------------------------------------------------
 
 template <int FMT, int NA, int EPI>
-__global__ void __launch_bounds__(Cfg<NA>::kThreads, 1) grouped_gemm_kernel(const Args a) {
-    using C = Cfg<NA>;
-    using Tr = FmtTraits<FMT>;
+__global__ void __launch_bounds__(Cfg<FMT, NA>::kThreads, 1)
+    grouped_gemm_kernel(const __grid_constant__ BMaps bm, const Args a) {
+    using C = Cfg<FMT, NA>;
     constexpr int kPart = C::kPart;
-    using Raw = typename Tr::template Raw<kPart>;
+    using Raw = typename FmtTraits<FMT>::template Raw<kPart>;
     constexpr int kNMax = C::kNMax;
-    constexpr int kSPB = Tr::kStepsPerBlk;
+    constexpr int kSPB = C::kSPB;
     constexpr int kStages = C::kStages;
-    constexpr int kLookB = C::kLookB;
-    constexpr int kProdWarps = C::kProdWarps;
+    constexpr int kRaw = C::kRaw;
     constexpr int kProdThreads = C::kProdThreads;
-    constexpr int kMmaWarp = C::kMmaWarp;
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::kBarOffset);
     uint64_t *empty = full + kStages;
-    uint64_t *accf = empty + kStages;
+    uint64_t *rfull = empty + kStages;
+    uint64_t *rempty = rfull + kRaw;
+    uint64_t *accf = rempty + kRaw;
     uint64_t *acce = accf + 2;
     uint64_t *fin = acce + 2;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(fin + 1);
@@ -440,8 +491,12 @@ __global__ void __launch_bounds__(Cfg<NA>::kThreads, 1) grouped_gemm_kernel(cons
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (tid == 0) {
         for (int s = 0; s < kStages; s++) {
-            mbar_init(full + s, kProdThreads);
+            mbar_init(full + s, kProdThreads + 1); // producers + the loader's expect_tx
             mbar_init(empty + s, NA == 2 ? 2 : 1);
+        }
+        for (int s = 0; s < kRaw; s++) {
+            mbar_init(rfull + s, 1);
+            mbar_init(rempty + s, kProdThreads);
         }
         for (int b = 0; b < 2; b++) {
             mbar_init(accf + b, 2);
@@ -451,7 +506,7 @@ __global__ void __launch_bounds__(Cfg<NA>::kThreads, 1) grouped_gemm_kernel(cons
         *abort = 0u;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    if (warp == kMmaWarp)
+    if (warp == C::kMmaWarp)
         umma::tmem_alloc(tmem_slot, kTmemCols);
     umma::fence_before_sync();
     __syncthreads();
@@ -462,120 +517,124 @@ __global__ void __launch_bounds__(Cfg<NA>::kThreads, 1) grouped_gemm_kernel(cons
     const int nk = a.Kd / kTileK;
     const int nblk = nk / kSPB;
     const int ntiles = num_groups(a, kNMax) * MT;
+    const int my_tiles = (int)blockIdx.x < ntiles ? (ntiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+    const int nsteps = my_tiles * nk;
     const uint32_t smem_base = umma::smem_addr(smem);
+    const uint32_t raw_base = smem_base + C::kRawOffset;
 
-    if (warp < kProdWarps) {
+    if (warp < C::kProdWarps) {
         // ---------------- producers ----------------
-        // Step j = (tile, K step) in order uses ring slot j % kStages (a TMEM A
-        // stage and a shared-memory B stage). The B rows of step j + kLookB are
-        // copied while step j is expanded.
-        constexpr int kBRows = C::kBRows;
+        // Step j (the CTA's tiles' K steps in order) uses ring slot j % kStages;
+        // raw block rb (kSPB steps) arrives in raw slot rb % kRaw.
         const int q = warp & 3, u = warp >> 2;
         const int row = 32 * q + lane;
         const int mat = u / C::kPartsPerMat;
         const int part = (u % C::kPartsPerMat) * (kPart / 16); // first quarter of the step owned
-        const int bc = tid & 7;                       // B chunk column of this thread
         const uint32_t a_lane = tmem + ((uint32_t)(32 * q) << 16) + 256 + mat * (kTileK / 2) + part * 8;
-        const int my_tiles = (int)blockIdx.x < ntiles ? (ntiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
-        const int nsteps = my_tiles * nk;
-        auto tile_of = [&](int tl) { return (int)blockIdx.x + tl * (int)gridDim.x; };
-        // B cursor: step jb = (tile ordinal b_tl, K step b_ks); row sources in bsrc
-        const uint16_t *bsrc[kBRows];
-        int b_tl = 0, b_ks = 0, b_col = 0;
-        auto b_rows = [&]() {
-            const int4 g = group_at(a, tile_of(b_tl) / MT, kNMax);
-#pragma unroll
-            for (int i = 0; i < kBRows; i++) {
-                const int n = (tid >> 3) + C::kBPass * i;
-                const uint16_t *src = nullptr;
-                if (n < g.z) {
-                    const int p = g.y + n;
-                    const int r = a.bmap ? __ldg(a.bmap + p) / a.bmap_div : p;
-                    src = a.b + (int64_t)r * a.ldb + bc * 8;
-                }
-                bsrc[i] = src;
-            }
-        };
-        auto issue_b = [&](int jb) {
-            if (jb < nsteps) {
-                const int slot = jb % kStages;
-                if (mbar_wait(empty + slot, ((jb / kStages) & 1) ^ 1, abort, a.status)) {
-                    const uint32_t b_tile = smem_base + slot * C::kBBytes;
-#pragma unroll
-                    for (int i = 0; i < kBRows; i++)
-                        if (bsrc[i])
-                            cp_async16(b_tile + umma::sw128_offset((tid >> 3) + C::kBPass * i, bc), bsrc[i] + b_col);
-                }
-                b_col += kTileK;
-                if (b_col == a.b_kwrap)
-                    b_col = 0;
-                if (++b_ks == nk) {
-                    b_ks = 0;
-                    b_col = 0;
-                    if (++b_tl < my_tiles)
-                        b_rows();
-                }
-            }
-            asm volatile("cp.async.commit_group;" ::: "memory");
-        };
-        // A cursor: quantised rows one block ahead in registers; the tile's
-        // group record is read once per tile
-        Raw nxt;
-        int a_tl = 0, a_kb = 0;
-        int64_t a_row = 0;
-        auto a_tile = [&]() {
-            const int t = tile_of(a_tl);
-            const int4 g = group_at(a, t / MT, kNMax);
-            a_row = (int64_t)g.x * a.M + (t % MT) * kTileM + row;
-        };
-        auto load_next = [&]() {
-            load_raw<kPart>(Tr::mat(a, mat), a_row, a_kb, part, nxt);
-            if (++a_kb == nblk) {
-                a_kb = 0;
-                if (++a_tl < my_tiles)
-                    a_tile();
-            }
-        };
-        if (nsteps > 0) {
-            a_tile();
-            load_next();
-            b_rows();
-        }
-#pragma unroll
-        for (int jb = 0; jb < kLookB; jb++)
-            issue_b(jb);
         const int nblocks = nsteps / kSPB;
-        for (int bi = 0; bi < nblocks && !*abort; bi++) {
-            const Raw cur = nxt;
-            if (bi + 1 < nblocks)
-                load_next();
+        for (int rb = 0; rb < nblocks; rb++) {
+            const int rs = rb % kRaw;
+            if (!mbar_wait(rfull + rs, (rb / kRaw) & 1, abort, a.status))
+                break;
+            Raw cur;
+            read_raw(raw_base + (rs * NA + mat) * C::kRawMat, row, part, cur);
+            mbar_arrive(rempty + rs);
+            bool ok = true;
 #pragma unroll
             for (int s = 0; s < kSPB; s++) {
-                const int j = bi * kSPB + s;
-                issue_b(j + kLookB);
+                const int j = rb * kSPB + s;
                 const int slot = j % kStages;
-                umma::fence_after_sync(); // the stage's empty wait came before
+                if (!mbar_wait(empty + slot, ((j / kStages) & 1) ^ 1, abort, a.status)) {
+                    ok = false;
+                    break;
+                }
+                umma::fence_after_sync();
                 uint32_t o[kPart / 2];
                 expand_step(cur, s, o);
+                const uint32_t ta = a_lane + slot * C::kACols;
                 if (kPart == 64) {
-                    tmem_st16(a_lane + slot * C::kACols, *reinterpret_cast<uint32_t(*)[16]>(o));
-                    tmem_st16(a_lane + slot * C::kACols + 16, *reinterpret_cast<uint32_t(*)[16]>(o + 16));
+                    tmem_st16(ta, *reinterpret_cast<uint32_t(*)[16]>(o));
+                    tmem_st16(ta + 16, *reinterpret_cast<uint32_t(*)[16]>(o + 16));
                 } else if (kPart == 32) {
-                    tmem_st16(a_lane + slot * C::kACols, *reinterpret_cast<uint32_t(*)[16]>(o));
+                    tmem_st16(ta, *reinterpret_cast<uint32_t(*)[16]>(o));
                 } else {
-                    tmem_st8(a_lane + slot * C::kACols, *reinterpret_cast<uint32_t(*)[8]>(o));
+                    tmem_st8(ta, *reinterpret_cast<uint32_t(*)[8]>(o));
                 }
                 tmem_st_wait();
-                asm volatile("cp.async.wait_group %0;" ::"n"(kLookB) : "memory");
-                umma::fence_smem_to_async();
                 umma::fence_before_sync();
                 mbar_arrive(full + slot);
             }
+            if (!ok)
+                break;
         }
-        cp_async_wait_all();
-    } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
+    } else if (warp == C::kLoadWarp) {
+        // ---------------- loader ----------------
+        // Two cursors over the CTA's tiles: raw blocks run a full raw ring
+        // ahead of the B copies, which advance with the MMA's stage releases.
+        if (lane == 0) {
+            const int nblocks = my_tiles * nblk;
+            // raw cursor: global block rb = (tile ordinal r_tl, block r_kb)
+            int r_tl = 0, r_kb = 0;
+            int64_t r_rt = 0;
+            auto raw_tile = [&]() {
+                const int t = (int)blockIdx.x + r_tl * (int)gridDim.x;
+                const int4 g = group_at(a, t / MT, kNMax);
+                r_rt = (int64_t)g.x * (a.M / kTileM) + t % MT;
+            };
+            auto issue_raw = [&](int rb) -> bool {
+                const int rs = rb % kRaw;
+                if (!mbar_wait(rempty + rs, ((rb / kRaw) & 1) ^ 1, abort, a.status))
+                    return false;
+                mbar_arrive_tx(rfull + rs, NA * C::kRawMat);
+#pragma unroll
+                for (int m = 0; m < NA; m++)
+                    copy_raw(MatOf<FMT>::get(a, m), r_rt, r_kb, raw_base + (rs * NA + m) * C::kRawMat, rfull + rs);
+                if (++r_kb == nblk) {
+                    r_kb = 0;
+                    if (++r_tl < my_tiles)
+                        raw_tile();
+                }
+                return true;
+            };
+            bool ok = true;
+            int rb_next = 0;
+            if (nblocks > 0)
+                raw_tile();
+            for (; rb_next < nblocks && rb_next < kRaw && ok; rb_next++)
+                ok = issue_raw(rb_next);
+            int j = 0, gb = 0;
+            for (int tl = 0; tl < my_tiles && ok; tl++) {
+                const int t = (int)blockIdx.x + tl * (int)gridDim.x;
+                const int4 g = group_at(a, t / MT, kNMax);
+                const int n_mma = max(16, (g.z + 15) & ~15);
+                const int box = n_mma <= 16 ? 0 : (n_mma <= 32 ? 1 : (n_mma <= 64 ? 2 : 3));
+                const unsigned bbytes = (16u << box) * kTileK * 2;
+                int col = 0;
+                for (int kb = 0; kb < nblk && ok; kb++, gb++) {
+                    for (int s = 0; s < kSPB; s++, j++) {
+                        const int slot = j % kStages;
+                        if (!mbar_wait(empty + slot, ((j / kStages) & 1) ^ 1, abort, a.status)) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_tx(full + slot, bbytes);
+                        tma_2d(smem_base + slot * C::kBBytes, &bm.m[box], col, g.y, full + slot);
+                        col += kTileK;
+                        if (col == a.b_kwrap)
+                            col = 0;
+                    }
+                    // the producers have started block gb: its raw slot is free for gb + kRaw
+                    if (ok && rb_next < nblocks) {
+                        ok = issue_raw(rb_next);
+                        rb_next++;
+                    }
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == C::kMmaWarp || warp == C::kMmaWarp + 1) {
         // ---------------- MMA issuers ----------------
-        const int iss = warp - kMmaWarp;
+        const int iss = warp - C::kMmaWarp;
         if (lane == 0) {
             int stage = 0;
             unsigned fph = 0;
@@ -667,32 +726,31 @@ __global__ void __launch_bounds__(Cfg<NA>::kThreads, 1) grouped_gemm_kernel(cons
                     umma::tmem_ld8(tbase + m * pl.stride + c0, r);
                     umma::tmem_ld_wait();
 #pragma unroll
-                    for (int j = 0; j < 8; j++)
-                        v[m][j] = __uint_as_float(r[j]);
+                    for (int jj = 0; jj < 8; jj++)
+                        v[m][jj] = __uint_as_float(r[jj]);
                 }
                 if (NA == 1) {
 #pragma unroll
-                    for (int j = 0; j < 8; j++)
-                        v[0][j] += v[1][j];
+                    for (int jj = 0; jj < 8; jj++)
+                        v[0][jj] += v[1][jj];
                 }
                 if (mrow >= a.M) {
                     // rows past a partial last m-tile
                 } else if (EPI == kEpiSwiGLU) {
                     uint16_t *out = static_cast<uint16_t *>(a.out);
 #pragma unroll
-                    for (int j = 0; j < 8; j++) {
-                        if (c0 + j < g.z) {
-                            const float h = silu(v[0][j]) * v[1][j];
-                            out[(int64_t)(g.y + c0 + j) * a.ldo + mrow] =
-                                (uint16_t)(pack_bf16x2(h, 0.f) & 0xFFFFu);
+                    for (int jj = 0; jj < 8; jj++) {
+                        if (c0 + jj < g.z) {
+                            const float h = silu(v[0][jj]) * v[1][jj];
+                            out[(int64_t)(g.y + c0 + jj) * a.ldo + mrow] = (uint16_t)(pack_bf16x2(h, 0.f) & 0xFFFFu);
                         }
                     }
                 } else {
                     float *out = static_cast<float *>(a.out);
 #pragma unroll
-                    for (int j = 0; j < 8; j++)
-                        if (c0 + j < g.z)
-                            out[(int64_t)(g.y + c0 + j) * a.ldo + mrow] = v[0][j];
+                    for (int jj = 0; jj < 8; jj++)
+                        if (c0 + jj < g.z)
+                            out[(int64_t)(g.y + c0 + jj) * a.ldo + mrow] = v[0][jj];
                 }
             }
             umma::fence_before_sync();
@@ -709,10 +767,22 @@ __global__ void __launch_bounds__(Cfg<NA>::kThreads, 1) grouped_gemm_kernel(cons
 
     umma::fence_before_sync();
     __syncthreads();
-    if (warp == kMmaWarp) {
+    if (warp == C::kMmaWarp) {
         umma::fence_after_sync();
         umma::tmem_dealloc(tmem, kTmemCols);
     }
+}
+
+// B rows of the routed gate/up in expert-grouped order: xp[pos] = x[perm[pos] / K];
+// one CTA per row.
+__global__ void gather_rows_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict__ perm, int K, int H,
+                                   uint16_t *__restrict__ xp) {
+    const int pos = blockIdx.x;
+    const int t = perm[pos] / K;
+    const uint4 *src = reinterpret_cast<const uint4 *>(x + (int64_t)t * H);
+    uint4 *dst = reinterpret_cast<uint4 *>(xp + (int64_t)pos * H);
+    for (int c = threadIdx.x; c < H / 8; c += blockDim.x)
+        dst[c] = __ldg(src + c);
 }
 
 // ---- routed tile groups -------------------------------------------------------------
