@@ -478,7 +478,8 @@ int run_router(ds4moe *h, const void *x, int T, float *sel_out) {
     launch(h, "router_select", [&] {
         const size_t smem = (size_t)kSelectWarps * 2 * L.E * sizeof(float);
         router_select_kernel<<<blocks_for(T, kSelectWarps), 32 * kSelectWarps, smem, st>>>(
-            S.logits, L.router_bias, T, L.E, L.K, S.idx, S.w, S.gap, sel_out);
+            S.logits, L.router_bias, T, L.E, L.K, S.idx, S.w, S.gap, sel_out,
+            T >= kRouterGemmMinT ? static_cast<const uint16_t *>(x) : nullptr, L.router_w, L.H);
     });
     return launch_rc();
 }
@@ -1117,6 +1118,6 @@ extern "C" int ds4moe_route_noalloc(const float *router_w, const float *router_b
                                                                                           logits);
     const size_t smem = (size_t)kSelectWarps * 2 * E * sizeof(float);
     router_select_kernel<<<blocks_for(T, kSelectWarps), 32 * kSelectWarps, smem, st>>>(
-        logits, router_bias, T, E, K, idx_out, w_out, nullptr, nullptr);
+        logits, router_bias, T, E, K, idx_out, w_out, nullptr, nullptr, nullptr, nullptr, 0);
     return launch_rc();
 }

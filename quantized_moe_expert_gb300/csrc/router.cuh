@@ -84,28 +84,18 @@ __global__ void router_logits_kernel(const float *__restrict__ x32, int T, int H
 // yields the runner-up score for the near-tie gap.
 constexpr int kSelectWarps = 4;
 
-__global__ void router_select_kernel(const float *__restrict__ logits, const float *__restrict__ bias, int T,
-                                     int E, int K, int32_t *__restrict__ idx, float *__restrict__ w,
-                                     float *__restrict__ gap, float *__restrict__ sel_out) {
-    extern __shared__ float smem[];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int t = blockIdx.x * kSelectWarps + warp;
-    if (t >= T)
-        return;
-    float *sel = smem + warp * 2 * E;
-    float *score = sel + E;
-    for (int e = lane; e < E; e += 32) {
-        float s = sigmoid(logits[(int64_t)t * E + e]);
-        float v = bias ? s + bias[e] : s;
-        score[e] = s;
-        sel[e] = v;
-        if (sel_out)
-            sel_out[(int64_t)t * E + e] = v;
-    }
-    __syncwarp();
-    float chosen_s[kMaxTopK];
-    int chosen_e[kMaxTopK];
-    float kth = 0.f, next = -INFINITY;
+// Selection scores within this distance of the approximate (K+1)-th best are
+// recomputed exactly before the decision when the logits came from the
+// tensor-core GEMM (its fp32 accumulation order differs from a plain dot
+// product by up to a few 1e-6 in score; the margin is 20x that).
+constexpr float kRefineMargin = 1e-4f;
+
+// One warp per token. The K (+1) best are found by K+1 rounds of a warp
+// arg-max over the selection scores (equal scores: lower index first).
+__device__ __forceinline__ void select_rounds(float *sel, const float *score, int E, int K, float (&chosen_s)[kMaxTopK],
+                                              int (&chosen_e)[kMaxTopK], float &kth, float &next, int lane) {
+    kth = 0.f;
+    next = -INFINITY;
     const int rounds = K < E ? K + 1 : K;
     for (int r = 0; r < rounds; r++) {
         float bv = -INFINITY;
@@ -140,6 +130,66 @@ __global__ void router_select_kernel(const float *__restrict__ logits, const flo
             next = bv;
         }
     }
+}
+
+// x_refine/wr/H: when x_refine is given, the logits are approximate and every
+// expert whose selection score is within kRefineMargin of the (K+1)-th best
+// gets its logit recomputed as an fp32 dot product of x (bf16) and its router
+// row before the final decision.
+__global__ void router_select_kernel(const float *__restrict__ logits, const float *__restrict__ bias, int T,
+                                     int E, int K, int32_t *__restrict__ idx, float *__restrict__ w,
+                                     float *__restrict__ gap, float *__restrict__ sel_out,
+                                     const uint16_t *__restrict__ x_refine, const float *__restrict__ wr, int H) {
+    extern __shared__ float smem[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int t = blockIdx.x * kSelectWarps + warp;
+    if (t >= T)
+        return;
+    float *sel = smem + warp * 2 * E;
+    float *score = sel + E;
+    for (int e = lane; e < E; e += 32) {
+        float s = sigmoid(logits[(int64_t)t * E + e]);
+        score[e] = s;
+        sel[e] = bias ? s + bias[e] : s;
+    }
+    __syncwarp();
+    float chosen_s[kMaxTopK];
+    int chosen_e[kMaxTopK];
+    float kth, next;
+    if (x_refine) {
+        select_rounds(sel, score, E, K, chosen_s, chosen_e, kth, next, lane);
+        const float thr = (K < E ? next : kth) - kRefineMargin;
+        for (int e = lane; e < E; e += 32) // restore the scores the rounds consumed
+            sel[e] = bias ? score[e] + bias[e] : score[e];
+        __syncwarp();
+        const uint2 *xr = reinterpret_cast<const uint2 *>(x_refine + (int64_t)t * H);
+        for (int e = 0; e < E; e++) {
+            if (!(sel[e] >= thr)) // warp-uniform: every lane reads the same score
+                continue;
+            const float4 *row = reinterpret_cast<const float4 *>(wr + (int64_t)e * H);
+            float acc = 0.f;
+            for (int c = lane; c < H / 4; c += 32) {
+                const float4 v = __ldg(row + c);
+                const uint2 xb = __ldg(xr + c);
+                acc = fmaf(__uint_as_float(xb.x << 16), v.x, acc);
+                acc = fmaf(__uint_as_float(xb.x & 0xFFFF0000u), v.y, acc);
+                acc = fmaf(__uint_as_float(xb.y << 16), v.z, acc);
+                acc = fmaf(__uint_as_float(xb.y & 0xFFFF0000u), v.w, acc);
+            }
+            acc = warp_sum(acc);
+            if (lane == 0) {
+                const float s = sigmoid(acc);
+                score[e] = s;
+                sel[e] = bias ? s + bias[e] : s;
+            }
+            __syncwarp();
+        }
+    }
+    if (sel_out)
+        for (int e = lane; e < E; e += 32)
+            sel_out[(int64_t)t * E + e] = sel[e];
+    __syncwarp();
+    select_rounds(sel, score, E, K, chosen_s, chosen_e, kth, next, lane);
     if (lane == 0) {
         float total = 0.f;
         for (int k = 0; k < K; k++)
