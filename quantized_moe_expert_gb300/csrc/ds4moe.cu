@@ -476,8 +476,8 @@ int run_router(ds4moe *h, const void *x, int T, float *sel_out) {
         });
     }
     launch(h, "router_select", [&] {
-        const size_t smem = (size_t)kSelectWarps * 2 * L.E * sizeof(float);
-        router_select_kernel<<<blocks_for(T, kSelectWarps), 32 * kSelectWarps, smem, st>>>(
+        const size_t smem = (size_t)3 * L.E * sizeof(float);
+        router_select_kernel<<<T, kSelectThreads, smem, st>>>(
             S.logits, L.router_bias, T, L.E, L.K, S.idx, S.w, S.gap, sel_out,
             T >= kRouterGemmMinT ? static_cast<const uint16_t *>(x) : nullptr, L.router_w, L.H);
     });
@@ -1116,8 +1116,8 @@ extern "C" int ds4moe_route_noalloc(const float *router_w, const float *router_b
                                                                          H, x32, xsum);
     router_logits_kernel<<<dim3(blocks_for(E, 8), blocks_for(T, kRouterTok)), 256, 0, st>>>(x32, T, H, router_w, E,
                                                                                           logits);
-    const size_t smem = (size_t)kSelectWarps * 2 * E * sizeof(float);
-    router_select_kernel<<<blocks_for(T, kSelectWarps), 32 * kSelectWarps, smem, st>>>(
+    const size_t smem = (size_t)3 * E * sizeof(float);
+    router_select_kernel<<<T, kSelectThreads, smem, st>>>(
         logits, router_bias, T, E, K, idx_out, w_out, nullptr, nullptr, nullptr, nullptr, 0);
     return launch_rc();
 }

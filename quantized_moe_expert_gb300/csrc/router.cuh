@@ -82,16 +82,15 @@ __global__ void router_logits_kernel(const float *__restrict__ x32, int T, int H
 // One warp per token: selection scores into shared memory, then K+1 rounds of
 // a warp-wide arg-max ordered by (score desc, index asc). Round K+1 only
 // yields the runner-up score for the near-tie gap.
-constexpr int kSelectWarps = 4;
-
 // Selection scores within this distance of the approximate (K+1)-th best are
 // recomputed exactly before the decision when the logits came from the
-// tensor-core GEMM (its fp32 accumulation order differs from a plain dot
-// product by up to a few 1e-6 in score; the margin is 20x that).
-constexpr float kRefineMargin = 1e-4f;
+// tensor-core GEMM (its fp32 accumulation order leaves scores up to ~5e-6 off
+// a plain dot product; the margin is 4x that).
+constexpr float kRefineMargin = 2e-5f;
+constexpr int kSelectThreads = 128; // one block per token
 
-// One warp per token. The K (+1) best are found by K+1 rounds of a warp
-// arg-max over the selection scores (equal scores: lower index first).
+// Warp-wide: the K (+1) best selection scores by K+1 rounds of a warp arg-max
+// (equal scores: lower index first). Consumes sel (chosen entries set to -inf).
 __device__ __forceinline__ void select_rounds(float *sel, const float *score, int E, int K, float (&chosen_s)[kMaxTopK],
                                               int (&chosen_e)[kMaxTopK], float &kth, float &next, int lane) {
     kth = 0.f;
@@ -132,45 +131,61 @@ __device__ __forceinline__ void select_rounds(float *sel, const float *score, in
     }
 }
 
-// x_refine/wr/H: when x_refine is given, the logits are approximate and every
-// expert whose selection score is within kRefineMargin of the (K+1)-th best
-// gets its logit recomputed as an fp32 dot product of x (bf16) and its router
-// row before the final decision.
+// One block of kSelectThreads per token. x_refine/wr/H: when x_refine is
+// given, the logits are approximate and every expert whose selection score is
+// within kRefineMargin of the (K+1)-th best gets its logit recomputed as an
+// fp32 dot product of x (bf16) and its router row (the block's warps share
+// the candidates) before the final decision.
+// Shared memory: 2 * E floats + E ints.
 __global__ void router_select_kernel(const float *__restrict__ logits, const float *__restrict__ bias, int T,
                                      int E, int K, int32_t *__restrict__ idx, float *__restrict__ w,
                                      float *__restrict__ gap, float *__restrict__ sel_out,
                                      const uint16_t *__restrict__ x_refine, const float *__restrict__ wr, int H) {
     extern __shared__ float smem[];
+    __shared__ int ncand;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int t = blockIdx.x * kSelectWarps + warp;
+    const int t = blockIdx.x;
     if (t >= T)
         return;
-    float *sel = smem + warp * 2 * E;
+    float *sel = smem;
     float *score = sel + E;
-    for (int e = lane; e < E; e += 32) {
+    int *cand = reinterpret_cast<int *>(score + E);
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
         float s = sigmoid(logits[(int64_t)t * E + e]);
         score[e] = s;
         sel[e] = bias ? s + bias[e] : s;
     }
-    __syncwarp();
+    __syncthreads();
     float chosen_s[kMaxTopK];
     int chosen_e[kMaxTopK];
     float kth, next;
     if (x_refine) {
-        select_rounds(sel, score, E, K, chosen_s, chosen_e, kth, next, lane);
-        const float thr = (K < E ? next : kth) - kRefineMargin;
-        for (int e = lane; e < E; e += 32) // restore the scores the rounds consumed
-            sel[e] = bias ? score[e] + bias[e] : score[e];
-        __syncwarp();
+        if (warp == 0) {
+            select_rounds(sel, score, E, K, chosen_s, chosen_e, kth, next, lane);
+            const float thr = (K < E ? next : kth) - kRefineMargin;
+            int n = 0;
+            for (int e0 = 0; e0 < E; e0 += 32) {
+                const int e = e0 + lane;
+                const float v = e < E ? (bias ? score[e] + bias[e] : score[e]) : -INFINITY;
+                if (e < E)
+                    sel[e] = v; // restore what the rounds consumed
+                const unsigned m = __ballot_sync(0xFFFFFFFFu, v >= thr);
+                if (v >= thr)
+                    cand[n + __popc(m & ((1u << lane) - 1u))] = e;
+                n += __popc(m);
+            }
+            if (lane == 0)
+                ncand = n;
+        }
+        __syncthreads();
         const uint2 *xr = reinterpret_cast<const uint2 *>(x_refine + (int64_t)t * H);
-        for (int e = 0; e < E; e++) {
-            if (!(sel[e] >= thr)) // warp-uniform: every lane reads the same score
-                continue;
+        for (int c = warp; c < ncand; c += kSelectThreads / 32) {
+            const int e = cand[c];
             const float4 *row = reinterpret_cast<const float4 *>(wr + (int64_t)e * H);
             float acc = 0.f;
-            for (int c = lane; c < H / 4; c += 32) {
-                const float4 v = __ldg(row + c);
-                const uint2 xb = __ldg(xr + c);
+            for (int q = lane; q < H / 4; q += 32) {
+                const float4 v = __ldg(row + q);
+                const uint2 xb = __ldg(xr + q);
                 acc = fmaf(__uint_as_float(xb.x << 16), v.x, acc);
                 acc = fmaf(__uint_as_float(xb.x & 0xFFFF0000u), v.y, acc);
                 acc = fmaf(__uint_as_float(xb.y << 16), v.z, acc);
@@ -182,13 +197,15 @@ __global__ void router_select_kernel(const float *__restrict__ logits, const flo
                 score[e] = s;
                 sel[e] = bias ? s + bias[e] : s;
             }
-            __syncwarp();
         }
+        __syncthreads();
     }
     if (sel_out)
-        for (int e = lane; e < E; e += 32)
+        for (int e = threadIdx.x; e < E; e += blockDim.x)
             sel_out[(int64_t)t * E + e] = sel[e];
-    __syncwarp();
+    __syncthreads();
+    if (warp != 0)
+        return;
     select_rounds(sel, score, E, K, chosen_s, chosen_e, kth, next, lane);
     if (lane == 0) {
         float total = 0.f;
