@@ -93,6 +93,10 @@ struct DecodeArgs {
     float *ysh;              // [8][H]
     unsigned *ctl;
     unsigned *status;
+    // Phased launches: the job range [jlo, jhi) of this launch, in the phased
+    // job order. Every dependency of a job then lies in an earlier launch, so
+    // no in-kernel wait is needed and the launch need not be cooperative.
+    int phased, jlo, jhi;
 };
 
 enum JobType : int { kJobEnd = 0, kJobR, kJobSgu, kJobSel, kJobGu, kJobSd, kJobD };
@@ -834,21 +838,34 @@ struct JobSpace {
     int oSGU, oSEL, oGU, oSD, oD, total;
 };
 
-__device__ __forceinline__ JobSpace job_space(const DecodeArgs &a) {
+// Fused order: R, SEL, SGU, GU, SD, D (the selection right after the router
+// rows: it is on the critical path). Phased order: R, SGU | SEL | GU, SD | D,
+// four launches, each a contiguous range.
+__host__ __device__ __forceinline__ JobSpace job_space(int E, int I, int H, int Ish, int T, int K, bool forced,
+                                                       bool phased) {
     JobSpace s;
-    s.nR = a.forced_idx ? 0 : a.E; // one router row per job
-    s.nSGU = a.Ish > 0 ? a.Ish / 16 : 0;
-    s.tilesI = a.I / 16;
-    s.tilesH = a.H / 16;
-    s.Umax = min(a.E, a.T * a.K);
-    // the selection comes right after the router rows: it is on the critical path
-    s.oSEL = s.nR;
-    s.oSGU = s.oSEL + 1;
-    s.oGU = s.oSGU + s.nSGU;
+    s.nR = forced ? 0 : E; // one router row per job
+    s.nSGU = Ish > 0 ? Ish / 16 : 0;
+    s.tilesI = I / 16;
+    s.tilesH = H / 16;
+    s.Umax = (T * K < E) ? T * K : E;
+    if (phased) {
+        s.oSGU = s.nR;
+        s.oSEL = s.oSGU + s.nSGU;
+        s.oGU = s.oSEL + 1;
+    } else {
+        s.oSEL = s.nR;
+        s.oSGU = s.oSEL + 1;
+        s.oGU = s.oSGU + s.nSGU;
+    }
     s.oSD = s.oGU + s.Umax * s.tilesI;
-    s.oD = s.oSD + (a.Ish > 0 ? s.tilesH : 0);
+    s.oD = s.oSD + (Ish > 0 ? s.tilesH : 0);
     s.total = s.oD + s.Umax * s.tilesH;
     return s;
+}
+
+__device__ __forceinline__ JobSpace job_space(const DecodeArgs &a) {
+    return job_space(a.E, a.I, a.H, a.Ish, a.T, a.K, a.forced_idx != nullptr, a.phased != 0);
 }
 
 __device__ __forceinline__ int pad_tp(int n) { return n <= 1 ? 1 : (n <= 2 ? 2 : (n <= 4 ? 4 : 8)); }
@@ -917,7 +934,7 @@ struct StageWriter {
         for (int i = 0; i < split; i++)
             bulk_g2s(sm.ring[slot] + dst[i], src[i], bytes[i], bar);
         if (split < np) {
-            if (!wait_counter(a, dep, target, false))
+            if (dep && !wait_counter(a, dep, target, false))
                 return false;
             // the data was written through the generic proxy by other CTAs; the
             // bulk copies read it through the async proxy
@@ -940,11 +957,12 @@ __device__ void producer(const DecodeArgs &a, DecodeSmem &sm, const JobSpace &js
     };
     bool ok = true;
     while (ok) {
-        const int j = ld_relaxed(a.ctl + kCtlAbort) ? js.total : (int)atomicAdd(a.ctl + kCtlJobNext, 1u);
-        if (j >= js.total)
+        const int j =
+            ld_relaxed(a.ctl + kCtlAbort) ? js.total : a.jlo + (int)atomicAdd(a.ctl + kCtlJobNext, 1u);
+        if (j >= a.jhi)
             break;
         if (j >= js.oGU && !routed) {
-            if (!wait_counter(a, a.ctl + kCtlRoutingEpoch, a.epoch, true))
+            if (!a.phased && !wait_counter(a, a.ctl + kCtlRoutingEpoch, a.epoch, true))
                 break;
             asm volatile("fence.proxy.async.global;" ::: "memory");
             routed = true;
@@ -954,11 +972,11 @@ __device__ void producer(const DecodeArgs &a, DecodeSmem &sm, const JobSpace &js
         int pos[kDecodeT], tok[kDecodeT];
         for (int i = 0; i < kDecodeT; i++)
             pos[i] = tok[i] = i < a.T ? i : 0;
-        if (j < js.oSEL) {
+        if (j < js.nR) {
             type = kJobR;
             a0 = j;
             per16 = 16 * (4 + 2 * a.T);
-        } else if (j < js.oSGU) {
+        } else if (j == js.oSEL) {
             type = kJobSel;
         } else if (j < js.oGU) {
             type = kJobSgu;
@@ -1092,7 +1110,8 @@ __device__ void producer(const DecodeArgs &a, DecodeSmem &sm, const JobSpace &js
                         sw.put(a.hsum + (int64_t)pos[t] * (K / 16) + c0 / 16, (unsigned)W / 4u);
                 }
             }
-            const unsigned *dep = type == kJobD ? a.ctl + kCtlGuDone + a0 : a.ctl + kCtlSguDone;
+            const unsigned *dep =
+                a.phased ? nullptr : (type == kJobD ? a.ctl + kCtlGuDone + a0 : a.ctl + kCtlSguDone);
             const unsigned target = type == kJobD ? (unsigned)js.tilesI : (unsigned)js.nSGU;
             n++;
             if (!sw.issue(a, dep, target)) {
@@ -1295,7 +1314,7 @@ __device__ void consumer(const DecodeArgs &a, DecodeSmem &sm, const JobSpace &js
                 (&out[0][0][0])[i] = 0.f;
             const unsigned *dep = nullptr;
             unsigned target = 0;
-            if (type == kJobSel) {
+            if (type == kJobSel && !a.phased) {
                 dep = a.ctl + kCtlRouterDone;
                 target = (unsigned)js.nR;
             }
@@ -1303,8 +1322,10 @@ __device__ void consumer(const DecodeArgs &a, DecodeSmem &sm, const JobSpace &js
                 if (threadIdx.x < kDecodeT * kMaxTopK)
                     (&sm.sel_idx[0][0])[threadIdx.x] = 0;
                 consumer_sync();
-                job_select(a, sm, warp, lane, true);
-                consumer_sync();
+                if (!a.phased) { // warm the selection's code while the router rows finish
+                    job_select(a, sm, warp, lane, true);
+                    consumer_sync();
+                }
             }
             if (dep && alive) {
                 if (threadIdx.x == 0)

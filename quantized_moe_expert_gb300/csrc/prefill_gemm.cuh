@@ -94,8 +94,12 @@ struct Args {
     unsigned *status;
 };
 
+#ifndef DS4_PF_PROD_WARPS
+#define DS4_PF_PROD_WARPS 8
+#endif
+
 template <int FMT, int NA> struct Cfg {
-    static constexpr int kProdWarps = 8;
+    static constexpr int kProdWarps = DS4_PF_PROD_WARPS; // 8 or 16
     static constexpr int kProdThreads = 32 * kProdWarps;
     static constexpr int kLoadWarp = kProdWarps;           // one loader warp
     static constexpr int kMmaWarp = kProdWarps + 1;        // two issuer warps
@@ -290,10 +294,12 @@ template <int P> __device__ __forceinline__ void read_raw(uint32_t slot, int r, 
         x.sc[1] = v.y;
         x.sc[P / 16 - 2] = v.z;
         x.sc[P / 16 - 1] = v.w;
-    } else {
+    } else if (P == 32) {
         const uint2 v = lds64(slot + 8192 + r * 16 + (part / 2) * 8);
         x.sc[0] = v.x;
         x.sc[P / 16 - 1] = v.y;
+    } else {
+        x.sc[0] = lds32(slot + 8192 + r * 16 + part * 4);
     }
     x.dm = lds32(slot + 10240 + r * 4);
 }
