@@ -480,7 +480,6 @@ __global__ void __launch_bounds__(Cfg<FMT, NA>::kThreads, 1)
     constexpr int kSPB = C::kSPB;
     constexpr int kStages = C::kStages;
     constexpr int kRaw = C::kRaw;
-    constexpr int kProdThreads = C::kProdThreads;
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -497,16 +496,16 @@ __global__ void __launch_bounds__(Cfg<FMT, NA>::kThreads, 1)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (tid == 0) {
         for (int s = 0; s < kStages; s++) {
-            mbar_init(full + s, kProdThreads + 1); // producers + the loader's expect_tx
+            mbar_init(full + s, C::kProdWarps + 1); // one arrival per producer warp + the loader's expect_tx
             mbar_init(empty + s, NA == 2 ? 2 : 1);
         }
         for (int s = 0; s < kRaw; s++) {
             mbar_init(rfull + s, 1);
-            mbar_init(rempty + s, kProdThreads);
+            mbar_init(rempty + s, C::kProdWarps);
         }
         for (int b = 0; b < 2; b++) {
             mbar_init(accf + b, 2);
-            mbar_init(acce + b, 128);
+            mbar_init(acce + b, 4);
         }
         mbar_init(fin, 2);
         *abort = 0u;
@@ -544,7 +543,9 @@ __global__ void __launch_bounds__(Cfg<FMT, NA>::kThreads, 1)
                 break;
             Raw cur;
             read_raw(raw_base + (rs * NA + mat) * C::kRawMat, row, part, cur);
-            mbar_arrive(rempty + rs);
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(rempty + rs);
             bool ok = true;
 #pragma unroll
             for (int s = 0; s < kSPB; s++) {
@@ -568,7 +569,9 @@ __global__ void __launch_bounds__(Cfg<FMT, NA>::kThreads, 1)
                 }
                 tmem_st_wait();
                 umma::fence_before_sync();
-                mbar_arrive(full + slot);
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(full + slot);
             }
             if (!ok)
                 break;
@@ -760,10 +763,13 @@ __global__ void __launch_bounds__(Cfg<FMT, NA>::kThreads, 1)
                 }
             }
             umma::fence_before_sync();
-            mbar_arrive(acce + s0);
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(acce + s0);
             use ^= 1u << s0;
             if (wide) {
-                mbar_arrive(acce + 1);
+                if (lane == 0)
+                    mbar_arrive(acce + 1);
                 use ^= 2u;
             } else {
                 next1 ^= 1;
