@@ -298,6 +298,10 @@ void layout_weights(ds4moe *h, Carver &c) {
     }
 }
 
+// Logits rows reserved for the router GEMM's K-split partials: tiles * split <=
+// grid <= 256 CTAs of 128 rows.
+constexpr int64_t kLogitRowsSplit = 256 * 128;
+
 void layout_scratch(ds4moe *h, Carver &c) {
     const LayerDev &L = h->L;
     Scratch &S = h->S;
@@ -305,7 +309,8 @@ void layout_scratch(ds4moe *h, Carver &c) {
     const int64_t U = P < L.E ? P : L.E;
     S.x32 = c.take<float>(T * L.H);
     S.xsum = c.take<float>(T * (L.H / 16));
-    S.logits = c.take<float>(T * L.E);
+    // the router GEMM may write up to (SM count * 128 / m-tiles) rows of K-split partial logits
+    S.logits = c.take<float>((T > kLogitRowsSplit ? T : kLogitRowsSplit) * L.E);
     S.idx = c.take<int32_t>(P);
     S.w = c.take<float>(P);
     S.gap = c.take<float>(T);
@@ -452,6 +457,7 @@ int run_router(ds4moe *h, const void *x, int T, float *sel_out) {
     const LayerDev &L = h->L;
     Scratch &S = h->S;
     cudaStream_t st = h->stream;
+    int nsplit = 1;
     if (T >= kRouterGemmMinT) {
         int rc = x_maps(h, x, T);
         if (rc)
@@ -465,6 +471,18 @@ int run_router(ds4moe *h, const void *x, int T, float *sel_out) {
         a.b_kwrap = L.H;
         a.out = S.logits;
         a.ldo = L.E;
+        // split K so that the tiles fill the GPU: the largest divisor of the K steps
+        // with tiles * split <= grid and at least 4 K steps per partial tile
+        const int tiles = ((L.E + 127) / 128) * ((T + 127) / 128);
+        const int nk = 3 * L.H / 64;
+        int split = 1;
+        for (int d = 1; d <= nk; d++)
+            if (nk % d == 0 && nk / d >= 4 && (int64_t)tiles * d <= g_pf_grid &&
+                (int64_t)d * T <= (T > kLogitRowsSplit ? T : kLogitRowsSplit))
+                split = d;
+        a.ksplit = split;
+        a.out_kstride = (int64_t)T * L.E;
+        nsplit = split;
         launch_gemm<pf::kFmtBF16, 1, pf::kEpiF32>(h, "router_logits_tc", h->map_x, a);
     } else {
         int rc = run_prep(h, x, T);
@@ -479,7 +497,8 @@ int run_router(ds4moe *h, const void *x, int T, float *sel_out) {
         const size_t smem = (size_t)3 * L.E * sizeof(float);
         router_select_kernel<<<T, kSelectThreads, smem, st>>>(
             S.logits, L.router_bias, T, L.E, L.K, S.idx, S.w, S.gap, sel_out,
-            T >= kRouterGemmMinT ? static_cast<const uint16_t *>(x) : nullptr, L.router_w, L.H);
+            T >= kRouterGemmMinT ? static_cast<const uint16_t *>(x) : nullptr, L.router_w, L.H, nsplit,
+            (int64_t)T * L.E);
     });
     return launch_rc();
 }
@@ -1150,6 +1169,6 @@ extern "C" int ds4moe_route_noalloc(const float *router_w, const float *router_b
                                                                                           logits);
     const size_t smem = (size_t)3 * E * sizeof(float);
     router_select_kernel<<<T, kSelectThreads, smem, st>>>(
-        logits, router_bias, T, E, K, idx_out, w_out, nullptr, nullptr, nullptr, nullptr, 0);
+        logits, router_bias, T, E, K, idx_out, w_out, nullptr, nullptr, nullptr, nullptr, 0, 1, 0);
     return launch_rc();
 }

@@ -91,6 +91,8 @@ struct Args {
     int b_kwrap;           // > 0: B column of reduction index k is k % b_kwrap
     void *out;             // bf16 (SwiGLU) or fp32 rows [group row][ldo]
     int ldo;
+    int ksplit;            // > 1: each tile is split over K into ksplit partial tiles (fp32 output
+    int64_t out_kstride;   // only), partial s written at out + s * out_kstride
     unsigned *status;
 };
 
@@ -519,9 +521,10 @@ __global__ void __launch_bounds__(Cfg<FMT, NA>::kThreads, 1)
     const uint32_t tmem = *tmem_slot;
 
     const int MT = (a.M + kTileM - 1) / kTileM; // a partial last m-tile only for plain bf16 rows
-    const int nk = a.Kd / kTileK;
+    const int ksplit = a.ksplit > 1 ? a.ksplit : 1;
+    const int nk = a.Kd / kTileK / ksplit; // K steps of one (partial) tile
     const int nblk = nk / kSPB;
-    const int ntiles = num_groups(a, kNMax) * MT;
+    const int ntiles = num_groups(a, kNMax) * MT * ksplit; // tile t: (group, m-tile) t / ksplit, K part t % ksplit
     const int my_tiles = (int)blockIdx.x < ntiles ? (ntiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
     const int nsteps = my_tiles * nk;
     const uint32_t smem_base = umma::smem_addr(smem);
@@ -583,12 +586,14 @@ __global__ void __launch_bounds__(Cfg<FMT, NA>::kThreads, 1)
         if (lane == 0) {
             const int nblocks = my_tiles * nblk;
             // raw cursor: global block rb = (tile ordinal r_tl, block r_kb)
-            int r_tl = 0, r_kb = 0;
+            int r_tl = 0, r_kb = 0, r_kb0 = 0;
             int64_t r_rt = 0;
             auto raw_tile = [&]() {
                 const int t = (int)blockIdx.x + r_tl * (int)gridDim.x;
-                const int4 g = group_at(a, t / MT, kNMax);
-                r_rt = (int64_t)g.x * (a.M / kTileM) + t % MT;
+                const int tg = t / ksplit;
+                const int4 g = group_at(a, tg / MT, kNMax);
+                r_rt = (int64_t)g.x * (a.M / kTileM) + tg % MT;
+                r_kb0 = (t % ksplit) * nblk;
             };
             auto issue_raw = [&](int rb) -> bool {
                 const int rs = rb % kRaw;
@@ -597,7 +602,8 @@ __global__ void __launch_bounds__(Cfg<FMT, NA>::kThreads, 1)
                 mbar_arrive_tx(rfull + rs, NA * C::kRawMat);
 #pragma unroll
                 for (int m = 0; m < NA; m++)
-                    copy_raw(MatOf<FMT>::get(a, m), r_rt, r_kb, raw_base + (rs * NA + m) * C::kRawMat, rfull + rs);
+                    copy_raw(MatOf<FMT>::get(a, m), r_rt, r_kb0 + r_kb, raw_base + (rs * NA + m) * C::kRawMat,
+                             rfull + rs);
                 if (++r_kb == nblk) {
                     r_kb = 0;
                     if (++r_tl < my_tiles)
@@ -614,11 +620,13 @@ __global__ void __launch_bounds__(Cfg<FMT, NA>::kThreads, 1)
             int j = 0, gb = 0;
             for (int tl = 0; tl < my_tiles && ok; tl++) {
                 const int t = (int)blockIdx.x + tl * (int)gridDim.x;
-                const int4 g = group_at(a, t / MT, kNMax);
+                const int4 g = group_at(a, t / ksplit / MT, kNMax);
                 const int n_mma = max(16, (g.z + 15) & ~15);
                 const int box = n_mma <= 16 ? 0 : (n_mma <= 32 ? 1 : (n_mma <= 64 ? 2 : 3));
                 const unsigned bbytes = (16u << box) * kTileK * 2;
-                int col = 0;
+                int col = (t % ksplit) * nk * kTileK;
+                if (a.b_kwrap > 0)
+                    col %= a.b_kwrap;
                 for (int kb = 0; kb < nblk && ok; kb++, gb++) {
                     for (int s = 0; s < kSPB; s++, j++) {
                         const int slot = j % kStages;
@@ -652,7 +660,7 @@ __global__ void __launch_bounds__(Cfg<FMT, NA>::kThreads, 1)
             bool ok = true;
             const uint64_t bdesc0 = umma::desc_sw128(smem_base);
             for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
-                const int4 g = group_at(a, t / MT, kNMax);
+                const int4 g = group_at(a, t / ksplit / MT, kNMax);
                 const int n_mma = max(16, (g.z + 15) & ~15);
                 const AccPlace pl = acc_place(n_mma, next1);
                 const bool wide = pl.wide;
@@ -714,7 +722,7 @@ __global__ void __launch_bounds__(Cfg<FMT, NA>::kThreads, 1)
         unsigned use = 0u;
         int next1 = 0;
         for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
-            const int4 g = group_at(a, t / MT, kNMax);
+            const int4 g = group_at(a, t / ksplit / MT, kNMax);
             const int n_mma = max(16, (g.z + 15) & ~15);
             const AccPlace pl = acc_place(n_mma, next1);
             const bool wide = pl.wide;
@@ -724,7 +732,7 @@ __global__ void __launch_bounds__(Cfg<FMT, NA>::kThreads, 1)
             if (wide && !mbar_wait(accf + 1, (use >> 1) & 1u, abort, a.status))
                 break;
             umma::fence_after_sync();
-            const int mrow = (t % MT) * kTileM + 32 * q + lane;
+            const int mrow = (t / ksplit % MT) * kTileM + 32 * q + lane;
             const uint32_t tbase = tmem + ((uint32_t)(32 * q) << 16) + pl.col;
             for (int c0 = 0; c0 < g.z; c0 += 8) {
                 // NA == 2: v[0] gate, v[1] up; NA == 1: the two partial sums, added
@@ -755,7 +763,7 @@ __global__ void __launch_bounds__(Cfg<FMT, NA>::kThreads, 1)
                         }
                     }
                 } else {
-                    float *out = static_cast<float *>(a.out);
+                    float *out = static_cast<float *>(a.out) + (int64_t)(t % ksplit) * a.out_kstride;
 #pragma unroll
                     for (int jj = 0; jj < 8; jj++)
                         if (c0 + jj < g.z)

@@ -131,7 +131,8 @@ __device__ __forceinline__ void select_rounds(float *sel, const float *score, in
     }
 }
 
-// One block of kSelectThreads per token. x_refine/wr/H: when x_refine is
+// One block of kSelectThreads per token; the logits are the sum of nsplit
+// partial arrays split_stride floats apart. x_refine/wr/H: when x_refine is
 // given, the logits are approximate and every expert whose selection score is
 // within kRefineMargin of the (K+1)-th best gets its logit recomputed as an
 // fp32 dot product of x (bf16) and its router row (the block's warps share
@@ -140,7 +141,8 @@ __device__ __forceinline__ void select_rounds(float *sel, const float *score, in
 __global__ void router_select_kernel(const float *__restrict__ logits, const float *__restrict__ bias, int T,
                                      int E, int K, int32_t *__restrict__ idx, float *__restrict__ w,
                                      float *__restrict__ gap, float *__restrict__ sel_out,
-                                     const uint16_t *__restrict__ x_refine, const float *__restrict__ wr, int H) {
+                                     const uint16_t *__restrict__ x_refine, const float *__restrict__ wr, int H,
+                                     int nsplit, int64_t split_stride) {
     extern __shared__ float smem[];
     __shared__ int ncand;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -151,7 +153,10 @@ __global__ void router_select_kernel(const float *__restrict__ logits, const flo
     float *score = sel + E;
     int *cand = reinterpret_cast<int *>(score + E);
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
-        float s = sigmoid(logits[(int64_t)t * E + e]);
+        float l = logits[(int64_t)t * E + e];
+        for (int q = 1; q < nsplit; q++) // partial logits of a K-split GEMM, added in order
+            l += logits[q * split_stride + (int64_t)t * E + e];
+        float s = sigmoid(l);
         score[e] = s;
         sel[e] = bias ? s + bias[e] : s;
     }
