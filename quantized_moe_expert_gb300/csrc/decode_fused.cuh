@@ -50,8 +50,8 @@ namespace ds4 {
 constexpr int kDecodeT = 8;             // tokens per launch
 constexpr int kMaxSlots = 64;           // distinct experts per launch <= 8 tokens * top-8
 constexpr uint64_t kWaitNs = 500000000; // 0.5 s
-constexpr int kRing = 3;                // shared-memory stages per CTA (two CTAs per SM)
-constexpr int kSlotBytes = 28672;       // bytes per stage
+constexpr int kRing = 2;                // shared-memory stages per CTA (two CTAs per SM)
+constexpr int kSlotBytes = 43008;       // bytes per stage (fewer, larger stages measured faster)
 constexpr int kConsumerWarps = 8;
 constexpr int kDecodeThreads = 32 * (kConsumerWarps + 1);
 
