@@ -239,6 +239,20 @@ __device__ bool wait_counter(const DecodeArgs &a, const unsigned *p, unsigned ta
 
 // ---- mbarrier, bulk copy and barrier helpers ------------------------------------
 
+// Order-preserving unsigned key of a float (larger float, larger key; -0 and
+// +0 share one key; NaN maps to 0, below every number) and its inverse for
+// non-NaN keys.
+__device__ __forceinline__ unsigned order_key(float v) {
+    const unsigned u = v == 0.f ? 0u : __float_as_uint(v);
+    if (v != v)
+        return 0u;
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ float order_key_value(unsigned k) {
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
@@ -622,27 +636,23 @@ __device__ __forceinline__ void select_token(const DecodeArgs &a, DecodeSmem &sm
     float chosen_s = 0.f, total = 0.f, kth = 0.f, next = -INFINITY;
     int chosen_e = 0;
     const int rounds = K < E ? K + 1 : K;
+    // score of the lane's candidate
+    float cs = 0.f;
+#pragma unroll
+    for (int i = 0; i < NV; i++)
+        if (i == ci)
+            cs = sco[i];
     for (int r = 0; r < rounds; r++) {
-        float bv = cv;
-        int be = ci < 0 ? 0x7FFFFFFF : lane + 32 * ci;
-        float bs = 0.f;
-#pragma unroll
-        for (int i = 0; i < NV; i++)
-            if (i == ci)
-                bs = sco[i];
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, o);
-            const int oe = __shfl_xor_sync(0xFFFFFFFFu, be, o);
-            const float os = __shfl_xor_sync(0xFFFFFFFFu, bs, o);
-            if (ov > bv || (ov == bv && oe < be)) {
-                bv = ov;
-                be = oe;
-                bs = os;
-            }
-        }
-        if (be >= E) // every remaining score was NaN: keep the index in range
+        // highest selection score by an order-preserving key (NaN lowest), then
+        // the lowest index among equals, by two warp reductions
+        const unsigned kl = ci >= 0 ? order_key(cv) : 0u;
+        const unsigned gk = __reduce_max_sync(0xFFFFFFFFu, kl);
+        const unsigned cand = (ci >= 0 && kl == gk) ? (unsigned)(lane + 32 * ci) : 0xFFFFFFFFu;
+        int be = (int)__reduce_min_sync(0xFFFFFFFFu, cand);
+        if (be >= E || be < 0) // every remaining score was NaN: keep the index in range
             be = 0;
+        const float bv = order_key_value(gk);
+        const float bs = __shfl_sync(0xFFFFFFFFu, cs, be & 31);
         if (r < K) {
             if (lane == r) {
                 chosen_e = be;
@@ -664,6 +674,11 @@ __device__ __forceinline__ void select_token(const DecodeArgs &a, DecodeSmem &sm
                         cv = sel[i];
                         ci = i;
                     }
+                cs = 0.f;
+#pragma unroll
+                for (int i = 0; i < NV; i++)
+                    if (i == ci)
+                        cs = sco[i];
             }
         } else {
             next = bv;
@@ -775,14 +790,23 @@ __device__ void job_select(const DecodeArgs &a, DecodeSmem &sm, int warp, int la
         int slot[2], rank[2];
 #pragma unroll
         for (int h = 0; h < 2; h++) {
-            const int p = lane + 32 * h, e = pe[h];
-            slot[h] = rank[h] = 0;
-            if (e >= 0) {
-                slot[h] = sm.word_prefix[e >> 5] + __popc(sm.bitmap[e >> 5] & ((1u << (e & 31)) - 1u));
-                for (int q = 0; q < p; q++)
-                    rank[h] += sm.sel_idx[q / K][q % K] == e;
-            }
+            const int e = pe[h];
+            slot[h] = e >= 0 ? sm.word_prefix[e >> 5] + __popc(sm.bitmap[e >> 5] & ((1u << (e & 31)) - 1u)) : 0;
         }
+        // rank of a pair among the earlier pairs of its expert: lanes holding the
+        // same expert in the same half, plus (second half) the first half's count
+        const unsigned lt = (1u << lane) - 1u;
+        const unsigned m0 = __match_any_sync(0xFFFFFFFFu, pe[0]);
+        const unsigned m1 = __match_any_sync(0xFFFFFFFFu, pe[1]);
+        rank[0] = __popc(m0 & lt);
+        if (lane < kMaxSlots / 2)
+            sm.slot_cnt[lane] = sm.slot_cnt[lane + 32] = 0;
+        __syncwarp();
+        if (pe[0] >= 0 && rank[0] == 0)
+            sm.slot_cnt[slot[0]] = __popc(m0);
+        __syncwarp();
+        rank[1] = pe[1] >= 0 ? sm.slot_cnt[slot[1]] + __popc(m1 & lt) : 0;
+        __syncwarp();
         // pairs per slot: the rank-0 pair of each expert counts its pairs
         if (lane < kMaxSlots / 2)
             sm.slot_cnt[lane] = sm.slot_cnt[lane + 32] = 0;
