@@ -53,6 +53,8 @@ constexpr uint64_t kWaitNs = 500000000; // 0.5 s
 constexpr int kRing = 2;                // shared-memory stages per CTA (two CTAs per SM)
 constexpr int kSlotBytes = 43008;       // bytes per stage (fewer, larger stages measured faster)
 constexpr int kConsumerWarps = 8;
+// the selection job's keys ([T][E]) and bias ([E]) fit its stage buffer (E <= 1024)
+static_assert(4 * (kDecodeT + 1) * 1024 <= kSlotBytes, "selection scratch");
 constexpr int kDecodeThreads = 32 * (kConsumerWarps + 1);
 
 // Control words (zeroed at create; every launch leaves them zeroed again).
@@ -601,137 +603,77 @@ __device__ __forceinline__ void router_stage(const uint8_t *sl, const StageDesc 
     }
 }
 
-// Top-k of one token by one warp. Lane l holds the scores of experts
-// l + 32 i, i < NV, in registers. Each lane keeps its own best candidate;
-// each round the warp takes the best of the 32 candidates (score desc, index
-// asc) and only the lane that lost its candidate looks for its next one.
-template <int NV>
-__device__ __forceinline__ void select_token(const DecodeArgs &a, DecodeSmem &sm, int t, int lane, bool warm) {
+// Selection key of a selection score: order_key with NaN moved from 0 to 1,
+// so that 0 can mark a taken expert (below everything, NaN included). Keys of
+// numbers are >= order_key(-inf) > 1.
+__device__ __forceinline__ unsigned sel_key(float v) { return v == v ? order_key(v) : 1u; }
+
+// Top-k of token t by one warp from the selection keys keys[e] (shared
+// memory, e < E). Lane l owns experts l, l + 32, ...; it keeps its best
+// (key desc, index asc) and each round the warp takes the best of the 32 by
+// two warp reductions; only the lane whose candidate was taken marks it and
+// rescans its experts. One round more than K gives the (K+1)-th score for the
+// near-tie gap.
+__device__ __forceinline__ void select_token(const DecodeArgs &a, DecodeSmem &sm, unsigned *keys, int t,
+                                             int lane) {
     const int E = a.E, K = a.K;
-    float sel[NV], sco[NV];
-    // unconditional (clamped) loads first, so that all NV loads are in flight together
-    float lg[NV], bi[NV];
-#pragma unroll
-    for (int i = 0; i < NV; i++) {
-        const int e = min(lane + 32 * i, E - 1);
-        lg[i] = __ldcg(a.logits + t * E + e);
-        bi[i] = a.router_bias ? __ldg(a.router_bias + e) : 0.f;
-    }
-#pragma unroll
-    for (int i = 0; i < NV; i++) {
-        const int e = lane + 32 * i;
-        const float s = sigmoid(lg[i]);
-        sco[i] = e < E ? s : 0.f;
-        sel[i] = e < E ? (a.router_bias ? s + bi[i] : s) : -INFINITY;
-    }
-    // the lane's best candidate: highest score, lowest index among equals
-    float cv = -INFINITY;
-    int ci = -1;
-#pragma unroll
-    for (int i = 0; i < NV; i++)
-        if (lane + 32 * i < E && (ci < 0 || sel[i] > cv)) {
-            cv = sel[i];
-            ci = i;
-        }
-    float chosen_s = 0.f, total = 0.f, kth = 0.f, next = -INFINITY;
-    int chosen_e = 0;
-    const int rounds = K < E ? K + 1 : K;
-    // score of the lane's candidate
-    float cs = 0.f;
-#pragma unroll
-    for (int i = 0; i < NV; i++)
-        if (i == ci)
-            cs = sco[i];
-    for (int r = 0; r < rounds; r++) {
-        // highest selection score by an order-preserving key (NaN lowest), then
-        // the lowest index among equals, by two warp reductions
-        const unsigned kl = ci >= 0 ? order_key(cv) : 0u;
-        const unsigned gk = __reduce_max_sync(0xFFFFFFFFu, kl);
-        const unsigned cand = (ci >= 0 && kl == gk) ? (unsigned)(lane + 32 * ci) : 0xFFFFFFFFu;
-        int be = (int)__reduce_min_sync(0xFFFFFFFFu, cand);
-        if (be >= E || be < 0) // every remaining score was NaN: keep the index in range
-            be = 0;
-        const float bv = order_key_value(gk);
-        const float bs = __shfl_sync(0xFFFFFFFFu, cs, be & 31);
-        if (r < K) {
-            if (lane == r) {
-                chosen_e = be;
-                chosen_s = bs;
+    unsigned best = 0u;
+    int bi = -1;
+    auto rescan = [&]() {
+        best = 0u;
+        bi = -1;
+        for (int e = lane; e < E; e += 32) {
+            const unsigned k = keys[e];
+            if (bi < 0 || k > best) {
+                best = k;
+                bi = e;
             }
-            total += bs;
+        }
+    };
+    rescan();
+    int chosen = 0;
+    float kth = 0.f, next = -INFINITY;
+    const int rounds = K < E ? K + 1 : K;
+    for (int r = 0; r < rounds; r++) {
+        const unsigned gk = __reduce_max_sync(0xFFFFFFFFu, best);
+        const unsigned cand = (bi >= 0 && best == gk) ? (unsigned)bi : 0xFFFFFFFFu;
+        const int be = (int)__reduce_min_sync(0xFFFFFFFFu, cand); // < E: every round has a candidate
+        const float bv = gk > 1u ? order_key_value(gk) : __uint_as_float(0x7FC00000u);
+        if (r < K) {
+            if (lane == r)
+                chosen = be;
             if (r == K - 1)
                 kth = bv;
-            if (ci >= 0 && lane + 32 * ci == be) { // this lane's candidate was taken
-#pragma unroll
-                for (int i = 0; i < NV; i++)
-                    if (i == ci)
-                        sel[i] = -INFINITY;
-                cv = -INFINITY;
-                ci = -1;
-#pragma unroll
-                for (int i = 0; i < NV; i++)
-                    if (lane + 32 * i < E && (ci < 0 || sel[i] > cv)) {
-                        cv = sel[i];
-                        ci = i;
-                    }
-                cs = 0.f;
-#pragma unroll
-                for (int i = 0; i < NV; i++)
-                    if (i == ci)
-                        cs = sco[i];
+            if (bi == be) { // this lane's candidate was taken
+                keys[be] = 0u;
+                rescan();
             }
         } else {
             next = bv;
         }
     }
+    // weights: the chosen experts' sigmoid scores (recomputed from the logits
+    // with the same function), renormalised in selection order
+    const float sc = lane < K ? sigmoid(__ldcg(a.logits + t * E + chosen)) : 0.f;
+    float total = 0.f;
+    for (int r = 0; r < K; r++)
+        total += __shfl_sync(0xFFFFFFFFu, sc, r);
     if (lane < K) {
-        sm.sel_idx[t][lane] = chosen_e;
-        if (!warm) {
-            a.idx[t * K + lane] = chosen_e;
-            a.w[t * K + lane] = total > 0.f ? chosen_s / total : 1.0f / K;
-        }
+        sm.sel_idx[t][lane] = chosen;
+        a.idx[t * K + lane] = chosen;
+        a.w[t * K + lane] = total > 0.f ? sc / total : 1.0f / K;
     }
-    if (lane == 0 && !warm)
+    if (lane == 0)
         a.gap[t] = K < E ? kth - next : INFINITY;
 }
 
-// Per-token selection (warp t handles token t); activation pre-scaling for the
-// 2-bit MMA (all consumer threads); then the grouping, computed in shared
-// memory and written out once. warm: a dry run on stale data that stores
-// nothing to global memory; it runs while the job waits for the router rows,
-// so the real run finds its instructions in the instruction cache.
-__device__ void job_select(const DecodeArgs &a, DecodeSmem &sm, int warp, int lane, bool warm) {
-    const int T = a.T, E = a.E, K = a.K, H = a.H;
-    if (warp < T) {
-        const int t = warp;
-        if (a.forced_idx) {
-            if (lane < K && !warm) {
-                int e = a.forced_idx[t * K + lane];
-                if (e < 0 || e >= E) {
-                    atomicOr(a.status, kErrIndex);
-                    e = e < 0 ? 0 : E - 1;
-                }
-                sm.sel_idx[t][lane] = e;
-                a.idx[t * K + lane] = e;
-                a.w[t * K + lane] = a.forced_w[t * K + lane];
-            }
-        } else if (E <= 32) {
-            select_token<1>(a, sm, t, lane, warm);
-        } else if (E <= 64) {
-            select_token<2>(a, sm, t, lane, warm);
-        } else if (E <= 128) {
-            select_token<4>(a, sm, t, lane, warm);
-        } else if (E <= 256) {
-            select_token<8>(a, sm, t, lane, warm);
-        } else if (E <= 384) {
-            select_token<12>(a, sm, t, lane, warm);
-        } else if (E <= 512) {
-            select_token<16>(a, sm, t, lane, warm);
-        } else {
-            select_token<32>(a, sm, t, lane, warm);
-        }
-    }
-    // activation pre-scaling: thread i takes sub-blocks i, i + 256, ... of all tokens
+// Work of the selection job that needs no router output (all consumer
+// threads, before the wait for the router rows): activation pre-scaling for
+// the 2-bit MMA, zeroed expert counts, and the router bias staged into the
+// job's stage buffer (bias at float offset kDecodeT * E of scratch).
+__device__ void select_prepare(const DecodeArgs &a, float *scratch) {
+    const int T = a.T, E = a.E, H = a.H;
+    // thread i takes sub-blocks i, i + 256, ... of all tokens
     const int nsub = H / 16;
     for (int q = threadIdx.x; q < T * nsub; q += 32 * kConsumerWarps) {
         const int t = q / nsub, j = q % nsub;
@@ -749,17 +691,66 @@ __device__ void job_select(const DecodeArgs &a, DecodeSmem &sm, int warp, int la
             ss += v0 + v1;
             outw[h2] = (f32_to_bf16_bits(s0) & 0xFFFFu) | (f32_to_bf16_bits(s1) << 16);
         }
-        if (!warm) {
-            uint4 *dst = reinterpret_cast<uint4 *>(a.xq + (int64_t)t * H + 16 * j);
-            dst[0] = make_uint4(outw[0], outw[1], outw[2], outw[3]);
-            dst[1] = make_uint4(outw[4], outw[5], outw[6], outw[7]);
-            a.xoff[t * nsub + j] = so;
-            a.xsum[t * nsub + j] = ss;
+        uint4 *dst = reinterpret_cast<uint4 *>(a.xq + (int64_t)t * H + 16 * j);
+        dst[0] = make_uint4(outw[0], outw[1], outw[2], outw[3]);
+        dst[1] = make_uint4(outw[4], outw[5], outw[6], outw[7]);
+        a.xoff[t * nsub + j] = so;
+        a.xsum[t * nsub + j] = ss;
+    }
+    for (int e = threadIdx.x; e < E; e += 32 * kConsumerWarps) {
+        a.counts[e] = 0;
+        if (!a.forced_idx)
+            scratch[kDecodeT * E + e] = a.router_bias ? __ldg(a.router_bias + e) : 0.f;
+    }
+}
+
+// Per-token selection after the router rows are complete: selection keys of
+// all (token, expert) pairs into the job's stage buffer (all consumer
+// threads), exact top-k (warp t takes token t), then the grouping, computed
+// in shared memory and written out once.
+__device__ void job_select(const DecodeArgs &a, DecodeSmem &sm, float *scratch, int warp, int lane) {
+    const int T = a.T, E = a.E, K = a.K;
+    unsigned *keys = reinterpret_cast<unsigned *>(scratch);
+    if (!a.forced_idx) {
+        const float *bias = scratch + kDecodeT * E;
+        const int n = T * E;
+        // four logits per thread in flight at a time
+        for (int q0 = threadIdx.x; q0 < n; q0 += 4 * 32 * kConsumerWarps) {
+            float lg[4];
+#pragma unroll
+            for (int u = 0; u < 4; u++) {
+                const int q = q0 + u * 32 * kConsumerWarps;
+                lg[u] = q < n ? __ldcg(a.logits + q) : 0.f;
+            }
+#pragma unroll
+            for (int u = 0; u < 4; u++) {
+                const int q = q0 + u * 32 * kConsumerWarps;
+                if (q < n) {
+                    const int e = q % E;
+                    const float sg = sigmoid(lg[u]);
+                    keys[q] = sel_key(a.router_bias ? sg + bias[e] : sg);
+                }
+            }
+        }
+        consumer_sync();
+    }
+    if (warp < T) {
+        const int t = warp;
+        if (a.forced_idx) {
+            if (lane < K) {
+                int e = a.forced_idx[t * K + lane];
+                if (e < 0 || e >= E) {
+                    atomicOr(a.status, kErrIndex);
+                    e = e < 0 ? 0 : E - 1;
+                }
+                sm.sel_idx[t][lane] = e;
+                a.idx[t * K + lane] = e;
+                a.w[t * K + lane] = a.forced_w[t * K + lane];
+            }
+        } else {
+            select_token(a, sm, keys + t * E, t, lane);
         }
     }
-    if (!warm)
-        for (int e = threadIdx.x; e < E; e += 32 * kConsumerWarps)
-            a.counts[e] = 0;
     if (threadIdx.x < 32)
         sm.bitmap[threadIdx.x] = 0;
     consumer_sync();
@@ -830,8 +821,6 @@ __device__ void job_select(const DecodeArgs &a, DecodeSmem &sm, int warp, int la
         sm.slot_cnt[2 * lane] = base;
         sm.slot_cnt[2 * lane + 1] = base + c0;
         __syncwarp();
-        if (warm)
-            return;
         if (2 * lane < nu)
             a.uoff[2 * lane] = base;
         if (2 * lane + 1 < nu)
@@ -1345,11 +1334,8 @@ __device__ void consumer(const DecodeArgs &a, DecodeSmem &sm, const JobSpace &js
             if (type == kJobSel && alive) {
                 if (threadIdx.x < kDecodeT * kMaxTopK)
                     (&sm.sel_idx[0][0])[threadIdx.x] = 0;
+                select_prepare(a, reinterpret_cast<float *>(sm.ring[slot]));
                 consumer_sync();
-                if (!a.phased) { // warm the selection's code while the router rows finish
-                    job_select(a, sm, warp, lane, true);
-                    consumer_sync();
-                }
             }
             if (dep && alive) {
                 if (threadIdx.x == 0)
@@ -1388,7 +1374,7 @@ __device__ void consumer(const DecodeArgs &a, DecodeSmem &sm, const JobSpace &js
                 consumer_sync();
                 signal(a, a.ctl + kCtlRouterDone);
             } else if (type == kJobSel) {
-                job_select(a, sm, warp, lane, false);
+                job_select(a, sm, reinterpret_cast<float *>(sm.ring[slot]), warp, lane);
                 consumer_sync();
                 if (threadIdx.x == 0) {
                     __threadfence();
