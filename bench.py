@@ -80,10 +80,6 @@ def kernel_bytes(name, shape, T, U):
         "combine": 4 * P * H + 4 * T * H + 4 * T * H,
         # one launch of the fused decode kernel does the whole layer for up to 8 tokens
         "decode_fused": layer_bytes(shape, T, U),
-        # phased decode launches
-        "decode_p1_router_shared": 4 * E * H + 2 * Ish * H * Q8_BPW + 2 * T * H,
-        "decode_p3_gateup": U * 2 * I * H * Q2_BPW + H * Ish * Q8_BPW,
-        "decode_p4_down": U * H * I * Q2_BPW + 4 * T * H,
     }
     return table.get(name)
 

@@ -5,26 +5,29 @@
 // weight tiles and activation rows into a ring of shared-memory stages with
 // bulk asynchronous copies (cp.async.bulk completing on an mbarrier); the
 // consumer warps multiply them on the tensor cores (mma.sync, see the layouts
-// in frag_layout.cuh) and release the stage. Stages hold up to 192 KB per SM
-// in flight, independent of registers, so the weight stream can run at the
-// HBM rate.
+// in frag_layout.cuh) and release the stage. Two CTAs per SM, each with two
+// 42 KB stages, keep up to 168 KB per SM in flight, independent of registers.
 //
 // Jobs are numbered so that each depends only on jobs with smaller numbers,
-// and a CTA takes its jobs in increasing order, so the oldest unfinished job
-// can always run: the queue cannot deadlock as long as all CTAs are resident,
+// and a CTA takes its jobs in increasing order (its first job is its own
+// index, the rest come from the queue), so the oldest unfinished job can
+// always run: the queue cannot deadlock as long as all CTAs are resident,
 // which the cooperative launch guarantees. The queue, in order:
 //
 //   R    one router row: fp32 logits for all T tokens
+//   SEL  one job: activation pre-scaling for the 2-bit MMA (before its wait);
+//        per-token sigmoid, exact top-k, weights; distinct-expert grouping;
+//        publishes the routing (waits for all R jobs)
 //   SGU  shared expert, one 16-row tile of gate and up: h_sh = silu(g) * u
-//   SEL  one job: per-token sigmoid, exact top-k, weights; activation
-//        pre-scaling for the 2-bit MMA; distinct-expert grouping; publishes
-//        the routing (waits for all R jobs)
+//   SD   shared expert down, one 16-row tile of H (waits: all SGU)
 //   GU   (distinct expert, 16-row tile of I): gate and up, h = silu(g) * u,
 //        stored as a bf16 hi/lo pair pre-scaled for the down MMA
-//   SD   shared expert down, one 16-row tile of H (waits: all SGU)
-//   D    (distinct expert, 16-row tile of H): down projection (waits: that
-//        expert's GU tiles); the last contribution to a tile combines it:
-//        y = sum_k w_k ye_k + ysh, in fixed order
+//   D    (distinct expert, 32-row tile of H): down projection (waits: that
+//        expert's GU tiles); the last of the experts' contributions to a tile
+//        combines it once all SD jobs are done: y = sum_k w_k ye_k + ysh, in
+//        fixed order
+// The shared expert's jobs sit between the selection and the routed jobs so
+// that they stream while the routing is computed and published.
 // The producer resolves the addresses of GU, SD and D jobs after the routing
 // is published; the weight loads of a job never wait for its data
 // dependencies, only its consumers do, so loads overlap those waits.
@@ -65,8 +68,9 @@ enum : int {
     kCtlSguDone = 3,
     kCtlFinished = 4,
     kCtlAbort = 5,
+    kCtlSdDone = 6,
     kCtlGuDone = 8,              // [kMaxSlots]
-    kCtlTileCnt = 8 + kMaxSlots, // [H / 16]
+    kCtlTileCnt = 8 + kMaxSlots, // [H / 32]
 };
 
 struct DecodeArgs {
@@ -95,10 +99,6 @@ struct DecodeArgs {
     float *ysh;              // [8][H]
     unsigned *ctl;
     unsigned *status;
-    // Phased launches: the job range [jlo, jhi) of this launch, in the phased
-    // job order. Every dependency of a job then lies in an earlier launch, so
-    // no in-kernel wait is needed and the launch need not be cooperative.
-    int phased, jlo, jhi;
 };
 
 enum JobType : int { kJobEnd = 0, kJobR, kJobSgu, kJobSel, kJobGu, kJobSd, kJobD };
@@ -847,38 +847,32 @@ __device__ void job_select(const DecodeArgs &a, DecodeSmem &sm, float *scratch, 
 // ---- job space ---------------------------------------------------------------------
 
 struct JobSpace {
-    int nR, nSGU, tilesI, tilesH, Umax;
-    int oSGU, oSEL, oGU, oSD, oD, total;
+    int nR, nSGU, nSD, tilesI, tilesD, Umax;
+    int oSEL, oSGU, oSD, oGU, oD, total;
 };
 
-// Fused order: R, SEL, SGU, GU, SD, D (the selection right after the router
-// rows: it is on the critical path). Phased order: R, SGU | SEL | GU, SD | D,
-// four launches, each a contiguous range.
-__host__ __device__ __forceinline__ JobSpace job_space(int E, int I, int H, int Ish, int T, int K, bool forced,
-                                                       bool phased) {
+// Job order: R, SEL, SGU, SD, GU, D. The selection comes right after the
+// router rows (it is on the critical path); the shared expert's jobs follow,
+// so that they fill the time in which the routing is computed and published.
+__host__ __device__ __forceinline__ JobSpace job_space(int E, int I, int H, int Ish, int T, int K, bool forced) {
     JobSpace s;
     s.nR = forced ? 0 : E; // one router row per job
     s.nSGU = Ish > 0 ? Ish / 16 : 0;
-    s.tilesI = I / 16;
-    s.tilesH = H / 16;
+    s.nSD = Ish > 0 ? H / 16 : 0;
+    s.tilesI = I / 16; // GU: one 16-row tile of gate and up
+    s.tilesD = H / 32; // D: two 16-row tiles of down
     s.Umax = (T * K < E) ? T * K : E;
-    if (phased) {
-        s.oSGU = s.nR;
-        s.oSEL = s.oSGU + s.nSGU;
-        s.oGU = s.oSEL + 1;
-    } else {
-        s.oSEL = s.nR;
-        s.oSGU = s.oSEL + 1;
-        s.oGU = s.oSGU + s.nSGU;
-    }
-    s.oSD = s.oGU + s.Umax * s.tilesI;
-    s.oD = s.oSD + (Ish > 0 ? s.tilesH : 0);
-    s.total = s.oD + s.Umax * s.tilesH;
+    s.oSEL = s.nR;
+    s.oSGU = s.oSEL + 1;
+    s.oSD = s.oSGU + s.nSGU;
+    s.oGU = s.oSD + s.nSD;
+    s.oD = s.oGU + s.Umax * s.tilesI;
+    s.total = s.oD + s.Umax * s.tilesD;
     return s;
 }
 
 __device__ __forceinline__ JobSpace job_space(const DecodeArgs &a) {
-    return job_space(a.E, a.I, a.H, a.Ish, a.T, a.K, a.forced_idx != nullptr, a.phased != 0);
+    return job_space(a.E, a.I, a.H, a.Ish, a.T, a.K, a.forced_idx != nullptr);
 }
 
 __device__ __forceinline__ int pad_tp(int n) { return n <= 1 ? 1 : (n <= 2 ? 2 : (n <= 4 ? 4 : 8)); }
@@ -969,13 +963,17 @@ __device__ void producer(const DecodeArgs &a, DecodeSmem &sm, const JobSpace &js
         return mbar_wait(a, &sm.empty[slot], ((n / kRing) & 1u) ^ 1u);
     };
     bool ok = true;
+    bool first = true;
     while (ok) {
-        const int j =
-            ld_relaxed(a.ctl + kCtlAbort) ? js.total : a.jlo + (int)atomicAdd(a.ctl + kCtlJobNext, 1u);
-        if (j >= a.jhi)
+        // the first job of each CTA is its own index; later ones come from the queue
+        const int j = ld_relaxed(a.ctl + kCtlAbort)
+                          ? js.total
+                          : (first ? (int)blockIdx.x : (int)gridDim.x + (int)atomicAdd(a.ctl + kCtlJobNext, 1u));
+        first = false;
+        if (j >= js.total)
             break;
         if (j >= js.oGU && !routed) {
-            if (!a.phased && !wait_counter(a, a.ctl + kCtlRoutingEpoch, a.epoch, true))
+            if (!wait_counter(a, a.ctl + kCtlRoutingEpoch, a.epoch, true))
                 break;
             asm volatile("fence.proxy.async.global;" ::: "memory");
             routed = true;
@@ -991,23 +989,23 @@ __device__ void producer(const DecodeArgs &a, DecodeSmem &sm, const JobSpace &js
             per16 = 16 * (4 + 2 * a.T);
         } else if (j == js.oSEL) {
             type = kJobSel;
-        } else if (j < js.oGU) {
+        } else if (j < js.oSD) {
             type = kJobSgu;
             a0 = j - js.oSGU;
             per16 = 2 * 16 * 17 + 16 * 2 * a.T; // two 8-bit tiles (17/16 B per column each) + bf16 x rows
-        } else if (j < js.oSD) {
-            type = kJobGu;
-            a0 = (j - js.oGU) / js.tilesI;
-            tile = (j - js.oGU) % js.tilesI;
-        } else if (j < js.oD) {
+        } else if (j < js.oGU) {
             type = kJobSd;
             a0 = j - js.oSD;
             K = a.Ish;
             per16 = 16 * 17 + 16 * 4 * a.T; // one 8-bit tile + binary16 hi and lo rows
+        } else if (j < js.oD) {
+            type = kJobGu;
+            a0 = (j - js.oGU) / js.tilesI;
+            tile = (j - js.oGU) % js.tilesI;
         } else {
             type = kJobD;
-            a0 = (j - js.oD) / js.tilesH;
-            tile = (j - js.oD) % js.tilesH;
+            a0 = (j - js.oD) / js.tilesD;
+            tile = (j - js.oD) % js.tilesD;
             K = a.I;
         }
         if ((type == kJobGu || type == kJobD)) {
@@ -1020,9 +1018,9 @@ __device__ void producer(const DecodeArgs &a, DecodeSmem &sm, const JobSpace &js
                 pos[i] = p0 + ii;
                 tok[i] = __ldcg(a.perm + p0 + ii) / a.K;
             }
-            // 2-bit tile(s): 84/256 B per column per 16 rows = 5.25 B; activations per token:
-            // GU x' (2 B) + off/sum (0.5 B); D hi + lo (4 B) + off/sum (0.5 B)
-            per16 = type == kJobGu ? 2 * 84 + ntok * 40 : 84 + ntok * 72;
+            // two 2-bit tiles: 84/256 B per column per 16 rows = 5.25 B each; activations per
+            // token: GU x' (2 B) + off/sum (0.5 B); D hi + lo (4 B) + off/sum (0.5 B)
+            per16 = type == kJobGu ? 2 * 84 + ntok * 40 : 2 * 84 + ntok * 72;
         }
         const int e = (type == kJobGu || type == kJobD) ? __ldcg(a.uexp + a0) : 0;
         const int W = type == kJobSel ? 0 : pick_w(K, per16);
@@ -1080,11 +1078,11 @@ __device__ void producer(const DecodeArgs &a, DecodeSmem &sm, const JobSpace &js
                 for (int t = 0; t < a.T; t++)
                     sw.put(a.hs_lo + (int64_t)t * a.Ish + c0, 2u * W);
             } else if (type == kJobGu || type == kJobD) {
-                const Q2Frag *M[2] = {type == kJobGu ? &a.gate : &a.down, &a.up};
-                const int nmat = type == kJobGu ? 2 : 1;
+                // GU: gate and up tile `tile`; D: down tiles 2 tile and 2 tile + 1
+                const Q2Frag *M[2] = {type == kJobGu ? &a.gate : &a.down, type == kJobGu ? &a.up : &a.down};
                 const int rows_per_e = type == kJobGu ? a.I : a.H;
-                const int64_t gt = (int64_t)e * (rows_per_e / 16) + tile;
-                for (int m = 0; m < nmat; m++) {
+                for (int m = 0; m < 2; m++) {
+                    const int64_t gt = (int64_t)e * (rows_per_e / 16) + (type == kJobGu ? tile : 2 * tile + m);
                     const int64_t u = gt * M[m]->nkc + c0 / 128;
                     d.oq[m] = sw.put(M[m]->qs + u * 32, (unsigned)(W / 128) * 512u);
                     d.os[m] = sw.put(M[m]->sc + u * 8, (unsigned)(W / 128) * 128u);
@@ -1123,8 +1121,7 @@ __device__ void producer(const DecodeArgs &a, DecodeSmem &sm, const JobSpace &js
                         sw.put(a.hsum + (int64_t)pos[t] * (K / 16) + c0 / 16, (unsigned)W / 4u);
                 }
             }
-            const unsigned *dep =
-                a.phased ? nullptr : (type == kJobD ? a.ctl + kCtlGuDone + a0 : a.ctl + kCtlSguDone);
+            const unsigned *dep = type == kJobD ? a.ctl + kCtlGuDone + a0 : a.ctl + kCtlSguDone;
             const unsigned target = type == kJobD ? (unsigned)js.tilesI : (unsigned)js.nSGU;
             n++;
             if (!sw.issue(a, dep, target)) {
@@ -1143,12 +1140,12 @@ __device__ void producer(const DecodeArgs &a, DecodeSmem &sm, const JobSpace &js
 
 // ---- consumers (warps 0..7) ----------------------------------------------------------
 
-// y for 16 rows (tile ti) and all tokens, in fixed order: sum over k, then
+// y for 32 rows (tile ti) and all tokens, in fixed order: sum over k, then
 // shared. Warp 0 of the consumers.
 __device__ void combine_tile(const DecodeArgs &a, int ti, int lane) {
-    for (int q = lane; q < 16 * a.T; q += 32) {
-        const int r = q & 15, t = q >> 4;
-        const int col = ti * 16 + r;
+    for (int q = lane; q < 32 * a.T; q += 32) {
+        const int r = q & 31, t = q >> 5;
+        const int col = ti * 32 + r;
         float v = 0.f;
         for (int k = 0; k < a.K; k++)
             v = fmaf(__ldcg(a.w + t * a.K + k), __ldcg(a.ye + (int64_t)__ldcg(a.inv + t * a.K + k) * a.H + col), v);
@@ -1158,21 +1155,24 @@ __device__ void combine_tile(const DecodeArgs &a, int ti, int lane) {
     }
 }
 
-// After the consumers' barrier that follows the job's result writes: warp 0
-// counts the contribution to H tile ti; the last contribution combines the
-// tile. The other warps go on with the next job.
-__device__ void arrive_tile(const DecodeArgs &a, int ti, int nuniq, int warp, int lane) {
+// After the consumers' barrier that follows a D job's result writes: warp 0
+// counts the contribution to the 32-row tile ti; the last of the nuniq
+// contributions combines the tile, once the shared expert's down rows are
+// complete (those jobs precede every D job in the queue, so the wait ends).
+// The other warps go on with the next job.
+__device__ void arrive_tile(const DecodeArgs &a, const JobSpace &js, int ti, int nuniq, int warp, int lane) {
     if (warp != 0)
         return;
     unsigned last = 0;
     if (lane == 0) {
         __threadfence();
-        const unsigned expected = (unsigned)nuniq + (a.Ish > 0 ? 1u : 0u);
         const unsigned old = atomicAdd(a.ctl + kCtlTileCnt + ti, 1u);
-        last = old + 1 == expected;
+        last = old + 1 == (unsigned)nuniq;
         if (last) {
             __threadfence();
             a.ctl[kCtlTileCnt + ti] = 0; // ready for the next launch
+            if (js.nSD > 0 && !wait_counter(a, a.ctl + kCtlSdDone, (unsigned)js.nSD, false))
+                last = 0;
         }
     }
     if (__shfl_sync(0xFFFFFFFFu, last, 0))
@@ -1195,17 +1195,17 @@ template <int TP> struct JobOps {
         case kJobSgu: q8_stage<TP, 2, false, true>(sl, d, warp, lane, out); break;
         case kJobGu: q2_stage<TP, 2, false>(sl, d, warp, lane, out); break;
         case kJobSd: q8_stage<TP, 1, true, false>(sl, d, warp, lane, out); break;
-        case kJobD: q2_stage<TP, 1, true>(sl, d, warp, lane, out); break;
+        case kJobD: q2_stage<TP, 2, true>(sl, d, warp, lane, out); break;
         default: break;
         }
     }
     // End of a job: combine the warps' partial sums (barrier 1), write the
     // results, barrier 2, then publish (thread 0 / warp 0, without a barrier).
-    static __device__ void finish(const DecodeArgs &a, DecodeSmem &sm, const StageDesc &d, int buf, int warp,
-                                  int lane, float (&out)[2][2][2]) {
+    static __device__ void finish(const DecodeArgs &a, const JobSpace &js, DecodeSmem &sm, const StageDesc &d,
+                                  int buf, int warp, int lane, float (&out)[2][2][2]) {
         const int tid = threadIdx.x;
         auto P = sm.part[buf];
-        if (d.type == kJobSgu || d.type == kJobGu) {
+        if (d.type != kJobSd) {
             reduce_out<TP, 2>(out);
             store_part<TP, 2>(sm, buf, warp, lane, out);
         } else {
@@ -1274,17 +1274,20 @@ template <int TP> struct JobOps {
                 a.ysh[(int64_t)t * a.H + d.a0 * 16 + r] = v;
             }
             consumer_sync();
-            arrive_tile(a, d.a0, d.nuniq, warp, lane);
-        } else { // kJobD
+            signal(a, a.ctl + kCtlSdDone);
+        } else { // kJobD: rows 32 tile + 16 m + r
             const int t = tid >> 4, r = tid & 15;
             if (t < d.ntok) {
-                float v = 0.f;
-                for (int w = 0; w < kConsumerWarps; w++)
-                    v += P[w][0][r][t];
-                a.ye[(int64_t)d.pos[t] * a.H + d.tile * 16 + r] = v;
+#pragma unroll
+                for (int m = 0; m < 2; m++) {
+                    float v = 0.f;
+                    for (int w = 0; w < kConsumerWarps; w++)
+                        v += P[w][m][r][t];
+                    a.ye[(int64_t)d.pos[t] * a.H + d.tile * 32 + 16 * m + r] = v;
+                }
             }
             consumer_sync();
-            arrive_tile(a, d.tile, d.nuniq, warp, lane);
+            arrive_tile(a, js, d.tile, d.nuniq, warp, lane);
         }
     }
 };
@@ -1299,13 +1302,13 @@ __device__ __forceinline__ void stage_tp(int tp, const DecodeArgs &a, const uint
     }
 }
 
-__device__ __forceinline__ void finish_tp(int tp, const DecodeArgs &a, DecodeSmem &sm, const StageDesc &d, int buf,
-                                          int warp, int lane, float (&out)[2][2][2]) {
+__device__ __forceinline__ void finish_tp(int tp, const DecodeArgs &a, const JobSpace &js, DecodeSmem &sm,
+                                          const StageDesc &d, int buf, int warp, int lane, float (&out)[2][2][2]) {
     switch (tp) {
-    case 1: JobOps<1>::finish(a, sm, d, buf, warp, lane, out); break;
-    case 2: JobOps<2>::finish(a, sm, d, buf, warp, lane, out); break;
-    case 4: JobOps<4>::finish(a, sm, d, buf, warp, lane, out); break;
-    default: JobOps<8>::finish(a, sm, d, buf, warp, lane, out); break;
+    case 1: JobOps<1>::finish(a, js, sm, d, buf, warp, lane, out); break;
+    case 2: JobOps<2>::finish(a, js, sm, d, buf, warp, lane, out); break;
+    case 4: JobOps<4>::finish(a, js, sm, d, buf, warp, lane, out); break;
+    default: JobOps<8>::finish(a, js, sm, d, buf, warp, lane, out); break;
     }
 }
 
@@ -1327,7 +1330,7 @@ __device__ void consumer(const DecodeArgs &a, DecodeSmem &sm, const JobSpace &js
                 (&out[0][0][0])[i] = 0.f;
             const unsigned *dep = nullptr;
             unsigned target = 0;
-            if (type == kJobSel && !a.phased) {
+            if (type == kJobSel) {
                 dep = a.ctl + kCtlRouterDone;
                 target = (unsigned)js.nR;
             }
@@ -1382,7 +1385,7 @@ __device__ void consumer(const DecodeArgs &a, DecodeSmem &sm, const JobSpace &js
                 }
             } else {
                 const int buf = (int)(jobs_done & 1u);
-                finish_tp(d.tp, a, sm, d, buf, warp, lane, out);
+                finish_tp(d.tp, a, js, sm, d, buf, warp, lane, out);
             }
             jobs_done++;
         }
@@ -1423,6 +1426,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_fused_kernel(DecodeA
                 a.ctl[kCtlJobNext] = 0;
                 a.ctl[kCtlRouterDone] = 0;
                 a.ctl[kCtlSguDone] = 0;
+                a.ctl[kCtlSdDone] = 0;
                 for (int s = 0; s < kMaxSlots; s++)
                     a.ctl[kCtlGuDone + s] = 0;
                 __threadfence();

@@ -352,7 +352,7 @@ void layout_scratch(ds4moe *h, Carver &c) {
     D.hs_lo = c.take<uint16_t>(Td * (L.Ish > 0 ? L.Ish : 2));
     D.ye = c.take<float>(Pd * L.H);
     D.ysh = c.take<float>(Td * L.H);
-    D.ctl_words = kCtlTileCnt + L.H / 16;
+    D.ctl_words = kCtlTileCnt + L.H / 32;
     D.ctl = c.take<unsigned>(D.ctl_words);
 }
 
@@ -588,11 +588,6 @@ int run_experts_prefill(ds4moe *h, const void *x, int T, float *y) {
     return launch_rc();
 }
 
-// Decode as four phased launches of the decode kernel (true) or as one
-// cooperative launch with in-kernel dependency waits (false). Measured on the
-// H=4096, E=384 layer at T=1: 125 us phased, 108 us fused; fused is the default.
-constexpr bool kDecodePhased = false;
-
 // The fused decode kernel over tokens [0, T) in launches of up to 8 tokens.
 // forced_idx/forced_w: caller routing (nullptr = route here). idx_out/w_out
 // receive the routing of every token ([T][K]).
@@ -647,41 +642,14 @@ int run_decode(ds4moe *h, const void *x, int T, float *y, const int32_t *forced_
         a.ysh = D.ysh;
         a.ctl = D.ctl;
         a.status = h->status;
-        if (kDecodePhased) {
-            // four launches: router rows + shared gate/up | selection | routed gate/up +
-            // shared down | routed down + combine
-            const JobSpace js = job_space(L.E, L.I, L.H, L.Ish, Tc, L.K, forced_idx != nullptr, true);
-            const int bounds[5] = {0, js.oSEL, js.oGU, js.oD, js.total};
-            static const char *names[4] = {"decode_p1_router_shared", "decode_p2_select", "decode_p3_gateup",
-                                           "decode_p4_down"};
-            a.phased = 1;
-            for (int ph = 0; ph < 4; ph++) {
-                a.jlo = bounds[ph];
-                a.jhi = bounds[ph + 1];
-                if (a.jhi <= a.jlo)
-                    continue;
-                const int jobs = a.jhi - a.jlo;
-                const int grid = jobs < D.grid ? jobs : D.grid;
-                launch(h, names[ph], [&] {
-                    decode_fused_kernel<<<grid, kDecodeThreads, sizeof(DecodeSmem), h->stream>>>(a);
-                });
-                int rc = launch_rc();
-                if (rc)
-                    return rc;
-            }
-        } else {
-            a.phased = 0;
-            a.jlo = 0;
-            a.jhi = job_space(L.E, L.I, L.H, L.Ish, Tc, L.K, forced_idx != nullptr, false).total;
-            void *args[] = {&a};
-            launch(h, "decode_fused", [&] {
-                cudaLaunchCooperativeKernel((const void *)decode_fused_kernel, dim3(D.grid), dim3(kDecodeThreads),
-                                            args, sizeof(DecodeSmem), h->stream);
-            });
-            int rc = launch_rc();
-            if (rc)
-                return rc;
-        }
+        void *args[] = {&a};
+        launch(h, "decode_fused", [&] {
+            cudaLaunchCooperativeKernel((const void *)decode_fused_kernel, dim3(D.grid), dim3(kDecodeThreads), args,
+                                        sizeof(DecodeSmem), h->stream);
+        });
+        int rc = launch_rc();
+        if (rc)
+            return rc;
     }
     return DS4MOE_OK;
 }
