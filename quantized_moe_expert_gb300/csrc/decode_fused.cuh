@@ -28,7 +28,7 @@
 //        fixed order
 // The shared expert's jobs sit between the selection and the routed jobs so
 // that they stream while the routing is computed and published.
-// The producer resolves the addresses of GU, SD and D jobs after the routing
+// The producer resolves the addresses of GU and D jobs after the routing
 // is published; the weight loads of a job never wait for its data
 // dependencies, only its consumers do, so loads overlap those waits.
 //
@@ -1129,6 +1129,10 @@ __device__ void producer(const DecodeArgs &a, DecodeSmem &sm, const JobSpace &js
                 break;
             }
         }
+        // the CTA that computes the routing takes no further job before it is
+        // published: a job queued behind the selection would wait for it
+        if (type == kJobSel && ok && !wait_counter(a, a.ctl + kCtlRoutingEpoch, a.epoch, true))
+            break;
     }
     // end of this CTA's jobs
     int slot;
@@ -1180,12 +1184,11 @@ __device__ void arrive_tile(const DecodeArgs &a, const JobSpace &js, int ti, int
 }
 
 // After the consumers' barrier that follows the job's result writes: thread 0
-// publishes the job (release fence, then the count); nobody waits for it here.
+// publishes the job with one release reduction on the count (the barrier
+// orders the other threads' writes before it); nobody waits for it here.
 __device__ __forceinline__ void signal(const DecodeArgs &a, unsigned *ctr) {
-    if (threadIdx.x == 0) {
-        __threadfence();
-        atomicAdd(ctr, 1u);
-    }
+    if (threadIdx.x == 0)
+        asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(ctr) : "memory");
 }
 
 template <int TP> struct JobOps {
