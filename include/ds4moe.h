@@ -150,6 +150,10 @@ int ds4moe_forward_path(ds4moe_t *h, const void *x_bf16, int32_t T, int32_t path
  * with 0 <= idx < E, w device fp32 [T][K]. Used to compare the expert and
  * combine stages on tokens whose routing is a near-tie. Indices out of range
  * are clamped by the kernels and reported as DS4MOE_EDEVICE by ds4moe_status.
+ * A token's K indices should be distinct: the decode path (T <= 8 per launch)
+ * replaces a repeated index by the smallest index the token's row does not
+ * hold and reports DS4MOE_EDEVICE; the prefill path applies the expert once per
+ * occurrence.
  */
 int ds4moe_forward_routed(ds4moe_t *h, const void *x_bf16, int32_t T, const int32_t *idx,
                           const float *w, int32_t path, float *y);

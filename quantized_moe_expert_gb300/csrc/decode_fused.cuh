@@ -14,10 +14,13 @@
 // always run: the queue cannot deadlock as long as all CTAs are resident,
 // which the cooperative launch guarantees. The queue, in order:
 //
-//   R    one router row: fp32 logits for all T tokens
-//   SEL  one job: activation pre-scaling for the 2-bit MMA (before its wait);
-//        per-token sigmoid, exact top-k, weights; distinct-expert grouping;
-//        publishes the routing (waits for all R jobs)
+//   SEL  one job, the first job of CTA 0: activation pre-scaling for the
+//        2-bit MMA; then, as the router rows arrive, per-token sigmoid, exact
+//        top-k, weights and the distinct-expert grouping; publishes one
+//        record per distinct expert (waits for all R jobs)
+//   R    one or two router rows: fp32 logits for all T tokens, each stored
+//        with the launch's epoch in the same 64-bit word (the value is its
+//        own completion flag)
 //   SGU  shared expert, one 16-row tile of gate and up: h_sh = silu(g) * u
 //   SD   shared expert down, one 16-row tile of H (waits: all SGU)
 //   GU   (distinct expert, 16-row tile of I): gate and up, h = silu(g) * u,
@@ -28,8 +31,9 @@
 //        fixed order
 // The shared expert's jobs sit between the selection and the routed jobs so
 // that they stream while the routing is computed and published.
-// The producer resolves the addresses of GU and D jobs after the routing
-// is published; the weight loads of a job never wait for its data
+// The producer of a GU or D job polls that expert's routing record (epoch-
+// tagged, so the poll and the lookup are one load) and then issues the
+// weight copies; the weight loads of a job never wait for its data
 // dependencies, only its consumers do, so loads overlap those waits.
 //
 // This follows the pages' decode engine in spirit - routed experts and the
@@ -63,14 +67,22 @@ constexpr int kDecodeThreads = 32 * (kConsumerWarps + 1);
 // Control words (zeroed at create; every launch leaves them zeroed again).
 enum : int {
     kCtlJobNext = 0,
-    kCtlRouterDone = 1,
-    kCtlRoutingEpoch = 2,
     kCtlSguDone = 3,
     kCtlFinished = 4,
     kCtlAbort = 5,
     kCtlSdDone = 6,
     kCtlGuDone = 8,              // [kMaxSlots]
     kCtlTileCnt = 8 + kMaxSlots, // [H / 32]
+};
+
+// Where the selection reads its logits and writes its results.
+struct SelIO {
+    const unsigned long long *lgt;
+    unsigned epoch;
+    int32_t *idx;
+    float *w, *gap;
+    int32_t *inv, *counts, *nuniq;
+    unsigned long long *srec;
 };
 
 struct DecodeArgs {
@@ -84,12 +96,13 @@ struct DecodeArgs {
     const int32_t *forced_idx; // [T][K] or nullptr
     const float *forced_w;
     unsigned epoch;
-    float *logits;   // [8][E]
+    unsigned long long *lgt;  // [8][E] router logits: fp32 bits | epoch << 32
+    unsigned long long *srec; // [kMaxSlots][2] routing record of each distinct-expert slot (| epoch << 32)
     int32_t *idx;    // [8][K]
     float *w;        // [8][K]
     float *gap;      // [8]
     int32_t *counts; // [E]
-    int32_t *nuniq, *uexp, *uoff, *perm, *inv;
+    int32_t *nuniq, *inv;
     uint16_t *xq;            // [8][H] bf16 x * 2^e(k)
     float *xoff, *xsum;      // [8][H/16]
     uint16_t *hq_hi, *hq_lo; // [64][I] bf16 h * 2^e(k) as hi + lo
@@ -99,6 +112,7 @@ struct DecodeArgs {
     float *ysh;              // [8][H]
     unsigned *ctl;
     unsigned *status;
+    SelIO io; // the selection's inputs and outputs (the buffers above)
 };
 
 enum JobType : int { kJobEnd = 0, kJobR, kJobSgu, kJobSel, kJobGu, kJobSd, kJobD };
@@ -130,6 +144,9 @@ struct DecodeSmem {
     unsigned bitmap[32];
     int word_prefix[32];
     int slot_cnt[kMaxSlots];
+    int pair_at[kMaxSlots]; // grouping: the pair at each expert-grouped position
+    unsigned rec[2][kMaxSlots]; // grouping: the slot records before publication
+    int sel_flag[2];            // selection: give-up decision of thread 0, double-buffered by poll round
     // the producer's list of bulk copies for the stage it is building
     const void *pc_src[40];
     unsigned pc_bytes[40];
@@ -150,8 +167,38 @@ __device__ __forceinline__ unsigned ld_acquire(const unsigned *p) {
     return v;
 }
 
-__device__ __forceinline__ void st_release(unsigned *p, unsigned v) {
-    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+__device__ __forceinline__ void st_relaxed_u64(unsigned long long *p, unsigned long long v) {
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long *p) {
+    unsigned long long v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long *p) {
+    unsigned long long v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// A routing record of one distinct-expert slot: word 0 = expert | first pair
+// position << 11 | token count << 18 | distinct experts << 22, word 1 = the
+// tokens of its pairs, 3 bits each in pair order; both | epoch << 32.
+struct SlotRec {
+    int e, p0, ntok, nuniq;
+    unsigned toks;
+};
+
+__device__ __forceinline__ SlotRec unpack_slot(unsigned w0, unsigned w1) {
+    SlotRec r;
+    r.e = (int)(w0 & 0x7FFu);
+    r.p0 = (int)((w0 >> 11) & 0x7Fu);
+    r.ntok = (int)((w0 >> 18) & 0xFu);
+    r.nuniq = (int)((w0 >> 22) & 0x7Fu);
+    r.toks = w1;
+    return r;
 }
 
 __device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
@@ -578,26 +625,33 @@ __device__ __forceinline__ void store_part(DecodeSmem &sm, int buf, int warp, in
         }
 }
 
-// Router row over the stage: fp32 weights at oq[0], bf16 x rows at oact; warp
-// w takes columns [w W/8, (w+1) W/8). out (as 8 floats) accumulates token t's
-// partial dot product in each lane.
+// Router rows over the stage: d.tile fp32 rows of d.W columns back to back at
+// oq[0], bf16 x rows at oact; warp w takes columns [w W/8, (w+1) W/8). out
+// (as 8 floats) accumulates the partial dot product of row r and token t at
+// index 4 r + t in each lane (two rows only when T <= 4).
 __device__ __forceinline__ void router_stage(const uint8_t *sl, const StageDesc &d, int T, int warp, int lane,
                                              float (&out)[2][2][2]) {
     float *acc = &out[0][0][0];
-    const float4 *wr = reinterpret_cast<const float4 *>(sl + d.oq[0]);
     const int n4 = d.W >> 2;
     const int b = n4 * warp / kConsumerWarps, e = n4 * (warp + 1) / kConsumerWarps;
-#pragma unroll 4
-    for (int i = b + lane; i < e; i += 32) {
-        const float4 wv = wr[i];
 #pragma unroll
-        for (int t = 0; t < kDecodeT; t++) {
-            if (t < T) {
-                const uint2 xv = reinterpret_cast<const uint2 *>(sl + d.oact + t * d.act_pitch)[i];
-                acc[t] = fmaf(wv.x, __uint_as_float(xv.x << 16), acc[t]);
-                acc[t] = fmaf(wv.y, __uint_as_float(xv.x & 0xFFFF0000u), acc[t]);
-                acc[t] = fmaf(wv.z, __uint_as_float(xv.y << 16), acc[t]);
-                acc[t] = fmaf(wv.w, __uint_as_float(xv.y & 0xFFFF0000u), acc[t]);
+    for (int r = 0; r < 2; r++) {
+        if (r >= d.tile)
+            break;
+        const float4 *wr = reinterpret_cast<const float4 *>(sl + d.oq[0] + r * 4 * d.W);
+#pragma unroll 4
+        for (int i = b + lane; i < e; i += 32) {
+            const float4 wv = wr[i];
+#pragma unroll
+            for (int t = 0; t < kDecodeT; t++) {
+                if (t < T && 4 * r + t < kDecodeT) {
+                    const uint2 xv = reinterpret_cast<const uint2 *>(sl + d.oact + t * d.act_pitch)[i];
+                    float &c = acc[4 * r + t];
+                    c = fmaf(wv.x, __uint_as_float(xv.x << 16), c);
+                    c = fmaf(wv.y, __uint_as_float(xv.x & 0xFFFF0000u), c);
+                    c = fmaf(wv.z, __uint_as_float(xv.y << 16), c);
+                    c = fmaf(wv.w, __uint_as_float(xv.y & 0xFFFF0000u), c);
+                }
             }
         }
     }
@@ -614,8 +668,8 @@ __device__ __forceinline__ unsigned sel_key(float v) { return v == v ? order_key
 // two warp reductions; only the lane whose candidate was taken marks it and
 // rescans its experts. One round more than K gives the (K+1)-th score for the
 // near-tie gap.
-__device__ __forceinline__ void select_token(const DecodeArgs &a, DecodeSmem &sm, unsigned *keys, int t,
-                                             int lane) {
+__device__ __forceinline__ void select_token(const DecodeArgs &a, const SelIO &io, DecodeSmem &sm, unsigned *keys,
+                                             int t, int lane) {
     const int E = a.E, K = a.K;
     unsigned best = 0u;
     int bi = -1;
@@ -632,6 +686,7 @@ __device__ __forceinline__ void select_token(const DecodeArgs &a, DecodeSmem &sm
     };
     rescan();
     int chosen = 0;
+    unsigned chosen_key = 0u;
     float kth = 0.f, next = -INFINITY;
     const int rounds = K < E ? K + 1 : K;
     for (int r = 0; r < rounds; r++) {
@@ -640,8 +695,10 @@ __device__ __forceinline__ void select_token(const DecodeArgs &a, DecodeSmem &sm
         const int be = (int)__reduce_min_sync(0xFFFFFFFFu, cand); // < E: every round has a candidate
         const float bv = gk > 1u ? order_key_value(gk) : __uint_as_float(0x7FC00000u);
         if (r < K) {
-            if (lane == r)
+            if (lane == r) {
                 chosen = be;
+                chosen_key = gk;
+            }
             if (r == K - 1)
                 kth = bv;
             if (bi == be) { // this lane's candidate was taken
@@ -652,19 +709,26 @@ __device__ __forceinline__ void select_token(const DecodeArgs &a, DecodeSmem &sm
             next = bv;
         }
     }
-    // weights: the chosen experts' sigmoid scores (recomputed from the logits
-    // with the same function), renormalised in selection order
-    const float sc = lane < K ? sigmoid(__ldcg(a.logits + t * E + chosen)) : 0.f;
+    // weights: the chosen experts' sigmoid scores, renormalised in selection
+    // order. Without a bias the selection key is the score itself; with one,
+    // the score is recomputed from the logit with the same function.
+    float sc = 0.f;
+    if (lane < K) {
+        if (a.router_bias)
+            sc = sigmoid(__uint_as_float((unsigned)ld_relaxed_u64(io.lgt + t * E + chosen)));
+        else
+            sc = chosen_key > 1u ? order_key_value(chosen_key) : __uint_as_float(0x7FC00000u);
+    }
     float total = 0.f;
     for (int r = 0; r < K; r++)
         total += __shfl_sync(0xFFFFFFFFu, sc, r);
     if (lane < K) {
         sm.sel_idx[t][lane] = chosen;
-        a.idx[t * K + lane] = chosen;
-        a.w[t * K + lane] = total > 0.f ? sc / total : 1.0f / K;
+        io.idx[t * K + lane] = chosen;
+        io.w[t * K + lane] = total > 0.f ? sc / total : 1.0f / K;
     }
     if (lane == 0)
-        a.gap[t] = K < E ? kth - next : INFINITY;
+        io.gap[t] = K < E ? kth - next : INFINITY;
 }
 
 // Work of the selection job that needs no router output (all consumer
@@ -704,51 +768,104 @@ __device__ void select_prepare(const DecodeArgs &a, float *scratch) {
     }
 }
 
-// Per-token selection after the router rows are complete: selection keys of
-// all (token, expert) pairs into the job's stage buffer (all consumer
-// threads), exact top-k (warp t takes token t), then the grouping, computed
-// in shared memory and written out once.
-__device__ void job_select(const DecodeArgs &a, DecodeSmem &sm, float *scratch, int warp, int lane) {
+// Per-token selection as the router rows arrive: every consumer thread polls
+// its share of the epoch-tagged logits until all are present (bounded),
+// turning each into its selection key in the job's stage buffer; exact top-k
+// (warp t takes token t); then the grouping, computed in shared memory, and
+// one routing record per distinct-expert slot, published after a fence.
+// Returns false if the wait for the router rows gave up.
+__device__ __forceinline__ bool job_select(const DecodeArgs &a, const SelIO &io, DecodeSmem &sm, float *scratch,
+                                           int warp, int lane) {
     const int T = a.T, E = a.E, K = a.K;
     unsigned *keys = reinterpret_cast<unsigned *>(scratch);
     if (!a.forced_idx) {
         const float *bias = scratch + kDecodeT * E;
         const int n = T * E;
-        // four logits per thread in flight at a time
-        for (int q0 = threadIdx.x; q0 < n; q0 += 4 * 32 * kConsumerWarps) {
-            float lg[4];
-#pragma unroll
-            for (int u = 0; u < 4; u++) {
-                const int q = q0 + u * 32 * kConsumerWarps;
-                lg[u] = q < n ? __ldcg(a.logits + q) : 0.f;
-            }
-#pragma unroll
-            for (int u = 0; u < 4; u++) {
-                const int q = q0 + u * 32 * kConsumerWarps;
-                if (q < n) {
-                    const int e = q % E;
-                    const float sg = sigmoid(lg[u]);
-                    keys[q] = sel_key(a.router_bias ? sg + bias[e] : sg);
+        constexpr int kStride = 32 * kConsumerWarps;
+        // thread i owns entries i, i + 256, ... (at most 32 of them: T E <= 8192)
+        unsigned pending = 0u;
+        for (int u = 0, q = threadIdx.x; q < n; u++, q += kStride)
+            pending |= 1u << u;
+        uint64_t t0 = 0;
+        for (unsigned it = 0;; it++) {
+            unsigned still = 0u;
+            for (int u = 0, q = threadIdx.x; q < n; u++, q += kStride) {
+                if (!(pending >> u & 1u))
+                    continue;
+                const unsigned long long v = ld_relaxed_u64(io.lgt + q);
+                if ((unsigned)(v >> 32) != io.epoch) {
+                    still |= 1u << u;
+                    continue;
                 }
+                const float sg = sigmoid(__uint_as_float((unsigned)v));
+                keys[q] = sel_key(a.router_bias ? sg + bias[q % E] : sg);
             }
+            pending = still;
+            // bounded: thread 0 decides for everyone; the flag of round it is
+            // rewritten only two barriers later, after every thread has read it
+            if (threadIdx.x == 0) {
+                int give_up = 0;
+                if ((it & 15) == 0) {
+                    const uint64_t now = globaltimer();
+                    if (it == 0)
+                        t0 = now;
+                    else if (now - t0 > kWaitNs) {
+                        atomicOr(a.status, kErrTimeout);
+                        atomicExch(a.ctl + kCtlAbort, 1u);
+                        give_up = 1;
+                    } else if (ld_relaxed(a.ctl + kCtlAbort)) {
+                        give_up = 1;
+                    }
+                }
+                sm.sel_flag[it & 1] = give_up;
+            }
+            int all_done;
+            asm volatile("{\n\t.reg .pred p, q;\n\tsetp.eq.u32 p, %1, 0;\n\t"
+                         "bar.red.and.pred q, 1, 256, p;\n\tselp.s32 %0, 1, 0, q;\n\t}"
+                         : "=r"(all_done)
+                         : "r"(pending)
+                         : "memory");
+            if (all_done)
+                break;
+            if (sm.sel_flag[it & 1])
+                return false;
+            __nanosleep(64);
         }
-        consumer_sync();
     }
     if (warp < T) {
         const int t = warp;
         if (a.forced_idx) {
+            int e = -1 - lane; // lanes >= K hold distinct non-experts
             if (lane < K) {
-                int e = a.forced_idx[t * K + lane];
+                e = a.forced_idx[t * K + lane];
                 if (e < 0 || e >= E) {
                     atomicOr(a.status, kErrIndex);
                     e = e < 0 ? 0 : E - 1;
                 }
+            }
+            // a token's experts must be distinct (each expert's job holds at most
+            // one column per token): a repeated one is replaced, in lane order,
+            // by the smallest index the row does not hold, and reported
+            for (int r = 1; r < K; r++) {
+                const int er = __shfl_sync(0xFFFFFFFFu, e, r);
+                const bool dup = __ballot_sync(0xFFFFFFFFu, lane < r && e == er) != 0u;
+                if (dup) {
+                    int c = 0;
+                    while (__ballot_sync(0xFFFFFFFFu, e == c) != 0u)
+                        c++; // ends below E: the row holds K <= E experts
+                    if (lane == r)
+                        e = c;
+                    if (lane == 0)
+                        atomicOr(a.status, kErrIndex);
+                }
+            }
+            if (lane < K) {
                 sm.sel_idx[t][lane] = e;
                 a.idx[t * K + lane] = e;
                 a.w[t * K + lane] = a.forced_w[t * K + lane];
             }
         } else {
-            select_token(a, sm, keys + t * E, t, lane);
+            select_token(a, io, sm, keys + t * E, t, lane);
         }
     }
     if (threadIdx.x < 32)
@@ -821,49 +938,77 @@ __device__ void job_select(const DecodeArgs &a, DecodeSmem &sm, float *scratch, 
         sm.slot_cnt[2 * lane] = base;
         sm.slot_cnt[2 * lane + 1] = base + c0;
         __syncwarp();
-        if (2 * lane < nu)
-            a.uoff[2 * lane] = base;
-        if (2 * lane + 1 < nu)
-            a.uoff[2 * lane + 1] = base + c0;
-        if (lane == 0) {
-            a.uoff[nu] = P;
-            *a.nuniq = nu;
-        }
+        if (lane == 0)
+            *io.nuniq = nu;
 #pragma unroll
         for (int h = 0; h < 2; h++) {
             const int p = lane + 32 * h, e = pe[h];
             if (e >= 0) {
                 const int pos = sm.slot_cnt[slot[h]] + rank[h];
-                a.inv[p] = pos;
-                a.perm[pos] = p;
-                if (rank[h] == 0)
-                    a.uexp[slot[h]] = e;
-                atomicAdd(a.counts + e, 1);
+                io.inv[p] = pos;
+                sm.pair_at[pos] = p;
+                atomicAdd(io.counts + e, 1);
+            }
+        }
+        __syncwarp();
+        // records of slots 2 lane and 2 lane + 1 (slot expert from any of its pairs)
+#pragma unroll
+        for (int h = 0; h < 2; h++) {
+            const int sl = 2 * lane + h;
+            unsigned w0 = (unsigned)nu << 22, w1 = 0u;
+            if (sl < nu) {
+                const int p0 = sm.slot_cnt[sl], p1 = sl + 1 < nu ? sm.slot_cnt[sl + 1] : P;
+                const int pf = sm.pair_at[p0];
+                w0 |= (unsigned)sm.sel_idx[pf / K][pf % K] | (unsigned)p0 << 11 | (unsigned)(p1 - p0) << 18;
+                for (int i = 0; i < p1 - p0; i++)
+                    w1 |= (unsigned)(sm.pair_at[p0 + i] / K) << (3 * i);
+            }
+            if (sl < kMaxSlots) {
+                sm.rec[0][sl] = w0;
+                sm.rec[1][sl] = w1;
             }
         }
     }
+    // Everything the later jobs read (pre-scaled activations, routing outputs,
+    // inverse positions) is written; each writer fences, then warp 0 publishes
+    // the slot records. A reader that sees a record's epoch sees all of it.
+    __threadfence();
+    consumer_sync();
+    if (warp == 0) {
+        const unsigned long long tag = (unsigned long long)io.epoch << 32;
+        const int umax = T * K < E ? T * K : E;
+        for (int sl = lane; sl < umax; sl += 32) {
+            st_relaxed_u64(io.srec + 2 * sl, tag | sm.rec[0][sl]);
+            st_relaxed_u64(io.srec + 2 * sl + 1, tag | sm.rec[1][sl]);
+        }
+    }
+    return true;
 }
 
 // ---- job space ---------------------------------------------------------------------
 
 struct JobSpace {
-    int nR, nSGU, nSD, tilesI, tilesD, Umax;
-    int oSEL, oSGU, oSD, oGU, oD, total;
+    int nR, rows, nSGU, nSD, tilesI, tilesD, Umax;
+    int oR, oSGU, oSD, oGU, oD, total;
 };
 
-// Job order: R, SEL, SGU, SD, GU, D. The selection comes right after the
-// router rows (it is on the critical path); the shared expert's jobs follow,
-// so that they fill the time in which the routing is computed and published.
+// Job order: SEL, R, SGU, SD, GU, D. The selection is CTA 0's first job, so
+// its consumers are idle and waiting when the last router row lands; the
+// router rows are the first jobs of the next CTAs (two rows per job while
+// both rows' accumulators fit, so that the router is one round of jobs);
+// the shared expert's jobs follow, so that they fill the time in which the
+// routing is computed and published.
 __host__ __device__ __forceinline__ JobSpace job_space(int E, int I, int H, int Ish, int T, int K, bool forced) {
     JobSpace s;
-    s.nR = forced ? 0 : E; // one router row per job
+    s.rows = T <= 4 ? 2 : 1; // router rows per job: rows * T accumulators per lane (<= 8)
+    s.nR = forced ? 0 : (E + s.rows - 1) / s.rows;
     s.nSGU = Ish > 0 ? Ish / 16 : 0;
     s.nSD = Ish > 0 ? H / 16 : 0;
     s.tilesI = I / 16; // GU: one 16-row tile of gate and up
     s.tilesD = H / 32; // D: two 16-row tiles of down
     s.Umax = (T * K < E) ? T * K : E;
-    s.oSEL = s.nR;
-    s.oSGU = s.oSEL + 1;
+    s.oR = 1;
+    s.oSGU = s.oR + s.nR;
     s.oSD = s.oSGU + s.nSGU;
     s.oGU = s.oSD + s.nSD;
     s.oD = s.oGU + s.Umax * s.tilesI;
@@ -953,10 +1098,39 @@ struct StageWriter {
     }
 };
 
+// The routing record of distinct-expert slot `sl`, polled until it carries this
+// launch's epoch (bounded). The acquire orders the later copies of data the
+// selection wrote before publishing the record.
+__device__ bool wait_slot(const DecodeArgs &a, int sl, SlotRec &r) {
+    uint64_t t0 = 0;
+    for (unsigned it = 0;; it++) {
+        const unsigned long long v0 = ld_acquire_u64(a.srec + 2 * sl);
+        const unsigned long long v1 = ld_acquire_u64(a.srec + 2 * sl + 1);
+        if ((unsigned)(v0 >> 32) == a.epoch && (unsigned)(v1 >> 32) == a.epoch) {
+            r = unpack_slot((unsigned)v0, (unsigned)v1);
+            asm volatile("fence.proxy.async.global;" ::: "memory");
+            return true;
+        }
+        if ((it & 63) == 0) {
+            if (ld_relaxed(a.ctl + kCtlAbort))
+                return false;
+            const uint64_t now = globaltimer();
+            if (it == 0)
+                t0 = now;
+            else if (now - t0 > kWaitNs) {
+                atomicOr(a.status, kErrTimeout);
+                atomicExch(a.ctl + kCtlAbort, 1u);
+                return false;
+            }
+        }
+        __nanosleep(64);
+    }
+}
+
 __device__ void producer(const DecodeArgs &a, DecodeSmem &sm, const JobSpace &js) {
     unsigned n = 0; // stages issued so far
-    bool routed = false;
-    int nu = 0;
+    int cached_slot = -1; // GU and D jobs come slot by slot: keep the last record
+    SlotRec rec{};
     // claim the next ring slot (waits until the consumers released it)
     auto claim = [&](int &slot) -> bool {
         slot = (int)(n % kRing);
@@ -966,29 +1140,24 @@ __device__ void producer(const DecodeArgs &a, DecodeSmem &sm, const JobSpace &js
     bool first = true;
     while (ok) {
         // the first job of each CTA is its own index; later ones come from the queue
-        const int j = ld_relaxed(a.ctl + kCtlAbort)
-                          ? js.total
-                          : (first ? (int)blockIdx.x : (int)gridDim.x + (int)atomicAdd(a.ctl + kCtlJobNext, 1u));
+        const int j = first ? (int)blockIdx.x
+                            : (ld_relaxed(a.ctl + kCtlAbort) ? js.total
+                                                             : (int)gridDim.x + (int)atomicAdd(a.ctl + kCtlJobNext, 1u));
         first = false;
         if (j >= js.total)
             break;
-        if (j >= js.oGU && !routed) {
-            if (!wait_counter(a, a.ctl + kCtlRoutingEpoch, a.epoch, true))
-                break;
-            asm volatile("fence.proxy.async.global;" ::: "memory");
-            routed = true;
-            nu = __ldcg(a.nuniq);
-        }
-        int type, a0 = 0, tile = 0, ntok = a.T, K = a.H, per16 = 0;
+        int type, a0 = 0, tile = 0, ntok = a.T, K = a.H, per16 = 0, nu = 0;
         int pos[kDecodeT], tok[kDecodeT];
+#pragma unroll
         for (int i = 0; i < kDecodeT; i++)
             pos[i] = tok[i] = i < a.T ? i : 0;
-        if (j < js.nR) {
-            type = kJobR;
-            a0 = j;
-            per16 = 16 * (4 + 2 * a.T);
-        } else if (j == js.oSEL) {
+        if (j == 0) {
             type = kJobSel;
+        } else if (j < js.oSGU) {
+            type = kJobR;
+            a0 = (j - js.oR) * js.rows;
+            tile = a.E - a0 < js.rows ? a.E - a0 : js.rows; // rows of this job
+            per16 = 16 * (4 * tile + 2 * a.T);
         } else if (j < js.oSD) {
             type = kJobSgu;
             a0 = j - js.oSGU;
@@ -1008,21 +1177,28 @@ __device__ void producer(const DecodeArgs &a, DecodeSmem &sm, const JobSpace &js
             tile = (j - js.oD) % js.tilesD;
             K = a.I;
         }
+        int e = 0;
         if ((type == kJobGu || type == kJobD)) {
+            if (a0 != cached_slot) {
+                if (!wait_slot(a, a0, rec))
+                    break;
+                cached_slot = a0;
+            }
+            nu = rec.nuniq;
             if (a0 >= nu)
                 continue; // fewer distinct experts than the bound
-            const int p0 = __ldcg(a.uoff + a0), p1 = __ldcg(a.uoff + a0 + 1);
-            ntok = p1 - p0;
+            e = rec.e;
+            ntok = rec.ntok;
+#pragma unroll
             for (int i = 0; i < kDecodeT; i++) {
                 const int ii = i < ntok ? i : 0;
-                pos[i] = p0 + ii;
-                tok[i] = __ldcg(a.perm + p0 + ii) / a.K;
+                pos[i] = rec.p0 + ii;
+                tok[i] = (int)((rec.toks >> (3 * ii)) & 7u);
             }
             // two 2-bit tiles: 84/256 B per column per 16 rows = 5.25 B each; activations per
             // token: GU x' (2 B) + off/sum (0.5 B); D hi + lo (4 B) + off/sum (0.5 B)
             per16 = type == kJobGu ? 2 * 84 + ntok * 40 : 2 * 84 + ntok * 72;
         }
-        const int e = (type == kJobGu || type == kJobD) ? __ldcg(a.uexp + a0) : 0;
         const int W = type == kJobSel ? 0 : pick_w(K, per16);
         const int nsub = type == kJobSel ? 1 : K / W;
         for (int sub = 0; sub < nsub && ok; sub++) {
@@ -1049,7 +1225,9 @@ __device__ void producer(const DecodeArgs &a, DecodeSmem &sm, const JobSpace &js
             StageWriter sw(sm, slot);
             const int c0 = sub * W;
             if (type == kJobR) {
-                d.oq[0] = sw.put(a.router_w + (int64_t)a0 * a.H + c0, 4u * W);
+                d.oq[0] = (int)sw.off;
+                for (int r = 0; r < tile; r++)
+                    sw.put(a.router_w + (int64_t)(a0 + r) * a.H + c0, 4u * W);
                 d.act_pitch = 2 * W;
                 d.oact = (int)sw.off;
                 for (int t = 0; t < a.T; t++)
@@ -1129,10 +1307,13 @@ __device__ void producer(const DecodeArgs &a, DecodeSmem &sm, const JobSpace &js
                 break;
             }
         }
-        // the CTA that computes the routing takes no further job before it is
-        // published: a job queued behind the selection would wait for it
-        if (type == kJobSel && ok && !wait_counter(a, a.ctl + kCtlRoutingEpoch, a.epoch, true))
-            break;
+        // The selection's CTA takes no further job before the routing is
+        // published: a router row queued behind the selection would never run.
+        if (type == kJobSel && ok) {
+            if (!wait_slot(a, 0, rec))
+                break;
+            cached_slot = 0;
+        }
     }
     // end of this CTA's jobs
     int slot;
@@ -1295,27 +1476,36 @@ template <int TP> struct JobOps {
     }
 };
 
+// Dispatch on the job's padded token count; a kernel built for at most TPM
+// tokens per job holds only the variants it can meet (smaller code, fewer
+// registers for the small batches).
+template <int TPM>
 __device__ __forceinline__ void stage_tp(int tp, const DecodeArgs &a, const uint8_t *sl, const StageDesc &d,
                                          int warp, int lane, float (&out)[2][2][2]) {
-    switch (tp) {
-    case 1: JobOps<1>::stage(a, sl, d, warp, lane, out); break;
-    case 2: JobOps<2>::stage(a, sl, d, warp, lane, out); break;
-    case 4: JobOps<4>::stage(a, sl, d, warp, lane, out); break;
-    default: JobOps<8>::stage(a, sl, d, warp, lane, out); break;
-    }
+    if (TPM == 1 || tp == 1)
+        JobOps<1>::stage(a, sl, d, warp, lane, out);
+    else if (TPM == 2 || tp == 2)
+        JobOps<(TPM >= 2 ? 2 : 1)>::stage(a, sl, d, warp, lane, out);
+    else if (TPM == 4 || tp == 4)
+        JobOps<(TPM >= 4 ? 4 : 1)>::stage(a, sl, d, warp, lane, out);
+    else
+        JobOps<TPM>::stage(a, sl, d, warp, lane, out);
 }
 
+template <int TPM>
 __device__ __forceinline__ void finish_tp(int tp, const DecodeArgs &a, const JobSpace &js, DecodeSmem &sm,
                                           const StageDesc &d, int buf, int warp, int lane, float (&out)[2][2][2]) {
-    switch (tp) {
-    case 1: JobOps<1>::finish(a, js, sm, d, buf, warp, lane, out); break;
-    case 2: JobOps<2>::finish(a, js, sm, d, buf, warp, lane, out); break;
-    case 4: JobOps<4>::finish(a, js, sm, d, buf, warp, lane, out); break;
-    default: JobOps<8>::finish(a, js, sm, d, buf, warp, lane, out); break;
-    }
+    if (TPM == 1 || tp == 1)
+        JobOps<1>::finish(a, js, sm, d, buf, warp, lane, out);
+    else if (TPM == 2 || tp == 2)
+        JobOps<(TPM >= 2 ? 2 : 1)>::finish(a, js, sm, d, buf, warp, lane, out);
+    else if (TPM == 4 || tp == 4)
+        JobOps<(TPM >= 4 ? 4 : 1)>::finish(a, js, sm, d, buf, warp, lane, out);
+    else
+        JobOps<TPM>::finish(a, js, sm, d, buf, warp, lane, out);
 }
 
-__device__ void consumer(const DecodeArgs &a, DecodeSmem &sm, const JobSpace &js, int warp, int lane) {
+template <int TPM> __device__ void consumer(const DecodeArgs &a, DecodeSmem &sm, const JobSpace &js, int warp, int lane) {
     unsigned n = 0, jobs_done = 0;
     float out[2][2][2];
     bool alive = true; // false after a failed dependency wait: drain the ring without computing
@@ -1331,23 +1521,10 @@ __device__ void consumer(const DecodeArgs &a, DecodeSmem &sm, const JobSpace &js
 #pragma unroll
             for (int i = 0; i < 8; i++)
                 (&out[0][0][0])[i] = 0.f;
-            const unsigned *dep = nullptr;
-            unsigned target = 0;
-            if (type == kJobSel) {
-                dep = a.ctl + kCtlRouterDone;
-                target = (unsigned)js.nR;
-            }
             if (type == kJobSel && alive) {
                 if (threadIdx.x < kDecodeT * kMaxTopK)
                     (&sm.sel_idx[0][0])[threadIdx.x] = 0;
                 select_prepare(a, reinterpret_cast<float *>(sm.ring[slot]));
-                consumer_sync();
-            }
-            if (dep && alive) {
-                if (threadIdx.x == 0)
-                    sm.flag = wait_counter(a, dep, target, false);
-                consumer_sync();
-                alive = sm.flag != 0;
                 consumer_sync();
             }
         }
@@ -1355,40 +1532,40 @@ __device__ void consumer(const DecodeArgs &a, DecodeSmem &sm, const JobSpace &js
             if (type == kJobR)
                 router_stage(sm.ring[slot], d, a.T, warp, lane, out);
             else if (type != kJobSel)
-                stage_tp(d.tp, a, sm.ring[slot], d, warp, lane, out);
+                stage_tp<TPM>(d.tp, a, sm.ring[slot], d, warp, lane, out);
         }
         const bool last = d.sub == d.nsub - 1;
         if (last && alive) {
             if (type == kJobR) {
+                // logit of row d.a0 + r, token t: index 4 r + t of the accumulators
                 const int buf = (int)(jobs_done & 1u);
                 float *acc = &out[0][0][0];
 #pragma unroll
-                for (int t = 0; t < kDecodeT; t++) {
+                for (int i = 0; i < kDecodeT; i++) {
+                    const int t = d.tile == 2 ? (i & 3) : i; // row i >> 2 (two rows) or 0
                     if (t < a.T) {
-                        const float v = warp_sum(acc[t]);
+                        const float v = warp_sum(acc[i]);
                         if (lane == 0)
-                            sm.part[buf][warp][0][0][t] = v;
+                            sm.part[buf][warp][0][0][i] = v;
                     }
                 }
                 consumer_sync();
-                if (threadIdx.x < a.T) {
-                    float v = 0.f;
-                    for (int w = 0; w < kConsumerWarps; w++)
-                        v += sm.part[buf][w][0][0][threadIdx.x];
-                    a.logits[threadIdx.x * a.E + d.a0] = v;
+                {
+                    const int i = threadIdx.x, r = d.tile == 2 ? i >> 2 : 0, t = d.tile == 2 ? (i & 3) : i;
+                    if (i < kDecodeT && t < a.T) {
+                        float v = 0.f;
+                        for (int w = 0; w < kConsumerWarps; w++)
+                            v += sm.part[buf][w][0][0][i];
+                        // the epoch in the same word marks the value as this launch's
+                        st_relaxed_u64(a.lgt + t * a.E + d.a0 + r,
+                                       (unsigned long long)a.epoch << 32 | __float_as_uint(v));
+                    }
                 }
-                consumer_sync();
-                signal(a, a.ctl + kCtlRouterDone);
             } else if (type == kJobSel) {
-                job_select(a, sm, reinterpret_cast<float *>(sm.ring[slot]), warp, lane);
-                consumer_sync();
-                if (threadIdx.x == 0) {
-                    __threadfence();
-                    st_release(a.ctl + kCtlRoutingEpoch, a.epoch);
-                }
+                alive = job_select(a, a.io, sm, reinterpret_cast<float *>(sm.ring[slot]), warp, lane);
             } else {
                 const int buf = (int)(jobs_done & 1u);
-                finish_tp(d.tp, a, js, sm, d, buf, warp, lane, out);
+                finish_tp<TPM>(d.tp, a, js, sm, d, buf, warp, lane, out);
             }
             jobs_done++;
         }
@@ -1399,7 +1576,8 @@ __device__ void consumer(const DecodeArgs &a, DecodeSmem &sm, const JobSpace &js
     }
 }
 
-__global__ void __launch_bounds__(kDecodeThreads, 2) decode_fused_kernel(DecodeArgs a) {
+// TPM: the largest padded token count of a job in this launch (1, 2, 4 or 8).
+template <int TPM> __global__ void __launch_bounds__(kDecodeThreads, 2) decode_fused_kernel(DecodeArgs a) {
     extern __shared__ __align__(128) uint8_t dsmem[];
     DecodeSmem &sm = *reinterpret_cast<DecodeSmem *>(dsmem);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -1416,7 +1594,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_fused_kernel(DecodeA
         if (lane == 0)
             producer(a, sm, js);
     } else {
-        consumer(a, sm, js, warp, lane);
+        consumer<TPM>(a, sm, js, warp, lane);
     }
     // the last CTA out resets the counters for the next launch
     __syncthreads();
@@ -1427,7 +1605,6 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_fused_kernel(DecodeA
             __threadfence();
             if (!ld_acquire(a.ctl + kCtlAbort)) {
                 a.ctl[kCtlJobNext] = 0;
-                a.ctl[kCtlRouterDone] = 0;
                 a.ctl[kCtlSguDone] = 0;
                 a.ctl[kCtlSdDone] = 0;
                 for (int s = 0; s < kMaxSlots; s++)

@@ -86,8 +86,9 @@ struct Profiler {
 struct DecodeState {
     Q2Frag gate, up, down;
     Q8Frag sh_gate, sh_up, sh_down;
-    float *logits = nullptr, *gap = nullptr;
-    int32_t *counts = nullptr, *nuniq = nullptr, *uexp = nullptr, *uoff = nullptr, *perm = nullptr, *inv = nullptr;
+    unsigned long long *lgt = nullptr, *srec = nullptr; // epoch-tagged logits and routing records
+    float *gap = nullptr;
+    int32_t *counts = nullptr, *nuniq = nullptr, *inv = nullptr;
     uint16_t *xq = nullptr;
     float *xoff = nullptr, *xsum = nullptr;
     uint16_t *hq_hi = nullptr, *hq_lo = nullptr;
@@ -333,13 +334,11 @@ void layout_scratch(ds4moe *h, Carver &c) {
     S.ystage = c.take<float>(T * L.H);
     DecodeState &D = h->D;
     const int64_t Td = kDecodeT, Pd = (int64_t)kDecodeT * L.K;
-    D.logits = c.take<float>(Td * L.E);
+    D.lgt = c.take<unsigned long long>(Td * L.E);
+    D.srec = c.take<unsigned long long>(2 * kMaxSlots);
     D.gap = c.take<float>(Td);
     D.counts = c.take<int32_t>(L.E);
     D.nuniq = c.take<int32_t>(1);
-    D.uexp = c.take<int32_t>(kMaxSlots);
-    D.uoff = c.take<int32_t>(kMaxSlots + 1);
-    D.perm = c.take<int32_t>(Pd);
     D.inv = c.take<int32_t>(Pd);
     D.xq = c.take<uint16_t>(Td * L.H);
     D.xoff = c.take<float>(Td * (L.H / 16));
@@ -619,15 +618,13 @@ int run_decode(ds4moe *h, const void *x, int T, float *y, const int32_t *forced_
         a.epoch = ++D.epoch;
         if (a.epoch == 0)
             a.epoch = ++D.epoch;
-        a.logits = D.logits;
+        a.lgt = D.lgt;
+        a.srec = D.srec;
         a.idx = S.idx + (int64_t)t0 * L.K;
         a.w = S.w + (int64_t)t0 * L.K;
         a.gap = S.gap + t0;
         a.counts = D.counts;
         a.nuniq = D.nuniq;
-        a.uexp = D.uexp;
-        a.uoff = D.uoff;
-        a.perm = D.perm;
         a.inv = D.inv;
         a.xq = D.xq;
         a.xoff = D.xoff;
@@ -642,10 +639,14 @@ int run_decode(ds4moe *h, const void *x, int T, float *y, const int32_t *forced_
         a.ysh = D.ysh;
         a.ctl = D.ctl;
         a.status = h->status;
+        a.io = SelIO{a.lgt, a.epoch, a.idx, a.w, a.gap, a.inv, a.counts, a.nuniq, a.srec};
         void *args[] = {&a};
         launch(h, "decode_fused", [&] {
-            cudaLaunchCooperativeKernel((const void *)decode_fused_kernel, dim3(D.grid), dim3(kDecodeThreads), args,
-                                        sizeof(DecodeSmem), h->stream);
+            const void *fn = Tc <= 1   ? (const void *)decode_fused_kernel<1>
+                             : Tc <= 2 ? (const void *)decode_fused_kernel<2>
+                             : Tc <= 4 ? (const void *)decode_fused_kernel<4>
+                                       : (const void *)decode_fused_kernel<8>;
+            cudaLaunchCooperativeKernel(fn, dim3(D.grid), dim3(kDecodeThreads), args, sizeof(DecodeSmem), h->stream);
         });
         int rc = launch_rc();
         if (rc)
@@ -830,9 +831,15 @@ int ds4moe_create(const ds4moe_layer_desc *desc, const ds4moe_weights *w, ds4moe
         rf8(w->sh_down, D.sh_down);
     }
     cudaMemsetAsync(D.ctl, 0, sizeof(unsigned) * D.ctl_words, st);
+    // no stale word may carry a future launch's epoch (epochs start at 1)
+    cudaMemsetAsync(D.lgt, 0, sizeof(unsigned long long) * kDecodeT * L.E, st);
+    cudaMemsetAsync(D.srec, 0, sizeof(unsigned long long) * 2 * kMaxSlots, st);
     int per_sm = 0, nsm = 0;
-    cudaFuncSetAttribute(decode_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(DecodeSmem));
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_fused_kernel, kDecodeThreads, sizeof(DecodeSmem));
+    for (const void *fn : {(const void *)decode_fused_kernel<1>, (const void *)decode_fused_kernel<2>,
+                           (const void *)decode_fused_kernel<4>, (const void *)decode_fused_kernel<8>})
+        cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(DecodeSmem));
+    // every variant has the same threads and shared memory and the same launch bound of two CTAs per SM
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_fused_kernel<8>, kDecodeThreads, sizeof(DecodeSmem));
     cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
     D.grid = per_sm * nsm;
     g_pf_grid = nsm;
