@@ -1,9 +1,10 @@
 // Decode path (T <= 8 tokens per launch): one persistent cooperative kernel.
 //
-// Each CTA is one producer warp and eight consumer warps. The producer's lane
-// 0 pulls jobs from a global queue (an atomic counter) and streams each job's
+// Each CTA is one producer warp and eight consumer warps. The producer warp
+// pulls jobs from a global queue (an atomic counter) and streams each job's
 // weight tiles and activation rows into a ring of shared-memory stages with
-// bulk asynchronous copies (cp.async.bulk completing on an mbarrier); the
+// bulk asynchronous copies (cp.async.bulk completing on an mbarrier; its lanes
+// issue a stage's copies side by side); the
 // consumer warps multiply them on the tensor cores (mma.sync, see the layouts
 // in frag_layout.cuh) and release the stage. Two CTAs per SM, each with two
 // 42 KB stages, keep up to 168 KB per SM in flight, independent of registers.
@@ -139,7 +140,7 @@ struct DecodeSmem {
     alignas(8) uint64_t full[kRing];
     alignas(8) uint64_t empty[kRing];
     float part[2][kConsumerWarps][2][16][kDecodeT]; // per-warp partial sums, double-buffered by job
-    int flag;
+    int combine[2]; // D jobs: whether this CTA combines the tile (double-buffered by job)
     int sel_idx[kDecodeT][kMaxTopK];
     unsigned bitmap[32];
     int word_prefix[32];
@@ -1032,7 +1033,7 @@ __device__ __forceinline__ int pick_w(int K, int per_col_x16) {
     return 256;
 }
 
-// ---- producer (lane 0 of the last warp) --------------------------------------------
+// ---- producer (the last warp, all lanes in lockstep) ------------------------------------
 
 // Lays out one stage: put() places a piece that the bulk copies bring in;
 // reserve() only sets space aside for a piece the consumers fill themselves
@@ -1073,17 +1074,25 @@ struct StageWriter {
     // Expect every byte, copy the weights, then (if the stage has dependent
     // pieces) wait for *dep >= target and copy the rest. Returns false if the
     // wait gave up; the stage is then never completed and the consumers drain.
+    // Run by the whole producer warp in lockstep (every lane built the same
+    // piece list): lane 0 arrives, and lane i issues piece i, so one warp
+    // instruction issues up to 32 copies.
     __device__ bool issue(const DecodeArgs &a, const unsigned *dep, unsigned target) {
+        const int lane = threadIdx.x & 31;
         uint64_t *bar = &sm.full[slot];
-        if (overflow)
+        __syncwarp(); // every lane's writes of the stage description precede the arrival
+        if (overflow && lane == 0)
             atomicOr(a.status, kErrInternal);
         if (tx == 0) {
-            mbar_arrive(bar);
+            if (lane == 0)
+                mbar_arrive(bar);
             return true;
         }
-        mbar_arrive_tx(bar, tx);
+        if (lane == 0)
+            mbar_arrive_tx(bar, tx);
+        __syncwarp();
         const int split = nindep < 0 ? np : nindep;
-        for (int i = 0; i < split; i++)
+        for (int i = lane; i < split; i += 32)
             bulk_g2s(sm.ring[slot] + dst[i], src[i], bytes[i], bar);
         if (split < np) {
             if (dep && !wait_counter(a, dep, target, false))
@@ -1091,7 +1100,8 @@ struct StageWriter {
             // the data was written through the generic proxy by other CTAs; the
             // bulk copies read it through the async proxy
             asm volatile("fence.proxy.async.global;" ::: "memory");
-            for (int i = split; i < np; i++)
+            __syncwarp();
+            for (int i = split + lane; i < np; i += 32)
                 bulk_g2s(sm.ring[slot] + dst[i], src[i], bytes[i], bar);
         }
         return true;
@@ -1137,15 +1147,25 @@ __device__ void producer(const DecodeArgs &a, DecodeSmem &sm, const JobSpace &js
         return mbar_wait(a, &sm.empty[slot], ((n / kRing) & 1u) ^ 1u);
     };
     bool ok = true;
-    bool first = true;
+    // the first job of each CTA is its own index; later ones come from the queue,
+    // claimed one job ahead so that the atomic's round trip overlaps this job's work
+    // (the whole warp runs this loop; lane 0 takes the job and all lanes get it)
+    auto next_job = [&]() -> int {
+        int v = 0;
+        if ((threadIdx.x & 31) == 0)
+            v = ld_relaxed(a.ctl + kCtlAbort) ? js.total
+                                               : (int)gridDim.x + (int)atomicAdd(a.ctl + kCtlJobNext, 1u);
+        return __shfl_sync(0xFFFFFFFFu, v, 0);
+    };
+    int j_next = (int)blockIdx.x;
     while (ok) {
-        // the first job of each CTA is its own index; later ones come from the queue
-        const int j = first ? (int)blockIdx.x
-                            : (ld_relaxed(a.ctl + kCtlAbort) ? js.total
-                                                             : (int)gridDim.x + (int)atomicAdd(a.ctl + kCtlJobNext, 1u));
-        first = false;
+        const int j = j_next;
         if (j >= js.total)
             break;
+        // (not during the selection: the job claimed would wait behind it, and a
+        // router row there would never run)
+        if (j != 0)
+            j_next = next_job();
         int type, a0 = 0, tile = 0, ntok = a.T, K = a.H, per16 = 0, nu = 0;
         int pos[kDecodeT], tok[kDecodeT];
 #pragma unroll
@@ -1313,43 +1333,66 @@ __device__ void producer(const DecodeArgs &a, DecodeSmem &sm, const JobSpace &js
             if (!wait_slot(a, 0, rec))
                 break;
             cached_slot = 0;
+            j_next = next_job();
         }
     }
     // end of this CTA's jobs
     int slot;
     if (claim(slot)) {
-        sm.desc[slot].type = kJobEnd;
-        mbar_arrive(&sm.full[slot]);
+        __syncwarp();
+        if ((threadIdx.x & 31) == 0) {
+            sm.desc[slot].type = kJobEnd;
+            mbar_arrive(&sm.full[slot]);
+        }
     }
 }
 
 // ---- consumers (warps 0..7) ----------------------------------------------------------
 
 // y for 32 rows (tile ti) and all tokens, in fixed order: sum over k, then
-// shared. Warp 0 of the consumers.
-__device__ void combine_tile(const DecodeArgs &a, int ti, int lane) {
-    for (int q = lane; q < 32 * a.T; q += 32) {
-        const int r = q & 31, t = q >> 5;
-        const int col = ti * 32 + r;
-        float v = 0.f;
-        for (int k = 0; k < a.K; k++)
-            v = fmaf(__ldcg(a.w + t * a.K + k), __ldcg(a.ye + (int64_t)__ldcg(a.inv + t * a.K + k) * a.H + col), v);
-        if (a.Ish > 0)
-            v += __ldcg(a.ysh + (int64_t)t * a.H + col);
-        a.y[(int64_t)t * a.H + col] = v;
+// shared. All consumer threads, one (token, row) each; the routing loads of a
+// thread are issued together, then its expert outputs. Not inlined, and given
+// plain values: it runs once per tile and its registers stay out of the hot
+// loops' budget.
+__device__ __noinline__ void combine_tile(const float *w, const int32_t *inv, const float *yes, const float *ysh,
+                                          float *y, int T, int K, int H, int ti) {
+    const int q = threadIdx.x, r = q & 31, t = q >> 5;
+    if (t >= T)
+        return;
+    const int col = ti * 32 + r;
+    float wk[kMaxTopK];
+    int pk[kMaxTopK];
+#pragma unroll
+    for (int k = 0; k < kMaxTopK; k++) {
+        if (k < K) {
+            wk[k] = __ldcg(w + t * K + k);
+            pk[k] = __ldcg(inv + t * K + k);
+        }
     }
+    float ye[kMaxTopK];
+#pragma unroll
+    for (int k = 0; k < kMaxTopK; k++)
+        if (k < K)
+            ye[k] = __ldcg(yes + (int64_t)pk[k] * H + col);
+    const float sh = ysh ? __ldcg(ysh + (int64_t)t * H + col) : 0.f;
+    float v = 0.f;
+#pragma unroll
+    for (int k = 0; k < kMaxTopK; k++)
+        if (k < K)
+            v = fmaf(wk[k], ye[k], v);
+    if (ysh)
+        v += sh;
+    y[(int64_t)t * H + col] = v;
 }
 
-// After the consumers' barrier that follows a D job's result writes: warp 0
+// After the consumers' barrier that follows a D job's result writes: thread 0
 // counts the contribution to the 32-row tile ti; the last of the nuniq
-// contributions combines the tile, once the shared expert's down rows are
-// complete (those jobs precede every D job in the queue, so the wait ends).
-// The other warps go on with the next job.
-__device__ void arrive_tile(const DecodeArgs &a, const JobSpace &js, int ti, int nuniq, int warp, int lane) {
-    if (warp != 0)
-        return;
-    unsigned last = 0;
-    if (lane == 0) {
+// contributions combines the tile (all consumer threads, after a second
+// barrier), once the shared expert's down rows are complete (those jobs
+// precede every D job in the queue, so the wait ends).
+__device__ void arrive_tile(const DecodeArgs &a, const JobSpace &js, DecodeSmem &sm, int buf, int ti, int nuniq) {
+    if (threadIdx.x == 0) {
+        unsigned last = 0;
         __threadfence();
         const unsigned old = atomicAdd(a.ctl + kCtlTileCnt + ti, 1u);
         last = old + 1 == (unsigned)nuniq;
@@ -1359,9 +1402,11 @@ __device__ void arrive_tile(const DecodeArgs &a, const JobSpace &js, int ti, int
             if (js.nSD > 0 && !wait_counter(a, a.ctl + kCtlSdDone, (unsigned)js.nSD, false))
                 last = 0;
         }
+        sm.combine[buf] = (int)last;
     }
-    if (__shfl_sync(0xFFFFFFFFu, last, 0))
-        combine_tile(a, ti, lane);
+    consumer_sync();
+    if (sm.combine[buf])
+        combine_tile(a.w, a.inv, a.ye, a.Ish > 0 ? a.ysh : nullptr, a.y, a.T, a.K, a.H, ti);
 }
 
 // After the consumers' barrier that follows the job's result writes: thread 0
@@ -1471,7 +1516,7 @@ template <int TP> struct JobOps {
                 }
             }
             consumer_sync();
-            arrive_tile(a, js, d.tile, d.nuniq, warp, lane);
+            arrive_tile(a, js, sm, buf, d.tile, d.nuniq);
         }
     }
 };
@@ -1591,8 +1636,7 @@ template <int TPM> __global__ void __launch_bounds__(kDecodeThreads, 2) decode_f
     __syncthreads();
     const JobSpace js = job_space(a);
     if (warp == kConsumerWarps) {
-        if (lane == 0)
-            producer(a, sm, js);
+        producer(a, sm, js);
     } else {
         consumer<TPM>(a, sm, js, warp, lane);
     }
