@@ -15,6 +15,9 @@
 // always run: the queue cannot deadlock as long as all CTAs are resident,
 // which the cooperative launch guarantees. The queue, in order:
 //
+//   REH  a rehearsal of the selection on dummy logits (CTA 1's first job):
+//        the selection runs once per launch through code that starts out of
+//        every cache; the rehearsal fetches it into L2 before the real one needs it
 //   SEL  one job, the first job of CTA 0: activation pre-scaling for the
 //        2-bit MMA; then, as the router rows arrive, per-token sigmoid, exact
 //        top-k, weights and the distinct-expert grouping; publishes one
@@ -23,15 +26,15 @@
 //        with the launch's epoch in the same 64-bit word (the value is its
 //        own completion flag)
 //   SGU  shared expert, one 16-row tile of gate and up: h_sh = silu(g) * u
-//   SD   shared expert down, one 16-row tile of H (waits: all SGU)
 //   GU   (distinct expert, 16-row tile of I): gate and up, h = silu(g) * u,
 //        stored as a bf16 hi/lo pair pre-scaled for the down MMA
+//   SD   shared expert down, one 16-row tile of H (waits: all SGU)
 //   D    (distinct expert, 32-row tile of H): down projection (waits: that
 //        expert's GU tiles); the last of the experts' contributions to a tile
 //        combines it once all SD jobs are done: y = sum_k w_k ye_k + ysh, in
 //        fixed order
-// The shared expert's jobs sit between the selection and the routed jobs so
-// that they stream while the routing is computed and published.
+// The shared expert's gate/up jobs sit between the router and the routed jobs
+// so that they stream while the routing is computed and published.
 // The producer of a GU or D job polls that expert's routing record (epoch-
 // tagged, so the poll and the lookup are one load) and then issues the
 // weight copies; the weight loads of a job never wait for its data
@@ -113,7 +116,8 @@ struct DecodeArgs {
     float *ysh;              // [8][H]
     unsigned *ctl;
     unsigned *status;
-    SelIO io; // the selection's inputs and outputs (the buffers above)
+    SelIO io;  // the selection's inputs and outputs (the buffers above)
+    SelIO dry; // the rehearsal's: zeroed logits with epoch 0, outputs nothing reads
 };
 
 enum JobType : int { kJobEnd = 0, kJobR, kJobSgu, kJobSel, kJobGu, kJobSd, kJobD };
@@ -990,15 +994,17 @@ __device__ __forceinline__ bool job_select(const DecodeArgs &a, const SelIO &io,
 
 struct JobSpace {
     int nR, rows, nSGU, nSD, tilesI, tilesD, Umax;
-    int oR, oSGU, oSD, oGU, oD, total;
+    int nREH, oR, oSGU, oSD, oGU, oD, total;
 };
 
-// Job order: SEL, R, SGU, SD, GU, D. The selection is CTA 0's first job, so
-// its consumers are idle and waiting when the last router row lands; the
-// router rows are the first jobs of the next CTAs (two rows per job while
-// both rows' accumulators fit, so that the router is one round of jobs);
-// the shared expert's jobs follow, so that they fill the time in which the
-// routing is computed and published.
+// Job order: SEL, REH, R, SGU, GU, SD, D. The selection is CTA 0's first
+// job, so its consumers are idle and waiting when the last router row lands;
+// the router rows are the first jobs of the next CTAs (two rows per job while
+// both rows' accumulators fit, so that the router is one round of jobs); the
+// shared expert's gate/up jobs follow, so that they fill the time in which
+// the routing is computed and published. The shared down jobs wait for all of
+// those: placed after the routed gate/up jobs they find them done, instead of
+// holding CTAs that the routed experts need the moment the routing lands.
 __host__ __device__ __forceinline__ JobSpace job_space(int E, int I, int H, int Ish, int T, int K, bool forced) {
     JobSpace s;
     s.rows = T <= 4 ? 2 : 1; // router rows per job: rows * T accumulators per lane (<= 8)
@@ -1008,11 +1014,12 @@ __host__ __device__ __forceinline__ JobSpace job_space(int E, int I, int H, int 
     s.tilesI = I / 16; // GU: one 16-row tile of gate and up
     s.tilesD = H / 32; // D: two 16-row tiles of down
     s.Umax = (T * K < E) ? T * K : E;
-    s.oR = 1;
+    s.nREH = forced ? 0 : 1; // job 1: the selection rehearsal
+    s.oR = 1 + s.nREH;
     s.oSGU = s.oR + s.nR;
-    s.oSD = s.oSGU + s.nSGU;
-    s.oGU = s.oSD + s.nSD;
-    s.oD = s.oGU + s.Umax * s.tilesI;
+    s.oGU = s.oSGU + s.nSGU;
+    s.oSD = s.oGU + s.Umax * s.tilesI;
+    s.oD = s.oSD + s.nSD;
     s.total = s.oD + s.Umax * s.tilesD;
     return s;
 }
@@ -1173,24 +1180,27 @@ __device__ void producer(const DecodeArgs &a, DecodeSmem &sm, const JobSpace &js
             pos[i] = tok[i] = i < a.T ? i : 0;
         if (j == 0) {
             type = kJobSel;
+        } else if (j < js.oR) {
+            type = kJobSel; // the rehearsal: same job, dummy logits and outputs
+            a0 = 1;
         } else if (j < js.oSGU) {
             type = kJobR;
             a0 = (j - js.oR) * js.rows;
             tile = a.E - a0 < js.rows ? a.E - a0 : js.rows; // rows of this job
             per16 = 16 * (4 * tile + 2 * a.T);
-        } else if (j < js.oSD) {
+        } else if (j < js.oGU) {
             type = kJobSgu;
             a0 = j - js.oSGU;
             per16 = 2 * 16 * 17 + 16 * 2 * a.T; // two 8-bit tiles (17/16 B per column each) + bf16 x rows
-        } else if (j < js.oGU) {
+        } else if (j < js.oSD) {
+            type = kJobGu;
+            a0 = (j - js.oGU) / js.tilesI;
+            tile = (j - js.oGU) % js.tilesI;
+        } else if (j < js.oD) {
             type = kJobSd;
             a0 = j - js.oSD;
             K = a.Ish;
             per16 = 16 * 17 + 16 * 4 * a.T; // one 8-bit tile + binary16 hi and lo rows
-        } else if (j < js.oD) {
-            type = kJobGu;
-            a0 = (j - js.oGU) / js.tilesI;
-            tile = (j - js.oGU) % js.tilesI;
         } else {
             type = kJobD;
             a0 = (j - js.oD) / js.tilesD;
@@ -1329,7 +1339,7 @@ __device__ void producer(const DecodeArgs &a, DecodeSmem &sm, const JobSpace &js
         }
         // The selection's CTA takes no further job before the routing is
         // published: a router row queued behind the selection would never run.
-        if (type == kJobSel && ok) {
+        if (type == kJobSel && a0 == 0 && ok) {
             if (!wait_slot(a, 0, rec))
                 break;
             cached_slot = 0;
@@ -1569,7 +1579,8 @@ template <int TPM> __device__ void consumer(const DecodeArgs &a, DecodeSmem &sm,
             if (type == kJobSel && alive) {
                 if (threadIdx.x < kDecodeT * kMaxTopK)
                     (&sm.sel_idx[0][0])[threadIdx.x] = 0;
-                select_prepare(a, reinterpret_cast<float *>(sm.ring[slot]));
+                if (d.a0 == 0)
+                    select_prepare(a, reinterpret_cast<float *>(sm.ring[slot]));
                 consumer_sync();
             }
         }
@@ -1607,7 +1618,11 @@ template <int TPM> __device__ void consumer(const DecodeArgs &a, DecodeSmem &sm,
                     }
                 }
             } else if (type == kJobSel) {
-                alive = job_select(a, a.io, sm, reinterpret_cast<float *>(sm.ring[slot]), warp, lane);
+                // one call site for the selection and its rehearsal: the same code
+                const SelIO io = d.a0 ? a.dry : a.io;
+                const bool ok = job_select(a, io, sm, reinterpret_cast<float *>(sm.ring[slot]), warp, lane);
+                if (d.a0 == 0)
+                    alive = ok;
             } else {
                 const int buf = (int)(jobs_done & 1u);
                 finish_tp<TPM>(d.tp, a, js, sm, d, buf, warp, lane, out);
