@@ -1,6 +1,9 @@
 // Decode path (T <= 8 tokens per launch): one persistent cooperative kernel.
 //
-// Each CTA is one producer warp and eight consumer warps. The producer warp
+// Each CTA is a producer warp, eight consumer warps and a publisher warp. The
+// consumers hand each finished job to the publisher, which makes it visible
+// GPU-wide (a release on the job's count, the output-tile arrivals and
+// combines), so that no GPU-scope fence or atomic stalls the math. The producer warp
 // pulls jobs from a global queue (an atomic counter) and streams each job's
 // weight tiles and activation rows into a ring of shared-memory stages with
 // bulk asynchronous copies (cp.async.bulk completing on an mbarrier; its lanes
@@ -66,7 +69,9 @@ constexpr int kSlotBytes = 43008;       // bytes per stage (fewer, larger stages
 constexpr int kConsumerWarps = 8;
 // the selection job's keys ([T][E]) and bias ([E]) fit its stage buffer (E <= 1024)
 static_assert(4 * (kDecodeT + 1) * 1024 <= kSlotBytes, "selection scratch");
-constexpr int kDecodeThreads = 32 * (kConsumerWarps + 1);
+constexpr int kPubQ = 4; // publication tasks in flight (consumers -> publisher warp)
+// consumers, the producer warp and the publisher warp
+constexpr int kDecodeThreads = 32 * (kConsumerWarps + 2);
 
 // Control words (zeroed at create; every launch leaves them zeroed again).
 enum : int {
@@ -121,6 +126,7 @@ struct DecodeArgs {
 };
 
 enum JobType : int { kJobEnd = 0, kJobR, kJobSgu, kJobSel, kJobGu, kJobSd, kJobD };
+enum PubKind : int { kPubSignal = 0, kPubTile, kPubEnd };
 
 // What the producer tells the consumers about one stage.
 struct StageDesc {
@@ -133,7 +139,7 @@ struct StageDesc {
     int nuniq;      // distinct experts of this launch (GU, SD, D)
     int pos[kDecodeT]; // pair position of each token column (GU, D outputs)
     int tok[kDecodeT]; // token of each column
-    int oq[2], os[2], od[2]; // byte offsets of the matrix pieces (codes, scales, d/dmin)
+    int oq[2];      // byte offsets of the matrix pieces (runs of records, frag_layout.cuh)
     int oact, olo, ooff, osum; // activation pieces
     int act_pitch, sub_pitch;  // bytes per token row of the hi/lo and off/sum pieces
 };
@@ -144,7 +150,16 @@ struct DecodeSmem {
     alignas(8) uint64_t full[kRing];
     alignas(8) uint64_t empty[kRing];
     float part[2][kConsumerWarps][2][16][kDecodeT]; // per-warp partial sums, double-buffered by job
-    int combine[2]; // D jobs: whether this CTA combines the tile (double-buffered by job)
+    // publication tasks: what the publisher warp makes visible GPU-wide after a job
+    struct PubTask {
+        unsigned *ctr; // the job count to increase, or the tile counter
+        int kind;      // kPubSignal, kPubTile, kPubEnd
+        int tile, nuniq;
+    } pub[kPubQ];
+    float cw[kDecodeT * kMaxTopK];   // publisher: routing weights of the tile being combined
+    int cinv[kDecodeT * kMaxTopK];   // and the positions of their pairs
+    alignas(8) uint64_t pub_full[kPubQ];
+    alignas(8) uint64_t pub_empty[kPubQ];
     int sel_idx[kDecodeT][kMaxTopK];
     unsigned bitmap[32];
     int word_prefix[32];
@@ -264,17 +279,15 @@ __device__ __forceinline__ unsigned ld_relaxed(const unsigned *p) {
     return v;
 }
 
-// One thread waits until *p >= target (or == target when eq): relaxed polls
-// with a short sleep between them, one acquire fence once the value is seen.
-// Returns false after kWaitNs or when another CTA aborted.
+// Waits until *p >= target (or == target when eq): acquire polls with a
+// short sleep between them. Returns false after kWaitNs or when another CTA
+// aborted.
 __device__ bool wait_counter(const DecodeArgs &a, const unsigned *p, unsigned target, bool eq) {
     uint64_t t0 = 0;
     for (unsigned it = 0;; it++) {
-        const unsigned v = ld_relaxed(p);
-        if (eq ? v == target : v >= target) {
-            __threadfence();
+        const unsigned v = ld_acquire(p);
+        if (eq ? v == target : v >= target)
             return true;
-        }
         if ((it & 63) == 0) {
             if (ld_relaxed(a.ctl + kCtlAbort))
                 return false;
@@ -410,8 +423,9 @@ __device__ __forceinline__ void q2_stage(const uint8_t *sl, const StageDesc &d, 
         uint4 q[NMAT], s[NMAT];
 #pragma unroll
         for (int m = 0; m < NMAT; m++) {
-            q[m] = reinterpret_cast<const uint4 *>(sl + d.oq[m])[kc * 32 + lane];
-            s[m] = reinterpret_cast<const uint4 *>(sl + d.os[m])[kc * 8 + g];
+            const uint8_t *rb = sl + d.oq[m] + (kc >> 1) * kQ2Rec; // the block's record
+            q[m] = reinterpret_cast<const uint4 *>(rb + (kc & 1) * 512)[lane];
+            s[m] = reinterpret_cast<const uint4 *>(rb + kQ2RecScales + (kc & 1) * 128)[g];
         }
         const int colbase = kc * 128 + 2 * tig; // column within the stage
 #pragma unroll
@@ -485,7 +499,7 @@ __device__ __forceinline__ void q2_stage(const uint8_t *sl, const StageDesc &d, 
         if ((kc & 1) == 1 || kc + 1 == ke) {
 #pragma unroll
             for (int m = 0; m < NMAT; m++) {
-                const uint2 dw = reinterpret_cast<const uint2 *>(sl + d.od[m])[(kc >> 1) * 8 + g];
+                const uint2 dw = reinterpret_cast<const uint2 *>(sl + d.oq[m] + (kc >> 1) * kQ2Rec + kQ2RecDm)[g];
                 const float dg = f16_to_f32(dw.x), mg = f16_to_f32(dw.x >> 16);
                 const float dg8 = f16_to_f32(dw.y), mg8 = f16_to_f32(dw.y >> 16);
 #pragma unroll
@@ -528,7 +542,7 @@ __device__ __forceinline__ void q8_stage(const uint8_t *sl, const StageDesc &d, 
                 uint4 q[NMAT];
 #pragma unroll
                 for (int m = 0; m < NMAT; m++)
-                    q[m] = reinterpret_cast<const uint4 *>(sl + d.oq[m])[bq * 32 + lane];
+                    q[m] = reinterpret_cast<const uint4 *>(sl + d.oq[m] + bq * kQ8Rec)[lane];
                 const bool on = bs == sl2;
 #pragma unroll
                 for (int c = 0; c < 2; c++) {
@@ -568,14 +582,14 @@ __device__ __forceinline__ void q8_stage(const uint8_t *sl, const StageDesc &d, 
         const int bqa = base + s0, bqb = base + s1;
 #pragma unroll
         for (int m = 0; m < NMAT; m++) {
-            const uint32_t *dv = reinterpret_cast<const uint32_t *>(sl + d.od[m]);
+            const uint8_t *rm = sl + d.oq[m] + kQ8RecD; // scale entries of block 0's record
             if (bqa < be) {
-                const uint32_t dw = dv[bqa * 8 + g];
+                const uint32_t dw = reinterpret_cast<const uint32_t *>(rm + bqa * kQ8Rec)[g];
                 out[m][0][0] = fmaf(f16_to_f32(dw), D[m][0], out[m][0][0]);
                 out[m][1][0] = fmaf(f16_to_f32(dw >> 16), D[m][2], out[m][1][0]);
             }
             if (bqb < be) {
-                const uint32_t dw = dv[bqb * 8 + g];
+                const uint32_t dw = reinterpret_cast<const uint32_t *>(rm + bqb * kQ8Rec)[g];
                 out[m][0][1] = fmaf(f16_to_f32(dw), D[m][1], out[m][0][1]);
                 out[m][1][1] = fmaf(f16_to_f32(dw >> 16), D[m][3], out[m][1][1]);
             }
@@ -1169,9 +1183,9 @@ __device__ void producer(const DecodeArgs &a, DecodeSmem &sm, const JobSpace &js
         const int j = j_next;
         if (j >= js.total)
             break;
-        // (not during the selection: the job claimed would wait behind it, and a
-        // router row there would never run)
-        if (j != 0)
+        // (not during the selection or its rehearsal: the job claimed would wait
+        // behind them, and a router row behind the selection would never run)
+        if (j >= js.oR)
             j_next = next_job();
         int type, a0 = 0, tile = 0, ntok = a.T, K = a.H, per16 = 0, nu = 0;
         int pos[kDecodeT], tok[kDecodeT];
@@ -1266,8 +1280,7 @@ __device__ void producer(const DecodeArgs &a, DecodeSmem &sm, const JobSpace &js
                 const Q8Frag *M[2] = {&a.sh_gate, &a.sh_up};
                 for (int m = 0; m < 2; m++) {
                     const int64_t u = (int64_t)a0 * M[m]->nbq + c0 / 32;
-                    d.oq[m] = sw.put(M[m]->qs + u * 32, (unsigned)(W / 32) * 512u);
-                    d.od[m] = sw.put(M[m]->d + u * 8, (unsigned)(W / 32) * 32u);
+                    d.oq[m] = sw.put(M[m]->rec + u * kQ8Rec, (unsigned)(W / 32) * kQ8Rec);
                 }
                 d.act_pitch = 2 * W;
                 d.oact = (int)sw.off;
@@ -1275,8 +1288,7 @@ __device__ void producer(const DecodeArgs &a, DecodeSmem &sm, const JobSpace &js
                     sw.put(a.x + (int64_t)t * a.H + c0, 2u * W);
             } else if (type == kJobSd) {
                 const int64_t u = (int64_t)a0 * a.sh_down.nbq + c0 / 32;
-                d.oq[0] = sw.put(a.sh_down.qs + u * 32, (unsigned)(W / 32) * 512u);
-                d.od[0] = sw.put(a.sh_down.d + u * 8, (unsigned)(W / 32) * 32u);
+                d.oq[0] = sw.put(a.sh_down.rec + u * kQ8Rec, (unsigned)(W / 32) * kQ8Rec);
                 d.act_pitch = 2 * W;
                 sw.dependent_from_here(); // h of the shared expert: written by the SGU jobs
                 d.oact = (int)sw.off;
@@ -1291,10 +1303,8 @@ __device__ void producer(const DecodeArgs &a, DecodeSmem &sm, const JobSpace &js
                 const int rows_per_e = type == kJobGu ? a.I : a.H;
                 for (int m = 0; m < 2; m++) {
                     const int64_t gt = (int64_t)e * (rows_per_e / 16) + (type == kJobGu ? tile : 2 * tile + m);
-                    const int64_t u = gt * M[m]->nkc + c0 / 128;
-                    d.oq[m] = sw.put(M[m]->qs + u * 32, (unsigned)(W / 128) * 512u);
-                    d.os[m] = sw.put(M[m]->sc + u * 8, (unsigned)(W / 128) * 128u);
-                    d.od[m] = sw.put(M[m]->dm + (gt * (M[m]->nkc / 2) + c0 / 256) * 8, (unsigned)(W / 256) * 64u);
+                    const int64_t u = gt * (M[m]->nkc / 2) + c0 / 256; // first record of the stage
+                    d.oq[m] = sw.put(M[m]->rec + u * kQ2Rec, (unsigned)(W / 256) * kQ2Rec);
                 }
                 const uint16_t *hi = a.xq;
                 const float *of = a.xoff, *su = a.xsum;
@@ -1338,11 +1348,19 @@ __device__ void producer(const DecodeArgs &a, DecodeSmem &sm, const JobSpace &js
             }
         }
         // The selection's CTA takes no further job before the routing is
-        // published: a router row queued behind the selection would never run.
-        if (type == kJobSel && a0 == 0 && ok) {
-            if (!wait_slot(a, 0, rec))
-                break;
-            cached_slot = 0;
+        // published (a router row queued behind the selection would never run),
+        // the rehearsal's none before the rehearsal is done (a job behind it
+        // would wait it out).
+        if (type == kJobSel && ok) {
+            if (a0 == 0) {
+                if (!wait_slot(a, 0, rec))
+                    break;
+                cached_slot = 0;
+            } else {
+                const unsigned m = n - 1; // the rehearsal's stage: wait for its release
+                if (!mbar_wait(a, &sm.empty[m % kRing], (m / kRing) & 1u))
+                    break;
+            }
             j_next = next_job();
         }
     }
@@ -1360,71 +1378,102 @@ __device__ void producer(const DecodeArgs &a, DecodeSmem &sm, const JobSpace &js
 // ---- consumers (warps 0..7) ----------------------------------------------------------
 
 // y for 32 rows (tile ti) and all tokens, in fixed order: sum over k, then
-// shared. All consumer threads, one (token, row) each; the routing loads of a
-// thread are issued together, then its expert outputs. Not inlined, and given
-// plain values: it runs once per tile and its registers stay out of the hot
-// loops' budget.
-__device__ __noinline__ void combine_tile(const float *w, const int32_t *inv, const float *yes, const float *ysh,
-                                          float *y, int T, int K, int H, int ti) {
-    const int q = threadIdx.x, r = q & 31, t = q >> 5;
-    if (t >= T)
-        return;
-    const int col = ti * 32 + r;
-    float wk[kMaxTopK];
-    int pk[kMaxTopK];
+// shared. The publisher warp, one row per lane: the routing weights and pair
+// positions of all tokens go through shared memory in one round trip, then
+// the expert outputs of two tokens at a time.
+__device__ void combine_tile(const DecodeArgs &a, DecodeSmem &sm, int ti, int lane) {
+    const int P = a.T * a.K;
+    for (int p = lane; p < P; p += 32) {
+        sm.cw[p] = __ldcg(a.w + p);
+        sm.cinv[p] = __ldcg(a.inv + p);
+    }
+    __syncwarp();
+    const int col = ti * 32 + lane;
+    for (int t0 = 0; t0 < a.T; t0 += 2) {
+        float ye[2][kMaxTopK], sh[2];
 #pragma unroll
-    for (int k = 0; k < kMaxTopK; k++) {
-        if (k < K) {
-            wk[k] = __ldcg(w + t * K + k);
-            pk[k] = __ldcg(inv + t * K + k);
+        for (int u = 0; u < 2; u++) {
+            const int t = t0 + u < a.T ? t0 + u : t0;
+#pragma unroll
+            for (int k = 0; k < kMaxTopK; k++)
+                if (k < a.K)
+                    ye[u][k] = __ldcg(a.ye + (int64_t)sm.cinv[t * a.K + k] * a.H + col);
+            sh[u] = a.Ish > 0 ? __ldcg(a.ysh + (int64_t)t * a.H + col) : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < 2; u++) {
+            const int t = t0 + u;
+            if (t < a.T) {
+                float v = 0.f;
+#pragma unroll
+                for (int k = 0; k < kMaxTopK; k++)
+                    if (k < a.K)
+                        v = fmaf(sm.cw[t * a.K + k], ye[u][k], v);
+                if (a.Ish > 0)
+                    v += sh[u];
+                a.y[(int64_t)t * a.H + col] = v;
+            }
         }
     }
-    float ye[kMaxTopK];
-#pragma unroll
-    for (int k = 0; k < kMaxTopK; k++)
-        if (k < K)
-            ye[k] = __ldcg(yes + (int64_t)pk[k] * H + col);
-    const float sh = ysh ? __ldcg(ysh + (int64_t)t * H + col) : 0.f;
-    float v = 0.f;
-#pragma unroll
-    for (int k = 0; k < kMaxTopK; k++)
-        if (k < K)
-            v = fmaf(wk[k], ye[k], v);
-    if (ysh)
-        v += sh;
-    y[(int64_t)t * H + col] = v;
 }
 
-// After the consumers' barrier that follows a D job's result writes: thread 0
-// counts the contribution to the 32-row tile ti; the last of the nuniq
-// contributions combines the tile (all consumer threads, after a second
-// barrier), once the shared expert's down rows are complete (those jobs
-// precede every D job in the queue, so the wait ends).
-__device__ void arrive_tile(const DecodeArgs &a, const JobSpace &js, DecodeSmem &sm, int buf, int ti, int nuniq) {
-    if (threadIdx.x == 0) {
-        unsigned last = 0;
-        __threadfence();
-        const unsigned old = atomicAdd(a.ctl + kCtlTileCnt + ti, 1u);
-        last = old + 1 == (unsigned)nuniq;
-        if (last) {
-            __threadfence();
-            a.ctl[kCtlTileCnt + ti] = 0; // ready for the next launch
-            if (js.nSD > 0 && !wait_counter(a, a.ctl + kCtlSdDone, (unsigned)js.nSD, false))
-                last = 0;
+// Consumer thread 0, after the consumers' barrier that follows a job's result
+// writes: hand the job's publication to the publisher warp (a job count to
+// increase, or a D job's arrival at its 32-row output tile). The mbarrier
+// arrival orders the job's writes before the publisher's GPU-scope release.
+// Returns false if the wait for a free task slot gave up.
+__device__ bool publish(const DecodeArgs &a, DecodeSmem &sm, unsigned &npub, int kind, unsigned *ctr, int tile,
+                        int nuniq) {
+    const int s = (int)(npub % kPubQ);
+    if (!mbar_wait(a, &sm.pub_empty[s], ((npub / kPubQ) & 1u) ^ 1u))
+        return false;
+    sm.pub[s].ctr = ctr;
+    sm.pub[s].kind = kind;
+    sm.pub[s].tile = tile;
+    sm.pub[s].nuniq = nuniq;
+    mbar_arrive(&sm.pub_full[s]);
+    npub++;
+    return true;
+}
+
+// The publisher warp: makes each job's results visible GPU-wide (one release
+// reduction on its count) off the consumers' path; for a D job, counts its
+// contribution to the 32-row tile, and the last of the nuniq contributions
+// combines the tile once the shared expert's down rows are complete (those
+// jobs precede every D job in the queue, so the wait ends).
+__device__ void publisher(const DecodeArgs &a, const JobSpace &js, DecodeSmem &sm, int lane) {
+    for (unsigned k = 0;; k++) {
+        const int s = (int)(k % kPubQ);
+        if (!mbar_wait(a, &sm.pub_full[s], (k / kPubQ) & 1u))
+            return;
+        const int kind = sm.pub[s].kind;
+        if (kind == kPubEnd)
+            return;
+        unsigned *ctr = sm.pub[s].ctr;
+        const int tile = sm.pub[s].tile, nuniq = sm.pub[s].nuniq;
+        if (kind == kPubSignal) {
+            if (lane == 0)
+                asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(ctr) : "memory");
+        } else {
+            unsigned last = 0;
+            if (lane == 0) {
+                __threadfence();
+                const unsigned old = atomicAdd(ctr, 1u);
+                last = old + 1 == (unsigned)nuniq;
+                if (last) {
+                    __threadfence();
+                    *ctr = 0; // ready for the next launch
+                    if (js.nSD > 0 && !wait_counter(a, a.ctl + kCtlSdDone, (unsigned)js.nSD, false))
+                        last = 0;
+                }
+            }
+            if (__shfl_sync(0xFFFFFFFFu, last, 0))
+                combine_tile(a, sm, tile, lane);
         }
-        sm.combine[buf] = (int)last;
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(&sm.pub_empty[s]);
     }
-    consumer_sync();
-    if (sm.combine[buf])
-        combine_tile(a.w, a.inv, a.ye, a.Ish > 0 ? a.ysh : nullptr, a.y, a.T, a.K, a.H, ti);
-}
-
-// After the consumers' barrier that follows the job's result writes: thread 0
-// publishes the job with one release reduction on the count (the barrier
-// orders the other threads' writes before it); nobody waits for it here.
-__device__ __forceinline__ void signal(const DecodeArgs &a, unsigned *ctr) {
-    if (threadIdx.x == 0)
-        asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(ctr) : "memory");
 }
 
 template <int TP> struct JobOps {
@@ -1441,7 +1490,7 @@ template <int TP> struct JobOps {
     // End of a job: combine the warps' partial sums (barrier 1), write the
     // results, barrier 2, then publish (thread 0 / warp 0, without a barrier).
     static __device__ void finish(const DecodeArgs &a, const JobSpace &js, DecodeSmem &sm, const StageDesc &d,
-                                  int buf, int warp, int lane, float (&out)[2][2][2]) {
+                                  int buf, int warp, int lane, float (&out)[2][2][2], unsigned &npub) {
         const int tid = threadIdx.x;
         auto P = sm.part[buf];
         if (d.type != kJobSd) {
@@ -1468,7 +1517,8 @@ template <int TP> struct JobOps {
                 a.hs_lo[o] = __half_as_ushort(lo);
             }
             consumer_sync();
-            signal(a, a.ctl + kCtlSguDone);
+            if (tid == 0)
+                publish(a, sm, npub, kPubSignal, a.ctl + kCtlSguDone, 0, 0);
         } else if (d.type == kJobGu) {
             // row r of the tile is column k = 16 tile + r of the down matrix
             const int t = tid >> 4, r = tid & 15;
@@ -1503,7 +1553,8 @@ template <int TP> struct JobOps {
                 a.hsum[d.pos[t] * (a.I / 16) + d.tile] = hv_sum;
             }
             consumer_sync();
-            signal(a, a.ctl + kCtlGuDone + d.a0);
+            if (tid == 0)
+                publish(a, sm, npub, kPubSignal, a.ctl + kCtlGuDone + d.a0, 0, 0);
         } else if (d.type == kJobSd) {
             if (tid < 16 * a.T) {
                 const int r = tid & 15, t = tid >> 4;
@@ -1513,7 +1564,8 @@ template <int TP> struct JobOps {
                 a.ysh[(int64_t)t * a.H + d.a0 * 16 + r] = v;
             }
             consumer_sync();
-            signal(a, a.ctl + kCtlSdDone);
+            if (tid == 0)
+                publish(a, sm, npub, kPubSignal, a.ctl + kCtlSdDone, 0, 0);
         } else { // kJobD: rows 32 tile + 16 m + r
             const int t = tid >> 4, r = tid & 15;
             if (t < d.ntok) {
@@ -1526,7 +1578,8 @@ template <int TP> struct JobOps {
                 }
             }
             consumer_sync();
-            arrive_tile(a, js, sm, buf, d.tile, d.nuniq);
+            if (tid == 0)
+                publish(a, sm, npub, kPubTile, a.ctl + kCtlTileCnt + d.tile, d.tile, d.nuniq);
         }
     }
 };
@@ -1549,19 +1602,20 @@ __device__ __forceinline__ void stage_tp(int tp, const DecodeArgs &a, const uint
 
 template <int TPM>
 __device__ __forceinline__ void finish_tp(int tp, const DecodeArgs &a, const JobSpace &js, DecodeSmem &sm,
-                                          const StageDesc &d, int buf, int warp, int lane, float (&out)[2][2][2]) {
+                                          const StageDesc &d, int buf, int warp, int lane, float (&out)[2][2][2],
+                                          unsigned &npub) {
     if (TPM == 1 || tp == 1)
-        JobOps<1>::finish(a, js, sm, d, buf, warp, lane, out);
+        JobOps<1>::finish(a, js, sm, d, buf, warp, lane, out, npub);
     else if (TPM == 2 || tp == 2)
-        JobOps<(TPM >= 2 ? 2 : 1)>::finish(a, js, sm, d, buf, warp, lane, out);
+        JobOps<(TPM >= 2 ? 2 : 1)>::finish(a, js, sm, d, buf, warp, lane, out, npub);
     else if (TPM == 4 || tp == 4)
-        JobOps<(TPM >= 4 ? 4 : 1)>::finish(a, js, sm, d, buf, warp, lane, out);
+        JobOps<(TPM >= 4 ? 4 : 1)>::finish(a, js, sm, d, buf, warp, lane, out, npub);
     else
-        JobOps<TPM>::finish(a, js, sm, d, buf, warp, lane, out);
+        JobOps<TPM>::finish(a, js, sm, d, buf, warp, lane, out, npub);
 }
 
 template <int TPM> __device__ void consumer(const DecodeArgs &a, DecodeSmem &sm, const JobSpace &js, int warp, int lane) {
-    unsigned n = 0, jobs_done = 0;
+    unsigned n = 0, jobs_done = 0, npub = 0;
     float out[2][2][2];
     bool alive = true; // false after a failed dependency wait: drain the ring without computing
     while (true) {
@@ -1625,7 +1679,7 @@ template <int TPM> __device__ void consumer(const DecodeArgs &a, DecodeSmem &sm,
                     alive = ok;
             } else {
                 const int buf = (int)(jobs_done & 1u);
-                finish_tp<TPM>(d.tp, a, js, sm, d, buf, warp, lane, out);
+                finish_tp<TPM>(d.tp, a, js, sm, d, buf, warp, lane, out, npub);
             }
             jobs_done++;
         }
@@ -1634,6 +1688,9 @@ template <int TPM> __device__ void consumer(const DecodeArgs &a, DecodeSmem &sm,
             mbar_arrive(&sm.empty[slot]);
         n++;
     }
+    // every job's publication is queued: tell the publisher warp to stop
+    if (threadIdx.x == 0)
+        publish(a, sm, npub, kPubEnd, nullptr, 0, 0);
 }
 
 // TPM: the largest padded token count of a job in this launch (1, 2, 4 or 8).
@@ -1646,12 +1703,18 @@ template <int TPM> __global__ void __launch_bounds__(kDecodeThreads, 2) decode_f
             mbar_init(&sm.full[i], 1);
             mbar_init(&sm.empty[i], kConsumerWarps);
         }
+        for (int i = 0; i < kPubQ; i++) {
+            mbar_init(&sm.pub_full[i], 1);
+            mbar_init(&sm.pub_empty[i], 1);
+        }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
     const JobSpace js = job_space(a);
     if (warp == kConsumerWarps) {
         producer(a, sm, js);
+    } else if (warp == kConsumerWarps + 1) {
+        publisher(a, js, sm, lane);
     } else {
         consumer<TPM>(a, sm, js, warp, lane);
     }

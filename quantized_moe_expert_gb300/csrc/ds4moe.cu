@@ -280,15 +280,12 @@ void layout_weights(ds4moe *h, Carver &c) {
     auto f2 = [&](Q2Frag &m, int64_t rows, int k) {
         m.rows = rows;
         m.nkc = k / 128;
-        m.qs = c.take<uint4>((uint64_t)(rows / 16) * m.nkc * 32);
-        m.sc = c.take<uint4>((uint64_t)(rows / 16) * m.nkc * 8);
-        m.dm = c.take<uint2>((uint64_t)(rows / 16) * (m.nkc / 2) * 8);
+        m.rec = c.take<uint8_t>((uint64_t)(rows / 16) * (m.nkc / 2) * kQ2Rec);
     };
     auto f8 = [&](Q8Frag &m, int64_t rows, int k) {
         m.rows = rows;
         m.nbq = k / 32;
-        m.qs = c.take<uint4>((uint64_t)(rows / 16) * m.nbq * 32);
-        m.d = c.take<uint32_t>((uint64_t)(rows / 16) * m.nbq * 8);
+        m.rec = c.take<uint8_t>((uint64_t)(rows / 16) * m.nbq * kQ8Rec);
     };
     f2(D.gate, (int64_t)L.E * L.I, L.H);
     f2(D.up, (int64_t)L.E * L.I, L.H);
@@ -825,13 +822,12 @@ int ds4moe_create(const ds4moe_layer_desc *desc, const ds4moe_weights *w, ds4moe
     auto rf2 = [&](const void *src, Q2Frag &m) {
         const int64_t n = (m.rows / 16) * m.nkc * 32;
         repack_q2_frag_kernel<<<blocks_for(n, 256), 256, 0, st>>>(static_cast<const uint8_t *>(src), m.rows, m.nkc / 2,
-                                                                   const_cast<uint4 *>(m.qs), const_cast<uint4 *>(m.sc),
-                                                                   const_cast<uint2 *>(m.dm));
+                                                                   const_cast<uint8_t *>(m.rec));
     };
     auto rf8 = [&](const void *src, Q8Frag &m) {
         const int64_t n = (m.rows / 16) * m.nbq * 32;
         repack_q8_frag_kernel<<<blocks_for(n, 256), 256, 0, st>>>(static_cast<const uint8_t *>(src), m.rows, m.nbq,
-                                                                   const_cast<uint4 *>(m.qs), const_cast<uint32_t *>(m.d));
+                                                                   const_cast<uint8_t *>(m.rec));
     };
     rf2(w->gate, D.gate);
     rf2(w->up, D.up);

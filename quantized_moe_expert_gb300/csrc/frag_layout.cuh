@@ -23,6 +23,11 @@
 // (one per 16-column sub-block of the chunk) of row g (bytes 0-7) and row g+8
 // (bytes 8-15). d/dmin, per (tile, 256-column block): 8 x uint2; entry g holds
 // the d|dmin word of row g and of row g+8.
+// All three sit together, one 1344-byte record per (tile, 256-column block)
+// (the 84 bytes of each of its 16 rows' blocks): codes of the block's two
+// chunks (2 x 512 B), their scale entries (2 x 128 B), the d/dmin entries
+// (64 B). A tile's column range is one contiguous run of records, so a stage
+// of one matrix tile is a single bulk copy.
 //
 // 8-bit codes, per (tile, bq), bq = 32-column block: lane l holds a uint4
 //   { V(g, 0), V(g+8, 0), V(g, 1), V(g+8, 1) }
@@ -30,26 +35,30 @@
 // in that order, each XOR 0x80 (the code plus 128). One PRMT with 0x64 bytes
 // turns two of them into the binary16 pair 1024 + (q + 128), and subtracting
 // 1152 gives q exactly. Scales per (tile, bq): 8 x uint32; entry g holds the
-// binary16 d of row g (low half) and row g+8 (high half).
+// binary16 d of row g (low half) and row g+8 (high half). Codes and scales of
+// a (tile, bq) sit together in one 544-byte record (512 B of codes, 32 B of
+// scales), a tile's column range being one contiguous run of records.
 #pragma once
 
 #include "common.cuh"
 
 namespace ds4 {
 
+constexpr int kQ2Rec = 1344; // bytes per (16-row tile, 256-column block) record
+constexpr int kQ2RecScales = 1024, kQ2RecDm = 1280; // offsets of the scale and d/dmin entries
+constexpr int kQ8Rec = 544;  // bytes per (16-row tile, 32-column block) record
+constexpr int kQ8RecD = 512; // offset of the scale entries
+
 struct Q2Frag {
-    const uint4 *qs; // [rows/16][nkc][32]
-    const uint4 *sc; // [rows/16][nkc][8]
-    const uint2 *dm; // [rows/16][nkc/2][8]
+    const uint8_t *rec; // [rows/16][nkc/2] records of kQ2Rec bytes
     int64_t rows;
-    int32_t nkc;     // K / 128
+    int32_t nkc;        // K / 128
 };
 
 struct Q8Frag {
-    const uint4 *qs;   // [rows/16][nbq][32]
-    const uint32_t *d; // [rows/16][nbq][8]
+    const uint8_t *rec; // [rows/16][nbq] records of kQ8Rec bytes
     int64_t rows;
-    int32_t nbq;       // K / 32
+    int32_t nbq;        // K / 32
 };
 
 __host__ __device__ constexpr int frag_shift(int r) { return r < 3 ? 0 : (r < 6 ? 6 : 12); }
@@ -83,8 +92,7 @@ __device__ __forceinline__ uint32_t canon_word2(const uint8_t *src, int64_t row,
 
 // One thread per (tile, kc, lane): codes; lanes < 8 also write the scale entry
 // of (tile, kc, g = lane); even kc also writes the d/dmin entry of the block.
-__global__ void repack_q2_frag_kernel(const uint8_t *__restrict__ src, int64_t rows, int nb, uint4 *__restrict__ qs,
-                                      uint4 *__restrict__ sc, uint2 *__restrict__ dm) {
+__global__ void repack_q2_frag_kernel(const uint8_t *__restrict__ src, int64_t rows, int nb, uint8_t *__restrict__ rec) {
     const int nkc = nb * 2;
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int64_t total = (rows / 16) * nkc * 32;
@@ -95,8 +103,10 @@ __global__ void repack_q2_frag_kernel(const uint8_t *__restrict__ src, int64_t r
     const int64_t tile = (i >> 5) / nkc;
     const int g = lane >> 2, tig = lane & 3;
     const int64_t r0 = tile * 16 + g, r1 = r0 + 8;
-    qs[i] = make_uint4(canon_word2(src, r0, nb, 2 * kc, tig), canon_word2(src, r1, nb, 2 * kc, tig),
-                       canon_word2(src, r0, nb, 2 * kc + 1, tig), canon_word2(src, r1, nb, 2 * kc + 1, tig));
+    uint8_t *const rec_blk = rec + (tile * nb + (kc >> 1)) * kQ2Rec; // this block's record
+    reinterpret_cast<uint4 *>(rec_blk + (kc & 1) * 512)[lane] =
+        make_uint4(canon_word2(src, r0, nb, 2 * kc, tig), canon_word2(src, r1, nb, 2 * kc, tig),
+                   canon_word2(src, r0, nb, 2 * kc + 1, tig), canon_word2(src, r1, nb, 2 * kc + 1, tig));
     if (lane < 8) {
         const int64_t ra = tile * 16 + lane, rb = ra + 8;
         const int blk = kc >> 1, j0 = (kc & 1) * 8; // 8 sub-blocks of this chunk within the block
@@ -110,20 +120,19 @@ __global__ void repack_q2_frag_kernel(const uint8_t *__restrict__ src, int64_t r
             v[2] |= (uint32_t)sb[j] << (8 * j);
             v[3] |= (uint32_t)sb[4 + j] << (8 * j);
         }
-        sc[((tile * nkc) + kc) * 8 + lane] = make_uint4(v[0], v[1], v[2], v[3]);
+        reinterpret_cast<uint4 *>(rec_blk + kQ2RecScales + (kc & 1) * 128)[lane] = make_uint4(v[0], v[1], v[2], v[3]);
         if ((kc & 1) == 0) {
             const uint8_t *da = src + (ra * nb + blk) * kQ2Bytes + 80;
             const uint8_t *db = src + (rb * nb + blk) * kQ2Bytes + 80;
             const uint32_t wa = da[0] | (da[1] << 8) | (da[2] << 16) | ((uint32_t)da[3] << 24);
             const uint32_t wb = db[0] | (db[1] << 8) | (db[2] << 16) | ((uint32_t)db[3] << 24);
-            dm[((tile * nb) + blk) * 8 + lane] = make_uint2(wa, wb);
+            reinterpret_cast<uint2 *>(rec_blk + kQ2RecDm)[lane] = make_uint2(wa, wb);
         }
     }
 }
 
 // One thread per (tile, bq, lane).
-__global__ void repack_q8_frag_kernel(const uint8_t *__restrict__ src, int64_t rows, int nbq, uint4 *__restrict__ qs,
-                                      uint32_t *__restrict__ d) {
+__global__ void repack_q8_frag_kernel(const uint8_t *__restrict__ src, int64_t rows, int nbq, uint8_t *__restrict__ rec) {
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int64_t total = (rows / 16) * nbq * 32;
     if (i >= total)
@@ -141,12 +150,14 @@ __global__ void repack_q8_frag_kernel(const uint8_t *__restrict__ src, int64_t r
         v[h] = ((uint32_t)(q[0] ^ 0x80)) | ((uint32_t)(q[1] ^ 0x80) << 8) | ((uint32_t)(q[8] ^ 0x80) << 16) |
                ((uint32_t)(q[9] ^ 0x80) << 24);
     }
-    qs[i] = make_uint4(v[0], v[1], v[2], v[3]);
+    uint8_t *const rec_blk = rec + (tile * nbq + bq) * kQ8Rec; // this block's record
+    reinterpret_cast<uint4 *>(rec_blk)[lane] = make_uint4(v[0], v[1], v[2], v[3]);
     if (lane < 8) {
         const int64_t ra = tile * 16 + lane, rb = ra + 8;
         const uint8_t *da = src + (ra * nbq + bq) * kQ8Bytes;
         const uint8_t *db = src + (rb * nbq + bq) * kQ8Bytes;
-        d[((tile * nbq) + bq) * 8 + lane] = (uint32_t)(da[0] | (da[1] << 8)) | ((uint32_t)(db[0] | (db[1] << 8)) << 16);
+        reinterpret_cast<uint32_t *>(rec_blk + kQ8RecD)[lane] =
+            (uint32_t)(da[0] | (da[1] << 8)) | ((uint32_t)(db[0] | (db[1] << 8)) << 16);
     }
 }
 
