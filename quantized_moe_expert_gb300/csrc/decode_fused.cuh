@@ -1188,7 +1188,7 @@ __device__ void producer(const DecodeArgs &a, DecodeSmem &sm, const JobSpace &js
         if (j >= js.oR)
             j_next = next_job();
         int type, a0 = 0, tile = 0, ntok = a.T, K = a.H, per16 = 0, nu = 0;
-        int pos[kDecodeT], tok[kDecodeT];
+        int pos[kDecodeT], tok[kDecodeT]; // (compile-time indices only: registers)
 #pragma unroll
         for (int i = 0; i < kDecodeT; i++)
             pos[i] = tok[i] = i < a.T ? i : 0;
@@ -1268,6 +1268,10 @@ __device__ void producer(const DecodeArgs &a, DecodeSmem &sm, const JobSpace &js
             }
             StageWriter sw(sm, slot);
             const int c0 = sub * W;
+            // token of the job's column t (routed jobs: from the routing record)
+            auto tok_of = [&](int t) -> int {
+                return (type == kJobGu || type == kJobD) ? (int)((rec.toks >> (3 * t)) & 7u) : t;
+            };
             if (type == kJobR) {
                 d.oq[0] = (int)sw.off;
                 for (int r = 0; r < tile; r++)
@@ -1315,28 +1319,28 @@ __device__ void producer(const DecodeArgs &a, DecodeSmem &sm, const JobSpace &js
                     // routing was published: safe to copy now
                     d.oact = (int)sw.off;
                     for (int t = 0; t < ntok; t++)
-                        sw.put(hi + (int64_t)tok[t] * K + c0, 2u * W);
+                        sw.put(hi + (int64_t)tok_of(t) * K + c0, 2u * W);
                     d.ooff = (int)sw.off;
                     for (int t = 0; t < ntok; t++)
-                        sw.put(of + (int64_t)tok[t] * (K / 16) + c0 / 16, (unsigned)W / 4u);
+                        sw.put(of + (int64_t)tok_of(t) * (K / 16) + c0 / 16, (unsigned)W / 4u);
                     d.osum = (int)sw.off;
                     for (int t = 0; t < ntok; t++)
-                        sw.put(su + (int64_t)tok[t] * (K / 16) + c0 / 16, (unsigned)W / 4u);
+                        sw.put(su + (int64_t)tok_of(t) * (K / 16) + c0 / 16, (unsigned)W / 4u);
                 } else {
                     // h rows of this expert: written by its GU jobs
                     sw.dependent_from_here();
                     d.oact = (int)sw.off;
                     for (int t = 0; t < ntok; t++)
-                        sw.put(a.hq_hi + (int64_t)pos[t] * K + c0, 2u * W);
+                        sw.put(a.hq_hi + (int64_t)(rec.p0 + t) * K + c0, 2u * W);
                     d.olo = (int)sw.off;
                     for (int t = 0; t < ntok; t++)
-                        sw.put(a.hq_lo + (int64_t)pos[t] * K + c0, 2u * W);
+                        sw.put(a.hq_lo + (int64_t)(rec.p0 + t) * K + c0, 2u * W);
                     d.ooff = (int)sw.off;
                     for (int t = 0; t < ntok; t++)
-                        sw.put(a.hoff + (int64_t)pos[t] * (K / 16) + c0 / 16, (unsigned)W / 4u);
+                        sw.put(a.hoff + (int64_t)(rec.p0 + t) * (K / 16) + c0 / 16, (unsigned)W / 4u);
                     d.osum = (int)sw.off;
                     for (int t = 0; t < ntok; t++)
-                        sw.put(a.hsum + (int64_t)pos[t] * (K / 16) + c0 / 16, (unsigned)W / 4u);
+                        sw.put(a.hsum + (int64_t)(rec.p0 + t) * (K / 16) + c0 / 16, (unsigned)W / 4u);
                 }
             }
             const unsigned *dep = type == kJobD ? a.ctl + kCtlGuDone + a0 : a.ctl + kCtlSguDone;
