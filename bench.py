@@ -255,8 +255,10 @@ def workload_batches(name):
     return [synth.make_tokens(name)]
 
 
-def cpu_oracle_rate(name, layers, batches, budget_tokens=None):
-    """Time the oracle on a bounded sample; returns (tokens/s, threads used, sample text, seconds)."""
+def cpu_oracle_rate(name, layers, batches, budget_tokens=None, min_seconds=0.0):
+    """Time the oracle on a bounded sample; returns (tokens/s, threads used, sample text, seconds).
+
+    The sample is run again until min_seconds of CPU time have passed (whole passes)."""
     import oracle
     import synth
     wl = synth.WORKLOADS[name]
@@ -270,10 +272,17 @@ def cpu_oracle_rate(name, layers, batches, budget_tokens=None):
         flat = batches[0][:n]
         sample = f"first {len(flat)} of the {wl.tokens} tokens through all {len(layers)} layer(s), oracle.forward"
     t0 = time.perf_counter()
-    for layer in layers:
-        oracle.forward(wl.shape, layer, np.ascontiguousarray(flat))
-    dt = time.perf_counter() - t0
-    return len(flat) / dt, min(cores, len(flat)), sample, dt
+    passes = 0
+    while True:
+        for layer in layers:
+            oracle.forward(wl.shape, layer, np.ascontiguousarray(flat))
+        passes += 1
+        dt = time.perf_counter() - t0
+        if dt >= min_seconds:
+            break
+    if passes > 1:
+        sample += f", {passes} passes"
+    return passes * len(flat) / dt, min(cores, len(flat)), sample, dt
 
 
 def dist_setup(args):
@@ -491,7 +500,8 @@ def main():
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        rate, cores, sample, dt = cpu_oracle_rate(args.workload, layers, batches)
+        # about 10 s of CPU work: whole passes over the sample until then
+        rate, cores, sample, dt = cpu_oracle_rate(args.workload, layers, batches, min_seconds=10.0)
         cpu = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample,
                "seconds": dt}
 
