@@ -756,10 +756,10 @@ __device__ __forceinline__ void select_token(const DecodeArgs &a, const SelIO &i
 // job's stage buffer (bias at float offset kDecodeT * E of scratch).
 __device__ void select_prepare(const DecodeArgs &a, float *scratch) {
     const int T = a.T, E = a.E, H = a.H;
-    // thread i takes sub-blocks i, i + 256, ... of all tokens
+    // thread i takes sub-blocks i, i + 256, ... of every token
     const int nsub = H / 16;
-    for (int q = threadIdx.x; q < T * nsub; q += 32 * kConsumerWarps) {
-        const int t = q / nsub, j = q % nsub;
+    for (int t = 0; t < T; t++)
+    for (int j = threadIdx.x; j < nsub; j += 32 * kConsumerWarps) {
         const uint4 *src = reinterpret_cast<const uint4 *>(a.x + (int64_t)t * H + 16 * j);
         const uint4 p0 = __ldg(src), p1 = __ldg(src + 1);
         const uint32_t wv[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
@@ -801,14 +801,21 @@ __device__ __forceinline__ bool job_select(const DecodeArgs &a, const SelIO &io,
         const float *bias = scratch + kDecodeT * E;
         const int n = T * E;
         constexpr int kStride = 32 * kConsumerWarps;
-        // thread i owns entries i, i + 256, ... (at most 32 of them: T E <= 8192)
+        // thread i owns entries i, i + 256, ... (at most 32 of them: T E <= 8192);
+        // the expert of entry q (q mod E) is followed incrementally
         unsigned pending = 0u;
         for (int u = 0, q = threadIdx.x; q < n; u++, q += kStride)
             pending |= 1u << u;
+        const int e0 = (int)threadIdx.x % E;
         uint64_t t0 = 0;
         for (unsigned it = 0;; it++) {
             unsigned still = 0u;
+            int e = e0;
             for (int u = 0, q = threadIdx.x; q < n; u++, q += kStride) {
+                const int eq = e;
+                e += kStride;
+                while (e >= E)
+                    e -= E;
                 if (!(pending >> u & 1u))
                     continue;
                 const unsigned long long v = ld_relaxed_u64(io.lgt + q);
@@ -817,7 +824,7 @@ __device__ __forceinline__ bool job_select(const DecodeArgs &a, const SelIO &io,
                     continue;
                 }
                 const float sg = sigmoid(__uint_as_float((unsigned)v));
-                keys[q] = sel_key(a.router_bias ? sg + bias[q % E] : sg);
+                keys[q] = sel_key(a.router_bias ? sg + bias[eq] : sg);
             }
             pending = still;
             // bounded: thread 0 decides for everyone; the flag of round it is
@@ -893,12 +900,31 @@ __device__ __forceinline__ bool job_select(const DecodeArgs &a, const SelIO &io,
     // grouping (warp 0): distinct experts in ascending order, the pairs of each
     // in pair order. P <= 64 pairs: lane l owns pairs l and l + 32.
     const int P = T * K;
-    if (warp == 0) {
+    // pair p = t K + k: t by a multiply-shift, exact for p < 64 and K <= 8
+    const unsigned kmagic = (65536u + (unsigned)K - 1u) / (unsigned)K;
+    auto tok_of_pair = [&](int p) -> int { return (int)(((unsigned)p * kmagic) >> 16); };
+    if (T == 1) {
+        // one token: its K experts are distinct, slot k is the k-th chosen
+        // expert with its single pair at position k (the slot order only
+        // numbers the jobs; the combine sums in k order either way)
+        if (warp == 0) {
+            if (lane < K) {
+                const int e = sm.sel_idx[0][lane];
+                io.inv[lane] = lane;
+                atomicAdd(io.counts + e, 1);
+                sm.rec[0][lane] = (unsigned)e | (unsigned)lane << 11 | 1u << 18 | (unsigned)K << 22;
+                sm.rec[1][lane] = 0u; // token 0
+            }
+            if (lane == 0)
+                *io.nuniq = K;
+        }
+    } else if (warp == 0) {
         int pe[2];
 #pragma unroll
         for (int h = 0; h < 2; h++) {
             const int p = lane + 32 * h;
-            pe[h] = p < P ? sm.sel_idx[p / K][p % K] : -1;
+            const int pt = tok_of_pair(p);
+            pe[h] = p < P ? sm.sel_idx[pt][p - pt * K] : -1;
             if (pe[h] >= 0)
                 atomicOr(&sm.bitmap[pe[h] >> 5], 1u << (pe[h] & 31));
         }
@@ -977,10 +1003,10 @@ __device__ __forceinline__ bool job_select(const DecodeArgs &a, const SelIO &io,
             unsigned w0 = (unsigned)nu << 22, w1 = 0u;
             if (sl < nu) {
                 const int p0 = sm.slot_cnt[sl], p1 = sl + 1 < nu ? sm.slot_cnt[sl + 1] : P;
-                const int pf = sm.pair_at[p0];
-                w0 |= (unsigned)sm.sel_idx[pf / K][pf % K] | (unsigned)p0 << 11 | (unsigned)(p1 - p0) << 18;
+                const int pf = sm.pair_at[p0], tf = tok_of_pair(pf);
+                w0 |= (unsigned)sm.sel_idx[tf][pf - tf * K] | (unsigned)p0 << 11 | (unsigned)(p1 - p0) << 18;
                 for (int i = 0; i < p1 - p0; i++)
-                    w1 |= (unsigned)(sm.pair_at[p0 + i] / K) << (3 * i);
+                    w1 |= (unsigned)tok_of_pair(sm.pair_at[p0 + i]) << (3 * i);
             }
             if (sl < kMaxSlots) {
                 sm.rec[0][sl] = w0;
