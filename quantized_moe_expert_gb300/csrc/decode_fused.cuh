@@ -811,20 +811,30 @@ __device__ __forceinline__ bool job_select(const DecodeArgs &a, const SelIO &io,
         for (unsigned it = 0;; it++) {
             unsigned still = 0u;
             int e = e0;
-            for (int u = 0, q = threadIdx.x; q < n; u++, q += kStride) {
-                const int eq = e;
-                e += kStride;
-                while (e >= E)
-                    e -= E;
-                if (!(pending >> u & 1u))
-                    continue;
-                const unsigned long long v = ld_relaxed_u64(io.lgt + q);
-                if ((unsigned)(v >> 32) != io.epoch) {
-                    still |= 1u << u;
-                    continue;
+            // eight entries' loads in flight at a time
+            for (int u0 = 0, q0 = threadIdx.x; q0 < n; u0 += 8, q0 += 8 * kStride) {
+                unsigned long long v[8];
+#pragma unroll
+                for (int i = 0; i < 8; i++) {
+                    const int q = q0 + i * kStride;
+                    v[i] = (q < n && (pending >> (u0 + i) & 1u)) ? ld_relaxed_u64(io.lgt + q) : 0ull;
                 }
-                const float sg = sigmoid(__uint_as_float((unsigned)v));
-                keys[q] = sel_key(a.router_bias ? sg + bias[eq] : sg);
+#pragma unroll
+                for (int i = 0; i < 8; i++) {
+                    const int q = q0 + i * kStride, u = u0 + i;
+                    const int eq = e;
+                    e += kStride;
+                    while (e >= E)
+                        e -= E;
+                    if (q >= n || !(pending >> u & 1u))
+                        continue;
+                    if ((unsigned)(v[i] >> 32) != io.epoch) {
+                        still |= 1u << u;
+                        continue;
+                    }
+                    const float sg = sigmoid(__uint_as_float((unsigned)v[i]));
+                    keys[q] = sel_key(a.router_bias ? sg + bias[eq] : sg);
+                }
             }
             pending = still;
             // bounded: thread 0 decides for everyone; the flag of round it is
