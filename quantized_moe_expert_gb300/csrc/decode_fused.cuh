@@ -811,8 +811,26 @@ __device__ __forceinline__ bool job_select(const DecodeArgs &a, const SelIO &io,
         for (unsigned it = 0;; it++) {
             unsigned still = 0u;
             int e = e0;
-            // eight entries' loads in flight at a time
-            for (int u0 = 0, q0 = threadIdx.x; q0 < n; u0 += 8, q0 += 8 * kStride) {
+            // one or two tokens: at most two entries per thread, one at a time
+            if (T <= 2) {
+                for (int u = 0, q = threadIdx.x; q < n; u++, q += kStride) {
+                    const int eq = e;
+                    e += kStride;
+                    while (e >= E)
+                        e -= E;
+                    if (!(pending >> u & 1u))
+                        continue;
+                    const unsigned long long v = ld_relaxed_u64(io.lgt + q);
+                    if ((unsigned)(v >> 32) != io.epoch) {
+                        still |= 1u << u;
+                        continue;
+                    }
+                    const float sg = sigmoid(__uint_as_float((unsigned)v));
+                    keys[q] = sel_key(a.router_bias ? sg + bias[eq] : sg);
+                }
+            }
+            // more tokens: eight entries' loads in flight at a time
+            for (int u0 = 0, q0 = threadIdx.x; T > 2 && q0 < n; u0 += 8, q0 += 8 * kStride) {
                 unsigned long long v[8];
 #pragma unroll
                 for (int i = 0; i < 8; i++) {
