@@ -148,6 +148,35 @@ def test_out_of_range_routed_index_is_reported(tiny):
     assert moe.status() == 0  # the sticky error was cleared
 
 
+def test_repeated_given_expert(tiny):
+    """A token whose given experts repeat: the decode path replaces each repeat (in k
+    order) by the smallest expert index the token's row does not hold and reports
+    DS4MOE_EDEVICE; the prefill path applies the expert once per occurrence."""
+    shape, layer, moe = tiny
+    K = shape.top_k
+    x = tokens(shape, 2, 777)
+    idx = np.array([[3, 3, 9, 3, 12, 20], [1, 2, 4, 8, 16, 31]], dtype=np.int32)[:, :K]
+    w = np.full((2, K), 1.0 / K, dtype=np.float32)
+    replaced = idx.copy()
+    for r in range(1, K):
+        if replaced[0, r] in replaced[0, :r]:
+            c = 0
+            while c in replaced[0]:
+                c += 1
+            replaced[0, r] = c
+    assert replaced[0].tolist() == [3, 0, 9, 1, 12, 20][:K]
+    y = moe.forward_routed(x_to_dev(x), torch.from_numpy(idx).cuda(), torch.from_numpy(w).cuda(),
+                           path=ds4.PATH_DECODE).cpu().numpy()
+    assert moe.status() == ds4.DS4MOE_EDEVICE
+    y_ref = oracle.forward_routed(shape, layer, x, replaced, w.astype(np.float64))
+    assert rel_l2(y, y_ref) <= TOL_DECODE
+    y = moe.forward_routed(x_to_dev(x), torch.from_numpy(idx).cuda(), torch.from_numpy(w).cuda(),
+                           path=ds4.PATH_PREFILL).cpu().numpy()
+    assert moe.status() == 0
+    y_ref = oracle.forward_routed(shape, layer, x, idx, w.astype(np.float64))
+    assert rel_l2(y, y_ref) <= TOL_PREFILL
+
+
 def test_create_rejects_host_weights():
     shape = synth.Shape(256, 256, 4, 2, 0)
     layer = synth.make_layer(shape, 1234)
