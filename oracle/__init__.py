@@ -79,6 +79,14 @@ def _configure(lib):
     lib.oracle_select.restype = ctypes.c_int
     lib.oracle_expert_q2.argtypes = [ctypes.POINTER(_Shape), _vp, _vp, _vp, _vp, _vp]
     lib.oracle_shared_q8.argtypes = [ctypes.POINTER(_Shape), _vp, _vp, _vp, _vp, _vp]
+    lib.oracle_e2m1.argtypes = [ctypes.c_uint8]
+    lib.oracle_e2m1.restype = ctypes.c_double
+    lib.oracle_e8m0.argtypes = [ctypes.c_uint8]
+    lib.oracle_e8m0.restype = ctypes.c_double
+    lib.oracle_gain_block.argtypes = [_vp, _vp]
+    lib.oracle_forward_routed_gain.argtypes = [ctypes.POINTER(_Shape), _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                                               _vp, ctypes.c_int32, _vp, _vp, _vp, ctypes.c_int32]
+    lib.oracle_forward_routed_gain.restype = ctypes.c_int
     lib.oracle_forward_routed.argtypes = [ctypes.POINTER(_Shape), _vp, _vp, _vp, _vp, _vp, _vp,
                                           _vp, ctypes.c_int32, _vp, _vp, _vp, ctypes.c_int32]
     lib.oracle_forward_routed.restype = ctypes.c_int
@@ -200,18 +208,40 @@ def select(shape, logits_tE: np.ndarray, router_bias):
     return {"idx": idx, "weights": w, "gap": gap, "sel": sel}
 
 
+def e2m1(code: int) -> float:
+    """Value of a 4-bit FP4 E2M1 code."""
+    return _load().oracle_e2m1(code)
+
+
+def e8m0(x: int) -> float:
+    """Value of an E8M0 block scale byte, 2^(x - 127)."""
+    return _load().oracle_e8m0(x)
+
+
+def gain_block(block: np.ndarray) -> np.ndarray:
+    """The 32 down gains of one 17-byte gain block."""
+    b = np.ascontiguousarray(block, dtype=np.uint8)
+    assert b.size == 17
+    s = np.empty(32, dtype=np.float64)
+    _load().oracle_gain_block(_p(b), _p(s))
+    return s
+
+
 def forward_routed(shape, layer: dict, x_bf16: np.ndarray, idx: np.ndarray, weights: np.ndarray,
                    nthreads: int = 0) -> np.ndarray:
-    """Layer output [T, H] float64 for the given routing."""
+    """Layer output [T, H] float64 for the given routing (with the layer's down gains
+    "down_gain" / "down_gain2", where present)."""
     x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
     T = x.shape[0]
     idx = np.ascontiguousarray(idx, dtype=np.int32)
     weights = np.ascontiguousarray(weights, dtype=np.float64)
     y = np.empty((T, shape.hidden), dtype=np.float64)
     s = _shape(shape)
-    rc = _load().oracle_forward_routed(ctypes.byref(s), _p(layer["gate"]), _p(layer["up"]), _p(layer["down"]),
-                                       _p(layer.get("sh_gate")), _p(layer.get("sh_up")), _p(layer.get("sh_down")),
-                                       _p(x), T, _p(idx), _p(weights), _p(y), nthreads)
+    rc = _load().oracle_forward_routed_gain(ctypes.byref(s), _p(layer["gate"]), _p(layer["up"]), _p(layer["down"]),
+                                            _p(layer.get("sh_gate")), _p(layer.get("sh_up")),
+                                            _p(layer.get("sh_down")), _p(layer.get("down_gain")),
+                                            _p(layer.get("down_gain2")), _p(x), T, _p(idx), _p(weights), _p(y),
+                                            nthreads)
     if rc != 0:
         raise ValueError("oracle_forward_routed rejected its arguments")
     return y

@@ -43,6 +43,17 @@
  *     codes;   w_i = d * q_i.
  *   Routed gate/up [E][I][H/256] blocks, down [E][H][I/256]; shared gate/up
  *   [I_sh][H/32], shared down [H][I_sh/32]; router fp32 [E][H]; x bf16 [T][H].
+ *
+ * Optional per-expert down gains (the sidecar and post-training files of
+ * "YoungAi - DeepSeek V4.1 Flash on one DGX Spark", sections 3 and 4.2: one
+ * multiplicative gain per output channel of each expert's down projection,
+ * g_eff = g_base * s_sidecar * s_posttrain, stored as FP4 E2M1 with one scale
+ * per 32 channels in 17-byte blocks that encode s - 1):
+ *   gain block, 17 bytes per 32 consecutive output channels of one expert:
+ *     16 bytes of E2M1 codes (channel i at byte i/2, low nibble first), then the
+ *     block scale X as E8M0 (2^(byte - 127));   s_i = 1 + X * e2m1(code_i).
+ *   Table [E][H/32] blocks; with gains the output is
+ *     y[t] = sum_k w_k * (s1_{e_k} * s2_{e_k}) * ye_k + ysh.
  */
 #include <math.h>
 #include <omp.h>
@@ -58,7 +69,7 @@ typedef struct {
     int32_t shared_inter; /* I_sh, 0 = no shared expert */
 } oracle_shape;
 
-enum { Q2_BYTES = 84, Q8_BYTES = 34 };
+enum { Q2_BYTES = 84, Q8_BYTES = 34, GAIN_BYTES = 17 };
 
 /* IEEE binary16 -> double: sign, 5-bit exponent (bias 15), 10-bit fraction. */
 double oracle_f16(uint16_t h)
@@ -93,6 +104,29 @@ double oracle_bf16(uint16_t b)
 }
 
 static uint16_t le16(const uint8_t *p) { return (uint16_t)(p[0] | (p[1] << 8)); }
+
+/* FP4 E2M1 (OCP microscaling element): sign bit 3, exponent bits 2-1 (bias 1),
+ * mantissa bit 0; exponent 0 is subnormal (0 or 0.5). */
+double oracle_e2m1(uint8_t code)
+{
+    const int sign = (code >> 3) & 1, ex = (code >> 1) & 3, man = code & 1;
+    const double mag = ex == 0 ? 0.5 * man : ldexp(1.0 + 0.5 * man, ex - 1);
+    return sign ? -mag : mag;
+}
+
+/* E8M0 block scale: 2^(x - 127); 0xFF is NaN. */
+double oracle_e8m0(uint8_t x)
+{
+    return x == 0xFF ? NAN : ldexp(1.0, (int)x - 127);
+}
+
+/* The 32 gains of one 17-byte gain block: s_i = 1 + X * e2m1(code_i). */
+void oracle_gain_block(const uint8_t *blk, double *s)
+{
+    const double X = oracle_e8m0(blk[16]);
+    for (int i = 0; i < 32; i++)
+        s[i] = 1.0 + X * oracle_e2m1((uint8_t)((blk[i / 2] >> (4 * (i % 2))) & 15));
+}
 
 /* One 2-bit block -> 256 weights. */
 void oracle_dequant_q2(const uint8_t *blk, double *w)
@@ -291,15 +325,17 @@ void oracle_shared_q8(const oracle_shape *s, const uint8_t *sh_gate, const uint8
 }
 
 /*
- * The layer output for given routing: y[T][H] = sum_k weights[t,k] ye_{idx[t,k]} + ysh.
+ * The layer output for given routing: y[T][H] = sum_k weights[t,k] (s1 s2)_{e} ye_{idx[t,k]} + ysh,
+ * s1 and s2 the down gains of the gain tables gain1 and gain2 (1 where NULL).
  * ysh is skipped when shared_inter == 0 or the shared pointers are NULL.
  * Tokens are independent and each row is computed by one thread in a fixed
  * order, so the result does not depend on nthreads (<= 0: library default).
  */
-int oracle_forward_routed(const oracle_shape *s, const uint8_t *gate, const uint8_t *up,
-                          const uint8_t *down, const uint8_t *sh_gate, const uint8_t *sh_up,
-                          const uint8_t *sh_down, const uint16_t *x, int32_t T, const int32_t *idx,
-                          const double *weights, double *y, int32_t nthreads)
+int oracle_forward_routed_gain(const oracle_shape *s, const uint8_t *gate, const uint8_t *up,
+                               const uint8_t *down, const uint8_t *sh_gate, const uint8_t *sh_up,
+                               const uint8_t *sh_down, const uint8_t *gain1, const uint8_t *gain2,
+                               const uint16_t *x, int32_t T, const int32_t *idx, const double *weights,
+                               double *y, int32_t nthreads)
 {
     const int H = s->hidden, I = s->inter, E = s->n_experts, K = s->top_k;
     if (H <= 0 || I <= 0 || H % 256 || I % 256 || K <= 0 || K > E || T < 0)
@@ -324,8 +360,17 @@ int oracle_forward_routed(const oracle_shape *s, const uint8_t *gate, const uint
             int e = idx[(int64_t)t * K + k];
             oracle_expert_q2(s, gate + e * expert_gate, up + e * expert_gate, down + e * expert_down, xt, ye);
             double wk = weights[(int64_t)t * K + k];
-            for (int j = 0; j < H; j++)
-                acc[j] += wk * ye[j];
+            for (int j0 = 0; j0 < H; j0 += 32) {
+                double s1[32], s2[32];
+                for (int i = 0; i < 32; i++)
+                    s1[i] = s2[i] = 1.0;
+                if (gain1)
+                    oracle_gain_block(gain1 + ((int64_t)e * (H / 32) + j0 / 32) * GAIN_BYTES, s1);
+                if (gain2)
+                    oracle_gain_block(gain2 + ((int64_t)e * (H / 32) + j0 / 32) * GAIN_BYTES, s2);
+                for (int i = 0; i < 32; i++)
+                    acc[j0 + i] += wk * (s1[i] * s2[i] * ye[j0 + i]);
+            }
         }
         if (has_shared) {
             oracle_shared_q8(s, sh_gate, sh_up, sh_down, xt, ye);
@@ -338,6 +383,16 @@ int oracle_forward_routed(const oracle_shape *s, const uint8_t *gate, const uint
         free(acc);
     }
     return 0;
+}
+
+/* oracle_forward_routed_gain without down gains. */
+int oracle_forward_routed(const oracle_shape *s, const uint8_t *gate, const uint8_t *up,
+                          const uint8_t *down, const uint8_t *sh_gate, const uint8_t *sh_up,
+                          const uint8_t *sh_down, const uint16_t *x, int32_t T, const int32_t *idx,
+                          const double *weights, double *y, int32_t nthreads)
+{
+    return oracle_forward_routed_gain(s, gate, up, down, sh_gate, sh_up, sh_down, NULL, NULL, x, T, idx, weights,
+                                      y, nthreads);
 }
 
 /* Route, then compute the layer. idx/weights/gap may be NULL. */

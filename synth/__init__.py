@@ -37,6 +37,9 @@ SEED_BASE = 0xD54E0000
 
 # stream ids of the counter-based generator
 S_ROUTER, S_GATE, S_UP, S_DOWN, S_SH_GATE, S_SH_UP, S_SH_DOWN, S_BIAS_RANK = range(1, 9)
+S_GAIN1, S_GAIN2 = 9, 10
+GAIN_BLOCK_BYTES = 17
+GAIN_SCALE_BYTE = 127 - 5  # E8M0 2^-5: gains 1 + 2^-5 * e2m1 in [0.8125, 1.1875]
 S_X = 16
 
 Q2_BLOCK_BYTES = 84
@@ -66,6 +69,7 @@ def _load():
         u8p = ctypes.POINTER(ctypes.c_uint8)
         lib.synth_fill_q2.argtypes = [u8p, ctypes.c_int64, ctypes.c_uint64, ctypes.c_uint64, ctypes.c_double]
         lib.synth_fill_q8.argtypes = [u8p, ctypes.c_int64, ctypes.c_uint64, ctypes.c_uint64, ctypes.c_double]
+        lib.synth_fill_gain.argtypes = [u8p, ctypes.c_int64, ctypes.c_uint64, ctypes.c_uint64, ctypes.c_uint8]
         lib.synth_fill_normal_f32.argtypes = [ctypes.POINTER(ctypes.c_float), ctypes.c_int64,
                                               ctypes.c_uint64, ctypes.c_uint64, ctypes.c_double]
         lib.synth_fill_normal_bf16.argtypes = [ctypes.POINTER(ctypes.c_uint16), ctypes.c_int64,
@@ -189,8 +193,19 @@ def zipf_beta(layer_seed: int) -> float:
     return float(table["beta"][str(layer_seed)])
 
 
-def make_layer(shape: Shape, seed: int, zipf: bool = False, zipf_beta_value: float | None = None) -> dict:
-    """All weights of one layer in canonical layout (host numpy arrays)."""
+def gain_table(n_experts: int, hidden: int, seed: int, stream: int, scale_byte: int = GAIN_SCALE_BYTE) -> np.ndarray:
+    """Per-expert down gains: [E][H/32] blocks of 17 bytes (FP4 codes, E8M0 scale)."""
+    n = n_experts * (hidden // 32)
+    out = np.empty(n * GAIN_BLOCK_BYTES, dtype=np.uint8)
+    _load().synth_fill_gain(_ptr(out, ctypes.c_uint8), n, seed, stream, scale_byte)
+    return out.reshape(n_experts, hidden // 32, GAIN_BLOCK_BYTES)
+
+
+def make_layer(shape: Shape, seed: int, zipf: bool = False, zipf_beta_value: float | None = None,
+               gains: int = 0) -> dict:
+    """All weights of one layer in canonical layout (host numpy arrays).
+
+    gains: number of down-gain tables to draw (0, 1 or 2) as "down_gain", "down_gain2"."""
     H, I, E, Ish = shape.hidden, shape.inter, shape.n_experts, shape.shared_inter
     layer = {
         "router_w": normal_f32(E * H, seed, S_ROUTER, 0.02).reshape(E, H),
@@ -208,6 +223,10 @@ def make_layer(shape: Shape, seed: int, zipf: bool = False, zipf_beta_value: flo
     if zipf:
         beta = zipf_beta(seed) if zipf_beta_value is None else zipf_beta_value
         layer["router_bias"] = (beta * zipf_profile(E, seed)).astype(np.float32)
+    if gains >= 1:
+        layer["down_gain"] = gain_table(E, H, seed, S_GAIN1)
+    if gains >= 2:
+        layer["down_gain2"] = gain_table(E, H, seed, S_GAIN2)
     return layer
 
 

@@ -142,6 +142,25 @@ void synth_fill_q2(uint8_t *out, int64_t nblocks, uint64_t seed, uint64_t stream
 }
 
 /*
+ * Down-gain blocks (17 bytes per 32 channels): 16 bytes of uniform random FP4
+ * codes, then the E8M0 scale byte `scale_byte` (the same for every block).
+ * Block b uses draws 2*b, 2*b+1 of the stream.
+ */
+void synth_fill_gain(uint8_t *out, int64_t nblocks, uint64_t seed, uint64_t stream, uint8_t scale_byte)
+{
+    uint64_t key = stream_key(seed, stream);
+#pragma omp parallel for schedule(static)
+    for (int64_t b = 0; b < nblocks; b++) {
+        uint8_t *blk = out + b * 17;
+        for (int w = 0; w < 2; w++) {
+            uint64_t r = draw(key, (uint64_t)b * 2 + w);
+            memcpy(blk + 8 * w, &r, 8);
+        }
+        blk[16] = scale_byte;
+    }
+}
+
+/*
  * 8-bit blocks: codes uniform in [-127, 127], d = |N(0, sigma)|.
  * Block b uses draws 18*b .. 18*b+17.
  */

@@ -43,3 +43,11 @@ def bf16_bits(v) -> np.ndarray:
     bits = a.view(np.uint32)
     assert (bits & 0xFFFF == 0).all(), "value not exact in bf16"
     return (bits >> 16).astype(np.uint16)
+
+
+def gain_block(codes, scale_byte: int) -> bytes:
+    """Down-gain block: 32 four-bit E2M1 codes, channel i in byte i // 2 with the
+    even channel in the low nibble, then the E8M0 scale byte."""
+    c = np.broadcast_to(np.asarray(codes, dtype=np.int64), (32,))
+    assert ((0 <= c) & (c < 16)).all() and 0 <= scale_byte < 256
+    return bytes(int(c[2 * b]) | (int(c[2 * b + 1]) << 4) for b in range(16)) + bytes([scale_byte])

@@ -46,7 +46,16 @@ MUTANTS = {
     "no_renormalisation": [("score[order[k].e] / total : 1.0 / K;", "score[order[k].e] : 1.0 / K;")],
     "gate_up_exchanged": [("h[i] = oracle_silu(g) * u;\n    }\n    for (int j = 0; j < H; j++) {\n        oracle_dequant_q2_row",
                            "h[i] = oracle_silu(u) * g;\n    }\n    for (int j = 0; j < H; j++) {\n        oracle_dequant_q2_row")],
-    "routing_weight_dropped": [("acc[j] += wk * ye[j];", "acc[j] += ye[j];")],
+    "routing_weight_dropped": [("acc[j0 + i] += wk * (s1[i] * s2[i] * ye[j0 + i]);",
+                                "acc[j0 + i] += (s1[i] * s2[i] * ye[j0 + i]);")],
+    "gain_nibble_high_first": [("(blk[i / 2] >> (4 * (i % 2))) & 15", "(blk[i / 2] >> (4 - 4 * (i % 2))) & 15")],
+    "gain_stores_s_not_s_minus_1": [("s[i] = 1.0 + X * oracle_e2m1", "s[i] = X * oracle_e2m1")],
+    "gain_tables_added": [("s1[i] * s2[i] * ye[j0 + i]", "(s1[i] + s2[i] - 1.0) * ye[j0 + i]")],
+    "gain_second_table_ignored": [("s1[i] * s2[i] * ye[j0 + i]", "s1[i] * ye[j0 + i]")],
+    "gain_indexed_by_slot": [("gain1 + ((int64_t)e * (H / 32)", "gain1 + ((int64_t)k * (H / 32)")],
+    "e2m1_exponent_bias": [("ldexp(1.0 + 0.5 * man, ex - 1)", "ldexp(1.0 + 0.5 * man, ex - 2)")],
+    "e2m1_no_subnormal": [("ex == 0 ? 0.5 * man :", "ex == 0 ? 0.0 :")],
+    "e8m0_bias": [("ldexp(1.0, (int)x - 127)", "ldexp(1.0, (int)x - 128)")],
     "shared_dropped": [("acc[j] += ye[j];\n        }", "acc[j] += 0.0 * ye[j];\n        }")],
     "shared_weighted": [("acc[j] += ye[j];\n        }", "acc[j] += weights[(int64_t)t * K] * ye[j];\n        }")],
     "down_uses_gate_activation": [("ye[j] = dot(w, h, I);", "ye[j] = dot(w, xt, I);")],

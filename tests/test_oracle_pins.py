@@ -16,7 +16,7 @@ import pytest
 
 import oracle
 import synth
-from handmade import as_u8, bf16_bits, f16_bits, q2_block, q8_block
+from handmade import as_u8, bf16_bits, f16_bits, gain_block, q2_block, q8_block
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "blocks.json")
 
@@ -430,3 +430,118 @@ def test_dense_cross_check(tiny):
     # routing by numpy over the oracle's own fp32 selection scores
     for t in range(x.shape[0]):
         assert list(r["idx"][t]) == list(_expected_topk(r["sel"][t], shape.top_k))
+
+
+# ---- per-expert down gains ---------------------------------------------------
+# "YoungAi - DeepSeek V4.1 Flash on one DGX Spark", section 4.2: the gains are
+# FP4 E2M1 with one scale per 32 channels in 17-byte blocks, the stored lattice
+# value is s - 1, and the block sum is y = sum_k rw_k (s_e ⊙ ye_k) + ysh;
+# section 3: g_eff = g_base * s_sidecar * s_posttrain (two tables multiply).
+
+# OCP microscaling E2M1: exponent bias 1, one mantissa bit, exponent 0 subnormal;
+# the eight magnitudes of the format as the standard lists them.
+E2M1_MAGNITUDES = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+
+
+def test_e2m1_code_table():
+    got = [oracle.e2m1(c) for c in range(16)]
+    assert got[:8] == E2M1_MAGNITUDES
+    assert got[8:] == [-v for v in E2M1_MAGNITUDES]
+    assert math.copysign(1.0, got[8]) == -1.0  # code 8 is negative zero
+    # "E2M1 has only 8 magnitudes"
+    assert len({abs(v) for v in got}) == 8
+
+
+def test_e8m0_scale():
+    assert oracle.e8m0(127) == 1.0
+    assert oracle.e8m0(127 - 5) == 2.0 ** -5
+    assert oracle.e8m0(0) == 2.0 ** -127
+    assert oracle.e8m0(254) == 2.0 ** 127
+    assert math.isnan(oracle.e8m0(255))
+
+
+def test_gain_block_fields():
+    """Channel i reads nibble i % 2 of byte i // 2 (even channel low), scale byte last."""
+    codes = [(5 * i + 3) % 16 for i in range(32)]
+    blk = np.frombuffer(gain_block(codes, 127 - 3), np.uint8)
+    want = [1.0 + 2.0 ** -3 * (E2M1_MAGNITUDES[c & 7] * (-1 if c & 8 else 1)) for c in codes]
+    assert list(oracle.gain_block(blk)) == want
+    # a single nonzero code lands on its own channel only
+    for ch in (0, 1, 6, 31):
+        c = [0] * 32
+        c[ch] = 7  # +6
+        s = oracle.gain_block(np.frombuffer(gain_block(c, 127 - 4), np.uint8))
+        assert s[ch] == 1.0 + 6 * 2.0 ** -4 and np.count_nonzero(s != 1.0) == 1
+
+
+def test_gain_table_sizes_match_the_pages():
+    """17 bytes per 32 channels of each expert: with the pages' 5,120 channels,
+    384 experts and top-6, about 40 MB for 39 layers and about 0.6 MB read per
+    decoded token (sections 3 and 4.2)."""
+    H, E, K, layers = 5120, 384, 6, 39
+    t = synth.gain_table(2, H, 1, synth.S_GAIN1)
+    assert t.shape == (2, H // 32, synth.GAIN_BLOCK_BYTES) and synth.GAIN_BLOCK_BYTES == 17
+    per_expert = t[0].nbytes
+    assert abs(E * per_expert * layers / 40e6 - 1) < 0.05
+    assert abs(K * per_expert * layers / 0.6e6 - 1) < 0.1
+
+
+def test_unit_gains_leave_the_layer_unchanged(tiny):
+    shape, layer, x = tiny
+    y0, r = oracle.forward(shape, layer, x)
+    L = dict(layer)
+    nb = shape.hidden // 32
+    ones = as_u8([[gain_block(0, 127) for _ in range(nb)] for _ in range(shape.n_experts)])
+    zeros_neg = as_u8([[gain_block(8, 3) for _ in range(nb)] for _ in range(shape.n_experts)])
+    L["down_gain"], L["down_gain2"] = ones, zeros_neg
+    y1 = oracle.forward_routed(shape, L, x, r["idx"], r["weights"])
+    assert np.array_equal(y0, y1)
+
+
+def test_gain_closed_form_one_expert():
+    """E=K=1: y_j = s1_j s2_j (c_j - e_j) sum_i h_i, per output channel."""
+    H, I = 512, 256
+    gate, up, down, xval, y_plain = _one_expert_layer(H, I)
+    nb = H // 32
+    c1 = [[(j + 3 * b) % 16 for j in range(32)] for b in range(nb)]
+    c2 = [[(7 * j + b) % 16 for j in range(32)] for b in range(nb)]
+    g1 = as_u8([[gain_block(c1[b], 127 - 3) for b in range(nb)]])
+    g2 = as_u8([[gain_block(c2[b], 127 - 4) for b in range(nb)]])
+
+    def val(c):
+        return E2M1_MAGNITUDES[c & 7] * (-1 if c & 8 else 1)
+    s1 = np.array([1 + 2.0 ** -3 * val(c1[j // 32][j % 32]) for j in range(H)])
+    s2 = np.array([1 + 2.0 ** -4 * val(c2[j // 32][j % 32]) for j in range(H)])
+    shape = synth.Shape(H, I, 1, 1, 0)
+    layer = {"gate": gate.reshape(1, I, H // 256, 84), "up": up.reshape(1, I, H // 256, 84),
+             "down": down.reshape(1, H, I // 256, 84), "sh_gate": None, "sh_up": None, "sh_down": None,
+             "down_gain": g1}
+    x = bf16_bits(np.float32(xval)[None, :])
+    idx, w = np.zeros((1, 1), np.int32), np.ones((1, 1))
+    y1 = oracle.forward_routed(shape, layer, x, idx, w)
+    assert np.allclose(y1[0], s1 * y_plain, rtol=1e-13, atol=0)
+    layer["down_gain2"] = g2
+    y2 = oracle.forward_routed(shape, layer, x, idx, w)
+    assert np.allclose(y2[0], s1 * s2 * y_plain, rtol=1e-13, atol=0)
+    del layer["down_gain"]
+    y3 = oracle.forward_routed(shape, layer, x, idx, w)
+    assert np.allclose(y3[0], s2 * y_plain, rtol=1e-13, atol=0)
+
+
+def test_gain_correction_is_routed_per_expert(tiny):
+    """Delta = sum_k rw_k (s_{e_k} - 1) ⊙ ye_k: the gains of the expert a token
+    picked, never those of its k-th slot or of another expert."""
+    shape, layer, x = tiny
+    y0, r = oracle.forward(shape, layer, x)
+    L = dict(layer)
+    L["down_gain"] = synth.gain_table(shape.n_experts, shape.hidden, 7, synth.S_GAIN1, 127 - 2)
+    y1 = oracle.forward_routed(shape, L, x, r["idx"], r["weights"])
+    xf = synth.bf16_bits_to_f32(x).astype(np.float64)
+    for t in range(x.shape[0]):
+        delta = np.zeros(shape.hidden)
+        for k in range(shape.top_k):
+            e = int(r["idx"][t, k])
+            s = np.concatenate([oracle.gain_block(b) for b in L["down_gain"][e]])
+            ye = oracle.expert(shape, layer["gate"][e], layer["up"][e], layer["down"][e], xf[t])
+            delta += r["weights"][t, k] * (s - 1) * ye
+        assert np.allclose(y1[t] - y0[t], delta, rtol=1e-9, atol=1e-12 * np.abs(y0[t]).max())
