@@ -42,10 +42,13 @@ def parse():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="decode_t1",
-                    choices=["decode_t1", "decode_t8", "prefill_t1024", "prefill_t4096_zipf4", "tiny", "prefill_profile"])
+                    choices=["decode_t1", "decode_t8", "prefill_t1024", "prefill_t4096_zipf4", "tiny", "prefill_profile",
+                             "decode_profile"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile-steps", type=int, default=20)
+    ap.add_argument("--gains", type=int, default=0, choices=[0, 1, 2],
+                    help="per-expert down-gain tables (sidecar, post-training) on every layer")
     return ap.parse_args()
 
 
@@ -55,10 +58,15 @@ Q2_BPW = 84 / 256  # bytes per 2-bit weight
 Q8_BPW = 34 / 32
 
 
-def layer_bytes(shape, T, U):
-    """Bytes the layer must move per call: selected experts, shared expert, router, x in, y out."""
+GAIN_BPC = 17 / 32  # bytes per output channel of one down-gain table
+
+
+def layer_bytes(shape, T, U, gains=0):
+    """Bytes the layer must move per call: selected experts (and their down-gain
+    blocks), shared expert, router, x in, y out."""
     H, I, E, Ish = shape.hidden, shape.inter, shape.n_experts, shape.shared_inter
-    return (U * 3 * H * I * Q2_BPW + 3 * H * Ish * Q8_BPW + 4 * E * H + 2 * T * H + 4 * T * H)
+    return (U * 3 * H * I * Q2_BPW + gains * U * H * GAIN_BPC + 3 * H * Ish * Q8_BPW + 4 * E * H + 2 * T * H
+            + 4 * T * H)
 
 
 def layer_flops(shape, T):
@@ -66,7 +74,7 @@ def layer_flops(shape, T):
     return T * (2 * K * 3 * H * I + 2 * 3 * H * Ish + 2 * E * H)
 
 
-def kernel_bytes(name, shape, T, U):
+def kernel_bytes(name, shape, T, U, gains=0):
     """Algorithmic bytes of one launch of a library kernel (weights it must read plus its activations)."""
     H, I, E, K, Ish = shape.hidden, shape.inter, shape.n_experts, shape.top_k, shape.shared_inter
     P = T * K
@@ -77,9 +85,9 @@ def kernel_bytes(name, shape, T, U):
         "prefill_down_q2": U * H * I * Q2_BPW + 2 * P * I + 4 * P * H,
         "prefill_gateup_q8": 2 * Ish * H * Q8_BPW + 2 * T * H + 2 * T * Ish,
         "prefill_down_q8": H * Ish * Q8_BPW + 2 * T * Ish + 4 * T * H,
-        "combine": 4 * P * H + 4 * T * H + 4 * T * H,
+        "combine": 4 * P * H + 4 * T * H + 4 * T * H + gains * U * H * GAIN_BPC,
         # one launch of the fused decode kernel does the whole layer for up to 8 tokens
-        "decode_fused": layer_bytes(shape, T, U),
+        "decode_fused": layer_bytes(shape, T, U, gains),
     }
     return table.get(name)
 
@@ -97,9 +105,9 @@ TRAFFIC = {
 }
 
 
-def kernel_traffic(name, workload):
+def kernel_traffic(name, workload, gains=0):
     import hashlib
-    rec = TRAFFIC.get((name, workload))
+    rec = TRAFFIC.get((name, workload)) if gains == 0 else None
     if rec is None:
         return None
     path = os.path.join(ROOT, "quantized_moe_expert_gb300", "csrc", rec[1])
@@ -233,10 +241,10 @@ class ClockSampler:
 
 # ---- the workload ----------------------------------------------------------------
 
-def workload_layers(name):
+def workload_layers(name, gains=0):
     import synth
     wl = synth.WORKLOADS[name]
-    return wl, [synth.make_layer(wl.shape, s, zipf=wl.zipf) for s in wl.layer_seeds]
+    return wl, [synth.make_layer(wl.shape, s, zipf=wl.zipf, gains=gains) for s in wl.layer_seeds]
 
 
 def workload_batches(name):
@@ -322,7 +330,7 @@ def run_reference(args, world, rank):
     import synth
     if rank != 0:
         return
-    wl, layers = workload_layers(args.workload)
+    wl, layers = workload_layers(args.workload, args.gains)
     batches = workload_batches(args.workload)
     times = []
     n_tok = None
@@ -336,18 +344,21 @@ def run_reference(args, world, rank):
     out = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * total / len(times),
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-           "config": workload_config(wl, args.workload, None),
+           "config": workload_config(wl, args.workload, None, args.gains),
            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(out))
 
 
-def workload_config(wl, name, l2_note):
+def workload_config(wl, name, l2_note, gains=0):
     s = wl.shape
     cfg = {"workload": name, "description": wl.description, "hidden": s.hidden, "inter": s.inter,
            "n_experts": s.n_experts, "top_k": s.top_k, "shared_inter": s.shared_inter,
            "tokens_per_step": wl.tokens, "layers_per_step": wl.n_layers,
            "weights": "routed 2-bit 84B/256 blocks, shared 8-bit 34B/32 blocks, router fp32"}
+    if gains:
+        cfg["down_gain_tables"] = gains
+        cfg["weights"] += f", {gains} down-gain table(s) of 17B/32-channel FP4 blocks"
     if l2_note:
         cfg["l2"] = l2_note
     return cfg
@@ -367,7 +378,7 @@ def main():
 
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    wl, layers = workload_layers(args.workload)
+    wl, layers = workload_layers(args.workload, args.gains)
     shape = wl.shape
     batches = workload_batches(args.workload)
     T = wl.tokens
@@ -445,7 +456,7 @@ def main():
         ds4.ds4moe_profile(m.handle, False)
     dom = max(ktimes, key=lambda k: ktimes[k][1])
     dom_avg_ms = ktimes[dom][1] / ktimes[dom][0]
-    dom_bytes = kernel_bytes(dom, shape, T, U_mean)
+    dom_bytes = kernel_bytes(dom, shape, T, U_mean, args.gains)
     peaks = {}
     pk_path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(pk_path):
@@ -463,19 +474,19 @@ def main():
         if t_tc > t_hbm:
             ach = dom_flops / sec / 1e12
             roofline = {"bound": "tensor", "kernel": dom, "achieved": ach, "peak": tf_peak, "unit": "TFLOP/s",
-                        "frac": ach / tf_peak, "traffic": kernel_traffic(dom, args.workload),
+                        "frac": ach / tf_peak, "traffic": kernel_traffic(dom, args.workload, args.gains),
                         "peak_source": peak_src + " bf16 burst",
                         "flops_per_launch": dom_flops, "bytes_per_launch": dom_bytes,
                         "hbm_frac": dom_bytes / sec / 1e9 / hbm_peak, "avg_launch_us": 1000 * dom_avg_ms}
         else:
             ach = dom_bytes / sec / 1e9
             roofline = {"bound": "hbm", "kernel": dom, "achieved": ach, "peak": hbm_peak, "unit": "GB/s",
-                        "frac": ach / hbm_peak, "traffic": kernel_traffic(dom, args.workload), "peak_source": peak_src,
+                        "frac": ach / hbm_peak, "traffic": kernel_traffic(dom, args.workload, args.gains), "peak_source": peak_src,
                         "bytes_per_launch": dom_bytes, "avg_launch_us": 1000 * dom_avg_ms}
             if dom_flops:
                 roofline["flops_per_launch"] = dom_flops
                 roofline["tensor_frac"] = dom_flops / sec / 1e12 / tf_peak
-    lay_bytes = layer_bytes(shape, T, U_mean) * len(handles)
+    lay_bytes = layer_bytes(shape, T, U_mean, args.gains) * len(handles)
     layer_gbs = lay_bytes / (ms_per_step / 1000.0) / 1e9
 
     # end to end through host memory
@@ -511,7 +522,7 @@ def main():
         out = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
                "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
                "vs_baseline": None, "dtype": "f32" if T <= 8 else "bf16", "data": "synthetic",
-               "config": workload_config(wl, args.workload, l2_note),
+               "config": workload_config(wl, args.workload, l2_note, args.gains),
                "roofline": roofline,
                "layer_roofline": {"bound": "hbm" if args.workload != "prefill_t4096_zipf4" else "tensor",
                                   "bytes_per_step": lay_bytes, "achieved_gbs": layer_gbs,

@@ -11,11 +11,17 @@
  *   w[t,k]   = s[t,idx[t,k]] / sum_j s[t,idx[t,j]]          mixing weights (bias-free)
  *   ye       = Wd[e] (silu(Wg[e] x_t) * (Wu[e] x_t))        SwiGLU expert, 2-bit weights
  *   ysh      = same with the 8-bit shared expert
- *   y[t]     = sum_k w[t,k] ye_{idx[t,k]}(x_t) + ysh(x_t)
+ *   y[t]     = sum_k w[t,k] (g_{idx[t,k]} * ye_{idx[t,k]}(x_t)) + ysh(x_t)
+ *              with g_e[j] = s1_e[j] * s2_e[j] the optional per-expert down
+ *              gains (elementwise over the H output channels; 1 when absent)
  *
  * The block sum with an unweighted shared expert is the engine's MoE sum of
  * "YoungAi - DeepSeek V4.1 Flash on one DGX Spark", section 4.2 ("The
- * objective", with every sidecar gain s_e = 1). The router bias is added to the
+ * objective"). Its per-expert, per-output-channel gains s_e are the sidecar and
+ * post-training files of the same page (section 3: g_eff = g_base * s_sidecar *
+ * s_posttrain, one factor per down-projection row of an expert; section 4.2:
+ * FP4 E2M1 values of s - 1 with one scale per 32 in 17-byte blocks): the two
+ * optional gain tables s1, s2 below. The router bias is added to the
  * selection score only, mixing weights untouched (same page, section 3 and
  * section 4.2, "The router bias"). 384 experts, 6 per token: same page,
  * section 2.2. Only the routed experts are 2-bit; the shared expert stays
@@ -36,6 +42,13 @@
  *   router_w   fp32 [E][H];  router_bias fp32 [E] or NULL
  *   gate, up   2-bit [E][I][H/256] blocks;  down 2-bit [E][H][I/256] blocks
  *   sh_gate, sh_up 8-bit [I_sh][H/32];  sh_down 8-bit [H][I_sh/32]
+ *   down-gain block, 17 bytes per 32 consecutive output channels of one expert:
+ *     [0,16)  FP4 E2M1 code c_i of channel i at byte i/2, low nibble for even i
+ *             (bit 3 sign, bits 2-1 exponent with bias 1, bit 0 mantissa;
+ *             magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6)
+ *     [16]    E8M0 scale X = 2^(byte - 127) (0xFF is NaN and propagates)
+ *     gain i = 1 + X * e2m1(c_i)
+ *   down_gain, down_gain2   [E][H/32] gain blocks each, or NULL (all gains 1)
  *
  * Conventions of every entry point:
  *   - Return 0 (DS4MOE_OK) or a negative DS4MOE_E* code; nothing is launched
@@ -60,7 +73,7 @@ extern "C" {
 #endif
 
 #define DS4MOE_MAGIC 0x454D3444u /* "D4ME" */
-#define DS4MOE_VERSION 1u
+#define DS4MOE_VERSION 2u /* 2: ds4moe_weights gained down_gain, down_gain2 */
 
 enum {
     DS4MOE_OK = 0,
@@ -105,12 +118,17 @@ typedef struct {
     const void *sh_gate;      /* 8-bit [I_sh][H/32], NULL iff I_sh == 0 */
     const void *sh_up;        /* 8-bit [I_sh][H/32], NULL iff I_sh == 0 */
     const void *sh_down;      /* 8-bit [H][I_sh/32], NULL iff I_sh == 0 */
+    const void *down_gain;    /* gain blocks [E][H/32] (sidecar), or NULL */
+    const void *down_gain2;   /* gain blocks [E][H/32] (post-training), or NULL */
 } ds4moe_weights;
 
 /*
  * Validate the description, copy every weight into library-owned device
  * memory in the kernels' layout, size the scratch for max_tokens, and
  * synchronise. The caller's weight buffers may be freed once this returns.
+ * Down-gain tables, when given, are decoded here into one fp32 gain per expert
+ * and output channel (the product of the two tables; 4*E*H bytes); a handle
+ * created with gains runs the decode kernel built for them.
  * Runs on the current device, which must be a GB300 (sm_103).
  * Errors: EINVAL (desc, NULL or host pointer), EUNSUPPORTED, ENOMEM, ECUDA.
  */

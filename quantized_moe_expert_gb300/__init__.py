@@ -16,7 +16,7 @@ import os
 from ._build import INCLUDE, LIB_PATH, NVCC_FLAGS, build, sources  # noqa: F401
 
 DS4MOE_MAGIC = 0x454D3444
-DS4MOE_VERSION = 1
+DS4MOE_VERSION = 2
 DS4MOE_OK, DS4MOE_EINVAL, DS4MOE_ENOMEM, DS4MOE_ECUDA, DS4MOE_EUNSUPPORTED, DS4MOE_ETIMEOUT, DS4MOE_EDEVICE = (
     0, -1, -2, -3, -4, -5, -6)
 DS4MOE_ESCRATCH = -7
@@ -33,7 +33,8 @@ class LayerDesc(ctypes.Structure):
 class Weights(ctypes.Structure):
     _fields_ = [("router_w", ctypes.c_void_p), ("router_bias", ctypes.c_void_p), ("gate", ctypes.c_void_p),
                 ("up", ctypes.c_void_p), ("down", ctypes.c_void_p), ("sh_gate", ctypes.c_void_p),
-                ("sh_up", ctypes.c_void_p), ("sh_down", ctypes.c_void_p)]
+                ("sh_up", ctypes.c_void_p), ("sh_down", ctypes.c_void_p), ("down_gain", ctypes.c_void_p),
+                ("down_gain2", ctypes.c_void_p)]
 
 
 class Stats(ctypes.Structure):
@@ -192,13 +193,15 @@ def make_desc(hidden, inter, n_experts, top_k, shared_inter, max_tokens, flags=0
 class MoELayer:
     """One ds4moe handle. Weights: dict of device torch tensors in the storage
     formats of ``include/ds4moe.h`` (keys router_w, router_bias, gate, up, down,
-    sh_gate, sh_up, sh_down; router_bias and the shared ones may be None)."""
+    sh_gate, sh_up, sh_down, down_gain, down_gain2; router_bias, the shared ones
+    and the gain tables may be None or absent)."""
 
     def __init__(self, shape, weights: dict, max_tokens: int):
         self.shape = shape
         desc = make_desc(shape.hidden, shape.inter, shape.n_experts, shape.top_k, shape.shared_inter, max_tokens)
         w = Weights(*(_addr(weights.get(k)) for k in
-                      ("router_w", "router_bias", "gate", "up", "down", "sh_gate", "sh_up", "sh_down")))
+                      ("router_w", "router_bias", "gate", "up", "down", "sh_gate", "sh_up", "sh_down", "down_gain",
+                       "down_gain2")))
         self.handle = ds4moe_create(desc, w)
         self.max_tokens = max_tokens
 

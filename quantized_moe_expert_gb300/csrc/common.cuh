@@ -84,6 +84,25 @@ __device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
 
 __device__ __forceinline__ float sigmoid(float z) { return 1.0f / (1.0f + expf(-z)); }
 
+// Down-gain blocks ("YoungAi - DeepSeek V4.1 Flash on one DGX Spark", sections
+// 3 and 4.2): per expert and 32 output channels, 16 bytes of FP4 E2M1 codes
+// (channel i at byte i/2, even channel in the low nibble) and one E8M0 scale
+// byte; gain i = 1 + 2^(scale - 127) * e2m1(code_i).
+constexpr int kGainBlockBytes = 17;
+
+// Twice the E2M1 magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6, one per nibble.
+constexpr unsigned kE2M1Twice = 0xC8643210u;
+
+// Gain of channel c (0..31) of the block at blk. Scale byte 0 gives 2^-127,
+// which leaves 1 + X * v at 1 in fp32 either way; 0xFF is NaN.
+__device__ __forceinline__ float down_gain(const uint8_t *blk, int c) {
+    const unsigned code = ((unsigned)__ldg(blk + (c >> 1)) >> ((c & 1) * 4)) & 15u;
+    const unsigned sb = __ldg(blk + 16);
+    const float X = __uint_as_float(sb == 255u ? 0x7FC00000u : sb << 23);
+    const float v = 0.5f * (float)((kE2M1Twice >> (4 * (code & 7u))) & 15u);
+    return fmaf(X, (code & 8u) ? -v : v, 1.0f);
+}
+
 // Scratch owned by a handle, sized for max_tokens at create time.
 // Pair index p = t * K + k names the k-th routed choice of token t.
 struct Scratch {
@@ -119,6 +138,7 @@ struct LayerDev {
     const float *router_bias;
     Q2Mat gate, up, down; // rows: gate/up E*I (K = H), down E*H (K = I)
     Q8Mat sh_gate, sh_up, sh_down;
+    const float *gain; // [E][H] per-expert down gains s1 * s2 expanded from the tables, or nullptr
 };
 
 } // namespace ds4

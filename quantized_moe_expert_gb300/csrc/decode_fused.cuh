@@ -123,6 +123,7 @@ struct DecodeArgs {
     unsigned *status;
     SelIO io;  // the selection's inputs and outputs (the buffers above)
     SelIO dry; // the rehearsal's: zeroed logits with epoch 0, outputs nothing reads
+    const float *gain; // [E][H] per-expert down gains (the kernel built with GAIN), or nullptr
 };
 
 enum JobType : int { kJobEnd = 0, kJobR, kJobSgu, kJobSel, kJobGu, kJobSd, kJobD };
@@ -171,6 +172,7 @@ struct DecodeSmem {
     const void *pc_src[40];
     unsigned pc_bytes[40];
     unsigned pc_dst[40];
+    int cexp[kDecodeT * kMaxTopK]; // publisher, with down gains: the experts of the tile's pairs
 };
 
 // ---- small PTX helpers --------------------------------------------------------
@@ -1212,7 +1214,7 @@ __device__ bool wait_slot(const DecodeArgs &a, int sl, SlotRec &r) {
     }
 }
 
-__device__ void producer(const DecodeArgs &a, DecodeSmem &sm, const JobSpace &js) {
+template <bool GAIN> __device__ void producer(const DecodeArgs &a, DecodeSmem &sm, const JobSpace &js) {
     unsigned n = 0; // stages issued so far
     int cached_slot = -1; // GU and D jobs come slot by slot: keep the last record
     SlotRec rec{};
@@ -1287,6 +1289,12 @@ __device__ void producer(const DecodeArgs &a, DecodeSmem &sm, const JobSpace &js
                 continue; // fewer distinct experts than the bound
             e = rec.e;
             ntok = rec.ntok;
+            if constexpr (GAIN) {
+                // the gains of this job's 32 output rows (one 128-byte line), read by the
+                // tile's combine: on their way to L2 long before it
+                if (type == kJobD && (threadIdx.x & 31) == 0)
+                    asm volatile("prefetch.global.L2 [%0];" ::"l"(a.gain + (int64_t)e * a.H + tile * 32));
+            }
 #pragma unroll
             for (int i = 0; i < kDecodeT; i++) {
                 const int ii = i < ntok ? i : 0;
@@ -1439,11 +1447,13 @@ __device__ void producer(const DecodeArgs &a, DecodeSmem &sm, const JobSpace &js
 // shared. The publisher warp, one row per lane: the routing weights and pair
 // positions of all tokens go through shared memory in one round trip, then
 // the expert outputs of two tokens at a time.
-__device__ void combine_tile(const DecodeArgs &a, DecodeSmem &sm, int ti, int lane) {
+template <bool GAIN> __device__ void combine_tile(const DecodeArgs &a, DecodeSmem &sm, int ti, int lane) {
     const int P = a.T * a.K;
     for (int p = lane; p < P; p += 32) {
         sm.cw[p] = __ldcg(a.w + p);
         sm.cinv[p] = __ldcg(a.inv + p);
+        if constexpr (GAIN)
+            sm.cexp[p] = __ldcg(a.idx + p);
     }
     __syncwarp();
     const int col = ti * 32 + lane;
@@ -1457,6 +1467,12 @@ __device__ void combine_tile(const DecodeArgs &a, DecodeSmem &sm, int ti, int la
                 if (k < a.K)
                     ye[u][k] = __ldcg(a.ye + (int64_t)sm.cinv[t * a.K + k] * a.H + col);
             sh[u] = a.Ish > 0 ? __ldcg(a.ysh + (int64_t)t * a.H + col) : 0.f;
+            if constexpr (GAIN) {
+#pragma unroll
+                for (int k = 0; k < kMaxTopK; k++)
+                    if (k < a.K)
+                        ye[u][k] *= __ldg(a.gain + (int64_t)sm.cexp[t * a.K + k] * a.H + col);
+            }
         }
 #pragma unroll
         for (int u = 0; u < 2; u++) {
@@ -1499,7 +1515,7 @@ __device__ bool publish(const DecodeArgs &a, DecodeSmem &sm, unsigned &npub, int
 // contribution to the 32-row tile, and the last of the nuniq contributions
 // combines the tile once the shared expert's down rows are complete (those
 // jobs precede every D job in the queue, so the wait ends).
-__device__ void publisher(const DecodeArgs &a, const JobSpace &js, DecodeSmem &sm, int lane) {
+template <bool GAIN> __device__ void publisher(const DecodeArgs &a, const JobSpace &js, DecodeSmem &sm, int lane) {
     for (unsigned k = 0;; k++) {
         const int s = (int)(k % kPubQ);
         if (!mbar_wait(a, &sm.pub_full[s], (k / kPubQ) & 1u))
@@ -1526,7 +1542,7 @@ __device__ void publisher(const DecodeArgs &a, const JobSpace &js, DecodeSmem &s
                 }
             }
             if (__shfl_sync(0xFFFFFFFFu, last, 0))
-                combine_tile(a, sm, tile, lane);
+                combine_tile<GAIN>(a, sm, tile, lane);
         }
         __syncwarp();
         if (lane == 0)
@@ -1752,7 +1768,8 @@ template <int TPM> __device__ void consumer(const DecodeArgs &a, DecodeSmem &sm,
 }
 
 // TPM: the largest padded token count of a job in this launch (1, 2, 4 or 8).
-template <int TPM> __global__ void __launch_bounds__(kDecodeThreads, 2) decode_fused_kernel(DecodeArgs a) {
+template <int TPM, bool GAIN = false>
+__global__ void __launch_bounds__(kDecodeThreads, 2) decode_fused_kernel(DecodeArgs a) {
     extern __shared__ __align__(128) uint8_t dsmem[];
     DecodeSmem &sm = *reinterpret_cast<DecodeSmem *>(dsmem);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -1770,9 +1787,9 @@ template <int TPM> __global__ void __launch_bounds__(kDecodeThreads, 2) decode_f
     __syncthreads();
     const JobSpace js = job_space(a);
     if (warp == kConsumerWarps) {
-        producer(a, sm, js);
+        producer<GAIN>(a, sm, js);
     } else if (warp == kConsumerWarps + 1) {
-        publisher(a, js, sm, lane);
+        publisher<GAIN>(a, js, sm, lane);
     } else {
         consumer<TPM>(a, sm, js, warp, lane);
     }

@@ -119,6 +119,7 @@ struct ds4moe {
     void *scratch_mem = nullptr;
     uint64_t scratch_bytes = 0;
     ds4moe_stats stats{};
+    bool has_gain[2] = {false, false};
 };
 
 namespace {
@@ -215,6 +216,23 @@ __global__ void repack_q8_kernel(const uint16_t *__restrict__ src, int64_t nbloc
     d[(ts * 128 + r) * 2 + hb] = s[0];
 }
 
+// Down-gain tables ([E][H/32] 17-byte blocks each, either may be null) -> one
+// fp32 gain per expert and output channel, the product s1 * s2.
+__global__ void expand_gain_kernel(const uint8_t *__restrict__ g1, const uint8_t *__restrict__ g2, int E, int H,
+                                   float *__restrict__ out) {
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= (int64_t)E * H)
+        return;
+    const int64_t blk = (i / 32) * kGainBlockBytes; // channel blocks of 32 run over [E][H/32]
+    const int c = (int)(i % 32);
+    float g = 1.f;
+    if (g1)
+        g = down_gain(g1 + blk, c);
+    if (g2)
+        g *= down_gain(g2 + blk, c);
+    out[i] = g;
+}
+
 // fp32 router rows -> three bf16 parts (round to nearest each), stored side by
 // side per row: w = hi + mid + lo exactly, since each remainder is exact in fp32
 // and three 8-bit significands cover fp32's 24.
@@ -276,6 +294,7 @@ void layout_weights(ds4moe *h, Carver &c) {
         q8(L.sh_up, L.Ish, L.H);
         q8(L.sh_down, L.H, L.Ish);
     }
+    L.gain = h->has_gain[0] || h->has_gain[1] ? c.take<float>((uint64_t)L.E * L.H) : nullptr;
     DecodeState &D = h->D;
     auto f2 = [&](Q2Frag &m, int64_t rows, int k) {
         m.rows = rows;
@@ -589,7 +608,7 @@ int run_experts_prefill(ds4moe *h, const void *x, int T, float *y) {
     }
     launch(h, "combine", [&] {
         combine_kernel<<<blocks_for((int64_t)T * L.H / 4, 256), 256, 0, st>>>(
-            S.ye, L.Ish > 0 ? S.ysh : nullptr, S.w, S.inv, T, L.H, L.K, y);
+            S.ye, L.Ish > 0 ? S.ysh : nullptr, S.w, S.inv, S.idx, L.gain, T, L.H, L.K, y);
     });
     return launch_rc();
 }
@@ -648,9 +667,13 @@ int run_decode(ds4moe *h, const void *x, int T, float *y, const int32_t *forced_
         a.status = h->status;
         a.io = SelIO{a.lgt, a.epoch, a.idx, a.w, a.gap, a.inv, a.counts, a.nuniq, a.srec};
         a.dry = D.dry;
+        a.gain = L.gain;
         void *args[] = {&a};
         launch(h, "decode_fused", [&] {
-            const void *fn = Tc <= 1   ? (const void *)decode_fused_kernel<1>
+            // with down gains: the kernels built for them (one token; up to 8)
+            const void *fn = L.gain    ? (Tc <= 1 ? (const void *)decode_fused_kernel<1, true>
+                                                  : (const void *)decode_fused_kernel<8, true>)
+                             : Tc <= 1 ? (const void *)decode_fused_kernel<1>
                              : Tc <= 2 ? (const void *)decode_fused_kernel<2>
                              : Tc <= 4 ? (const void *)decode_fused_kernel<4>
                                        : (const void *)decode_fused_kernel<8>;
@@ -720,6 +743,8 @@ int ds4moe_create(const ds4moe_layer_desc *desc, const ds4moe_weights *w, ds4moe
         return DS4MOE_EINVAL;
     if (w->router_bias && !is_device_ptr(w->router_bias))
         return DS4MOE_EINVAL;
+    if ((w->down_gain && !is_device_ptr(w->down_gain)) || (w->down_gain2 && !is_device_ptr(w->down_gain2)))
+        return DS4MOE_EINVAL;
     const bool has_shared = desc->shared_inter > 0;
     if (has_shared != (w->sh_gate != nullptr) || has_shared != (w->sh_up != nullptr) ||
         has_shared != (w->sh_down != nullptr))
@@ -751,6 +776,8 @@ int ds4moe_create(const ds4moe_layer_desc *desc, const ds4moe_weights *w, ds4moe
     L.K = desc->top_k;
     L.Ish = desc->shared_inter;
     L.Tmax = desc->max_tokens;
+    h->has_gain[0] = w->down_gain != nullptr;
+    h->has_gain[1] = w->down_gain2 != nullptr;
 
     Carver probe{nullptr};
     layout_weights(h, probe);
@@ -818,6 +845,10 @@ int ds4moe_create(const ds4moe_layer_desc *desc, const ds4moe_weights *w, ds4moe
         rq8(w->sh_up, L.sh_up);
         rq8(w->sh_down, L.sh_down);
     }
+    if (L.gain)
+        expand_gain_kernel<<<blocks_for((int64_t)L.E * L.H, 256), 256, 0, st>>>(
+            static_cast<const uint8_t *>(w->down_gain), static_cast<const uint8_t *>(w->down_gain2), L.E, L.H,
+            const_cast<float *>(L.gain));
     DecodeState &D = h->D;
     auto rf2 = [&](const void *src, Q2Frag &m) {
         const int64_t n = (m.rows / 16) * m.nkc * 32;
@@ -845,7 +876,8 @@ int ds4moe_create(const ds4moe_layer_desc *desc, const ds4moe_weights *w, ds4moe
     cudaMemsetAsync(const_cast<unsigned long long *>(D.dry.lgt), 0, sizeof(unsigned long long) * kDecodeT * L.E, st);
     int per_sm = 0, nsm = 0;
     for (const void *fn : {(const void *)decode_fused_kernel<1>, (const void *)decode_fused_kernel<2>,
-                           (const void *)decode_fused_kernel<4>, (const void *)decode_fused_kernel<8>})
+                           (const void *)decode_fused_kernel<4>, (const void *)decode_fused_kernel<8>,
+                           (const void *)decode_fused_kernel<1, true>, (const void *)decode_fused_kernel<8, true>})
         cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(DecodeSmem));
     // every variant has the same threads and shared memory and the same launch bound of two CTAs per SM
     cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_fused_kernel<8>, kDecodeThreads, sizeof(DecodeSmem));

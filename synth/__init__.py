@@ -131,6 +131,11 @@ WORKLOADS = {
     "prefill_profile": Workload("prefill_profile", Shape(4096, 2048, 48, 6, 2048), 128, 1, False,
                                 (SEED_BASE + 5,),
                                 "profiling case: H=4096 I=2048 E=48 top-6 I_sh=2048, T=128"),
+    # The same for the decode kernel: one token, the full-size expert matrices,
+    # 48 experts, so a full profiler capture holds ~0.8 GB on the device.
+    "decode_profile": Workload("decode_profile", Shape(4096, 2048, 48, 6, 2048), 1, 1, False,
+                               (SEED_BASE + 7,),
+                               "profiling case: H=4096 I=2048 E=48 top-6 I_sh=2048, T=1"),
 }
 
 
@@ -258,4 +263,6 @@ def make_tokens(workload: str, T: int | None = None, first: int = 0) -> np.ndarr
         return normal_bf16(T * H, SEED_BASE + 4 + 0x10000, S_X).reshape(T, H)
     if workload == "prefill_profile":
         return normal_bf16(T * H, SEED_BASE + 5 + 0x10000, S_X).reshape(T, H)
+    if workload == "decode_profile":
+        return normal_bf16(T * H, SEED_BASE + 7 + 0x10000, S_X).reshape(T, H)
     raise KeyError(workload)

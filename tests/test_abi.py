@@ -48,8 +48,9 @@ def test_create_rejects_bad_descriptions_on_the_host():
     d.magic = 0
     assert ds4._lib.ds4moe_create(ctypes.byref(d), ctypes.byref(w), ctypes.byref(h)) == ds4.DS4MOE_EINVAL
     d = ds4.make_desc(**good)
-    d.version = 2
-    assert ds4._lib.ds4moe_create(ctypes.byref(d), ctypes.byref(w), ctypes.byref(h)) == ds4.DS4MOE_EINVAL
+    for v in (ds4.DS4MOE_VERSION - 1, ds4.DS4MOE_VERSION + 1):
+        d.version = v
+        assert ds4._lib.ds4moe_create(ctypes.byref(d), ctypes.byref(w), ctypes.byref(h)) == ds4.DS4MOE_EINVAL
     # good description, NULL weight pointers
     d = ds4.make_desc(**good)
     assert ds4._lib.ds4moe_create(ctypes.byref(d), ctypes.byref(w), ctypes.byref(h)) == ds4.DS4MOE_EINVAL
