@@ -99,9 +99,9 @@ def kernel_bytes(name, shape, T, U, gains=0):
 TRAFFIC = {
     ("prefill_gateup_q2", "prefill_t1024"): (2188943104, "prefill_gemm.cuh", "176ab889561ec6a276190a5b483d024d2b135d84"),
     ("prefill_down_q2", "prefill_t1024"): (1173745664, "prefill_gemm.cuh", "176ab889561ec6a276190a5b483d024d2b135d84"),
-    ("decode_fused", "decode_t1"): (83702912, "decode_fused.cuh", "fb3b603c48074acc7e1711de5e382639e51e2b47"),
+    ("decode_fused", "decode_t1"): (83795456, "decode_fused.cuh", "c3a4518df8e819c3a4930bd75a1d2552eb01a012"),
     # mean of two batches of the pool (43-47 distinct experts each; the traffic follows the batch's experts)
-    ("decode_fused", "decode_t8"): (404590208, "decode_fused.cuh", "fb3b603c48074acc7e1711de5e382639e51e2b47"),
+    ("decode_fused", "decode_t8"): (404583680, "decode_fused.cuh", "c3a4518df8e819c3a4930bd75a1d2552eb01a012"),
 }
 
 

@@ -5,7 +5,8 @@
 // expert for all rows that chose it - is the verify-batch expert kernel of
 // "YoungAi - DeepSeek V4.1 Flash on one DGX Spark", section 4.4 ("a persistent
 // expert kernel over (unique expert x rows) that reads each chosen expert's
-// bits once").
+// bits once"). The prefill path's weighted combine, which reads the grouped
+// outputs back in token order, sits at the end.
 #pragma once
 
 #include "common.cuh"
@@ -91,6 +92,46 @@ __global__ void dispatch_place_kernel(const int32_t *__restrict__ idx, int npair
         base += total;
         __syncthreads();
     }
+}
+
+// The prefill path's combine, after its grouped GEMMs.
+// y[t][j] = sum_k w[t][k] * (g[e][j] * ye[inv[t*K+k]][j]) + ysh[t][j], e =
+// idx[t*K+k], summed in k order and then the shared term, so the result does
+// not depend on the schedule. g: [E][H] per-expert down gains, or nullptr (1).
+__global__ void combine_kernel(const float *__restrict__ ye, const float *__restrict__ ysh,
+                               const float *__restrict__ w, const int32_t *__restrict__ inv,
+                               const int32_t *__restrict__ idx, const float *__restrict__ g, int T, int H, int K,
+                               float *__restrict__ y) {
+    const int64_t i4 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t n4 = (int64_t)T * H / 4;
+    if (i4 >= n4)
+        return;
+    const int t = (int)((i4 * 4) / H);
+    const int j = (int)((i4 * 4) % H);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int k = 0; k < K; k++) {
+        const float wk = w[(int64_t)t * K + k];
+        float4 v = *reinterpret_cast<const float4 *>(ye + (int64_t)inv[(int64_t)t * K + k] * H + j);
+        if (g) {
+            const float4 s = __ldg(reinterpret_cast<const float4 *>(g + (int64_t)idx[(int64_t)t * K + k] * H + j));
+            v.x *= s.x;
+            v.y *= s.y;
+            v.z *= s.z;
+            v.w *= s.w;
+        }
+        acc.x = fmaf(wk, v.x, acc.x);
+        acc.y = fmaf(wk, v.y, acc.y);
+        acc.z = fmaf(wk, v.z, acc.z);
+        acc.w = fmaf(wk, v.w, acc.w);
+    }
+    if (ysh) {
+        const float4 s = *reinterpret_cast<const float4 *>(ysh + (int64_t)t * H + j);
+        acc.x += s.x;
+        acc.y += s.y;
+        acc.z += s.z;
+        acc.w += s.w;
+    }
+    *reinterpret_cast<float4 *>(y + (int64_t)t * H + j) = acc;
 }
 
 } // namespace ds4
