@@ -47,6 +47,9 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile-steps", type=int, default=20)
+    ap.add_argument("--crossover", action="store_true",
+                    help="time the decode and the prefill path on the decode layer for T = 1..64 and print "
+                         "one JSON line of the per-T medians (not a bench line)")
     ap.add_argument("--gains", type=int, default=0, choices=[0, 1, 2],
                     help="per-expert down-gain tables (sidecar, post-training) on every layer")
     return ap.parse_args()
@@ -97,8 +100,8 @@ def kernel_bytes(name, shape, T, U, gains=0):
 # with the SHA-1 of the kernel's source file at capture time: the figure is
 # reported only while that source is unchanged.
 TRAFFIC = {
-    ("prefill_gateup_q2", "prefill_t1024"): (2188943104, "prefill_gemm.cuh", "176ab889561ec6a276190a5b483d024d2b135d84"),
-    ("prefill_down_q2", "prefill_t1024"): (1173745664, "prefill_gemm.cuh", "176ab889561ec6a276190a5b483d024d2b135d84"),
+    ("prefill_gateup_q2", "prefill_t1024"): (2188538368, "prefill_gemm.cuh", "d7c7eaefd5d9bbc2898ca2a38b0ed443da38ec51"),
+    ("prefill_down_q2", "prefill_t1024"): (1174258176, "prefill_gemm.cuh", "d7c7eaefd5d9bbc2898ca2a38b0ed443da38ec51"),
     ("decode_fused", "decode_t1"): (83795456, "decode_fused.cuh", "c3a4518df8e819c3a4930bd75a1d2552eb01a012"),
     # mean of two batches of the pool (43-47 distinct experts each; the traffic follows the batch's experts)
     ("decode_fused", "decode_t8"): (404583680, "decode_fused.cuh", "c3a4518df8e819c3a4930bd75a1d2552eb01a012"),
@@ -364,11 +367,71 @@ def workload_config(wl, name, l2_note, gains=0):
     return cfg
 
 
+CROSSOVER_T = (1, 2, 4, 6, 8, 9, 12, 16, 24, 32, 48, 64)
+
+
+def run_crossover(args):
+    """Both paths on the H=4096, E=384 decode layer for each T of CROSSOVER_T:
+    tokens ~N(0,1) bf16 from seed SEED_BASE + 0x100 + T, L2 flushed before every
+    call, median of 15 calls after 3 warm-up calls (CUDA events)."""
+    import torch
+
+    import quantized_moe_expert_gb300 as ds4
+    import synth
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    wl, layers = workload_layers("decode_t1", args.gains)
+    shape = wl.shape
+    w = {k: (None if v is None else torch.from_numpy(np.ascontiguousarray(v)).to(dev)) for k, v in layers[0].items()}
+    moe = ds4.MoELayer(shape, w, max_tokens=max(CROSSOVER_T))
+    del w
+    torch.cuda.empty_cache()
+    stream = torch.cuda.current_stream(dev)
+    moe.set_stream(stream)
+    flush = torch.empty(2 * torch.cuda.get_device_properties(dev).L2_cache_size, dtype=torch.uint8, device=dev)
+    gpu_id = getattr(torch.cuda.get_device_properties(dev), "uuid", None)
+    gpu_id = ("GPU-" + str(gpu_id)) if gpu_id is not None and not str(gpu_id).startswith("GPU-") else gpu_id
+    rows = {}
+    with ClockSampler(gpu_id) as clk:
+        for T in CROSSOVER_T:
+            xb = synth.normal_bf16(T * shape.hidden, synth.SEED_BASE + 0x100 + T, synth.S_X)
+            x = torch.from_numpy(xb.reshape(T, shape.hidden).view(np.int16)).to(dev)
+            y = torch.empty((T, shape.hidden), dtype=torch.float32, device=dev)
+            idx, _, _, _ = moe.route(x)
+            row = {"unique_experts": int(torch.unique(idx).numel())}
+            for name, path in (("decode_us", ds4.PATH_DECODE), ("prefill_us", ds4.PATH_PREFILL)):
+                ts = []
+                for it in range(18):
+                    flush.zero_()
+                    a = torch.cuda.Event(enable_timing=True)
+                    b = torch.cuda.Event(enable_timing=True)
+                    a.record(stream)
+                    ds4.ds4moe_forward_path(moe.handle, x, T, path, y)
+                    b.record(stream)
+                    torch.cuda.synchronize()
+                    if it >= 3:
+                        ts.append(1000.0 * a.elapsed_time(b))
+                row[name] = float(np.median(ts))
+            row["faster"] = "decode" if row["decode_us"] <= row["prefill_us"] else "prefill"
+            rows[T] = row
+    if moe.status() != 0:
+        raise RuntimeError("device error during the crossover sweep")
+    moe.close()
+    print(json.dumps({"crossover": rows, "auto_decode_max_t": ds4.AUTO_DECODE_MAX_T,
+                      "config": workload_config(wl, "decode_t1", "flushed before every call", args.gains),
+                      "clocks": clk.summary()}))
+
+
 def main():
     args = parse()
     world, rank, local = dist_setup(args)
     if args.impl == "reference":
         run_reference(args, world, rank)
+        return
+    if args.crossover:
+        if rank == 0:
+            run_crossover(args)
         return
 
     import torch
@@ -521,7 +584,7 @@ def main():
     if rank == 0:
         out = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
                "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-               "vs_baseline": None, "dtype": "f32" if T <= 8 else "bf16", "data": "synthetic",
+               "vs_baseline": None, "dtype": "f32" if T <= ds4.AUTO_DECODE_MAX_T else "bf16", "data": "synthetic",
                "config": workload_config(wl, args.workload, l2_note, args.gains),
                "roofline": roofline,
                "layer_roofline": {"bound": "hbm" if args.workload != "prefill_t4096_zipf4" else "tensor",

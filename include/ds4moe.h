@@ -86,9 +86,16 @@ enum {
     DS4MOE_ESCRATCH = -7      /* request needs more than the fixed scratch of ds4moe_route_noalloc */
 };
 
+/*
+ * Largest T for which DS4MOE_PATH_AUTO takes the decode path (launches of up to
+ * 8 tokens): the measured crossover of the two paths on a GB300 at H=4096,
+ * I=2048, E=384, top-6 (decode faster up to T=12, prefill from T=16).
+ */
+#define DS4MOE_AUTO_DECODE_MAX_T 12
+
 /* Execution paths for ds4moe_forward_path. */
 enum {
-    DS4MOE_PATH_AUTO = 0,    /* decode for T <= 8, prefill above */
+    DS4MOE_PATH_AUTO = 0,    /* decode for T <= DS4MOE_AUTO_DECODE_MAX_T, prefill above */
     DS4MOE_PATH_DECODE = 1,  /* fused dequant-GEMV (memory-bound regime) */
     DS4MOE_PATH_PREFILL = 2  /* grouped GEMM on tcgen05 tensor cores */
 };
@@ -148,8 +155,8 @@ int ds4moe_route(ds4moe_t *h, const void *x_bf16, int32_t T, int32_t *idx_out, f
 
 /*
  * The layer. x_bf16: device [T][H] bf16; y: device fp32 [T][H].
- * 0 <= T <= max_tokens; T == 0 does nothing. Picks the decode path for T <= 8
- * and the prefill path otherwise.
+ * 0 <= T <= max_tokens; T == 0 does nothing. Picks the decode path for
+ * T <= DS4MOE_AUTO_DECODE_MAX_T and the prefill path otherwise.
  */
 int ds4moe_forward(ds4moe_t *h, const void *x_bf16, int32_t T, float *y);
 

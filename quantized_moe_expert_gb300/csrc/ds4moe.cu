@@ -702,7 +702,7 @@ int forward_impl(ds4moe *h, const void *x, int T, int path, float *y) {
     h->stats = ds4moe_stats{};
     h->stats.tokens = T;
     if (path == DS4MOE_PATH_AUTO)
-        path = T <= 8 ? DS4MOE_PATH_DECODE : DS4MOE_PATH_PREFILL;
+        path = T <= DS4MOE_AUTO_DECODE_MAX_T ? DS4MOE_PATH_DECODE : DS4MOE_PATH_PREFILL;
     h->stats.path = path;
     if (path == DS4MOE_PATH_DECODE)
         return run_decode(h, x, T, y, nullptr, nullptr);
@@ -989,7 +989,8 @@ int ds4moe_forward_routed(ds4moe_t *h, const void *x, int32_t T, const int32_t *
     cudaStream_t st = h->stream;
     h->stats = ds4moe_stats{};
     h->stats.tokens = T;
-    h->stats.path = path == DS4MOE_PATH_AUTO ? (T <= 8 ? DS4MOE_PATH_DECODE : DS4MOE_PATH_PREFILL) : path;
+    h->stats.path = path == DS4MOE_PATH_AUTO ? (T <= DS4MOE_AUTO_DECODE_MAX_T ? DS4MOE_PATH_DECODE : DS4MOE_PATH_PREFILL)
+                                             : path;
     if (h->stats.path == DS4MOE_PATH_DECODE)
         return run_decode(h, x, T, y, idx, w);
     cudaMemcpyAsync(S.idx, idx, sizeof(int32_t) * T * L.K, cudaMemcpyDeviceToDevice, st);

@@ -28,6 +28,21 @@ def test_library_exports_every_declared_symbol():
         assert name in ds4.SIGNATURES, f"{name} has no binding"
 
 
+def test_binding_constants_match_the_header():
+    import re
+    text = open(HEADER).read()
+
+    def macro(name):
+        return int(re.search(r"#define\s+" + name + r"\s+(0x[0-9A-Fa-f]+|\d+)u?", text).group(1), 0)
+    assert macro("DS4MOE_MAGIC") == ds4.DS4MOE_MAGIC
+    assert macro("DS4MOE_VERSION") == ds4.DS4MOE_VERSION
+    assert macro("DS4MOE_AUTO_DECODE_MAX_T") == ds4.AUTO_DECODE_MAX_T
+    # the weights struct the binding passes has the header's fields in order
+    body = re.search(r"typedef struct \{([^}]*)\} ds4moe_weights;", text).group(1)
+    fields = re.findall(r"\*\s*(\w+);", body)
+    assert fields == [f[0] for f in ds4.Weights._fields_]
+
+
 def test_strerror_names_every_code():
     for code in (0, -1, -2, -3, -4, -5, -6, -7):
         assert ds4.ds4moe_strerror(code) not in ("", "unknown ds4moe error")

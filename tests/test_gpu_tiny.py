@@ -39,7 +39,7 @@ def test_route_matches_oracle(tiny):
     assert moe.status() == 0
 
 
-@pytest.mark.parametrize("T", [1, 2, 3, 4, 5, 8])
+@pytest.mark.parametrize("T", [1, 2, 3, 4, 5, 8, 12, 16])
 def test_decode_path(tiny, T):
     shape, layer, moe = tiny
     x = tokens(shape, T, 200 + T)
@@ -61,14 +61,16 @@ def test_prefill_path(tiny, T):
 
 def test_auto_path_and_stats(tiny):
     shape, layer, moe = tiny
-    x = tokens(shape, 12, 401)
+    x = tokens(shape, 16, 401)
     moe.forward(x_to_dev(x[:4]))
     s = moe.stats()
     assert s.path == ds4.PATH_DECODE and s.tokens == 4 and s.kernel_count > 0
     r = oracle.route(shape, layer["router_w"], None, x[:4])
     assert s.n_unique == len(np.unique(r["idx"]))
     assert s.max_load == np.bincount(r["idx"].ravel()).max()
-    moe.forward(x_to_dev(x))
+    moe.forward(x_to_dev(x[:ds4.AUTO_DECODE_MAX_T]))
+    assert moe.stats().path == ds4.PATH_DECODE
+    moe.forward(x_to_dev(x[:ds4.AUTO_DECODE_MAX_T + 1]))
     assert moe.stats().path == ds4.PATH_PREFILL
 
 
