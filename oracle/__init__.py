@@ -84,6 +84,15 @@ def _configure(lib):
     lib.oracle_e8m0.argtypes = [ctypes.c_uint8]
     lib.oracle_e8m0.restype = ctypes.c_double
     lib.oracle_gain_block.argtypes = [_vp, _vp]
+    lib.oracle_dequant_mx4.argtypes = [_vp, _vp]
+    lib.oracle_act_q8.argtypes = [_vp, ctypes.c_int64, _vp, _vp]
+    lib.oracle_act_mx4.argtypes = [_vp, ctypes.c_int64, _vp, _vp]
+    lib.oracle_e2m1_nearest.argtypes = [ctypes.c_double]
+    lib.oracle_e2m1_nearest.restype = ctypes.c_uint8
+    lib.oracle_expert_mx4.argtypes = [ctypes.POINTER(_Shape), ctypes.c_int32, _vp, _vp, _vp, _vp, _vp]
+    lib.oracle_forward_routed_mx4.argtypes = [ctypes.POINTER(_Shape), ctypes.c_int32, _vp, _vp, _vp, _vp, _vp, _vp,
+                                              _vp, _vp, _vp, ctypes.c_int32, _vp, _vp, _vp, ctypes.c_int32]
+    lib.oracle_forward_routed_mx4.restype = ctypes.c_int
     lib.oracle_forward_routed_gain.argtypes = [ctypes.POINTER(_Shape), _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                                                _vp, ctypes.c_int32, _vp, _vp, _vp, ctypes.c_int32]
     lib.oracle_forward_routed_gain.restype = ctypes.c_int
@@ -227,30 +236,80 @@ def gain_block(block: np.ndarray) -> np.ndarray:
     return s
 
 
+ACT = {"exact": 0, "q8": 1, "mx4": 2}
+
+
+def dequant_mx4(block: np.ndarray) -> np.ndarray:
+    """The 32 weights of one 17-byte MXFP4 block."""
+    b = np.ascontiguousarray(block, dtype=np.uint8)
+    assert b.size == 17
+    w = np.empty(32, dtype=np.float64)
+    _load().oracle_dequant_mx4(_p(b), _p(w))
+    return w
+
+
+def act_q8(x_f32: np.ndarray):
+    """Q8 activation blocks of a float32 vector: (d float32 [n/32], q int8 [n])."""
+    x = np.ascontiguousarray(x_f32, dtype=np.float32)
+    d = np.empty(x.size // 32, dtype=np.float32)
+    q = np.empty(x.size, dtype=np.int8)
+    _load().oracle_act_q8(_p(x), x.size, _p(d), _p(q))
+    return d, q
+
+
+def act_mx4(x_f32: np.ndarray):
+    """MXFP4 activation blocks of a float32 vector: (E8M0 bytes [n/32], E2M1 codes [n])."""
+    x = np.ascontiguousarray(x_f32, dtype=np.float32)
+    sc = np.empty(x.size // 32, dtype=np.uint8)
+    c = np.empty(x.size, dtype=np.uint8)
+    _load().oracle_act_mx4(_p(x), x.size, _p(sc), _p(c))
+    return sc, c
+
+
+def e2m1_nearest(r: float) -> int:
+    return int(_load().oracle_e2m1_nearest(r))
+
+
+def expert_mx4(shape, act: str, gate_e: np.ndarray, up_e: np.ndarray, down_e: np.ndarray,
+               xt: np.ndarray) -> np.ndarray:
+    """One MXFP4 routed expert on one float64 activation vector, activations quantised by act."""
+    xt = np.ascontiguousarray(xt, dtype=np.float64)
+    ye = np.empty(shape.hidden, dtype=np.float64)
+    s = _shape(shape)
+    g, u, d = (np.ascontiguousarray(a, dtype=np.uint8) for a in (gate_e, up_e, down_e))
+    _load().oracle_expert_mx4(ctypes.byref(s), ACT[act], _p(g), _p(u), _p(d), _p(xt), _p(ye))
+    return ye
+
+
 def forward_routed(shape, layer: dict, x_bf16: np.ndarray, idx: np.ndarray, weights: np.ndarray,
-                   nthreads: int = 0) -> np.ndarray:
+                   nthreads: int = 0, act: str | None = None) -> np.ndarray:
     """Layer output [T, H] float64 for the given routing (with the layer's down gains
-    "down_gain" / "down_gain2", where present)."""
+    "down_gain" / "down_gain2", where present). A layer whose "routed_format" is
+    "mx4" needs act: the activation quantisation of its expert products ("q8"
+    decode, "mx4" prefill, "exact")."""
     x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
     T = x.shape[0]
     idx = np.ascontiguousarray(idx, dtype=np.int32)
     weights = np.ascontiguousarray(weights, dtype=np.float64)
     y = np.empty((T, shape.hidden), dtype=np.float64)
     s = _shape(shape)
-    rc = _load().oracle_forward_routed_gain(ctypes.byref(s), _p(layer["gate"]), _p(layer["up"]), _p(layer["down"]),
-                                            _p(layer.get("sh_gate")), _p(layer.get("sh_up")),
-                                            _p(layer.get("sh_down")), _p(layer.get("down_gain")),
-                                            _p(layer.get("down_gain2")), _p(x), T, _p(idx), _p(weights), _p(y),
-                                            nthreads)
+    common = (_p(layer["gate"]), _p(layer["up"]), _p(layer["down"]), _p(layer.get("sh_gate")),
+              _p(layer.get("sh_up")), _p(layer.get("sh_down")), _p(layer.get("down_gain")),
+              _p(layer.get("down_gain2")), _p(x), T, _p(idx), _p(weights), _p(y), nthreads)
+    if layer.get("routed_format", "q2") == "mx4":
+        rc = _load().oracle_forward_routed_mx4(ctypes.byref(s), ACT[act], *common)
+    else:
+        assert act in (None, "exact"), "2-bit routed experts take exact activations"
+        rc = _load().oracle_forward_routed_gain(ctypes.byref(s), *common)
     if rc != 0:
         raise ValueError("oracle_forward_routed rejected its arguments")
     return y
 
 
-def forward(shape, layer: dict, x_bf16: np.ndarray, nthreads: int = 0):
+def forward(shape, layer: dict, x_bf16: np.ndarray, nthreads: int = 0, act: str | None = None):
     """Route, then compute the layer. Returns (y [T,H] f64, routing dict)."""
     r = route(shape, layer["router_w"], layer.get("router_bias"), x_bf16)
-    y = forward_routed(shape, layer, x_bf16, r["idx"], r["weights"], nthreads)
+    y = forward_routed(shape, layer, x_bf16, r["idx"], r["weights"], nthreads, act)
     return y, r
 
 

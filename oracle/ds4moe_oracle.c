@@ -54,6 +54,24 @@
  *     block scale X as E8M0 (2^(byte - 127));   s_i = 1 + X * e2m1(code_i).
  *   Table [E][H/32] blocks; with gains the output is
  *     y[t] = sum_k w_k * (s1_{e_k} * s2_{e_k}) * ye_k + ysh.
+ *
+ * MXFP4 routed experts ("Running DeepSeek V4 Flash on an RTX 5080 ...", model
+ * list: the MXFP4 GGUF keeps DeepSeek's released MXFP4 routed-expert weights;
+ * Blackwell devices run batched expert work with FP4 activations on native FP4
+ * matrix instructions, decode uses Q8 activations). Element and scale types are
+ * the OCP microscaling ones (E2M1 elements, one E8M0 scale per 32):
+ *   MXFP4 block, 17 bytes per 32 consecutive weights of one row: 16 bytes of
+ *     E2M1 codes (weight i at byte i/2, low nibble for even i), then the E8M0
+ *     scale X;   w_i = X * e2m1(code_i). Routed gate/up [E][I][H/32] blocks,
+ *     down [E][H][I/32]; router and shared expert as above.
+ *   Activations of each routed-expert matrix product are quantised first:
+ *     Q8 (decode): per 32 values, d = amax / 127 and q_i = x_i / d rounded to
+ *       the nearest integer (ties to even), in binary32; the product uses d*q_i.
+ *     MXFP4 (prefill): per 32 values, the OCP conversion: X = 2^(floor(log2
+ *       amax) - 2), element = E2M1 nearest to x_i / X (ties to even, magnitude
+ *       saturating at 6); the product uses X*e2m1.
+ *   The input x (bf16) is exact in binary32; the SwiGLU output h is rounded to
+ *   binary32 (the kernels' precision) before it is quantised.
  */
 #include <math.h>
 #include <omp.h>
@@ -69,7 +87,8 @@ typedef struct {
     int32_t shared_inter; /* I_sh, 0 = no shared expert */
 } oracle_shape;
 
-enum { Q2_BYTES = 84, Q8_BYTES = 34, GAIN_BYTES = 17 };
+enum { Q2_BYTES = 84, Q8_BYTES = 34, GAIN_BYTES = 17, MX4_BYTES = 17 };
+enum { ACT_EXACT = 0, ACT_Q8 = 1, ACT_MX4 = 2 };
 
 /* IEEE binary16 -> double: sign, 5-bit exponent (bias 15), 10-bit fraction. */
 double oracle_f16(uint16_t h)
@@ -126,6 +145,112 @@ void oracle_gain_block(const uint8_t *blk, double *s)
     const double X = oracle_e8m0(blk[16]);
     for (int i = 0; i < 32; i++)
         s[i] = 1.0 + X * oracle_e2m1((uint8_t)((blk[i / 2] >> (4 * (i % 2))) & 15));
+}
+
+/* One MXFP4 block -> 32 weights: w_i = X * e2m1(code_i). */
+void oracle_dequant_mx4(const uint8_t *blk, double *w)
+{
+    const double X = oracle_e8m0(blk[16]);
+    for (int i = 0; i < 32; i++)
+        w[i] = X * oracle_e2m1((uint8_t)((blk[i / 2] >> (4 * (i % 2))) & 15));
+}
+
+/* One row of k weights in MXFP4 blocks. */
+void oracle_dequant_mx4_row(const uint8_t *row, int64_t k, double *w)
+{
+    for (int64_t b = 0; b < k / 32; b++)
+        oracle_dequant_mx4(row + b * MX4_BYTES, w + b * 32);
+}
+
+/* Q8 activation blocks: per 32 values d = amax / 127, q_i = nearest integer
+ * to x_i / d (ties to even), in binary32 arithmetic; amax = 0 gives d = 0 and
+ * q = 0. n is a multiple of 32. */
+void oracle_act_q8(const float *x, int64_t n, float *d, int8_t *q)
+{
+    for (int64_t b = 0; b < n / 32; b++) {
+        float amax = 0.0f;
+        for (int i = 0; i < 32; i++) {
+            const float a = fabsf(x[b * 32 + i]);
+            if (a > amax)
+                amax = a;
+        }
+        const float db = amax / 127.0f;
+        d[b] = db;
+        for (int i = 0; i < 32; i++) {
+            const float r = db > 0.0f ? x[b * 32 + i] / db : 0.0f;
+            q[b * 32 + i] = (int8_t)nearbyintf(r);
+        }
+    }
+}
+
+/* Nearest E2M1 code to r (ties to the even code, magnitude saturating at 6);
+ * the sign bit follows the sign of r. */
+uint8_t oracle_e2m1_nearest(double r)
+{
+    const double a = fabs(r);
+    int best = 0;
+    double bd = INFINITY;
+    for (int c = 0; c < 8; c++) {
+        const double dist = fabs(a - oracle_e2m1((uint8_t)c));
+        if (dist < bd || (dist == bd && c % 2 == 0)) {
+            bd = dist;
+            best = c;
+        }
+    }
+    return (uint8_t)(best | (signbit(r) ? 8 : 0));
+}
+
+/* MXFP4 activation blocks (OCP MX conversion): per 32 values the scale byte
+ * of X = 2^(floor(log2 amax) - 2) (clamped to the E8M0 range; amax = 0 gives
+ * byte 0) and one E2M1 code per value, the nearest to x_i / X. */
+void oracle_act_mx4(const float *x, int64_t n, uint8_t *scale, uint8_t *codes)
+{
+    for (int64_t b = 0; b < n / 32; b++) {
+        double amax = 0.0;
+        for (int i = 0; i < 32; i++)
+            if (fabs((double)x[b * 32 + i]) > amax)
+                amax = fabs((double)x[b * 32 + i]);
+        int sb = 0;
+        if (amax > 0.0) {
+            int e;
+            frexp(amax, &e); /* amax = m 2^e, m in [0.5, 1): floor(log2 amax) = e - 1 */
+            sb = (e - 1) - 2 + 127;
+            sb = sb < 0 ? 0 : sb > 254 ? 254 : sb;
+        }
+        scale[b] = (uint8_t)sb;
+        const double X = oracle_e8m0((uint8_t)sb);
+        for (int i = 0; i < 32; i++)
+            codes[b * 32 + i] = oracle_e2m1_nearest((double)x[b * 32 + i] / X);
+    }
+}
+
+/* The values a routed-expert product sees for activations v[n]: v itself
+ * (ACT_EXACT), or v rounded to binary32 and quantised (ACT_Q8, ACT_MX4). */
+static void quantise_act(int act, const double *v, int64_t n, double *out)
+{
+    if (act == ACT_EXACT) {
+        memcpy(out, v, sizeof(double) * (size_t)n);
+        return;
+    }
+    float *f = (float *)malloc(sizeof(float) * (size_t)n);
+    uint8_t *c = (uint8_t *)malloc((size_t)n);
+    float *d = (float *)malloc(sizeof(float) * (size_t)(n / 32));
+    uint8_t *sc = (uint8_t *)malloc((size_t)(n / 32));
+    for (int64_t i = 0; i < n; i++)
+        f[i] = (float)v[i];
+    if (act == ACT_Q8) {
+        oracle_act_q8(f, n, d, (int8_t *)c);
+        for (int64_t i = 0; i < n; i++)
+            out[i] = (double)d[i / 32] * (double)((int8_t *)c)[i];
+    } else {
+        oracle_act_mx4(f, n, sc, c);
+        for (int64_t i = 0; i < n; i++)
+            out[i] = oracle_e8m0(sc[i / 32]) * oracle_e2m1(c[i]);
+    }
+    free(f);
+    free(c);
+    free(d);
+    free(sc);
 }
 
 /* One 2-bit block -> 256 weights. */
@@ -302,6 +427,37 @@ void oracle_expert_q2(const oracle_shape *s, const uint8_t *gate_e, const uint8_
 }
 
 /* The shared expert on one token: ysh[H]. */
+/* One MXFP4 routed expert: ye = Wd (silu(Wg a) * (Wu a)) with a the quantised
+ * activations of x (act: ACT_Q8 decode, ACT_MX4 prefill, ACT_EXACT none) and
+ * the down product on the quantised SwiGLU output. */
+void oracle_expert_mx4(const oracle_shape *s, int32_t act, const uint8_t *gate_e, const uint8_t *up_e,
+                       const uint8_t *down_e, const double *xt, double *ye)
+{
+    const int H = s->hidden, I = s->inter;
+    const int64_t gate_row = (int64_t)(H / 32) * MX4_BYTES, down_row = (int64_t)(I / 32) * MX4_BYTES;
+    double *w = (double *)malloc(sizeof(double) * (H > I ? H : I));
+    double *a = (double *)malloc(sizeof(double) * H);
+    double *h = (double *)malloc(sizeof(double) * I);
+    double *hq = (double *)malloc(sizeof(double) * I);
+    quantise_act(act, xt, H, a);
+    for (int i = 0; i < I; i++) {
+        oracle_dequant_mx4_row(gate_e + i * gate_row, H, w);
+        double g = dot(w, a, H);
+        oracle_dequant_mx4_row(up_e + i * gate_row, H, w);
+        double u = dot(w, a, H);
+        h[i] = oracle_silu(g) * u;
+    }
+    quantise_act(act, h, I, hq);
+    for (int j = 0; j < H; j++) {
+        oracle_dequant_mx4_row(down_e + j * down_row, I, w);
+        ye[j] = dot(w, hq, I);
+    }
+    free(w);
+    free(a);
+    free(h);
+    free(hq);
+}
+
 void oracle_shared_q8(const oracle_shape *s, const uint8_t *sh_gate, const uint8_t *sh_up,
                       const uint8_t *sh_down, const double *xt, double *ysh)
 {
@@ -331,14 +487,16 @@ void oracle_shared_q8(const oracle_shape *s, const uint8_t *sh_gate, const uint8
  * Tokens are independent and each row is computed by one thread in a fixed
  * order, so the result does not depend on nthreads (<= 0: library default).
  */
-int oracle_forward_routed_gain(const oracle_shape *s, const uint8_t *gate, const uint8_t *up,
-                               const uint8_t *down, const uint8_t *sh_gate, const uint8_t *sh_up,
-                               const uint8_t *sh_down, const uint8_t *gain1, const uint8_t *gain2,
-                               const uint16_t *x, int32_t T, const int32_t *idx, const double *weights,
-                               double *y, int32_t nthreads)
+static int forward_routed_any(const oracle_shape *s, int mx4, int32_t act, const uint8_t *gate, const uint8_t *up,
+                              const uint8_t *down, const uint8_t *sh_gate, const uint8_t *sh_up,
+                              const uint8_t *sh_down, const uint8_t *gain1, const uint8_t *gain2,
+                              const uint16_t *x, int32_t T, const int32_t *idx, const double *weights,
+                              double *y, int32_t nthreads)
 {
     const int H = s->hidden, I = s->inter, E = s->n_experts, K = s->top_k;
     if (H <= 0 || I <= 0 || H % 256 || I % 256 || K <= 0 || K > E || T < 0)
+        return -1;
+    if (act < ACT_EXACT || act > ACT_MX4 || (!mx4 && act != ACT_EXACT))
         return -1;
     const int has_shared = s->shared_inter > 0 && sh_gate && sh_up && sh_down;
     if (has_shared && s->shared_inter % 32)
@@ -346,8 +504,8 @@ int oracle_forward_routed_gain(const oracle_shape *s, const uint8_t *gate, const
     for (int64_t p = 0; p < (int64_t)T * K; p++)
         if (idx[p] < 0 || idx[p] >= E)
             return -1;
-    const int64_t expert_gate = (int64_t)I * (H / 256) * Q2_BYTES;
-    const int64_t expert_down = (int64_t)H * (I / 256) * Q2_BYTES;
+    const int64_t expert_gate = mx4 ? (int64_t)I * (H / 32) * MX4_BYTES : (int64_t)I * (H / 256) * Q2_BYTES;
+    const int64_t expert_down = mx4 ? (int64_t)H * (I / 32) * MX4_BYTES : (int64_t)H * (I / 256) * Q2_BYTES;
     const int nt = nthreads > 0 ? nthreads : omp_get_max_threads();
 #pragma omp parallel for schedule(dynamic, 1) num_threads(nt)
     for (int32_t t = 0; t < T; t++) {
@@ -358,7 +516,11 @@ int oracle_forward_routed_gain(const oracle_shape *s, const uint8_t *gate, const
             xt[h] = oracle_bf16(x[(int64_t)t * H + h]);
         for (int k = 0; k < K; k++) {
             int e = idx[(int64_t)t * K + k];
-            oracle_expert_q2(s, gate + e * expert_gate, up + e * expert_gate, down + e * expert_down, xt, ye);
+            if (mx4)
+                oracle_expert_mx4(s, act, gate + e * expert_gate, up + e * expert_gate, down + e * expert_down, xt,
+                                  ye);
+            else
+                oracle_expert_q2(s, gate + e * expert_gate, up + e * expert_gate, down + e * expert_down, xt, ye);
             double wk = weights[(int64_t)t * K + k];
             for (int j0 = 0; j0 < H; j0 += 32) {
                 double s1[32], s2[32];
@@ -383,6 +545,27 @@ int oracle_forward_routed_gain(const oracle_shape *s, const uint8_t *gate, const
         free(acc);
     }
     return 0;
+}
+
+int oracle_forward_routed_gain(const oracle_shape *s, const uint8_t *gate, const uint8_t *up,
+                               const uint8_t *down, const uint8_t *sh_gate, const uint8_t *sh_up,
+                               const uint8_t *sh_down, const uint8_t *gain1, const uint8_t *gain2,
+                               const uint16_t *x, int32_t T, const int32_t *idx, const double *weights,
+                               double *y, int32_t nthreads)
+{
+    return forward_routed_any(s, 0, ACT_EXACT, gate, up, down, sh_gate, sh_up, sh_down, gain1, gain2, x, T, idx,
+                              weights, y, nthreads);
+}
+
+/* The layer with MXFP4 routed experts and act-quantised expert activations. */
+int oracle_forward_routed_mx4(const oracle_shape *s, int32_t act, const uint8_t *gate, const uint8_t *up,
+                              const uint8_t *down, const uint8_t *sh_gate, const uint8_t *sh_up,
+                              const uint8_t *sh_down, const uint8_t *gain1, const uint8_t *gain2,
+                              const uint16_t *x, int32_t T, const int32_t *idx, const double *weights,
+                              double *y, int32_t nthreads)
+{
+    return forward_routed_any(s, 1, act, gate, up, down, sh_gate, sh_up, sh_down, gain1, gain2, x, T, idx, weights,
+                              y, nthreads);
 }
 
 /* oracle_forward_routed_gain without down gains. */

@@ -40,6 +40,8 @@ S_ROUTER, S_GATE, S_UP, S_DOWN, S_SH_GATE, S_SH_UP, S_SH_DOWN, S_BIAS_RANK = ran
 S_GAIN1, S_GAIN2 = 9, 10
 GAIN_BLOCK_BYTES = 17
 GAIN_SCALE_BYTE = 127 - 5  # E8M0 2^-5: gains 1 + 2^-5 * e2m1 in [0.8125, 1.1875]
+MX4_BLOCK_BYTES = 17
+MX4_SCALE_BYTE = 127 - 6  # MXFP4 weight scales 2^-6, 2^-7, 2^-8: |w| <= 6 * 2^-6
 S_X = 16
 
 Q2_BLOCK_BYTES = 84
@@ -70,6 +72,7 @@ def _load():
         lib.synth_fill_q2.argtypes = [u8p, ctypes.c_int64, ctypes.c_uint64, ctypes.c_uint64, ctypes.c_double]
         lib.synth_fill_q8.argtypes = [u8p, ctypes.c_int64, ctypes.c_uint64, ctypes.c_uint64, ctypes.c_double]
         lib.synth_fill_gain.argtypes = [u8p, ctypes.c_int64, ctypes.c_uint64, ctypes.c_uint64, ctypes.c_uint8]
+        lib.synth_fill_mx4.argtypes = [u8p, ctypes.c_int64, ctypes.c_uint64, ctypes.c_uint64, ctypes.c_uint8]
         lib.synth_fill_normal_f32.argtypes = [ctypes.POINTER(ctypes.c_float), ctypes.c_int64,
                                               ctypes.c_uint64, ctypes.c_uint64, ctypes.c_double]
         lib.synth_fill_normal_bf16.argtypes = [ctypes.POINTER(ctypes.c_uint16), ctypes.c_int64,
@@ -206,19 +209,33 @@ def gain_table(n_experts: int, hidden: int, seed: int, stream: int, scale_byte: 
     return out.reshape(n_experts, hidden // 32, GAIN_BLOCK_BYTES)
 
 
+def mx4_matrix(rows: int, k: int, seed: int, stream: int, base_byte: int = MX4_SCALE_BYTE) -> np.ndarray:
+    """MXFP4 weights [rows][k/32] blocks of 17 bytes."""
+    assert k % 32 == 0
+    out = np.empty((rows, k // 32, MX4_BLOCK_BYTES), dtype=np.uint8)
+    _load().synth_fill_mx4(_ptr(out, ctypes.c_uint8), out.shape[0] * out.shape[1], seed, stream, base_byte)
+    return out
+
+
 def make_layer(shape: Shape, seed: int, zipf: bool = False, zipf_beta_value: float | None = None,
-               gains: int = 0) -> dict:
+               gains: int = 0, routed_format: str = "q2") -> dict:
     """All weights of one layer in canonical layout (host numpy arrays).
 
-    gains: number of down-gain tables to draw (0, 1 or 2) as "down_gain", "down_gain2"."""
+    gains: number of down-gain tables to draw (0, 1 or 2) as "down_gain", "down_gain2".
+    routed_format: "q2" (2-bit blocks) or "mx4" (MXFP4 blocks, same streams)."""
     H, I, E, Ish = shape.hidden, shape.inter, shape.n_experts, shape.shared_inter
-    layer = {
-        "router_w": normal_f32(E * H, seed, S_ROUTER, 0.02).reshape(E, H),
-        "gate": q2_matrix(E * I, H, seed, S_GATE).reshape(E, I, H // 256, Q2_BLOCK_BYTES),
-        "up": q2_matrix(E * I, H, seed, S_UP).reshape(E, I, H // 256, Q2_BLOCK_BYTES),
-        "down": q2_matrix(E * H, I, seed, S_DOWN).reshape(E, H, I // 256, Q2_BLOCK_BYTES),
-        "router_bias": None,
-    }
+    layer = {"router_w": normal_f32(E * H, seed, S_ROUTER, 0.02).reshape(E, H), "router_bias": None}
+    if routed_format == "q2":
+        layer["gate"] = q2_matrix(E * I, H, seed, S_GATE).reshape(E, I, H // 256, Q2_BLOCK_BYTES)
+        layer["up"] = q2_matrix(E * I, H, seed, S_UP).reshape(E, I, H // 256, Q2_BLOCK_BYTES)
+        layer["down"] = q2_matrix(E * H, I, seed, S_DOWN).reshape(E, H, I // 256, Q2_BLOCK_BYTES)
+    elif routed_format == "mx4":
+        layer["gate"] = mx4_matrix(E * I, H, seed, S_GATE).reshape(E, I, H // 32, MX4_BLOCK_BYTES)
+        layer["up"] = mx4_matrix(E * I, H, seed, S_UP).reshape(E, I, H // 32, MX4_BLOCK_BYTES)
+        layer["down"] = mx4_matrix(E * H, I, seed, S_DOWN).reshape(E, H, I // 32, MX4_BLOCK_BYTES)
+        layer["routed_format"] = "mx4"
+    else:
+        raise ValueError(routed_format)
     if Ish > 0:
         layer["sh_gate"] = q8_matrix(Ish, H, seed, S_SH_GATE)
         layer["sh_up"] = q8_matrix(Ish, H, seed, S_SH_UP)

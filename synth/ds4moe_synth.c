@@ -161,6 +161,25 @@ void synth_fill_gain(uint8_t *out, int64_t nblocks, uint64_t seed, uint64_t stre
 }
 
 /*
+ * MXFP4 blocks (17 bytes per 32 weights): 16 bytes of uniform random E2M1
+ * codes, then the E8M0 scale byte base_byte - (r mod 3) (three scales a
+ * factor of 2 apart). Block b uses draws 3*b .. 3*b+2 of the stream.
+ */
+void synth_fill_mx4(uint8_t *out, int64_t nblocks, uint64_t seed, uint64_t stream, uint8_t base_byte)
+{
+    uint64_t key = stream_key(seed, stream);
+#pragma omp parallel for schedule(static)
+    for (int64_t b = 0; b < nblocks; b++) {
+        uint8_t *blk = out + b * 17;
+        for (int w = 0; w < 2; w++) {
+            uint64_t r = draw(key, (uint64_t)b * 3 + w);
+            memcpy(blk + 8 * w, &r, 8);
+        }
+        blk[16] = (uint8_t)(base_byte - (uint8_t)(draw(key, (uint64_t)b * 3 + 2) % 3));
+    }
+}
+
+/*
  * 8-bit blocks: codes uniform in [-127, 127], d = |N(0, sigma)|.
  * Block b uses draws 18*b .. 18*b+17.
  */

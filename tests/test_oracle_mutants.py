@@ -48,7 +48,8 @@ MUTANTS = {
                            "h[i] = oracle_silu(u) * g;\n    }\n    for (int j = 0; j < H; j++) {\n        oracle_dequant_q2_row")],
     "routing_weight_dropped": [("acc[j0 + i] += wk * (s1[i] * s2[i] * ye[j0 + i]);",
                                 "acc[j0 + i] += (s1[i] * s2[i] * ye[j0 + i]);")],
-    "gain_nibble_high_first": [("(blk[i / 2] >> (4 * (i % 2))) & 15", "(blk[i / 2] >> (4 - 4 * (i % 2))) & 15")],
+    "gain_nibble_high_first": [("s[i] = 1.0 + X * oracle_e2m1((uint8_t)((blk[i / 2] >> (4 * (i % 2))) & 15));",
+                                "s[i] = 1.0 + X * oracle_e2m1((uint8_t)((blk[i / 2] >> (4 - 4 * (i % 2))) & 15));")],
     "gain_stores_s_not_s_minus_1": [("s[i] = 1.0 + X * oracle_e2m1", "s[i] = X * oracle_e2m1")],
     "gain_tables_added": [("s1[i] * s2[i] * ye[j0 + i]", "(s1[i] + s2[i] - 1.0) * ye[j0 + i]")],
     "gain_second_table_ignored": [("s1[i] * s2[i] * ye[j0 + i]", "s1[i] * ye[j0 + i]")],
@@ -56,6 +57,17 @@ MUTANTS = {
     "e2m1_exponent_bias": [("ldexp(1.0 + 0.5 * man, ex - 1)", "ldexp(1.0 + 0.5 * man, ex - 2)")],
     "e2m1_no_subnormal": [("ex == 0 ? 0.5 * man :", "ex == 0 ? 0.0 :")],
     "e8m0_bias": [("ldexp(1.0, (int)x - 127)", "ldexp(1.0, (int)x - 128)")],
+    "mx4_nibble_high_first": [("w[i] = X * oracle_e2m1((uint8_t)((blk[i / 2] >> (4 * (i % 2))) & 15));",
+                               "w[i] = X * oracle_e2m1((uint8_t)((blk[i / 2] >> (4 - 4 * (i % 2))) & 15));")],
+    "mx4_scale_ignored": [("w[i] = X * oracle_e2m1((uint8_t)", "w[i] = 1.0 * oracle_e2m1((uint8_t)")],
+    "q8_truncates": [("q[b * 32 + i] = (int8_t)nearbyintf(r);", "q[b * 32 + i] = (int8_t)r;")],
+    "q8_scale_128": [("const float db = amax / 127.0f;", "const float db = amax / 128.0f;")],
+    "mx4_act_scale_off_by_one": [("sb = (e - 1) - 2 + 127;", "sb = (e - 1) - 1 + 127;")],
+    "mx4_act_ties_to_odd": [("(dist == bd && c % 2 == 0)", "(dist == bd && c % 2 == 1)")],
+    "mx4_act_sign_dropped": [("return (uint8_t)(best | (signbit(r) ? 8 : 0));", "return (uint8_t)best;")],
+    "x_not_quantised": [("quantise_act(act, xt, H, a);", "quantise_act(ACT_EXACT, xt, H, a);")],
+    "h_not_quantised": [("quantise_act(act, h, I, hq);", "quantise_act(ACT_EXACT, h, I, hq);")],
+    "h_quantised_in_double": [("        f[i] = (float)v[i];", "        f[i] = (float)(v[i] * (1.0 + 1e-7));")],
     "shared_dropped": [("acc[j] += ye[j];\n        }", "acc[j] += 0.0 * ye[j];\n        }")],
     "shared_weighted": [("acc[j] += ye[j];\n        }", "acc[j] += weights[(int64_t)t * K] * ye[j];\n        }")],
     "down_uses_gate_activation": [("ye[j] = dot(w, h, I);", "ye[j] = dot(w, xt, I);")],

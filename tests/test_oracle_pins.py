@@ -545,3 +545,168 @@ def test_gain_correction_is_routed_per_expert(tiny):
             ye = oracle.expert(shape, layer["gate"][e], layer["up"][e], layer["down"][e], xf[t])
             delta += r["weights"][t, k] * (s - 1) * ye
         assert np.allclose(y1[t] - y0[t], delta, rtol=1e-9, atol=1e-12 * np.abs(y0[t]).max())
+
+
+# ---- MXFP4 routed experts ----------------------------------------------------
+# "Running DeepSeek V4 Flash on an RTX 5080 ...", model list: MXFP4 routed
+# experts; batched expert work on FP4 activations, decode on Q8 activations.
+# Element and scale types: OCP microscaling (E2M1, E8M0 per 32).
+
+def _mx4_layer_one_expert(H=256, I=256, code_g=2, code_u=4, sc_gu=127 - 6, down_codes=None, sc_d=127 - 5):
+    """E=K=1 MXFP4 layer: every gate row the constant e2m1(code_g) 2^(sc-127),
+    up likewise, down row j the constant code down_codes[j]."""
+    if down_codes is None:
+        down_codes = [(j % 7) + 1 + 8 * (j % 2) for j in range(H)]
+    gate = as_u8([[gain_block(code_g, sc_gu) for _ in range(H // 32)] for _ in range(I)])
+    up = as_u8([[gain_block(code_u, sc_gu) for _ in range(H // 32)] for _ in range(I)])
+    down = as_u8([[gain_block(down_codes[j], sc_d) for _ in range(I // 32)] for j in range(H)])
+    layer = {"gate": gate.reshape(1, I, H // 32, 17), "up": up.reshape(1, I, H // 32, 17),
+             "down": down.reshape(1, H, I // 32, 17), "sh_gate": None, "sh_up": None, "sh_down": None,
+             "routed_format": "mx4"}
+    return layer
+
+
+def _e2m1(c):
+    return E2M1_MAGNITUDES[c & 7] * (-1.0 if c & 8 else 1.0)
+
+
+def _np_q8(v):
+    """Q8 blocks in numpy float32 arithmetic (IEEE): d = amax/127, q = rint(v/d)."""
+    v = np.asarray(v, dtype=np.float32).reshape(-1, 32)
+    amax = np.abs(v).max(axis=1)
+    d = amax / np.float32(127)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        q = np.where(d[:, None] > 0, np.rint(v / d[:, None]), 0).astype(np.int8)
+    return d, q.reshape(-1)
+
+
+def _np_mx4_code(r):
+    """E2M1 code nearest to r: all 16 codes, least distance, ties to the code
+    with mantissa bit 0; magnitudes above 6 go to 6; sign follows r."""
+    mag = min(abs(r), 6.0)
+    cands = sorted(range(8), key=lambda c: (abs(mag - E2M1_MAGNITUDES[c]), c & 1))
+    return cands[0] | (8 if math.copysign(1.0, r) < 0 else 0)
+
+
+def _np_mx4(v):
+    v = np.asarray(v, dtype=np.float32).reshape(-1, 32).astype(np.float64)
+    sc, codes = [], []
+    for blk in v:
+        amax = np.abs(blk).max()
+        if amax == 0:
+            b = 0
+        else:
+            m, e = np.frexp(amax)
+            b = int(min(max(e - 1 - 2 + 127, 0), 254))
+        X = 2.0 ** (b - 127)
+        sc.append(b)
+        codes += [_np_mx4_code(r / X) for r in blk]
+    return np.array(sc, np.uint8), np.array(codes, np.uint8)
+
+
+def test_mx4_block_fields():
+    codes = [(5 * i + 3) % 16 for i in range(32)]
+    blk = np.frombuffer(gain_block(codes, 127 - 6), np.uint8)
+    assert list(oracle.dequant_mx4(blk)) == [2.0 ** -6 * _e2m1(c) for c in codes]
+    for ch in (0, 1, 17, 31):
+        c = [0] * 32
+        c[ch] = 5  # +3
+        w = oracle.dequant_mx4(np.frombuffer(gain_block(c, 127 + 2), np.uint8))
+        assert w[ch] == 12.0 and np.count_nonzero(w) == 1
+
+
+def test_act_q8_is_binary32_round_to_nearest_even():
+    rng = np.random.default_rng(3)
+    x = np.concatenate([rng.standard_normal(32 * 6).astype(np.float32), np.zeros(32, np.float32),
+                        # amax 127: d = 1, ties x.5 go to the even integer
+                        np.array([127.0, 2.5, 3.5, -2.5, -3.5, 0.5, 1.5, -126.5] + [0.0] * 24, np.float32)])
+    d, q = oracle.act_q8(x)
+    dw, qw = _np_q8(x)
+    assert np.array_equal(d, dw) and np.array_equal(q, qw)
+    assert list(q[-32:-24]) == [127, 2, 4, -2, -4, 0, 2, -126]
+    assert d[6] == 0 and not q[192:224].any()
+
+
+def test_act_mx4_is_the_ocp_conversion():
+    # element rounding on the E2M1 grid (X = 1 when the block maximum is in [4, 8))
+    vals = [6.0, 2.5, 3.5, 5.0, 0.25, 0.75, 1.25, 1.75, -2.6, -0.1, 4.9, 0.0]
+    want = [7, 4, 6, 6, 0, 2, 2, 4, 13, 8, 6, 0]
+    sc, c = oracle.act_mx4(np.array(vals + [0.0] * 20, np.float32))
+    assert sc[0] == 127 and list(c[:12]) == want
+    # the scale: 2^(floor(log2 amax) - 2); values above 6 X saturate
+    for amax, byte in ((15.5, 128), (8.0, 128), (7.99, 127), (0.3, 123), (2.0 ** -130, 0)):
+        sc, c = oracle.act_mx4(np.array([amax] + [0.0] * 31, np.float32))
+        assert sc[0] == byte
+    rng = np.random.default_rng(4)
+    x = (rng.standard_normal(32 * 8) * np.repeat(2.0 ** rng.integers(-6, 6, 8), 32)).astype(np.float32)
+    sc, c = oracle.act_mx4(x)
+    scw, cw = _np_mx4(x)
+    assert np.array_equal(sc, scw) and np.array_equal(c, cw)
+
+
+def test_mx4_expert_closed_form_q8_and_mx4_activations():
+    """Constant gate/up rows: g = a * sum(a_x), u = b * sum(a_x) with a_x the
+    quantised x; h quantised again; down row j constant c_j: ye_j = c_j sum(hq)."""
+    H, I = 256, 256
+    layer = _mx4_layer_one_expert(H, I)
+    shape = synth.Shape(H, I, 1, 1, 0)
+    a, b = 2.0 ** -6 * 1.0, 2.0 ** -6 * 2.0
+    c = np.array([2.0 ** -5 * _e2m1((j % 7) + 1 + 8 * (j % 2)) for j in range(H)])
+    rng = np.random.default_rng(5)
+    x = rng.standard_normal(H).astype(np.float32)
+    xb = (x.view(np.uint32) & 0xFFFF0000).view(np.float32)  # exact in bf16
+    for act in ("q8", "mx4"):
+        if act == "q8":
+            d, q = _np_q8(xb)
+            ax = np.repeat(d.astype(np.float64), 32) * q
+        else:
+            sc, cc = _np_mx4(xb)
+            ax = np.repeat(2.0 ** (sc.astype(np.float64) - 127), 32) * np.array([_e2m1(v) for v in cc])
+        g, u = a * ax.sum(), b * ax.sum()
+        h = np.full(I, np.float32(g / (1 + math.exp(-g)) * u))
+        if act == "q8":
+            d, q = _np_q8(h)
+            hq = np.repeat(d.astype(np.float64), 32) * q
+        else:
+            sc, cc = _np_mx4(h)
+            hq = np.repeat(2.0 ** (sc.astype(np.float64) - 127), 32) * np.array([_e2m1(v) for v in cc])
+        want = c * hq.sum()
+        y = oracle.forward_routed(shape, layer, bf16_bits(xb[None, :]), np.zeros((1, 1), np.int32),
+                                  np.ones((1, 1)), act=act)
+        assert np.allclose(y[0], want, rtol=1e-12, atol=0)
+        ye = oracle.expert_mx4(shape, act, layer["gate"][0], layer["up"][0], layer["down"][0], xb)
+        assert np.allclose(ye, want, rtol=1e-12, atol=0)
+
+
+def test_mx4_exact_activations_match_dense_numpy():
+    shape = synth.Shape(512, 256, 4, 2, 0)
+    layer = synth.make_layer(shape, 77, routed_format="mx4")
+    layer["sh_gate"] = layer["sh_up"] = layer["sh_down"] = None
+    x = synth.normal_bf16(3 * 512, 78, synth.S_X).reshape(3, 512)
+    xf = synth.bf16_bits_to_f32(x).astype(np.float64)
+    tab = np.array([_e2m1(c) for c in range(16)])
+
+    def dq(m):
+        m = m.reshape(-1, 17)
+        lo, hi = m[:, :16] & 15, m[:, :16] >> 4
+        codes = np.stack([lo, hi], axis=2).reshape(-1, 32)
+        return (tab[codes] * 2.0 ** (m[:, 16:17].astype(np.float64) - 127)).reshape(-1)
+    Wg = dq(layer["gate"]).reshape(4, 256, 512)
+    Wu = dq(layer["up"]).reshape(4, 256, 512)
+    Wd = dq(layer["down"]).reshape(4, 512, 256)
+    idx = np.array([[0, 3], [2, 1], [3, 0]], np.int32)
+    w = np.array([[0.75, 0.25], [0.5, 0.5], [0.125, 0.875]])
+    y = oracle.forward_routed(shape, layer, x, idx, w, act="exact")
+    for t in range(3):
+        want = np.zeros(512)
+        for k in range(2):
+            e = idx[t, k]
+            g, u = Wg[e] @ xf[t], Wu[e] @ xf[t]
+            want += w[t, k] * (Wd[e] @ (g / (1 + np.exp(-g)) * u))
+        assert np.allclose(y[t], want, rtol=1e-12, atol=1e-15)
+    # quantised activations stay close to exact ones: Q8 within a few 1e-2, FP4 within 0.3
+    y8 = oracle.forward_routed(shape, layer, x, idx, w, act="q8")
+    y4 = oracle.forward_routed(shape, layer, x, idx, w, act="mx4")
+    e8 = np.linalg.norm(y8 - y) / np.linalg.norm(y)
+    e4 = np.linalg.norm(y4 - y) / np.linalg.norm(y)
+    assert 0 < e8 < 3e-2 and e8 < e4 < 0.3, (e8, e4)

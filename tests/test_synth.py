@@ -89,3 +89,20 @@ def test_zipf_bias_profile():
         assert 0.05 < beta < 4.0
         p = synth.zipf_profile(384, seed)
         assert np.isclose(p.max(), 1.0) and np.isclose(np.sort(p)[-2], 2.0 ** -1.1)
+
+
+def test_gain_and_mx4_distributions():
+    g = synth.gain_table(8, 512, 3, synth.S_GAIN1)
+    assert g.shape == (8, 16, 17) and (g[..., 16] == synth.GAIN_SCALE_BYTE).all()
+    nib = np.concatenate([g[..., :16] & 15, g[..., :16] >> 4]).ravel()
+    assert set(np.unique(nib)) == set(range(16))
+    assert np.array_equal(g, synth.gain_table(8, 512, 3, synth.S_GAIN1))
+    m = synth.mx4_matrix(64, 512, 5, synth.S_GATE)
+    assert m.shape == (64, 16, 17)
+    sc = m[..., 16].ravel()
+    assert set(np.unique(sc)) == {synth.MX4_SCALE_BYTE - 2, synth.MX4_SCALE_BYTE - 1, synth.MX4_SCALE_BYTE}
+    nib = np.concatenate([m[..., :16] & 15, m[..., :16] >> 4]).ravel()
+    counts = np.bincount(nib, minlength=16)
+    assert counts.min() > 0.9 * nib.size / 16 and counts.max() < 1.1 * nib.size / 16
+    # a prefix of the blocks does not depend on how many are drawn
+    assert np.array_equal(synth.mx4_matrix(8, 512, 5, synth.S_GATE), m[:8])
