@@ -50,6 +50,8 @@ def parse():
     ap.add_argument("--crossover", action="store_true",
                     help="time the decode and the prefill path on the decode layer for T = 1..64 and print "
                          "one JSON line of the per-T medians (not a bench line)")
+    ap.add_argument("--routed-format", default="q2", choices=["q2", "mx4"],
+                    help="routed experts in the 2-bit format or in MXFP4 (Q8 activations)")
     ap.add_argument("--gains", type=int, default=0, choices=[0, 1, 2],
                     help="per-expert down-gain tables (sidecar, post-training) on every layer")
     return ap.parse_args()
@@ -62,13 +64,15 @@ Q8_BPW = 34 / 32
 
 
 GAIN_BPC = 17 / 32  # bytes per output channel of one down-gain table
+MX4_BPW = 17 / 32  # bytes per MXFP4 weight
 
 
-def layer_bytes(shape, T, U, gains=0):
+def layer_bytes(shape, T, U, gains=0, fmt="q2"):
     """Bytes the layer must move per call: selected experts (and their down-gain
     blocks), shared expert, router, x in, y out."""
     H, I, E, Ish = shape.hidden, shape.inter, shape.n_experts, shape.shared_inter
-    return (U * 3 * H * I * Q2_BPW + gains * U * H * GAIN_BPC + 3 * H * Ish * Q8_BPW + 4 * E * H + 2 * T * H
+    bpw = MX4_BPW if fmt == "mx4" else Q2_BPW
+    return (U * 3 * H * I * bpw + gains * U * H * GAIN_BPC + 3 * H * Ish * Q8_BPW + 4 * E * H + 2 * T * H
             + 4 * T * H)
 
 
@@ -77,7 +81,7 @@ def layer_flops(shape, T):
     return T * (2 * K * 3 * H * I + 2 * 3 * H * Ish + 2 * E * H)
 
 
-def kernel_bytes(name, shape, T, U, gains=0):
+def kernel_bytes(name, shape, T, U, gains=0, fmt="q2"):
     """Algorithmic bytes of one launch of a library kernel (weights it must read plus its activations)."""
     H, I, E, K, Ish = shape.hidden, shape.inter, shape.n_experts, shape.top_k, shape.shared_inter
     P = T * K
@@ -91,6 +95,9 @@ def kernel_bytes(name, shape, T, U, gains=0):
         "combine": 4 * P * H + 4 * T * H + 4 * T * H + gains * U * H * GAIN_BPC,
         # one launch of the fused decode kernel does the whole layer for up to 8 tokens
         "decode_fused": layer_bytes(shape, T, U, gains),
+        # MXFP4 experts: weights of the distinct experts, fp32 activation rows in, results out
+        "mx4_gateup": U * 2 * I * H * MX4_BPW + 4 * T * H + 4 * P * I,
+        "mx4_down": U * H * I * MX4_BPW + 4 * P * I + 4 * P * H,
     }
     return table.get(name)
 
@@ -244,10 +251,10 @@ class ClockSampler:
 
 # ---- the workload ----------------------------------------------------------------
 
-def workload_layers(name, gains=0):
+def workload_layers(name, gains=0, fmt="q2"):
     import synth
     wl = synth.WORKLOADS[name]
-    return wl, [synth.make_layer(wl.shape, s, zipf=wl.zipf, gains=gains) for s in wl.layer_seeds]
+    return wl, [synth.make_layer(wl.shape, s, zipf=wl.zipf, gains=gains, routed_format=fmt) for s in wl.layer_seeds]
 
 
 def workload_batches(name):
@@ -288,7 +295,8 @@ def cpu_oracle_rate(name, layers, batches, budget_tokens=None, min_seconds=0.0):
     passes = 0
     while True:
         for layer in layers:
-            oracle.forward(wl.shape, layer, np.ascontiguousarray(flat))
+            oracle.forward(wl.shape, layer, np.ascontiguousarray(flat),
+                           act="q8" if layer.get("routed_format") == "mx4" else None)
         passes += 1
         dt = time.perf_counter() - t0
         if dt >= min_seconds:
@@ -333,7 +341,7 @@ def run_reference(args, world, rank):
     import synth
     if rank != 0:
         return
-    wl, layers = workload_layers(args.workload, args.gains)
+    wl, layers = workload_layers(args.workload, args.gains, args.routed_format)
     batches = workload_batches(args.workload)
     times = []
     n_tok = None
@@ -347,18 +355,19 @@ def run_reference(args, world, rank):
     out = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * total / len(times),
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-           "config": workload_config(wl, args.workload, None, args.gains),
+           "config": workload_config(wl, args.workload, None, args.gains, args.routed_format),
            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(out))
 
 
-def workload_config(wl, name, l2_note, gains=0):
+def workload_config(wl, name, l2_note, gains=0, fmt="q2"):
     s = wl.shape
     cfg = {"workload": name, "description": wl.description, "hidden": s.hidden, "inter": s.inter,
            "n_experts": s.n_experts, "top_k": s.top_k, "shared_inter": s.shared_inter,
            "tokens_per_step": wl.tokens, "layers_per_step": wl.n_layers,
-           "weights": "routed 2-bit 84B/256 blocks, shared 8-bit 34B/32 blocks, router fp32"}
+           "weights": ("routed MXFP4 17B/32 blocks on Q8 activations" if fmt == "mx4" else "routed 2-bit 84B/256 blocks")
+           + ", shared 8-bit 34B/32 blocks, router fp32"}
     if gains:
         cfg["down_gain_tables"] = gains
         cfg["weights"] += f", {gains} down-gain table(s) of 17B/32-channel FP4 blocks"
@@ -441,14 +450,16 @@ def main():
 
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    wl, layers = workload_layers(args.workload, args.gains)
+    wl, layers = workload_layers(args.workload, args.gains, args.routed_format)
     shape = wl.shape
     batches = workload_batches(args.workload)
     T = wl.tokens
     handles = []
     for layer in layers:
-        w = {k: (None if v is None else torch.from_numpy(np.ascontiguousarray(v)).to(dev)) for k, v in layer.items()}
-        handles.append(ds4.MoELayer(shape, w, max_tokens=max(T, 8)))
+        w = {k: (None if v is None else torch.from_numpy(np.ascontiguousarray(v)).to(dev)) for k, v in layer.items()
+             if v is None or isinstance(v, np.ndarray)}
+        handles.append(ds4.MoELayer(shape, w, max_tokens=max(T, 8),
+                                    flags=ds4.FLAG_MXFP4 if args.routed_format == "mx4" else 0))
         del w
     torch.cuda.empty_cache()
     stream = torch.cuda.current_stream(dev)
@@ -519,7 +530,7 @@ def main():
         ds4.ds4moe_profile(m.handle, False)
     dom = max(ktimes, key=lambda k: ktimes[k][1])
     dom_avg_ms = ktimes[dom][1] / ktimes[dom][0]
-    dom_bytes = kernel_bytes(dom, shape, T, U_mean, args.gains)
+    dom_bytes = kernel_bytes(dom, shape, T, U_mean, args.gains, args.routed_format)
     peaks = {}
     pk_path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(pk_path):
@@ -537,19 +548,19 @@ def main():
         if t_tc > t_hbm:
             ach = dom_flops / sec / 1e12
             roofline = {"bound": "tensor", "kernel": dom, "achieved": ach, "peak": tf_peak, "unit": "TFLOP/s",
-                        "frac": ach / tf_peak, "traffic": kernel_traffic(dom, args.workload, args.gains),
+                        "frac": ach / tf_peak, "traffic": kernel_traffic(dom, args.workload, args.gains if args.routed_format == "q2" else -1),
                         "peak_source": peak_src + " bf16 burst",
                         "flops_per_launch": dom_flops, "bytes_per_launch": dom_bytes,
                         "hbm_frac": dom_bytes / sec / 1e9 / hbm_peak, "avg_launch_us": 1000 * dom_avg_ms}
         else:
             ach = dom_bytes / sec / 1e9
             roofline = {"bound": "hbm", "kernel": dom, "achieved": ach, "peak": hbm_peak, "unit": "GB/s",
-                        "frac": ach / hbm_peak, "traffic": kernel_traffic(dom, args.workload, args.gains), "peak_source": peak_src,
+                        "frac": ach / hbm_peak, "traffic": kernel_traffic(dom, args.workload, args.gains if args.routed_format == "q2" else -1), "peak_source": peak_src,
                         "bytes_per_launch": dom_bytes, "avg_launch_us": 1000 * dom_avg_ms}
             if dom_flops:
                 roofline["flops_per_launch"] = dom_flops
                 roofline["tensor_frac"] = dom_flops / sec / 1e12 / tf_peak
-    lay_bytes = layer_bytes(shape, T, U_mean, args.gains) * len(handles)
+    lay_bytes = layer_bytes(shape, T, U_mean, args.gains, args.routed_format) * len(handles)
     layer_gbs = lay_bytes / (ms_per_step / 1000.0) / 1e9
 
     # end to end through host memory
@@ -585,7 +596,7 @@ def main():
         out = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
                "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
                "vs_baseline": None, "dtype": "f32" if T <= ds4.AUTO_DECODE_MAX_T else "bf16", "data": "synthetic",
-               "config": workload_config(wl, args.workload, l2_note, args.gains),
+               "config": workload_config(wl, args.workload, l2_note, args.gains, args.routed_format),
                "roofline": roofline,
                "layer_roofline": {"bound": "hbm" if args.workload != "prefill_t4096_zipf4" else "tensor",
                                   "bytes_per_step": lay_bytes, "achieved_gbs": layer_gbs,

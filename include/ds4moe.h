@@ -87,6 +87,24 @@ enum {
 };
 
 /*
+ * Layer flag: the routed gate/up/down weights are MXFP4 instead of 2-bit
+ * ("Running DeepSeek V4 Flash on an RTX 5080 ...", model list: the MXFP4 GGUF
+ * keeps DeepSeek's released MXFP4 routed experts; decode runs them on Q8
+ * activations). OCP microscaling element and scale types:
+ *   MXFP4 block, 17 bytes per 32 consecutive weights of one row: 16 bytes of
+ *     E2M1 codes (weight i at byte i/2, low nibble for even i), then the E8M0
+ *     scale X = 2^(byte - 127);   w_i = X * e2m1(c_i).
+ *   gate, up [E][I][H/32] blocks; down [E][H][I/32] blocks (router, shared
+ *   expert and down gains unchanged).
+ * Each routed-expert product quantises its input per 32 values first (x, and
+ * the SwiGLU rows before the down product): d = amax / 127, q = x / d rounded
+ * to the nearest integer (ties to even), both in binary32; the product uses
+ * d * q. Such a layer runs one path for every T (the path argument and
+ * DS4MOE_AUTO_DECODE_MAX_T do not apply).
+ */
+#define DS4MOE_FLAG_MXFP4 1u
+
+/*
  * Largest T for which DS4MOE_PATH_AUTO takes the decode path (launches of up to
  * 8 tokens): the measured crossover of the two paths on a GB300 at H=4096,
  * I=2048, E=384, top-6 (decode faster up to T=12, prefill from T=16).
@@ -112,7 +130,7 @@ typedef struct {
     int32_t top_k;        /* K, 1..min(E, 8) */
     int32_t shared_inter; /* I_sh, multiple of 256, or 0 for no shared expert */
     int32_t max_tokens;   /* largest T any call will pass, 1..65536 */
-    uint32_t flags;       /* reserved, must be 0 */
+    uint32_t flags;       /* 0 or DS4MOE_FLAG_MXFP4 */
 } ds4moe_layer_desc;
 
 /* Device pointers to the weights in the storage formats above. */

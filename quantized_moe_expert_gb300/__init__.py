@@ -23,6 +23,7 @@ DS4MOE_ESCRATCH = -7
 DS4MOE_NOALLOC_SCRATCH = 4 << 20
 PATH_AUTO, PATH_DECODE, PATH_PREFILL = 0, 1, 2
 AUTO_DECODE_MAX_T = 12
+FLAG_MXFP4 = 1
 
 
 class LayerDesc(ctypes.Structure):
@@ -197,9 +198,10 @@ class MoELayer:
     sh_gate, sh_up, sh_down, down_gain, down_gain2; router_bias, the shared ones
     and the gain tables may be None or absent)."""
 
-    def __init__(self, shape, weights: dict, max_tokens: int):
+    def __init__(self, shape, weights: dict, max_tokens: int, flags: int = 0):
         self.shape = shape
-        desc = make_desc(shape.hidden, shape.inter, shape.n_experts, shape.top_k, shape.shared_inter, max_tokens)
+        desc = make_desc(shape.hidden, shape.inter, shape.n_experts, shape.top_k, shape.shared_inter, max_tokens,
+                         flags)
         w = Weights(*(_addr(weights.get(k)) for k in
                       ("router_w", "router_bias", "gate", "up", "down", "sh_gate", "sh_up", "sh_down", "down_gain",
                        "down_gain2")))

@@ -129,6 +129,18 @@ struct Scratch {
     float *ysh;        // [Tmax][H]
     uint16_t *xstage;  // [Tmax][H] bf16 staging for host-memory calls
     float *ystage;     // [Tmax][H]
+    float *ax;         // MXFP4 layers: [Tmax][H] Q8-quantised token rows (d * q)
+    float *hf;         // MXFP4 layers: [Tmax*K][I] fp32 SwiGLU rows, expert-grouped order
+    float *ah;         // MXFP4 layers: [Tmax*K][I] their Q8-quantised values
+};
+
+// MXFP4 weights: per row and 32-weight block the 16 E2M1 code bytes as one
+// uint4 and the E8M0 scale byte.
+struct Mx4Mat {
+    const uint4 *codes;   // [rows][nb]
+    const uint8_t *scale; // [rows][nb]
+    int64_t rows;
+    int32_t nb; // 32-weight blocks per row
 };
 
 struct LayerDev {
@@ -139,6 +151,8 @@ struct LayerDev {
     Q2Mat gate, up, down; // rows: gate/up E*I (K = H), down E*H (K = I)
     Q8Mat sh_gate, sh_up, sh_down;
     const float *gain; // [E][H] per-expert down gains s1 * s2 expanded from the tables, or nullptr
+    bool mx4;          // routed experts in MXFP4 (mgate, mup, mdown) instead of 2-bit
+    Mx4Mat mgate, mup, mdown;
 };
 
 } // namespace ds4

@@ -18,6 +18,7 @@
 #include "decode_fused.cuh"
 #include "frag_layout.cuh"
 #include "dispatch.cuh"
+#include "mx4_experts.cuh"
 #include "prefill_gemm.cuh"
 #include "router.cuh"
 
@@ -140,7 +141,7 @@ bool is_device_ptr(const void *p) {
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 int check_desc(const ds4moe_layer_desc *d) {
-    if (!d || d->magic != DS4MOE_MAGIC || d->version != DS4MOE_VERSION || d->flags != 0)
+    if (!d || d->magic != DS4MOE_MAGIC || d->version != DS4MOE_VERSION || (d->flags & ~DS4MOE_FLAG_MXFP4) != 0)
         return DS4MOE_EINVAL;
     if (d->hidden <= 0 || d->hidden % 256 || d->inter <= 0 || d->inter % 256)
         return DS4MOE_EINVAL;
@@ -286,9 +287,21 @@ void layout_weights(ds4moe *h, Carver &c) {
     L.router_w3.nks = 3 * L.H / 64;
     L.router_w3.p = c.take<uint4>((uint64_t)((L.E + 127) / 128) * 128 * 3 * L.H / 8);
     L.router_bias = c.take<float>(L.E);
-    q2(L.gate, (int64_t)L.E * L.I, L.H);
-    q2(L.up, (int64_t)L.E * L.I, L.H);
-    q2(L.down, (int64_t)L.E * L.H, L.I);
+    auto m4 = [&](Mx4Mat &m, int64_t rows, int k) {
+        m.rows = rows;
+        m.nb = k / 32;
+        m.codes = c.take<uint4>((uint64_t)rows * m.nb);
+        m.scale = c.take<uint8_t>((uint64_t)rows * m.nb);
+    };
+    if (L.mx4) {
+        m4(L.mgate, (int64_t)L.E * L.I, L.H);
+        m4(L.mup, (int64_t)L.E * L.I, L.H);
+        m4(L.mdown, (int64_t)L.E * L.H, L.I);
+    } else {
+        q2(L.gate, (int64_t)L.E * L.I, L.H);
+        q2(L.up, (int64_t)L.E * L.I, L.H);
+        q2(L.down, (int64_t)L.E * L.H, L.I);
+    }
     if (L.Ish > 0) {
         q8(L.sh_gate, L.Ish, L.H);
         q8(L.sh_up, L.Ish, L.H);
@@ -306,6 +319,8 @@ void layout_weights(ds4moe *h, Carver &c) {
         m.nbq = k / 32;
         m.rec = c.take<uint8_t>((uint64_t)(rows / 16) * m.nbq * kQ8Rec);
     };
+    if (L.mx4)
+        return; // MXFP4 layers do not use the fused decode kernel or its layouts
     f2(D.gate, (int64_t)L.E * L.I, L.H);
     f2(D.up, (int64_t)L.E * L.I, L.H);
     f2(D.down, (int64_t)L.E * L.H, L.I);
@@ -349,6 +364,9 @@ void layout_scratch(ds4moe *h, Carver &c) {
     S.ysh = c.take<float>(T * L.H);
     S.xstage = c.take<uint16_t>(T * L.H);
     S.ystage = c.take<float>(T * L.H);
+    S.ax = L.mx4 ? c.take<float>(T * L.H) : nullptr;
+    S.hf = L.mx4 ? c.take<float>(P * L.I) : nullptr;
+    S.ah = L.mx4 ? c.take<float>(P * L.I) : nullptr;
     DecodeState &D = h->D;
     const int64_t Td = kDecodeT, Pd = (int64_t)kDecodeT * L.K;
     D.lgt = c.take<unsigned long long>(Td * L.E);
@@ -547,6 +565,34 @@ int run_dispatch(ds4moe *h, int T) {
     return launch_rc();
 }
 
+// The shared expert on tensor cores (dense over the T token rows of x): SwiGLU
+// rows into S.hsh, then the down product into S.ysh.
+int run_shared_gemms(ds4moe *h, const void *x, int T) {
+    const LayerDev &L = h->L;
+    Scratch &S = h->S;
+    int rc;
+    rc = x_maps(h, x, T);
+    if (rc)
+        return rc;
+    pf::Args s{};
+    s.status = h->status;
+    s.q8[0] = L.sh_gate;
+    s.q8[1] = L.sh_up;
+    s.M = L.Ish;
+    s.Kd = L.H;
+    s.dense_n = T;
+    s.out = S.hsh;
+    s.ldo = L.Ish;
+    launch_gemm<pf::kFmtQ8, 2, pf::kEpiSwiGLU>(h, "prefill_gateup_q8", h->map_x, s);
+    s.q8[0] = L.sh_down;
+    s.M = L.H;
+    s.Kd = L.Ish;
+    s.out = S.ysh;
+    s.ldo = L.H;
+    launch_gemm<pf::kFmtQ8, 1, pf::kEpiF32>(h, "prefill_down_q8", h->map_hsh, s);
+    return launch_rc();
+}
+
 // Experts and combine for the routing already in S.idx / S.w: grouped
 // tensor-core GEMMs over the expert-grouped rows.
 int run_experts_prefill(ds4moe *h, const void *x, int T, float *y) {
@@ -586,25 +632,47 @@ int run_experts_prefill(ds4moe *h, const void *x, int T, float *y) {
     a.ldo = L.H;
     launch_gemm<pf::kFmtQ2, 1, pf::kEpiF32>(h, "prefill_down_q2", h->map_h, a);
     if (L.Ish > 0) {
-        rc = x_maps(h, x, T);
+        rc = run_shared_gemms(h, x, T);
         if (rc)
             return rc;
-        pf::Args s{};
-        s.status = h->status;
-        s.q8[0] = L.sh_gate;
-        s.q8[1] = L.sh_up;
-        s.M = L.Ish;
-        s.Kd = L.H;
-        s.dense_n = T;
-        s.out = S.hsh;
-        s.ldo = L.Ish;
-        launch_gemm<pf::kFmtQ8, 2, pf::kEpiSwiGLU>(h, "prefill_gateup_q8", h->map_x, s);
-        s.q8[0] = L.sh_down;
-        s.M = L.H;
-        s.Kd = L.Ish;
-        s.out = S.ysh;
-        s.ldo = L.H;
-        launch_gemm<pf::kFmtQ8, 1, pf::kEpiF32>(h, "prefill_down_q8", h->map_hsh, s);
+    }
+    launch(h, "combine", [&] {
+        combine_kernel<<<blocks_for((int64_t)T * L.H / 4, 256), 256, 0, st>>>(
+            S.ye, L.Ish > 0 ? S.ysh : nullptr, S.w, S.inv, S.idx, L.gain, T, L.H, L.K, y);
+    });
+    return launch_rc();
+}
+
+// MXFP4 routed experts for the routing already in S.idx / S.w, every T: Q8
+// token rows, the gate/up product with SwiGLU, Q8 SwiGLU rows, the down
+// product, the shared expert, the combine.
+int run_experts_mx4(ds4moe *h, const void *x, int T, float *y) {
+    const LayerDev &L = h->L;
+    Scratch &S = h->S;
+    cudaStream_t st = h->stream;
+    int rc = run_dispatch(h, T);
+    if (rc)
+        return rc;
+    const int P = T * L.K;
+    const int U = P < L.E ? P : L.E; // bound on the distinct experts
+    launch(h, "mx4_act_x", [&] {
+        act_q8_kernel<<<blocks_for((int64_t)T * L.H, 256), 256, 0, st>>>(x, 1, (int64_t)T * L.H, S.ax);
+    });
+    launch(h, "mx4_gateup", [&] {
+        mx4_product_kernel<true><<<dim3((L.I + 7) / 8, U), 256, 0, st>>>(L.mgate, L.mup, S.ax, S.uexp, S.uoff,
+                                                                         S.nuniq, S.perm, L.K, L.I, L.H, S.hf);
+    });
+    launch(h, "mx4_act_h", [&] {
+        act_q8_kernel<<<blocks_for((int64_t)P * L.I, 256), 256, 0, st>>>(S.hf, 0, (int64_t)P * L.I, S.ah);
+    });
+    launch(h, "mx4_down", [&] {
+        mx4_product_kernel<false><<<dim3((L.H + 7) / 8, U), 256, 0, st>>>(L.mdown, L.mdown, S.ah, S.uexp, S.uoff,
+                                                                          S.nuniq, S.perm, L.K, L.H, L.I, S.ye);
+    });
+    if (L.Ish > 0) {
+        rc = run_shared_gemms(h, x, T);
+        if (rc)
+            return rc;
     }
     launch(h, "combine", [&] {
         combine_kernel<<<blocks_for((int64_t)T * L.H / 4, 256), 256, 0, st>>>(
@@ -704,6 +772,10 @@ int forward_impl(ds4moe *h, const void *x, int T, int path, float *y) {
     if (path == DS4MOE_PATH_AUTO)
         path = T <= DS4MOE_AUTO_DECODE_MAX_T ? DS4MOE_PATH_DECODE : DS4MOE_PATH_PREFILL;
     h->stats.path = path;
+    if (h->L.mx4) { // one path for every T
+        int rc = run_router(h, x, T, nullptr);
+        return rc ? rc : run_experts_mx4(h, x, T, y);
+    }
     if (path == DS4MOE_PATH_DECODE)
         return run_decode(h, x, T, y, nullptr, nullptr);
     int rc = run_router(h, x, T, nullptr);
@@ -776,6 +848,7 @@ int ds4moe_create(const ds4moe_layer_desc *desc, const ds4moe_weights *w, ds4moe
     L.K = desc->top_k;
     L.Ish = desc->shared_inter;
     L.Tmax = desc->max_tokens;
+    L.mx4 = (desc->flags & DS4MOE_FLAG_MXFP4) != 0;
     h->has_gain[0] = w->down_gain != nullptr;
     h->has_gain[1] = w->down_gain2 != nullptr;
 
@@ -837,9 +910,21 @@ int ds4moe_create(const ds4moe_layer_desc *desc, const ds4moe_weights *w, ds4moe
             static_cast<const uint16_t *>(src), nblk, m.nks * 2, const_cast<uint4 *>(m.qs),
             reinterpret_cast<uint16_t *>(const_cast<uint32_t *>(m.d)));
     };
-    rq2(w->gate, L.gate);
-    rq2(w->up, L.up);
-    rq2(w->down, L.down);
+    auto rm4 = [&](const void *src, Mx4Mat &m) {
+        const int64_t nblk = m.rows * m.nb;
+        repack_mx4_kernel<<<blocks_for(nblk, 256), 256, 0, st>>>(static_cast<const uint8_t *>(src), nblk,
+                                                                 const_cast<uint4 *>(m.codes),
+                                                                 const_cast<uint8_t *>(m.scale));
+    };
+    if (L.mx4) {
+        rm4(w->gate, L.mgate);
+        rm4(w->up, L.mup);
+        rm4(w->down, L.mdown);
+    } else {
+        rq2(w->gate, L.gate);
+        rq2(w->up, L.up);
+        rq2(w->down, L.down);
+    }
     if (has_shared) {
         rq8(w->sh_gate, L.sh_gate);
         rq8(w->sh_up, L.sh_up);
@@ -860,13 +945,15 @@ int ds4moe_create(const ds4moe_layer_desc *desc, const ds4moe_weights *w, ds4moe
         repack_q8_frag_kernel<<<blocks_for(n, 256), 256, 0, st>>>(static_cast<const uint8_t *>(src), m.rows, m.nbq,
                                                                    const_cast<uint8_t *>(m.rec));
     };
-    rf2(w->gate, D.gate);
-    rf2(w->up, D.up);
-    rf2(w->down, D.down);
-    if (has_shared) {
-        rf8(w->sh_gate, D.sh_gate);
-        rf8(w->sh_up, D.sh_up);
-        rf8(w->sh_down, D.sh_down);
+    if (!L.mx4) {
+        rf2(w->gate, D.gate);
+        rf2(w->up, D.up);
+        rf2(w->down, D.down);
+        if (has_shared) {
+            rf8(w->sh_gate, D.sh_gate);
+            rf8(w->sh_up, D.sh_up);
+            rf8(w->sh_down, D.sh_down);
+        }
     }
     cudaMemsetAsync(D.ctl, 0, sizeof(unsigned) * D.ctl_words, st);
     // no stale word may carry a future launch's epoch (epochs start at 1)
@@ -991,14 +1078,14 @@ int ds4moe_forward_routed(ds4moe_t *h, const void *x, int32_t T, const int32_t *
     h->stats.tokens = T;
     h->stats.path = path == DS4MOE_PATH_AUTO ? (T <= DS4MOE_AUTO_DECODE_MAX_T ? DS4MOE_PATH_DECODE : DS4MOE_PATH_PREFILL)
                                              : path;
-    if (h->stats.path == DS4MOE_PATH_DECODE)
+    if (h->stats.path == DS4MOE_PATH_DECODE && !L.mx4)
         return run_decode(h, x, T, y, idx, w);
     cudaMemcpyAsync(S.idx, idx, sizeof(int32_t) * T * L.K, cudaMemcpyDeviceToDevice, st);
     cudaMemcpyAsync(S.w, w, sizeof(float) * T * L.K, cudaMemcpyDeviceToDevice, st);
     rc = launch_rc();
     if (rc)
         return rc;
-    return run_experts_prefill(h, x, T, y);
+    return L.mx4 ? run_experts_mx4(h, x, T, y) : run_experts_prefill(h, x, T, y);
 }
 
 int ds4moe_forward_host(ds4moe_t *h, const void *x_host, int32_t T, float *y_host) {

@@ -41,7 +41,7 @@ S_GAIN1, S_GAIN2 = 9, 10
 GAIN_BLOCK_BYTES = 17
 GAIN_SCALE_BYTE = 127 - 5  # E8M0 2^-5: gains 1 + 2^-5 * e2m1 in [0.8125, 1.1875]
 MX4_BLOCK_BYTES = 17
-MX4_SCALE_BYTE = 127 - 6  # MXFP4 weight scales 2^-6, 2^-7, 2^-8: |w| <= 6 * 2^-6
+MX4_SCALE_BYTE = 127 - 3  # MXFP4 weight scales 2^-3, 2^-4, 2^-5: |w| <= 0.75
 S_X = 16
 
 Q2_BLOCK_BYTES = 84

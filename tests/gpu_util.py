@@ -15,7 +15,9 @@ NEAR_TIE = 1e-5
 
 
 def to_dev(layer: dict, dev="cuda") -> dict:
-    return {k: (None if v is None else torch.from_numpy(np.ascontiguousarray(v)).to(dev)) for k, v in layer.items()}
+    """The layer's arrays as device tensors (other entries, e.g. "routed_format", are left out)."""
+    return {k: (None if v is None else torch.from_numpy(np.ascontiguousarray(v)).to(dev)) for k, v in layer.items()
+            if v is None or isinstance(v, np.ndarray)}
 
 
 def x_to_dev(x: np.ndarray, dev="cuda") -> torch.Tensor:

@@ -37,6 +37,7 @@ def test_binding_constants_match_the_header():
     assert macro("DS4MOE_MAGIC") == ds4.DS4MOE_MAGIC
     assert macro("DS4MOE_VERSION") == ds4.DS4MOE_VERSION
     assert macro("DS4MOE_AUTO_DECODE_MAX_T") == ds4.AUTO_DECODE_MAX_T
+    assert macro("DS4MOE_FLAG_MXFP4") == ds4.FLAG_MXFP4
     # the weights struct the binding passes has the header's fields in order
     body = re.search(r"typedef struct \{([^}]*)\} ds4moe_weights;", text).group(1)
     fields = re.findall(r"\*\s*(\w+);", body)
@@ -55,7 +56,7 @@ def test_create_rejects_bad_descriptions_on_the_host():
     good = dict(hidden=512, inter=256, n_experts=32, top_k=6, shared_inter=256, max_tokens=8)
     bad = [dict(good, hidden=500), dict(good, inter=100), dict(good, n_experts=0), dict(good, top_k=9),
            dict(good, top_k=33), dict(good, shared_inter=32), dict(good, max_tokens=0),
-           dict(good, n_experts=2000)]
+           dict(good, n_experts=2000), dict(good, flags=2)]
     for b in bad:
         d = ds4.make_desc(**b)
         assert ds4._lib.ds4moe_create(ctypes.byref(d), ctypes.byref(w), ctypes.byref(h)) == ds4.DS4MOE_EINVAL

@@ -1,0 +1,117 @@
+"""GPU parity of layers with MXFP4 routed experts (DS4MOE_FLAG_MXFP4).
+
+The experts' products run on Q8-quantised activations, as the oracle's "q8"
+arithmetic does; routing, shared expert, down gains and combine are the ones of
+the 2-bit layer. Every compute call goes through the C ABI.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import quantized_moe_expert_gb300 as ds4
+import synth
+from gpu_util import TOL_DECODE, check_routing, rel_l2, to_dev, x_to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+def tokens(shape, T, seed):
+    return synth.normal_bf16(T * shape.hidden, seed, synth.S_X).reshape(T, shape.hidden)
+
+
+@pytest.fixture(scope="module")
+def tiny():
+    wl = synth.WORKLOADS["tiny"]
+    layer = synth.make_layer(wl.shape, wl.layer_seeds[0], routed_format="mx4")
+    moe = ds4.MoELayer(wl.shape, to_dev(layer), max_tokens=80, flags=ds4.FLAG_MXFP4)
+    yield wl.shape, layer, moe
+    moe.close()
+
+
+@pytest.mark.parametrize("T", [1, 3, 8, 13, 80])
+def test_forward_matches_oracle(tiny, T):
+    shape, layer, moe = tiny
+    x = tokens(shape, T, 1100 + T)
+    xd = x_to_dev(x)
+    y = moe.forward(xd).cpu().numpy()
+    idx, w, gap, _ = moe.route(xd)
+    y_ref, r = oracle.forward(shape, layer, x, act="q8")
+    near = check_routing(idx.cpu().numpy(), w.cpu().numpy(), gap.cpu().numpy(), r, shape.top_k)
+    if near.any():
+        y_ref = oracle.forward_routed(shape, layer, x, idx.cpu().numpy(), w.cpu().numpy().astype(np.float64),
+                                      act="q8")
+    assert rel_l2(y, y_ref) <= TOL_DECODE
+    assert moe.status() == 0
+
+
+def test_both_path_arguments_give_the_same_layer(tiny):
+    shape, layer, moe = tiny
+    xd = x_to_dev(tokens(shape, 5, 1201))
+    a = moe.forward(xd, path=ds4.PATH_DECODE)
+    b = moe.forward(xd, path=ds4.PATH_PREFILL)
+    assert torch.equal(a, b)
+    assert moe.status() == 0
+
+
+def test_forward_routed_and_gains(tiny):
+    shape, layer, _ = tiny
+    L = dict(layer)
+    L["down_gain"] = synth.gain_table(shape.n_experts, shape.hidden, 12, synth.S_GAIN1, 127 - 2)
+    moe = ds4.MoELayer(shape, to_dev(L), max_tokens=16, flags=ds4.FLAG_MXFP4)
+    try:
+        rng = np.random.default_rng(9)
+        T = 6
+        x = tokens(shape, T, 1301)
+        idx = np.stack([rng.choice(shape.n_experts, shape.top_k, replace=False) for _ in range(T)]).astype(np.int32)
+        w = rng.random((T, shape.top_k)).astype(np.float32)
+        y = moe.forward_routed(x_to_dev(x), torch.from_numpy(idx).cuda(), torch.from_numpy(w).cuda()).cpu().numpy()
+        y_ref = oracle.forward_routed(shape, L, x, idx, w.astype(np.float64), act="q8")
+        y_plain = oracle.forward_routed(shape, layer, x, idx, w.astype(np.float64), act="q8")
+        assert rel_l2(y_plain, y_ref) > 0.1
+        assert rel_l2(y, y_ref) <= TOL_DECODE
+        assert moe.status() == 0
+    finally:
+        moe.close()
+
+
+def test_q8_activations_are_what_the_layer_uses(tiny):
+    """The oracle with exact activations is measurably farther from the kernels
+    than the oracle with Q8 activations (the quantisation is really applied)."""
+    shape, layer, moe = tiny
+    T = 8
+    x = tokens(shape, T, 1401)
+    r = oracle.route(shape, layer["router_w"], None, x)
+    w32 = r["weights"].astype(np.float32)
+    y = moe.forward_routed(x_to_dev(x), torch.from_numpy(r["idx"]).cuda(), torch.from_numpy(w32).cuda()).cpu().numpy()
+    yq = oracle.forward_routed(shape, layer, x, r["idx"], w32.astype(np.float64), act="q8")
+    ye = oracle.forward_routed(shape, layer, x, r["idx"], w32.astype(np.float64), act="exact")
+    assert rel_l2(y, yq) <= TOL_DECODE < rel_l2(y, ye)
+
+
+@pytest.fixture(scope="module")
+def big():
+    wl = synth.WORKLOADS["decode_t1"]
+    layer = synth.make_layer(wl.shape, wl.layer_seeds[0], routed_format="mx4")
+    dev = to_dev(layer)
+    moe = ds4.MoELayer(wl.shape, dev, max_tokens=8, flags=ds4.FLAG_MXFP4)
+    del dev
+    torch.cuda.empty_cache()
+    yield wl.shape, layer, moe
+    moe.close()
+
+
+def test_full_size_t1_and_t8(big):
+    """H=4096, E=384 MXFP4 layer: the decode token pool's first token and the
+    eight-token batch, each on the library's own routing (checked too)."""
+    shape, layer, moe = big
+    for x in (synth.make_tokens("decode_t1", T=1), synth.make_tokens("decode_t8")):
+        xd = x_to_dev(x)
+        y = moe.forward(xd).cpu().numpy()
+        idx, w, gap, _ = moe.route(xd)
+        idx, w = idx.cpu().numpy(), w.cpu().numpy()
+        r = oracle.route(shape, layer["router_w"], None, x)
+        check_routing(idx, w, gap.cpu().numpy(), r, shape.top_k)
+        y_ref = oracle.forward_routed(shape, layer, x, idx, w.astype(np.float64), act="q8")
+        assert rel_l2(y, y_ref) <= TOL_DECODE
+    assert moe.status() == 0
