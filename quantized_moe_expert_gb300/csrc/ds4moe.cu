@@ -658,16 +658,26 @@ int run_experts_mx4(ds4moe *h, const void *x, int T, float *y) {
     launch(h, "mx4_act_x", [&] {
         act_q8_kernel<<<blocks_for((int64_t)T * L.H, 256), 256, 0, st>>>(x, 1, (int64_t)T * L.H, S.ax);
     });
+    // an expert holds at most T rows when a token's experts are distinct; more come in chunks
+    const int nt = T <= 1 ? 1 : T <= 2 ? 2 : T <= 4 ? 4 : 8;
     launch(h, "mx4_gateup", [&] {
-        mx4_product_kernel<true><<<dim3((L.I + 7) / 8, U), 256, 0, st>>>(L.mgate, L.mup, S.ax, S.uexp, S.uoff,
-                                                                         S.nuniq, S.perm, L.K, L.I, L.H, S.hf);
+        const dim3 grid((L.I + 7) / 8, U);
+        auto k = nt == 1   ? mx4_product_kernel<true, 1>
+                 : nt == 2 ? mx4_product_kernel<true, 2>
+                 : nt == 4 ? mx4_product_kernel<true, 4>
+                           : mx4_product_kernel<true, 8>;
+        k<<<grid, 256, 0, st>>>(L.mgate, L.mup, S.ax, S.uexp, S.uoff, S.nuniq, S.perm, L.K, L.I, L.H, S.hf);
     });
     launch(h, "mx4_act_h", [&] {
         act_q8_kernel<<<blocks_for((int64_t)P * L.I, 256), 256, 0, st>>>(S.hf, 0, (int64_t)P * L.I, S.ah);
     });
     launch(h, "mx4_down", [&] {
-        mx4_product_kernel<false><<<dim3((L.H + 7) / 8, U), 256, 0, st>>>(L.mdown, L.mdown, S.ah, S.uexp, S.uoff,
-                                                                          S.nuniq, S.perm, L.K, L.H, L.I, S.ye);
+        const dim3 grid((L.H + 7) / 8, U);
+        auto k = nt == 1   ? mx4_product_kernel<false, 1>
+                 : nt == 2 ? mx4_product_kernel<false, 2>
+                 : nt == 4 ? mx4_product_kernel<false, 4>
+                           : mx4_product_kernel<false, 8>;
+        k<<<grid, 256, 0, st>>>(L.mdown, L.mdown, S.ah, S.uexp, S.uoff, S.nuniq, S.perm, L.K, L.H, L.I, S.ye);
     });
     if (L.Ish > 0) {
         rc = run_shared_gemms(h, x, T);

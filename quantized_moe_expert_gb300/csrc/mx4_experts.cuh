@@ -78,7 +78,12 @@ __device__ __forceinline__ float e2m1_value(unsigned c) {
 // GATEUP) with activation rows act[row_of(pos)][0..Kd).
 // GATEUP: A = gate, B = up, act rows are tokens perm[pos] / K, out = h (fp32);
 // else A = down, act rows are grouped positions, out = ye.
-template <bool GATEUP>
+// NT: rows of the expert handled together (the launch's bound on an expert's
+// rows, 1, 2, 4 or 8; more are taken in chunks of NT). A lane first loads the
+// codes and scales of up to kMx4LaneBlocks of its blocks, then multiplies.
+constexpr int kMx4LaneBlocks = 4;
+
+template <bool GATEUP, int NT>
 __global__ void __launch_bounds__(256) mx4_product_kernel(Mx4Mat A, Mx4Mat B, const float *__restrict__ act,
                                                           const int32_t *__restrict__ uexp,
                                                           const int32_t *__restrict__ uoff,
@@ -96,66 +101,82 @@ __global__ void __launch_bounds__(256) mx4_product_kernel(Mx4Mat A, Mx4Mat B, co
     const int p0 = __ldg(uoff + u), p1 = __ldg(uoff + u + 1);
     const int nb = Kd / 32;
     const int64_t row = ((int64_t)e * M + r) * nb;
-    for (int c0 = p0; c0 < p1; c0 += 8) {
-        const int n = p1 - c0 < 8 ? p1 - c0 : 8;
-        const float *arow[8];
+    for (int c0 = p0; c0 < p1; c0 += NT) {
+        const int n = p1 - c0 < NT ? p1 - c0 : NT;
+        const float *arow[NT];
 #pragma unroll
-        for (int t = 0; t < 8; t++) {
+        for (int t = 0; t < NT; t++) {
             const int pos = c0 + (t < n ? t : 0);
             const int64_t ar = GATEUP ? __ldg(perm + pos) / K : pos;
             arow[t] = act + ar * Kd;
         }
-        float ga[8], ua[8];
+        float ga[NT], ua[NT];
 #pragma unroll
-        for (int t = 0; t < 8; t++)
+        for (int t = 0; t < NT; t++)
             ga[t] = ua[t] = 0.f;
-        for (int b = lane; b < nb; b += 32) {
-            const uint4 ca = __ldg(A.codes + row + b);
-            const float Xa = e8m0_value(__ldg(A.scale + row + b));
-            uint4 cb = make_uint4(0, 0, 0, 0);
-            float Xb = 0.f;
-            if (GATEUP) {
-                cb = __ldg(B.codes + row + b);
-                Xb = e8m0_value(__ldg(B.scale + row + b));
-            }
-            const uint32_t wa[4] = {ca.x, ca.y, ca.z, ca.w};
-            const uint32_t wb[4] = {cb.x, cb.y, cb.z, cb.w};
-            float pa[8], pb[8];
+        for (int b0 = lane; b0 < nb; b0 += 32 * kMx4LaneBlocks) {
+            uint4 ca[kMx4LaneBlocks], cb[kMx4LaneBlocks];
+            unsigned sa[kMx4LaneBlocks], sb[kMx4LaneBlocks];
 #pragma unroll
-            for (int t = 0; t < 8; t++)
-                pa[t] = pb[t] = 0.f;
-#pragma unroll
-            for (int q = 0; q < 4; q++) { // 8 weights per code word
-                float va[8], vb[8];
-#pragma unroll
-                for (int i = 0; i < 8; i++) {
-                    va[i] = e2m1_value(wa[q] >> (4 * i));
-                    vb[i] = GATEUP ? e2m1_value(wb[q] >> (4 * i)) : 0.f;
-                }
-#pragma unroll
-                for (int t = 0; t < 8; t++) {
-                    if (t < n) {
-                        const float4 x0 = __ldg(reinterpret_cast<const float4 *>(arow[t] + b * 32 + 8 * q));
-                        const float4 x1 = __ldg(reinterpret_cast<const float4 *>(arow[t] + b * 32 + 8 * q + 4));
-                        const float xv[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-#pragma unroll
-                        for (int i = 0; i < 8; i++) {
-                            pa[t] = fmaf(va[i], xv[i], pa[t]);
-                            if (GATEUP)
-                                pb[t] = fmaf(vb[i], xv[i], pb[t]);
-                        }
+            for (int j = 0; j < kMx4LaneBlocks; j++) {
+                const int b = b0 + 32 * j;
+                ca[j] = cb[j] = make_uint4(0, 0, 0, 0);
+                sa[j] = sb[j] = 0;
+                if (b < nb) {
+                    ca[j] = __ldg(A.codes + row + b);
+                    sa[j] = __ldg(A.scale + row + b);
+                    if (GATEUP) {
+                        cb[j] = __ldg(B.codes + row + b);
+                        sb[j] = __ldg(B.scale + row + b);
                     }
                 }
             }
 #pragma unroll
-            for (int t = 0; t < 8; t++) {
-                ga[t] = fmaf(Xa, pa[t], ga[t]);
-                if (GATEUP)
-                    ua[t] = fmaf(Xb, pb[t], ua[t]);
+            for (int j = 0; j < kMx4LaneBlocks; j++) {
+                const int b = b0 + 32 * j;
+                if (b < nb) {
+                    const uint32_t wa[4] = {ca[j].x, ca[j].y, ca[j].z, ca[j].w};
+                    const uint32_t wb[4] = {cb[j].x, cb[j].y, cb[j].z, cb[j].w};
+                    float pa[NT], pb[NT];
+#pragma unroll
+                    for (int t = 0; t < NT; t++)
+                        pa[t] = pb[t] = 0.f;
+#pragma unroll
+                    for (int q = 0; q < 4; q++) { // 8 weights per code word
+                        float va[8], vb[8];
+#pragma unroll
+                        for (int i = 0; i < 8; i++) {
+                            va[i] = e2m1_value(wa[q] >> (4 * i));
+                            vb[i] = GATEUP ? e2m1_value(wb[q] >> (4 * i)) : 0.f;
+                        }
+#pragma unroll
+                        for (int t = 0; t < NT; t++) {
+                            if (t < n) {
+                                const float4 x0 = __ldg(reinterpret_cast<const float4 *>(arow[t] + b * 32 + 8 * q));
+                                const float4 x1 =
+                                    __ldg(reinterpret_cast<const float4 *>(arow[t] + b * 32 + 8 * q + 4));
+                                const float xv[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+#pragma unroll
+                                for (int i = 0; i < 8; i++) {
+                                    pa[t] = fmaf(va[i], xv[i], pa[t]);
+                                    if (GATEUP)
+                                        pb[t] = fmaf(vb[i], xv[i], pb[t]);
+                                }
+                            }
+                        }
+                    }
+                    const float Xa = e8m0_value(sa[j]), Xb = GATEUP ? e8m0_value(sb[j]) : 0.f;
+#pragma unroll
+                    for (int t = 0; t < NT; t++) {
+                        ga[t] = fmaf(Xa, pa[t], ga[t]);
+                        if (GATEUP)
+                            ua[t] = fmaf(Xb, pb[t], ua[t]);
+                    }
+                }
             }
         }
 #pragma unroll
-        for (int t = 0; t < 8; t++) {
+        for (int t = 0; t < NT; t++) {
             const float g = warp_sum(ga[t]);
             const float uu = GATEUP ? warp_sum(ua[t]) : 0.f;
             if (lane == 0 && t < n)
