@@ -37,6 +37,10 @@ _lib = None
 _vp = ctypes.c_void_p
 
 
+class _VqMat(ctypes.Structure):
+    _fields_ = [("stream", ctypes.c_void_p), ("plane", ctypes.c_void_p), ("gains", ctypes.c_void_p)]
+
+
 def _load():
     global _lib
     if _lib is None:
@@ -85,6 +89,17 @@ def _configure(lib):
     lib.oracle_e8m0.restype = ctypes.c_double
     lib.oracle_gain_block.argtypes = [_vp, _vp]
     lib.oracle_dequant_mx4.argtypes = [_vp, _vp]
+    lib.oracle_e4m3.argtypes = [ctypes.c_uint8]
+    lib.oracle_e4m3.restype = ctypes.c_double
+    lib.oracle_vq_index.argtypes = [_vp, _vp, ctypes.c_int64]
+    lib.oracle_vq_index.restype = ctypes.c_int32
+    lib.oracle_dequant_vq_row.argtypes = [_vp, _vp, _vp, _vp, ctypes.c_int64, ctypes.c_int64, _vp]
+    lib.oracle_expert_vq.argtypes = [ctypes.POINTER(_Shape), _vp, ctypes.POINTER(_VqMat), ctypes.POINTER(_VqMat),
+                                     ctypes.POINTER(_VqMat), ctypes.c_int32, _vp, _vp]
+    lib.oracle_forward_routed_vq.argtypes = [ctypes.POINTER(_Shape), _vp, ctypes.POINTER(_VqMat),
+                                             ctypes.POINTER(_VqMat), ctypes.POINTER(_VqMat), _vp, _vp, _vp, _vp, _vp,
+                                             _vp, ctypes.c_int32, _vp, _vp, _vp, ctypes.c_int32]
+    lib.oracle_forward_routed_vq.restype = ctypes.c_int
     lib.oracle_act_q8.argtypes = [_vp, ctypes.c_int64, _vp, _vp]
     lib.oracle_act_mx4.argtypes = [_vp, ctypes.c_int64, _vp, _vp]
     lib.oracle_e2m1_nearest.argtypes = [ctypes.c_double]
@@ -281,6 +296,53 @@ def expert_mx4(shape, act: str, gate_e: np.ndarray, up_e: np.ndarray, down_e: np
     return ye
 
 
+def e4m3(b: int) -> float:
+    """Value of an FP8 E4M3 byte."""
+    return _load().oracle_e4m3(b)
+
+
+def vq_index(stream: np.ndarray, plane, k: int) -> int:
+    """Index k of a VQ index stream (with bit 12 from the plane, if given)."""
+    st = np.ascontiguousarray(stream, dtype=np.uint8)
+    pl = None if plane is None else np.ascontiguousarray(plane, dtype=np.uint8)
+    return int(_load().oracle_vq_index(_p(st), _p(pl), k))
+
+
+def dequant_vq_row(codebook, stream, plane, gains, r: int, k: int) -> np.ndarray:
+    """Row r (k weights) of one expert's VQ matrix."""
+    cb = np.ascontiguousarray(codebook, dtype=np.uint8)
+    st = np.ascontiguousarray(stream, dtype=np.uint8)
+    pl = None if plane is None else np.ascontiguousarray(plane, dtype=np.uint8)
+    g = np.ascontiguousarray(gains, dtype=np.uint16)
+    w = np.empty(k, dtype=np.float64)
+    _load().oracle_dequant_vq_row(_p(cb), _p(st), _p(pl), _p(g), r, k, _p(w))
+    return w
+
+
+def _vq_mats(layer):
+    keep = []
+    mats = []
+    for name in ("gate", "up", "down"):
+        arrs = [np.ascontiguousarray(layer[name], dtype=np.uint8),
+                None if layer.get(name + "_plane") is None else np.ascontiguousarray(layer[name + "_plane"],
+                                                                                     dtype=np.uint8),
+                np.ascontiguousarray(layer[name + "_rowgain"], dtype=np.uint16)]
+        keep += arrs
+        mats.append(_VqMat(*(_p(a) for a in arrs)))
+    return mats, keep
+
+
+def expert_vq(shape, layer: dict, e: int, xt: np.ndarray) -> np.ndarray:
+    """VQ routed expert e of the layer on one float64 activation vector."""
+    xt = np.ascontiguousarray(xt, dtype=np.float64)
+    ye = np.empty(shape.hidden, dtype=np.float64)
+    s = _shape(shape)
+    mats, keep = _vq_mats(layer)
+    cb = np.ascontiguousarray(layer["codebook"], dtype=np.uint8)
+    _load().oracle_expert_vq(ctypes.byref(s), _p(cb), *(ctypes.byref(m) for m in mats), e, _p(xt), _p(ye))
+    return ye
+
+
 def forward_routed(shape, layer: dict, x_bf16: np.ndarray, idx: np.ndarray, weights: np.ndarray,
                    nthreads: int = 0, act: str | None = None) -> np.ndarray:
     """Layer output [T, H] float64 for the given routing (with the layer's down gains
@@ -296,7 +358,12 @@ def forward_routed(shape, layer: dict, x_bf16: np.ndarray, idx: np.ndarray, weig
     common = (_p(layer["gate"]), _p(layer["up"]), _p(layer["down"]), _p(layer.get("sh_gate")),
               _p(layer.get("sh_up")), _p(layer.get("sh_down")), _p(layer.get("down_gain")),
               _p(layer.get("down_gain2")), _p(x), T, _p(idx), _p(weights), _p(y), nthreads)
-    if layer.get("routed_format", "q2") == "mx4":
+    if layer.get("routed_format", "q2") == "vq":
+        mats, keep = _vq_mats(layer)
+        cb = np.ascontiguousarray(layer["codebook"], dtype=np.uint8)
+        rc = _load().oracle_forward_routed_vq(ctypes.byref(s), _p(cb), *(ctypes.byref(m) for m in mats),
+                                              *common[3:])
+    elif layer.get("routed_format", "q2") == "mx4":
         rc = _load().oracle_forward_routed_mx4(ctypes.byref(s), ACT[act], *common)
     else:
         assert act in (None, "exact"), "2-bit routed experts take exact activations"

@@ -72,6 +72,22 @@
  *       saturating at 6); the product uses X*e2m1.
  *   The input x (bf16) is exact in binary32; the SwiGLU output h is rounded to
  *   binary32 (the kernels' precision) before it is quantised.
+ *
+ * VQ routed experts ("YoungAi - DeepSeek V4.1 Flash on one DGX Spark",
+ * section 4.1): every 8 consecutive weights of a row are one codeword of a
+ * per-layer codebook (shared by all experts and all three matrices) times one
+ * gain per row:  w[r, 8j .. 8j+7] = g_r * C[idx[r, j]].
+ *   codebook C: 2^bits x 8 codeword values as OCP FP8 E4M3 bytes (bits = 12
+ *     or 13), entry n at bytes 8n .. 8n+7;
+ *   index stream of one expert matrix: the rows' indices back to back (row r,
+ *     group j at position r * K/8 + j), 12 bits each, packed least significant
+ *     bit first (index k at bits 12k .. 12k+11 of the byte string), so every
+ *     256 indices fill one 384-byte block;
+ *   13-bit layers add a bit plane: bit k (least significant first) is bit 12
+ *     of index k;
+ *   gains: one binary16 g_r per row.
+ *   Matrices [E] streams of rows = I (gate, up; K = H) or H (down; K = I).
+ *   Activations are not quantised.
  */
 #include <math.h>
 #include <omp.h>
@@ -251,6 +267,43 @@ static void quantise_act(int act, const double *v, int64_t n, double *out)
     free(c);
     free(d);
     free(sc);
+}
+
+/* OCP FP8 E4M3: sign bit 7, exponent bits 6-3 (bias 7), mantissa bits 2-0;
+ * exponent 0 is subnormal; S.1111.111 is NaN (no infinities). */
+double oracle_e4m3(uint8_t b)
+{
+    const int sign = b >> 7, ex = (b >> 3) & 15, man = b & 7;
+    if (ex == 15 && man == 7)
+        return NAN;
+    const double mag = ex == 0 ? ldexp((double)man, -9) : ldexp(8.0 + man, ex - 10);
+    return sign ? -mag : mag;
+}
+
+/* Index k of a VQ index stream (12-bit, least significant bit first), with
+ * bit 12 from the bit plane when plane is not NULL. */
+int32_t oracle_vq_index(const uint8_t *stream, const uint8_t *plane, int64_t k)
+{
+    int32_t v = 0;
+    for (int i = 0; i < 12; i++) {
+        const int64_t bit = 12 * k + i;
+        v |= ((stream[bit / 8] >> (bit % 8)) & 1) << i;
+    }
+    if (plane)
+        v |= ((plane[k / 8] >> (k % 8)) & 1) << 12;
+    return v;
+}
+
+/* Row r (k weights) of a VQ matrix: w = g_r * C[idx]. */
+void oracle_dequant_vq_row(const uint8_t *codebook, const uint8_t *stream, const uint8_t *plane,
+                           const uint16_t *gains, int64_t r, int64_t k, double *w)
+{
+    const double g = oracle_f16(gains[r]);
+    for (int64_t j = 0; j < k / 8; j++) {
+        const int32_t n = oracle_vq_index(stream, plane, r * (k / 8) + j);
+        for (int i = 0; i < 8; i++)
+            w[8 * j + i] = g * oracle_e4m3(codebook[8 * n + i]);
+    }
 }
 
 /* One 2-bit block -> 256 weights. */
@@ -458,6 +511,44 @@ void oracle_expert_mx4(const oracle_shape *s, int32_t act, const uint8_t *gate_e
     free(hq);
 }
 
+/* One VQ matrix of a layer: the expert's index stream, bit plane (13-bit
+ * layers; NULL for 12-bit) and row gains are at expert e of these arrays. */
+typedef struct {
+    const uint8_t *stream; /* [E][rows * K/8 * 12/8] */
+    const uint8_t *plane;  /* [E][rows * K/8 / 8] or NULL */
+    const uint16_t *gains; /* [E][rows] binary16 */
+} oracle_vq_mat;
+
+static void vq_row(const uint8_t *codebook, const oracle_vq_mat *m, int e, int64_t rows, int64_t r, int64_t k,
+                   double *w)
+{
+    const int64_t n = rows * (k / 8);
+    oracle_dequant_vq_row(codebook, m->stream + e * (n * 12 / 8), m->plane ? m->plane + e * (n / 8) : NULL,
+                          m->gains + e * rows, r, k, w);
+}
+
+/* One VQ routed expert e: ye = Wd (silu(Wg x) * (Wu x)). */
+void oracle_expert_vq(const oracle_shape *s, const uint8_t *codebook, const oracle_vq_mat *gate,
+                      const oracle_vq_mat *up, const oracle_vq_mat *down, int32_t e, const double *xt, double *ye)
+{
+    const int H = s->hidden, I = s->inter;
+    double *w = (double *)malloc(sizeof(double) * (H > I ? H : I));
+    double *h = (double *)malloc(sizeof(double) * I);
+    for (int i = 0; i < I; i++) {
+        vq_row(codebook, gate, e, I, i, H, w);
+        double g = dot(w, xt, H);
+        vq_row(codebook, up, e, I, i, H, w);
+        double u = dot(w, xt, H);
+        h[i] = oracle_silu(g) * u;
+    }
+    for (int j = 0; j < H; j++) {
+        vq_row(codebook, down, e, H, j, I, w);
+        ye[j] = dot(w, h, I);
+    }
+    free(w);
+    free(h);
+}
+
 void oracle_shared_q8(const oracle_shape *s, const uint8_t *sh_gate, const uint8_t *sh_up,
                       const uint8_t *sh_down, const double *xt, double *ysh)
 {
@@ -487,8 +578,8 @@ void oracle_shared_q8(const oracle_shape *s, const uint8_t *sh_gate, const uint8
  * Tokens are independent and each row is computed by one thread in a fixed
  * order, so the result does not depend on nthreads (<= 0: library default).
  */
-static int forward_routed_any(const oracle_shape *s, int mx4, int32_t act, const uint8_t *gate, const uint8_t *up,
-                              const uint8_t *down, const uint8_t *sh_gate, const uint8_t *sh_up,
+static int forward_routed_any(const oracle_shape *s, int mx4, int32_t act, const uint8_t *codebook,
+                              const oracle_vq_mat *vq, const uint8_t *gate, const uint8_t *up, const uint8_t *down, const uint8_t *sh_gate, const uint8_t *sh_up,
                               const uint8_t *sh_down, const uint8_t *gain1, const uint8_t *gain2,
                               const uint16_t *x, int32_t T, const int32_t *idx, const double *weights,
                               double *y, int32_t nthreads)
@@ -496,7 +587,7 @@ static int forward_routed_any(const oracle_shape *s, int mx4, int32_t act, const
     const int H = s->hidden, I = s->inter, E = s->n_experts, K = s->top_k;
     if (H <= 0 || I <= 0 || H % 256 || I % 256 || K <= 0 || K > E || T < 0)
         return -1;
-    if (act < ACT_EXACT || act > ACT_MX4 || (!mx4 && act != ACT_EXACT))
+    if (act < ACT_EXACT || act > ACT_MX4 || (!mx4 && act != ACT_EXACT) || (vq && !codebook))
         return -1;
     const int has_shared = s->shared_inter > 0 && sh_gate && sh_up && sh_down;
     if (has_shared && s->shared_inter % 32)
@@ -516,7 +607,9 @@ static int forward_routed_any(const oracle_shape *s, int mx4, int32_t act, const
             xt[h] = oracle_bf16(x[(int64_t)t * H + h]);
         for (int k = 0; k < K; k++) {
             int e = idx[(int64_t)t * K + k];
-            if (mx4)
+            if (vq)
+                oracle_expert_vq(s, codebook, &vq[0], &vq[1], &vq[2], e, xt, ye);
+            else if (mx4)
                 oracle_expert_mx4(s, act, gate + e * expert_gate, up + e * expert_gate, down + e * expert_down, xt,
                                   ye);
             else
@@ -553,8 +646,8 @@ int oracle_forward_routed_gain(const oracle_shape *s, const uint8_t *gate, const
                                const uint16_t *x, int32_t T, const int32_t *idx, const double *weights,
                                double *y, int32_t nthreads)
 {
-    return forward_routed_any(s, 0, ACT_EXACT, gate, up, down, sh_gate, sh_up, sh_down, gain1, gain2, x, T, idx,
-                              weights, y, nthreads);
+    return forward_routed_any(s, 0, ACT_EXACT, NULL, NULL, gate, up, down, sh_gate, sh_up, sh_down, gain1, gain2, x,
+                              T, idx, weights, y, nthreads);
 }
 
 /* The layer with MXFP4 routed experts and act-quantised expert activations. */
@@ -564,8 +657,20 @@ int oracle_forward_routed_mx4(const oracle_shape *s, int32_t act, const uint8_t 
                               const uint16_t *x, int32_t T, const int32_t *idx, const double *weights,
                               double *y, int32_t nthreads)
 {
-    return forward_routed_any(s, 1, act, gate, up, down, sh_gate, sh_up, sh_down, gain1, gain2, x, T, idx, weights,
-                              y, nthreads);
+    return forward_routed_any(s, 1, act, NULL, NULL, gate, up, down, sh_gate, sh_up, sh_down, gain1, gain2, x, T, idx,
+                              weights, y, nthreads);
+}
+
+/* The layer with VQ routed experts (codebook and the three matrices). */
+int oracle_forward_routed_vq(const oracle_shape *s, const uint8_t *codebook, const oracle_vq_mat *gate,
+                             const oracle_vq_mat *up, const oracle_vq_mat *down, const uint8_t *sh_gate,
+                             const uint8_t *sh_up, const uint8_t *sh_down, const uint8_t *gain1,
+                             const uint8_t *gain2, const uint16_t *x, int32_t T, const int32_t *idx,
+                             const double *weights, double *y, int32_t nthreads)
+{
+    const oracle_vq_mat vq[3] = {*gate, *up, *down};
+    return forward_routed_any(s, 0, ACT_EXACT, codebook, vq, NULL, NULL, NULL, sh_gate, sh_up, sh_down, gain1, gain2,
+                              x, T, idx, weights, y, nthreads);
 }
 
 /* oracle_forward_routed_gain without down gains. */

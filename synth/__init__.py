@@ -38,6 +38,11 @@ SEED_BASE = 0xD54E0000
 # stream ids of the counter-based generator
 S_ROUTER, S_GATE, S_UP, S_DOWN, S_SH_GATE, S_SH_UP, S_SH_DOWN, S_BIAS_RANK = range(1, 9)
 S_GAIN1, S_GAIN2 = 9, 10
+# VQ experts: codebook, then per matrix (gate, up, down) its bit plane and row gains
+S_CODEBOOK = 11
+S_GATE_PLANE, S_UP_PLANE, S_DOWN_PLANE = 12, 13, 14
+S_GATE_ROWGAIN, S_UP_ROWGAIN, S_DOWN_ROWGAIN = 17, 18, 19
+VQ_ROWGAIN_SIGMA = 0.05
 GAIN_BLOCK_BYTES = 17
 GAIN_SCALE_BYTE = 127 - 5  # E8M0 2^-5: gains 1 + 2^-5 * e2m1 in [0.8125, 1.1875]
 MX4_BLOCK_BYTES = 17
@@ -73,6 +78,10 @@ def _load():
         lib.synth_fill_q8.argtypes = [u8p, ctypes.c_int64, ctypes.c_uint64, ctypes.c_uint64, ctypes.c_double]
         lib.synth_fill_gain.argtypes = [u8p, ctypes.c_int64, ctypes.c_uint64, ctypes.c_uint64, ctypes.c_uint8]
         lib.synth_fill_mx4.argtypes = [u8p, ctypes.c_int64, ctypes.c_uint64, ctypes.c_uint64, ctypes.c_uint8]
+        lib.synth_fill_bytes.argtypes = [u8p, ctypes.c_int64, ctypes.c_uint64, ctypes.c_uint64]
+        lib.synth_fill_e4m3_codebook.argtypes = [u8p, ctypes.c_int64, ctypes.c_uint64, ctypes.c_uint64]
+        lib.synth_fill_f16_abs_normal.argtypes = [ctypes.POINTER(ctypes.c_uint16), ctypes.c_int64, ctypes.c_uint64,
+                                                  ctypes.c_uint64, ctypes.c_double]
         lib.synth_fill_normal_f32.argtypes = [ctypes.POINTER(ctypes.c_float), ctypes.c_int64,
                                               ctypes.c_uint64, ctypes.c_uint64, ctypes.c_double]
         lib.synth_fill_normal_bf16.argtypes = [ctypes.POINTER(ctypes.c_uint16), ctypes.c_int64,
@@ -217,12 +226,43 @@ def mx4_matrix(rows: int, k: int, seed: int, stream: int, base_byte: int = MX4_S
     return out
 
 
+def random_bytes(n: int, seed: int, stream: int) -> np.ndarray:
+    out = np.empty(n, dtype=np.uint8)
+    _load().synth_fill_bytes(_ptr(out, ctypes.c_uint8), n, seed, stream)
+    return out
+
+
+def e4m3_codebook(entries: int, seed: int, stream: int = S_CODEBOOK) -> np.ndarray:
+    """[entries][8] FP8 E4M3 codeword bytes."""
+    out = np.empty(entries * 8, dtype=np.uint8)
+    _load().synth_fill_e4m3_codebook(_ptr(out, ctypes.c_uint8), out.size, seed, stream)
+    return out.reshape(entries, 8)
+
+
+def f16_abs_normal(n: int, seed: int, stream: int, sigma: float) -> np.ndarray:
+    out = np.empty(n, dtype=np.uint16)
+    _load().synth_fill_f16_abs_normal(_ptr(out, ctypes.c_uint16), n, seed, stream, sigma)
+    return out
+
+
+def vq_matrix(n_experts: int, rows: int, k: int, bits: int, seed: int, stream: int, plane_stream: int,
+              gain_stream: int):
+    """One VQ matrix: (index streams [E][rows*k/8*3/2] bytes, bit planes [E][rows*k/64] or
+    None, row gains [E][rows] binary16 bits). Indices are uniform."""
+    n = rows * (k // 8)
+    idx = random_bytes(n_experts * n * 3 // 2, seed, stream).reshape(n_experts, n * 3 // 2)
+    plane = random_bytes(n_experts * n // 8, seed, plane_stream).reshape(n_experts, n // 8) if bits == 13 else None
+    g = f16_abs_normal(n_experts * rows, seed, gain_stream, VQ_ROWGAIN_SIGMA).reshape(n_experts, rows)
+    return idx, plane, g
+
+
 def make_layer(shape: Shape, seed: int, zipf: bool = False, zipf_beta_value: float | None = None,
-               gains: int = 0, routed_format: str = "q2") -> dict:
+               gains: int = 0, routed_format: str = "q2", vq_bits: int = 12) -> dict:
     """All weights of one layer in canonical layout (host numpy arrays).
 
     gains: number of down-gain tables to draw (0, 1 or 2) as "down_gain", "down_gain2".
-    routed_format: "q2" (2-bit blocks) or "mx4" (MXFP4 blocks, same streams)."""
+    routed_format: "q2" (2-bit blocks), "mx4" (MXFP4 blocks, same streams) or "vq"
+    (vq_bits-bit indices into one E4M3 codebook, with row gains)."""
     H, I, E, Ish = shape.hidden, shape.inter, shape.n_experts, shape.shared_inter
     layer = {"router_w": normal_f32(E * H, seed, S_ROUTER, 0.02).reshape(E, H), "router_bias": None}
     if routed_format == "q2":
@@ -234,6 +274,16 @@ def make_layer(shape: Shape, seed: int, zipf: bool = False, zipf_beta_value: flo
         layer["up"] = mx4_matrix(E * I, H, seed, S_UP).reshape(E, I, H // 32, MX4_BLOCK_BYTES)
         layer["down"] = mx4_matrix(E * H, I, seed, S_DOWN).reshape(E, H, I // 32, MX4_BLOCK_BYTES)
         layer["routed_format"] = "mx4"
+    elif routed_format == "vq":
+        assert vq_bits in (12, 13)
+        layer["routed_format"] = "vq"
+        layer["vq_bits"] = vq_bits
+        layer["codebook"] = e4m3_codebook(1 << vq_bits, seed)
+        for name, rows, k, s_idx, s_plane, s_gain in (("gate", I, H, S_GATE, S_GATE_PLANE, S_GATE_ROWGAIN),
+                                                      ("up", I, H, S_UP, S_UP_PLANE, S_UP_ROWGAIN),
+                                                      ("down", H, I, S_DOWN, S_DOWN_PLANE, S_DOWN_ROWGAIN)):
+            layer[name], layer[name + "_plane"], layer[name + "_rowgain"] = vq_matrix(
+                E, rows, k, vq_bits, seed, s_idx, s_plane, s_gain)
     else:
         raise ValueError(routed_format)
     if Ish > 0:

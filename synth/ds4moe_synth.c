@@ -179,6 +179,47 @@ void synth_fill_mx4(uint8_t *out, int64_t nblocks, uint64_t seed, uint64_t strea
     }
 }
 
+/* Uniform random bytes: byte i is byte i % 8 of draw i / 8 of the stream. */
+void synth_fill_bytes(uint8_t *out, int64_t n, uint64_t seed, uint64_t stream)
+{
+    uint64_t key = stream_key(seed, stream);
+#pragma omp parallel for schedule(static)
+    for (int64_t w = 0; w < (n + 7) / 8; w++) {
+        uint64_t r = draw(key, (uint64_t)w);
+        for (int b = 0; b < 8 && 8 * w + b < n; b++)
+            out[8 * w + b] = (uint8_t)(r >> (8 * b));
+    }
+}
+
+/*
+ * VQ codebook entries as FP8 E4M3 bytes: random sign and mantissa, exponent
+ * field uniform in 5..9 (magnitudes 2^-2 .. 2^2 * 1.875), never NaN.
+ * Byte i uses draw i of the stream.
+ */
+void synth_fill_e4m3_codebook(uint8_t *out, int64_t n, uint64_t seed, uint64_t stream)
+{
+    uint64_t key = stream_key(seed, stream);
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < n; i++) {
+        uint64_t r = draw(key, (uint64_t)i);
+        const unsigned sign = (unsigned)(r & 1), man = (unsigned)((r >> 1) & 7);
+        const unsigned ex = 5u + (unsigned)(((r >> 32) * 5u) >> 32);
+        out[i] = (uint8_t)(sign << 7 | ex << 3 | man);
+    }
+}
+
+/* Row gains: binary16 of |N(0, sigma)|; row i uses draws 2i and 2i+1 of the stream. */
+void synth_fill_f16_abs_normal(uint16_t *out, int64_t n, uint64_t seed, uint64_t stream, double sigma)
+{
+    uint64_t key = stream_key(seed, stream);
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < n; i++) {
+        double z0, z1;
+        normal_pair(draw(key, 2 * (uint64_t)i), draw(key, 2 * (uint64_t)i + 1), &z0, &z1);
+        out[i] = to_f16((float)(fabs(z0) * sigma));
+    }
+}
+
 /*
  * 8-bit blocks: codes uniform in [-127, 127], d = |N(0, sigma)|.
  * Block b uses draws 18*b .. 18*b+17.

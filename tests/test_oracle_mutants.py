@@ -68,6 +68,19 @@ MUTANTS = {
     "x_not_quantised": [("quantise_act(act, xt, H, a);", "quantise_act(ACT_EXACT, xt, H, a);")],
     "h_not_quantised": [("quantise_act(act, h, I, hq);", "quantise_act(ACT_EXACT, h, I, hq);")],
     "h_quantised_in_double": [("        f[i] = (float)v[i];", "        f[i] = (float)(v[i] * (1.0 + 1e-7));")],
+    "vq_index_msb_first": [("v |= ((stream[bit / 8] >> (bit % 8)) & 1) << i;",
+                            "v |= ((stream[bit / 8] >> (7 - bit % 8)) & 1) << i;")],
+    "vq_plane_ignored": [("v |= ((plane[k / 8] >> (k % 8)) & 1) << 12;", "v |= 0;")],
+    "vq_plane_bit_low": [("v |= ((plane[k / 8] >> (k % 8)) & 1) << 12;", "v ^= ((plane[k / 8] >> (k % 8)) & 1);")],
+    "vq_row_gain_ignored": [("const double g = oracle_f16(gains[r]);", "const double g = 1.0;")],
+    "e4m3_exponent_bias": [("ldexp(8.0 + man, ex - 10)", "ldexp(8.0 + man, ex - 11)")],
+    "e4m3_subnormal_scale": [("ldexp((double)man, -9)", "ldexp((double)man, -10)")],
+    "vq_codeword_reversed": [("w[8 * j + i] = g * oracle_e4m3(codebook[8 * n + i]);",
+                              "w[8 * j + i] = g * oracle_e4m3(codebook[8 * n + 7 - i]);")],
+    "vq_groups_reversed_in_row": [("oracle_vq_index(stream, plane, r * (k / 8) + j)",
+                                   "oracle_vq_index(stream, plane, r * (k / 8) + (k / 8 - 1 - j))")],
+    "vq_expert_stream_offset_dropped": [("m->stream + e * (n * 12 / 8)", "m->stream + 0 * (n * 12 / 8)")],
+    "vq_expert_gains_offset_dropped": [("m->gains + e * rows", "m->gains")],
     "shared_dropped": [("acc[j] += ye[j];\n        }", "acc[j] += 0.0 * ye[j];\n        }")],
     "shared_weighted": [("acc[j] += ye[j];\n        }", "acc[j] += weights[(int64_t)t * K] * ye[j];\n        }")],
     "down_uses_gate_activation": [("ye[j] = dot(w, h, I);", "ye[j] = dot(w, xt, I);")],
@@ -85,6 +98,8 @@ def _pin_functions(tiny):
             out += [(f"{name}[{c}]", (lambda c=c, fn=fn: fn(c))) for c in pins.Q2_CLOSED]
         elif name in ("test_q8_golden_blocks",):
             out += [(f"{name}[{c}]", (lambda c=c, fn=fn: fn(c))) for c in pins.Q8_CLOSED]
+        elif name == "test_vq_layer_matches_dense_numpy":
+            out += [(f"{name}[{b}]", (lambda b=b, fn=fn: fn(b))) for b in (12, 13)]
         elif fn.__code__.co_argcount == 1:
             out.append((name, (lambda fn=fn: fn(tiny))))
         else:

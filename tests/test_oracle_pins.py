@@ -710,3 +710,127 @@ def test_mx4_exact_activations_match_dense_numpy():
     e8 = np.linalg.norm(y8 - y) / np.linalg.norm(y)
     e4 = np.linalg.norm(y4 - y) / np.linalg.norm(y)
     assert 0 < e8 < 3e-2 and e8 < e4 < 0.3, (e8, e4)
+
+
+# ---- VQ routed experts -------------------------------------------------------
+# "YoungAi - DeepSeek V4.1 Flash on one DGX Spark", section 4.1: every 8 weights
+# of a row are one 12- or 13-bit index into a per-layer E4M3 codebook, times one
+# binary16 gain per row; 13-bit layers keep a 12-bit stream plus a bit plane.
+
+def _pack12(indices):
+    """Index k at bits 12k .. 12k+11, least significant bit first."""
+    bits = np.zeros(len(indices) * 12, np.uint8)
+    for k, v in enumerate(indices):
+        for i in range(12):
+            bits[12 * k + i] = (v >> i) & 1
+    return np.packbits(bits, bitorder="little")
+
+
+def _plane(indices):
+    return np.packbits(np.array([(v >> 12) & 1 for v in indices], np.uint8), bitorder="little")
+
+
+def _e4m3_torch(b):
+    import torch
+    return torch.from_numpy(np.asarray(b, np.uint8)).view(torch.float8_e4m3fn).float().numpy().astype(np.float64)
+
+
+def test_e4m3_matches_torch_for_every_byte():
+    want = _e4m3_torch(np.arange(256))
+    got = np.array([oracle.e4m3(b) for b in range(256)])
+    nan = np.isnan(want)
+    assert list(np.nonzero(nan)[0]) == [0x7F, 0xFF] and np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], want[~nan])
+    assert oracle.e4m3(0x7E) == 448.0 and oracle.e4m3(0x01) == 2.0 ** -9 and oracle.e4m3(0x38) == 1.0
+
+
+def test_vq_index_stream_and_bit_plane():
+    rng = np.random.default_rng(8)
+    idx13 = rng.integers(0, 8192, 600)
+    stream, plane = _pack12(idx13 & 4095), _plane(idx13)
+    assert stream.size == 900  # 256 indices fill 384 bytes
+    for k in (0, 1, 2, 255, 256, 257, 511, 599):
+        assert oracle.vq_index(stream, None, k) == idx13[k] & 4095
+        assert oracle.vq_index(stream, plane, k) == idx13[k]
+    # index 256 starts at byte 384, bit 0
+    one = _pack12([0] * 256 + [1])
+    assert one[384] == 1 and oracle.vq_index(one, None, 256) == 1
+
+
+def test_vq_row_is_gain_times_codewords():
+    cb = np.zeros((4096, 8), np.uint8)
+    cb[5] = [0x38, 0x40, 0x30, 0xB8, 0x00, 0x01, 0x7E, 0x44]  # 1, 2, 0.5, -1, 0, 2^-9, 448, 3
+    cb[4095] = 0x3C  # 1.5
+    idx = [5, 4095, 5, 0]
+    gains = np.array([f16_bits(0.75), f16_bits(-2.0)], np.uint16)
+    stream = _pack12([0] * 4 + idx)  # row 0: indices 0..3, row 1: the ones above
+    w = oracle.dequant_vq_row(cb, stream, None, gains, 1, 32)
+    c5 = [1, 2, 0.5, -1, 0, 2.0 ** -9, 448, 3]
+    want = -2.0 * np.array(c5 + [1.5] * 8 + c5 + [0.0] * 8)
+    assert np.array_equal(w, want)
+
+
+def _vq_one_expert(H=256, I=256):
+    """E=K=1 VQ layer: gate row i = a_i (codeword of ones times gain a_i), up
+    row i = b_i, down row j = c_j * (+1 on the first I/2 columns, -1 after)."""
+    cb = np.zeros((4096, 8), np.uint8)
+    cb[1] = 0x38  # all 1.0
+    cb[2] = 0xB8  # all -1.0
+    a = np.array([2.0 ** -9 * (1 + i % 5) for i in range(I)])
+    b = np.array([2.0 ** -8 * (1 + i % 3) for i in range(I)])
+    c = np.array([2.0 ** -6 * (1 + j % 7) for j in range(H)])
+    gate = _pack12([1] * (I * H // 8))
+    down_idx = [1 if 8 * j < I // 2 else 2 for _ in range(H) for j in range(I // 8)]
+    layer = {"routed_format": "vq", "codebook": cb,
+             "gate": gate[None], "gate_plane": None, "gate_rowgain": np.array([[f16_bits(v) for v in a]], np.uint16),
+             "up": gate[None], "up_plane": None, "up_rowgain": np.array([[f16_bits(v) for v in b]], np.uint16),
+             "down": _pack12(down_idx)[None], "down_plane": None,
+             "down_rowgain": np.array([[f16_bits(v) for v in c]], np.uint16),
+             "sh_gate": None, "sh_up": None, "sh_down": None}
+    return layer, a, b, c
+
+
+def test_vq_expert_closed_form():
+    H, I = 256, 256
+    layer, a, b, c = _vq_one_expert(H, I)
+    x = np.where(np.arange(H) % 3 == 0, 1.0, -0.5).astype(np.float32)
+    xs = float(x.astype(np.float64).sum())
+    g, u = a * xs, b * xs
+    h = g / (1 + np.exp(-g)) * u
+    want = c * (h[:I // 2].sum() - h[I // 2:].sum())
+    shape = synth.Shape(H, I, 1, 1, 0)
+    y = oracle.forward_routed(shape, layer, bf16_bits(x[None, :]), np.zeros((1, 1), np.int32), np.ones((1, 1)))
+    assert np.allclose(y[0], want, rtol=1e-12, atol=0)
+    assert np.allclose(oracle.expert_vq(shape, layer, 0, x), want, rtol=1e-12, atol=0)
+
+
+@pytest.mark.parametrize("bits", [12, 13])
+def test_vq_layer_matches_dense_numpy(bits):
+    shape = synth.Shape(512, 256, 3, 2, 0)
+    layer = synth.make_layer(shape, 91, routed_format="vq", vq_bits=bits)
+    layer["sh_gate"] = layer["sh_up"] = layer["sh_down"] = None
+    cbv = _e4m3_torch(layer["codebook"].reshape(-1)).reshape(-1, 8)
+
+    def dense(name, rows, k):
+        out = []
+        for e in range(shape.n_experts):
+            bits_ = np.unpackbits(layer[name][e], bitorder="little").reshape(-1, 12).astype(np.int64)
+            idx = (bits_ << np.arange(12)).sum(axis=1)
+            if bits == 13:
+                idx |= np.unpackbits(layer[name + "_plane"][e], bitorder="little").astype(np.int64) << 12
+            g = layer[name + "_rowgain"][e].view(np.float16).astype(np.float64)
+            out.append(cbv[idx].reshape(rows, k) * g[:, None])
+        return out
+    Wg, Wu, Wd = dense("gate", 256, 512), dense("up", 256, 512), dense("down", 512, 256)
+    x = synth.normal_bf16(2 * 512, 92, synth.S_X).reshape(2, 512)
+    xf = synth.bf16_bits_to_f32(x).astype(np.float64)
+    idx = np.array([[2, 0], [1, 2]], np.int32)
+    w = np.array([[0.25, 0.75], [0.5, 0.5]])
+    y = oracle.forward_routed(shape, layer, x, idx, w)
+    for t in range(2):
+        want = np.zeros(512)
+        for k in range(2):
+            e = idx[t, k]
+            gg, uu = Wg[e] @ xf[t], Wu[e] @ xf[t]
+            want += w[t, k] * (Wd[e] @ (gg / (1 + np.exp(-gg)) * uu))
+        assert np.allclose(y[t], want, rtol=1e-12, atol=1e-12 * np.abs(want).max())

@@ -106,3 +106,18 @@ def test_gain_and_mx4_distributions():
     assert counts.min() > 0.9 * nib.size / 16 and counts.max() < 1.1 * nib.size / 16
     # a prefix of the blocks does not depend on how many are drawn
     assert np.array_equal(synth.mx4_matrix(8, 512, 5, synth.S_GATE), m[:8])
+
+
+def test_vq_generators():
+    cb = synth.e4m3_codebook(4096, 3)
+    ex = (cb >> 3) & 15
+    assert cb.shape == (4096, 8) and ex.min() == 5 and ex.max() == 9  # magnitudes 2^-2 .. 2^2 * 1.875, no NaN
+    assert abs((cb >> 7).mean() - 0.5) < 0.02
+    layer = synth.make_layer(synth.Shape(512, 256, 2, 2, 0), 4, routed_format="vq", vq_bits=13)
+    assert layer["gate"].shape == (2, 256 * 64 * 3 // 2) and layer["gate_plane"].shape == (2, 256 * 64 // 8)
+    assert layer["down"].shape == (2, 512 * 32 * 3 // 2) and layer["down_rowgain"].shape == (2, 512)
+    g = layer["up_rowgain"].view(np.float16).astype(np.float64)
+    assert (g >= 0).all() and abs(g.mean() - synth.VQ_ROWGAIN_SIGMA * np.sqrt(2 / np.pi)) < 0.01
+    again = synth.make_layer(synth.Shape(512, 256, 2, 2, 0), 4, routed_format="vq", vq_bits=13)
+    assert all(np.array_equal(layer[k], again[k]) for k in ("codebook", "gate", "gate_plane", "down_rowgain"))
+    assert synth.make_layer(synth.Shape(512, 256, 2, 2, 0), 4, routed_format="vq")["gate_plane"] is None
