@@ -1148,7 +1148,9 @@ int ds4moe_get_stats(ds4moe_t *h, ds4moe_stats *out) {
         return rc;
     *out = h->stats;
     if (h->stats.tokens > 0) {
-        const bool dec = h->stats.path == DS4MOE_PATH_DECODE;
+        // the fused decode kernel keeps its own grouping; every other path (and every
+        // MXFP4 layer) the dispatch kernels'
+        const bool dec = h->stats.path == DS4MOE_PATH_DECODE && !h->L.mx4;
         int32_t n = 0;
         cudaMemcpy(&n, dec ? h->D.nuniq : h->S.nuniq, sizeof(int32_t), cudaMemcpyDeviceToHost);
         out->n_unique = n;

@@ -35,7 +35,9 @@ def test_forward_matches_oracle(tiny, T):
     x = tokens(shape, T, 1100 + T)
     xd = x_to_dev(x)
     y = moe.forward(xd).cpu().numpy()
+    s = moe.stats()  # of the forward call (route() below replaces them)
     idx, w, gap, _ = moe.route(xd)
+    assert s.tokens == T and s.n_unique == len(np.unique(idx.cpu().numpy()))
     y_ref, r = oracle.forward(shape, layer, x, act="q8")
     near = check_routing(idx.cpu().numpy(), w.cpu().numpy(), gap.cpu().numpy(), r, shape.top_k)
     if near.any():
