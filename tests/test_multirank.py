@@ -70,3 +70,34 @@ def test_reference_arm_runs_on_rank_zero_only():
     with redirect_stdout(buf):
         bench.run_reference(Args(), world=2, rank=1)
     assert buf.getvalue() == ""
+
+
+@pytest.mark.parametrize("fmt,gains", [("q2", 0), ("mx4", 2)])
+def test_reference_arm_prints_the_contract_line(fmt, gains):
+    """Rank 0 of the reference arm (the oracle on the host's cores) prints one
+    JSON line with the keys the benchmark contract names."""
+    import json
+
+    import bench
+
+    class Args:
+        workload = "tiny"
+        steps = 2
+        warmup = 1
+        gpus = 1
+        routed_format = fmt
+
+    Args.gains = gains
+    buf = io.StringIO()
+    with redirect_stdout(buf):
+        bench.run_reference(Args(), world=1, rank=0)
+    lines = buf.getvalue().strip().splitlines()
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["value"] > 0 and d["steps"] == 2 and d["warmup"] == 1
+    assert d["unit"] == bench.UNIT and d["metric"] == bench.METRIC and d["higher_is_better"] is True
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    assert d["cpu_baseline"]["value"] == d["value"] and d["e2e"]["value"] == d["value"]
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
+    assert d["config"]["workload"] == "tiny" and ("MXFP4" in d["config"]["weights"]) == (fmt == "mx4")
+    assert d["config"].get("down_gain_tables", 0) == gains
