@@ -115,9 +115,10 @@ TRAFFIC = {
 }
 
 
-def kernel_traffic(name, workload, gains=0):
+def kernel_traffic(name, workload, gains=0, fmt="q2"):
+    """The recorded DRAM bytes per launch, for the plain 2-bit layer the capture ran on."""
     import hashlib
-    rec = TRAFFIC.get((name, workload)) if gains == 0 else None
+    rec = TRAFFIC.get((name, workload)) if gains == 0 and fmt == "q2" else None
     if rec is None:
         return None
     path = os.path.join(ROOT, "quantized_moe_expert_gb300", "csrc", rec[1])
@@ -548,14 +549,14 @@ def main():
         if t_tc > t_hbm:
             ach = dom_flops / sec / 1e12
             roofline = {"bound": "tensor", "kernel": dom, "achieved": ach, "peak": tf_peak, "unit": "TFLOP/s",
-                        "frac": ach / tf_peak, "traffic": kernel_traffic(dom, args.workload, args.gains if args.routed_format == "q2" else -1),
+                        "frac": ach / tf_peak, "traffic": kernel_traffic(dom, args.workload, args.gains, args.routed_format),
                         "peak_source": peak_src + " bf16 burst",
                         "flops_per_launch": dom_flops, "bytes_per_launch": dom_bytes,
                         "hbm_frac": dom_bytes / sec / 1e9 / hbm_peak, "avg_launch_us": 1000 * dom_avg_ms}
         else:
             ach = dom_bytes / sec / 1e9
             roofline = {"bound": "hbm", "kernel": dom, "achieved": ach, "peak": hbm_peak, "unit": "GB/s",
-                        "frac": ach / hbm_peak, "traffic": kernel_traffic(dom, args.workload, args.gains if args.routed_format == "q2" else -1), "peak_source": peak_src,
+                        "frac": ach / hbm_peak, "traffic": kernel_traffic(dom, args.workload, args.gains, args.routed_format), "peak_source": peak_src,
                         "bytes_per_launch": dom_bytes, "avg_launch_us": 1000 * dom_avg_ms}
             if dom_flops:
                 roofline["flops_per_launch"] = dom_flops
