@@ -365,11 +365,19 @@ typedef struct {
     int32_t e;
 } scored;
 
+/* Descending selection score, equal scores by ascending expert index. A NaN
+ * score is not a number to rank: it sorts after every number (including -inf),
+ * NaNs among themselves by index, so a NaN expert is chosen only when fewer
+ * than K experts have numeric scores. */
 static int by_score_then_index(const void *pa, const void *pb)
 {
     const scored *a = (const scored *)pa, *b = (const scored *)pb;
-    if (a->sel > b->sel) return -1;
-    if (a->sel < b->sel) return 1;
+    const int a_nan = a->sel != a->sel, b_nan = b->sel != b->sel;
+    if (a_nan != b_nan) return a_nan - b_nan;
+    if (!a_nan) {
+        if (a->sel > b->sel) return -1;
+        if (a->sel < b->sel) return 1;
+    }
     return (a->e > b->e) - (a->e < b->e);
 }
 
@@ -456,59 +464,85 @@ int oracle_route(const oracle_shape *s, const float *router_w, const float *rout
 
 /* ---- experts ------------------------------------------------------------ */
 
-/* One routed expert on one token: ye[H] = Wd (silu(Wg x) * (Wu x)). */
-void oracle_expert_q2(const oracle_shape *s, const uint8_t *gate_e, const uint8_t *up_e,
-                      const uint8_t *down_e, const double *xt, double *ye)
+/* One routed expert on one token: ye[H] = Wd (silu(Wg x) * (Wu x)).
+ * rows_threads > 1 spreads the rows of each product over that many threads;
+ * every row is still one thread's sequential dot product, so the result does
+ * not depend on it. */
+static void expert_q2_rows(const oracle_shape *s, const uint8_t *gate_e, const uint8_t *up_e,
+                           const uint8_t *down_e, const double *xt, double *ye, int rows_threads)
 {
     const int H = s->hidden, I = s->inter;
     const int64_t gate_row = (int64_t)(H / 256) * Q2_BYTES, down_row = (int64_t)(I / 256) * Q2_BYTES;
-    double *w = (double *)malloc(sizeof(double) * (H > I ? H : I));
     double *h = (double *)malloc(sizeof(double) * I);
-    for (int i = 0; i < I; i++) {
-        oracle_dequant_q2_row(gate_e + i * gate_row, H, w);
-        double g = dot(w, xt, H);
-        oracle_dequant_q2_row(up_e + i * gate_row, H, w);
-        double u = dot(w, xt, H);
-        h[i] = oracle_silu(g) * u;
+#pragma omp parallel num_threads(rows_threads > 1 ? rows_threads : 1) if (rows_threads > 1)
+    {
+        double *w = (double *)malloc(sizeof(double) * (H > I ? H : I));
+#pragma omp for schedule(static)
+        for (int i = 0; i < I; i++) {
+            oracle_dequant_q2_row(gate_e + i * gate_row, H, w);
+            double g = dot(w, xt, H);
+            oracle_dequant_q2_row(up_e + i * gate_row, H, w);
+            double u = dot(w, xt, H);
+            h[i] = oracle_silu(g) * u;
+        }
+#pragma omp for schedule(static)
+        for (int j = 0; j < H; j++) {
+            oracle_dequant_q2_row(down_e + j * down_row, I, w);
+            ye[j] = dot(w, h, I);
+        }
+        free(w);
     }
-    for (int j = 0; j < H; j++) {
-        oracle_dequant_q2_row(down_e + j * down_row, I, w);
-        ye[j] = dot(w, h, I);
-    }
-    free(w);
     free(h);
+}
+
+void oracle_expert_q2(const oracle_shape *s, const uint8_t *gate_e, const uint8_t *up_e,
+                      const uint8_t *down_e, const double *xt, double *ye)
+{
+    expert_q2_rows(s, gate_e, up_e, down_e, xt, ye, 1);
 }
 
 /* The shared expert on one token: ysh[H]. */
 /* One MXFP4 routed expert: ye = Wd (silu(Wg a) * (Wu a)) with a the quantised
  * activations of x (act: ACT_Q8 decode, ACT_MX4 prefill, ACT_EXACT none) and
  * the down product on the quantised SwiGLU output. */
-void oracle_expert_mx4(const oracle_shape *s, int32_t act, const uint8_t *gate_e, const uint8_t *up_e,
-                       const uint8_t *down_e, const double *xt, double *ye)
+static void expert_mx4_rows(const oracle_shape *s, int32_t act, const uint8_t *gate_e, const uint8_t *up_e,
+                            const uint8_t *down_e, const double *xt, double *ye, int rows_threads)
 {
     const int H = s->hidden, I = s->inter;
     const int64_t gate_row = (int64_t)(H / 32) * MX4_BYTES, down_row = (int64_t)(I / 32) * MX4_BYTES;
-    double *w = (double *)malloc(sizeof(double) * (H > I ? H : I));
     double *a = (double *)malloc(sizeof(double) * H);
     double *h = (double *)malloc(sizeof(double) * I);
     double *hq = (double *)malloc(sizeof(double) * I);
     quantise_act(act, xt, H, a);
-    for (int i = 0; i < I; i++) {
-        oracle_dequant_mx4_row(gate_e + i * gate_row, H, w);
-        double g = dot(w, a, H);
-        oracle_dequant_mx4_row(up_e + i * gate_row, H, w);
-        double u = dot(w, a, H);
-        h[i] = oracle_silu(g) * u;
+#pragma omp parallel num_threads(rows_threads > 1 ? rows_threads : 1) if (rows_threads > 1)
+    {
+        double *w = (double *)malloc(sizeof(double) * (H > I ? H : I));
+#pragma omp for schedule(static)
+        for (int i = 0; i < I; i++) {
+            oracle_dequant_mx4_row(gate_e + i * gate_row, H, w);
+            double g = dot(w, a, H);
+            oracle_dequant_mx4_row(up_e + i * gate_row, H, w);
+            double u = dot(w, a, H);
+            h[i] = oracle_silu(g) * u;
+        }
+#pragma omp single
+        quantise_act(act, h, I, hq);
+#pragma omp for schedule(static)
+        for (int j = 0; j < H; j++) {
+            oracle_dequant_mx4_row(down_e + j * down_row, I, w);
+            ye[j] = dot(w, hq, I);
+        }
+        free(w);
     }
-    quantise_act(act, h, I, hq);
-    for (int j = 0; j < H; j++) {
-        oracle_dequant_mx4_row(down_e + j * down_row, I, w);
-        ye[j] = dot(w, hq, I);
-    }
-    free(w);
     free(a);
     free(h);
     free(hq);
+}
+
+void oracle_expert_mx4(const oracle_shape *s, int32_t act, const uint8_t *gate_e, const uint8_t *up_e,
+                       const uint8_t *down_e, const double *xt, double *ye)
+{
+    expert_mx4_rows(s, act, gate_e, up_e, down_e, xt, ye, 1);
 }
 
 /* One VQ matrix of a layer: the expert's index stream, bit plane (13-bit
@@ -528,47 +562,71 @@ static void vq_row(const uint8_t *codebook, const oracle_vq_mat *m, int e, int64
 }
 
 /* One VQ routed expert e: ye = Wd (silu(Wg x) * (Wu x)). */
-void oracle_expert_vq(const oracle_shape *s, const uint8_t *codebook, const oracle_vq_mat *gate,
-                      const oracle_vq_mat *up, const oracle_vq_mat *down, int32_t e, const double *xt, double *ye)
+static void expert_vq_rows(const oracle_shape *s, const uint8_t *codebook, const oracle_vq_mat *gate,
+                           const oracle_vq_mat *up, const oracle_vq_mat *down, int32_t e, const double *xt,
+                           double *ye, int rows_threads)
 {
     const int H = s->hidden, I = s->inter;
-    double *w = (double *)malloc(sizeof(double) * (H > I ? H : I));
     double *h = (double *)malloc(sizeof(double) * I);
-    for (int i = 0; i < I; i++) {
-        vq_row(codebook, gate, e, I, i, H, w);
-        double g = dot(w, xt, H);
-        vq_row(codebook, up, e, I, i, H, w);
-        double u = dot(w, xt, H);
-        h[i] = oracle_silu(g) * u;
+#pragma omp parallel num_threads(rows_threads > 1 ? rows_threads : 1) if (rows_threads > 1)
+    {
+        double *w = (double *)malloc(sizeof(double) * (H > I ? H : I));
+#pragma omp for schedule(static)
+        for (int i = 0; i < I; i++) {
+            vq_row(codebook, gate, e, I, i, H, w);
+            double g = dot(w, xt, H);
+            vq_row(codebook, up, e, I, i, H, w);
+            double u = dot(w, xt, H);
+            h[i] = oracle_silu(g) * u;
+        }
+#pragma omp for schedule(static)
+        for (int j = 0; j < H; j++) {
+            vq_row(codebook, down, e, H, j, I, w);
+            ye[j] = dot(w, h, I);
+        }
+        free(w);
     }
-    for (int j = 0; j < H; j++) {
-        vq_row(codebook, down, e, H, j, I, w);
-        ye[j] = dot(w, h, I);
-    }
-    free(w);
     free(h);
 }
 
-void oracle_shared_q8(const oracle_shape *s, const uint8_t *sh_gate, const uint8_t *sh_up,
-                      const uint8_t *sh_down, const double *xt, double *ysh)
+void oracle_expert_vq(const oracle_shape *s, const uint8_t *codebook, const oracle_vq_mat *gate,
+                      const oracle_vq_mat *up, const oracle_vq_mat *down, int32_t e, const double *xt, double *ye)
+{
+    expert_vq_rows(s, codebook, gate, up, down, e, xt, ye, 1);
+}
+
+static void shared_q8_rows(const oracle_shape *s, const uint8_t *sh_gate, const uint8_t *sh_up,
+                           const uint8_t *sh_down, const double *xt, double *ysh, int rows_threads)
 {
     const int H = s->hidden, I = s->shared_inter;
     const int64_t gate_row = (int64_t)(H / 32) * Q8_BYTES, down_row = (int64_t)(I / 32) * Q8_BYTES;
-    double *w = (double *)malloc(sizeof(double) * (H > I ? H : I));
     double *h = (double *)malloc(sizeof(double) * I);
-    for (int i = 0; i < I; i++) {
-        oracle_dequant_q8_row(sh_gate + i * gate_row, H, w);
-        double g = dot(w, xt, H);
-        oracle_dequant_q8_row(sh_up + i * gate_row, H, w);
-        double u = dot(w, xt, H);
-        h[i] = oracle_silu(g) * u;
+#pragma omp parallel num_threads(rows_threads > 1 ? rows_threads : 1) if (rows_threads > 1)
+    {
+        double *w = (double *)malloc(sizeof(double) * (H > I ? H : I));
+#pragma omp for schedule(static)
+        for (int i = 0; i < I; i++) {
+            oracle_dequant_q8_row(sh_gate + i * gate_row, H, w);
+            double g = dot(w, xt, H);
+            oracle_dequant_q8_row(sh_up + i * gate_row, H, w);
+            double u = dot(w, xt, H);
+            h[i] = oracle_silu(g) * u;
+        }
+#pragma omp for schedule(static)
+        for (int j = 0; j < H; j++) {
+            oracle_dequant_q8_row(sh_down + j * down_row, I, w);
+            ysh[j] = dot(w, h, I);
+        }
+        free(w);
     }
-    for (int j = 0; j < H; j++) {
-        oracle_dequant_q8_row(sh_down + j * down_row, I, w);
-        ysh[j] = dot(w, h, I);
-    }
-    free(w);
     free(h);
+}
+
+/* The shared expert on one token: ysh[H]. */
+void oracle_shared_q8(const oracle_shape *s, const uint8_t *sh_gate, const uint8_t *sh_up,
+                      const uint8_t *sh_down, const double *xt, double *ysh)
+{
+    shared_q8_rows(s, sh_gate, sh_up, sh_down, xt, ysh, 1);
 }
 
 /*
@@ -577,6 +635,9 @@ void oracle_shared_q8(const oracle_shape *s, const uint8_t *sh_gate, const uint8
  * ysh is skipped when shared_inter == 0 or the shared pointers are NULL.
  * Tokens are independent and each row is computed by one thread in a fixed
  * order, so the result does not depend on nthreads (<= 0: library default).
+ * With at least as many tokens as threads the threads take whole tokens;
+ * with fewer, the tokens run one after another and the threads share the
+ * rows of each product.
  */
 static int forward_routed_any(const oracle_shape *s, int mx4, int32_t act, const uint8_t *codebook,
                               const oracle_vq_mat *vq, const uint8_t *gate, const uint8_t *up, const uint8_t *down, const uint8_t *sh_gate, const uint8_t *sh_up,
@@ -598,7 +659,8 @@ static int forward_routed_any(const oracle_shape *s, int mx4, int32_t act, const
     const int64_t expert_gate = mx4 ? (int64_t)I * (H / 32) * MX4_BYTES : (int64_t)I * (H / 256) * Q2_BYTES;
     const int64_t expert_down = mx4 ? (int64_t)H * (I / 32) * MX4_BYTES : (int64_t)H * (I / 256) * Q2_BYTES;
     const int nt = nthreads > 0 ? nthreads : omp_get_max_threads();
-#pragma omp parallel for schedule(dynamic, 1) num_threads(nt)
+    const int rows_threads = T < nt ? nt : 1; /* too few tokens to occupy the threads */
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nt) if (rows_threads == 1)
     for (int32_t t = 0; t < T; t++) {
         double *xt = (double *)malloc(sizeof(double) * H);
         double *ye = (double *)malloc(sizeof(double) * H);
@@ -608,12 +670,13 @@ static int forward_routed_any(const oracle_shape *s, int mx4, int32_t act, const
         for (int k = 0; k < K; k++) {
             int e = idx[(int64_t)t * K + k];
             if (vq)
-                oracle_expert_vq(s, codebook, &vq[0], &vq[1], &vq[2], e, xt, ye);
+                expert_vq_rows(s, codebook, &vq[0], &vq[1], &vq[2], e, xt, ye, rows_threads);
             else if (mx4)
-                oracle_expert_mx4(s, act, gate + e * expert_gate, up + e * expert_gate, down + e * expert_down, xt,
-                                  ye);
+                expert_mx4_rows(s, act, gate + e * expert_gate, up + e * expert_gate, down + e * expert_down, xt,
+                                ye, rows_threads);
             else
-                oracle_expert_q2(s, gate + e * expert_gate, up + e * expert_gate, down + e * expert_down, xt, ye);
+                expert_q2_rows(s, gate + e * expert_gate, up + e * expert_gate, down + e * expert_down, xt, ye,
+                               rows_threads);
             double wk = weights[(int64_t)t * K + k];
             for (int j0 = 0; j0 < H; j0 += 32) {
                 double s1[32], s2[32];
@@ -628,7 +691,7 @@ static int forward_routed_any(const oracle_shape *s, int mx4, int32_t act, const
             }
         }
         if (has_shared) {
-            oracle_shared_q8(s, sh_gate, sh_up, sh_down, xt, ye);
+            shared_q8_rows(s, sh_gate, sh_up, sh_down, xt, ye, rows_threads);
             for (int j = 0; j < H; j++)
                 acc[j] += ye[j];
         }

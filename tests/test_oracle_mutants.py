@@ -38,14 +38,17 @@ MUTANTS = {
     "router_transposed": [("L += xt[h] * (double)router_w[(int64_t)e * H + h];",
                            "L += xt[h] * (double)router_w[(int64_t)h * E + e];")],
     "ties_prefer_higher_index": [("return (a->e > b->e) - (a->e < b->e);", "return (a->e < b->e) - (a->e > b->e);")],
+    "nan_ranked_first": [("if (a_nan != b_nan) return a_nan - b_nan;", "if (a_nan != b_nan) return b_nan - a_nan;")],
     "ascending_selection": [("if (a->sel > b->sel) return -1;", "if (a->sel > b->sel) return 1;"),
                             ("if (a->sel < b->sel) return 1;", "if (a->sel < b->sel) return -1;")],
     "bias_in_weights": [("total += score[order[k].e];", "total += (double)order[k].sel;"),
                         ("weights[(int64_t)t * K + k] = total > 0.0 ? score[order[k].e] / total : 1.0 / K;",
                          "weights[(int64_t)t * K + k] = total > 0.0 ? (double)order[k].sel / total : 1.0 / K;")],
     "no_renormalisation": [("score[order[k].e] / total : 1.0 / K;", "score[order[k].e] : 1.0 / K;")],
-    "gate_up_exchanged": [("h[i] = oracle_silu(g) * u;\n    }\n    for (int j = 0; j < H; j++) {\n        oracle_dequant_q2_row",
-                           "h[i] = oracle_silu(u) * g;\n    }\n    for (int j = 0; j < H; j++) {\n        oracle_dequant_q2_row")],
+    "gate_up_exchanged": [("h[i] = oracle_silu(g) * u;\n        }\n#pragma omp for schedule(static)\n"
+                           "        for (int j = 0; j < H; j++) {\n            oracle_dequant_q2_row",
+                           "h[i] = oracle_silu(u) * g;\n        }\n#pragma omp for schedule(static)\n"
+                           "        for (int j = 0; j < H; j++) {\n            oracle_dequant_q2_row")],
     "routing_weight_dropped": [("acc[j0 + i] += wk * (s1[i] * s2[i] * ye[j0 + i]);",
                                 "acc[j0 + i] += (s1[i] * s2[i] * ye[j0 + i]);")],
     "gain_nibble_high_first": [("s[i] = 1.0 + X * oracle_e2m1((uint8_t)((blk[i / 2] >> (4 * (i % 2))) & 15));",

@@ -196,6 +196,32 @@ def test_topk_ties_prefer_lower_index():
     assert np.allclose(r["weights"][0], 0.25, rtol=0, atol=1e-15)
 
 
+def _policy_topk(sel32, K):
+    """Brute-force ranking under the selection policy: numbers by descending
+    score then ascending index, every NaN after them by ascending index."""
+    num = [e for e in range(sel32.size) if not np.isnan(sel32[e])]
+    nan = [e for e in range(sel32.size) if np.isnan(sel32[e])]
+    num.sort(key=lambda e: (-float(sel32[e]), e))
+    return (num + nan)[:K]
+
+
+def test_topk_nan_scores_rank_below_every_number():
+    rng = np.random.default_rng(11)
+    E, K = 24, 6
+    shape = synth.Shape(256, 256, E, K, 0)
+    for trial in range(300):
+        L = rng.integers(-3, 4, size=(1, E)).astype(np.float64) / 4.0  # many exact ties
+        L[0, rng.random(E) < rng.random()] = np.nan
+        if trial % 7 == 0:
+            L[0, rng.integers(E)] = -np.inf
+        r = oracle.select(shape, L, None)
+        assert list(r["idx"][0]) == _policy_topk(r["sel"][0], K), (trial, L)
+    # a token with every score NaN takes the K lowest indices with equal weights
+    r = oracle.select(shape, np.full((1, E), np.nan), None)
+    assert list(r["idx"][0]) == list(range(K))
+    assert np.all(r["weights"][0] == 1.0 / K) and np.isnan(r["gap"][0])
+
+
 def test_topk_degenerate_k_equals_e_and_single_expert():
     r = _route_logits([[0.5, -1.0, 3.0]], 3)
     assert list(r["idx"][0]) == [2, 0, 1]
@@ -355,7 +381,8 @@ def test_token_independence_and_thread_count(tiny):
     shape, layer, x = tiny
     y_all, _ = oracle.forward(shape, layer, x, nthreads=4)
     y_one, _ = oracle.forward(shape, layer, x, nthreads=1)
-    assert (y_all == y_one).all()
+    y_rows, _ = oracle.forward(shape, layer, x, nthreads=16)  # fewer tokens than threads: rows shared
+    assert (y_all == y_one).all() and (y_rows == y_one).all()
     for t in range(x.shape[0]):
         yt, _ = oracle.forward(shape, layer, x[t:t + 1])
         assert (yt[0] == y_all[t]).all()
