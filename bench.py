@@ -47,6 +47,8 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile-steps", type=int, default=20)
+    ap.add_argument("--headline-only", action="store_true",
+                    help="with the default decode_t1 workload, skip the other full-size workloads")
     ap.add_argument("--crossover", action="store_true",
                     help="time the decode and the prefill path on the decode layer for T = 1..64 and print "
                          "one JSON line of the per-T medians (not a bench line)")
@@ -304,7 +306,7 @@ def cpu_oracle_rate(name, layers, batches, budget_tokens=None, min_seconds=0.0):
             break
     if passes > 1:
         sample += f", {passes} passes"
-    return passes * len(flat) / dt, min(cores, len(flat)), sample, dt
+    return passes * len(flat) / dt, cores, sample, dt
 
 
 def dist_setup(args):
@@ -433,6 +435,197 @@ def run_crossover(args):
                       "clocks": clk.summary()}))
 
 
+# The full-size configurations besides the headline, measured in the same run
+# (same L2 flush between steps): workload -> (steps, warmup, profiled steps,
+# end-to-end steps, seconds of CPU baseline).
+SIDE_WORKLOADS = {
+    "decode_t8": (20, 3, 10, 10, 5.0),
+    "prefill_t1024": (8, 3, 4, 4, 5.0),
+    "prefill_t4096_zipf4": (4, 3, 2, 2, 5.0),
+}
+
+
+def peaks_table():
+    pk_path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    peaks = {}
+    if os.path.exists(pk_path):
+        with open(pk_path) as f:
+            peaks = json.load(f)
+    return peaks
+
+
+def measure(ctx, name, handles, layers, steps, warmup, profile_steps, e2e_steps, cpu_seconds):
+    """Time one workload on its handles: the step loop (device-resident inputs),
+    the per-kernel pass, the end-to-end pass through host memory and the CPU
+    baseline. Returns the fields of a bench line."""
+    import torch
+
+    import quantized_moe_expert_gb300 as ds4
+    import synth
+
+    args, world, rank, dev, stream, flush, gpu_id = (ctx[k] for k in ("args", "world", "rank", "dev", "stream",
+                                                                        "flush", "gpu_id"))
+    wl = synth.WORKLOADS[name]
+    shape = wl.shape
+    batches = workload_batches(name)
+    T = wl.tokens
+    xs = [torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).to(dev) for b in batches]
+    y = torch.empty((T, shape.hidden), dtype=torch.float32, device=dev)
+
+    def step(i):
+        x = xs[i % len(xs)]
+        for m in handles:
+            ds4.ds4moe_forward(m.handle, x, T, y)
+
+    # distinct experts per batch, from the library's own routing
+    uniq = []
+    for x in xs[:min(len(xs), 64)]:
+        uniq.append([len(torch.unique(m.route(x)[0])) for m in handles])
+    U_mean = float(np.mean(uniq))
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    for i in range(warmup):
+        flush.zero_()
+        step(i)
+    torch.cuda.synchronize()
+    launches_per_step = handles[0].stats().kernel_count * len(handles)
+
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(gpu_id) as clk:
+        for i in range(steps):
+            flush.zero_()
+            evs[i][0].record(stream)
+            step(warmup + i)
+            evs[i][1].record(stream)
+        torch.cuda.synchronize()
+    barrier()
+    step_ms = [a.elapsed_time(b) for a, b in evs]
+    total_ms = max_over_ranks(sum(step_ms), world, dev)
+    value = job_rate(world, T, steps, total_ms)
+    ms_per_step = total_ms / steps
+
+    # per-kernel device times, recorded by the library around each launch
+    for m in handles:
+        ds4.ds4moe_profile(m.handle, True)
+    for i in range(profile_steps):
+        flush.zero_()
+        step(i)
+    ktimes = {}
+    for m in handles:
+        for kname, (n, ms) in ds4.ds4moe_profile_read(m.handle).items():
+            a = ktimes.setdefault(kname, [0, 0.0])
+            a[0] += n
+            a[1] += ms
+        ds4.ds4moe_profile(m.handle, False)
+    dom = max(ktimes, key=lambda k: ktimes[k][1])
+    if launches_per_step == 1:
+        # the step is this one launch: its time is the timed region's own
+        dom_avg_ms = ms_per_step
+        time_source = "timed region (the step is one launch of this kernel)"
+    else:
+        dom_avg_ms = ktimes[dom][1] / ktimes[dom][0]
+        time_source = ("per-launch CUDA events in a pass of %d steps right after the timed region; the profiled "
+                       "kernels sum to %.4f ms per step against %.4f ms timed" % (
+                           profile_steps, sum(v[1] for v in ktimes.values()) / profile_steps, ms_per_step))
+    dom_bytes = kernel_bytes(dom, shape, T, U_mean, args.gains, args.routed_format)
+    peaks = peaks_table()
+    hbm_peak = peaks.get("hbm_gbs", 6800.0)
+    tf_peak = peaks.get("bf16_tflops", 1900.0)
+    peak_src = "measured" if "hbm_gbs" in peaks else "fallback"
+    roofline = None
+    dom_flops = kernel_flops(dom, shape, T)
+    if dom_bytes is not None:
+        sec = dom_avg_ms / 1000.0
+        t_hbm = dom_bytes / (hbm_peak * 1e9)
+        t_tc = dom_flops / (tf_peak * 1e12) if dom_flops else 0.0
+        traffic = kernel_traffic(dom, name, args.gains, args.routed_format)
+        if t_tc > t_hbm:
+            ach = dom_flops / sec / 1e12
+            roofline = {"bound": "tensor", "kernel": dom, "achieved": ach, "peak": tf_peak, "unit": "TFLOP/s",
+                        "frac": ach / tf_peak, "traffic": traffic, "peak_source": peak_src + " bf16 burst",
+                        "flops_per_launch": dom_flops, "bytes_per_launch": dom_bytes,
+                        "hbm_frac": dom_bytes / sec / 1e9 / hbm_peak, "avg_launch_us": 1000 * dom_avg_ms,
+                        "kernel_time_source": time_source}
+        else:
+            ach = dom_bytes / sec / 1e9
+            roofline = {"bound": "hbm", "kernel": dom, "achieved": ach, "peak": hbm_peak, "unit": "GB/s",
+                        "frac": ach / hbm_peak, "traffic": traffic, "peak_source": peak_src,
+                        "bytes_per_launch": dom_bytes, "avg_launch_us": 1000 * dom_avg_ms,
+                        "kernel_time_source": time_source}
+            if dom_flops:
+                roofline["flops_per_launch"] = dom_flops
+                roofline["tensor_frac"] = dom_flops / sec / 1e12 / tf_peak
+    lay_bytes = layer_bytes(shape, T, U_mean, args.gains, args.routed_format) * len(handles)
+    layer_gbs = lay_bytes / (ms_per_step / 1000.0) / 1e9
+    lay_flops = layer_flops(shape, T) * len(handles)
+    layer_tf = lay_flops / (ms_per_step / 1000) / 1e12
+
+    # end to end through host memory
+    xh = [torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).pin_memory() for b in batches]
+    yh = torch.empty((T, shape.hidden), dtype=torch.float32).pin_memory()
+    e2e_ms = []
+    for i in range(warmup + e2e_steps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for m in handles:
+            ds4.ds4moe_forward_host(m.handle, xh[i % len(xh)].data_ptr(), T, yh.data_ptr())
+        b.record(stream)
+        b.synchronize()
+        if i >= warmup:
+            e2e_ms.append(a.elapsed_time(b))
+    e2e_total = max_over_ranks(sum(e2e_ms), world, dev)
+    e2e = {"value": job_rate(world, T, e2e_steps, e2e_total), "unit": UNIT, "steps": e2e_steps,
+           "h2d_bytes_per_step": 2 * T * shape.hidden * len(handles),
+           "d2h_bytes_per_step": 4 * T * shape.hidden * len(handles)}
+    for m in handles:
+        if m.status() != 0:
+            raise RuntimeError("device error reported by the library")
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        # whole passes over a bounded sample until cpu_seconds of CPU work
+        rate, cores, sample, dt = cpu_oracle_rate(name, layers, batches, min_seconds=cpu_seconds)
+        cpu = {"value": rate, "unit": UNIT, "cores": cores, "host_cores": os.cpu_count(), "kind": "oracle",
+               "sample": sample, "seconds": dt}
+    l2_note = "flushed between steps: %d MiB device write outside the timed events" % (
+        flush.numel() // (1 << 20))
+    return {"value": value, "ms_per_step": ms_per_step, "steps": steps, "warmup": warmup,
+            "dtype": "f32" if T <= ds4.AUTO_DECODE_MAX_T else "bf16",
+            "config": workload_config(wl, name, l2_note, args.gains, args.routed_format),
+            "roofline": roofline,
+            "layer_roofline": {"bound": "tensor" if lay_flops / (tf_peak * 1e12) > lay_bytes / (hbm_peak * 1e9)
+                               else "hbm",
+                               "bytes_per_step": lay_bytes, "achieved_gbs": layer_gbs,
+                               "frac_hbm": layer_gbs / hbm_peak, "tflops": layer_tf, "frac_tensor": layer_tf / tf_peak,
+                               "unique_experts_mean": U_mean},
+            "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches_per_step * steps,
+            "clocks": clk.summary(),
+            "kernels_us": {k: round(1000 * v[1] / v[0], 2) for k, v in ktimes.items()}}
+
+
+def make_handles(layers, shape, dev, max_tokens, fmt, stream):
+    import torch
+
+    import quantized_moe_expert_gb300 as ds4
+    handles = []
+    for layer in layers:
+        w = {k: (None if v is None else torch.from_numpy(np.ascontiguousarray(v)).to(dev)) for k, v in layer.items()
+             if v is None or isinstance(v, np.ndarray)}
+        handles.append(ds4.MoELayer(shape, w, max_tokens=max_tokens, flags=ds4.FLAG_MXFP4 if fmt == "mx4" else 0))
+        del w
+    torch.cuda.empty_cache()
+    for m in handles:
+        m.set_stream(stream)
+    return handles
+
+
 def main():
     args = parse()
     world, rank, local = dist_setup(args)
@@ -446,168 +639,54 @@ def main():
 
     import torch
 
-    import quantized_moe_expert_gb300 as ds4
     import synth
 
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    wl, layers = workload_layers(args.workload, args.gains, args.routed_format)
-    shape = wl.shape
-    batches = workload_batches(args.workload)
-    T = wl.tokens
-    handles = []
-    for layer in layers:
-        w = {k: (None if v is None else torch.from_numpy(np.ascontiguousarray(v)).to(dev)) for k, v in layer.items()
-             if v is None or isinstance(v, np.ndarray)}
-        handles.append(ds4.MoELayer(shape, w, max_tokens=max(T, 8),
-                                    flags=ds4.FLAG_MXFP4 if args.routed_format == "mx4" else 0))
-        del w
-    torch.cuda.empty_cache()
     stream = torch.cuda.current_stream(dev)
-    for m in handles:
-        m.set_stream(stream)
-    xs = [torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).to(dev) for b in batches]
-    y = torch.empty((T, shape.hidden), dtype=torch.float32, device=dev)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
-    l2_note = f"flushed between steps: {2 * l2 // (1 << 20)} MiB device write outside the timed events"
-
-    def step(i):
-        x = xs[i % len(xs)]
-        for m in handles:
-            ds4.ds4moe_forward(m.handle, x, T, y)
-
-    # unique experts per batch, from the library's own routing
-    uniq = []
-    for x in xs[:min(len(xs), 64)]:
-        per_layer = []
-        for m in handles:
-            idx, _, _, _ = m.route(x)
-            per_layer.append(len(torch.unique(idx)))
-        uniq.append(per_layer)
-    U_mean = float(np.mean(uniq))
-
-    def barrier():
-        if world > 1:
-            import torch.distributed as dist
-            dist.barrier()
-
-    for i in range(args.warmup):
-        flush.zero_()
-        step(i)
-    torch.cuda.synchronize()
-    launches_per_step = handles[0].stats().kernel_count * len(handles)
-
     gpu_id = getattr(torch.cuda.get_device_properties(dev), "uuid", None)
     gpu_id = ("GPU-" + str(gpu_id)) if gpu_id is not None and not str(gpu_id).startswith("GPU-") else gpu_id
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    barrier()
-    torch.cuda.synchronize()
-    with ClockSampler(gpu_id) as clk:
-        for i in range(args.steps):
-            flush.zero_()
-            evs[i][0].record(stream)
-            step(args.warmup + i)
-            evs[i][1].record(stream)
-        torch.cuda.synchronize()
-    barrier()
-    step_ms = [a.elapsed_time(b) for a, b in evs]
-    total_ms = max_over_ranks(sum(step_ms), world, dev)
-    value = job_rate(world, T, args.steps, total_ms)
-    ms_per_step = total_ms / args.steps
+    ctx = {"args": args, "world": world, "rank": rank, "dev": dev, "stream": stream, "flush": flush,
+           "gpu_id": gpu_id}
 
-    # per-kernel device times, recorded by the library around each launch
-    for m in handles:
-        ds4.ds4moe_profile(m.handle, True)
-    for i in range(args.profile_steps):
-        flush.zero_()
-        step(i)
-    ktimes = {}
-    for m in handles:
-        for name, (n, ms) in ds4.ds4moe_profile_read(m.handle).items():
-            a = ktimes.setdefault(name, [0, 0.0])
-            a[0] += n
-            a[1] += ms
-        ds4.ds4moe_profile(m.handle, False)
-    dom = max(ktimes, key=lambda k: ktimes[k][1])
-    dom_avg_ms = ktimes[dom][1] / ktimes[dom][0]
-    dom_bytes = kernel_bytes(dom, shape, T, U_mean, args.gains, args.routed_format)
-    peaks = {}
-    pk_path = os.path.join(ROOT, "MEASURED_PEAKS.json")
-    if os.path.exists(pk_path):
-        with open(pk_path) as f:
-            peaks = json.load(f)
-    hbm_peak = peaks.get("hbm_gbs", 6800.0)
-    tf_peak = peaks.get("bf16_tflops", 1872.7)
-    peak_src = "measured" if "hbm_gbs" in peaks else "fallback"
-    roofline = None
-    dom_flops = kernel_flops(dom, shape, T)
-    if dom_bytes is not None:
-        sec = dom_avg_ms / 1000.0
-        t_hbm = dom_bytes / (hbm_peak * 1e9)
-        t_tc = dom_flops / (tf_peak * 1e12) if dom_flops else 0.0
-        if t_tc > t_hbm:
-            ach = dom_flops / sec / 1e12
-            roofline = {"bound": "tensor", "kernel": dom, "achieved": ach, "peak": tf_peak, "unit": "TFLOP/s",
-                        "frac": ach / tf_peak, "traffic": kernel_traffic(dom, args.workload, args.gains, args.routed_format),
-                        "peak_source": peak_src + " bf16 burst",
-                        "flops_per_launch": dom_flops, "bytes_per_launch": dom_bytes,
-                        "hbm_frac": dom_bytes / sec / 1e9 / hbm_peak, "avg_launch_us": 1000 * dom_avg_ms}
-        else:
-            ach = dom_bytes / sec / 1e9
-            roofline = {"bound": "hbm", "kernel": dom, "achieved": ach, "peak": hbm_peak, "unit": "GB/s",
-                        "frac": ach / hbm_peak, "traffic": kernel_traffic(dom, args.workload, args.gains, args.routed_format), "peak_source": peak_src,
-                        "bytes_per_launch": dom_bytes, "avg_launch_us": 1000 * dom_avg_ms}
-            if dom_flops:
-                roofline["flops_per_launch"] = dom_flops
-                roofline["tensor_frac"] = dom_flops / sec / 1e12 / tf_peak
-    lay_bytes = layer_bytes(shape, T, U_mean, args.gains, args.routed_format) * len(handles)
-    layer_gbs = lay_bytes / (ms_per_step / 1000.0) / 1e9
-
-    # end to end through host memory
-    xh = [torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).pin_memory() for b in batches]
-    yh = torch.empty((T, shape.hidden), dtype=torch.float32).pin_memory()
-    e2e_ms = []
-    for i in range(args.warmup + args.steps):
-        flush.zero_()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
+    head = args.workload
+    side = [w for w in SIDE_WORKLOADS if head == "decode_t1" and not args.headline_only]
+    wl, layers = workload_layers(head, args.gains, args.routed_format)
+    # decode_t1, decode_t8 and prefill_t1024 share one layer: one handle sized for all of them
+    shares = [w for w in side if synth.WORKLOADS[w].layer_seeds == wl.layer_seeds]
+    max_t = max([wl.tokens, 8] + [synth.WORKLOADS[w].tokens for w in shares])
+    handles = make_handles(layers, wl.shape, dev, max_t, args.routed_format, stream)
+    out = measure(ctx, head, handles, layers, args.steps, args.warmup, args.profile_steps, args.steps, 10.0)
+    extra = {}
+    for name in side:
+        steps, warmup, prof, e2e_steps, cpu_s = SIDE_WORKLOADS[name]
+        if name in shares:
+            extra[name] = measure(ctx, name, handles, layers, steps, warmup, prof, e2e_steps, cpu_s)
+            continue
         for m in handles:
-            ds4.ds4moe_forward_host(m.handle, xh[i % len(xh)].data_ptr(), T, yh.data_ptr())
-        b.record(stream)
-        b.synchronize()
-        if i >= args.warmup:
-            e2e_ms.append(a.elapsed_time(b))
-    e2e_total = max_over_ranks(sum(e2e_ms), world, dev)
-    e2e = {"value": job_rate(world, T, args.steps, e2e_total), "unit": UNIT,
-           "h2d_bytes_per_step": 2 * T * shape.hidden * len(handles),
-           "d2h_bytes_per_step": 4 * T * shape.hidden * len(handles)}
+            m.close()
+        handles = []
+        torch.cuda.empty_cache()
+        swl, slayers = workload_layers(name, args.gains, args.routed_format)
+        handles = make_handles(slayers, swl.shape, dev, swl.tokens, args.routed_format, stream)
+        extra[name] = measure(ctx, name, handles, slayers, steps, warmup, prof, e2e_steps, cpu_s)
+        del slayers
     for m in handles:
-        if m.status() != 0:
-            raise RuntimeError("device error reported by the library")
-
-    cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        # about 10 s of CPU work: whole passes over the sample until then
-        rate, cores, sample, dt = cpu_oracle_rate(args.workload, layers, batches, min_seconds=10.0)
-        cpu = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample,
-               "seconds": dt}
+        m.close()
 
     if rank == 0:
-        out = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-               "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-               "vs_baseline": None, "dtype": "f32" if T <= ds4.AUTO_DECODE_MAX_T else "bf16", "data": "synthetic",
-               "config": workload_config(wl, args.workload, l2_note, args.gains, args.routed_format),
-               "roofline": roofline,
-               "layer_roofline": {"bound": "hbm" if args.workload != "prefill_t4096_zipf4" else "tensor",
-                                  "bytes_per_step": lay_bytes, "achieved_gbs": layer_gbs,
-                                  "frac_hbm": layer_gbs / hbm_peak,
-                                  "tflops": layer_flops(shape, T) * len(handles) / (ms_per_step / 1000) / 1e12,
-                                  "unique_experts_mean": U_mean},
-               "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
-               "clocks": clk.summary(),
-               "kernels_us": {k: round(1000 * v[1] / v[0], 2) for k, v in ktimes.items()}}
-        print(json.dumps(out))
+        line = {"metric": METRIC, "value": out["value"], "unit": UNIT, "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": out["ms_per_step"], "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": out["dtype"], "data": "synthetic",
+                "config": out["config"], "roofline": out["roofline"], "layer_roofline": out["layer_roofline"],
+                "cpu_baseline": out["cpu_baseline"], "e2e": out["e2e"], "gpu_launches": out["gpu_launches"],
+                "clocks": out["clocks"], "kernels_us": out["kernels_us"]}
+        if extra:
+            line["workloads"] = {k: dict(v, metric=METRIC, unit=UNIT, higher_is_better=True, vs_baseline=None)
+                                 for k, v in extra.items()}
+        print(json.dumps(line))
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()

@@ -224,6 +224,29 @@ typedef struct {
 
 int ds4moe_get_stats(ds4moe_t *h, ds4moe_stats *out);
 
+/*
+ * Test entry point: the routing and the token-to-expert grouping of the last
+ * forward call, copied to HOST buffers (synchronises the stream). T must be
+ * that call's token count. Any output may be NULL.
+ *   idx [T][K], w [T][K], gap [T]   the routing the call used (for the router
+ *                                   paths: the experts, weights and K-th minus
+ *                                   (K+1)-th selection score of each token)
+ *   counts [E]                      (token, k) pairs per expert
+ *   inv [T][K]                      position of pair p = t*K + k in the
+ *                                   expert-grouped order: experts ascending,
+ *                                   pairs of one expert in ascending p
+ *   uexp [n_unique], ustart [n_unique + 1]
+ *                                   the distinct experts in that order and the
+ *                                   first position of each (ustart[n] = T*K)
+ *   n_unique                        number of distinct experts
+ * The decode path keeps the grouping of its last launch of up to 8 tokens only:
+ * after a decode call with T > 8 the grouping outputs must be NULL.
+ * Errors: EINVAL (NULL handle, T not the last call's, grouping after a long
+ * decode call), ECUDA, EDEVICE (a grouping the kernels left inconsistent).
+ */
+int ds4moe_inspect(ds4moe_t *h, int32_t T, int32_t *idx, float *w, float *gap, int32_t *counts, int32_t *inv,
+                   int32_t *uexp, int32_t *ustart, int32_t *n_unique);
+
 /* Device bytes the handle owns: repacked weights and scratch. */
 int ds4moe_memory(ds4moe_t *h, uint64_t *weight_bytes, uint64_t *scratch_bytes);
 
@@ -269,14 +292,18 @@ int ds4moe_profile_read(ds4moe_t *h, ds4moe_kernel_time *out, int32_t max, int32
  * H=4096 and E=384 that is T <= 221). The call never calls cudaMalloc or
  * cudaFree and launches three kernels on `stream`.
  *
- * The first call on each device, with that device current, resolves the
- * array's device address (cudaGetSymbolAddress) and caches it; make that
- * first call before any stream capture. All calls share the one array, which
- * keeps the last call's contents (nothing in it needs to start at zero):
- * calls whose kernels can overlap on the GPU, such as calls on different
- * streams that are not ordered, race on it and must be serialised by the
- * caller.
- * Errors: EINVAL, ESCRATCH, EUNSUPPORTED (device not sm_103), ECUDA.
+ * Every call runs on the current device: all buffers must be memory of that
+ * device and `stream` a stream of it (else EINVAL). Each call looks the
+ * array's device address up for the current device and context
+ * (cudaGetSymbolAddress: a lookup that allocates nothing), so the entry point
+ * stays valid after cudaDeviceReset or under another context. The first call
+ * on a device may load the library's device code: make it before any stream
+ * capture. All calls share the one array, which keeps the last call's
+ * contents (nothing in it needs to start at zero): calls whose kernels can
+ * overlap on the GPU, such as calls on different streams that are not
+ * ordered, race on it and must be serialised by the caller.
+ * Errors: EINVAL, ESCRATCH (checked first), EUNSUPPORTED (device not sm_103),
+ * ECUDA.
  */
 #define DS4MOE_NOALLOC_SCRATCH (4u << 20)
 

@@ -62,6 +62,7 @@ SIGNATURES = {
     "ds4moe_route_detail": (ctypes.c_int, [_vp, _vp, _i32, _vp, _vp, _vp, _vp]),
     "ds4moe_status": (ctypes.c_int, [_vp]),
     "ds4moe_get_stats": (ctypes.c_int, [_vp, ctypes.POINTER(Stats)]),
+    "ds4moe_inspect": (ctypes.c_int, [_vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.POINTER(_i32)]),
     "ds4moe_memory": (ctypes.c_int, [_vp, ctypes.POINTER(ctypes.c_uint64), ctypes.POINTER(ctypes.c_uint64)]),
     "ds4moe_profile": (ctypes.c_int, [_vp, _i32]),
     "ds4moe_profile_read": (ctypes.c_int, [_vp, ctypes.POINTER(KernelTime), _i32, ctypes.POINTER(_i32)]),
@@ -154,6 +155,29 @@ def ds4moe_get_stats(h: int) -> Stats:
     s = Stats()
     _check(_lib.ds4moe_get_stats(h, ctypes.byref(s)), "ds4moe_get_stats")
     return s
+
+
+def ds4moe_inspect(h: int, T: int, K: int, E: int, grouping: bool = True) -> dict:
+    """Routing (and, with grouping, the expert grouping) of the last forward call, as numpy arrays."""
+    import numpy as np
+    idx = np.empty((T, K), dtype=np.int32)
+    w = np.empty((T, K), dtype=np.float32)
+    gap = np.empty((T,), dtype=np.float32)
+    out = {"idx": idx, "w": w, "gap": gap}
+    ptr = lambda a: a.ctypes.data if a is not None else None  # noqa: E731
+    counts = inv = uexp = ustart = None
+    nu = _i32()
+    if grouping:
+        counts = np.empty((E,), dtype=np.int32)
+        inv = np.empty((T * K,), dtype=np.int32)
+        uexp = np.empty((min(T * K, E),), dtype=np.int32)
+        ustart = np.empty((min(T * K, E) + 1,), dtype=np.int32)
+    _check(_lib.ds4moe_inspect(h, T, ptr(idx), ptr(w), ptr(gap), ptr(counts), ptr(inv), ptr(uexp), ptr(ustart),
+                               ctypes.byref(nu) if grouping else None), "ds4moe_inspect")
+    if grouping:
+        n = nu.value
+        out.update(counts=counts, inv=inv, uexp=uexp[:n].copy(), ustart=ustart[:n + 1].copy(), n_unique=n)
+    return out
 
 
 def ds4moe_memory(h: int):
@@ -253,3 +277,6 @@ class MoELayer:
 
     def stats(self) -> Stats:
         return ds4moe_get_stats(self.handle)
+
+    def inspect(self, T: int, grouping: bool = True) -> dict:
+        return ds4moe_inspect(self.handle, T, self.shape.top_k, self.shape.n_experts, grouping)

@@ -84,6 +84,32 @@ __device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
 
 __device__ __forceinline__ float sigmoid(float z) { return 1.0f / (1.0f + expf(-z)); }
 
+// Order-preserving unsigned key of a float (larger float, larger key; -0 and
+// +0 share one key; NaN maps to 0, below every number) and its inverse for
+// non-NaN keys.
+__device__ __forceinline__ unsigned order_key(float v) {
+    const unsigned u = v == 0.f ? 0u : __float_as_uint(v);
+    if (v != v)
+        return 0u;
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ float order_key_value(unsigned k) {
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
+// Selection key of a selection score: order_key with NaN moved from 0 to 1,
+// so that 0 can mark a taken expert. The selection policy of every kernel:
+// larger score first, equal scores (and NaNs among themselves) by lower
+// expert index, a NaN score below every number including -inf. Keys of
+// numbers are >= order_key(-inf) > 1.
+__device__ __forceinline__ unsigned sel_key(float v) { return v == v ? order_key(v) : 1u; }
+
+// The score a selection key stands for (NaN for the NaN key).
+__device__ __forceinline__ float sel_key_value(unsigned k) {
+    return k > 1u ? order_key_value(k) : __uint_as_float(0x7FC00000u);
+}
+
 // Down-gain blocks ("YoungAi - DeepSeek V4.1 Flash on one DGX Spark", sections
 // 3 and 4.2): per expert and 32 output channels, 16 bytes of FP4 E2M1 codes
 // (channel i at byte i/2, even channel in the low nibble) and one E8M0 scale

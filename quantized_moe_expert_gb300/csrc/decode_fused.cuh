@@ -308,20 +308,6 @@ __device__ bool wait_counter(const DecodeArgs &a, const unsigned *p, unsigned ta
 
 // ---- mbarrier, bulk copy and barrier helpers ------------------------------------
 
-// Order-preserving unsigned key of a float (larger float, larger key; -0 and
-// +0 share one key; NaN maps to 0, below every number) and its inverse for
-// non-NaN keys.
-__device__ __forceinline__ unsigned order_key(float v) {
-    const unsigned u = v == 0.f ? 0u : __float_as_uint(v);
-    if (v != v)
-        return 0u;
-    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-
-__device__ __forceinline__ float order_key_value(unsigned k) {
-    return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
-}
-
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
@@ -678,11 +664,6 @@ __device__ __forceinline__ void router_stage(const uint8_t *sl, const StageDesc 
     }
 }
 
-// Selection key of a selection score: order_key with NaN moved from 0 to 1,
-// so that 0 can mark a taken expert (below everything, NaN included). Keys of
-// numbers are >= order_key(-inf) > 1.
-__device__ __forceinline__ unsigned sel_key(float v) { return v == v ? order_key(v) : 1u; }
-
 // Top-k of token t by one warp from the selection keys keys[e] (shared
 // memory, e < E). Lane l owns experts l, l + 32, ...; it keeps its best
 // (key desc, index asc) and each round the warp takes the best of the 32 by
@@ -714,7 +695,7 @@ __device__ __forceinline__ void select_token(const DecodeArgs &a, const SelIO &i
         const unsigned gk = __reduce_max_sync(0xFFFFFFFFu, best);
         const unsigned cand = (bi >= 0 && best == gk) ? (unsigned)bi : 0xFFFFFFFFu;
         const int be = (int)__reduce_min_sync(0xFFFFFFFFu, cand); // < E: every round has a candidate
-        const float bv = gk > 1u ? order_key_value(gk) : __uint_as_float(0x7FC00000u);
+        const float bv = sel_key_value(gk);
         if (r < K) {
             if (lane == r) {
                 chosen = be;
@@ -738,7 +719,7 @@ __device__ __forceinline__ void select_token(const DecodeArgs &a, const SelIO &i
         if (a.router_bias)
             sc = sigmoid(__uint_as_float((unsigned)ld_relaxed_u64(io.lgt + t * E + chosen)));
         else
-            sc = chosen_key > 1u ? order_key_value(chosen_key) : __uint_as_float(0x7FC00000u);
+            sc = sel_key_value(chosen_key);
     }
     float total = 0.f;
     for (int r = 0; r < K; r++)
@@ -934,16 +915,19 @@ __device__ __forceinline__ bool job_select(const DecodeArgs &a, const SelIO &io,
     const unsigned kmagic = (65536u + (unsigned)K - 1u) / (unsigned)K;
     auto tok_of_pair = [&](int p) -> int { return (int)(((unsigned)p * kmagic) >> 16); };
     if (T == 1) {
-        // one token: its K experts are distinct, slot k is the k-th chosen
-        // expert with its single pair at position k (the slot order only
-        // numbers the jobs; the combine sums in k order either way)
+        // one token: its K experts are distinct; the slot of the k-th chosen
+        // expert is its rank among them (ascending expert index, as for more
+        // tokens), holding its single pair at that position
         if (warp == 0) {
+            const int e = lane < K ? sm.sel_idx[0][lane] : 0x7FFFFFFF;
+            int rank = 0;
+            for (int j = 0; j < K; j++)
+                rank += __shfl_sync(0xFFFFFFFFu, e, j) < e ? 1 : 0;
             if (lane < K) {
-                const int e = sm.sel_idx[0][lane];
-                io.inv[lane] = lane;
+                io.inv[lane] = rank;
                 atomicAdd(io.counts + e, 1);
-                sm.rec[0][lane] = (unsigned)e | (unsigned)lane << 11 | 1u << 18 | (unsigned)K << 22;
-                sm.rec[1][lane] = 0u; // token 0
+                sm.rec[0][rank] = (unsigned)e | (unsigned)rank << 11 | 1u << 18 | (unsigned)K << 22;
+                sm.rec[1][rank] = 0u; // token 0
             }
             if (lane == 0)
                 *io.nuniq = K;

@@ -1,12 +1,11 @@
 // Token-to-expert grouping: per-expert counts, their exclusive scan, the list
 // of distinct experts, and a stable permutation of the (token, k) pairs into
 // expert-grouped order (pairs of one expert keep ascending pair index), so the
-// grouping is deterministic. The batched-union idea - one dispatch per distinct
-// expert for all rows that chose it - is the verify-batch expert kernel of
-// "YoungAi - DeepSeek V4.1 Flash on one DGX Spark", section 4.4 ("a persistent
-// expert kernel over (unique expert x rows) that reads each chosen expert's
-// bits once"). The prefill path's weighted combine, which reads the grouped
-// outputs back in token order, sits at the end.
+// grouping is deterministic. Grouping the rows by distinct expert lets each
+// chosen expert's weights be read once for all the rows that picked it, the
+// batching the verify-batch expert kernel of "YoungAi - DeepSeek V4.1 Flash on
+// one DGX Spark", section 4.4, is built on. The prefill path's weighted
+// combine, which reads the grouped outputs back in token order, sits at the end.
 #pragma once
 
 #include "common.cuh"

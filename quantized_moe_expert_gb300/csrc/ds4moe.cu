@@ -8,7 +8,6 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
-#include <mutex>
 #include <new>
 #include <string>
 #include <vector>
@@ -537,7 +536,7 @@ int run_router(ds4moe *h, const void *x, int T, float *sel_out) {
         });
     }
     launch(h, "router_select", [&] {
-        const size_t smem = (size_t)3 * L.E * sizeof(float);
+        const size_t smem = (size_t)kSelectSmemPerExpert * L.E;
         router_select_kernel<<<T, kSelectThreads, smem, st>>>(
             S.logits, L.router_bias, T, L.E, L.K, S.idx, S.w, S.gap, sel_out,
             T >= kRouterGemmMinT ? static_cast<const uint16_t *>(x) : nullptr, L.router_w, L.H, nsplit,
@@ -1168,6 +1167,60 @@ int ds4moe_get_stats(ds4moe_t *h, ds4moe_stats *out) {
     return cuda_rc(cudaGetLastError());
 }
 
+int ds4moe_inspect(ds4moe_t *h, int32_t T, int32_t *idx, float *w, float *gap, int32_t *counts, int32_t *inv,
+                   int32_t *uexp, int32_t *ustart, int32_t *n_unique) {
+    if (!h || T < 0 || T != h->stats.tokens)
+        return DS4MOE_EINVAL;
+    int rc = cuda_rc(cudaStreamSynchronize(h->stream));
+    if (rc || T == 0)
+        return rc;
+    const LayerDev &L = h->L;
+    const Scratch &S = h->S;
+    const int64_t P = (int64_t)T * L.K;
+    auto get = [&](void *dst, const void *src, size_t bytes) {
+        if (dst && rc == DS4MOE_OK)
+            rc = cuda_rc(cudaMemcpy(dst, src, bytes, cudaMemcpyDeviceToHost));
+    };
+    get(idx, S.idx, sizeof(int32_t) * P);
+    get(w, S.w, sizeof(float) * P);
+    get(gap, S.gap, sizeof(float) * T);
+    if (rc || !(counts || inv || uexp || ustart || n_unique))
+        return rc;
+    const bool dec = h->stats.path == DS4MOE_PATH_DECODE && !L.mx4;
+    if (dec && T > kDecodeT)
+        return DS4MOE_EINVAL; // the fused kernel keeps the grouping of its last launch only
+    int32_t nu = 0;
+    get(&nu, dec ? h->D.nuniq : S.nuniq, sizeof(int32_t));
+    if (rc)
+        return rc;
+    if (nu < 0 || nu > P || nu > L.E)
+        return DS4MOE_EDEVICE;
+    if (n_unique)
+        *n_unique = nu;
+    get(counts, dec ? h->D.counts : S.counts, sizeof(int32_t) * L.E);
+    get(inv, dec ? h->D.inv : S.inv, sizeof(int32_t) * P);
+    if (!dec) {
+        get(uexp, S.uexp, sizeof(int32_t) * nu);
+        get(ustart, S.uoff, sizeof(int32_t) * (nu + 1));
+        return rc;
+    }
+    // the decode kernel's slot records: expert in bits 0-10, first position in bits 11-17
+    std::vector<unsigned long long> rec(2 * (size_t)nu);
+    get(rec.data(), h->D.srec, sizeof(unsigned long long) * rec.size());
+    if (rc)
+        return rc;
+    for (int s = 0; s < nu; s++) {
+        const unsigned w0 = (unsigned)rec[2 * s];
+        if (uexp)
+            uexp[s] = (int32_t)(w0 & 0x7FFu);
+        if (ustart)
+            ustart[s] = (int32_t)((w0 >> 11) & 0x7Fu);
+    }
+    if (ustart)
+        ustart[nu] = (int32_t)P;
+    return rc;
+}
+
 int ds4moe_profile(ds4moe_t *h, int32_t enable) {
     if (!h)
         return DS4MOE_EINVAL;
@@ -1215,41 +1268,46 @@ int ds4moe_memory(ds4moe_t *h, uint64_t *weight_bytes, uint64_t *scratch_bytes) 
 // ---- routing without allocation ------------------------------------------------
 //
 // The scratch of ds4moe_route_noalloc lives in this file-scope device array.
-// Host code may not use the symbol as a pointer: its device address is
-// resolved once per device with cudaGetSymbolAddress and cached.
+// Host code may not use the symbol as a pointer: its device address is looked
+// up with cudaGetSymbolAddress for the current device and context on every
+// call (a lookup, no allocation), so a context that was reset or replaced
+// never receives a stale address.
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[DS4MOE_NOALLOC_SCRATCH];
 
 namespace {
 
-constexpr int kNoAllocMaxDevices = 64;
-std::mutex g_noalloc_mutex;
-void *g_noalloc_ptr[kNoAllocMaxDevices] = {};
-
-// Device address of the scratch array on the current device.
-int noalloc_scratch(void **out) {
-    int dev = 0;
-    int rc = cuda_rc(cudaGetDevice(&dev));
+// Device address of the scratch array on the current device; *dev gets that device.
+int noalloc_scratch(void **out, int *dev) {
+    int rc = cuda_rc(cudaGetDevice(dev));
     if (rc)
         return rc;
-    if (dev < 0 || dev >= kNoAllocMaxDevices)
+    int major = 0, minor = 0;
+    rc = cuda_rc(cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, *dev));
+    if (!rc)
+        rc = cuda_rc(cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, *dev));
+    if (rc)
+        return rc;
+    if (major != 10 || minor != 3)
         return DS4MOE_EUNSUPPORTED;
-    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
-    if (!g_noalloc_ptr[dev]) {
-        cudaDeviceProp prop;
-        rc = cuda_rc(cudaGetDeviceProperties(&prop, dev));
-        if (rc)
-            return rc;
-        if (prop.major != 10 || prop.minor != 3)
-            return DS4MOE_EUNSUPPORTED;
-        void *p = nullptr;
-        rc = cuda_rc(cudaGetSymbolAddress(&p, g_noalloc_scratch));
-        if (rc)
-            return rc;
-        g_noalloc_ptr[dev] = p;
-    }
-    *out = g_noalloc_ptr[dev];
+    void *p = nullptr;
+    rc = cuda_rc(cudaGetSymbolAddress(&p, g_noalloc_scratch));
+    if (rc)
+        return rc;
+    *out = p;
     return DS4MOE_OK;
+}
+
+// A device (or managed) pointer of device `dev`.
+bool on_device(const void *p, int dev) {
+    if (!p)
+        return false;
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) && a.device == dev;
 }
 
 uint64_t round256(uint64_t n) { return (n + 255) & ~uint64_t(255); }
@@ -1263,18 +1321,29 @@ extern "C" int ds4moe_route_noalloc(const float *router_w, const float *router_b
         return DS4MOE_EINVAL;
     if (T == 0)
         return DS4MOE_OK;
-    if (!is_device_ptr(router_w) || !aligned(router_w, 16) || !is_device_ptr(x_bf16) || !aligned(x_bf16, 16) ||
-        !is_device_ptr(idx_out) || !is_device_ptr(w_out) || (router_bias && !is_device_ptr(router_bias)))
-        return DS4MOE_EINVAL;
     const uint64_t x32_bytes = round256(4ull * T * H);
     const uint64_t xsum_bytes = round256(4ull * T * (H / 16));
     const uint64_t logit_bytes = round256(4ull * T * E);
     if (x32_bytes + xsum_bytes + logit_bytes > DS4MOE_NOALLOC_SCRATCH)
         return DS4MOE_ESCRATCH;
     void *base = nullptr;
-    int rc = noalloc_scratch(&base);
+    int dev = 0;
+    int rc = noalloc_scratch(&base, &dev);
     if (rc)
         return rc;
+    // every buffer and the stream on the current device (the scratch's)
+    if (!on_device(router_w, dev) || !aligned(router_w, 16) || !on_device(x_bf16, dev) || !aligned(x_bf16, 16) ||
+        !on_device(idx_out, dev) || !on_device(w_out, dev) || (router_bias && !on_device(router_bias, dev)))
+        return DS4MOE_EINVAL;
+    if (stream) {
+        int sdev = -1;
+        if (cudaStreamGetDevice(static_cast<cudaStream_t>(stream), &sdev) != cudaSuccess) {
+            cudaGetLastError();
+            return DS4MOE_EINVAL;
+        }
+        if (sdev != dev)
+            return DS4MOE_EINVAL;
+    }
     float *x32 = static_cast<float *>(base);
     float *xsum = reinterpret_cast<float *>(static_cast<char *>(base) + x32_bytes);
     float *logits = reinterpret_cast<float *>(static_cast<char *>(base) + x32_bytes + xsum_bytes);
@@ -1283,7 +1352,7 @@ extern "C" int ds4moe_route_noalloc(const float *router_w, const float *router_b
                                                                          H, x32, xsum);
     router_logits_kernel<<<dim3(blocks_for(E, 8), blocks_for(T, kRouterTok)), 256, 0, st>>>(x32, T, H, router_w, E,
                                                                                           logits);
-    const size_t smem = (size_t)3 * E * sizeof(float);
+    const size_t smem = (size_t)kSelectSmemPerExpert * E;
     router_select_kernel<<<T, kSelectThreads, smem, st>>>(
         logits, router_bias, T, E, K, idx_out, w_out, nullptr, nullptr, nullptr, nullptr, 0, 1, 0);
     return launch_rc();

@@ -88,45 +88,42 @@ __global__ void router_logits_kernel(const float *__restrict__ x32, int T, int H
 // a plain dot product; the margin is 4x that).
 constexpr float kRefineMargin = 2e-5f;
 constexpr int kSelectThreads = 128; // one block per token
+constexpr int kSelectSmemPerExpert = 16;
 
-// Warp-wide: the K (+1) best selection scores by K+1 rounds of a warp arg-max
-// (equal scores: lower index first). Consumes sel (chosen entries set to -inf).
-__device__ __forceinline__ void select_rounds(float *sel, const float *score, int E, int K, float (&chosen_s)[kMaxTopK],
-                                              int (&chosen_e)[kMaxTopK], float &kth, float &next, int lane) {
+// Warp-wide: the K (+1) best selection keys (sel_key) by K+1 rounds of a
+// warp arg-max (larger key first, equal keys by lower index). Consumes keys
+// (a chosen expert's key becomes 0). kth / next: the scores of the K-th and
+// (K+1)-th choice (NaN for a NaN score).
+__device__ __forceinline__ void select_rounds(unsigned *keys, const float *score, int E, int K,
+                                              float (&chosen_s)[kMaxTopK], int (&chosen_e)[kMaxTopK], float &kth,
+                                              float &next, int lane) {
     kth = 0.f;
     next = -INFINITY;
     const int rounds = K < E ? K + 1 : K;
     for (int r = 0; r < rounds; r++) {
-        float bv = -INFINITY;
+        // every round has an untaken expert (K < E, or r < K = E), whose key is >= 1
+        unsigned bk = 0u;
         int be = 0x7FFFFFFF;
-        for (int e = lane; e < E; e += 32) {
-            float v = sel[e];
-            if (v > bv || (v == bv && e < be)) {
-                bv = v;
+        for (int e = lane; e < E; e += 32) { // ascending e: strict > keeps the lower index
+            const unsigned k = keys[e];
+            if (k > bk) {
+                bk = k;
                 be = e;
             }
         }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, o);
-            int oe = __shfl_xor_sync(0xFFFFFFFFu, be, o);
-            if (ov > bv || (ov == bv && oe < be)) {
-                bv = ov;
-                be = oe;
-            }
-        }
-        if (be >= E) // every remaining score was NaN: keep the index in range
-            be = 0;
+        const unsigned gk = __reduce_max_sync(0xFFFFFFFFu, bk);
+        const int ge = (int)__reduce_min_sync(0xFFFFFFFFu, bk == gk ? (unsigned)be : 0xFFFFFFFFu);
+        const float gv = sel_key_value(gk);
         if (r < K) {
-            chosen_e[r] = be;
-            chosen_s[r] = score[be];
+            chosen_e[r] = ge;
+            chosen_s[r] = score[ge];
             if (r == K - 1)
-                kth = bv;
-            if (lane == (be & 31))
-                sel[be] = -INFINITY;
+                kth = gv;
+            if (lane == (ge & 31))
+                keys[ge] = 0u;
             __syncwarp();
         } else {
-            next = bv;
+            next = gv;
         }
     }
 }
@@ -137,7 +134,7 @@ __device__ __forceinline__ void select_rounds(float *sel, const float *score, in
 // within kRefineMargin of the (K+1)-th best gets its logit recomputed as an
 // fp32 dot product of x (bf16) and its router row (the block's warps share
 // the candidates) before the final decision.
-// Shared memory: 2 * E floats + E ints.
+// Shared memory: 2 * E floats + 2 * E ints (kSelectSmemPerExpert bytes per expert).
 __global__ void router_select_kernel(const float *__restrict__ logits, const float *__restrict__ bias, int T,
                                      int E, int K, int32_t *__restrict__ idx, float *__restrict__ w,
                                      float *__restrict__ gap, float *__restrict__ sel_out,
@@ -152,6 +149,7 @@ __global__ void router_select_kernel(const float *__restrict__ logits, const flo
     float *sel = smem;
     float *score = sel + E;
     int *cand = reinterpret_cast<int *>(score + E);
+    unsigned *keys = reinterpret_cast<unsigned *>(cand + E);
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
         float l = logits[(int64_t)t * E + e];
         for (int q = 1; q < nsplit; q++) // partial logits of a K-split GEMM, added in order
@@ -159,6 +157,7 @@ __global__ void router_select_kernel(const float *__restrict__ logits, const flo
         float s = sigmoid(l);
         score[e] = s;
         sel[e] = bias ? s + bias[e] : s;
+        keys[e] = sel_key(sel[e]);
     }
     __syncthreads();
     float chosen_s[kMaxTopK];
@@ -166,14 +165,12 @@ __global__ void router_select_kernel(const float *__restrict__ logits, const flo
     float kth, next;
     if (x_refine) {
         if (warp == 0) {
-            select_rounds(sel, score, E, K, chosen_s, chosen_e, kth, next, lane);
-            const float thr = (K < E ? next : kth) - kRefineMargin;
+            select_rounds(keys, score, E, K, chosen_s, chosen_e, kth, next, lane);
+            const float thr = (K < E ? next : kth) - kRefineMargin; // NaN: no candidate
             int n = 0;
             for (int e0 = 0; e0 < E; e0 += 32) {
                 const int e = e0 + lane;
-                const float v = e < E ? (bias ? score[e] + bias[e] : score[e]) : -INFINITY;
-                if (e < E)
-                    sel[e] = v; // restore what the rounds consumed
+                const float v = e < E ? sel[e] : -INFINITY;
                 const unsigned m = __ballot_sync(0xFFFFFFFFu, v >= thr);
                 if (v >= thr)
                     cand[n + __popc(m & ((1u << lane) - 1u))] = e;
@@ -205,13 +202,15 @@ __global__ void router_select_kernel(const float *__restrict__ logits, const flo
         }
         __syncthreads();
     }
-    if (sel_out)
-        for (int e = threadIdx.x; e < E; e += blockDim.x)
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        if (sel_out)
             sel_out[(int64_t)t * E + e] = sel[e];
+        keys[e] = sel_key(sel[e]);
+    }
     __syncthreads();
     if (warp != 0)
         return;
-    select_rounds(sel, score, E, K, chosen_s, chosen_e, kth, next, lane);
+    select_rounds(keys, score, E, K, chosen_s, chosen_e, kth, next, lane);
     if (lane == 0) {
         float total = 0.f;
         for (int k = 0; k < K; k++)

@@ -30,6 +30,25 @@ def rel_l2(y: np.ndarray, ref: np.ndarray) -> float:
     return float(np.linalg.norm(y - ref) / np.linalg.norm(ref))
 
 
+def rel_l2_rows(y: np.ndarray, ref: np.ndarray) -> np.ndarray:
+    """Relative L2 error of each token (row) of a [T, H] output."""
+    y = np.asarray(y, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    return np.linalg.norm(y - ref, axis=1) / np.linalg.norm(ref, axis=1)
+
+
+def assert_close(y: np.ndarray, ref: np.ndarray, tol: float):
+    """The output within tol of the oracle's, as relative L2 over the whole
+    [T, H] array and over every token on its own (a wrong token cannot hide
+    behind many right ones). Returns (whole-array error, worst token error)."""
+    whole = rel_l2(y, ref)
+    rows = rel_l2_rows(np.atleast_2d(y), np.atleast_2d(ref))
+    worst = int(np.argmax(rows))
+    assert whole <= tol, f"relative L2 {whole:.3e} above {tol:.0e}"
+    assert rows[worst] <= tol, f"token {worst}: relative L2 {rows[worst]:.3e} above {tol:.0e}"
+    return whole, float(rows[worst])
+
+
 def check_routing(idx, w, gap, ref: dict, K: int):
     """idx/w/gap from the GPU vs the oracle's routing dict.
 

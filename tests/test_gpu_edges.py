@@ -9,7 +9,7 @@ import pytest
 import oracle
 import quantized_moe_expert_gb300 as ds4
 import synth
-from gpu_util import TOL_DECODE, TOL_PREFILL, check_routing, rel_l2, to_dev, x_to_dev
+from gpu_util import assert_close, TOL_DECODE, TOL_PREFILL, check_routing, rel_l2, to_dev, x_to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -28,7 +28,7 @@ def run_and_check(moe, shape, layer, x, path, tol):
         y_ref = oracle.forward_routed(shape, layer, x, idx.cpu().numpy(), w.cpu().numpy().astype(np.float64))
     else:
         y_ref, _ = oracle.forward(shape, layer, x)
-    assert rel_l2(y, y_ref) <= tol
+    assert_close(y, y_ref, tol)
     assert np.isfinite(y).all()
     assert moe.status() == 0
 

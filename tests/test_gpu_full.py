@@ -11,7 +11,7 @@ import torch
 import oracle
 import quantized_moe_expert_gb300 as ds4
 import synth
-from gpu_util import TOL_DECODE, TOL_PREFILL, check_routing, rel_l2, to_dev, x_to_dev
+from gpu_util import assert_close, TOL_DECODE, TOL_PREFILL, check_routing, rel_l2, to_dev, x_to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -44,7 +44,7 @@ def test_decode_t1(big):
         if near.any():
             y_ref = oracle.forward_routed(shape, layer, xt, idx.cpu().numpy(),
                                           w.cpu().numpy().astype(np.float64))
-        assert rel_l2(y, y_ref) <= TOL_DECODE
+        assert_close(y, y_ref, TOL_DECODE)
     assert moe.status() == 0
 
 
@@ -58,7 +58,7 @@ def test_decode_t8(big):
     y_ref, r = oracle.forward(shape, layer, x)
     check_routing(idx.cpu().numpy(), w.cpu().numpy(), gap.cpu().numpy(), r, shape.top_k)
     assert s.path == ds4.PATH_DECODE and s.n_unique == len(np.unique(r["idx"]))
-    assert rel_l2(y, y_ref) <= TOL_DECODE
+    assert_close(y, y_ref, TOL_DECODE)
     assert moe.status() == 0
 
 
@@ -79,6 +79,6 @@ def test_prefill_t1024(big):
     ridx = np.where(use_gpu_routing, gi, r["idx"][rows])
     rw = np.where(use_gpu_routing, gw, r["weights"][rows])
     y_ref = oracle.forward_routed(shape, layer, np.ascontiguousarray(x[rows]), ridx, rw)
-    assert rel_l2(y[rows], y_ref) <= TOL_PREFILL
+    assert_close(y[rows], y_ref, TOL_PREFILL)
     assert np.isfinite(y).all()
     assert moe.status() == 0

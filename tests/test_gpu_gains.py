@@ -14,7 +14,7 @@ import torch
 import oracle
 import quantized_moe_expert_gb300 as ds4
 import synth
-from gpu_util import TOL_DECODE, TOL_PREFILL, rel_l2, to_dev, x_to_dev
+from gpu_util import assert_close, TOL_DECODE, TOL_PREFILL, rel_l2, to_dev, x_to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -66,7 +66,7 @@ def test_gains_match_oracle(tiny, tables, path, T):
     y_plain = oracle.forward_routed(shape, layer, x, r["idx"], w32.astype(np.float64))
     # the gains move the output by far more than the tolerance
     assert rel_l2(y_plain, y_ref) > 20 * TOL_PREFILL
-    assert rel_l2(y, y_ref) <= (TOL_DECODE if path == ds4.PATH_DECODE else TOL_PREFILL)
+    assert_close(y, y_ref, (TOL_DECODE if path == ds4.PATH_DECODE else TOL_PREFILL))
     assert moe.status() == 0
 
 
@@ -103,7 +103,7 @@ def test_gains_follow_the_expert_not_the_slot(tiny):
     for path, tol in ((ds4.PATH_DECODE, TOL_DECODE), (ds4.PATH_PREFILL, TOL_PREFILL)):
         a = routed(moe, x, r["idx"], w32, path)
         b = routed(moe, x, np.ascontiguousarray(r["idx"][:, perm]), np.ascontiguousarray(w32[:, perm]), path)
-        assert rel_l2(b, a) <= tol
+        assert_close(b, a, tol)
 
 
 @pytest.fixture(scope="module")
@@ -128,7 +128,7 @@ def test_full_size_decode_t8_and_prefill_rows(big):
     idx, w, _, _ = moe.route(xd)
     idx, w = idx.cpu().numpy(), w.cpu().numpy().astype(np.float64)
     y_ref = oracle.forward_routed(shape, layer, x, idx, w)
-    assert rel_l2(y, y_ref) <= TOL_DECODE
+    assert_close(y, y_ref, TOL_DECODE)
     xp = synth.make_tokens("prefill_t1024")
     xpd = x_to_dev(xp)
     yp = moe.forward(xpd).cpu().numpy()
@@ -136,5 +136,5 @@ def test_full_size_decode_t8_and_prefill_rows(big):
     rows = [0, 1, 127, 128, 511, 1023]
     idx, w = idx.cpu().numpy()[rows], w.cpu().numpy()[rows].astype(np.float64)
     y_ref = oracle.forward_routed(shape, layer, xp[rows], idx, w)
-    assert rel_l2(yp[rows], y_ref) <= TOL_PREFILL
+    assert_close(yp[rows], y_ref, TOL_PREFILL)
     assert moe.status() == 0

@@ -11,7 +11,7 @@ import torch
 import oracle
 import quantized_moe_expert_gb300 as ds4
 import synth
-from gpu_util import TOL_DECODE, check_routing, rel_l2, to_dev, x_to_dev
+from gpu_util import assert_close, TOL_DECODE, check_routing, rel_l2, to_dev, x_to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -43,7 +43,7 @@ def test_forward_matches_oracle(tiny, T):
     if near.any():
         y_ref = oracle.forward_routed(shape, layer, x, idx.cpu().numpy(), w.cpu().numpy().astype(np.float64),
                                       act="q8")
-    assert rel_l2(y, y_ref) <= TOL_DECODE
+    assert_close(y, y_ref, TOL_DECODE)
     assert moe.status() == 0
 
 
@@ -71,7 +71,7 @@ def test_forward_routed_and_gains(tiny):
         y_ref = oracle.forward_routed(shape, L, x, idx, w.astype(np.float64), act="q8")
         y_plain = oracle.forward_routed(shape, layer, x, idx, w.astype(np.float64), act="q8")
         assert rel_l2(y_plain, y_ref) > 0.1
-        assert rel_l2(y, y_ref) <= TOL_DECODE
+        assert_close(y, y_ref, TOL_DECODE)
         assert moe.status() == 0
     finally:
         moe.close()
@@ -115,5 +115,5 @@ def test_full_size_t1_and_t8(big):
         r = oracle.route(shape, layer["router_w"], None, x)
         check_routing(idx, w, gap.cpu().numpy(), r, shape.top_k)
         y_ref = oracle.forward_routed(shape, layer, x, idx, w.astype(np.float64), act="q8")
-        assert rel_l2(y, y_ref) <= TOL_DECODE
+        assert_close(y, y_ref, TOL_DECODE)
     assert moe.status() == 0

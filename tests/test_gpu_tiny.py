@@ -11,7 +11,7 @@ import torch
 import oracle
 import quantized_moe_expert_gb300 as ds4
 import synth
-from gpu_util import TOL_DECODE, TOL_PREFILL, check_routing, rel_l2, to_dev, x_to_dev
+from gpu_util import assert_close, TOL_DECODE, TOL_PREFILL, check_routing, rel_l2, to_dev, x_to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -45,7 +45,7 @@ def test_decode_path(tiny, T):
     x = tokens(shape, T, 200 + T)
     y = moe.forward(x_to_dev(x), path=ds4.PATH_DECODE).cpu().numpy()
     y_ref, _ = oracle.forward(shape, layer, x)
-    assert rel_l2(y, y_ref) <= TOL_DECODE
+    assert_close(y, y_ref, TOL_DECODE)
     assert moe.status() == 0
 
 
@@ -55,7 +55,7 @@ def test_prefill_path(tiny, T):
     x = tokens(shape, T, 300 + T)
     y = moe.forward(x_to_dev(x), path=ds4.PATH_PREFILL).cpu().numpy()
     y_ref, r = oracle.forward(shape, layer, x)
-    assert rel_l2(y, y_ref) <= TOL_PREFILL
+    assert_close(y, y_ref, TOL_PREFILL)
     assert moe.status() == 0
 
 
@@ -85,7 +85,7 @@ def test_forward_routed_uses_given_routing(tiny):
         y = moe.forward_routed(x_to_dev(x), torch.from_numpy(idx).cuda(),
                                torch.from_numpy(w.astype(np.float32)).cuda(), path=path).cpu().numpy()
         y_ref = oracle.forward_routed(shape, layer, x, idx, w.astype(np.float32).astype(np.float64))
-        assert rel_l2(y, y_ref) <= tol
+        assert_close(y, y_ref, tol)
     assert moe.status() == 0
 
 
@@ -171,12 +171,12 @@ def test_repeated_given_expert(tiny):
                            path=ds4.PATH_DECODE).cpu().numpy()
     assert moe.status() == ds4.DS4MOE_EDEVICE
     y_ref = oracle.forward_routed(shape, layer, x, replaced, w.astype(np.float64))
-    assert rel_l2(y, y_ref) <= TOL_DECODE
+    assert_close(y, y_ref, TOL_DECODE)
     y = moe.forward_routed(x_to_dev(x), torch.from_numpy(idx).cuda(), torch.from_numpy(w).cuda(),
                            path=ds4.PATH_PREFILL).cpu().numpy()
     assert moe.status() == 0
     y_ref = oracle.forward_routed(shape, layer, x, idx, w.astype(np.float64))
-    assert rel_l2(y, y_ref) <= TOL_PREFILL
+    assert_close(y, y_ref, TOL_PREFILL)
 
 
 def test_create_rejects_host_weights():
@@ -204,7 +204,7 @@ def test_shape_variants(shape):
         y_ref, r = oracle.forward(shape, layer, x)
         idx, w, gap, _ = moe.route(x_to_dev(x))
         check_routing(idx.cpu().numpy(), w.cpu().numpy(), None, r, shape.top_k)
-        assert rel_l2(y, y_ref) <= tol
+        assert_close(y, y_ref, tol)
     assert moe.status() == 0
     moe.close()
 
@@ -220,5 +220,5 @@ def test_router_bias_changes_selection_only():
     check_routing(idx.cpu().numpy(), w.cpu().numpy(), gap.cpu().numpy(), ref, shape.top_k)
     y = moe.forward(x_to_dev(x), path=ds4.PATH_DECODE).cpu().numpy()
     y_ref = oracle.forward_routed(shape, layer, x, ref["idx"], ref["weights"])
-    assert rel_l2(y, y_ref) <= TOL_DECODE
+    assert_close(y, y_ref, TOL_DECODE)
     moe.close()

@@ -13,7 +13,7 @@ import torch
 import oracle
 import quantized_moe_expert_gb300 as ds4
 import synth
-from gpu_util import TOL_PREFILL, check_routing, rel_l2, to_dev, x_to_dev
+from gpu_util import assert_close, TOL_PREFILL, check_routing, rel_l2, to_dev, x_to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -48,7 +48,7 @@ def test_prefill_t4096_zipf_layer(layer_no):
         ridx = np.where(use_gpu, idx[rows], r["idx"][rows])
         rw = np.where(use_gpu, w[rows].astype(np.float64), r["weights"][rows])
         y_ref = oracle.forward_routed(shape, layer, np.ascontiguousarray(x[rows]), ridx, rw)
-        assert rel_l2(y[rows], y_ref) <= TOL_PREFILL
+        assert_close(y[rows], y_ref, TOL_PREFILL)
         assert np.isfinite(y).all()
         assert moe.status() == 0
     finally:
