@@ -59,8 +59,9 @@
  *     default: the legacy default stream). Caller buffers must stay valid until
  *     the stream reaches the call. A handle may not be used by two host threads
  *     at once; calls on one handle are serialised by its stream.
- *   - Errors found by kernels (a wait that timed out) are sticky in the handle
- *     and reported by ds4moe_status.
+ *   - Errors found by kernels (a wait that timed out, a routed index that had
+ *     to be clamped or replaced) are sticky in the handle and reported by
+ *     ds4moe_status.
  *   - NaN or Inf inputs are not checked and propagate.
  */
 #ifndef DS4MOE_H
@@ -154,9 +155,9 @@ typedef struct {
 typedef struct {
     const float *router_w;    /* [E][H] */
     const float *router_bias; /* [E] or NULL */
-    const void *gate;         /* 2-bit [E][I][H/256] */
-    const void *up;           /* 2-bit [E][I][H/256] */
-    const void *down;         /* 2-bit [E][H][I/256] */
+    const void *gate;         /* 2-bit [E][I][H/256] (MXFP4 layers: [E][I][H/32] MXFP4 blocks) */
+    const void *up;           /* 2-bit [E][I][H/256] (MXFP4 layers: [E][I][H/32]) */
+    const void *down;         /* 2-bit [E][H][I/256] (MXFP4 layers: [E][H][I/32]) */
     const void *sh_gate;      /* 8-bit [I_sh][H/32], NULL iff I_sh == 0 */
     const void *sh_up;        /* 8-bit [I_sh][H/32], NULL iff I_sh == 0 */
     const void *sh_down;      /* 8-bit [H][I_sh/32], NULL iff I_sh == 0 */
