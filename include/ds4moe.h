@@ -155,9 +155,9 @@ typedef struct {
 typedef struct {
     const float *router_w;    /* [E][H] */
     const float *router_bias; /* [E] or NULL */
-    const void *gate;         /* 2-bit [E][I][H/256] (MXFP4 layers: [E][I][H/32] MXFP4 blocks) */
-    const void *up;           /* 2-bit [E][I][H/256] (MXFP4 layers: [E][I][H/32]) */
-    const void *down;         /* 2-bit [E][H][I/256] (MXFP4 layers: [E][H][I/32]) */
+    const void *gate;         /* 2-bit [E][I][H/256] (MXFP4: [E][I][H/32] blocks; VQ: index streams) */
+    const void *up;           /* 2-bit [E][I][H/256] (MXFP4: [E][I][H/32]; VQ: index streams) */
+    const void *down;         /* 2-bit [E][H][I/256] (MXFP4: [E][H][I/32]; VQ: index streams) */
     const void *sh_gate;      /* 8-bit [I_sh][H/32], NULL iff I_sh == 0 */
     const void *sh_up;        /* 8-bit [I_sh][H/32], NULL iff I_sh == 0 */
     const void *sh_down;      /* 8-bit [H][I_sh/32], NULL iff I_sh == 0 */
