@@ -52,8 +52,8 @@ def parse():
     ap.add_argument("--crossover", action="store_true",
                     help="time the decode and the prefill path on the decode layer for T = 1..64 and print "
                          "one JSON line of the per-T medians (not a bench line)")
-    ap.add_argument("--routed-format", default="q2", choices=["q2", "mx4"],
-                    help="routed experts in the 2-bit format or in MXFP4 (Q8 activations)")
+    ap.add_argument("--routed-format", default="q2", choices=["q2", "mx4", "vq12", "vq13"],
+                    help="routed experts in the 2-bit format, in MXFP4 (Q8 activations) or VQ with 12/13-bit indices")
     ap.add_argument("--gains", type=int, default=0, choices=[0, 1, 2],
                     help="per-expert down-gain tables (sidecar, post-training) on every layer")
     return ap.parse_args()
@@ -67,13 +67,14 @@ Q8_BPW = 34 / 32
 
 GAIN_BPC = 17 / 32  # bytes per output channel of one down-gain table
 MX4_BPW = 17 / 32  # bytes per MXFP4 weight
+VQ_BITS = {"vq12": 12, "vq13": 13}  # index bits per 8 weights
 
 
 def layer_bytes(shape, T, U, gains=0, fmt="q2"):
     """Bytes the layer must move per call: selected experts (and their down-gain
     blocks), shared expert, router, x in, y out."""
     H, I, E, Ish = shape.hidden, shape.inter, shape.n_experts, shape.shared_inter
-    bpw = MX4_BPW if fmt == "mx4" else Q2_BPW
+    bpw = {"mx4": MX4_BPW, "vq12": 12 / 64, "vq13": 13 / 64}.get(fmt, Q2_BPW)
     return (U * 3 * H * I * bpw + gains * U * H * GAIN_BPC + 3 * H * Ish * Q8_BPW + 4 * E * H + 2 * T * H
             + 4 * T * H)
 
@@ -100,6 +101,9 @@ def kernel_bytes(name, shape, T, U, gains=0, fmt="q2"):
         # MXFP4 experts: weights of the distinct experts, fp32 activation rows in, results out
         "mx4_gateup": U * 2 * I * H * MX4_BPW + 4 * T * H + 4 * P * I,
         "mx4_down": U * H * I * MX4_BPW + 4 * P * I + 4 * P * H,
+        # VQ experts: index streams (+ bit planes) and row gains of the distinct experts
+        "vq_gateup": U * 2 * I * H * VQ_BITS.get(fmt, 12) / 64 + U * 2 * I * 2 + 4 * T * H + 4 * P * I,
+        "vq_down": U * H * I * VQ_BITS.get(fmt, 12) / 64 + U * H * 2 + 4 * P * I + 4 * P * H,
     }
     return table.get(name)
 
@@ -257,7 +261,9 @@ class ClockSampler:
 def workload_layers(name, gains=0, fmt="q2"):
     import synth
     wl = synth.WORKLOADS[name]
-    return wl, [synth.make_layer(wl.shape, s, zipf=wl.zipf, gains=gains, routed_format=fmt) for s in wl.layer_seeds]
+    kind = "vq" if fmt in VQ_BITS else fmt
+    return wl, [synth.make_layer(wl.shape, s, zipf=wl.zipf, gains=gains, routed_format=kind,
+                                 vq_bits=VQ_BITS.get(fmt, 12)) for s in wl.layer_seeds]
 
 
 def workload_batches(name):
@@ -369,8 +375,10 @@ def workload_config(wl, name, l2_note, gains=0, fmt="q2"):
     cfg = {"workload": name, "description": wl.description, "hidden": s.hidden, "inter": s.inter,
            "n_experts": s.n_experts, "top_k": s.top_k, "shared_inter": s.shared_inter,
            "tokens_per_step": wl.tokens, "layers_per_step": wl.n_layers,
-           "weights": ("routed MXFP4 17B/32 blocks on Q8 activations" if fmt == "mx4" else "routed 2-bit 84B/256 blocks")
-           + ", shared 8-bit 34B/32 blocks, router fp32"}
+           "weights": {"mx4": "routed MXFP4 17B/32 blocks on Q8 activations",
+                       "vq12": "routed VQ, 12-bit indices per 8 weights into a 4096 x 8 E4M3 codebook, f16 row gains",
+                       "vq13": "routed VQ, 13-bit indices per 8 weights into an 8192 x 8 E4M3 codebook, f16 row gains"
+                       }.get(fmt, "routed 2-bit 84B/256 blocks") + ", shared 8-bit 34B/32 blocks, router fp32"}
     if gains:
         cfg["down_gain_tables"] = gains
         cfg["weights"] += f", {gains} down-gain table(s) of 17B/32-channel FP4 blocks"
@@ -618,7 +626,8 @@ def make_handles(layers, shape, dev, max_tokens, fmt, stream):
     for layer in layers:
         w = {k: (None if v is None else torch.from_numpy(np.ascontiguousarray(v)).to(dev)) for k, v in layer.items()
              if v is None or isinstance(v, np.ndarray)}
-        handles.append(ds4.MoELayer(shape, w, max_tokens=max_tokens, flags=ds4.FLAG_MXFP4 if fmt == "mx4" else 0))
+        flags = {"mx4": ds4.FLAG_MXFP4, "vq12": ds4.FLAG_VQ12, "vq13": ds4.FLAG_VQ13}.get(fmt, 0)
+        handles.append(ds4.MoELayer(shape, w, max_tokens=max_tokens, flags=flags))
         del w
     torch.cuda.empty_cache()
     for m in handles:

@@ -74,7 +74,7 @@ extern "C" {
 #endif
 
 #define DS4MOE_MAGIC 0x454D3444u /* "D4ME" */
-#define DS4MOE_VERSION 2u /* 2: ds4moe_weights gained down_gain, down_gain2 */
+#define DS4MOE_VERSION 3u /* 2: ds4moe_weights gained down_gain, down_gain2; 3: the VQ fields */
 
 enum {
     DS4MOE_OK = 0,
@@ -106,6 +106,23 @@ enum {
 #define DS4MOE_FLAG_MXFP4 1u
 
 /*
+ * Layer flags: the routed experts are vector-quantised ("YoungAi - DeepSeek
+ * V4.1 Flash on one DGX Spark", section 4.1): every 8 consecutive weights of a
+ * row are one codeword of a per-layer codebook (2^bits entries of 8 OCP FP8
+ * E4M3 values, shared by all experts and the three matrices) times one
+ * binary16 gain per row, w[r, 8j .. 8j+7] = g_r * C[idx[r, j]].
+ *   gate, up, down: per expert the index stream of the matrix, its rows back
+ *     to back (row r, group j = index r * K/8 + j), 12 bits per index, least
+ *     significant bit first (index k at bits 12k .. 12k+11): I*H*3/16 bytes
+ *     per expert for gate and up, H*I*3/16 for down;
+ *   *_plane: 13-bit layers, bit k (least significant first) = bit 12 of index k;
+ *   *_rowgain: binary16 g_r per row; vq_codebook: entry n at bytes 8n .. 8n+7.
+ * Activations are not quantised. Such a layer runs one path for every T.
+ */
+#define DS4MOE_FLAG_VQ12 2u
+#define DS4MOE_FLAG_VQ13 4u
+
+/*
  * Largest T for which DS4MOE_PATH_AUTO takes the decode path (launches of up to
  * 8 tokens): the measured crossover of the two paths on a GB300 at H=4096,
  * I=2048, E=384, top-6 (decode faster up to T=12, prefill from T=16).
@@ -131,21 +148,29 @@ typedef struct {
     int32_t top_k;        /* K, 1..min(E, 8) */
     int32_t shared_inter; /* I_sh, multiple of 256, or 0 for no shared expert */
     int32_t max_tokens;   /* largest T any call will pass, 1..65536 */
-    uint32_t flags;       /* 0 or DS4MOE_FLAG_MXFP4 */
+    uint32_t flags;       /* 0 or one of DS4MOE_FLAG_MXFP4, DS4MOE_FLAG_VQ12, DS4MOE_FLAG_VQ13 */
 } ds4moe_layer_desc;
 
 /* Device pointers to the weights in the storage formats above. */
 typedef struct {
     const float *router_w;    /* [E][H] */
     const float *router_bias; /* [E] or NULL */
-    const void *gate;         /* 2-bit [E][I][H/256] (MXFP4 layers: [E][I][H/32] MXFP4 blocks) */
-    const void *up;           /* 2-bit [E][I][H/256] (MXFP4 layers: [E][I][H/32]) */
-    const void *down;         /* 2-bit [E][H][I/256] (MXFP4 layers: [E][H][I/32]) */
+    const void *gate;         /* 2-bit [E][I][H/256] (MXFP4: [E][I][H/32] blocks; VQ: index streams) */
+    const void *up;           /* 2-bit [E][I][H/256] (MXFP4: [E][I][H/32]; VQ: index streams) */
+    const void *down;         /* 2-bit [E][H][I/256] (MXFP4: [E][H][I/32]; VQ: index streams) */
     const void *sh_gate;      /* 8-bit [I_sh][H/32], NULL iff I_sh == 0 */
     const void *sh_up;        /* 8-bit [I_sh][H/32], NULL iff I_sh == 0 */
     const void *sh_down;      /* 8-bit [H][I_sh/32], NULL iff I_sh == 0 */
     const void *down_gain;    /* gain blocks [E][H/32] (sidecar), or NULL */
     const void *down_gain2;   /* gain blocks [E][H/32] (post-training), or NULL */
+    /* VQ layers only (DS4MOE_FLAG_VQ12 / DS4MOE_FLAG_VQ13), else NULL: */
+    const void *vq_codebook;  /* 2^bits x 8 E4M3 bytes */
+    const void *gate_plane;   /* bit planes [E][I*H/64] bytes (13-bit only, else NULL) */
+    const void *up_plane;     /* [E][I*H/64] */
+    const void *down_plane;   /* [E][H*I/64] */
+    const void *gate_rowgain; /* binary16 [E][I] */
+    const void *up_rowgain;   /* binary16 [E][I] */
+    const void *down_rowgain; /* binary16 [E][H] */
 } ds4moe_weights;
 
 /*

@@ -338,7 +338,7 @@ def expert_vq(shape, layer: dict, e: int, xt: np.ndarray) -> np.ndarray:
     ye = np.empty(shape.hidden, dtype=np.float64)
     s = _shape(shape)
     mats, keep = _vq_mats(layer)
-    cb = np.ascontiguousarray(layer["codebook"], dtype=np.uint8)
+    cb = np.ascontiguousarray(layer["vq_codebook"], dtype=np.uint8)
     _load().oracle_expert_vq(ctypes.byref(s), _p(cb), *(ctypes.byref(m) for m in mats), e, _p(xt), _p(ye))
     return ye
 
@@ -360,7 +360,7 @@ def forward_routed(shape, layer: dict, x_bf16: np.ndarray, idx: np.ndarray, weig
               _p(layer.get("down_gain2")), _p(x), T, _p(idx), _p(weights), _p(y), nthreads)
     if layer.get("routed_format", "q2") == "vq":
         mats, keep = _vq_mats(layer)
-        cb = np.ascontiguousarray(layer["codebook"], dtype=np.uint8)
+        cb = np.ascontiguousarray(layer["vq_codebook"], dtype=np.uint8)
         rc = _load().oracle_forward_routed_vq(ctypes.byref(s), _p(cb), *(ctypes.byref(m) for m in mats),
                                               *common[3:])
     elif layer.get("routed_format", "q2") == "mx4":

@@ -16,7 +16,7 @@ import os
 from ._build import INCLUDE, LIB_PATH, NVCC_FLAGS, build, sources  # noqa: F401
 
 DS4MOE_MAGIC = 0x454D3444
-DS4MOE_VERSION = 2
+DS4MOE_VERSION = 3
 DS4MOE_OK, DS4MOE_EINVAL, DS4MOE_ENOMEM, DS4MOE_ECUDA, DS4MOE_EUNSUPPORTED, DS4MOE_ETIMEOUT, DS4MOE_EDEVICE = (
     0, -1, -2, -3, -4, -5, -6)
 DS4MOE_ESCRATCH = -7
@@ -24,6 +24,7 @@ DS4MOE_NOALLOC_SCRATCH = 4 << 20
 PATH_AUTO, PATH_DECODE, PATH_PREFILL = 0, 1, 2
 AUTO_DECODE_MAX_T = 12
 FLAG_MXFP4 = 1
+FLAG_VQ12, FLAG_VQ13 = 2, 4
 
 
 class LayerDesc(ctypes.Structure):
@@ -36,7 +37,9 @@ class Weights(ctypes.Structure):
     _fields_ = [("router_w", ctypes.c_void_p), ("router_bias", ctypes.c_void_p), ("gate", ctypes.c_void_p),
                 ("up", ctypes.c_void_p), ("down", ctypes.c_void_p), ("sh_gate", ctypes.c_void_p),
                 ("sh_up", ctypes.c_void_p), ("sh_down", ctypes.c_void_p), ("down_gain", ctypes.c_void_p),
-                ("down_gain2", ctypes.c_void_p)]
+                ("down_gain2", ctypes.c_void_p), ("vq_codebook", ctypes.c_void_p), ("gate_plane", ctypes.c_void_p),
+                ("up_plane", ctypes.c_void_p), ("down_plane", ctypes.c_void_p), ("gate_rowgain", ctypes.c_void_p),
+                ("up_rowgain", ctypes.c_void_p), ("down_rowgain", ctypes.c_void_p)]
 
 
 class Stats(ctypes.Structure):
@@ -218,17 +221,16 @@ def make_desc(hidden, inter, n_experts, top_k, shared_inter, max_tokens, flags=0
 
 class MoELayer:
     """One ds4moe handle. Weights: dict of device torch tensors in the storage
-    formats of ``include/ds4moe.h`` (keys router_w, router_bias, gate, up, down,
-    sh_gate, sh_up, sh_down, down_gain, down_gain2; router_bias, the shared ones
-    and the gain tables may be None or absent)."""
+    formats of ``include/ds4moe.h``, keyed by the ``ds4moe_weights`` field names
+    (router_w, router_bias, gate, up, down, sh_gate, sh_up, sh_down, down_gain,
+    down_gain2, and for VQ layers vq_codebook, *_plane, *_rowgain); optional
+    ones may be None or absent."""
 
     def __init__(self, shape, weights: dict, max_tokens: int, flags: int = 0):
         self.shape = shape
         desc = make_desc(shape.hidden, shape.inter, shape.n_experts, shape.top_k, shape.shared_inter, max_tokens,
                          flags)
-        w = Weights(*(_addr(weights.get(k)) for k in
-                      ("router_w", "router_bias", "gate", "up", "down", "sh_gate", "sh_up", "sh_down", "down_gain",
-                       "down_gain2")))
+        w = Weights(*(_addr(weights.get(k)) for k, _ in Weights._fields_))
         self.handle = ds4moe_create(desc, w)
         self.max_tokens = max_tokens
 

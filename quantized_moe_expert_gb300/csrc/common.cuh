@@ -155,8 +155,8 @@ struct Scratch {
     float *ysh;        // [Tmax][H]
     uint16_t *xstage;  // [Tmax][H] bf16 staging for host-memory calls
     float *ystage;     // [Tmax][H]
-    float *ax;         // MXFP4 layers: [Tmax][H] Q8-quantised token rows (d * q)
-    float *hf;         // MXFP4 layers: [Tmax*K][I] fp32 SwiGLU rows, expert-grouped order
+    float *ax;         // MXFP4 layers: [Tmax][H] Q8-quantised token rows (d * q); VQ layers: x in fp32
+    float *hf;         // MXFP4 and VQ layers: [Tmax*K][I] fp32 SwiGLU rows, expert-grouped order
     float *ah;         // MXFP4 layers: [Tmax*K][I] their Q8-quantised values
 };
 
@@ -169,6 +169,16 @@ struct Mx4Mat {
     int32_t nb; // 32-weight blocks per row
 };
 
+// VQ weights of one matrix: per expert the index stream, the bit plane
+// (13-bit layers) and the binary16 row gains.
+struct VqMat {
+    const uint32_t *stream; // [E][rows * k * 3 / 64] words
+    const uint8_t *plane;   // [E][rows * k / 64] or nullptr
+    const uint16_t *gain;   // [E][rows]
+    int64_t rows;           // rows per expert
+    int32_t k;              // weights per row
+};
+
 struct LayerDev {
     int H, I, E, K, Ish, Tmax;
     const float *router_w;
@@ -179,6 +189,9 @@ struct LayerDev {
     const float *gain; // [E][H] per-expert down gains s1 * s2 expanded from the tables, or nullptr
     bool mx4;          // routed experts in MXFP4 (mgate, mup, mdown) instead of 2-bit
     Mx4Mat mgate, mup, mdown;
+    int vq;            // 12 or 13: routed experts vector-quantised (vgate, vup, vdown, codebook); 0: not
+    VqMat vgate, vup, vdown;
+    const uint8_t *codebook; // [2^vq][8] E4M3
 };
 
 } // namespace ds4

@@ -18,6 +18,7 @@
 #include "frag_layout.cuh"
 #include "dispatch.cuh"
 #include "mx4_experts.cuh"
+#include "vq_experts.cuh"
 #include "prefill_gemm.cuh"
 #include "router.cuh"
 
@@ -140,7 +141,9 @@ bool is_device_ptr(const void *p) {
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 int check_desc(const ds4moe_layer_desc *d) {
-    if (!d || d->magic != DS4MOE_MAGIC || d->version != DS4MOE_VERSION || (d->flags & ~DS4MOE_FLAG_MXFP4) != 0)
+    if (!d || d->magic != DS4MOE_MAGIC || d->version != DS4MOE_VERSION ||
+        (d->flags != 0 && d->flags != DS4MOE_FLAG_MXFP4 && d->flags != DS4MOE_FLAG_VQ12 &&
+         d->flags != DS4MOE_FLAG_VQ13))
         return DS4MOE_EINVAL;
     if (d->hidden <= 0 || d->hidden % 256 || d->inter <= 0 || d->inter % 256)
         return DS4MOE_EINVAL;
@@ -292,7 +295,20 @@ void layout_weights(ds4moe *h, Carver &c) {
         m.codes = c.take<uint4>((uint64_t)rows * m.nb);
         m.scale = c.take<uint8_t>((uint64_t)rows * m.nb);
     };
-    if (L.mx4) {
+    auto vqm = [&](VqMat &m, int64_t rows, int k) {
+        m.rows = rows;
+        m.k = k;
+        const uint64_t n = (uint64_t)L.E * rows * (k / 8); // indices of all experts
+        m.stream = c.take<uint32_t>(n * 12 / 32);
+        m.plane = L.vq == 13 ? c.take<uint8_t>(n / 8) : nullptr;
+        m.gain = c.take<uint16_t>((uint64_t)L.E * rows);
+    };
+    if (L.vq) {
+        vqm(L.vgate, L.I, L.H);
+        vqm(L.vup, L.I, L.H);
+        vqm(L.vdown, L.H, L.I);
+        L.codebook = c.take<uint8_t>((uint64_t)8 << L.vq);
+    } else if (L.mx4) {
         m4(L.mgate, (int64_t)L.E * L.I, L.H);
         m4(L.mup, (int64_t)L.E * L.I, L.H);
         m4(L.mdown, (int64_t)L.E * L.H, L.I);
@@ -318,8 +334,8 @@ void layout_weights(ds4moe *h, Carver &c) {
         m.nbq = k / 32;
         m.rec = c.take<uint8_t>((uint64_t)(rows / 16) * m.nbq * kQ8Rec);
     };
-    if (L.mx4)
-        return; // MXFP4 layers do not use the fused decode kernel or its layouts
+    if (L.mx4 || L.vq)
+        return; // MXFP4 and VQ layers do not use the fused decode kernel or its layouts
     f2(D.gate, (int64_t)L.E * L.I, L.H);
     f2(D.up, (int64_t)L.E * L.I, L.H);
     f2(D.down, (int64_t)L.E * L.H, L.I);
@@ -363,8 +379,8 @@ void layout_scratch(ds4moe *h, Carver &c) {
     S.ysh = c.take<float>(T * L.H);
     S.xstage = c.take<uint16_t>(T * L.H);
     S.ystage = c.take<float>(T * L.H);
-    S.ax = L.mx4 ? c.take<float>(T * L.H) : nullptr;
-    S.hf = L.mx4 ? c.take<float>(P * L.I) : nullptr;
+    S.ax = L.mx4 || L.vq ? c.take<float>(T * L.H) : nullptr;
+    S.hf = L.mx4 || L.vq ? c.take<float>(P * L.I) : nullptr;
     S.ah = L.mx4 ? c.take<float>(P * L.I) : nullptr;
     DecodeState &D = h->D;
     const int64_t Td = kDecodeT, Pd = (int64_t)kDecodeT * L.K;
@@ -690,6 +706,58 @@ int run_experts_mx4(ds4moe *h, const void *x, int T, float *y) {
     return launch_rc();
 }
 
+// VQ routed experts for the routing already in S.idx / S.w, every T: x in fp32,
+// the gate/up product with SwiGLU, the down product, the shared expert, the
+// combine. The product kernels are persistent (two CTAs per SM) and load the
+// codebook into shared memory once per CTA.
+int run_experts_vq(ds4moe *h, const void *x, int T, float *y) {
+    const LayerDev &L = h->L;
+    Scratch &S = h->S;
+    cudaStream_t st = h->stream;
+    int rc = run_dispatch(h, T);
+    if (rc)
+        return rc;
+    const int P = T * L.K;
+    const int U = P < L.E ? P : L.E; // bound on the distinct experts
+    const int nt = T <= 1 ? 1 : T <= 2 ? 2 : T <= 4 ? 4 : 8;
+    const int entries = 1 << L.vq;
+    const size_t smem = (size_t)8 << L.vq;
+    launch(h, "vq_widen_x", [&] {
+        widen_bf16_kernel<<<blocks_for((int64_t)T * L.H, 256), 256, 0, st>>>(static_cast<const uint16_t *>(x),
+                                                                              (int64_t)T * L.H, S.ax);
+    });
+    launch(h, "vq_gateup", [&] {
+        const int work = U * ((L.I + 7) / 8);
+        const int grid = work < 2 * g_pf_grid ? work : 2 * g_pf_grid;
+        auto k = nt == 1   ? vq_product_kernel<true, 1>
+                 : nt == 2 ? vq_product_kernel<true, 2>
+                 : nt == 4 ? vq_product_kernel<true, 4>
+                           : vq_product_kernel<true, 8>;
+        k<<<grid, 256, smem, st>>>(L.vgate, L.vup, L.codebook, entries, S.ax, S.uexp, S.uoff, S.nuniq, S.perm, L.K,
+                                   L.I, L.H, U, S.hf);
+    });
+    launch(h, "vq_down", [&] {
+        const int work = U * ((L.H + 7) / 8);
+        const int grid = work < 2 * g_pf_grid ? work : 2 * g_pf_grid;
+        auto k = nt == 1   ? vq_product_kernel<false, 1>
+                 : nt == 2 ? vq_product_kernel<false, 2>
+                 : nt == 4 ? vq_product_kernel<false, 4>
+                           : vq_product_kernel<false, 8>;
+        k<<<grid, 256, smem, st>>>(L.vdown, L.vdown, L.codebook, entries, S.hf, S.uexp, S.uoff, S.nuniq, S.perm, L.K,
+                                   L.H, L.I, U, S.ye);
+    });
+    if (L.Ish > 0) {
+        rc = run_shared_gemms(h, x, T);
+        if (rc)
+            return rc;
+    }
+    launch(h, "combine", [&] {
+        combine_kernel<<<blocks_for((int64_t)T * L.H / 4, 256), 256, 0, st>>>(
+            S.ye, L.Ish > 0 ? S.ysh : nullptr, S.w, S.inv, S.idx, L.gain, T, L.H, L.K, y);
+    });
+    return launch_rc();
+}
+
 // The fused decode kernel over tokens [0, T) in launches of up to 8 tokens.
 // forced_idx/forced_w: caller routing (nullptr = route here). idx_out/w_out
 // receive the routing of every token ([T][K]).
@@ -781,9 +849,9 @@ int forward_impl(ds4moe *h, const void *x, int T, int path, float *y) {
     if (path == DS4MOE_PATH_AUTO)
         path = T <= DS4MOE_AUTO_DECODE_MAX_T ? DS4MOE_PATH_DECODE : DS4MOE_PATH_PREFILL;
     h->stats.path = path;
-    if (h->L.mx4) { // one path for every T
+    if (h->L.mx4 || h->L.vq) { // one path for every T
         int rc = run_router(h, x, T, nullptr);
-        return rc ? rc : run_experts_mx4(h, x, T, y);
+        return rc ? rc : h->L.vq ? run_experts_vq(h, x, T, y) : run_experts_mx4(h, x, T, y);
     }
     if (path == DS4MOE_PATH_DECODE)
         return run_decode(h, x, T, y, nullptr, nullptr);
@@ -826,6 +894,19 @@ int ds4moe_create(const ds4moe_layer_desc *desc, const ds4moe_weights *w, ds4moe
         return DS4MOE_EINVAL;
     if ((w->down_gain && !is_device_ptr(w->down_gain)) || (w->down_gain2 && !is_device_ptr(w->down_gain2)))
         return DS4MOE_EINVAL;
+    {
+        const int vq = desc->flags == DS4MOE_FLAG_VQ12 ? 12 : desc->flags == DS4MOE_FLAG_VQ13 ? 13 : 0;
+        const void *rowgains[3] = {w->gate_rowgain, w->up_rowgain, w->down_rowgain};
+        const void *planes[3] = {w->gate_plane, w->up_plane, w->down_plane};
+        if ((vq != 0) != (w->vq_codebook != nullptr) || (vq && !is_device_ptr(w->vq_codebook)))
+            return DS4MOE_EINVAL;
+        for (int m = 0; m < 3; m++) {
+            if ((vq != 0) != (rowgains[m] != nullptr) || (vq && !is_device_ptr(rowgains[m])))
+                return DS4MOE_EINVAL;
+            if ((vq == 13) != (planes[m] != nullptr) || (vq == 13 && !is_device_ptr(planes[m])))
+                return DS4MOE_EINVAL;
+        }
+    }
     const bool has_shared = desc->shared_inter > 0;
     if (has_shared != (w->sh_gate != nullptr) || has_shared != (w->sh_up != nullptr) ||
         has_shared != (w->sh_down != nullptr))
@@ -858,6 +939,7 @@ int ds4moe_create(const ds4moe_layer_desc *desc, const ds4moe_weights *w, ds4moe
     L.Ish = desc->shared_inter;
     L.Tmax = desc->max_tokens;
     L.mx4 = (desc->flags & DS4MOE_FLAG_MXFP4) != 0;
+    L.vq = desc->flags == DS4MOE_FLAG_VQ12 ? 12 : desc->flags == DS4MOE_FLAG_VQ13 ? 13 : 0;
     h->has_gain[0] = w->down_gain != nullptr;
     h->has_gain[1] = w->down_gain2 != nullptr;
 
@@ -925,7 +1007,21 @@ int ds4moe_create(const ds4moe_layer_desc *desc, const ds4moe_weights *w, ds4moe
                                                                  const_cast<uint4 *>(m.codes),
                                                                  const_cast<uint8_t *>(m.scale));
     };
-    if (L.mx4) {
+    auto cvq = [&](const void *stream, const void *plane, const void *rowgain, VqMat &m) {
+        const uint64_t n = (uint64_t)L.E * m.rows * (m.k / 8);
+        cudaMemcpyAsync(const_cast<uint32_t *>(m.stream), stream, n * 12 / 8, cudaMemcpyDeviceToDevice, st);
+        if (m.plane)
+            cudaMemcpyAsync(const_cast<uint8_t *>(m.plane), plane, n / 8, cudaMemcpyDeviceToDevice, st);
+        cudaMemcpyAsync(const_cast<uint16_t *>(m.gain), rowgain, (uint64_t)L.E * m.rows * 2, cudaMemcpyDeviceToDevice,
+                        st);
+    };
+    if (L.vq) {
+        cvq(w->gate, w->gate_plane, w->gate_rowgain, L.vgate);
+        cvq(w->up, w->up_plane, w->up_rowgain, L.vup);
+        cvq(w->down, w->down_plane, w->down_rowgain, L.vdown);
+        cudaMemcpyAsync(const_cast<uint8_t *>(L.codebook), w->vq_codebook, (size_t)8 << L.vq, cudaMemcpyDeviceToDevice,
+                        st);
+    } else if (L.mx4) {
         rm4(w->gate, L.mgate);
         rm4(w->up, L.mup);
         rm4(w->down, L.mdown);
@@ -954,7 +1050,7 @@ int ds4moe_create(const ds4moe_layer_desc *desc, const ds4moe_weights *w, ds4moe
         repack_q8_frag_kernel<<<blocks_for(n, 256), 256, 0, st>>>(static_cast<const uint8_t *>(src), m.rows, m.nbq,
                                                                    const_cast<uint8_t *>(m.rec));
     };
-    if (!L.mx4) {
+    if (!L.mx4 && !L.vq) {
         rf2(w->gate, D.gate);
         rf2(w->up, D.up);
         rf2(w->down, D.down);
@@ -975,6 +1071,11 @@ int ds4moe_create(const ds4moe_layer_desc *desc, const ds4moe_weights *w, ds4moe
                            (const void *)decode_fused_kernel<4>, (const void *)decode_fused_kernel<8>,
                            (const void *)decode_fused_kernel<1, true>, (const void *)decode_fused_kernel<8, true>})
         cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(DecodeSmem));
+    for (const void *fn : {(const void *)vq_product_kernel<true, 1>, (const void *)vq_product_kernel<true, 2>,
+                           (const void *)vq_product_kernel<true, 4>, (const void *)vq_product_kernel<true, 8>,
+                           (const void *)vq_product_kernel<false, 1>, (const void *)vq_product_kernel<false, 2>,
+                           (const void *)vq_product_kernel<false, 4>, (const void *)vq_product_kernel<false, 8>})
+        cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, 8 << 13);
     // every variant has the same threads and shared memory and the same launch bound of two CTAs per SM
     cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_fused_kernel<8>, kDecodeThreads, sizeof(DecodeSmem));
     cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
@@ -1087,14 +1188,14 @@ int ds4moe_forward_routed(ds4moe_t *h, const void *x, int32_t T, const int32_t *
     h->stats.tokens = T;
     h->stats.path = path == DS4MOE_PATH_AUTO ? (T <= DS4MOE_AUTO_DECODE_MAX_T ? DS4MOE_PATH_DECODE : DS4MOE_PATH_PREFILL)
                                              : path;
-    if (h->stats.path == DS4MOE_PATH_DECODE && !L.mx4)
+    if (h->stats.path == DS4MOE_PATH_DECODE && !L.mx4 && !L.vq)
         return run_decode(h, x, T, y, idx, w);
     cudaMemcpyAsync(S.idx, idx, sizeof(int32_t) * T * L.K, cudaMemcpyDeviceToDevice, st);
     cudaMemcpyAsync(S.w, w, sizeof(float) * T * L.K, cudaMemcpyDeviceToDevice, st);
     rc = launch_rc();
     if (rc)
         return rc;
-    return L.mx4 ? run_experts_mx4(h, x, T, y) : run_experts_prefill(h, x, T, y);
+    return L.vq ? run_experts_vq(h, x, T, y) : L.mx4 ? run_experts_mx4(h, x, T, y) : run_experts_prefill(h, x, T, y);
 }
 
 int ds4moe_forward_host(ds4moe_t *h, const void *x_host, int32_t T, float *y_host) {
@@ -1149,7 +1250,7 @@ int ds4moe_get_stats(ds4moe_t *h, ds4moe_stats *out) {
     if (h->stats.tokens > 0) {
         // the fused decode kernel keeps its own grouping; every other path (and every
         // MXFP4 layer) the dispatch kernels'
-        const bool dec = h->stats.path == DS4MOE_PATH_DECODE && !h->L.mx4;
+        const bool dec = h->stats.path == DS4MOE_PATH_DECODE && !h->L.mx4 && !h->L.vq;
         int32_t n = 0;
         cudaMemcpy(&n, dec ? h->D.nuniq : h->S.nuniq, sizeof(int32_t), cudaMemcpyDeviceToHost);
         out->n_unique = n;

@@ -278,7 +278,7 @@ def make_layer(shape: Shape, seed: int, zipf: bool = False, zipf_beta_value: flo
         assert vq_bits in (12, 13)
         layer["routed_format"] = "vq"
         layer["vq_bits"] = vq_bits
-        layer["codebook"] = e4m3_codebook(1 << vq_bits, seed)
+        layer["vq_codebook"] = e4m3_codebook(1 << vq_bits, seed)
         for name, rows, k, s_idx, s_plane, s_gain in (("gate", I, H, S_GATE, S_GATE_PLANE, S_GATE_ROWGAIN),
                                                       ("up", I, H, S_UP, S_UP_PLANE, S_UP_ROWGAIN),
                                                       ("down", H, I, S_DOWN, S_DOWN_PLANE, S_DOWN_ROWGAIN)):

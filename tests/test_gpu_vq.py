@@ -1,0 +1,105 @@
+"""GPU parity of layers with VQ-12/13 routed experts (DS4MOE_FLAG_VQ12/VQ13).
+
+Every 8 weights of a row are a codeword of the layer's E4M3 codebook times a
+binary16 row gain; activations are not quantised, so the bound is the decode
+path's. Every compute call goes through the C ABI.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import quantized_moe_expert_gb300 as ds4
+import synth
+from gpu_util import TOL_DECODE, check_routing, rel_l2, to_dev, x_to_dev
+
+pytestmark = pytest.mark.gpu
+
+FLAGS = {12: ds4.FLAG_VQ12, 13: ds4.FLAG_VQ13}
+
+
+def tokens(shape, T, seed):
+    return synth.normal_bf16(T * shape.hidden, seed, synth.S_X).reshape(T, shape.hidden)
+
+
+@pytest.fixture(scope="module", params=[12, 13])
+def tiny(request):
+    bits = request.param
+    wl = synth.WORKLOADS["tiny"]
+    layer = synth.make_layer(wl.shape, wl.layer_seeds[0], routed_format="vq", vq_bits=bits)
+    moe = ds4.MoELayer(wl.shape, to_dev(layer), max_tokens=80, flags=FLAGS[bits])
+    yield wl.shape, layer, moe
+    moe.close()
+
+
+@pytest.mark.parametrize("T", [1, 3, 8, 13, 80])
+def test_forward_matches_oracle(tiny, T):
+    shape, layer, moe = tiny
+    x = tokens(shape, T, 1500 + T)
+    xd = x_to_dev(x)
+    y = moe.forward(xd).cpu().numpy()
+    s = moe.stats()
+    idx, w, gap, _ = moe.route(xd)
+    assert s.tokens == T and s.n_unique == len(np.unique(idx.cpu().numpy()))
+    y_ref, r = oracle.forward(shape, layer, x)
+    near = check_routing(idx.cpu().numpy(), w.cpu().numpy(), gap.cpu().numpy(), r, shape.top_k)
+    if near.any():
+        y_ref = oracle.forward_routed(shape, layer, x, idx.cpu().numpy(), w.cpu().numpy().astype(np.float64))
+    assert rel_l2(y, y_ref) <= TOL_DECODE
+    assert moe.status() == 0
+
+
+def test_forward_routed_with_gains(tiny):
+    shape, layer, _ = tiny
+    L = dict(layer)
+    L["down_gain"] = synth.gain_table(shape.n_experts, shape.hidden, 13, synth.S_GAIN1, 127 - 2)
+    bits = layer["vq_bits"]
+    moe = ds4.MoELayer(shape, to_dev(L), max_tokens=16, flags=FLAGS[bits])
+    try:
+        rng = np.random.default_rng(10)
+        T = 6
+        x = tokens(shape, T, 1601)
+        idx = np.stack([rng.choice(shape.n_experts, shape.top_k, replace=False) for _ in range(T)]).astype(np.int32)
+        w = rng.random((T, shape.top_k)).astype(np.float32)
+        y = moe.forward_routed(x_to_dev(x), torch.from_numpy(idx).cuda(), torch.from_numpy(w).cuda()).cpu().numpy()
+        y_ref = oracle.forward_routed(shape, L, x, idx, w.astype(np.float64))
+        assert rel_l2(y, y_ref) <= TOL_DECODE
+        assert moe.status() == 0
+    finally:
+        moe.close()
+
+
+def test_create_checks_the_vq_fields():
+    wl = synth.WORKLOADS["tiny"]
+    layer = synth.make_layer(wl.shape, wl.layer_seeds[0], routed_format="vq", vq_bits=12)
+    dev = to_dev(layer)
+    missing = dict(dev)
+    missing.pop("gate_rowgain")
+    with pytest.raises(ds4.DS4MoEError):
+        ds4.MoELayer(wl.shape, missing, max_tokens=8, flags=ds4.FLAG_VQ12)
+    with pytest.raises(ds4.DS4MoEError):  # a 12-bit layer given as 13-bit: no planes
+        ds4.MoELayer(wl.shape, dev, max_tokens=8, flags=ds4.FLAG_VQ13)
+
+
+@pytest.fixture(scope="module")
+def big():
+    wl = synth.WORKLOADS["decode_t1"]
+    layer = synth.make_layer(wl.shape, wl.layer_seeds[0], routed_format="vq", vq_bits=12)
+    dev = to_dev(layer)
+    moe = ds4.MoELayer(wl.shape, dev, max_tokens=8, flags=ds4.FLAG_VQ12)
+    del dev
+    torch.cuda.empty_cache()
+    yield wl.shape, layer, moe
+    moe.close()
+
+
+def test_full_size_t1_and_t8(big):
+    shape, layer, moe = big
+    for x in (synth.make_tokens("decode_t1", T=1), synth.make_tokens("decode_t8")):
+        xd = x_to_dev(x)
+        y = moe.forward(xd).cpu().numpy()
+        idx, w, gap, _ = moe.route(xd)
+        idx, w = idx.cpu().numpy(), w.cpu().numpy()
+        y_ref = oracle.forward_routed(shape, layer, x, idx, w.astype(np.float64))
+        assert rel_l2(y, y_ref) <= TOL_DECODE
+    assert moe.status() == 0

@@ -72,7 +72,7 @@ def test_reference_arm_runs_on_rank_zero_only():
     assert buf.getvalue() == ""
 
 
-@pytest.mark.parametrize("fmt,gains", [("q2", 0), ("mx4", 2)])
+@pytest.mark.parametrize("fmt,gains", [("q2", 0), ("mx4", 2), ("vq13", 1)])
 def test_reference_arm_prints_the_contract_line(fmt, gains):
     """Rank 0 of the reference arm (the oracle on the host's cores) prints one
     JSON line with the keys the benchmark contract names."""

@@ -808,7 +808,7 @@ def _vq_one_expert(H=256, I=256):
     c = np.array([2.0 ** -6 * (1 + j % 7) for j in range(H)])
     gate = _pack12([1] * (I * H // 8))
     down_idx = [1 if 8 * j < I // 2 else 2 for _ in range(H) for j in range(I // 8)]
-    layer = {"routed_format": "vq", "codebook": cb,
+    layer = {"routed_format": "vq", "vq_codebook": cb,
              "gate": gate[None], "gate_plane": None, "gate_rowgain": np.array([[f16_bits(v) for v in a]], np.uint16),
              "up": gate[None], "up_plane": None, "up_rowgain": np.array([[f16_bits(v) for v in b]], np.uint16),
              "down": _pack12(down_idx)[None], "down_plane": None,
@@ -836,7 +836,7 @@ def test_vq_layer_matches_dense_numpy(bits):
     shape = synth.Shape(512, 256, 3, 2, 0)
     layer = synth.make_layer(shape, 91, routed_format="vq", vq_bits=bits)
     layer["sh_gate"] = layer["sh_up"] = layer["sh_down"] = None
-    cbv = _e4m3_torch(layer["codebook"].reshape(-1)).reshape(-1, 8)
+    cbv = _e4m3_torch(layer["vq_codebook"].reshape(-1)).reshape(-1, 8)
 
     def dense(name, rows, k):
         out = []

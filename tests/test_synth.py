@@ -119,5 +119,5 @@ def test_vq_generators():
     g = layer["up_rowgain"].view(np.float16).astype(np.float64)
     assert (g >= 0).all() and abs(g.mean() - synth.VQ_ROWGAIN_SIGMA * np.sqrt(2 / np.pi)) < 0.01
     again = synth.make_layer(synth.Shape(512, 256, 2, 2, 0), 4, routed_format="vq", vq_bits=13)
-    assert all(np.array_equal(layer[k], again[k]) for k in ("codebook", "gate", "gate_plane", "down_rowgain"))
+    assert all(np.array_equal(layer[k], again[k]) for k in ("vq_codebook", "gate", "gate_plane", "down_rowgain"))
     assert synth.make_layer(synth.Shape(512, 256, 2, 2, 0), 4, routed_format="vq")["gate_plane"] is None
