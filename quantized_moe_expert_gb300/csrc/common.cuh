@@ -155,9 +155,12 @@ struct Scratch {
     float *ysh;        // [Tmax][H]
     uint16_t *xstage;  // [Tmax][H] bf16 staging for host-memory calls
     float *ystage;     // [Tmax][H]
-    float *ax;         // MXFP4 layers: [Tmax][H] Q8-quantised token rows (d * q); VQ layers: x in fp32
+    float *ax;         // VQ layers: [Tmax][H] x in fp32
+    int8_t *xq;        // MXFP4 layers: [Tmax][H] Q8 codes of the token rows
+    float *xd;         // MXFP4 layers: [Tmax][H/32] their block scales
     float *hf;         // MXFP4 and VQ layers: [Tmax*K][I] fp32 SwiGLU rows, expert-grouped order
-    float *ah;         // MXFP4 layers: [Tmax*K][I] their Q8-quantised values
+    int8_t *hq;        // MXFP4 layers: [Tmax*K][I] Q8 codes of the SwiGLU rows
+    float *hd;         // MXFP4 layers: [Tmax*K][I/32] their block scales
 };
 
 // MXFP4 weights: per row and 32-weight block the 16 E2M1 code bytes as one

@@ -379,9 +379,12 @@ void layout_scratch(ds4moe *h, Carver &c) {
     S.ysh = c.take<float>(T * L.H);
     S.xstage = c.take<uint16_t>(T * L.H);
     S.ystage = c.take<float>(T * L.H);
-    S.ax = L.mx4 || L.vq ? c.take<float>(T * L.H) : nullptr;
+    S.ax = L.vq ? c.take<float>(T * L.H) : nullptr;
+    S.xq = L.mx4 ? c.take<int8_t>(T * L.H) : nullptr;
+    S.xd = L.mx4 ? c.take<float>(T * (L.H / 32)) : nullptr;
     S.hf = L.mx4 || L.vq ? c.take<float>(P * L.I) : nullptr;
-    S.ah = L.mx4 ? c.take<float>(P * L.I) : nullptr;
+    S.hq = L.mx4 ? c.take<int8_t>(P * L.I) : nullptr;
+    S.hd = L.mx4 ? c.take<float>(P * (L.I / 32)) : nullptr;
     DecodeState &D = h->D;
     const int64_t Td = kDecodeT, Pd = (int64_t)kDecodeT * L.K;
     D.lgt = c.take<unsigned long long>(Td * L.E);
@@ -671,7 +674,7 @@ int run_experts_mx4(ds4moe *h, const void *x, int T, float *y) {
     const int P = T * L.K;
     const int U = P < L.E ? P : L.E; // bound on the distinct experts
     launch(h, "mx4_act_x", [&] {
-        act_q8_kernel<<<blocks_for((int64_t)T * L.H, 256), 256, 0, st>>>(x, 1, (int64_t)T * L.H, S.ax);
+        act_q8_kernel<<<blocks_for((int64_t)T * L.H, 256), 256, 0, st>>>(x, 1, (int64_t)T * L.H, S.xq, S.xd);
     });
     // an expert holds at most T rows when a token's experts are distinct; more come in chunks
     const int nt = T <= 1 ? 1 : T <= 2 ? 2 : T <= 4 ? 4 : 8;
@@ -681,10 +684,10 @@ int run_experts_mx4(ds4moe *h, const void *x, int T, float *y) {
                  : nt == 2 ? mx4_product_kernel<true, 2>
                  : nt == 4 ? mx4_product_kernel<true, 4>
                            : mx4_product_kernel<true, 8>;
-        k<<<grid, 256, 0, st>>>(L.mgate, L.mup, S.ax, S.uexp, S.uoff, S.nuniq, S.perm, L.K, L.I, L.H, S.hf);
+        k<<<grid, 256, 0, st>>>(L.mgate, L.mup, S.xq, S.xd, S.uexp, S.uoff, S.nuniq, S.perm, L.K, L.I, L.H, S.hf);
     });
     launch(h, "mx4_act_h", [&] {
-        act_q8_kernel<<<blocks_for((int64_t)P * L.I, 256), 256, 0, st>>>(S.hf, 0, (int64_t)P * L.I, S.ah);
+        act_q8_kernel<<<blocks_for((int64_t)P * L.I, 256), 256, 0, st>>>(S.hf, 0, (int64_t)P * L.I, S.hq, S.hd);
     });
     launch(h, "mx4_down", [&] {
         const dim3 grid((L.H + 7) / 8, U);
@@ -692,7 +695,7 @@ int run_experts_mx4(ds4moe *h, const void *x, int T, float *y) {
                  : nt == 2 ? mx4_product_kernel<false, 2>
                  : nt == 4 ? mx4_product_kernel<false, 4>
                            : mx4_product_kernel<false, 8>;
-        k<<<grid, 256, 0, st>>>(L.mdown, L.mdown, S.ah, S.uexp, S.uoff, S.nuniq, S.perm, L.K, L.H, L.I, S.ye);
+        k<<<grid, 256, 0, st>>>(L.mdown, L.mdown, S.hq, S.hd, S.uexp, S.uoff, S.nuniq, S.perm, L.K, L.H, L.I, S.ye);
     });
     if (L.Ish > 0) {
         rc = run_shared_gemms(h, x, T);

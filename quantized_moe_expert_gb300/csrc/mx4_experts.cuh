@@ -47,10 +47,12 @@ __global__ void repack_mx4_kernel(const uint8_t *__restrict__ src, int64_t nbloc
     scale[i] = b[16];
 }
 
-// Q8 activation blocks, dequantised: out[i] = d * q_i for the 32-value block of
-// i. One thread per value; a warp is one block (n is a multiple of 32).
-// src is bf16 (src_bf16) or fp32.
-__global__ void act_q8_kernel(const void *__restrict__ src, int src_bf16, int64_t n, float *__restrict__ out) {
+// Q8 activation blocks: per 32 values d = amax / 127 and q_i = x_i / d
+// rounded to the nearest integer (ties to even), both IEEE binary32 (the build
+// has no fast-math flags). One thread per value, a warp per block (n is a
+// multiple of 32); codes to q, block scales to d. src is bf16 (src_bf16) or fp32.
+__global__ void act_q8_kernel(const void *__restrict__ src, int src_bf16, int64_t n, int8_t *__restrict__ q,
+                              float *__restrict__ d) {
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (i - (threadIdx.x & 31) >= n) // whole warps past the end
         return;
@@ -61,30 +63,42 @@ __global__ void act_q8_kernel(const void *__restrict__ src, int src_bf16, int64_
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1)
         amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
-    const float d = amax / 127.0f; // IEEE division: the build does not use fast math
-    const float q = d > 0.f ? rintf(v / d) : 0.f;
-    if (i < n)
-        out[i] = d * q;
+    const float db = amax / 127.0f;
+    if (i < n) {
+        q[i] = (int8_t)(db > 0.f ? rintf(v / db) : 0.f);
+        if ((threadIdx.x & 31) == 0)
+            d[i / 32] = db;
+    }
 }
 
-// E2M1 value of the low nibble of c (a multiple of 0.5 in [-6, 6]).
-__device__ __forceinline__ float e2m1_value(unsigned c) {
-    const float m = 0.5f * (float)((kE2M1Twice >> (4u * (c & 7u))) & 15u);
-    return (c & 8u) ? -m : m;
+// Four consecutive E2M1 codes (the nibbles of the low 16 bits of h) as signed
+// int8 lanes of 2 * e2m1: the magnitude by a byte permute of the table
+// 0, 1, 2, 3, 4, 6, 8, 12; the sign as a byte mask M (0x00 / 0xFF) by a second
+// permute that picks byte 0 (0x00) for a clear sign bit and replicates the top
+// bit of byte 4 (0x80) for a set one. Returns the magnitudes; M in *neg.
+__device__ __forceinline__ uint32_t e2m1x4_twice(uint32_t h, uint32_t *neg) {
+    const uint32_t mag = __byte_perm(0x03020100u, 0x0C080604u, h & 0x7777u);
+    const uint32_t s = h & 0x8888u;
+    uint32_t m; // prmt's generic mode: a selector nibble with bit 3 set replicates the byte's sign bit
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(m) : "r"(0u), "r"(0x80u), "r"(s | (s >> 1)));
+    *neg = m;
+    return mag;
 }
 
 // out[pos][r] for the expert-grouped rows pos of distinct expert u, r in the
 // expert's M rows: the MXFP4 product of matrix A (or SwiGLU of gate/up when
-// GATEUP) with activation rows act[row_of(pos)][0..Kd).
-// GATEUP: A = gate, B = up, act rows are tokens perm[pos] / K, out = h (fp32);
-// else A = down, act rows are grouped positions, out = ye.
-// NT: rows of the expert handled together (the launch's bound on an expert's
-// rows, 1, 2, 4 or 8; more are taken in chunks of NT). A lane first loads the
-// codes and scales of up to kMx4LaneBlocks of its blocks, then multiplies.
+// GATEUP) with Q8 activation rows (codes aq [rows][Kd], scales ad [rows][Kd/32]).
+// GATEUP: A = gate, B = up, activation rows are tokens perm[pos] / K, out = h
+// (fp32); else A = down, rows are grouped positions, out = ye.
+// Per 32-weight block and activation row the sum of 2 e2m1(c_i) q_i is exact in
+// int32 (two dp4a per 4 weights: all magnitudes, minus twice the negative
+// ones), then scaled once by X d / 2 in fp32.
+// NT: rows of the expert handled together (1, 2, 4 or 8; more in chunks).
 constexpr int kMx4LaneBlocks = 4;
 
 template <bool GATEUP, int NT>
-__global__ void __launch_bounds__(256) mx4_product_kernel(Mx4Mat A, Mx4Mat B, const float *__restrict__ act,
+__global__ void __launch_bounds__(256) mx4_product_kernel(Mx4Mat A, Mx4Mat B, const int8_t *__restrict__ aq,
+                                                          const float *__restrict__ ad,
                                                           const int32_t *__restrict__ uexp,
                                                           const int32_t *__restrict__ uoff,
                                                           const int32_t *__restrict__ nuniq,
@@ -103,12 +117,11 @@ __global__ void __launch_bounds__(256) mx4_product_kernel(Mx4Mat A, Mx4Mat B, co
     const int64_t row = ((int64_t)e * M + r) * nb;
     for (int c0 = p0; c0 < p1; c0 += NT) {
         const int n = p1 - c0 < NT ? p1 - c0 : NT;
-        const float *arow[NT];
+        int64_t arow[NT];
 #pragma unroll
         for (int t = 0; t < NT; t++) {
             const int pos = c0 + (t < n ? t : 0);
-            const int64_t ar = GATEUP ? __ldg(perm + pos) / K : pos;
-            arow[t] = act + ar * Kd;
+            arow[t] = GATEUP ? __ldg(perm + pos) / K : pos;
         }
         float ga[NT], ua[NT];
 #pragma unroll
@@ -135,42 +148,43 @@ __global__ void __launch_bounds__(256) mx4_product_kernel(Mx4Mat A, Mx4Mat B, co
             for (int j = 0; j < kMx4LaneBlocks; j++) {
                 const int b = b0 + 32 * j;
                 if (b < nb) {
+                    // weights 8q+4h .. 8q+4h+3 are the nibbles of half h of code word q
+                    uint32_t ma[8], na[8], mb[8], nbm[8];
                     const uint32_t wa[4] = {ca[j].x, ca[j].y, ca[j].z, ca[j].w};
                     const uint32_t wb[4] = {cb[j].x, cb[j].y, cb[j].z, cb[j].w};
-                    float pa[NT], pb[NT];
 #pragma unroll
-                    for (int t = 0; t < NT; t++)
-                        pa[t] = pb[t] = 0.f;
+                    for (int q = 0; q < 4; q++)
 #pragma unroll
-                    for (int q = 0; q < 4; q++) { // 8 weights per code word
-                        float va[8], vb[8];
-#pragma unroll
-                        for (int i = 0; i < 8; i++) {
-                            va[i] = e2m1_value(wa[q] >> (4 * i));
-                            vb[i] = GATEUP ? e2m1_value(wb[q] >> (4 * i)) : 0.f;
-                        }
-#pragma unroll
-                        for (int t = 0; t < NT; t++) {
-                            if (t < n) {
-                                const float4 x0 = __ldg(reinterpret_cast<const float4 *>(arow[t] + b * 32 + 8 * q));
-                                const float4 x1 =
-                                    __ldg(reinterpret_cast<const float4 *>(arow[t] + b * 32 + 8 * q + 4));
-                                const float xv[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-#pragma unroll
-                                for (int i = 0; i < 8; i++) {
-                                    pa[t] = fmaf(va[i], xv[i], pa[t]);
-                                    if (GATEUP)
-                                        pb[t] = fmaf(vb[i], xv[i], pb[t]);
-                                }
+                        for (int hh = 0; hh < 2; hh++) {
+                            ma[2 * q + hh] = e2m1x4_twice(wa[q] >> (16 * hh), &na[2 * q + hh]);
+                            na[2 * q + hh] &= ma[2 * q + hh];
+                            if (GATEUP) {
+                                mb[2 * q + hh] = e2m1x4_twice(wb[q] >> (16 * hh), &nbm[2 * q + hh]);
+                                nbm[2 * q + hh] &= mb[2 * q + hh];
                             }
                         }
-                    }
-                    const float Xa = e8m0_value(sa[j]), Xb = GATEUP ? e8m0_value(sb[j]) : 0.f;
+                    const float Xa = 0.5f * e8m0_value(sa[j]), Xb = GATEUP ? 0.5f * e8m0_value(sb[j]) : 0.f;
 #pragma unroll
                     for (int t = 0; t < NT; t++) {
-                        ga[t] = fmaf(Xa, pa[t], ga[t]);
-                        if (GATEUP)
-                            ua[t] = fmaf(Xb, pb[t], ua[t]);
+                        if (t < n) {
+                            const int4 *qp = reinterpret_cast<const int4 *>(aq + arow[t] * Kd + b * 32);
+                            const int4 q0 = __ldg(qp), q1 = __ldg(qp + 1);
+                            const int qw[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+                            int sa_ = 0, sn = 0, sbm = 0, snb = 0;
+#pragma unroll
+                            for (int m = 0; m < 8; m++) {
+                                sa_ = __dp4a((int)ma[m], qw[m], sa_);
+                                sn = __dp4a((int)na[m], qw[m], sn);
+                                if (GATEUP) {
+                                    sbm = __dp4a((int)mb[m], qw[m], sbm);
+                                    snb = __dp4a((int)nbm[m], qw[m], snb);
+                                }
+                            }
+                            const float dt = __ldg(ad + arow[t] * (Kd / 32) + b);
+                            ga[t] = fmaf(Xa * dt, (float)(sa_ - 2 * sn), ga[t]);
+                            if (GATEUP)
+                                ua[t] = fmaf(Xb * dt, (float)(sbm - 2 * snb), ua[t]);
+                        }
                     }
                 }
             }

@@ -11,7 +11,7 @@ import torch
 import oracle
 import quantized_moe_expert_gb300 as ds4
 import synth
-from gpu_util import TOL_DECODE, check_routing, rel_l2, to_dev, x_to_dev
+from gpu_util import TOL_DECODE, assert_close, check_routing, to_dev, x_to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -45,7 +45,7 @@ def test_forward_matches_oracle(tiny, T):
     near = check_routing(idx.cpu().numpy(), w.cpu().numpy(), gap.cpu().numpy(), r, shape.top_k)
     if near.any():
         y_ref = oracle.forward_routed(shape, layer, x, idx.cpu().numpy(), w.cpu().numpy().astype(np.float64))
-    assert rel_l2(y, y_ref) <= TOL_DECODE
+    assert_close(y, y_ref, TOL_DECODE)
     assert moe.status() == 0
 
 
@@ -63,7 +63,7 @@ def test_forward_routed_with_gains(tiny):
         w = rng.random((T, shape.top_k)).astype(np.float32)
         y = moe.forward_routed(x_to_dev(x), torch.from_numpy(idx).cuda(), torch.from_numpy(w).cuda()).cpu().numpy()
         y_ref = oracle.forward_routed(shape, L, x, idx, w.astype(np.float64))
-        assert rel_l2(y, y_ref) <= TOL_DECODE
+        assert_close(y, y_ref, TOL_DECODE)
         assert moe.status() == 0
     finally:
         moe.close()
@@ -101,5 +101,5 @@ def test_full_size_t1_and_t8(big):
         idx, w, gap, _ = moe.route(xd)
         idx, w = idx.cpu().numpy(), w.cpu().numpy()
         y_ref = oracle.forward_routed(shape, layer, x, idx, w.astype(np.float64))
-        assert rel_l2(y, y_ref) <= TOL_DECODE
+        assert_close(y, y_ref, TOL_DECODE)
     assert moe.status() == 0
