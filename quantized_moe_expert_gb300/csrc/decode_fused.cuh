@@ -112,10 +112,10 @@ struct DecodeArgs {
     float *gap;      // [8]
     int32_t *counts; // [E]
     int32_t *nuniq, *inv;
-    uint16_t *xq;            // [8][H] bf16 x * 2^e(k)
-    float *xoff, *xsum;      // [8][H/16]
-    uint16_t *hq_hi, *hq_lo; // [64][I] bf16 h * 2^e(k) as hi + lo
-    float *hoff, *hsum;      // [64][I/16]
+    uint16_t *xq;            // [8][H] bf16 x * 4^-p, permuted (q2_act_index)
+    uint16_t *xsums;         // [8][H/8] bf16 hi and lo of each 16-column sum of x (q2_sum_index)
+    uint16_t *hq_hi, *hq_lo; // [64][I] SwiGLU rows h * 4^-p as a bf16 hi + lo pair, permuted
+    uint16_t *hsums;         // [64][I/8] the 16-column sums of h, hi and lo
     uint16_t *hs_hi, *hs_lo; // [8][Ish] binary16 shared h as hi + lo
     float *ye;               // [64][H]
     float *ysh;              // [8][H]
@@ -237,13 +237,6 @@ __device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1,
                  "{%0,%1,%2,%3};"
                  : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
                  : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-__device__ __forceinline__ uint32_t lop3_magic(uint32_t v, uint32_t mask) {
-    uint32_t r;
-    // (v & mask) | 0x3F803F80
-    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(v), "r"(mask), "r"(0x3F803F80u));
-    return r;
 }
 
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
@@ -371,134 +364,177 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, 256;
 
 // ---- tensor-core tile GEMV over one stage -----------------------------------------
 //
-// A warp multiplies one 16-row tile by TP token columns (1, 2, 4 or 8). The 8
-// columns of each m16n8k16 MMA are (slot, token) pairs with 8/TP slots:
-// chunk c (16 columns) feeds only the columns of slot c % (8/TP), so one
-// accumulator tile holds 8/TP chunks' dot products side by side and each
-// chunk's scale is applied once per accumulator tile rather than per MMA.
-// out[m][rr][col] accumulates row g + 8*rr (g = lane/4) and token
-// (2*(lane%4) + col) % TP over the warp's columns; reduce_out combines the
-// lanes that share a (row, token) at the end of the job.
+// 2-bit matrices (layout in frag_layout.cuh): a warp takes whole 256-column
+// blocks of the stage; per block and matrix it turns the sub-block scales of
+// its two rows and four sub-blocks into bf16 multipliers once, then runs 16
+// MMAs whose A registers are one LOP3 and one packed FMA each (sc q 4^p,
+// exact), and two MMAs for the min term. The 8 MMA columns are the job's
+// tokens (padded columns repeat token 0 and are ignored). At the end of a
+// block, out[m][rho][col] (row g + 8 rho, token 2 tig + col) gains
+// d D - dmin Dm.
 
 template <int TP> __device__ __forceinline__ int srow(const StageDesc &d, int t) { return t < d.ntok ? t : 0; }
 
-// 2-bit matrices (NMAT of them share the activations) over the stage's kc
-// range of this warp. Activations in the stage: bf16 pairs of x * 2^e(k)
-// (and the low parts when SPLIT), per-sub-block offset sums and plain sums.
-template <int TP, int NMAT, bool SPLIT>
-__device__ __forceinline__ void q2_stage(const uint8_t *sl, const StageDesc &d, int warp, int lane,
-                                         float (&out)[2][2][2]) {
-    constexpr int S = 8 / TP;
-    const int g = lane >> 2, tig = lane & 3;
-    const int bs = g / TP, bt = g % TP;
-    const int n0 = 2 * tig, n1 = 2 * tig + 1;
-    const int s0 = n0 / TP, t0 = n0 % TP, s1 = n1 / TP, t1 = n1 % TP;
-    const int nkc = d.W >> 7;
-    const int kb = nkc * warp / kConsumerWarps, ke = nkc * (warp + 1) / kConsumerWarps;
-    const uint32_t *act = reinterpret_cast<const uint32_t *>(sl + d.oact + srow<TP>(d, bt) * d.act_pitch);
-    const uint32_t *act_lo = reinterpret_cast<const uint32_t *>(sl + d.olo + srow<TP>(d, bt) * d.act_pitch);
-    const float *off0 = reinterpret_cast<const float *>(sl + d.ooff + srow<TP>(d, t0) * d.sub_pitch);
-    const float *sum0 = reinterpret_cast<const float *>(sl + d.osum + srow<TP>(d, t0) * d.sub_pitch);
-    const float *off1 = reinterpret_cast<const float *>(sl + d.ooff + srow<TP>(d, t1) * d.sub_pitch);
-    const float *sum1 = reinterpret_cast<const float *>(sl + d.osum + srow<TP>(d, t1) * d.sub_pitch);
-    float asc[NMAT][2][2], amn[NMAT][2][2];
+constexpr uint32_t kBf2Mag = 0x43004300u;   // bf16 pair (128, 128)
+constexpr uint32_t kBf2One = 0x3F803F80u;   // (1, 1)
+constexpr uint32_t kBf2M128 = 0xC300C300u;  // (-128, -128)
+constexpr uint32_t kBf2P16384 = 0x46804680u; // (16384, 16384)
+
+// (v & mask) | (128, 128) as a bf16 pair: 128 + the masked bits
+__device__ __forceinline__ uint32_t lop_mag(uint32_t v, uint32_t mask) {
+    uint32_t r;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(v), "r"(mask), "r"(kBf2Mag));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t bf2_fma(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t r;
+    asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(c));
+    return r;
+}
+
+// Multipliers of one block for one matrix: C = (sc, sc') and O = -128 C for
+// the four registers (rho, kappa), and the min-term A fragment M.
+struct Q2Mult {
+    uint32_t C[4], O[4], M[4]; // index 2 kappa + rho: the MMA's a0, a1, a2, a3
+};
+
+__device__ __forceinline__ void q2_mult(const uint2 sw, Q2Mult &q) {
 #pragma unroll
-    for (int m = 0; m < NMAT; m++)
+    for (int rho = 0; rho < 2; rho++) {
+        const uint32_t w = rho ? sw.y : sw.x;
 #pragma unroll
-        for (int r = 0; r < 2; r++)
-            asc[m][r][0] = asc[m][r][1] = amn[m][r][0] = amn[m][r][1] = 0.f;
-    for (int kc = kb; kc < ke; kc++) {
-        uint4 q[NMAT], s[NMAT];
-#pragma unroll
-        for (int m = 0; m < NMAT; m++) {
-            const uint8_t *rb = sl + d.oq[m] + (kc >> 1) * kQ2Rec; // the block's record
-            q[m] = reinterpret_cast<const uint4 *>(rb + (kc & 1) * 512)[lane];
-            s[m] = reinterpret_cast<const uint4 *>(rb + kQ2RecScales + (kc & 1) * 128)[g];
-        }
-        const int colbase = kc * 128 + 2 * tig; // column within the stage
-#pragma unroll
-        for (int nt = 0; nt < 8 / S; nt++) {
-            // two accumulators (even and odd slots) halve the dependent MMA chain
-            float D[NMAT][4], D2[NMAT][4];
-#pragma unroll
-            for (int m = 0; m < NMAT; m++)
-#pragma unroll
-                for (int i = 0; i < 4; i++)
-                    D[m][i] = D2[m][i] = 0.f;
-#pragma unroll
-            for (int sl2 = 0; sl2 < S; sl2++) {
-                const int c = nt * S + sl2; // chunk 0..7 within kc
-                const int G = c >> 2, cc = c & 3;
-                const int r_lo = 2 * cc, r_hi = 2 * cc + 1;
-                const bool on = bs == sl2;
-                const int col = colbase + 16 * c;
-                const uint32_t b0 = on ? act[col >> 1] : 0u;
-                const uint32_t b1 = on ? act[(col + 8) >> 1] : 0u;
-                uint32_t c0 = 0, c1 = 0;
-                if (SPLIT) {
-                    c0 = on ? act_lo[col >> 1] : 0u;
-                    c1 = on ? act_lo[(col + 8) >> 1] : 0u;
-                }
-#pragma unroll
-                for (int m = 0; m < NMAT; m++) {
-                    const uint32_t wg = G ? q[m].z : q[m].x, wg8 = G ? q[m].w : q[m].y;
-                    constexpr uint32_t k3 = 0x00030003u;
-                    const uint32_t a0 = lop3_magic(wg >> frag_shift(r_lo), k3 << frag_pos(r_lo));
-                    const uint32_t a1 = lop3_magic(wg8 >> frag_shift(r_lo), k3 << frag_pos(r_lo));
-                    const uint32_t a2 = lop3_magic(wg >> frag_shift(r_hi), k3 << frag_pos(r_hi));
-                    const uint32_t a3 = lop3_magic(wg8 >> frag_shift(r_hi), k3 << frag_pos(r_hi));
-                    if (SPLIT) { // hi parts and lo parts in separate chains
-                        mma_bf16(D[m], a0, a1, a2, a3, b0, b1);
-                        mma_bf16(D2[m], a0, a1, a2, a3, c0, c1);
-                    } else {
-                        float(&acc)[4] = (sl2 & 1) ? D2[m] : D[m];
-                        mma_bf16(acc, a0, a1, a2, a3, b0, b1);
-                    }
-                }
-            }
-#pragma unroll
-            for (int m = 0; m < NMAT; m++)
-#pragma unroll
-                for (int i = 0; i < 4; i++)
-                    D[m][i] += D2[m][i];
-            // scale and min terms of the accumulator tile, per (row, chunk)
-            const int ca = nt * S + s0, cb = nt * S + s1;
-            const int ja = kc * 8 + ca, jb = kc * 8 + cb;
-            const float oa = off0[ja], ua = sum0[ja], ob = off1[jb], ub = sum1[jb];
-            const int sha = 8 * (ca & 3), shb = 8 * (cb & 3);
-#pragma unroll
-            for (int m = 0; m < NMAT; m++) {
-                const uint32_t ba = ((ca < 4 ? s[m].x : s[m].y) >> sha) & 0xFFu;
-                const uint32_t bb = ((cb < 4 ? s[m].x : s[m].y) >> shb) & 0xFFu;
-                const uint32_t ba8 = ((ca < 4 ? s[m].z : s[m].w) >> sha) & 0xFFu;
-                const uint32_t bb8 = ((cb < 4 ? s[m].z : s[m].w) >> shb) & 0xFFu;
-                asc[m][0][0] = fmaf(nib_to_f(ba & 15u), D[m][0] - oa, asc[m][0][0]);
-                amn[m][0][0] = fmaf(nib_to_f(ba >> 4), ua, amn[m][0][0]);
-                asc[m][0][1] = fmaf(nib_to_f(bb & 15u), D[m][1] - ob, asc[m][0][1]);
-                amn[m][0][1] = fmaf(nib_to_f(bb >> 4), ub, amn[m][0][1]);
-                asc[m][1][0] = fmaf(nib_to_f(ba8 & 15u), D[m][2] - oa, asc[m][1][0]);
-                amn[m][1][0] = fmaf(nib_to_f(ba8 >> 4), ua, amn[m][1][0]);
-                asc[m][1][1] = fmaf(nib_to_f(bb8 & 15u), D[m][3] - ob, asc[m][1][1]);
-                amn[m][1][1] = fmaf(nib_to_f(bb8 >> 4), ub, amn[m][1][1]);
-            }
-        }
-        // end of a 256-column block (stages start on block boundaries) or of this
-        // warp's range: apply the block's d and dmin
-        if ((kc & 1) == 1 || kc + 1 == ke) {
-#pragma unroll
-            for (int m = 0; m < NMAT; m++) {
-                const uint2 dw = reinterpret_cast<const uint2 *>(sl + d.oq[m] + (kc >> 1) * kQ2Rec + kQ2RecDm)[g];
-                const float dg = f16_to_f32(dw.x), mg = f16_to_f32(dw.x >> 16);
-                const float dg8 = f16_to_f32(dw.y), mg8 = f16_to_f32(dw.y >> 16);
-#pragma unroll
-                for (int col = 0; col < 2; col++) {
-                    out[m][0][col] += dg * asc[m][0][col] - mg * amn[m][0][col];
-                    out[m][1][col] += dg8 * asc[m][1][col] - mg8 * amn[m][1][col];
-                    asc[m][0][col] = asc[m][1][col] = amn[m][0][col] = amn[m][1][col] = 0.f;
-                }
-            }
+        for (int kappa = 0; kappa < 2; kappa++) {
+            const uint32_t cr = lop_mag(w >> (4 * kappa), 0x000F000Fu);    // 128 + sc
+            const uint32_t mr = lop_mag(w >> (8 + 4 * kappa), 0x000F000Fu); // 128 + m
+            q.C[2 * kappa + rho] = bf2_fma(cr, kBf2One, kBf2M128);        // sc
+            q.O[2 * kappa + rho] = bf2_fma(cr, kBf2M128, kBf2P16384);     // -128 sc
+            q.M[2 * kappa + rho] = bf2_fma(mr, kBf2One, kBf2M128);        // m
         }
     }
+}
+
+// A register of MMA c (c & 3 == cl) from the lane's word pair (wa, wb) and
+// its shifts: the two codes at q2_slot(cl, kappa), row rho.
+template <int CL, int KAPPA, int RHO>
+__device__ __forceinline__ uint32_t q2_areg(const uint32_t (&sh)[2][3], const Q2Mult &q) {
+    constexpr Q2Slot s = q2_slot(CL, KAPPA);
+    constexpr int w = RHO ? s.w1 : s.w0;
+    constexpr int si = (RHO ? s.s1 : s.s0) / 6;
+    const uint32_t raw = lop_mag(sh[w][si], 0x00030003u << (2 * s.p));
+    return bf2_fma(raw, q.C[2 * KAPPA + RHO], q.O[2 * KAPPA + RHO]);
+}
+
+template <int CL, int NMAT>
+__device__ __forceinline__ void q2_mma4(float (&D)[NMAT][4], const uint32_t (&sh)[NMAT][2][3], const Q2Mult (&q)[NMAT],
+                                        uint2 b) {
+#pragma unroll
+    for (int m = 0; m < NMAT; m++)
+        mma_bf16(D[m], q2_areg<CL, 0, 0>(sh[m], q[m]), q2_areg<CL, 0, 1>(sh[m], q[m]), q2_areg<CL, 1, 0>(sh[m], q[m]),
+                 q2_areg<CL, 1, 1>(sh[m], q[m]), b.x, b.y);
+}
+
+// NMAT 2-bit matrices of the stage sharing the activations; SPLIT: the
+// activations are a bf16 hi + lo pair (both multiplied by the same A).
+template <int NMAT, bool SPLIT>
+__device__ __forceinline__ void q2_stage(const uint8_t *sl, const StageDesc &d, int warp, int lane,
+                                         float (&out)[2][2][2]) {
+    const int g = lane >> 2, tig = lane & 3;
+    const int nb = d.W >> 8;
+    const int bb = nb * warp / kConsumerWarps, be = nb * (warp + 1) / kConsumerWarps;
+    const int t = g < d.ntok ? g : 0; // this lane's B column's token
+    const uint8_t *xa = sl + d.oact + t * d.act_pitch + 8 * tig;
+    const uint8_t *xl = sl + d.olo + t * d.act_pitch + 8 * tig;
+    const uint8_t *xs = sl + d.osum + t * d.sub_pitch + 8 * tig;
+    for (int b = bb; b < be; b++) {
+        const uint8_t *rb[NMAT];
+        Q2Mult q[NMAT];
+#pragma unroll
+        for (int m = 0; m < NMAT; m++) {
+            rb[m] = sl + d.oq[m] + b * kQ2Rec;
+            q2_mult(reinterpret_cast<const uint2 *>(rb[m] + kQ2RecScales)[lane], q[m]);
+        }
+        float D[NMAT][4], Dm[NMAT][4];
+#pragma unroll
+        for (int m = 0; m < NMAT; m++)
+#pragma unroll
+            for (int i = 0; i < 4; i++)
+                D[m][i] = Dm[m][i] = 0.f;
+        // min term: m x (sum of the activations over each sub-block), hi and lo parts
+        {
+            const uint2 shi = *reinterpret_cast<const uint2 *>(xs + 64 * b);
+            const uint2 slo = *reinterpret_cast<const uint2 *>(xs + 64 * b + 32);
+#pragma unroll
+            for (int m = 0; m < NMAT; m++) {
+                mma_bf16(Dm[m], q[m].M[0], q[m].M[1], q[m].M[2], q[m].M[3], shi.x, shi.y);
+                mma_bf16(Dm[m], q[m].M[0], q[m].M[1], q[m].M[2], q[m].M[3], slo.x, slo.y);
+            }
+        }
+#pragma unroll
+        for (int half = 0; half < 2; half++) {
+            uint4 qw[NMAT];
+#pragma unroll
+            for (int m = 0; m < NMAT; m++)
+                qw[m] = reinterpret_cast<const uint4 *>(rb[m] + 512 * half)[lane];
+#pragma unroll
+            for (int pr = 0; pr < 2; pr++) {
+                uint32_t sh[NMAT][2][3];
+#pragma unroll
+                for (int m = 0; m < NMAT; m++) {
+                    const uint32_t wa = pr ? qw[m].z : qw[m].x, wb = pr ? qw[m].w : qw[m].y;
+                    sh[m][0][0] = wa;
+                    sh[m][0][1] = wa >> 6;
+                    sh[m][0][2] = wa >> 12;
+                    sh[m][1][0] = wb;
+                    sh[m][1][1] = wb >> 6;
+                    sh[m][1][2] = wb >> 12;
+                }
+                const int c0 = 8 * half + 4 * pr;
+                const uint8_t *xb = xa + 32 * (16 * b + c0);
+                const uint8_t *lb = xl + 32 * (16 * b + c0);
+                q2_mma4<0, NMAT>(D, sh, q, *reinterpret_cast<const uint2 *>(xb));
+                if (SPLIT)
+                    q2_mma4<0, NMAT>(D, sh, q, *reinterpret_cast<const uint2 *>(lb));
+                q2_mma4<1, NMAT>(D, sh, q, *reinterpret_cast<const uint2 *>(xb + 32));
+                if (SPLIT)
+                    q2_mma4<1, NMAT>(D, sh, q, *reinterpret_cast<const uint2 *>(lb + 32));
+                q2_mma4<2, NMAT>(D, sh, q, *reinterpret_cast<const uint2 *>(xb + 64));
+                if (SPLIT)
+                    q2_mma4<2, NMAT>(D, sh, q, *reinterpret_cast<const uint2 *>(lb + 64));
+                q2_mma4<3, NMAT>(D, sh, q, *reinterpret_cast<const uint2 *>(xb + 96));
+                if (SPLIT)
+                    q2_mma4<3, NMAT>(D, sh, q, *reinterpret_cast<const uint2 *>(lb + 96));
+            }
+        }
+        // the block's d and dmin
+#pragma unroll
+        for (int m = 0; m < NMAT; m++) {
+            const uint2 dw = reinterpret_cast<const uint2 *>(rb[m] + kQ2RecDm)[g];
+            const float dg = f16_to_f32(dw.x), mg = f16_to_f32(dw.x >> 16);
+            const float dg8 = f16_to_f32(dw.y), mg8 = f16_to_f32(dw.y >> 16);
+            out[m][0][0] += dg * D[m][0] - mg * Dm[m][0];
+            out[m][0][1] += dg * D[m][1] - mg * Dm[m][1];
+            out[m][1][0] += dg8 * D[m][2] - mg8 * Dm[m][2];
+            out[m][1][1] += dg8 * D[m][3] - mg8 * Dm[m][3];
+        }
+    }
+}
+
+// Partial sums of a 2-bit job (q2_stage's layout: each (row, token) in one
+// lane) into the warp's slot of the job's reduction buffer.
+__device__ __forceinline__ void store_part_q2(DecodeSmem &sm, int buf, int warp, int lane, const float (&out)[2][2][2],
+                                              int ntok) {
+    const int g = lane >> 2, tig = lane & 3;
+#pragma unroll
+    for (int m = 0; m < 2; m++)
+#pragma unroll
+        for (int col = 0; col < 2; col++) {
+            const int t = 2 * tig + col;
+            if (t < ntok) {
+                sm.part[buf][warp][m][g][t] = out[m][0][col];
+                sm.part[buf][warp][m][g + 8][t] = out[m][1][col];
+            }
+        }
 }
 
 // 8-bit matrices: A = the codes as exact binary16 integers, B = binary16
@@ -734,8 +770,9 @@ __device__ __forceinline__ void select_token(const DecodeArgs &a, const SelIO &i
 }
 
 // Work of the selection job that needs no router output (all consumer
-// threads, before the wait for the router rows): activation pre-scaling for
-// the 2-bit MMA, zeroed expert counts, and the router bias staged into the
+// threads, before the wait for the router rows): the activations in the
+// 2-bit GEMV's permuted layout (x 4^-p, exact) with their 16-column sums as a
+// bf16 hi + lo pair, zeroed expert counts, and the router bias staged into the
 // job's stage buffer (bias at float offset kDecodeT * E of scratch).
 __device__ void select_prepare(const DecodeArgs &a, float *scratch) {
     const int T = a.T, E = a.E, H = a.H;
@@ -746,22 +783,21 @@ __device__ void select_prepare(const DecodeArgs &a, float *scratch) {
         const uint4 *src = reinterpret_cast<const uint4 *>(a.x + (int64_t)t * H + 16 * j);
         const uint4 p0 = __ldg(src), p1 = __ldg(src + 1);
         const uint32_t wv[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
-        uint32_t outw[8];
-        float so = 0.f, ss = 0.f;
+        const int kappa = (j & 15) >> 3;
+        uint16_t *xt = a.xq + (int64_t)t * H;
+        float sum = 0.f;
 #pragma unroll
-        for (int h2 = 0; h2 < 8; h2++) {
-            const float e2 = (float)(1 << frag_exp(16 * j + 2 * h2)); // same exponent for both columns
-            const float v0 = __uint_as_float(wv[h2] << 16), v1 = __uint_as_float(wv[h2] & 0xFFFF0000u);
-            const float s0 = v0 * e2, s1 = v1 * e2; // exact: power-of-two scaling of bf16
-            so += s0 + s1;
-            ss += v0 + v1;
-            outw[h2] = (f32_to_bf16_bits(s0) & 0xFFFFu) | (f32_to_bf16_bits(s1) << 16);
+        for (int c = 0; c < 16; c++) {
+            const float v = __uint_as_float(c & 1 ? wv[c >> 1] & 0xFFFF0000u : wv[c >> 1] << 16);
+            sum += v;
+            const float sv = v * (1.0f / (float)(1 << (2 * q2_p(c, kappa)))); // exact: power of two
+            xt[q2_act_index(16 * j + c)] = (uint16_t)f32_to_bf16_bits(sv);
         }
-        uint4 *dst = reinterpret_cast<uint4 *>(a.xq + (int64_t)t * H + 16 * j);
-        dst[0] = make_uint4(outw[0], outw[1], outw[2], outw[3]);
-        dst[1] = make_uint4(outw[4], outw[5], outw[6], outw[7]);
-        a.xoff[t * nsub + j] = so;
-        a.xsum[t * nsub + j] = ss;
+        const uint32_t hi = f32_to_bf16_bits(sum);
+        const uint32_t lo = f32_to_bf16_bits(sum - __uint_as_float(hi << 16));
+        uint16_t *st = a.xsums + (int64_t)t * (H / 8);
+        st[q2_sum_index(j >> 4, j & 15, 0)] = (uint16_t)hi;
+        st[q2_sum_index(j >> 4, j & 15, 1)] = (uint16_t)lo;
     }
     for (int e = threadIdx.x; e < E; e += 32 * kConsumerWarps) {
         a.counts[e] = 0;
@@ -1094,6 +1130,22 @@ __device__ __forceinline__ int pick_w(int K, int per_col_x16) {
     return 256;
 }
 
+// Bytes of a 2-bit stage of W columns: two matrices' records, and per token
+// the activation rows (hi and lo when split) and their sums, each row padded
+// by 16 bytes so that the token rows of a warp's loads fall in different banks.
+__device__ __forceinline__ int q2_stage_bytes(int W, int ntok, bool split) {
+    return 2 * (W / 256) * kQ2Rec + ntok * ((2 * W + 16) * (split ? 2 : 1) + W / 4 + 16);
+}
+
+// Widest such stage (a multiple of 256 dividing K) that fits one ring slot.
+__device__ __forceinline__ int pick_w_q2(int K, int ntok, bool split) {
+    const int nb = K / 256;
+    for (int m = nb; m >= 1; m--)
+        if (nb % m == 0 && q2_stage_bytes(256 * m, ntok, split) <= kSlotBytes)
+            return 256 * m;
+    return 256;
+}
+
 // ---- producer (the last warp, all lanes in lockstep) ------------------------------------
 
 // Lays out one stage: put() places a piece that the bulk copies bring in;
@@ -1128,6 +1180,8 @@ struct StageWriter {
         tx += n;
         return o;
     }
+    // leave n bytes of the stage unwritten (padding)
+    __device__ void skip(unsigned n) { off += n; }
     int nindep = -1; // pieces before this index need no dependency wait
     // Pieces put after this call are data other CTAs of this launch are still
     // producing: issue() copies them only after the dependency is met.
@@ -1285,11 +1339,10 @@ template <bool GAIN> __device__ void producer(const DecodeArgs &a, DecodeSmem &s
                 pos[i] = rec.p0 + ii;
                 tok[i] = (int)((rec.toks >> (3 * ii)) & 7u);
             }
-            // two 2-bit tiles: 84/256 B per column per 16 rows = 5.25 B each; activations per
-            // token: GU x' (2 B) + off/sum (0.5 B); D hi + lo (4 B) + off/sum (0.5 B)
-            per16 = type == kJobGu ? 2 * 84 + ntok * 40 : 2 * 84 + ntok * 72;
         }
-        const int W = type == kJobSel ? 0 : pick_w(K, per16);
+        const int W = type == kJobSel                      ? 0
+                      : (type == kJobGu || type == kJobD) ? pick_w_q2(K, ntok, type == kJobD)
+                                                          : pick_w(K, per16);
         const int nsub = type == kJobSel ? 1 : K / W;
         for (int sub = 0; sub < nsub && ok; sub++) {
             int slot;
@@ -1356,37 +1409,42 @@ template <bool GAIN> __device__ void producer(const DecodeArgs &a, DecodeSmem &s
                     const int64_t u = gt * (M[m]->nkc / 2) + c0 / 256; // first record of the stage
                     d.oq[m] = sw.put(M[m]->rec + u * kQ2Rec, (unsigned)(W / 256) * kQ2Rec);
                 }
-                const uint16_t *hi = a.xq;
-                const float *of = a.xoff, *su = a.xsum;
-                d.act_pitch = 2 * W;
-                d.sub_pitch = W / 4;
+                // activation rows in the permuted layout: a block of 256 columns is 512
+                // contiguous bytes of a row, its 16 sums (hi, lo) 64 bytes
+                d.act_pitch = 2 * W + 16;
+                d.sub_pitch = W / 4 + 16;
                 if (type == kJobGu) {
                     // x rows were written by the selection job, which completed before the
                     // routing was published: safe to copy now
                     d.oact = (int)sw.off;
-                    for (int t = 0; t < ntok; t++)
-                        sw.put(hi + (int64_t)tok_of(t) * K + c0, 2u * W);
-                    d.ooff = (int)sw.off;
-                    for (int t = 0; t < ntok; t++)
-                        sw.put(of + (int64_t)tok_of(t) * (K / 16) + c0 / 16, (unsigned)W / 4u);
+                    for (int t = 0; t < ntok; t++) {
+                        sw.put(a.xq + (int64_t)tok_of(t) * K + c0, 2u * W);
+                        sw.skip(16);
+                    }
+                    d.olo = d.oact;
                     d.osum = (int)sw.off;
-                    for (int t = 0; t < ntok; t++)
-                        sw.put(su + (int64_t)tok_of(t) * (K / 16) + c0 / 16, (unsigned)W / 4u);
+                    for (int t = 0; t < ntok; t++) {
+                        sw.put(a.xsums + (int64_t)tok_of(t) * (K / 8) + c0 / 8, (unsigned)W / 4u);
+                        sw.skip(16);
+                    }
                 } else {
                     // h rows of this expert: written by its GU jobs
                     sw.dependent_from_here();
                     d.oact = (int)sw.off;
-                    for (int t = 0; t < ntok; t++)
+                    for (int t = 0; t < ntok; t++) {
                         sw.put(a.hq_hi + (int64_t)(rec.p0 + t) * K + c0, 2u * W);
+                        sw.skip(16);
+                    }
                     d.olo = (int)sw.off;
-                    for (int t = 0; t < ntok; t++)
+                    for (int t = 0; t < ntok; t++) {
                         sw.put(a.hq_lo + (int64_t)(rec.p0 + t) * K + c0, 2u * W);
-                    d.ooff = (int)sw.off;
-                    for (int t = 0; t < ntok; t++)
-                        sw.put(a.hoff + (int64_t)(rec.p0 + t) * (K / 16) + c0 / 16, (unsigned)W / 4u);
+                        sw.skip(16);
+                    }
                     d.osum = (int)sw.off;
-                    for (int t = 0; t < ntok; t++)
-                        sw.put(a.hsum + (int64_t)(rec.p0 + t) * (K / 16) + c0 / 16, (unsigned)W / 4u);
+                    for (int t = 0; t < ntok; t++) {
+                        sw.put(a.hsums + (int64_t)(rec.p0 + t) * (K / 8) + c0 / 8, (unsigned)W / 4u);
+                        sw.skip(16);
+                    }
                 }
             }
             const unsigned *dep = type == kJobD ? a.ctl + kCtlGuDone + a0 : a.ctl + kCtlSguDone;
@@ -1539,10 +1597,8 @@ template <int TP> struct JobOps {
                                  float (&out)[2][2][2]) {
         switch (d.type) {
         case kJobSgu: q8_stage<TP, 2, false, true>(sl, d, warp, lane, out); break;
-        case kJobGu: q2_stage<TP, 2, false>(sl, d, warp, lane, out); break;
         case kJobSd: q8_stage<TP, 1, true, false>(sl, d, warp, lane, out); break;
-        case kJobD: q2_stage<TP, 2, true>(sl, d, warp, lane, out); break;
-        default: break;
+        default: break; // the 2-bit jobs do not depend on the token count (q2_stage)
         }
     }
     // End of a job: combine the warps' partial sums (barrier 1), write the
@@ -1551,7 +1607,9 @@ template <int TP> struct JobOps {
                                   int buf, int warp, int lane, float (&out)[2][2][2], unsigned &npub) {
         const int tid = threadIdx.x;
         auto P = sm.part[buf];
-        if (d.type != kJobSd) {
+        if (d.type == kJobGu || d.type == kJobD) {
+            store_part_q2(sm, buf, warp, lane, out, d.ntok);
+        } else if (d.type != kJobSd) {
             reduce_out<TP, 2>(out);
             store_part<TP, 2>(sm, buf, warp, lane, out);
         } else {
@@ -1578,9 +1636,11 @@ template <int TP> struct JobOps {
             if (tid == 0)
                 publish(a, sm, npub, kPubSignal, a.ctl + kCtlSguDone, 0, 0);
         } else if (d.type == kJobGu) {
-            // row r of the tile is column k = 16 tile + r of the down matrix
+            // row r of the tile is column k = 16 tile + r of the down matrix: position
+            // r of its sub-block j = tile % 16 in block tile / 16
             const int t = tid >> 4, r = tid & 15;
-            float hv_sum = 0.f, hv_off = 0.f;
+            const int blk = d.tile >> 4, j = d.tile & 15;
+            float hs = 0.f;
             if (t < d.ntok) {
                 float gs = 0.f, us = 0.f;
                 for (int w = 0; w < kConsumerWarps; w++) {
@@ -1588,27 +1648,26 @@ template <int TP> struct JobOps {
                     us += P[w][1][r][t];
                 }
                 const float hv = silu(gs) * us;
-                const int k = d.tile * 16 + r;
-                const float sc = (float)(1 << frag_exp(k));
-                const float hp = hv * sc;
+                const int e2 = 2 * q2_p(r, j >> 3);
+                const float hp = hv * (1.0f / (float)(1 << e2)); // exact: power of two
                 const uint32_t hi = f32_to_bf16_bits(hp);
                 const float hif = __uint_as_float(hi << 16);
                 const uint32_t lo = f32_to_bf16_bits(hp - hif);
                 const float lof = __uint_as_float(lo << 16);
-                const int64_t o = (int64_t)d.pos[t] * a.I + k;
+                const int64_t o = (int64_t)d.pos[t] * a.I + q2_act_index(d.tile * 16 + r);
                 a.hq_hi[o] = (uint16_t)hi;
                 a.hq_lo[o] = (uint16_t)lo;
-                hv_off = hif + lof;
-                hv_sum = hv_off / sc;
+                hs = (hif + lof) * (float)(1 << e2); // the value the down product sees
             }
 #pragma unroll
-            for (int o = 8; o > 0; o >>= 1) { // over the 16 rows: one sub-block of the down columns
-                hv_off += __shfl_xor_sync(0xFFFFFFFFu, hv_off, o);
-                hv_sum += __shfl_xor_sync(0xFFFFFFFFu, hv_sum, o);
-            }
+            for (int o = 8; o > 0; o >>= 1) // over the 16 rows: one sub-block of the down columns
+                hs += __shfl_xor_sync(0xFFFFFFFFu, hs, o);
             if (t < d.ntok && r == 0) {
-                a.hoff[d.pos[t] * (a.I / 16) + d.tile] = hv_off;
-                a.hsum[d.pos[t] * (a.I / 16) + d.tile] = hv_sum;
+                const uint32_t hi = f32_to_bf16_bits(hs);
+                const uint32_t lo = f32_to_bf16_bits(hs - __uint_as_float(hi << 16));
+                uint16_t *st = a.hsums + (int64_t)d.pos[t] * (a.I / 8);
+                st[q2_sum_index(blk, j, 0)] = (uint16_t)hi;
+                st[q2_sum_index(blk, j, 1)] = (uint16_t)lo;
             }
             consumer_sync();
             if (tid == 0)
@@ -1699,6 +1758,10 @@ template <int TPM> __device__ void consumer(const DecodeArgs &a, DecodeSmem &sm,
         if (alive) {
             if (type == kJobR)
                 router_stage(sm.ring[slot], d, a.T, warp, lane, out);
+            else if (type == kJobGu)
+                q2_stage<2, false>(sm.ring[slot], d, warp, lane, out);
+            else if (type == kJobD)
+                q2_stage<2, true>(sm.ring[slot], d, warp, lane, out);
             else if (type != kJobSel)
                 stage_tp<TPM>(d.tp, a, sm.ring[slot], d, warp, lane, out);
         }

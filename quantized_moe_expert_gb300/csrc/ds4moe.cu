@@ -91,10 +91,8 @@ struct DecodeState {
     SelIO dry{};                                        // the selection rehearsal's buffers
     float *gap = nullptr;
     int32_t *counts = nullptr, *nuniq = nullptr, *inv = nullptr;
-    uint16_t *xq = nullptr;
-    float *xoff = nullptr, *xsum = nullptr;
-    uint16_t *hq_hi = nullptr, *hq_lo = nullptr;
-    float *hoff = nullptr, *hsum = nullptr;
+    uint16_t *xq = nullptr, *xsums = nullptr;
+    uint16_t *hq_hi = nullptr, *hq_lo = nullptr, *hsums = nullptr;
     uint16_t *hs_hi = nullptr, *hs_lo = nullptr;
     float *ye = nullptr, *ysh = nullptr;
     unsigned *ctl = nullptr;
@@ -403,12 +401,10 @@ void layout_scratch(ds4moe *h, Carver &c) {
     D.nuniq = c.take<int32_t>(1);
     D.inv = c.take<int32_t>(Pd);
     D.xq = c.take<uint16_t>(Td * L.H);
-    D.xoff = c.take<float>(Td * (L.H / 16));
-    D.xsum = c.take<float>(Td * (L.H / 16));
+    D.xsums = c.take<uint16_t>(Td * (L.H / 8));
     D.hq_hi = c.take<uint16_t>(Pd * L.I);
     D.hq_lo = c.take<uint16_t>(Pd * L.I);
-    D.hoff = c.take<float>(Pd * (L.I / 16));
-    D.hsum = c.take<float>(Pd * (L.I / 16));
+    D.hsums = c.take<uint16_t>(Pd * (L.I / 8));
     D.hs_hi = c.take<uint16_t>(Td * (L.Ish > 0 ? L.Ish : 2));
     D.hs_lo = c.take<uint16_t>(Td * (L.Ish > 0 ? L.Ish : 2));
     D.ye = c.take<float>(Pd * L.H);
@@ -801,12 +797,10 @@ int run_decode(ds4moe *h, const void *x, int T, float *y, const int32_t *forced_
         a.nuniq = D.nuniq;
         a.inv = D.inv;
         a.xq = D.xq;
-        a.xoff = D.xoff;
-        a.xsum = D.xsum;
+        a.xsums = D.xsums;
         a.hq_hi = D.hq_hi;
         a.hq_lo = D.hq_lo;
-        a.hoff = D.hoff;
-        a.hsum = D.hsum;
+        a.hsums = D.hsums;
         a.hs_hi = D.hs_hi;
         a.hs_lo = D.hs_lo;
         a.ye = D.ye;
@@ -1044,7 +1038,7 @@ int ds4moe_create(const ds4moe_layer_desc *desc, const ds4moe_weights *w, ds4moe
             const_cast<float *>(L.gain));
     DecodeState &D = h->D;
     auto rf2 = [&](const void *src, Q2Frag &m) {
-        const int64_t n = (m.rows / 16) * m.nkc * 32;
+        const int64_t n = (m.rows / 16) * (m.nkc / 2) * 32; // one thread per (tile, block, lane)
         repack_q2_frag_kernel<<<blocks_for(n, 256), 256, 0, st>>>(static_cast<const uint8_t *>(src), m.rows, m.nkc / 2,
                                                                    const_cast<uint8_t *>(m.rec));
     };

@@ -1,33 +1,37 @@
 // Fragment-major weight layouts for the tensor-core GEMV of the decode path.
 //
 // A warp multiplies a tile of 16 weight rows by the activations with
-// mma.sync.m16n8k16 (A = weights, row-major 16x16 per chunk of 16 columns).
-// The layouts below store each (16-row tile, column range) so that lane
-// l = 4*g + tig fetches exactly the bits its A fragment needs with one 16-byte
-// load, and a warp's 32 loads cover one contiguous 512-byte span.
+// mma.sync.m16n8k16 (A = weights, 16 rows x 16 k per MMA; B = activations,
+// 16 k x 8 token columns). The layouts below store each (16-row tile, column
+// range) so that lane l = 4*g + tig fetches exactly the bits its A fragment
+// needs with 16-byte loads, and a warp's loads cover contiguous 512-byte spans.
 //
-// 2-bit codes, per (tile, kc), kc = 128-column chunk: lane l holds a uint4
-//   { W(g, G0), W(g+8, G0), W(g, G1), W(g+8, G1) },  G0 = 2kc, G1 = 2kc+1
-// where W(row, G) packs the 16 codes of `row` at columns 64G + 16c + 2tig + o
-// (+0 and +1), c = 0..3, o in {0, 8}. Register r = 2c + o/8 of the fragment
-// takes the code of column k at bit s_r + p_r and of column k+1 at bit
-// 16 + s_r + p_r, with (s_r, p_r) = (0,0) (0,2) (0,4) (6,0) (6,2) (6,4) (12,0)
-// (12,2). After shifting the word right by s_r, one LOP3
-//   (v & (3 << p | 3 << (16 + p))) | 0x3F803F80
-// yields the bf16 pair (1 + q_k 2^(p-7), 1 + q_(k+1) 2^(p-7)) exactly.
-// The activations are pre-scaled by 2^(7-p) per column, so each product is
-// x_k 2^(7-p) + q_k x_k and the per-sub-block offset sum_k x_k 2^(7-p) is
-// subtracted in the epilogue.
-//
-// Scale/min bytes, per (tile, kc): 8 x uint4; entry g holds the 8 scale bytes
-// (one per 16-column sub-block of the chunk) of row g (bytes 0-7) and row g+8
-// (bytes 8-15). d/dmin, per (tile, 256-column block): 8 x uint2; entry g holds
-// the d|dmin word of row g and of row g+8.
-// All three sit together, one 1344-byte record per (tile, 256-column block)
-// (the 84 bytes of each of its 16 rows' blocks): codes of the block's two
-// chunks (2 x 512 B), their scale entries (2 x 128 B), the d/dmin entries
-// (64 B). A tile's column range is one contiguous run of records, so a stage
-// of one matrix tile is a single bulk copy.
+// 2-bit blocks: one 1344-byte record per (16-row tile, 256-column block) (the
+// 84 bytes of each of its 16 rows' blocks). Inside a block the MMA's k index
+// is the 16-weight sub-block j and MMA number c (0..15) takes column 16 j + c
+// of every sub-block, so lane (g, tig) meets the same sub-blocks
+// {2tig, 2tig+1} (fragment registers a0, a1) and {2tig+8, 2tig+9} (a2, a3) of
+// rows g and g+8 in all 16 MMAs of a block: their scales are turned into
+// multipliers once per block.
+//   codes   [0, 1024): lane l's 32 bytes are words W0..W7 (W0..W3 at 16 l,
+//           W4..W7 at 512 + 16 l). Words W(2i), W(2i+1) hold MMAs c = 4i..4i+3:
+//           each A register (row g + 8 rho, sub-block pair kappa) is two codes
+//           at bits s + 2p of the low and high halves of one word (the low half
+//           the even sub-block), placed by q2_slot below; one LOP3 with 0x4300
+//           makes the bf16 pair 128 + q 4^p exactly (p <= 2). Within an MMA
+//           the two rows of a sub-block pair share p, so p(c, kappa) can be
+//           undone on the activation side.
+//   scales  [1024, 1280): lane l, uint2 {row g, row g+8}; each word holds
+//           sc(2tig), sc(2tig+8), m(2tig), m(2tig+8) in nibbles 0..3 and
+//           sc(2tig+1), sc(2tig+9), m(2tig+1), m(2tig+9) in nibbles 4..7,
+//           so one LOP3 (after a shift of 0, 4, 8 or 12) gives the bf16 pair
+//           128 + v for the two sub-blocks of a register.
+//   d/dmin  [1280, 1344): entry g (uint2) = the d | dmin << 16 words of rows g
+//           and g + 8.
+// With the sub-block scale folded in, A = (128 + q 4^p) sc - 128 sc = sc q 4^p
+// (one packed bf16 FMA, exact), the activations are x 4^-p (exact), so every
+// product is sc q x exactly; the min term sum_j m_j (sum of x over j) is two
+// more MMAs per block (m as exact bf16, the sums as a bf16 hi + lo pair).
 //
 // 8-bit codes, per (tile, bq), bq = 32-column block: lane l holds a uint4
 //   { V(g, 0), V(g+8, 0), V(g, 1), V(g+8, 1) }
@@ -46,6 +50,42 @@ namespace ds4 {
 
 constexpr int kQ2Rec = 1344; // bytes per (16-row tile, 256-column block) record
 constexpr int kQ2RecScales = 1024, kQ2RecDm = 1280; // offsets of the scale and d/dmin entries
+
+// Where the two codes of A register (rho, kappa) of MMA c = 4 i + cl live:
+// word W(2i + w) shifted right by s, at bit 2p of each half, for row g (rho 0)
+// and row g + 8 (rho 1). Every (word, s, p) slot of a word pair is used once.
+struct Q2Slot {
+    int w0, s0, w1, s1, p;
+};
+__host__ __device__ constexpr Q2Slot q2_slot(int cl, int kappa) {
+    return cl == 0 ? (kappa == 0 ? Q2Slot{0, 0, 0, 6, 0} : Q2Slot{0, 0, 0, 6, 1})
+         : cl == 1 ? (kappa == 0 ? Q2Slot{0, 0, 0, 6, 2} : Q2Slot{0, 12, 1, 0, 0})
+         : cl == 2 ? (kappa == 0 ? Q2Slot{0, 12, 1, 0, 1} : Q2Slot{1, 0, 1, 6, 2})
+                   : (kappa == 0 ? Q2Slot{1, 6, 1, 12, 0} : Q2Slot{1, 6, 1, 12, 1});
+}
+
+// Exponent p of the activations of MMA c, sub-block pair kappa (the B side
+// carries the factor 4^-p).
+__host__ __device__ constexpr int q2_p(int c, int kappa) { return q2_slot(c & 3, kappa).p; }
+
+// Position of column k (0..K) in the permuted activation layout of the decode
+// kernel: per 256-column block, per MMA c, per tig: the bf16 pairs of the
+// sub-blocks (2tig, 2tig+1) then (2tig+8, 2tig+9). Returns the element index.
+__host__ __device__ constexpr int64_t q2_act_index(int64_t k) {
+    const int64_t b = k >> 8;
+    const int j = (int)((k >> 4) & 15), c = (int)(k & 15);
+    const int kappa = j >> 3, tig = (j & 7) >> 1, half = j & 1;
+    return (((b * 16 + c) * 4 + tig) * 2 + kappa) * 2 + half;
+}
+
+// Position of the sum of sub-block j of block b in the permuted sum layout:
+// per block, hi parts then lo parts, each per tig the pairs (2tig, 2tig+1),
+// (2tig+8, 2tig+9). part: 0 hi, 1 lo.
+__host__ __device__ constexpr int64_t q2_sum_index(int64_t b, int j, int part) {
+    const int kappa = j >> 3, tig = (j & 7) >> 1, half = j & 1;
+    return ((b * 2 + part) * 4 + tig) * 4 + kappa * 2 + half;
+}
+
 constexpr int kQ8Rec = 544;  // bytes per (16-row tile, 32-column block) record
 constexpr int kQ8RecD = 512; // offset of the scale entries
 
@@ -61,73 +101,56 @@ struct Q8Frag {
     int32_t nbq;        // K / 32
 };
 
-__host__ __device__ constexpr int frag_shift(int r) { return r < 3 ? 0 : (r < 6 ? 6 : 12); }
-__host__ __device__ constexpr int frag_pos(int r) { return r < 3 ? 2 * r : (r < 6 ? 2 * (r - 3) : 2 * (r - 6)); }
-
-// Pre-scale exponent of column k for the 2-bit fragment: 7 - p of the register
-// holding it (depends on k mod 64 only).
-__host__ __device__ inline int frag_exp(int k) {
-    const int c = (k & 63) >> 4, o = (k & 15) >= 8 ? 1 : 0;
-    return 7 - frag_pos(2 * c + o);
-}
-
 // Canonical 2-bit block field readers (84-byte blocks, see include/ds4moe.h).
-__device__ __forceinline__ int canon_code(const uint8_t *src, int64_t row, int nb, int k) {
-    const uint8_t *blk = src + (row * nb + (k >> 8)) * kQ2Bytes;
-    const int i = k & 255;
-    return (blk[16 + (i >> 2)] >> (2 * (i & 3))) & 3;
+__device__ __forceinline__ const uint8_t *canon_block(const uint8_t *src, int64_t row, int nb, int blk) {
+    return src + (row * nb + blk) * kQ2Bytes;
 }
 
-__device__ __forceinline__ uint32_t canon_word2(const uint8_t *src, int64_t row, int nb, int G, int tig) {
-    uint32_t w = 0;
-#pragma unroll
-    for (int r = 0; r < 8; r++) {
-        const int k = 64 * G + 16 * (r >> 1) + 2 * tig + 8 * (r & 1);
-        const int b = frag_shift(r) + frag_pos(r);
-        w |= (uint32_t)canon_code(src, row, nb, k) << b;
-        w |= (uint32_t)canon_code(src, row, nb, k + 1) << (16 + b);
-    }
-    return w;
-}
+__device__ __forceinline__ uint32_t canon_code(const uint8_t *blk, int i) { return (blk[16 + (i >> 2)] >> (2 * (i & 3))) & 3u; }
 
-// One thread per (tile, kc, lane): codes; lanes < 8 also write the scale entry
-// of (tile, kc, g = lane); even kc also writes the d/dmin entry of the block.
+// One thread per (tile, 256-column block, lane): the lane's code words, its
+// scale words and (tig == 0) the d/dmin entry of its row pair.
 __global__ void repack_q2_frag_kernel(const uint8_t *__restrict__ src, int64_t rows, int nb, uint8_t *__restrict__ rec) {
-    const int nkc = nb * 2;
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    const int64_t total = (rows / 16) * nkc * 32;
+    const int64_t total = (rows / 16) * nb * 32;
     if (i >= total)
         return;
     const int lane = (int)(i & 31);
-    const int kc = (int)((i >> 5) % nkc);
-    const int64_t tile = (i >> 5) / nkc;
+    const int blk = (int)((i >> 5) % nb);
+    const int64_t tile = (i >> 5) / nb;
     const int g = lane >> 2, tig = lane & 3;
-    const int64_t r0 = tile * 16 + g, r1 = r0 + 8;
-    uint8_t *const rec_blk = rec + (tile * nb + (kc >> 1)) * kQ2Rec; // this block's record
-    reinterpret_cast<uint4 *>(rec_blk + (kc & 1) * 512)[lane] =
-        make_uint4(canon_word2(src, r0, nb, 2 * kc, tig), canon_word2(src, r1, nb, 2 * kc, tig),
-                   canon_word2(src, r0, nb, 2 * kc + 1, tig), canon_word2(src, r1, nb, 2 * kc + 1, tig));
-    if (lane < 8) {
-        const int64_t ra = tile * 16 + lane, rb = ra + 8;
-        const int blk = kc >> 1, j0 = (kc & 1) * 8; // 8 sub-blocks of this chunk within the block
-        const uint8_t *sa = src + (ra * nb + blk) * kQ2Bytes + j0;
-        const uint8_t *sb = src + (rb * nb + blk) * kQ2Bytes + j0;
-        uint32_t v[4] = {0, 0, 0, 0};
-#pragma unroll
-        for (int j = 0; j < 4; j++) {
-            v[0] |= (uint32_t)sa[j] << (8 * j);
-            v[1] |= (uint32_t)sa[4 + j] << (8 * j);
-            v[2] |= (uint32_t)sb[j] << (8 * j);
-            v[3] |= (uint32_t)sb[4 + j] << (8 * j);
+    const uint8_t *rb[2] = {canon_block(src, tile * 16 + g, nb, blk), canon_block(src, tile * 16 + g + 8, nb, blk)};
+    uint8_t *const out = rec + (tile * nb + blk) * kQ2Rec;
+    uint32_t w[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+    for (int c = 0; c < 16; c++) {
+        const int pair = c >> 2, cl = c & 3;
+        for (int kappa = 0; kappa < 2; kappa++) {
+            const Q2Slot sl = q2_slot(cl, kappa);
+            for (int rho = 0; rho < 2; rho++) {
+                const int word = 2 * pair + (rho ? sl.w1 : sl.w0);
+                const int bit = (rho ? sl.s1 : sl.s0) + 2 * sl.p;
+                for (int half = 0; half < 2; half++) {
+                    const int j = 2 * tig + 8 * kappa + half; // sub-block
+                    w[word] |= canon_code(rb[rho], 16 * j + c) << (16 * half + bit);
+                }
+            }
         }
-        reinterpret_cast<uint4 *>(rec_blk + kQ2RecScales + (kc & 1) * 128)[lane] = make_uint4(v[0], v[1], v[2], v[3]);
-        if ((kc & 1) == 0) {
-            const uint8_t *da = src + (ra * nb + blk) * kQ2Bytes + 80;
-            const uint8_t *db = src + (rb * nb + blk) * kQ2Bytes + 80;
-            const uint32_t wa = da[0] | (da[1] << 8) | (da[2] << 16) | ((uint32_t)da[3] << 24);
-            const uint32_t wb = db[0] | (db[1] << 8) | (db[2] << 16) | ((uint32_t)db[3] << 24);
-            reinterpret_cast<uint2 *>(rec_blk + kQ2RecDm)[lane] = make_uint2(wa, wb);
-        }
+    }
+    reinterpret_cast<uint4 *>(out)[lane] = make_uint4(w[0], w[1], w[2], w[3]);
+    reinterpret_cast<uint4 *>(out + 512)[lane] = make_uint4(w[4], w[5], w[6], w[7]);
+    uint32_t s[2];
+    for (int rho = 0; rho < 2; rho++) {
+        const uint8_t *sc = rb[rho]; // scales[16]: low nibble sc, high nibble m
+        const uint32_t j0 = sc[2 * tig], j1 = sc[2 * tig + 1], j2 = sc[2 * tig + 8], j3 = sc[2 * tig + 9];
+        s[rho] = (j0 & 15u) | (j2 & 15u) << 4 | (j0 >> 4) << 8 | (j2 >> 4) << 12 | (j1 & 15u) << 16 |
+                 (j3 & 15u) << 20 | (j1 >> 4) << 24 | (j3 >> 4) << 28;
+    }
+    reinterpret_cast<uint2 *>(out + kQ2RecScales)[lane] = make_uint2(s[0], s[1]);
+    if (tig == 0) {
+        const uint8_t *da = rb[0] + 80, *db = rb[1] + 80;
+        const uint32_t wa = da[0] | (da[1] << 8) | (da[2] << 16) | ((uint32_t)da[3] << 24);
+        const uint32_t wb = db[0] | (db[1] << 8) | (db[2] << 16) | ((uint32_t)db[3] << 24);
+        reinterpret_cast<uint2 *>(out + kQ2RecDm)[g] = make_uint2(wa, wb);
     }
 }
 
