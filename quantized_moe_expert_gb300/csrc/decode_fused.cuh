@@ -64,11 +64,12 @@ namespace ds4 {
 constexpr int kDecodeT = 8;             // tokens per launch
 constexpr int kMaxSlots = 64;           // distinct experts per launch <= 8 tokens * top-8
 constexpr uint64_t kWaitNs = 500000000; // 0.5 s
-constexpr int kRing = 2;                // shared-memory stages per CTA (two CTAs per SM)
-constexpr int kSlotBytes = 43008;       // bytes per stage (fewer, larger stages measured faster)
+constexpr int kRing = 3;                // shared-memory stages per CTA (two CTAs per SM)
+constexpr int kSlotBytes = 33792;       // bytes per stage
 constexpr int kConsumerWarps = 8;
-// the selection job's keys ([T][E]) and bias ([E]) fit its stage buffer (E <= 1024)
-static_assert(4 * (kDecodeT + 1) * 1024 <= kSlotBytes, "selection scratch");
+// the selection job's keys ([T][E]) fit its stage buffer, the bias ([E]) the
+// reduction buffer (E <= 1024)
+static_assert(4 * kDecodeT * 1024 <= kSlotBytes, "selection scratch");
 constexpr int kPubQ = 4; // publication tasks in flight (consumers -> publisher warp)
 // consumers, the producer warp and the publisher warp
 constexpr int kDecodeThreads = 32 * (kConsumerWarps + 2);
@@ -150,7 +151,8 @@ struct DecodeSmem {
     StageDesc desc[kRing];
     alignas(8) uint64_t full[kRing];
     alignas(8) uint64_t empty[kRing];
-    float part[2][kConsumerWarps][2][16][kDecodeT]; // per-warp partial sums, double-buffered by job
+    float part[kConsumerWarps][2][16][kDecodeT]; // per-warp partial sums of the job being finished
+                                                 // (the selection job: the router bias)
     // publication tasks: what the publisher warp makes visible GPU-wide after a job
     struct PubTask {
         unsigned *ctr; // the job count to increase, or the tile counter
@@ -168,12 +170,17 @@ struct DecodeSmem {
     int pair_at[kMaxSlots]; // grouping: the pair at each expert-grouped position
     unsigned rec[2][kMaxSlots]; // grouping: the slot records before publication
     int sel_flag[2];            // selection: give-up decision of thread 0, double-buffered by poll round
+    // the producer's next stage, built before its ring slot is free
+    StageDesc pdesc;
+    // the routing records of this launch (raw words), cached by the producer
+    unsigned rcache[kMaxSlots][2];
     // the producer's list of bulk copies for the stage it is building
     const void *pc_src[40];
     unsigned pc_bytes[40];
     unsigned pc_dst[40];
     int cexp[kDecodeT * kMaxTopK]; // publisher, with down gains: the experts of the tile's pairs
 };
+static_assert(sizeof(DecodeSmem::part) >= 4 * 1024, "router bias staging");
 
 // ---- small PTX helpers --------------------------------------------------------
 
@@ -522,8 +529,7 @@ __device__ __forceinline__ void q2_stage(const uint8_t *sl, const StageDesc &d, 
 
 // Partial sums of a 2-bit job (q2_stage's layout: each (row, token) in one
 // lane) into the warp's slot of the job's reduction buffer.
-__device__ __forceinline__ void store_part_q2(DecodeSmem &sm, int buf, int warp, int lane, const float (&out)[2][2][2],
-                                              int ntok) {
+__device__ __forceinline__ void store_part_q2(DecodeSmem &sm, int warp, int lane, const float (&out)[2][2][2], int ntok) {
     const int g = lane >> 2, tig = lane & 3;
 #pragma unroll
     for (int m = 0; m < 2; m++)
@@ -531,8 +537,8 @@ __device__ __forceinline__ void store_part_q2(DecodeSmem &sm, int buf, int warp,
         for (int col = 0; col < 2; col++) {
             const int t = 2 * tig + col;
             if (t < ntok) {
-                sm.part[buf][warp][m][g][t] = out[m][0][col];
-                sm.part[buf][warp][m][g + 8][t] = out[m][1][col];
+                sm.part[warp][m][g][t] = out[m][0][col];
+                sm.part[warp][m][g + 8][t] = out[m][1][col];
             }
         }
 }
@@ -652,7 +658,7 @@ template <int TP> __device__ __forceinline__ bool tile_owner(int lane) {
 }
 
 template <int TP, int NMAT>
-__device__ __forceinline__ void store_part(DecodeSmem &sm, int buf, int warp, int lane, const float (&out)[2][2][2]) {
+__device__ __forceinline__ void store_part(DecodeSmem &sm, int warp, int lane, const float (&out)[2][2][2]) {
     if (!tile_owner<TP>(lane))
         return;
     const int g = lane >> 2;
@@ -663,8 +669,8 @@ __device__ __forceinline__ void store_part(DecodeSmem &sm, int buf, int warp, in
             if (TP == 1 && col == 1)
                 continue;
             const int t = (2 * (lane & 3) + col) % TP;
-            sm.part[buf][warp][m][g][t] = out[m][0][col];
-            sm.part[buf][warp][m][g + 8][t] = out[m][1][col];
+            sm.part[warp][m][g][t] = out[m][0][col];
+            sm.part[warp][m][g + 8][t] = out[m][1][col];
         }
 }
 
@@ -772,9 +778,9 @@ __device__ __forceinline__ void select_token(const DecodeArgs &a, const SelIO &i
 // Work of the selection job that needs no router output (all consumer
 // threads, before the wait for the router rows): the activations in the
 // 2-bit GEMV's permuted layout (x 4^-p, exact) with their 16-column sums as a
-// bf16 hi + lo pair, zeroed expert counts, and the router bias staged into the
-// job's stage buffer (bias at float offset kDecodeT * E of scratch).
-__device__ void select_prepare(const DecodeArgs &a, float *scratch) {
+// bf16 hi + lo pair, zeroed expert counts, and the router bias staged into
+// shared memory (the reduction buffer, free during the selection job).
+__device__ void select_prepare(const DecodeArgs &a, float *bias) {
     const int T = a.T, E = a.E, H = a.H;
     // thread i takes sub-blocks i, i + 256, ... of every token
     const int nsub = H / 16;
@@ -802,7 +808,7 @@ __device__ void select_prepare(const DecodeArgs &a, float *scratch) {
     for (int e = threadIdx.x; e < E; e += 32 * kConsumerWarps) {
         a.counts[e] = 0;
         if (!a.forced_idx)
-            scratch[kDecodeT * E + e] = a.router_bias ? __ldg(a.router_bias + e) : 0.f;
+            bias[e] = a.router_bias ? __ldg(a.router_bias + e) : 0.f;
     }
 }
 
@@ -817,7 +823,7 @@ __device__ __forceinline__ bool job_select(const DecodeArgs &a, const SelIO &io,
     const int T = a.T, E = a.E, K = a.K;
     unsigned *keys = reinterpret_cast<unsigned *>(scratch);
     if (!a.forced_idx) {
-        const float *bias = scratch + kDecodeT * E;
+        const float *bias = &sm.part[0][0][0][0];
         const int n = T * E;
         constexpr int kStride = 32 * kConsumerWarps;
         // thread i owns entries i, i + 256, ... (at most 32 of them: T E <= 8192);
@@ -1153,7 +1159,7 @@ __device__ __forceinline__ int pick_w_q2(int K, int ntok, bool split) {
 // after their dependency wait (data other CTAs are still producing).
 struct StageWriter {
     DecodeSmem &sm;
-    int slot;
+    int slot = -1; // ring slot, set once claimed
     // Most pieces of one stage: a D stage with 8 tokens has 3 weight pieces and
     // 4 activation pieces per token (hi, lo, offsets, sums) = 35.
     static constexpr int kMaxPieces = 40;
@@ -1164,7 +1170,7 @@ struct StageWriter {
     unsigned *dst;
     int np = 0;
     bool overflow = false;
-    __device__ StageWriter(DecodeSmem &s, int sl) : sm(s), slot(sl), src(s.pc_src), bytes(s.pc_bytes), dst(s.pc_dst) {}
+    __device__ explicit StageWriter(DecodeSmem &s) : sm(s), src(s.pc_src), bytes(s.pc_bytes), dst(s.pc_dst) {}
     __device__ int put(const void *p, unsigned n) {
         const int o = (int)off;
         if (np == kMaxPieces) { // cannot happen with the stage shapes above; never write past the arrays
@@ -1224,16 +1230,15 @@ struct StageWriter {
 };
 
 // The routing record of distinct-expert slot `sl`, polled until it carries this
-// launch's epoch (bounded). The acquire orders the later copies of data the
-// selection wrote before publishing the record.
-__device__ bool wait_slot(const DecodeArgs &a, int sl, SlotRec &r) {
+// launch's epoch (bounded); raw words out.
+__device__ bool wait_slot(const DecodeArgs &a, int sl, unsigned &w0, unsigned &w1) {
     uint64_t t0 = 0;
     for (unsigned it = 0;; it++) {
         const unsigned long long v0 = ld_acquire_u64(a.srec + 2 * sl);
         const unsigned long long v1 = ld_acquire_u64(a.srec + 2 * sl + 1);
         if ((unsigned)(v0 >> 32) == a.epoch && (unsigned)(v1 >> 32) == a.epoch) {
-            r = unpack_slot((unsigned)v0, (unsigned)v1);
-            asm volatile("fence.proxy.async.global;" ::: "memory");
+            w0 = (unsigned)v0;
+            w1 = (unsigned)v1;
             return true;
         }
         if ((it & 63) == 0) {
@@ -1252,25 +1257,44 @@ __device__ bool wait_slot(const DecodeArgs &a, int sl, SlotRec &r) {
     }
 }
 
+// Every routing record of the launch into shared memory (the selection
+// publishes them together): lane l polls slots l, l + 32 (the whole producer
+// warp). The acquires order the later bulk copies of data the selection wrote
+// before publishing. Returns false if a wait gave up.
+__device__ bool load_records(const DecodeArgs &a, const JobSpace &js, DecodeSmem &sm) {
+    bool good = true;
+    for (int sl = threadIdx.x & 31; sl < js.Umax && good; sl += 32) {
+        unsigned w0 = 0, w1 = 0;
+        good = wait_slot(a, sl, w0, w1);
+        sm.rcache[sl][0] = w0;
+        sm.rcache[sl][1] = w1;
+    }
+    good = __all_sync(0xFFFFFFFFu, good);
+    __threadfence();
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    return good;
+}
+
 template <bool GAIN> __device__ void producer(const DecodeArgs &a, DecodeSmem &sm, const JobSpace &js) {
-    unsigned n = 0; // stages issued so far
-    int cached_slot = -1; // GU and D jobs come slot by slot: keep the last record
-    SlotRec rec{};
+    const int lane = threadIdx.x & 31;
+    unsigned n = 0;        // stages issued so far
+    bool have_recs = false; // the launch's routing records are in sm.rcache
     // claim the next ring slot (waits until the consumers released it)
     auto claim = [&](int &slot) -> bool {
         slot = (int)(n % kRing);
         return mbar_wait(a, &sm.empty[slot], ((n / kRing) & 1u) ^ 1u);
     };
     bool ok = true;
-    // the first job of each CTA is its own index; later ones come from the queue,
-    // claimed one job ahead so that the atomic's round trip overlaps this job's work
-    // (the whole warp runs this loop; lane 0 takes the job and all lanes get it)
-    auto next_job = [&]() -> int {
-        int v = 0;
-        if ((threadIdx.x & 31) == 0)
-            v = ld_relaxed(a.ctl + kCtlAbort) ? js.total
-                                               : (int)gridDim.x + (int)atomicAdd(a.ctl + kCtlJobNext, 1u);
-        return __shfl_sync(0xFFFFFFFFu, v, 0);
+    // the first job of each CTA is its own index; later ones come from the queue.
+    // Lane 0 starts the atomic; its value is read (broadcast to the warp, which
+    // runs this loop in lockstep) only once the current job's stages are issued,
+    // so the round trip overlaps that work.
+    auto start_claim = [&]() -> unsigned {
+        unsigned v = 0;
+        if (lane == 0)
+            v = ld_relaxed(a.ctl + kCtlAbort) ? (unsigned)js.total
+                                               : gridDim.x + atomicAdd(a.ctl + kCtlJobNext, 1u);
+        return v;
     };
     int j_next = (int)blockIdx.x;
     while (ok) {
@@ -1279,8 +1303,8 @@ template <bool GAIN> __device__ void producer(const DecodeArgs &a, DecodeSmem &s
             break;
         // (not during the selection or its rehearsal: the job claimed would wait
         // behind them, and a router row behind the selection would never run)
-        if (j >= js.oR)
-            j_next = next_job();
+        const bool ahead = j >= js.oR;
+        const unsigned v_next = ahead ? start_claim() : 0u;
         int type, a0 = 0, tile = 0, ntok = a.T, K = a.H, per16 = 0, nu = 0;
         int pos[kDecodeT], tok[kDecodeT]; // (compile-time indices only: registers)
 #pragma unroll
@@ -1316,21 +1340,25 @@ template <bool GAIN> __device__ void producer(const DecodeArgs &a, DecodeSmem &s
             K = a.I;
         }
         int e = 0;
+        SlotRec rec{};
         if ((type == kJobGu || type == kJobD)) {
-            if (a0 != cached_slot) {
-                if (!wait_slot(a, a0, rec))
+            if (!have_recs) {
+                if (!load_records(a, js, sm))
                     break;
-                cached_slot = a0;
+                have_recs = true;
             }
+            rec = unpack_slot(sm.rcache[a0][0], sm.rcache[a0][1]);
             nu = rec.nuniq;
-            if (a0 >= nu)
-                continue; // fewer distinct experts than the bound
+            if (a0 >= nu) { // fewer distinct experts than the bound
+                j_next = (int)__shfl_sync(0xFFFFFFFFu, v_next, 0);
+                continue;
+            }
             e = rec.e;
             ntok = rec.ntok;
             if constexpr (GAIN) {
                 // the gains of this job's 32 output rows (one 128-byte line), read by the
                 // tile's combine: on their way to L2 long before it
-                if (type == kJobD && (threadIdx.x & 31) == 0)
+                if (type == kJobD && lane == 0)
                     asm volatile("prefetch.global.L2 [%0];" ::"l"(a.gain + (int64_t)e * a.H + tile * 32));
             }
 #pragma unroll
@@ -1345,12 +1373,8 @@ template <bool GAIN> __device__ void producer(const DecodeArgs &a, DecodeSmem &s
                                                           : pick_w(K, per16);
         const int nsub = type == kJobSel ? 1 : K / W;
         for (int sub = 0; sub < nsub && ok; sub++) {
-            int slot;
-            if (!claim(slot)) {
-                ok = false;
-                break;
-            }
-            StageDesc &d = sm.desc[slot];
+            // the stage is described and its copies listed before its slot is free
+            StageDesc &d = sm.pdesc;
             d.type = type;
             d.a0 = a0;
             d.tile = tile;
@@ -1365,7 +1389,7 @@ template <bool GAIN> __device__ void producer(const DecodeArgs &a, DecodeSmem &s
                 d.pos[i] = pos[i];
                 d.tok[i] = tok[i];
             }
-            StageWriter sw(sm, slot);
+            StageWriter sw(sm);
             const int c0 = sub * W;
             // token of the job's column t (routed jobs: from the routing record)
             auto tok_of = [&](int t) -> int {
@@ -1449,27 +1473,41 @@ template <bool GAIN> __device__ void producer(const DecodeArgs &a, DecodeSmem &s
             }
             const unsigned *dep = type == kJobD ? a.ctl + kCtlGuDone + a0 : a.ctl + kCtlSguDone;
             const unsigned target = type == kJobD ? (unsigned)js.tilesI : (unsigned)js.nSGU;
+            int slot;
+            if (!claim(slot)) {
+                ok = false;
+                break;
+            }
+            {
+                int *to = reinterpret_cast<int *>(&sm.desc[slot]);
+                const int *from = reinterpret_cast<const int *>(&sm.pdesc);
+                for (int i = lane; i < (int)(sizeof(StageDesc) / sizeof(int)); i += 32)
+                    to[i] = from[i];
+            }
+            sw.slot = slot;
             n++;
             if (!sw.issue(a, dep, target)) {
                 ok = false;
                 break;
             }
         }
+        if (ahead)
+            j_next = (int)__shfl_sync(0xFFFFFFFFu, v_next, 0);
         // The selection's CTA takes no further job before the routing is
         // published (a router row queued behind the selection would never run),
         // the rehearsal's none before the rehearsal is done (a job behind it
         // would wait it out).
         if (type == kJobSel && ok) {
             if (a0 == 0) {
-                if (!wait_slot(a, 0, rec))
+                if (!load_records(a, js, sm))
                     break;
-                cached_slot = 0;
+                have_recs = true;
             } else {
                 const unsigned m = n - 1; // the rehearsal's stage: wait for its release
                 if (!mbar_wait(a, &sm.empty[m % kRing], (m / kRing) & 1u))
                     break;
             }
-            j_next = next_job();
+            j_next = (int)__shfl_sync(0xFFFFFFFFu, start_claim(), 0);
         }
     }
     // end of this CTA's jobs
@@ -1604,17 +1642,17 @@ template <int TP> struct JobOps {
     // End of a job: combine the warps' partial sums (barrier 1), write the
     // results, barrier 2, then publish (thread 0 / warp 0, without a barrier).
     static __device__ void finish(const DecodeArgs &a, const JobSpace &js, DecodeSmem &sm, const StageDesc &d,
-                                  int buf, int warp, int lane, float (&out)[2][2][2], unsigned &npub) {
+                                  int warp, int lane, float (&out)[2][2][2], unsigned &npub) {
         const int tid = threadIdx.x;
-        auto P = sm.part[buf];
+        auto &P = sm.part;
         if (d.type == kJobGu || d.type == kJobD) {
-            store_part_q2(sm, buf, warp, lane, out, d.ntok);
+            store_part_q2(sm, warp, lane, out, d.ntok);
         } else if (d.type != kJobSd) {
             reduce_out<TP, 2>(out);
-            store_part<TP, 2>(sm, buf, warp, lane, out);
+            store_part<TP, 2>(sm, warp, lane, out);
         } else {
             reduce_out<TP, 1>(out);
-            store_part<TP, 1>(sm, buf, warp, lane, out);
+            store_part<TP, 1>(sm, warp, lane, out);
         }
         consumer_sync();
         if (d.type == kJobSgu) {
@@ -1719,20 +1757,20 @@ __device__ __forceinline__ void stage_tp(int tp, const DecodeArgs &a, const uint
 
 template <int TPM>
 __device__ __forceinline__ void finish_tp(int tp, const DecodeArgs &a, const JobSpace &js, DecodeSmem &sm,
-                                          const StageDesc &d, int buf, int warp, int lane, float (&out)[2][2][2],
+                                          const StageDesc &d, int warp, int lane, float (&out)[2][2][2],
                                           unsigned &npub) {
     if (TPM == 1 || tp == 1)
-        JobOps<1>::finish(a, js, sm, d, buf, warp, lane, out, npub);
+        JobOps<1>::finish(a, js, sm, d, warp, lane, out, npub);
     else if (TPM == 2 || tp == 2)
-        JobOps<(TPM >= 2 ? 2 : 1)>::finish(a, js, sm, d, buf, warp, lane, out, npub);
+        JobOps<(TPM >= 2 ? 2 : 1)>::finish(a, js, sm, d, warp, lane, out, npub);
     else if (TPM == 4 || tp == 4)
-        JobOps<(TPM >= 4 ? 4 : 1)>::finish(a, js, sm, d, buf, warp, lane, out, npub);
+        JobOps<(TPM >= 4 ? 4 : 1)>::finish(a, js, sm, d, warp, lane, out, npub);
     else
-        JobOps<TPM>::finish(a, js, sm, d, buf, warp, lane, out, npub);
+        JobOps<TPM>::finish(a, js, sm, d, warp, lane, out, npub);
 }
 
 template <int TPM> __device__ void consumer(const DecodeArgs &a, DecodeSmem &sm, const JobSpace &js, int warp, int lane) {
-    unsigned n = 0, jobs_done = 0, npub = 0;
+    unsigned n = 0, npub = 0;
     float out[2][2][2];
     bool alive = true; // false after a failed dependency wait: drain the ring without computing
     while (true) {
@@ -1751,7 +1789,7 @@ template <int TPM> __device__ void consumer(const DecodeArgs &a, DecodeSmem &sm,
                 if (threadIdx.x < kDecodeT * kMaxTopK)
                     (&sm.sel_idx[0][0])[threadIdx.x] = 0;
                 if (d.a0 == 0)
-                    select_prepare(a, reinterpret_cast<float *>(sm.ring[slot]));
+                    select_prepare(a, &sm.part[0][0][0][0]);
                 consumer_sync();
             }
         }
@@ -1769,7 +1807,6 @@ template <int TPM> __device__ void consumer(const DecodeArgs &a, DecodeSmem &sm,
         if (last && alive) {
             if (type == kJobR) {
                 // logit of row d.a0 + r, token t: index 4 r + t of the accumulators
-                const int buf = (int)(jobs_done & 1u);
                 float *acc = &out[0][0][0];
 #pragma unroll
                 for (int i = 0; i < kDecodeT; i++) {
@@ -1777,7 +1814,7 @@ template <int TPM> __device__ void consumer(const DecodeArgs &a, DecodeSmem &sm,
                     if (t < a.T) {
                         const float v = warp_sum(acc[i]);
                         if (lane == 0)
-                            sm.part[buf][warp][0][0][i] = v;
+                            sm.part[warp][0][0][i] = v;
                     }
                 }
                 consumer_sync();
@@ -1786,12 +1823,13 @@ template <int TPM> __device__ void consumer(const DecodeArgs &a, DecodeSmem &sm,
                     if (i < kDecodeT && t < a.T) {
                         float v = 0.f;
                         for (int w = 0; w < kConsumerWarps; w++)
-                            v += sm.part[buf][w][0][0][i];
+                            v += sm.part[w][0][0][i];
                         // the epoch in the same word marks the value as this launch's
                         st_relaxed_u64(a.lgt + t * a.E + d.a0 + r,
                                        (unsigned long long)a.epoch << 32 | __float_as_uint(v));
                     }
                 }
+                consumer_sync(); // the reduction buffer is read before the next job writes it
             } else if (type == kJobSel) {
                 // one call site for the selection and its rehearsal: the same code
                 const SelIO io = d.a0 ? a.dry : a.io;
@@ -1799,10 +1837,8 @@ template <int TPM> __device__ void consumer(const DecodeArgs &a, DecodeSmem &sm,
                 if (d.a0 == 0)
                     alive = ok;
             } else {
-                const int buf = (int)(jobs_done & 1u);
-                finish_tp<TPM>(d.tp, a, js, sm, d, buf, warp, lane, out, npub);
+                finish_tp<TPM>(d.tp, a, js, sm, d, warp, lane, out, npub);
             }
-            jobs_done++;
         }
         __syncwarp();
         if (lane == 0)
