@@ -161,6 +161,7 @@ struct DecodeSmem {
     } pub[kPubQ];
     float cw[kDecodeT * kMaxTopK];   // publisher: routing weights of the tile being combined
     int cinv[kDecodeT * kMaxTopK];   // and the positions of their pairs
+    alignas(8) uint64_t reh_done; // the selection rehearsal's consumers are done with the ring
     alignas(8) uint64_t pub_full[kPubQ];
     alignas(8) uint64_t pub_empty[kPubQ];
     int sel_idx[kDecodeT][kMaxTopK];
@@ -674,36 +675,64 @@ __device__ __forceinline__ void store_part(DecodeSmem &sm, int warp, int lane, c
         }
 }
 
-// Router rows over the stage: d.tile fp32 rows of d.W columns back to back at
-// oq[0], bf16 x rows at oact; warp w takes columns [w W/8, (w+1) W/8). out
-// (as 8 floats) accumulates the partial dot product of row r and token t at
-// index 4 r + t in each lane (two rows only when T <= 4).
-__device__ __forceinline__ void router_stage(const uint8_t *sl, const StageDesc &d, int T, int warp, int lane,
-                                             float (&out)[2][2][2]) {
-    float *acc = &out[0][0][0];
-    const int n4 = d.W >> 2;
-    const int b = n4 * warp / kConsumerWarps, e = n4 * (warp + 1) / kConsumerWarps;
+// Router rows a0 .. a0 + nrows - 1 (nrows <= 2, and nrows * T <= 8) for all T
+// tokens, straight from global memory by the consumer threads (no stage):
+// thread i takes float4 columns i, i + 256, ... of each row, all its loads in
+// flight together; the warps' partial sums are added in warp order, and each
+// logit is stored with the launch's epoch in the same 64-bit word (the value
+// is its own completion flag). Ends with a consumer barrier.
+__device__ void router_rows(const DecodeArgs &a, DecodeSmem &sm, int a0, int nrows, int warp, int lane) {
+    const int T = a.T, n4 = a.H / 4;
+    float acc[kDecodeT]; // index 4 r + t with two rows (T <= 4), else t
 #pragma unroll
-    for (int r = 0; r < 2; r++) {
-        if (r >= d.tile)
-            break;
-        const float4 *wr = reinterpret_cast<const float4 *>(sl + d.oq[0] + r * 4 * d.W);
+    for (int i = 0; i < kDecodeT; i++)
+        acc[i] = 0.f;
 #pragma unroll 4
-        for (int i = b + lane; i < e; i += 32) {
-            const float4 wv = wr[i];
+    for (int q = threadIdx.x; q < n4; q += 32 * kConsumerWarps) {
+        float4 wv[2];
 #pragma unroll
-            for (int t = 0; t < kDecodeT; t++) {
-                if (t < T && 4 * r + t < kDecodeT) {
-                    const uint2 xv = reinterpret_cast<const uint2 *>(sl + d.oact + t * d.act_pitch)[i];
-                    float &c = acc[4 * r + t];
-                    c = fmaf(wv.x, __uint_as_float(xv.x << 16), c);
-                    c = fmaf(wv.y, __uint_as_float(xv.x & 0xFFFF0000u), c);
-                    c = fmaf(wv.z, __uint_as_float(xv.y << 16), c);
-                    c = fmaf(wv.w, __uint_as_float(xv.y & 0xFFFF0000u), c);
+        for (int r = 0; r < 2; r++)
+            wv[r] = r < nrows ? __ldg(reinterpret_cast<const float4 *>(a.router_w + (int64_t)(a0 + r) * a.H) + q)
+                              : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int t = 0; t < kDecodeT; t++) {
+            if (t < T) {
+                const uint2 xv = __ldg(reinterpret_cast<const uint2 *>(a.x + (int64_t)t * a.H) + q);
+                const float x0 = __uint_as_float(xv.x << 16), x1 = __uint_as_float(xv.x & 0xFFFF0000u);
+                const float x2 = __uint_as_float(xv.y << 16), x3 = __uint_as_float(xv.y & 0xFFFF0000u);
+#pragma unroll
+                for (int r = 0; r < 2; r++) {
+                    if (r < nrows && 4 * r + t < kDecodeT) {
+                        float &cc = acc[4 * r + t];
+                        cc = fmaf(wv[r].x, x0, cc);
+                        cc = fmaf(wv[r].y, x1, cc);
+                        cc = fmaf(wv[r].z, x2, cc);
+                        cc = fmaf(wv[r].w, x3, cc);
+                    }
                 }
             }
         }
     }
+#pragma unroll
+    for (int i = 0; i < kDecodeT; i++) {
+        const int t = nrows == 2 ? (i & 3) : i; // row i >> 2 (two rows) or 0
+        if (t < T) {
+            const float v = warp_sum(acc[i]);
+            if (lane == 0)
+                sm.part[warp][0][0][i] = v;
+        }
+    }
+    consumer_sync();
+    {
+        const int i = threadIdx.x, r = nrows == 2 ? i >> 2 : 0, t = nrows == 2 ? (i & 3) : i;
+        if (i < kDecodeT && t < T && r < nrows) {
+            float v = 0.f;
+            for (int w = 0; w < kConsumerWarps; w++)
+                v += sm.part[w][0][0][i];
+            st_relaxed_u64(a.lgt + t * a.E + a0 + r, (unsigned long long)a.epoch << 32 | __float_as_uint(v));
+        }
+    }
+    consumer_sync(); // the reduction buffer is read before the next job writes it
 }
 
 // Top-k of token t by one warp from the selection keys keys[e] (shared
@@ -1296,30 +1325,34 @@ template <bool GAIN> __device__ void producer(const DecodeArgs &a, DecodeSmem &s
                                                : gridDim.x + atomicAdd(a.ctl + kCtlJobNext, 1u);
         return v;
     };
+    // The consumers run the CTA's first job at once when it needs no stage (the
+    // selection, its rehearsal, router rows). Behind the selection the CTA takes
+    // no job before the routing is published (a router row queued behind it
+    // would never run), behind the rehearsal none before the rehearsal is done
+    // (a job behind it would wait it out).
     int j_next = (int)blockIdx.x;
+    if (j_next == 0) {
+        ok = load_records(a, js, sm);
+        have_recs = ok;
+    } else if (j_next < js.oR) {
+        ok = mbar_wait(a, &sm.reh_done, 0u);
+    }
+    if (ok && j_next < js.oSGU)
+        j_next = (int)__shfl_sync(0xFFFFFFFFu, start_claim(), 0);
     while (ok) {
         const int j = j_next;
         if (j >= js.total)
             break;
-        // (not during the selection or its rehearsal: the job claimed would wait
-        // behind them, and a router row behind the selection would never run)
-        const bool ahead = j >= js.oR;
-        const unsigned v_next = ahead ? start_claim() : 0u;
+        const unsigned v_next = start_claim(); // the job after this one
         int type, a0 = 0, tile = 0, ntok = a.T, K = a.H, per16 = 0, nu = 0;
         int pos[kDecodeT], tok[kDecodeT]; // (compile-time indices only: registers)
 #pragma unroll
         for (int i = 0; i < kDecodeT; i++)
             pos[i] = tok[i] = i < a.T ? i : 0;
-        if (j == 0) {
-            type = kJobSel;
-        } else if (j < js.oR) {
-            type = kJobSel; // the rehearsal: same job, dummy logits and outputs
-            a0 = 1;
-        } else if (j < js.oSGU) {
+        if (j < js.oSGU) { // router rows from the queue: the consumers read them directly
             type = kJobR;
             a0 = (j - js.oR) * js.rows;
             tile = a.E - a0 < js.rows ? a.E - a0 : js.rows; // rows of this job
-            per16 = 16 * (4 * tile + 2 * a.T);
         } else if (j < js.oGU) {
             type = kJobSgu;
             a0 = j - js.oSGU;
@@ -1368,10 +1401,10 @@ template <bool GAIN> __device__ void producer(const DecodeArgs &a, DecodeSmem &s
                 tok[i] = (int)((rec.toks >> (3 * ii)) & 7u);
             }
         }
-        const int W = type == kJobSel                      ? 0
+        const int W = type == kJobR                        ? 0
                       : (type == kJobGu || type == kJobD) ? pick_w_q2(K, ntok, type == kJobD)
                                                           : pick_w(K, per16);
-        const int nsub = type == kJobSel ? 1 : K / W;
+        const int nsub = type == kJobR ? 1 : K / W;
         for (int sub = 0; sub < nsub && ok; sub++) {
             // the stage is described and its copies listed before its slot is free
             StageDesc &d = sm.pdesc;
@@ -1395,15 +1428,7 @@ template <bool GAIN> __device__ void producer(const DecodeArgs &a, DecodeSmem &s
             auto tok_of = [&](int t) -> int {
                 return (type == kJobGu || type == kJobD) ? (int)((rec.toks >> (3 * t)) & 7u) : t;
             };
-            if (type == kJobR) {
-                d.oq[0] = (int)sw.off;
-                for (int r = 0; r < tile; r++)
-                    sw.put(a.router_w + (int64_t)(a0 + r) * a.H + c0, 4u * W);
-                d.act_pitch = 2 * W;
-                d.oact = (int)sw.off;
-                for (int t = 0; t < a.T; t++)
-                    sw.put(a.x + (int64_t)t * a.H + c0, 2u * W);
-            } else if (type == kJobSgu) {
+            if (type == kJobSgu) {
                 const Q8Frag *M[2] = {&a.sh_gate, &a.sh_up};
                 for (int m = 0; m < 2; m++) {
                     const int64_t u = (int64_t)a0 * M[m]->nbq + c0 / 32;
@@ -1491,24 +1516,7 @@ template <bool GAIN> __device__ void producer(const DecodeArgs &a, DecodeSmem &s
                 break;
             }
         }
-        if (ahead)
-            j_next = (int)__shfl_sync(0xFFFFFFFFu, v_next, 0);
-        // The selection's CTA takes no further job before the routing is
-        // published (a router row queued behind the selection would never run),
-        // the rehearsal's none before the rehearsal is done (a job behind it
-        // would wait it out).
-        if (type == kJobSel && ok) {
-            if (a0 == 0) {
-                if (!load_records(a, js, sm))
-                    break;
-                have_recs = true;
-            } else {
-                const unsigned m = n - 1; // the rehearsal's stage: wait for its release
-                if (!mbar_wait(a, &sm.empty[m % kRing], (m / kRing) & 1u))
-                    break;
-            }
-            j_next = (int)__shfl_sync(0xFFFFFFFFu, start_claim(), 0);
-        }
+        j_next = (int)__shfl_sync(0xFFFFFFFFu, v_next, 0);
     }
     // end of this CTA's jobs
     int slot;
@@ -1773,6 +1781,31 @@ template <int TPM> __device__ void consumer(const DecodeArgs &a, DecodeSmem &sm,
     unsigned n = 0, npub = 0;
     float out[2][2][2];
     bool alive = true; // false after a failed dependency wait: drain the ring without computing
+    // The CTA's first job is its own index and needs no stage: the selection
+    // (its keys in ring slot 0, which the producer leaves alone until the
+    // routing is published), the rehearsal, or router rows run at once.
+    {
+        const int j0 = (int)blockIdx.x;
+        if (j0 < js.oR) {
+            const bool real = j0 == 0;
+            if (threadIdx.x < kDecodeT * kMaxTopK)
+                (&sm.sel_idx[0][0])[threadIdx.x] = 0;
+            if (real)
+                select_prepare(a, &sm.part[0][0][0][0]);
+            consumer_sync();
+            const bool ok = job_select(a, real ? a.io : a.dry, sm, reinterpret_cast<float *>(sm.ring[0]), warp, lane);
+            if (real) {
+                alive = ok;
+            } else {
+                consumer_sync(); // done with ring slot 0
+                if (threadIdx.x == 0)
+                    mbar_arrive(&sm.reh_done);
+            }
+        } else if (j0 < js.oSGU) {
+            const int a0 = (j0 - js.oR) * js.rows;
+            router_rows(a, sm, a0, a.E - a0 < js.rows ? a.E - a0 : js.rows, warp, lane);
+        }
+    }
     while (true) {
         const int slot = (int)(n % kRing);
         if (!mbar_wait(a, &sm.full[slot], (n / kRing) & 1u))
@@ -1785,60 +1818,21 @@ template <int TPM> __device__ void consumer(const DecodeArgs &a, DecodeSmem &sm,
 #pragma unroll
             for (int i = 0; i < 8; i++)
                 (&out[0][0][0])[i] = 0.f;
-            if (type == kJobSel && alive) {
-                if (threadIdx.x < kDecodeT * kMaxTopK)
-                    (&sm.sel_idx[0][0])[threadIdx.x] = 0;
-                if (d.a0 == 0)
-                    select_prepare(a, &sm.part[0][0][0][0]);
-                consumer_sync();
-            }
         }
         if (alive) {
             if (type == kJobR)
-                router_stage(sm.ring[slot], d, a.T, warp, lane, out);
+                router_rows(a, sm, d.a0, d.tile, warp, lane);
             else if (type == kJobGu)
                 q2_stage<2, false>(sm.ring[slot], d, warp, lane, out);
             else if (type == kJobD)
                 q2_stage<2, true>(sm.ring[slot], d, warp, lane, out);
-            else if (type != kJobSel)
+            else
                 stage_tp<TPM>(d.tp, a, sm.ring[slot], d, warp, lane, out);
         }
         const bool last = d.sub == d.nsub - 1;
         if (last && alive) {
-            if (type == kJobR) {
-                // logit of row d.a0 + r, token t: index 4 r + t of the accumulators
-                float *acc = &out[0][0][0];
-#pragma unroll
-                for (int i = 0; i < kDecodeT; i++) {
-                    const int t = d.tile == 2 ? (i & 3) : i; // row i >> 2 (two rows) or 0
-                    if (t < a.T) {
-                        const float v = warp_sum(acc[i]);
-                        if (lane == 0)
-                            sm.part[warp][0][0][i] = v;
-                    }
-                }
-                consumer_sync();
-                {
-                    const int i = threadIdx.x, r = d.tile == 2 ? i >> 2 : 0, t = d.tile == 2 ? (i & 3) : i;
-                    if (i < kDecodeT && t < a.T) {
-                        float v = 0.f;
-                        for (int w = 0; w < kConsumerWarps; w++)
-                            v += sm.part[w][0][0][i];
-                        // the epoch in the same word marks the value as this launch's
-                        st_relaxed_u64(a.lgt + t * a.E + d.a0 + r,
-                                       (unsigned long long)a.epoch << 32 | __float_as_uint(v));
-                    }
-                }
-                consumer_sync(); // the reduction buffer is read before the next job writes it
-            } else if (type == kJobSel) {
-                // one call site for the selection and its rehearsal: the same code
-                const SelIO io = d.a0 ? a.dry : a.io;
-                const bool ok = job_select(a, io, sm, reinterpret_cast<float *>(sm.ring[slot]), warp, lane);
-                if (d.a0 == 0)
-                    alive = ok;
-            } else {
+            if (type != kJobR) // (router rows end in router_rows)
                 finish_tp<TPM>(d.tp, a, js, sm, d, warp, lane, out, npub);
-            }
         }
         __syncwarp();
         if (lane == 0)
@@ -1865,6 +1859,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_fused_kernel(DecodeA
             mbar_init(&sm.pub_full[i], 1);
             mbar_init(&sm.pub_empty[i], 1);
         }
+        mbar_init(&sm.reh_done, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
