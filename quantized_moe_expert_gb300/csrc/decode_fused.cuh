@@ -9,8 +9,8 @@
 // bulk asynchronous copies (cp.async.bulk completing on an mbarrier; its lanes
 // issue a stage's copies side by side); the
 // consumer warps multiply them on the tensor cores (mma.sync, see the layouts
-// in frag_layout.cuh) and release the stage. Two CTAs per SM, each with two
-// 42 KB stages, keep up to 168 KB per SM in flight, independent of registers.
+// in frag_layout.cuh) and release the stage. Two CTAs per SM, each with three
+// 33 KB stages, keep up to 198 KB per SM in flight, independent of registers.
 //
 // Jobs are numbered so that each depends only on jobs with smaller numbers,
 // and a CTA takes its jobs in increasing order (its first job is its own
@@ -18,19 +18,21 @@
 // always run: the queue cannot deadlock as long as all CTAs are resident,
 // which the cooperative launch guarantees. The queue, in order:
 //
-//   REH  a rehearsal of the selection on dummy logits (CTA 1's first job):
-//        the selection runs once per launch through code that starts out of
-//        every cache; the rehearsal fetches it into L2 before the real one needs it
-//   SEL  one job, the first job of CTA 0: activation pre-scaling for the
-//        2-bit MMA; then, as the router rows arrive, per-token sigmoid, exact
-//        top-k, weights and the distinct-expert grouping; publishes one
-//        record per distinct expert (waits for all R jobs)
+//   SEL  one job, the first job of CTA 0, run by its consumers at once: the
+//        activations in the 2-bit MMA's layout; the selection on dummy logits
+//        (its code starts out of every cache after each launch; the dry run
+//        fetches it while the router rows are computed); then, as the router
+//        rows arrive, per-token sigmoid, exact top-k, weights and the
+//        distinct-expert grouping; publishes one record per distinct expert
+//        (waits for all R jobs)
 //   R    one or two router rows: fp32 logits for all T tokens, each stored
 //        with the launch's epoch in the same 64-bit word (the value is its
-//        own completion flag)
+//        own completion flag); read straight from global memory by the
+//        consumers (a CTA's first job at once, later ones on a descriptor-only
+//        stage)
 //   SGU  shared expert, one 16-row tile of gate and up: h_sh = silu(g) * u
 //   GU   (distinct expert, 16-row tile of I): gate and up, h = silu(g) * u,
-//        stored as a bf16 hi/lo pair pre-scaled for the down MMA
+//        stored as a bf16 hi/lo pair in the down MMA's activation layout
 //   SD   shared expert down, one 16-row tile of H (waits: all SGU)
 //   D    (distinct expert, 32-row tile of H): down projection (waits: that
 //        expert's GU tiles); the last of the experts' contributions to a tile
@@ -161,7 +163,6 @@ struct DecodeSmem {
     } pub[kPubQ];
     float cw[kDecodeT * kMaxTopK];   // publisher: routing weights of the tile being combined
     int cinv[kDecodeT * kMaxTopK];   // and the positions of their pairs
-    alignas(8) uint64_t reh_done; // the selection rehearsal's consumers are done with the ring
     alignas(8) uint64_t pub_full[kPubQ];
     alignas(8) uint64_t pub_empty[kPubQ];
     int sel_idx[kDecodeT][kMaxTopK];
@@ -1119,10 +1120,10 @@ __device__ __forceinline__ bool job_select(const DecodeArgs &a, const SelIO &io,
 
 struct JobSpace {
     int nR, rows, nSGU, nSD, tilesI, tilesD, Umax;
-    int nREH, oR, oSGU, oSD, oGU, oD, total;
+    int oR, oSGU, oSD, oGU, oD, total;
 };
 
-// Job order: SEL, REH, R, SGU, GU, SD, D. The selection is CTA 0's first
+// Job order: SEL, R, SGU, GU, SD, D. The selection is CTA 0's first
 // job, so its consumers are idle and waiting when the last router row lands;
 // the router rows are the first jobs of the next CTAs (two rows per job while
 // both rows' accumulators fit, so that the router is one round of jobs); the
@@ -1139,8 +1140,7 @@ __host__ __device__ __forceinline__ JobSpace job_space(int E, int I, int H, int 
     s.tilesI = I / 16; // GU: one 16-row tile of gate and up
     s.tilesD = H / 32; // D: two 16-row tiles of down
     s.Umax = (T * K < E) ? T * K : E;
-    s.nREH = forced ? 0 : 1; // job 1: the selection rehearsal
-    s.oR = 1 + s.nREH;
+    s.oR = 1;
     s.oSGU = s.oR + s.nR;
     s.oGU = s.oSGU + s.nSGU;
     s.oSD = s.oGU + s.Umax * s.tilesI;
@@ -1326,16 +1326,12 @@ template <bool GAIN> __device__ void producer(const DecodeArgs &a, DecodeSmem &s
         return v;
     };
     // The consumers run the CTA's first job at once when it needs no stage (the
-    // selection, its rehearsal, router rows). Behind the selection the CTA takes
-    // no job before the routing is published (a router row queued behind it
-    // would never run), behind the rehearsal none before the rehearsal is done
-    // (a job behind it would wait it out).
+    // selection, router rows). Behind the selection the CTA takes no job before
+    // the routing is published (a router row queued behind it would never run).
     int j_next = (int)blockIdx.x;
     if (j_next == 0) {
         ok = load_records(a, js, sm);
         have_recs = ok;
-    } else if (j_next < js.oR) {
-        ok = mbar_wait(a, &sm.reh_done, 0u);
     }
     if (ok && j_next < js.oSGU)
         j_next = (int)__shfl_sync(0xFFFFFFFFu, start_claim(), 0);
@@ -1783,27 +1779,44 @@ template <int TPM> __device__ void consumer(const DecodeArgs &a, DecodeSmem &sm,
     bool alive = true; // false after a failed dependency wait: drain the ring without computing
     // The CTA's first job is its own index and needs no stage: the selection
     // (its keys in ring slot 0, which the producer leaves alone until the
-    // routing is published), the rehearsal, or router rows run at once.
+    // routing is published) or router rows run at once.
     {
         const int j0 = (int)blockIdx.x;
-        if (j0 < js.oR) {
-            const bool real = j0 == 0;
-            if (threadIdx.x < kDecodeT * kMaxTopK)
-                (&sm.sel_idx[0][0])[threadIdx.x] = 0;
-            if (real)
-                select_prepare(a, &sm.part[0][0][0][0]);
-            consumer_sync();
-            const bool ok = job_select(a, real ? a.io : a.dry, sm, reinterpret_cast<float *>(sm.ring[0]), warp, lane);
-            if (real) {
-                alive = ok;
-            } else {
-                consumer_sync(); // done with ring slot 0
-                if (threadIdx.x == 0)
-                    mbar_arrive(&sm.reh_done);
+        if (j0 == 0) {
+            // the selection runs once per launch through code that starts out of every
+            // cache: it first runs on dummy logits (epoch 0, present from the start;
+            // outputs nothing reads) while the router rows are computed
+            select_prepare(a, &sm.part[0][0][0][0]);
+            for (int pass = a.forced_idx ? 1 : 0; pass < 2; pass++) {
+                if (threadIdx.x < kDecodeT * kMaxTopK)
+                    (&sm.sel_idx[0][0])[threadIdx.x] = 0;
+                consumer_sync();
+                const bool ok =
+                    job_select(a, pass ? a.io : a.dry, sm, reinterpret_cast<float *>(sm.ring[0]), warp, lane);
+                if (pass)
+                    alive = ok;
+                consumer_sync();
             }
         } else if (j0 < js.oSGU) {
             const int a0 = (j0 - js.oR) * js.rows;
             router_rows(a, sm, a0, a.E - a0 < js.rows ? a.E - a0 : js.rows, warp, lane);
+        }
+        // the 2-bit tile code, likewise cold, runs once on whatever the reduction
+        // buffer holds (results dropped) while the routing is computed
+        if (alive) {
+            StageDesc w{};
+            w.W = 256;
+            w.ntok = 1;
+            float dummy[2][2][2] = {};
+            q2_stage<2, false>(reinterpret_cast<const uint8_t *>(&sm.part[0][0][0][0]), w, warp, lane, dummy);
+            q2_stage<2, true>(reinterpret_cast<const uint8_t *>(&sm.part[0][0][0][0]), w, warp, lane, dummy);
+            float keep = 0.f;
+#pragma unroll
+            for (int i = 0; i < 8; i++)
+                keep += (&dummy[0][0][0])[i];
+            if (keep == 1.2345e-30f) // the results must look used, or the calls vanish
+                sm.cw[0] = keep;
+            consumer_sync(); // the reduction buffer is free again for the first job's finish
         }
     }
     while (true) {
@@ -1859,7 +1872,6 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_fused_kernel(DecodeA
             mbar_init(&sm.pub_full[i], 1);
             mbar_init(&sm.pub_empty[i], 1);
         }
-        mbar_init(&sm.reh_done, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
