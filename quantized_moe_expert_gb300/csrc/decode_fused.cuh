@@ -58,6 +58,8 @@
 // its ring and leave.
 #pragma once
 
+#include <cstddef>
+
 #include "common.cuh"
 #include "frag_layout.cuh"
 
@@ -153,7 +155,9 @@ struct DecodeSmem {
     StageDesc desc[kRing];
     alignas(8) uint64_t full[kRing];
     alignas(8) uint64_t empty[kRing];
-    float part[kConsumerWarps][2][16][kDecodeT]; // per-warp partial sums of the job being finished
+    // per-warp partial sums of the job being finished; 16-byte aligned, since
+    // the 2-bit code's warm-up reads it as a stage with vector loads
+    alignas(16) float part[kConsumerWarps][2][16][kDecodeT];
                                                  // (the selection job: the router bias)
     // publication tasks: what the publisher warp makes visible GPU-wide after a job
     struct PubTask {
@@ -183,6 +187,8 @@ struct DecodeSmem {
     int cexp[kDecodeT * kMaxTopK]; // publisher, with down gains: the experts of the tile's pairs
 };
 static_assert(sizeof(DecodeSmem::part) >= 4 * 1024, "router bias staging");
+static_assert(offsetof(DecodeSmem, part) % 16 == 0, "vector loads of the warm-up stage");
+static_assert(sizeof(DecodeSmem::part) >= 2 * kQ2Rec, "the warm-up stage: two 2-bit records");
 
 // ---- small PTX helpers --------------------------------------------------------
 
