@@ -19,10 +19,8 @@
 // which the cooperative launch guarantees. The queue, in order:
 //
 //   SEL  one job, the first job of CTA 0, run by its consumers at once: the
-//        activations in the 2-bit MMA's layout; the selection on dummy logits
-//        (its code starts out of every cache after each launch; the dry run
-//        fetches it while the router rows are computed); then, as the router
-//        rows arrive, per-token sigmoid, exact top-k, weights and the
+//        activations in the 2-bit MMA's layout; then, as the router rows
+//        arrive, per-token sigmoid, exact top-k, weights and the
 //        distinct-expert grouping; publishes one record per distinct expert
 //        (waits for all R jobs)
 //   R    one or two router rows: fp32 logits for all T tokens, each stored
@@ -57,8 +55,6 @@
 // kErrTimeout in the status word and an abort flag that makes every CTA drain
 // its ring and leave.
 #pragma once
-
-#include <cstddef>
 
 #include "common.cuh"
 #include "frag_layout.cuh"
@@ -126,8 +122,7 @@ struct DecodeArgs {
     float *ysh;              // [8][H]
     unsigned *ctl;
     unsigned *status;
-    SelIO io;  // the selection's inputs and outputs (the buffers above)
-    SelIO dry; // the rehearsal's: zeroed logits with epoch 0, outputs nothing reads
+    SelIO io; // the selection's inputs and outputs (the buffers above)
     const float *gain; // [E][H] per-expert down gains (the kernel built with GAIN), or nullptr
 };
 
@@ -155,8 +150,7 @@ struct DecodeSmem {
     StageDesc desc[kRing];
     alignas(8) uint64_t full[kRing];
     alignas(8) uint64_t empty[kRing];
-    // per-warp partial sums of the job being finished; 16-byte aligned, since
-    // the 2-bit code's warm-up reads it as a stage with vector loads
+    // per-warp partial sums of the job being finished
     alignas(16) float part[kConsumerWarps][2][16][kDecodeT];
                                                  // (the selection job: the router bias)
     // publication tasks: what the publisher warp makes visible GPU-wide after a job
@@ -187,8 +181,7 @@ struct DecodeSmem {
     int cexp[kDecodeT * kMaxTopK]; // publisher, with down gains: the experts of the tile's pairs
 };
 static_assert(sizeof(DecodeSmem::part) >= 4 * 1024, "router bias staging");
-static_assert(offsetof(DecodeSmem, part) % 16 == 0, "vector loads of the warm-up stage");
-static_assert(sizeof(DecodeSmem::part) >= 2 * kQ2Rec, "the warm-up stage: two 2-bit records");
+
 
 // ---- small PTX helpers --------------------------------------------------------
 
@@ -743,36 +736,38 @@ __device__ void router_rows(const DecodeArgs &a, DecodeSmem &sm, int a0, int nro
 }
 
 // Top-k of token t by one warp from the selection keys keys[e] (shared
-// memory, e < E). Lane l owns experts l, l + 32, ...; it keeps its best
-// (key desc, index asc) and each round the warp takes the best of the 32 by
-// two warp reductions; only the lane whose candidate was taken marks it and
-// rescans its experts. One round more than K gives the (K+1)-th score for the
-// near-tie gap.
+// memory, e < E). Each expert is the 64-bit value key << 32 | ~e (larger key
+// first, then lower index; all distinct, and above 0 since keys of untaken
+// experts are >= 1). Lane l keeps the best K+1 of its experts l, l + 32, ...
+// sorted in registers; each round the warp takes the largest head by two warp
+// reductions and the owning lane shifts its list. One round more than K gives
+// the (K+1)-th score for the near-tie gap.
 __device__ __forceinline__ void select_token(const DecodeArgs &a, const SelIO &io, DecodeSmem &sm, unsigned *keys,
                                              int t, int lane) {
     const int E = a.E, K = a.K;
-    unsigned best = 0u;
-    int bi = -1;
-    auto rescan = [&]() {
-        best = 0u;
-        bi = -1;
-        for (int e = lane; e < E; e += 32) {
-            const unsigned k = keys[e];
-            if (bi < 0 || k > best) {
-                best = k;
-                bi = e;
-            }
+    constexpr int R = kMaxTopK + 1;
+    uint64_t top[R];
+#pragma unroll
+    for (int i = 0; i < R; i++)
+        top[i] = 0ull;
+    for (int e = lane; e < E; e += 32) {
+        uint64_t v = (uint64_t)keys[e] << 32 | (0xFFFFFFFFu - (unsigned)e);
+#pragma unroll
+        for (int i = 0; i < R; i++) { // insertion into the descending list
+            const uint64_t hi = top[i] > v ? top[i] : v;
+            v = top[i] > v ? v : top[i];
+            top[i] = hi;
         }
-    };
-    rescan();
+    }
     int chosen = 0;
     unsigned chosen_key = 0u;
     float kth = 0.f, next = -INFINITY;
     const int rounds = K < E ? K + 1 : K;
     for (int r = 0; r < rounds; r++) {
-        const unsigned gk = __reduce_max_sync(0xFFFFFFFFu, best);
-        const unsigned cand = (bi >= 0 && best == gk) ? (unsigned)bi : 0xFFFFFFFFu;
-        const int be = (int)__reduce_min_sync(0xFFFFFFFFu, cand); // < E: every round has a candidate
+        const unsigned hk = (unsigned)(top[0] >> 32);
+        const unsigned gk = __reduce_max_sync(0xFFFFFFFFu, hk);
+        const unsigned gl = __reduce_max_sync(0xFFFFFFFFu, hk == gk ? (unsigned)top[0] : 0u);
+        const int be = (int)(0xFFFFFFFFu - gl); // < E: every round has a candidate
         const float bv = sel_key_value(gk);
         if (r < K) {
             if (lane == r) {
@@ -781,9 +776,11 @@ __device__ __forceinline__ void select_token(const DecodeArgs &a, const SelIO &i
             }
             if (r == K - 1)
                 kth = bv;
-            if (bi == be) { // this lane's candidate was taken
-                keys[be] = 0u;
-                rescan();
+            if (hk == gk && (unsigned)top[0] == gl) { // this lane's head was taken
+#pragma unroll
+                for (int i = 0; i + 1 < R; i++)
+                    top[i] = top[i + 1];
+                top[R - 1] = 0ull;
             }
         } else {
             next = bv;
@@ -1789,40 +1786,14 @@ template <int TPM> __device__ void consumer(const DecodeArgs &a, DecodeSmem &sm,
     {
         const int j0 = (int)blockIdx.x;
         if (j0 == 0) {
-            // the selection runs once per launch through code that starts out of every
-            // cache: it first runs on dummy logits (epoch 0, present from the start;
-            // outputs nothing reads) while the router rows are computed
             select_prepare(a, &sm.part[0][0][0][0]);
-            for (int pass = a.forced_idx ? 1 : 0; pass < 2; pass++) {
-                if (threadIdx.x < kDecodeT * kMaxTopK)
-                    (&sm.sel_idx[0][0])[threadIdx.x] = 0;
-                consumer_sync();
-                const bool ok =
-                    job_select(a, pass ? a.io : a.dry, sm, reinterpret_cast<float *>(sm.ring[0]), warp, lane);
-                if (pass)
-                    alive = ok;
-                consumer_sync();
-            }
+            if (threadIdx.x < kDecodeT * kMaxTopK)
+                (&sm.sel_idx[0][0])[threadIdx.x] = 0;
+            consumer_sync();
+            alive = job_select(a, a.io, sm, reinterpret_cast<float *>(sm.ring[0]), warp, lane);
         } else if (j0 < js.oSGU) {
             const int a0 = (j0 - js.oR) * js.rows;
             router_rows(a, sm, a0, a.E - a0 < js.rows ? a.E - a0 : js.rows, warp, lane);
-        }
-        // the 2-bit tile code, likewise cold, runs once on whatever the reduction
-        // buffer holds (results dropped) while the routing is computed
-        if (alive) {
-            StageDesc w{};
-            w.W = 256;
-            w.ntok = 1;
-            float dummy[2][2][2] = {};
-            q2_stage<2, false>(reinterpret_cast<const uint8_t *>(&sm.part[0][0][0][0]), w, warp, lane, dummy);
-            q2_stage<2, true>(reinterpret_cast<const uint8_t *>(&sm.part[0][0][0][0]), w, warp, lane, dummy);
-            float keep = 0.f;
-#pragma unroll
-            for (int i = 0; i < 8; i++)
-                keep += (&dummy[0][0][0])[i];
-            if (keep == 1.2345e-30f) // the results must look used, or the calls vanish
-                sm.cw[0] = keep;
-            consumer_sync(); // the reduction buffer is free again for the first job's finish
         }
     }
     while (true) {

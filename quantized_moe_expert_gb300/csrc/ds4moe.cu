@@ -88,7 +88,6 @@ struct DecodeState {
     Q2Frag gate, up, down;
     Q8Frag sh_gate, sh_up, sh_down;
     unsigned long long *lgt = nullptr, *srec = nullptr; // epoch-tagged logits and routing records
-    SelIO dry{};                                        // the selection rehearsal's buffers
     float *gap = nullptr;
     int32_t *counts = nullptr, *nuniq = nullptr, *inv = nullptr;
     uint16_t *xq = nullptr, *xsums = nullptr;
@@ -387,15 +386,6 @@ void layout_scratch(ds4moe *h, Carver &c) {
     const int64_t Td = kDecodeT, Pd = (int64_t)kDecodeT * L.K;
     D.lgt = c.take<unsigned long long>(Td * L.E);
     D.srec = c.take<unsigned long long>(2 * kMaxSlots);
-    D.dry.lgt = c.take<unsigned long long>(Td * L.E);
-    D.dry.epoch = 0;
-    D.dry.idx = c.take<int32_t>(Pd);
-    D.dry.w = c.take<float>(Pd);
-    D.dry.gap = c.take<float>(Td);
-    D.dry.inv = c.take<int32_t>(Pd);
-    D.dry.counts = c.take<int32_t>(L.E);
-    D.dry.nuniq = c.take<int32_t>(1);
-    D.dry.srec = c.take<unsigned long long>(2 * kMaxSlots);
     D.gap = c.take<float>(Td);
     D.counts = c.take<int32_t>(L.E);
     D.nuniq = c.take<int32_t>(1);
@@ -808,7 +798,6 @@ int run_decode(ds4moe *h, const void *x, int T, float *y, const int32_t *forced_
         a.ctl = D.ctl;
         a.status = h->status;
         a.io = SelIO{a.lgt, a.epoch, a.idx, a.w, a.gap, a.inv, a.counts, a.nuniq, a.srec};
-        a.dry = D.dry;
         a.gain = L.gain;
         void *args[] = {&a};
         launch(h, "decode_fused", [&] {
@@ -1062,7 +1051,6 @@ int ds4moe_create(const ds4moe_layer_desc *desc, const ds4moe_weights *w, ds4moe
     cudaMemsetAsync(D.lgt, 0, sizeof(unsigned long long) * kDecodeT * L.E, st);
     cudaMemsetAsync(D.srec, 0, sizeof(unsigned long long) * 2 * kMaxSlots, st);
     // the rehearsal's logits: 0.0 with epoch 0, present from the start
-    cudaMemsetAsync(const_cast<unsigned long long *>(D.dry.lgt), 0, sizeof(unsigned long long) * kDecodeT * L.E, st);
     int per_sm = 0, nsm = 0;
     for (const void *fn : {(const void *)decode_fused_kernel<1>, (const void *)decode_fused_kernel<2>,
                            (const void *)decode_fused_kernel<4>, (const void *)decode_fused_kernel<8>,
