@@ -43,7 +43,7 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="decode_t1",
                     choices=["decode_t1", "decode_t8", "prefill_t1024", "prefill_t4096_zipf4", "tiny", "prefill_profile",
-                             "decode_profile"])
+                             "decode_profile", "prefill_hot_profile"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile-steps", type=int, default=20)

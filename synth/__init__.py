@@ -148,6 +148,12 @@ WORKLOADS = {
     "decode_profile": Workload("decode_profile", Shape(4096, 2048, 48, 6, 2048), 1, 1, False,
                                (SEED_BASE + 7,),
                                "profiling case: H=4096 I=2048 E=48 top-6 I_sh=2048, T=1"),
+    # Hot experts for the tensor-bound regime of the skewed prefill (whose
+    # hottest experts take ~1,280 tokens): 8 experts, 1024 tokens, ~768 tokens
+    # per expert; ~0.2 GB of expert rows, so a full capture stays small.
+    "prefill_hot_profile": Workload("prefill_hot_profile", Shape(4096, 2048, 8, 6, 2048), 1024, 1, False,
+                                    (SEED_BASE + 8,),
+                                    "profiling case: H=4096 I=2048 E=8 top-6 I_sh=2048, T=1024 (~768 tokens per expert)"),
 }
 
 
@@ -332,4 +338,6 @@ def make_tokens(workload: str, T: int | None = None, first: int = 0) -> np.ndarr
         return normal_bf16(T * H, SEED_BASE + 5 + 0x10000, S_X).reshape(T, H)
     if workload == "decode_profile":
         return normal_bf16(T * H, SEED_BASE + 7 + 0x10000, S_X).reshape(T, H)
+    if workload == "prefill_hot_profile":
+        return normal_bf16(T * H, SEED_BASE + 8 + 0x10000, S_X).reshape(T, H)
     raise KeyError(workload)
