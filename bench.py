@@ -115,9 +115,9 @@ def kernel_bytes(name, shape, T, U, gains=0, fmt="q2"):
 TRAFFIC = {
     ("prefill_gateup_q2", "prefill_t1024"): (2188538368, "prefill_gemm.cuh", "d7c7eaefd5d9bbc2898ca2a38b0ed443da38ec51"),
     ("prefill_down_q2", "prefill_t1024"): (1174258176, "prefill_gemm.cuh", "d7c7eaefd5d9bbc2898ca2a38b0ed443da38ec51"),
-    ("decode_fused", "decode_t1"): (83795456, "decode_fused.cuh", "c3a4518df8e819c3a4930bd75a1d2552eb01a012"),
+    ("decode_fused", "decode_t1"): (83687424, "decode_fused.cuh", "706623878407df8cb54985e1f126854688daed79"),
     # mean of two batches of the pool (43-47 distinct experts each; the traffic follows the batch's experts)
-    ("decode_fused", "decode_t8"): (404583680, "decode_fused.cuh", "c3a4518df8e819c3a4930bd75a1d2552eb01a012"),
+    ("decode_fused", "decode_t8"): (404592256, "decode_fused.cuh", "706623878407df8cb54985e1f126854688daed79"),
 }
 
 
