@@ -391,7 +391,8 @@ CROSSOVER_T = (1, 2, 4, 6, 8, 9, 12, 16, 24, 32, 48, 64)
 
 
 def run_crossover(args):
-    """Both paths on the H=4096, E=384 decode layer for each T of CROSSOVER_T:
+    """Every path (decode, prefill, and batch up to its token limit) on the
+    H=4096, E=384 decode layer for each T of CROSSOVER_T:
     tokens ~N(0,1) bf16 from seed SEED_BASE + 0x100 + T, L2 flushed before every
     call, median of 15 calls after 3 warm-up calls (CUDA events)."""
     import torch
@@ -420,7 +421,10 @@ def run_crossover(args):
             y = torch.empty((T, shape.hidden), dtype=torch.float32, device=dev)
             idx, _, _, _ = moe.route(x)
             row = {"unique_experts": int(torch.unique(idx).numel())}
-            for name, path in (("decode_us", ds4.PATH_DECODE), ("prefill_us", ds4.PATH_PREFILL)):
+            paths = [("decode_us", ds4.PATH_DECODE), ("prefill_us", ds4.PATH_PREFILL)]
+            if T <= ds4.BATCH_MAX_T:
+                paths.append(("batch_us", ds4.PATH_BATCH))
+            for name, path in paths:
                 ts = []
                 for it in range(18):
                     flush.zero_()
@@ -433,12 +437,13 @@ def run_crossover(args):
                     if it >= 3:
                         ts.append(1000.0 * a.elapsed_time(b))
                 row[name] = float(np.median(ts))
-            row["faster"] = "decode" if row["decode_us"] <= row["prefill_us"] else "prefill"
+            row["fastest"] = min((row[n], n[:-3]) for n, _ in paths)[1]
             rows[T] = row
     if moe.status() != 0:
         raise RuntimeError("device error during the crossover sweep")
     moe.close()
     print(json.dumps({"crossover": rows, "auto_decode_max_t": ds4.AUTO_DECODE_MAX_T,
+                      "auto_batch_max_t": ds4.AUTO_BATCH_MAX_T,
                       "config": workload_config(wl, "decode_t1", "flushed before every call", args.gains),
                       "clocks": clk.summary()}))
 

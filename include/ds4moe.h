@@ -123,17 +123,25 @@ enum {
 #define DS4MOE_FLAG_VQ13 4u
 
 /*
- * Largest T for which DS4MOE_PATH_AUTO takes the decode path (launches of up to
- * 8 tokens): the measured crossover of the two paths on a GB300 at H=4096,
- * I=2048, E=384, top-6 (decode faster up to T=12, prefill from T=16).
+ * DS4MOE_PATH_AUTO takes the decode path for T <= DS4MOE_AUTO_DECODE_MAX_T,
+ * the batch path for T <= DS4MOE_AUTO_BATCH_MAX_T (where the layer has one)
+ * and the prefill path above: the measured crossovers on a GB300 at H=4096,
+ * I=2048, E=384, top-6.
  */
 #define DS4MOE_AUTO_DECODE_MAX_T 12
+#define DS4MOE_AUTO_BATCH_MAX_T 64
+
+/* Most tokens one call of the batch path takes. */
+#define DS4MOE_BATCH_MAX_T 64
 
 /* Execution paths for ds4moe_forward_path. */
 enum {
-    DS4MOE_PATH_AUTO = 0,    /* decode for T <= DS4MOE_AUTO_DECODE_MAX_T, prefill above */
-    DS4MOE_PATH_DECODE = 1,  /* fused dequant-GEMV (memory-bound regime) */
-    DS4MOE_PATH_PREFILL = 2  /* grouped GEMM on tcgen05 tensor cores */
+    DS4MOE_PATH_AUTO = 0,    /* by T, see DS4MOE_AUTO_DECODE_MAX_T */
+    DS4MOE_PATH_DECODE = 1,  /* fused dequant-GEMV kernel, launches of up to 8 tokens */
+    DS4MOE_PATH_PREFILL = 2, /* grouped GEMM on tcgen05 tensor cores */
+    DS4MOE_PATH_BATCH = 3    /* 2-bit layers, T <= min(max_tokens, DS4MOE_BATCH_MAX_T): routing and
+                                grouping, then two persistent tile-GEMV kernels that read each
+                                chosen expert once for up to 8 of its (token, k) pairs */
 };
 
 typedef struct ds4moe ds4moe_t; /* opaque handle */
@@ -199,8 +207,8 @@ int ds4moe_route(ds4moe_t *h, const void *x_bf16, int32_t T, int32_t *idx_out, f
 
 /*
  * The layer. x_bf16: device [T][H] bf16; y: device fp32 [T][H].
- * 0 <= T <= max_tokens; T == 0 does nothing. Picks the decode path for
- * T <= DS4MOE_AUTO_DECODE_MAX_T and the prefill path otherwise.
+ * 0 <= T <= max_tokens; T == 0 does nothing. Picks the path by T
+ * (DS4MOE_PATH_AUTO, see DS4MOE_AUTO_DECODE_MAX_T).
  */
 int ds4moe_forward(ds4moe_t *h, const void *x_bf16, int32_t T, float *y);
 
@@ -211,7 +219,12 @@ int ds4moe_forward(ds4moe_t *h, const void *x_bf16, int32_t T, float *y);
  */
 int ds4moe_forward_host(ds4moe_t *h, const void *x_host, int32_t T, float *y_host);
 
-/* ds4moe_forward with an explicit path (DS4MOE_PATH_*). Both paths accept any T. */
+/*
+ * ds4moe_forward with an explicit path (DS4MOE_PATH_*). The decode and prefill
+ * paths accept any T; the batch path T <= min(max_tokens, DS4MOE_BATCH_MAX_T)
+ * (DS4MOE_EINVAL above that, or when the layer's shared memory plan does not
+ * fit the device). MXFP4 and VQ layers run their one pipeline for every path.
+ */
 int ds4moe_forward_path(ds4moe_t *h, const void *x_bf16, int32_t T, int32_t path, float *y);
 
 /*
@@ -221,7 +234,7 @@ int ds4moe_forward_path(ds4moe_t *h, const void *x_bf16, int32_t T, int32_t path
  * are clamped by the kernels and reported as DS4MOE_EDEVICE by ds4moe_status.
  * A token's K indices should be distinct: the decode path (T <= 8 per launch)
  * replaces a repeated index by the smallest index the token's row does not
- * hold and reports DS4MOE_EDEVICE; the prefill path applies the expert once per
+ * hold and reports DS4MOE_EDEVICE; the prefill and batch paths apply the expert once per
  * occurrence.
  */
 int ds4moe_forward_routed(ds4moe_t *h, const void *x_bf16, int32_t T, const int32_t *idx,
@@ -241,7 +254,7 @@ int ds4moe_status(ds4moe_t *h);
 /* Statistics of the last forward call (read after ds4moe_status). */
 typedef struct {
     int32_t tokens;        /* T of the last call */
-    int32_t path;          /* DS4MOE_PATH_DECODE or DS4MOE_PATH_PREFILL */
+    int32_t path;          /* DS4MOE_PATH_DECODE, DS4MOE_PATH_PREFILL or DS4MOE_PATH_BATCH */
     int32_t n_unique;      /* distinct routed experts touched */
     int32_t max_load;      /* most (token, k) pairs on one expert */
     int32_t kernel_count;  /* kernels the call launched */

@@ -21,8 +21,10 @@ DS4MOE_OK, DS4MOE_EINVAL, DS4MOE_ENOMEM, DS4MOE_ECUDA, DS4MOE_EUNSUPPORTED, DS4M
     0, -1, -2, -3, -4, -5, -6)
 DS4MOE_ESCRATCH = -7
 DS4MOE_NOALLOC_SCRATCH = 4 << 20
-PATH_AUTO, PATH_DECODE, PATH_PREFILL = 0, 1, 2
+PATH_AUTO, PATH_DECODE, PATH_PREFILL, PATH_BATCH = 0, 1, 2, 3
 AUTO_DECODE_MAX_T = 12
+AUTO_BATCH_MAX_T = 64
+BATCH_MAX_T = 64
 FLAG_MXFP4 = 1
 FLAG_VQ12, FLAG_VQ13 = 2, 4
 

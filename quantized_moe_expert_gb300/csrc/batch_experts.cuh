@@ -1,0 +1,417 @@
+// Batch path for 2-bit layers, up to 64 tokens per call: the expert products
+// run as persistent kernels (one CTA per SM) over items (slot, row tile). For
+// the routed experts a slot is a distinct expert with up to kBatchCols of its
+// (token, k) pairs, i.e. the 8 columns of one mma.sync; for the shared expert
+// a group of up to 8 tokens. Each CTA takes a contiguous range of items, keeps
+// a ring of stages of tile records in flight (bulk copies; an 8-bit item spans
+// several stages, each a range of columns) and holds the activation rows of its
+// current slot; per stage the 16 warps run the tile GEMVs of tile_gemv.cuh
+// (exact products, fp32 accumulation, the decode path's arithmetic) and after
+// an item's last stage the CTA writes its results. Every routed expert's
+// weights are read once for all the rows that chose it (an expert with more
+// than kBatchCols pairs once per group of them): the batching of the
+// verify-batch expert kernel of "YoungAi - DeepSeek V4.1 Flash on one DGX
+// Spark", section 4.4. No CTA waits on another; every wait on a copy is bounded.
+#pragma once
+
+#include "common.cuh"
+#include "frag_layout.cuh"
+#include "tile_gemv.cuh"
+
+namespace ds4 {
+
+constexpr int kBatchCols = 8;  // pairs per virtual slot: the MMA's columns
+constexpr int kBatchMaxT = 64; // tokens per call of the batch path
+constexpr int kBatchThreads = 512;
+constexpr int kBatchWarps = kBatchThreads / 32;
+constexpr uint64_t kBatchWaitNs = 1000000000ull; // 1 s: far beyond any legitimate wait
+constexpr int kBatchStageCap = 48 << 10; // most bytes of one 8-bit stage
+
+// The four products, one kernel instantiation each.
+enum BatchMode : int {
+    kBq2GateUp = 0, // routed gate and up: a 16-row tile of each per item, SwiGLU into hq
+    kBq2Down = 1,   // routed down: four 16-row tiles per item, into ye
+    kBq8GateUp = 2, // shared gate and up (8-bit), SwiGLU into hs
+    kBq8Down = 3    // shared down (8-bit), into ysh
+};
+
+struct BatchArgs {
+    int H, I, K, Ish, T;
+    Q2Frag gate, up, down;
+    Q8Frag sh_gate, sh_up, sh_down;
+    const uint16_t *x;       // [T][H] bf16 token rows
+    const uint16_t *xq;      // [T][H] bf16 x * 4^-p in the permuted layout
+    const uint16_t *xsums;   // [T][H/8] the 16-column sums of x, bf16 hi and lo
+    uint16_t *hq_hi, *hq_lo; // [P][I] SwiGLU rows as a bf16 hi + lo pair, permuted, by grouped position
+    uint16_t *hsums;         // [P][I/8]
+    float *ye;               // [P][H] routed expert outputs by grouped position
+    uint16_t *hs_hi, *hs_lo; // [T][Ish] shared SwiGLU rows as a binary16 hi + lo pair
+    float *ysh;              // [T][H] shared expert output
+    const int4 *vslot;       // {expert, first grouped position, pairs, 0}
+    const int32_t *nvslot;
+    const int32_t *perm;     // grouped position -> pair t * K + k
+    int nstage;              // stages in each CTA's ring
+    int chunk;               // columns per stage of the 8-bit products
+    unsigned *status;
+};
+
+// x bf16 [T][H] -> the permuted, pre-scaled layout and the sub-block sums
+// (hi, lo). One thread per 16-column sub-block.
+__global__ void batch_prep_x_kernel(const uint16_t *__restrict__ x, int T, int H, uint16_t *__restrict__ xq,
+                                    uint16_t *__restrict__ xsums) {
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int nsub = H / 16;
+    if (i >= (int64_t)T * nsub)
+        return;
+    const int t = (int)(i / nsub), j = (int)(i % nsub);
+    const uint4 *src = reinterpret_cast<const uint4 *>(x + (int64_t)t * H + 16 * j);
+    const uint4 p0 = src[0], p1 = src[1];
+    const uint32_t wv[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+    const int kappa = (j & 15) >> 3;
+    uint16_t *xt = xq + (int64_t)t * H;
+    float sum = 0.f;
+#pragma unroll
+    for (int c = 0; c < 16; c++) {
+        const float v = __uint_as_float(c & 1 ? wv[c >> 1] & 0xFFFF0000u : wv[c >> 1] << 16);
+        sum += v;
+        const float sv = v * (1.0f / (float)(1 << (2 * q2_p(c, kappa)))); // exact: power of two
+        xt[q2_act_index(16 * j + c)] = (uint16_t)f32_to_bf16_bits(sv);
+    }
+    const uint32_t hi = f32_to_bf16_bits(sum);
+    const uint32_t lo = f32_to_bf16_bits(sum - __uint_as_float(hi << 16));
+    uint16_t *st = xsums + (int64_t)t * (H / 8);
+    st[q2_sum_index(j >> 4, j & 15, 0)] = (uint16_t)hi;
+    st[q2_sum_index(j >> 4, j & 15, 1)] = (uint16_t)lo;
+}
+
+// Virtual slots from the grouping: distinct expert u with n pairs gives
+// ceil(n / kBatchCols) slots, in the order of the grouped positions. One block
+// of 1024 threads (at most 1024 distinct experts).
+__global__ void batch_plan_kernel(const int32_t *__restrict__ uexp, const int32_t *__restrict__ uoff,
+                                  const int32_t *__restrict__ nuniq, int4 *__restrict__ vslot,
+                                  int32_t *__restrict__ nvslot) {
+    __shared__ int32_t sc[1024];
+    const int u = threadIdx.x, nu = *nuniq;
+    const int n = u < nu ? uoff[u + 1] - uoff[u] : 0;
+    const int c = (n + kBatchCols - 1) / kBatchCols;
+    sc[u] = c;
+    __syncthreads();
+    for (int o = 1; o < 1024; o <<= 1) { // inclusive Hillis-Steele scan
+        const int v = u >= o ? sc[u - o] : 0;
+        __syncthreads();
+        sc[u] += v;
+        __syncthreads();
+    }
+    const int base = sc[u] - c;
+    for (int i = 0; i < c; i++) {
+        const int first = uoff[u] + i * kBatchCols;
+        vslot[base + i] = make_int4(uexp[u], first, min(kBatchCols, uoff[u + 1] - first), 0);
+    }
+    if (u == 1023)
+        *nvslot = sc[1023];
+}
+
+// Shared memory of a batch CTA for product MODE: the ring of stages (2-bit:
+// an item's whole records; 8-bit: `chunk` columns of them), the slot's
+// activation rows (hi, and lo for the down products) and, for 2-bit, their
+// sub-block sums, each row padded by 16 bytes, the per-warp partial sums, the
+// copy barriers.
+struct BatchPlan {
+    int K, chunk, nsub, nblk, mat_bytes, stage_bytes, nstage;
+    int act_pitch, sum_pitch;
+    int oact, olo, osum, opart, obar, total;
+    __host__ __device__ BatchPlan(int mode, int H, int I, int Ish, int chunk8, int ns) {
+        const bool q2 = mode == kBq2GateUp || mode == kBq2Down;
+        const bool down = mode == kBq2Down || mode == kBq8Down;
+        K = mode == kBq2Down ? I : mode == kBq8Down ? Ish : H;
+        chunk = q2 ? K : chunk8;
+        nsub = K / chunk;
+        nblk = q2 ? chunk / 256 : chunk / 32; // blocks of one tile in a stage
+        mat_bytes = nblk * (q2 ? kQ2Rec : kQ8Rec);
+        stage_bytes = (down ? 4 : 2) * mat_bytes;
+        nstage = ns;
+        act_pitch = 2 * K + 16;
+        sum_pitch = q2 ? K / 4 + 16 : 0;
+        oact = ns * stage_bytes;
+        olo = oact + kBatchCols * act_pitch;
+        osum = olo + (down ? kBatchCols * act_pitch : 0);
+        opart = osum + kBatchCols * sum_pitch;
+        obar = opart + kBatchWarps * 2 * 16 * kBatchCols * (int)sizeof(float);
+        total = obar + 8 * (ns + 1);
+    }
+};
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// Bounded wait for phase `parity` of a copy barrier; false if it gave up.
+__device__ __forceinline__ bool batch_wait(uint64_t *bar, unsigned parity) {
+    uint64_t t0 = 0;
+    for (unsigned it = 0;; it++) {
+        uint32_t done;
+        asm volatile("{\n\t.reg .pred p;\n\t"
+                     "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                     "selp.u32 %0, 1, 0, p;\n\t}"
+                     : "=r"(done)
+                     : "r"(smem_addr(bar)), "r"(parity)
+                     : "memory");
+        if (done)
+            return true;
+        if ((it & 63) == 0) {
+            uint64_t now;
+            asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(now));
+            if (it == 0)
+                t0 = now;
+            else if (now - t0 > kBatchWaitNs)
+                return false;
+        }
+    }
+}
+
+__device__ __forceinline__ void batch_expect(uint64_t *bar, unsigned bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void batch_copy(uint8_t *dst, const void *src, unsigned bytes, uint64_t *bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_addr(dst)),
+                 "l"(src), "r"(bytes), "r"(smem_addr(bar))
+                 : "memory");
+}
+
+// One product over the items of this CTA (see BatchMode). Gate/up items: rows
+// 16 tile .. 16 tile + 15 of gate and up; the SwiGLU rows go to the down
+// product's activation layout (routed: by grouped position, permuted, bf16
+// hi + lo and sums; shared: by token, binary16 hi + lo). Down items: rows
+// 64 tile .. 64 tile + 63 (warps 0-7 the first two 16-row tiles, warps 8-15
+// the other two).
+template <int MODE> __global__ void __launch_bounds__(kBatchThreads, 1) batch_product_kernel(const BatchArgs a) {
+    constexpr bool Q2 = MODE == kBq2GateUp || MODE == kBq2Down;
+    constexpr bool DOWN = MODE == kBq2Down || MODE == kBq8Down;
+    extern __shared__ __align__(128) uint8_t sm[];
+    const BatchPlan pl(MODE, a.H, a.I, a.Ish, a.chunk, a.nstage);
+    uint64_t *const bars = reinterpret_cast<uint64_t *>(sm + pl.obar); // [nstage] stages, then the activations
+    uint64_t *const actbar = bars + pl.nstage;
+    float *const part = reinterpret_cast<float *>(sm + pl.opart); // [warp][matrix][row][column]
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, tig = lane & 3;
+    const int K = pl.K, ns = pl.nstage, nsub = pl.nsub;
+    const int rows_out = MODE == kBq2GateUp ? a.I : MODE == kBq8GateUp ? a.Ish : a.H;
+    const int ntiles = DOWN ? rows_out / 64 : rows_out / 16; // items per slot
+    const int nslots = Q2 ? *a.nvslot : (a.T + kBatchCols - 1) / kBatchCols;
+    const int64_t nitems = (int64_t)nslots * ntiles;
+    const int64_t i0 = nitems * blockIdx.x / gridDim.x;
+    const int cnt = (int)(nitems * (blockIdx.x + 1) / gridDim.x - i0);
+    if (cnt <= 0)
+        return;
+    const int nq = cnt * nsub; // stages this CTA streams
+    const int64_t tile_bytes = (int64_t)(K / 256) * kQ2Rec; // a 2-bit tile's records over all K
+
+    // thread 0: bring stage q (item q / nsub, columns (q % nsub) chunk ..) into ring slot q % ns
+    auto issue = [&](int q) {
+        const int64_t it = i0 + q / nsub;
+        const int sub = q % nsub;
+        const int v = (int)(it / ntiles), tile = (int)(it % ntiles);
+        uint64_t *bar = bars + q % ns;
+        uint8_t *dst = sm + (q % ns) * pl.stage_bytes;
+        batch_expect(bar, (unsigned)pl.stage_bytes);
+        if constexpr (MODE == kBq2GateUp) {
+            const int64_t gt = (int64_t)a.vslot[v].x * (a.I / 16) + tile;
+            batch_copy(dst, a.gate.rec + gt * tile_bytes, (unsigned)pl.mat_bytes, bar);
+            batch_copy(dst + pl.mat_bytes, a.up.rec + gt * tile_bytes, (unsigned)pl.mat_bytes, bar);
+        } else if constexpr (MODE == kBq2Down) {
+            const int64_t gt = (int64_t)a.vslot[v].x * (a.H / 16) + 4 * tile;
+            batch_copy(dst, a.down.rec + gt * tile_bytes, (unsigned)pl.stage_bytes, bar);
+        } else {
+            const int64_t nbq = K / 32, b0 = (int64_t)sub * pl.nblk;
+            if constexpr (MODE == kBq8GateUp) {
+                batch_copy(dst, a.sh_gate.rec + (tile * nbq + b0) * kQ8Rec, (unsigned)pl.mat_bytes, bar);
+                batch_copy(dst + pl.mat_bytes, a.sh_up.rec + (tile * nbq + b0) * kQ8Rec, (unsigned)pl.mat_bytes,
+                           bar);
+            } else {
+                for (int m = 0; m < 4; m++)
+                    batch_copy(dst + m * pl.mat_bytes, a.sh_down.rec + ((4 * tile + m) * nbq + b0) * kQ8Rec,
+                               (unsigned)pl.mat_bytes, bar);
+            }
+        }
+    };
+    // after a wait gave up: record it and (bounded) let this CTA's copies land
+    auto fail = [&](int q, bool act_pending, unsigned actph) {
+        if (tid == 0) {
+            atomicOr(a.status, kErrTimeout);
+            for (int k = q; k < nq && k < q + ns; k++)
+                batch_wait(bars + k % ns, (unsigned)(k / ns) & 1u);
+            if (act_pending)
+                batch_wait(actbar, actph);
+        }
+    };
+
+    if (tid == 0) {
+        for (int s = 0; s <= ns; s++)
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(bars + s)) : "memory");
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        for (int q = 0; q < nq && q < ns; q++)
+            issue(q);
+    }
+    __syncthreads();
+
+    int cur_v = -1, p0 = 0, n = 0;
+    unsigned actph = 0;
+    for (int li = 0; li < cnt; li++) {
+        const int64_t it = i0 + li;
+        const int v = (int)(it / ntiles), tile = (int)(it % ntiles);
+        if (v != cur_v) { // a new slot: its activation rows (every thread is past the last item's reads)
+            if constexpr (Q2) {
+                const int4 vs = a.vslot[v];
+                p0 = vs.y;
+                n = vs.z;
+            } else {
+                p0 = kBatchCols * v; // first token of the group
+                n = min(kBatchCols, a.T - p0);
+            }
+            cur_v = v;
+            if (tid == 0) {
+                const unsigned row_bytes = (DOWN ? 4u : 2u) * K + (Q2 ? K / 4 : 0);
+                batch_expect(actbar, (unsigned)n * row_bytes);
+                for (int c = 0; c < n; c++) {
+                    const int64_t pos = p0 + c;
+                    const uint16_t *hi, *lo = nullptr, *sums = nullptr;
+                    if (MODE == kBq2GateUp) {
+                        const int t = __ldg(a.perm + pos) / a.K;
+                        hi = a.xq + (int64_t)t * K;
+                        sums = a.xsums + (int64_t)t * (K / 8);
+                    } else if (MODE == kBq2Down) {
+                        hi = a.hq_hi + pos * K;
+                        lo = a.hq_lo + pos * K;
+                        sums = a.hsums + pos * (K / 8);
+                    } else if (MODE == kBq8GateUp) {
+                        hi = a.x + pos * K;
+                    } else {
+                        hi = a.hs_hi + pos * K;
+                        lo = a.hs_lo + pos * K;
+                    }
+                    batch_copy(sm + pl.oact + c * pl.act_pitch, hi, 2 * K, actbar);
+                    if (DOWN)
+                        batch_copy(sm + pl.olo + c * pl.act_pitch, lo, 2 * K, actbar);
+                    if (Q2)
+                        batch_copy(sm + pl.osum + c * pl.sum_pitch, sums, K / 4, actbar);
+                }
+            }
+            const bool ok = batch_wait(actbar, actph);
+            if (__syncthreads_or(!ok)) {
+                fail(li * nsub, true, actph);
+                return;
+            }
+            actph ^= 1u;
+        }
+        const int col = g < n ? g : 0; // this lane's MMA column (a repeated row is discarded)
+        const uint8_t *xrow = sm + pl.oact + col * pl.act_pitch;
+        const uint8_t *lrow = sm + pl.olo + col * pl.act_pitch;
+        const uint8_t *srow = sm + pl.osum + col * pl.sum_pitch;
+        const int grp = warp >> 3, wl = warp & 7; // down products: tile pair, warp within it
+        float out[2][2][2] = {};
+        for (int sub = 0; sub < nsub; sub++) {
+            const int q = li * nsub + sub;
+            const bool ok = batch_wait(bars + q % ns, (unsigned)(q / ns) & 1u);
+            if (__syncthreads_or(!ok)) {
+                fail(q, false, 0);
+                return;
+            }
+            const uint8_t *stage = sm + (q % ns) * pl.stage_bytes;
+            const int nblk = pl.nblk;
+            if constexpr (MODE == kBq2GateUp) {
+                const uint8_t *rec[2] = {stage, stage + pl.mat_bytes};
+                q2_gemv<2, false>(rec, xrow, xrow, srow, nblk * warp / kBatchWarps, nblk * (warp + 1) / kBatchWarps,
+                                  lane, out);
+            } else if constexpr (MODE == kBq2Down) {
+                const uint8_t *rec[2] = {stage + (2 * grp) * pl.mat_bytes, stage + (2 * grp + 1) * pl.mat_bytes};
+                q2_gemv<2, true>(rec, xrow, lrow, srow, nblk * wl / 8, nblk * (wl + 1) / 8, lane, out);
+            } else if constexpr (MODE == kBq8GateUp) {
+                const uint8_t *rec[2] = {stage, stage + pl.mat_bytes};
+                const uint8_t *xs = xrow + 2 * sub * pl.chunk;
+                q8_gemv<2, false, true>(rec, xs, xs, nblk * warp / kBatchWarps, nblk * (warp + 1) / kBatchWarps, lane,
+                                        out);
+            } else {
+                const uint8_t *rec[2] = {stage + (2 * grp) * pl.mat_bytes, stage + (2 * grp + 1) * pl.mat_bytes};
+                q8_gemv<2, true, false>(rec, xrow + 2 * sub * pl.chunk, lrow + 2 * sub * pl.chunk, nblk * wl / 8,
+                                        nblk * (wl + 1) / 8, lane, out);
+            }
+            __syncthreads(); // every warp is done with ring slot q % ns
+            if (tid == 0 && q + ns < nq)
+                issue(q + ns);
+        }
+#pragma unroll
+        for (int m = 0; m < 2; m++)
+#pragma unroll
+            for (int cc = 0; cc < 2; cc++) {
+                const int c = 2 * tig + cc;
+                part[((warp * 2 + m) * 16 + g) * kBatchCols + c] = out[m][0][cc];
+                part[((warp * 2 + m) * 16 + g + 8) * kBatchCols + c] = out[m][1][cc];
+            }
+        __syncthreads(); // the partial sums are complete
+        if constexpr (DOWN) {
+            // thread (c, m, r): row 64 tile + 16 m + r of column c, summed over its group's warps
+            const int c = tid >> 6, m = (tid >> 4) & 3, r = tid & 15;
+            if (c < n) {
+                float acc = 0.f;
+                for (int w = 8 * (m >> 1); w < 8 * (m >> 1) + 8; w++)
+                    acc += part[((w * 2 + (m & 1)) * 16 + r) * kBatchCols + c];
+                if (MODE == kBq2Down)
+                    a.ye[(int64_t)(p0 + c) * a.H + 64 * tile + 16 * m + r] = acc;
+                else
+                    a.ysh[(int64_t)(p0 + c) * a.H + 64 * tile + 16 * m + r] = acc;
+            }
+        } else if (tid < 16 * kBatchCols) {
+            const int c = tid >> 4, r = tid & 15;
+            float hv = 0.f;
+            if (c < n) {
+                float gs = 0.f, us = 0.f;
+                for (int w = 0; w < kBatchWarps; w++) {
+                    gs += part[((w * 2) * 16 + r) * kBatchCols + c];
+                    us += part[((w * 2 + 1) * 16 + r) * kBatchCols + c];
+                }
+                hv = silu(gs) * us;
+            }
+            if constexpr (MODE == kBq8GateUp) {
+                if (c < n) {
+                    const __half hi = __float2half_rn(hv);
+                    const __half lo = __float2half_rn(hv - __half2float(hi));
+                    const int64_t o = (int64_t)(p0 + c) * a.Ish + 16 * tile + r;
+                    a.hs_hi[o] = __half_as_ushort(hi);
+                    a.hs_lo[o] = __half_as_ushort(lo);
+                }
+            } else {
+                // row r of the tile is column k = 16 tile + r of the down matrix: position r of
+                // its sub-block j = tile % 16 in block tile / 16
+                const int blk = tile >> 4, j = tile & 15;
+                float hs = 0.f;
+                if (c < n) {
+                    const int e2 = 2 * q2_p(r, j >> 3);
+                    const float hp = hv * (1.0f / (float)(1 << e2)); // exact: power of two
+                    const uint32_t h1 = f32_to_bf16_bits(hp);
+                    const float h1f = __uint_as_float(h1 << 16);
+                    const uint32_t h2 = f32_to_bf16_bits(hp - h1f);
+                    const float h2f = __uint_as_float(h2 << 16);
+                    const int64_t o = (int64_t)(p0 + c) * a.I + q2_act_index(tile * 16 + r);
+                    a.hq_hi[o] = (uint16_t)h1;
+                    a.hq_lo[o] = (uint16_t)h2;
+                    hs = (h1f + h2f) * (float)(1 << e2); // the value the down product sees
+                }
+#pragma unroll
+                for (int o = 8; o > 0; o >>= 1) // over the 16 rows: one sub-block of the down columns
+                    hs += __shfl_xor_sync(0xFFFFFFFFu, hs, o);
+                if (c < n && r == 0) {
+                    const uint32_t h1 = f32_to_bf16_bits(hs);
+                    const uint32_t h2 = f32_to_bf16_bits(hs - __uint_as_float(h1 << 16));
+                    uint16_t *so = a.hsums + (int64_t)(p0 + c) * (a.I / 8);
+                    so[q2_sum_index(blk, j, 0)] = (uint16_t)h1;
+                    so[q2_sum_index(blk, j, 1)] = (uint16_t)h2;
+                }
+            }
+        }
+        __syncthreads(); // the partial sums and the activation rows may be reused
+    }
+}
+
+} // namespace ds4

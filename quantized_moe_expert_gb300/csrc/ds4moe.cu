@@ -15,6 +15,7 @@
 #include "../../include/ds4moe.h"
 #include "common.cuh"
 #include "decode_fused.cuh"
+#include "batch_experts.cuh"
 #include "frag_layout.cuh"
 #include "dispatch.cuh"
 #include "mx4_experts.cuh"
@@ -100,6 +101,23 @@ struct DecodeState {
     unsigned epoch = 0;
 };
 
+static_assert(kBatchMaxT == DS4MOE_BATCH_MAX_T, "batch path token limit");
+
+// Buffers and launch shape of the batch path (2-bit layers, up to kBatchMaxT
+// tokens per call).
+struct BatchState {
+    uint16_t *xq = nullptr, *xsums = nullptr;                      // [Tb][H], [Tb][H/8]
+    uint16_t *hq_hi = nullptr, *hq_lo = nullptr, *hsums = nullptr; // [Pb][I], [Pb][I], [Pb][I/8]
+    uint16_t *hs_hi = nullptr, *hs_lo = nullptr;                   // [Tb][Ish] binary16
+    int4 *vslot = nullptr;                                         // [Pb] virtual slots
+    int32_t *nvslot = nullptr;
+    int tmax = 0;                 // tokens per call; 0: the path is unavailable for this layer
+    int nstage[4] = {0, 0, 0, 0}; // ring depth of each product (BatchMode)
+    int smem[4] = {0, 0, 0, 0};   // its dynamic shared memory
+    int chunk[4] = {0, 0, 0, 0};  // columns per stage of the 8-bit products
+    int grid = 0;
+};
+
 struct ds4moe {
     Profiler prof;
     pf::BMaps map_xp, map_h, map_hsh; // B tensor maps over scratch (fixed addresses)
@@ -109,6 +127,7 @@ struct ds4moe {
     LayerDev L;
     Scratch S;
     DecodeState D;
+    BatchState B;
     int device = 0;
     cudaStream_t stream = nullptr;
     unsigned *status = nullptr; // device word of kErr* bits
@@ -401,6 +420,19 @@ void layout_scratch(ds4moe *h, Carver &c) {
     D.ysh = c.take<float>(Td * L.H);
     D.ctl_words = kCtlTileCnt + L.H / 32;
     D.ctl = c.take<unsigned>(D.ctl_words);
+    if (!L.mx4 && !L.vq) {
+        BatchState &B = h->B;
+        const int64_t Tb = T < kBatchMaxT ? T : kBatchMaxT, Pb = Tb * L.K;
+        B.xq = c.take<uint16_t>(Tb * L.H);
+        B.xsums = c.take<uint16_t>(Tb * (L.H / 8));
+        B.hq_hi = c.take<uint16_t>(Pb * L.I);
+        B.hq_lo = c.take<uint16_t>(Pb * L.I);
+        B.hsums = c.take<uint16_t>(Pb * (L.I / 8));
+        B.hs_hi = c.take<uint16_t>(Tb * (L.Ish > 0 ? L.Ish : 2));
+        B.hs_lo = c.take<uint16_t>(Tb * (L.Ish > 0 ? L.Ish : 2));
+        B.vslot = c.take<int4>(Pb);
+        B.nvslot = c.take<int32_t>(1);
+    }
 }
 
 int cuda_rc(cudaError_t e) {
@@ -647,6 +679,71 @@ int run_experts_prefill(ds4moe *h, const void *x, int T, float *y) {
     return launch_rc();
 }
 
+// Experts and combine for the routing already in S.idx / S.w, T <= B.tmax:
+// the grouping, x in the 2-bit tile GEMV's layout, the virtual slots, the four
+// persistent products (routed gate/up and down, 2-bit; shared gate/up and down,
+// 8-bit), the combine.
+int run_experts_batch(ds4moe *h, const void *x, int T, float *y) {
+    const LayerDev &L = h->L;
+    Scratch &S = h->S;
+    BatchState &B = h->B;
+    DecodeState &D = h->D;
+    cudaStream_t st = h->stream;
+    int rc = run_dispatch(h, T);
+    if (rc)
+        return rc;
+    launch(h, "batch_prep_x", [&] {
+        batch_prep_x_kernel<<<blocks_for((int64_t)T * L.H / 16, 256), 256, 0, st>>>(static_cast<const uint16_t *>(x),
+                                                                                    T, L.H, B.xq, B.xsums);
+    });
+    launch(h, "batch_plan", [&] {
+        batch_plan_kernel<<<1, 1024, 0, st>>>(S.uexp, S.uoff, S.nuniq, B.vslot, B.nvslot);
+    });
+    BatchArgs a;
+    a.H = L.H;
+    a.I = L.I;
+    a.K = L.K;
+    a.Ish = L.Ish;
+    a.T = T;
+    a.gate = D.gate;
+    a.up = D.up;
+    a.down = D.down;
+    a.sh_gate = D.sh_gate;
+    a.sh_up = D.sh_up;
+    a.sh_down = D.sh_down;
+    a.x = static_cast<const uint16_t *>(x);
+    a.xq = B.xq;
+    a.xsums = B.xsums;
+    a.hq_hi = B.hq_hi;
+    a.hq_lo = B.hq_lo;
+    a.hsums = B.hsums;
+    a.ye = S.ye;
+    a.hs_hi = B.hs_hi;
+    a.hs_lo = B.hs_lo;
+    a.ysh = S.ysh;
+    a.vslot = B.vslot;
+    a.nvslot = B.nvslot;
+    a.perm = S.perm;
+    a.status = h->status;
+    auto product = [&](int mode, const char *name, const void *fn) {
+        a.nstage = B.nstage[mode];
+        a.chunk = B.chunk[mode];
+        void *args[] = {&a};
+        launch(h, name, [&] { cudaLaunchKernel(fn, dim3(B.grid), dim3(kBatchThreads), args, B.smem[mode], st); });
+    };
+    product(kBq2GateUp, "batch_gateup_q2", (const void *)batch_product_kernel<kBq2GateUp>);
+    product(kBq2Down, "batch_down_q2", (const void *)batch_product_kernel<kBq2Down>);
+    if (L.Ish > 0) {
+        product(kBq8GateUp, "batch_gateup_q8", (const void *)batch_product_kernel<kBq8GateUp>);
+        product(kBq8Down, "batch_down_q8", (const void *)batch_product_kernel<kBq8Down>);
+    }
+    launch(h, "combine", [&] {
+        combine_kernel<<<blocks_for((int64_t)T * L.H / 4, 256), 256, 0, st>>>(
+            S.ye, L.Ish > 0 ? S.ysh : nullptr, S.w, S.inv, S.idx, L.gain, T, L.H, L.K, y);
+    });
+    return launch_rc();
+}
+
 // MXFP4 routed experts for the routing already in S.idx / S.w, every T: Q8
 // token rows, the gate/up product with SwiGLU, Q8 SwiGLU rows, the down
 // product, the shared expert, the combine.
@@ -829,11 +926,23 @@ int check_call(ds4moe *h, const void *x, int T) {
     return DS4MOE_OK;
 }
 
+// The path a call takes: DS4MOE_PATH_AUTO resolved by T; -1 if an explicit
+// batch path cannot take the call (more than B.tmax tokens, or no batch path
+// for this layer). MXFP4 and VQ layers run one pipeline whatever the path.
+int resolve_path(const ds4moe *h, int T, int path) {
+    if (path == DS4MOE_PATH_AUTO) {
+        if (T <= DS4MOE_AUTO_DECODE_MAX_T)
+            return DS4MOE_PATH_DECODE;
+        return T <= DS4MOE_AUTO_BATCH_MAX_T && T <= h->B.tmax ? DS4MOE_PATH_BATCH : DS4MOE_PATH_PREFILL;
+    }
+    if (path == DS4MOE_PATH_BATCH && !h->L.mx4 && !h->L.vq && T > h->B.tmax)
+        return -1;
+    return path;
+}
+
 int forward_impl(ds4moe *h, const void *x, int T, int path, float *y) {
     h->stats = ds4moe_stats{};
     h->stats.tokens = T;
-    if (path == DS4MOE_PATH_AUTO)
-        path = T <= DS4MOE_AUTO_DECODE_MAX_T ? DS4MOE_PATH_DECODE : DS4MOE_PATH_PREFILL;
     h->stats.path = path;
     if (h->L.mx4 || h->L.vq) { // one path for every T
         int rc = run_router(h, x, T, nullptr);
@@ -844,7 +953,7 @@ int forward_impl(ds4moe *h, const void *x, int T, int path, float *y) {
     int rc = run_router(h, x, T, nullptr);
     if (rc)
         return rc;
-    return run_experts_prefill(h, x, T, y);
+    return path == DS4MOE_PATH_BATCH ? run_experts_batch(h, x, T, y) : run_experts_prefill(h, x, T, y);
 }
 
 } // namespace
@@ -1066,6 +1175,41 @@ int ds4moe_create(const ds4moe_layer_desc *desc, const ds4moe_weights *w, ds4moe
     cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
     D.grid = per_sm * nsm;
     g_pf_grid = nsm;
+    if (!L.mx4 && !L.vq) {
+        // the batch path where its shared memory fits: three stages per ring, else two (the
+        // attribute belongs to the kernel, not to the layer: it allows the device maximum).
+        // An 8-bit stage holds the widest column range that divides K within kBatchStageCap.
+        BatchState &B = h->B;
+        const int optin = (int)prop.sharedMemPerBlockOptin;
+        bool fits = true;
+        for (int mode = 0; mode < 4; mode++) {
+            if (mode >= kBq8GateUp && L.Ish == 0)
+                continue;
+            int chunk = 0;
+            if (mode >= kBq8GateUp) {
+                const int K = mode == kBq8Down ? L.Ish : L.H, tiles = mode == kBq8Down ? 4 : 2;
+                for (int c = K; c >= 32 && !chunk; c -= 32)
+                    if (K % c == 0 && tiles * (c / 32) * kQ8Rec <= kBatchStageCap)
+                        chunk = c;
+            }
+            int ns = 3;
+            while (ns >= 2 && BatchPlan(mode, L.H, L.I, L.Ish, chunk, ns).total > optin)
+                ns--;
+            fits = fits && ns >= 2;
+            B.nstage[mode] = ns;
+            B.chunk[mode] = chunk;
+            B.smem[mode] = BatchPlan(mode, L.H, L.I, L.Ish, chunk, ns).total;
+        }
+        if (fits) {
+            B.tmax = L.Tmax < kBatchMaxT ? L.Tmax : kBatchMaxT;
+            B.grid = nsm;
+            for (const void *fn : {(const void *)batch_product_kernel<kBq2GateUp>,
+                                   (const void *)batch_product_kernel<kBq2Down>,
+                                   (const void *)batch_product_kernel<kBq8GateUp>,
+                                   (const void *)batch_product_kernel<kBq8Down>})
+                cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+        }
+    }
     rc = setup_gemm<pf::kFmtQ2, 2, pf::kEpiSwiGLU>();
     if (!rc)
         rc = setup_gemm<pf::kFmtQ2, 1, pf::kEpiF32>();
@@ -1142,11 +1286,14 @@ int ds4moe_forward_path(ds4moe_t *h, const void *x, int32_t T, int32_t path, flo
     int rc = check_call(h, x, T);
     if (rc)
         return rc;
-    if (path < DS4MOE_PATH_AUTO || path > DS4MOE_PATH_PREFILL)
+    if (path < DS4MOE_PATH_AUTO || path > DS4MOE_PATH_BATCH)
         return DS4MOE_EINVAL;
     if (T == 0)
         return DS4MOE_OK;
     if (!is_device_ptr(y) || !aligned(y, 16))
+        return DS4MOE_EINVAL;
+    path = resolve_path(h, T, path);
+    if (path < 0)
         return DS4MOE_EINVAL;
     return forward_impl(h, x, T, path, y);
 }
@@ -1160,27 +1307,33 @@ int ds4moe_forward_routed(ds4moe_t *h, const void *x, int32_t T, const int32_t *
     int rc = check_call(h, x, T);
     if (rc)
         return rc;
-    if (path < DS4MOE_PATH_AUTO || path > DS4MOE_PATH_PREFILL)
+    if (path < DS4MOE_PATH_AUTO || path > DS4MOE_PATH_BATCH)
         return DS4MOE_EINVAL;
     if (T == 0)
         return DS4MOE_OK;
     if (!is_device_ptr(idx) || !is_device_ptr(w) || !is_device_ptr(y) || !aligned(y, 16))
+        return DS4MOE_EINVAL;
+    path = resolve_path(h, T, path);
+    if (path < 0)
         return DS4MOE_EINVAL;
     const LayerDev &L = h->L;
     Scratch &S = h->S;
     cudaStream_t st = h->stream;
     h->stats = ds4moe_stats{};
     h->stats.tokens = T;
-    h->stats.path = path == DS4MOE_PATH_AUTO ? (T <= DS4MOE_AUTO_DECODE_MAX_T ? DS4MOE_PATH_DECODE : DS4MOE_PATH_PREFILL)
-                                             : path;
-    if (h->stats.path == DS4MOE_PATH_DECODE && !L.mx4 && !L.vq)
+    h->stats.path = path;
+    if (path == DS4MOE_PATH_DECODE && !L.mx4 && !L.vq)
         return run_decode(h, x, T, y, idx, w);
     cudaMemcpyAsync(S.idx, idx, sizeof(int32_t) * T * L.K, cudaMemcpyDeviceToDevice, st);
     cudaMemcpyAsync(S.w, w, sizeof(float) * T * L.K, cudaMemcpyDeviceToDevice, st);
     rc = launch_rc();
     if (rc)
         return rc;
-    return L.vq ? run_experts_vq(h, x, T, y) : L.mx4 ? run_experts_mx4(h, x, T, y) : run_experts_prefill(h, x, T, y);
+    if (L.vq)
+        return run_experts_vq(h, x, T, y);
+    if (L.mx4)
+        return run_experts_mx4(h, x, T, y);
+    return path == DS4MOE_PATH_BATCH ? run_experts_batch(h, x, T, y) : run_experts_prefill(h, x, T, y);
 }
 
 int ds4moe_forward_host(ds4moe_t *h, const void *x_host, int32_t T, float *y_host) {
@@ -1195,7 +1348,7 @@ int ds4moe_forward_host(ds4moe_t *h, const void *x_host, int32_t T, float *y_hos
     int rc = cuda_rc(cudaMemcpyAsync(h->S.xstage, x_host, sizeof(uint16_t) * T * L.H, cudaMemcpyHostToDevice, st));
     if (rc)
         return rc;
-    rc = forward_impl(h, h->S.xstage, T, DS4MOE_PATH_AUTO, h->S.ystage);
+    rc = forward_impl(h, h->S.xstage, T, resolve_path(h, T, DS4MOE_PATH_AUTO), h->S.ystage);
     if (rc)
         return rc;
     rc = cuda_rc(cudaMemcpyAsync(y_host, h->S.ystage, sizeof(float) * T * L.H, cudaMemcpyDeviceToHost, st));
@@ -1272,7 +1425,7 @@ int ds4moe_inspect(ds4moe_t *h, int32_t T, int32_t *idx, float *w, float *gap, i
     get(gap, S.gap, sizeof(float) * T);
     if (rc || !(counts || inv || uexp || ustart || n_unique))
         return rc;
-    const bool dec = h->stats.path == DS4MOE_PATH_DECODE && !L.mx4;
+    const bool dec = h->stats.path == DS4MOE_PATH_DECODE && !L.mx4 && !L.vq;
     if (dec && T > kDecodeT)
         return DS4MOE_EINVAL; // the fused kernel keeps the grouping of its last launch only
     int32_t nu = 0;

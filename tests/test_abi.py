@@ -37,6 +37,12 @@ def test_binding_constants_match_the_header():
     assert macro("DS4MOE_MAGIC") == ds4.DS4MOE_MAGIC
     assert macro("DS4MOE_VERSION") == ds4.DS4MOE_VERSION
     assert macro("DS4MOE_AUTO_DECODE_MAX_T") == ds4.AUTO_DECODE_MAX_T
+    assert macro("DS4MOE_AUTO_BATCH_MAX_T") == ds4.AUTO_BATCH_MAX_T
+    assert macro("DS4MOE_BATCH_MAX_T") == ds4.BATCH_MAX_T
+    paths = dict(re.findall(r"(DS4MOE_PATH_\w+)\s*=\s*(\d+)", text))
+    assert {k: int(v) for k, v in paths.items()} == {
+        "DS4MOE_PATH_AUTO": ds4.PATH_AUTO, "DS4MOE_PATH_DECODE": ds4.PATH_DECODE,
+        "DS4MOE_PATH_PREFILL": ds4.PATH_PREFILL, "DS4MOE_PATH_BATCH": ds4.PATH_BATCH}
     assert macro("DS4MOE_FLAG_MXFP4") == ds4.FLAG_MXFP4
     # the weights struct the binding passes has the header's fields in order
     body = re.search(r"typedef struct \{([^}]*)\} ds4moe_weights;", text).group(1)

@@ -53,7 +53,8 @@ def tiny():
 
 @pytest.mark.parametrize("tables", [1, 2, 3])
 @pytest.mark.parametrize("path,T", [(ds4.PATH_DECODE, 1), (ds4.PATH_DECODE, 3), (ds4.PATH_DECODE, 8),
-                                    (ds4.PATH_PREFILL, 9), (ds4.PATH_PREFILL, 80)])
+                                    (ds4.PATH_PREFILL, 9), (ds4.PATH_PREFILL, 80), (ds4.PATH_BATCH, 9),
+                                    (ds4.PATH_BATCH, 64)])
 def test_gains_match_oracle(tiny, tables, path, T):
     shape, layer, handles = tiny
     moe = handles[tables]
@@ -66,7 +67,7 @@ def test_gains_match_oracle(tiny, tables, path, T):
     y_plain = oracle.forward_routed(shape, layer, x, r["idx"], w32.astype(np.float64))
     # the gains move the output by far more than the tolerance
     assert rel_l2(y_plain, y_ref) > 20 * TOL_PREFILL
-    assert_close(y, y_ref, (TOL_DECODE if path == ds4.PATH_DECODE else TOL_PREFILL))
+    assert_close(y, y_ref, (TOL_PREFILL if path == ds4.PATH_PREFILL else TOL_DECODE))
     assert moe.status() == 0
 
 
@@ -80,7 +81,7 @@ def test_unit_gains_are_bit_identical(tiny):
     plain = ds4.MoELayer(shape, to_dev(layer), max_tokens=40)
     unit = ds4.MoELayer(shape, to_dev(L), max_tokens=40)
     try:
-        for T, path in ((1, ds4.PATH_DECODE), (8, ds4.PATH_DECODE), (40, ds4.PATH_PREFILL)):
+        for T, path in ((1, ds4.PATH_DECODE), (8, ds4.PATH_DECODE), (40, ds4.PATH_PREFILL), (20, ds4.PATH_BATCH)):
             xd = x_to_dev(tokens(shape, T, 800 + T))
             a = plain.forward(xd, path=path)
             b = unit.forward(xd, path=path)
@@ -100,7 +101,7 @@ def test_gains_follow_the_expert_not_the_slot(tiny):
     r = oracle.route(shape, layer["router_w"], None, x)
     w32 = r["weights"].astype(np.float32)
     perm = np.array([5, 3, 0, 4, 1, 2])
-    for path, tol in ((ds4.PATH_DECODE, TOL_DECODE), (ds4.PATH_PREFILL, TOL_PREFILL)):
+    for path, tol in ((ds4.PATH_DECODE, TOL_DECODE), (ds4.PATH_PREFILL, TOL_PREFILL), (ds4.PATH_BATCH, TOL_DECODE)):
         a = routed(moe, x, r["idx"], w32, path)
         b = routed(moe, x, np.ascontiguousarray(r["idx"][:, perm]), np.ascontiguousarray(w32[:, perm]), path)
         assert_close(b, a, tol)

@@ -1,7 +1,8 @@
 """GPU parity on the routing contract's edge cases, for all three selection
 implementations: the fused decode kernel (T <= 8 per launch), the fp32
 router with its selection kernel (T < 16) and the tensor-core router with
-exact refinement (T >= 16).
+exact refinement (T >= 16), and the outputs of the decode, batch and prefill
+paths on those routings.
 
 * Exact ties at the K-th boundary: two identical router rows with the same
   bias always tie for the K-th place; the lower expert index must win on
@@ -71,7 +72,9 @@ def edge(request):
 # (how the routing is produced, T): the decode kernel's own selection, the fp32
 # router, the tensor-core router (route and the prefill forward)
 CASES = [("decode", 1), ("decode", 5), ("decode", 8), ("route", 5), ("route", 12), ("route", 40),
-         ("prefill", 40)]
+         ("prefill", 40), ("batch", 13), ("batch", 64)]
+PATHS = {"decode": ds4.PATH_DECODE, "prefill": ds4.PATH_PREFILL, "batch": ds4.PATH_BATCH}
+TOLS = {"decode": TOL_DECODE, "batch": TOL_DECODE, "prefill": TOL_PREFILL}
 
 
 def gpu_routing(moe, x, how):
@@ -81,7 +84,7 @@ def gpu_routing(moe, x, how):
     if how == "route":
         idx, w, gap, _ = moe.route(xd)
         return idx.cpu().numpy(), w.cpu().numpy(), gap.cpu().numpy(), None
-    y = moe.forward(xd, path=ds4.PATH_DECODE if how == "decode" else ds4.PATH_PREFILL).cpu().numpy()
+    y = moe.forward(xd, path=PATHS[how]).cpu().numpy()
     r = moe.inspect(T, grouping=False)
     return r["idx"], r["w"], r["gap"], y
 
@@ -116,13 +119,13 @@ def test_selection_edges(edge, how, T):
         assert not (idx == NAN_EXPERT).any()
         check_routing(idx, w, gap, r, shape.top_k)
     if y is not None:
-        tol = TOL_DECODE if how == "decode" else TOL_PREFILL
+        tol = TOLS[how]
         y_ref = oracle.forward_routed(shape, layer, x, idx, w.astype(np.float64))
         assert_close(y, y_ref, tol)
     assert moe.status() == 0
 
 
-@pytest.mark.parametrize("path,T", [(ds4.PATH_DECODE, 5), (ds4.PATH_PREFILL, 40)])
+@pytest.mark.parametrize("path,T", [(ds4.PATH_DECODE, 5), (ds4.PATH_PREFILL, 40), (ds4.PATH_BATCH, 40)])
 def test_near_tie_output_on_the_oracles_routing(edge, path, T):
     kind, layer, moe = edge
     if kind != "near":
@@ -132,11 +135,12 @@ def test_near_tie_output_on_the_oracles_routing(edge, path, T):
     y_ref, r = oracle.forward(shape, layer, x)
     y = moe.forward_routed(x_to_dev(x), torch.from_numpy(r["idx"]).cuda(),
                            torch.from_numpy(r["weights"].astype(np.float32)).cuda(), path=path).cpu().numpy()
-    assert_close(y, y_ref, TOL_DECODE if path == ds4.PATH_DECODE else TOL_PREFILL)
+    assert_close(y, y_ref, TOL_PREFILL if path == ds4.PATH_PREFILL else TOL_DECODE)
     assert moe.status() == 0
 
 
-@pytest.mark.parametrize("how,T", [("decode", 1), ("decode", 4), ("route", 6), ("route", 20), ("prefill", 20)])
+@pytest.mark.parametrize("how,T", [("decode", 1), ("decode", 4), ("route", 6), ("route", 20), ("prefill", 20),
+                                   ("batch", 20)])
 def test_all_nan_token_takes_the_lowest_indices(how, T):
     shape = synth.TINY_SHAPE
     layer = synth.make_layer(shape, synth.SEED_BASE)
@@ -155,7 +159,7 @@ def test_all_nan_token_takes_the_lowest_indices(how, T):
             check_routing(idx[good], w[good], gap[good], {k: v[good] for k, v in r.items()}, shape.top_k)
         if y is not None and good.any():
             y_ref = oracle.forward_routed(shape, layer, x[good], idx[good], w[good].astype(np.float64))
-            assert_close(y[good], y_ref, TOL_DECODE if how == "decode" else TOL_PREFILL)
+            assert_close(y[good], y_ref, TOLS[how])
         assert moe.status() == 0
     finally:
         moe.close()
@@ -185,7 +189,8 @@ def check_grouping(moe, T, E):
 
 
 @pytest.mark.parametrize("path,T", [(ds4.PATH_DECODE, 1), (ds4.PATH_DECODE, 3), (ds4.PATH_DECODE, 8),
-                                    (ds4.PATH_PREFILL, 16), (ds4.PATH_PREFILL, 64)])
+                                    (ds4.PATH_PREFILL, 16), (ds4.PATH_PREFILL, 64), (ds4.PATH_BATCH, 9),
+                                    (ds4.PATH_BATCH, 64)])
 def test_grouping_is_a_stable_counting_sort(path, T):
     shape = synth.TINY_SHAPE
     layer = synth.make_layer(shape, synth.SEED_BASE)

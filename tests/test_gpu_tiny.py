@@ -61,7 +61,7 @@ def test_prefill_path(tiny, T):
 
 def test_auto_path_and_stats(tiny):
     shape, layer, moe = tiny
-    x = tokens(shape, 16, 401)
+    x = tokens(shape, ds4.AUTO_BATCH_MAX_T + 1, 401)
     moe.forward(x_to_dev(x[:4]))
     s = moe.stats()
     assert s.path == ds4.PATH_DECODE and s.tokens == 4 and s.kernel_count > 0
@@ -71,6 +71,10 @@ def test_auto_path_and_stats(tiny):
     moe.forward(x_to_dev(x[:ds4.AUTO_DECODE_MAX_T]))
     assert moe.stats().path == ds4.PATH_DECODE
     moe.forward(x_to_dev(x[:ds4.AUTO_DECODE_MAX_T + 1]))
+    assert moe.stats().path == ds4.PATH_BATCH
+    moe.forward(x_to_dev(x[:ds4.AUTO_BATCH_MAX_T]))
+    assert moe.stats().path == ds4.PATH_BATCH
+    moe.forward(x_to_dev(x[:ds4.AUTO_BATCH_MAX_T + 1]))
     assert moe.stats().path == ds4.PATH_PREFILL
 
 
