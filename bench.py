@@ -42,8 +42,8 @@ def parse():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="decode_t1",
-                    choices=["decode_t1", "decode_t8", "prefill_t1024", "prefill_t4096_zipf4", "tiny", "prefill_profile",
-                             "decode_profile", "prefill_hot_profile"])
+                    choices=["decode_t1", "decode_t8", "batch_t64", "prefill_t1024", "prefill_t4096_zipf4", "tiny",
+                             "prefill_profile", "decode_profile", "prefill_hot_profile", "batch_profile"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile-steps", type=int, default=20)
@@ -96,6 +96,11 @@ def kernel_bytes(name, shape, T, U, gains=0, fmt="q2"):
         "prefill_gateup_q8": 2 * Ish * H * Q8_BPW + 2 * T * H + 2 * T * Ish,
         "prefill_down_q8": H * Ish * Q8_BPW + 2 * T * Ish + 4 * T * H,
         "combine": 4 * P * H + 4 * T * H + 4 * T * H + gains * U * H * GAIN_BPC,
+        # batch path: the distinct experts' 2-bit rows, the shared expert's 8-bit rows, activations in and out
+        "batch_gateup_q2": U * 2 * I * H * Q2_BPW + 2 * T * H + 4 * P * I,
+        "batch_down_q2": U * H * I * Q2_BPW + 4 * P * I + 4 * P * H,
+        "batch_gateup_q8": 2 * Ish * H * Q8_BPW + 2 * T * H + 4 * T * Ish,
+        "batch_down_q8": H * Ish * Q8_BPW + 4 * T * Ish + 4 * T * H,
         # one launch of the fused decode kernel does the whole layer for up to 8 tokens
         "decode_fused": layer_bytes(shape, T, U, gains),
         # MXFP4 experts: weights of the distinct experts, fp32 activation rows in, results out
@@ -453,6 +458,7 @@ def run_crossover(args):
 # end-to-end steps, seconds of CPU baseline).
 SIDE_WORKLOADS = {
     "decode_t8": (20, 3, 10, 10, 5.0),
+    "batch_t64": (10, 3, 5, 5, 5.0),
     "prefill_t1024": (8, 3, 4, 4, 5.0),
     "prefill_t4096_zipf4": (4, 3, 2, 2, 5.0),
 }
@@ -506,6 +512,7 @@ def measure(ctx, name, handles, layers, steps, warmup, profile_steps, e2e_steps,
         step(i)
     torch.cuda.synchronize()
     launches_per_step = handles[0].stats().kernel_count * len(handles)
+    path_taken = handles[0].stats().path
 
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     barrier()
@@ -610,7 +617,8 @@ def measure(ctx, name, handles, layers, steps, warmup, profile_steps, e2e_steps,
     l2_note = "flushed between steps: %d MiB device write outside the timed events" % (
         flush.numel() // (1 << 20))
     return {"value": value, "ms_per_step": ms_per_step, "steps": steps, "warmup": warmup,
-            "dtype": "f32" if T <= ds4.AUTO_DECODE_MAX_T else "bf16",
+            # decode and batch paths: exact products, fp32 accumulation; prefill: bf16 tensor cores
+            "dtype": "bf16" if path_taken == ds4.PATH_PREFILL else "f32",
             "config": workload_config(wl, name, l2_note, args.gains, args.routed_format),
             "roofline": roofline,
             "layer_roofline": {"bound": "tensor" if lay_flops / (tf_peak * 1e12) > lay_bytes / (hbm_peak * 1e9)

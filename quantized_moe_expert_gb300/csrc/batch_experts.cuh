@@ -22,8 +22,15 @@ namespace ds4 {
 
 constexpr int kBatchCols = 8;  // pairs per virtual slot: the MMA's columns
 constexpr int kBatchMaxT = 64; // tokens per call of the batch path
-constexpr int kBatchThreads = 512;
-constexpr int kBatchWarps = kBatchThreads / 32;
+// Warp roles of a batch CTA: 16 compute warps, a producer warp (its lane 0
+// issues every copy), 2 epilogue warps; they meet only at mbarriers. 19 warps
+// leave 96 registers a thread (at most 5 warps on each of the 4 schedulers).
+constexpr int kBatchComputeWarps = 16;
+constexpr int kBatchProducerWarp = kBatchComputeWarps;
+constexpr int kBatchEpiWarps = 2;
+constexpr int kBatchEpiThreads = 32 * kBatchEpiWarps;
+constexpr int kBatchThreads = 32 * (kBatchComputeWarps + 1 + kBatchEpiWarps);
+constexpr int kPartPitch = 20; // floats per (warp, matrix, column) run of 16 row sums: 20 avoids bank conflicts
 constexpr uint64_t kBatchWaitNs = 1000000000ull; // 1 s: far beyond any legitimate wait
 constexpr int kBatchStageCap = 48 << 10; // most bytes of one 8-bit stage
 
@@ -55,10 +62,13 @@ struct BatchArgs {
     unsigned *status;
 };
 
-// x bf16 [T][H] -> the permuted, pre-scaled layout and the sub-block sums
-// (hi, lo). One thread per 16-column sub-block.
+// x bf16 [T][H] -> the 2-bit GEMV's activation layout (x 4^-p, permuted) and
+// the 16-column sums (bf16 hi + lo), for calls whose router did not write them.
+// One thread per 16-column sub-block.
 __global__ void batch_prep_x_kernel(const uint16_t *__restrict__ x, int T, int H, uint16_t *__restrict__ xq,
                                     uint16_t *__restrict__ xsums) {
+    pdl_launch_next();
+    pdl_wait();
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int nsub = H / 16;
     if (i >= (int64_t)T * nsub)
@@ -84,42 +94,123 @@ __global__ void batch_prep_x_kernel(const uint16_t *__restrict__ x, int T, int H
     st[q2_sum_index(j >> 4, j & 15, 1)] = (uint16_t)lo;
 }
 
-// Virtual slots from the grouping: distinct expert u with n pairs gives
-// ceil(n / kBatchCols) slots, in the order of the grouped positions. One block
-// of 1024 threads (at most 1024 distinct experts).
-__global__ void batch_plan_kernel(const int32_t *__restrict__ uexp, const int32_t *__restrict__ uoff,
-                                  const int32_t *__restrict__ nuniq, int4 *__restrict__ vslot,
-                                  int32_t *__restrict__ nvslot) {
-    __shared__ int32_t sc[1024];
-    const int u = threadIdx.x, nu = *nuniq;
-    const int n = u < nu ? uoff[u + 1] - uoff[u] : 0;
-    const int c = (n + kBatchCols - 1) / kBatchCols;
-    sc[u] = c;
+// The grouping of the batch path in one block of 1024 threads (at most 1024
+// pairs, E <= 1024): per-expert counts, their exclusive scan, the distinct
+// experts, the stable expert-grouped order of the pairs (perm, and inv its
+// inverse: pairs of one expert keep ascending pair index) and the virtual
+// slots (distinct expert u with n pairs gives ceil(n / kBatchCols) slots of
+// consecutive grouped positions). Out-of-range indices are clamped and
+// reported (kErrIndex). The same results as the three grouping kernels of the
+// prefill path, in one launch.
+__global__ void __launch_bounds__(1024) batch_group_kernel(int32_t *__restrict__ idx, int P, int E,
+                                                           int32_t *__restrict__ counts, int32_t *__restrict__ offsets,
+                                                           int32_t *__restrict__ uexp, int32_t *__restrict__ uoff,
+                                                           int32_t *__restrict__ nuniq, int32_t *__restrict__ perm,
+                                                           int32_t *__restrict__ inv, int4 *__restrict__ vslot,
+                                                           int32_t *__restrict__ nvslot, unsigned *__restrict__ status) {
+    pdl_launch_next();
+    pdl_wait();
+    __shared__ int32_t cnt[1024], sc[1024], sf[1024], cur[1024], ue[1024], uo[1025];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    cnt[tid] = 0;
     __syncthreads();
-    for (int o = 1; o < 1024; o <<= 1) { // inclusive Hillis-Steele scan
-        const int v = u >= o ? sc[u - o] : 0;
+    int e = -1;
+    if (tid < P) {
+        e = idx[tid];
+        if (e < 0 || e >= E) {
+            atomicOr(status, kErrIndex);
+            e = e < 0 ? 0 : E - 1;
+            idx[tid] = e;
+        }
+        atomicAdd(cnt + e, 1);
+    }
+    __syncthreads();
+    const int c = cnt[tid]; // tid as an expert index (0 beyond E)
+    sc[tid] = c;
+    sf[tid] = c > 0;
+    __syncthreads();
+    for (int o = 1; o < 1024; o <<= 1) { // inclusive Hillis-Steele scans
+        const int a = tid >= o ? sc[tid - o] : 0;
+        const int b = tid >= o ? sf[tid - o] : 0;
         __syncthreads();
-        sc[u] += v;
+        sc[tid] += a;
+        sf[tid] += b;
         __syncthreads();
     }
-    const int base = sc[u] - c;
-    for (int i = 0; i < c; i++) {
-        const int first = uoff[u] + i * kBatchCols;
-        vslot[base + i] = make_int4(uexp[u], first, min(kBatchCols, uoff[u + 1] - first), 0);
+    const int nu = sf[1023];
+    if (tid < E) {
+        counts[tid] = c;
+        offsets[tid] = sc[tid] - c;
+        cur[tid] = sc[tid] - c;
+        if (c > 0) {
+            uexp[sf[tid] - 1] = tid;
+            uoff[sf[tid] - 1] = sc[tid] - c;
+            ue[sf[tid] - 1] = tid;
+            uo[sf[tid] - 1] = sc[tid] - c;
+        }
     }
-    if (u == 1023)
+    if (tid == 0) {
+        *nuniq = nu;
+        uoff[nu] = P;
+        uo[nu] = P;
+        offsets[E] = P;
+    }
+    __syncthreads();
+    // stable placement: the warps take their 32 pairs in turn; within a warp the
+    // lanes of one expert are ranked by lane
+    const int nwarps = (P + 31) / 32;
+    for (int w = 0; w < nwarps; w++) {
+        if (warp == w) {
+            const unsigned m = __match_any_sync(0xFFFFFFFFu, e);
+            const int leader = __ffs(m) - 1;
+            int base = 0;
+            if (e >= 0 && lane == leader) {
+                base = cur[e];
+                cur[e] = base + __popc(m);
+            }
+            base = __shfl_sync(0xFFFFFFFFu, base, leader);
+            if (e >= 0) {
+                const int pos = base + __popc(m & ((1u << lane) - 1u));
+                perm[pos] = tid;
+                inv[tid] = pos;
+            }
+        }
+        __syncthreads();
+    }
+    // virtual slots of the distinct experts, in grouped order
+    int ns_u = 0, first = 0, npairs = 0, eu = 0;
+    if (tid < nu) {
+        eu = ue[tid];
+        first = uo[tid];
+        npairs = uo[tid + 1] - first;
+        ns_u = (npairs + kBatchCols - 1) / kBatchCols;
+    }
+    sc[tid] = ns_u; // (every earlier read of sc is behind the placement loop's barriers)
+    __syncthreads();
+    __syncthreads();
+    for (int o = 1; o < 1024; o <<= 1) {
+        const int a = tid >= o ? sc[tid - o] : 0;
+        __syncthreads();
+        sc[tid] += a;
+        __syncthreads();
+    }
+    const int base = sc[tid] - ns_u;
+    for (int i = 0; i < ns_u; i++)
+        vslot[base + i] = make_int4(eu, first + i * kBatchCols, min(kBatchCols, npairs - i * kBatchCols), 0);
+    if (tid == 1023)
         *nvslot = sc[1023];
 }
 
 // Shared memory of a batch CTA for product MODE: the ring of stages (2-bit:
 // an item's whole records; 8-bit: `chunk` columns of them), the slot's
 // activation rows (hi, and lo for the down products) and, for 2-bit, their
-// sub-block sums, each row padded by 16 bytes, the per-warp partial sums, the
-// copy barriers.
+// sub-block sums, each row padded by 32 bytes, the compute warps' partial sums
+// of one item, the barriers (full and empty per stage; activations full and
+// empty; partial sums full and empty) and the abort flag.
 struct BatchPlan {
     int K, chunk, nsub, nblk, mat_bytes, stage_bytes, nstage;
     int act_pitch, sum_pitch;
-    int oact, olo, osum, opart, obar, total;
+    int oact, olo, osum, opart, obar, oflag, total;
     __host__ __device__ BatchPlan(int mode, int H, int I, int Ish, int chunk8, int ns) {
         const bool q2 = mode == kBq2GateUp || mode == kBq2Down;
         const bool down = mode == kBq2Down || mode == kBq8Down;
@@ -130,14 +221,15 @@ struct BatchPlan {
         mat_bytes = nblk * (q2 ? kQ2Rec : kQ8Rec);
         stage_bytes = (down ? 4 : 2) * mat_bytes;
         nstage = ns;
-        act_pitch = 2 * K + 16;
-        sum_pitch = q2 ? K / 4 + 16 : 0;
+        act_pitch = 2 * K + 32; // 32: the 8-byte loads of rows g = 0..3 (one half-warp) hit distinct banks
+        sum_pitch = q2 ? K / 4 + 32 : 0;
         oact = ns * stage_bytes;
         olo = oact + kBatchCols * act_pitch;
         osum = olo + (down ? kBatchCols * act_pitch : 0);
         opart = osum + kBatchCols * sum_pitch;
-        obar = opart + kBatchWarps * 2 * 16 * kBatchCols * (int)sizeof(float);
-        total = obar + 8 * (ns + 1);
+        obar = opart + kBatchComputeWarps * 2 * kBatchCols * kPartPitch * (int)sizeof(float);
+        oflag = obar + 8 * (2 * ns + 4);
+        total = oflag + 16;
     }
 };
 
@@ -145,28 +237,64 @@ __device__ __forceinline__ uint32_t smem_addr(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
-// Bounded wait for phase `parity` of a copy barrier; false if it gave up.
-__device__ __forceinline__ bool batch_wait(uint64_t *bar, unsigned parity) {
+// One try_wait: the thread may sleep up to kBatchSuspendNs for the phase to
+// complete, so a waiting warp issues few instructions.
+constexpr unsigned kBatchSuspendNs = 20000;
+__device__ __forceinline__ bool batch_try(uint64_t *bar, unsigned parity) {
+    uint32_t done;
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(done)
+                 : "r"(smem_addr(bar)), "r"(parity), "r"(kBatchSuspendNs)
+                 : "memory");
+    return done != 0;
+}
+
+// Bounded wait for phase `parity` of a barrier. false if the CTA's abort flag
+// is set or the wait ran out (which sets the flag and the status word's
+// kErrTimeout), so that every role of the CTA stops within one poll.
+__device__ __forceinline__ bool batch_wait(uint64_t *bar, unsigned parity, volatile int *abort, unsigned *status) {
     uint64_t t0 = 0;
     for (unsigned it = 0;; it++) {
-        uint32_t done;
-        asm volatile("{\n\t.reg .pred p;\n\t"
-                     "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-                     "selp.u32 %0, 1, 0, p;\n\t}"
-                     : "=r"(done)
-                     : "r"(smem_addr(bar)), "r"(parity)
-                     : "memory");
-        if (done)
+        if (batch_try(bar, parity))
             return true;
-        if ((it & 63) == 0) {
+        if ((it & 3) == 0) {
+            if (*abort)
+                return false;
+            uint64_t now;
+            asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(now));
+            if (it == 0) {
+                t0 = now;
+            } else if (now - t0 > kBatchWaitNs) {
+                *abort = 1;
+                atomicOr(status, kErrTimeout);
+                return false;
+            }
+        }
+    }
+}
+
+// Bounded wait that ignores the abort flag: the producer's last look at its
+// own copies before the CTA leaves.
+__device__ __forceinline__ void batch_drain(uint64_t *bar, unsigned parity) {
+    uint64_t t0 = 0;
+    for (unsigned it = 0;; it++) {
+        if (batch_try(bar, parity))
+            return;
+        if ((it & 3) == 0) {
             uint64_t now;
             asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(now));
             if (it == 0)
                 t0 = now;
             else if (now - t0 > kBatchWaitNs)
-                return false;
+                return;
         }
     }
+}
+
+__device__ __forceinline__ void batch_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 
 __device__ __forceinline__ void batch_expect(uint64_t *bar, unsigned bytes) {
@@ -185,18 +313,32 @@ __device__ __forceinline__ void batch_copy(uint8_t *dst, const void *src, unsign
 // 16 tile .. 16 tile + 15 of gate and up; the SwiGLU rows go to the down
 // product's activation layout (routed: by grouped position, permuted, bf16
 // hi + lo and sums; shared: by token, binary16 hi + lo). Down items: rows
-// 64 tile .. 64 tile + 63 (warps 0-7 the first two 16-row tiles, warps 8-15
-// the other two).
+// 64 tile .. 64 tile + 63 (compute warps 0-7 the first two 16-row tiles,
+// warps 8-15 the other two).
+//
+// Roles: the producer streams the stages of the CTA's items through the ring
+// (waiting for a slot's release by all compute warps) and loads a slot's
+// activation rows once every compute warp is done with the previous slot's;
+// each compute warp runs its share of every stage as soon as it lands and
+// leaves its partial sums of an item for the epilogue warps, which reduce
+// them and write the results while the next item computes.
 template <int MODE> __global__ void __launch_bounds__(kBatchThreads, 1) batch_product_kernel(const BatchArgs a) {
+    pdl_launch_next();
+    pdl_wait();
     constexpr bool Q2 = MODE == kBq2GateUp || MODE == kBq2Down;
     constexpr bool DOWN = MODE == kBq2Down || MODE == kBq8Down;
     extern __shared__ __align__(128) uint8_t sm[];
     const BatchPlan pl(MODE, a.H, a.I, a.Ish, a.chunk, a.nstage);
-    uint64_t *const bars = reinterpret_cast<uint64_t *>(sm + pl.obar); // [nstage] stages, then the activations
-    uint64_t *const actbar = bars + pl.nstage;
-    float *const part = reinterpret_cast<float *>(sm + pl.opart); // [warp][matrix][row][column]
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, tig = lane & 3;
-    const int K = pl.K, ns = pl.nstage, nsub = pl.nsub;
+    const int ns = pl.nstage, nsub = pl.nsub, K = pl.K;
+    uint64_t *const full = reinterpret_cast<uint64_t *>(sm + pl.obar); // [ns]
+    uint64_t *const empty = full + ns;                                 // [ns]
+    uint64_t *const act_full = empty + ns;
+    uint64_t *const act_empty = act_full + 1;
+    uint64_t *const part_full = act_full + 2;
+    uint64_t *const part_empty = act_full + 3;
+    volatile int *const abort = reinterpret_cast<volatile int *>(sm + pl.oflag);
+    float *const part = reinterpret_cast<float *>(sm + pl.opart); // [warp][matrix][column][kPartPitch]
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int rows_out = MODE == kBq2GateUp ? a.I : MODE == kBq8GateUp ? a.Ish : a.H;
     const int ntiles = DOWN ? rows_out / 64 : rows_out / 16; // items per slot
     const int nslots = Q2 ? *a.nvslot : (a.T + kBatchCols - 1) / kBatchCols;
@@ -207,210 +349,277 @@ template <int MODE> __global__ void __launch_bounds__(kBatchThreads, 1) batch_pr
         return;
     const int nq = cnt * nsub; // stages this CTA streams
     const int64_t tile_bytes = (int64_t)(K / 256) * kQ2Rec; // a 2-bit tile's records over all K
-
-    // thread 0: bring stage q (item q / nsub, columns (q % nsub) chunk ..) into ring slot q % ns
-    auto issue = [&](int q) {
-        const int64_t it = i0 + q / nsub;
-        const int sub = q % nsub;
-        const int v = (int)(it / ntiles), tile = (int)(it % ntiles);
-        uint64_t *bar = bars + q % ns;
-        uint8_t *dst = sm + (q % ns) * pl.stage_bytes;
-        batch_expect(bar, (unsigned)pl.stage_bytes);
-        if constexpr (MODE == kBq2GateUp) {
-            const int64_t gt = (int64_t)a.vslot[v].x * (a.I / 16) + tile;
-            batch_copy(dst, a.gate.rec + gt * tile_bytes, (unsigned)pl.mat_bytes, bar);
-            batch_copy(dst + pl.mat_bytes, a.up.rec + gt * tile_bytes, (unsigned)pl.mat_bytes, bar);
-        } else if constexpr (MODE == kBq2Down) {
-            const int64_t gt = (int64_t)a.vslot[v].x * (a.H / 16) + 4 * tile;
-            batch_copy(dst, a.down.rec + gt * tile_bytes, (unsigned)pl.stage_bytes, bar);
-        } else {
-            const int64_t nbq = K / 32, b0 = (int64_t)sub * pl.nblk;
-            if constexpr (MODE == kBq8GateUp) {
-                batch_copy(dst, a.sh_gate.rec + (tile * nbq + b0) * kQ8Rec, (unsigned)pl.mat_bytes, bar);
-                batch_copy(dst + pl.mat_bytes, a.sh_up.rec + (tile * nbq + b0) * kQ8Rec, (unsigned)pl.mat_bytes,
-                           bar);
-            } else {
-                for (int m = 0; m < 4; m++)
-                    batch_copy(dst + m * pl.mat_bytes, a.sh_down.rec + ((4 * tile + m) * nbq + b0) * kQ8Rec,
-                               (unsigned)pl.mat_bytes, bar);
-            }
+    // items run slot-major: item i0 + li is (slot, tile) = ((i0 + li) / ntiles, (i0 + li) % ntiles);
+    // every role steps through them with one division at the start
+    const int v0 = (int)(i0 / ntiles), t0 = (int)(i0 % ntiles);
+    auto step = [&](int &v, int &tile) {
+        if (++tile == ntiles) {
+            tile = 0;
+            v++;
         }
     };
-    // after a wait gave up: record it and (bounded) let this CTA's copies land
-    auto fail = [&](int q, bool act_pending, unsigned actph) {
-        if (tid == 0) {
-            atomicOr(a.status, kErrTimeout);
-            for (int k = q; k < nq && k < q + ns; k++)
-                batch_wait(bars + k % ns, (unsigned)(k / ns) & 1u);
-            if (act_pending)
-                batch_wait(actbar, actph);
+    // first grouped position (routed) or token (shared) of slot v, and its columns
+    auto slot_cols = [&](int v, int &p0, int &n) {
+        if constexpr (Q2) {
+            const int4 vs = a.vslot[v];
+            p0 = vs.y;
+            n = vs.z;
+        } else {
+            p0 = kBatchCols * v;
+            n = min(kBatchCols, a.T - p0);
         }
     };
 
     if (tid == 0) {
-        for (int s = 0; s <= ns; s++)
-            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(bars + s)) : "memory");
+        for (int s = 0; s < ns; s++) {
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(full + s)) : "memory");
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(empty + s)),
+                         "r"(kBatchComputeWarps)
+                         : "memory");
+        }
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(act_full)) : "memory");
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(act_empty)), "r"(kBatchComputeWarps)
+                     : "memory");
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(part_full)), "r"(kBatchComputeWarps)
+                     : "memory");
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(part_empty)), "r"(kBatchEpiWarps)
+                     : "memory");
+        *abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        for (int q = 0; q < nq && q < ns; q++)
-            issue(q);
     }
     __syncthreads();
 
-    int cur_v = -1, p0 = 0, n = 0;
-    unsigned actph = 0;
-    for (int li = 0; li < cnt; li++) {
-        const int64_t it = i0 + li;
-        const int v = (int)(it / ntiles), tile = (int)(it % ntiles);
-        if (v != cur_v) { // a new slot: its activation rows (every thread is past the last item's reads)
-            if constexpr (Q2) {
-                const int4 vs = a.vslot[v];
-                p0 = vs.y;
-                n = vs.z;
-            } else {
-                p0 = kBatchCols * v; // first token of the group
-                n = min(kBatchCols, a.T - p0);
+    if (warp == kBatchProducerWarp) {
+        if (lane != 0)
+            return;
+        int issued = 0, k = -1, cur_v = -1;
+        int v = v0, tile = t0, sub = 0;
+        for (int q = 0; q < nq; q++) {
+            if (q > 0 && ++sub == nsub) {
+                sub = 0;
+                step(v, tile);
             }
-            cur_v = v;
-            if (tid == 0) {
+            if (q >= ns && !batch_wait(empty + q % ns, (unsigned)(q / ns - 1) & 1u, abort, a.status))
+                break;
+            uint64_t *bar = full + q % ns;
+            uint8_t *dst = sm + (q % ns) * pl.stage_bytes;
+            batch_expect(bar, (unsigned)pl.stage_bytes);
+            if constexpr (MODE == kBq2GateUp) {
+                const int64_t gt = (int64_t)a.vslot[v].x * (a.I / 16) + tile;
+                batch_copy(dst, a.gate.rec + gt * tile_bytes, (unsigned)pl.mat_bytes, bar);
+                batch_copy(dst + pl.mat_bytes, a.up.rec + gt * tile_bytes, (unsigned)pl.mat_bytes, bar);
+            } else if constexpr (MODE == kBq2Down) {
+                const int64_t gt = (int64_t)a.vslot[v].x * (a.H / 16) + 4 * tile;
+                batch_copy(dst, a.down.rec + gt * tile_bytes, (unsigned)pl.stage_bytes, bar);
+            } else {
+                const int64_t nbq = K / 32, b0 = (int64_t)sub * pl.nblk;
+                if constexpr (MODE == kBq8GateUp) {
+                    batch_copy(dst, a.sh_gate.rec + (tile * nbq + b0) * kQ8Rec, (unsigned)pl.mat_bytes, bar);
+                    batch_copy(dst + pl.mat_bytes, a.sh_up.rec + (tile * nbq + b0) * kQ8Rec, (unsigned)pl.mat_bytes,
+                               bar);
+                } else {
+                    for (int m = 0; m < 4; m++)
+                        batch_copy(dst + m * pl.mat_bytes, a.sh_down.rec + ((4 * tile + m) * nbq + b0) * kQ8Rec,
+                                   (unsigned)pl.mat_bytes, bar);
+                }
+            }
+            issued = q + 1;
+            if (sub == 0 && v != cur_v) { // the first stage of a new slot: its activation rows
+                k++;
+                cur_v = v;
+                if (k > 0 && !batch_wait(act_empty, (unsigned)(k - 1) & 1u, abort, a.status)) {
+                    k--; // not issued
+                    break;
+                }
+                int p0, n;
+                slot_cols(v, p0, n);
                 const unsigned row_bytes = (DOWN ? 4u : 2u) * K + (Q2 ? K / 4 : 0);
-                batch_expect(actbar, (unsigned)n * row_bytes);
+                batch_expect(act_full, (unsigned)n * row_bytes);
                 for (int c = 0; c < n; c++) {
                     const int64_t pos = p0 + c;
                     const uint16_t *hi, *lo = nullptr, *sums = nullptr;
-                    if (MODE == kBq2GateUp) {
+                    if constexpr (MODE == kBq2GateUp) {
                         const int t = __ldg(a.perm + pos) / a.K;
                         hi = a.xq + (int64_t)t * K;
                         sums = a.xsums + (int64_t)t * (K / 8);
-                    } else if (MODE == kBq2Down) {
+                    } else if constexpr (MODE == kBq2Down) {
                         hi = a.hq_hi + pos * K;
                         lo = a.hq_lo + pos * K;
                         sums = a.hsums + pos * (K / 8);
-                    } else if (MODE == kBq8GateUp) {
+                    } else if constexpr (MODE == kBq8GateUp) {
                         hi = a.x + pos * K;
                     } else {
                         hi = a.hs_hi + pos * K;
                         lo = a.hs_lo + pos * K;
                     }
-                    batch_copy(sm + pl.oact + c * pl.act_pitch, hi, 2 * K, actbar);
+                    batch_copy(sm + pl.oact + c * pl.act_pitch, hi, 2 * K, act_full);
                     if (DOWN)
-                        batch_copy(sm + pl.olo + c * pl.act_pitch, lo, 2 * K, actbar);
+                        batch_copy(sm + pl.olo + c * pl.act_pitch, lo, 2 * K, act_full);
                     if (Q2)
-                        batch_copy(sm + pl.osum + c * pl.sum_pitch, sums, K / 4, actbar);
+                        batch_copy(sm + pl.osum + c * pl.sum_pitch, sums, K / 4, act_full);
                 }
             }
-            const bool ok = batch_wait(actbar, actph);
-            if (__syncthreads_or(!ok)) {
-                fail(li * nsub, true, actph);
-                return;
+        }
+        // the copies still owned by the ring and the last activation load land before the CTA leaves
+        for (int q = issued - ns > 0 ? issued - ns : 0; q < issued; q++)
+            batch_drain(full + q % ns, (unsigned)(q / ns) & 1u);
+        if (k >= 0)
+            batch_drain(act_full, (unsigned)k & 1u);
+        return;
+    }
+
+    if (warp > kBatchProducerWarp) { // epilogue warps: thread et of kBatchEpiThreads
+        const int et = (warp - kBatchProducerWarp - 1) * 32 + lane;
+        int cur_v = -1, p0 = 0, n = 0;
+        int v = v0, tile = t0;
+        for (int li = 0; li < cnt; li++, step(v, tile)) {
+            if (v != cur_v) {
+                slot_cols(v, p0, n);
+                cur_v = v;
             }
-            actph ^= 1u;
+            if (!batch_wait(part_full, (unsigned)li & 1u, abort, a.status))
+                return;
+            if constexpr (DOWN) {
+                // output o = (c, m, r): row 64 tile + 16 m + r of column c, summed over its group's warps
+#pragma unroll
+                for (int k4 = 0; k4 < 16 * 4 * kBatchCols / kBatchEpiThreads; k4++) {
+                    const int o = et + kBatchEpiThreads * k4;
+                    const int c = o >> 6, m = (o >> 4) & 3, r = o & 15;
+                    if (c < n) {
+                        float acc = 0.f;
+#pragma unroll
+                        for (int w = 8 * (m >> 1); w < 8 * (m >> 1) + 8; w++)
+                            acc += part[((w * 2 + (m & 1)) * kBatchCols + c) * kPartPitch + r];
+                        if (MODE == kBq2Down)
+                            a.ye[(int64_t)(p0 + c) * a.H + 64 * tile + 16 * m + r] = acc;
+                        else
+                            a.ysh[(int64_t)(p0 + c) * a.H + 64 * tile + 16 * m + r] = acc;
+                    }
+                }
+            } else {
+#pragma unroll
+              for (int k2 = 0; k2 < 16 * kBatchCols / kBatchEpiThreads; k2++) {
+                const int c = (et >> 4) + (kBatchEpiThreads / 16) * k2, r = et & 15;
+                float hv = 0.f;
+                if (c < n) {
+                    float gs = 0.f, us = 0.f;
+#pragma unroll
+                    for (int w = 0; w < kBatchComputeWarps; w++) {
+                        gs += part[((w * 2) * kBatchCols + c) * kPartPitch + r];
+                        us += part[((w * 2 + 1) * kBatchCols + c) * kPartPitch + r];
+                    }
+                    hv = silu(gs) * us;
+                }
+                if constexpr (MODE == kBq8GateUp) {
+                    if (c < n) {
+                        const __half hi = __float2half_rn(hv);
+                        const __half lo = __float2half_rn(hv - __half2float(hi));
+                        const int64_t o = (int64_t)(p0 + c) * a.Ish + 16 * tile + r;
+                        a.hs_hi[o] = __half_as_ushort(hi);
+                        a.hs_lo[o] = __half_as_ushort(lo);
+                    }
+                } else {
+                    // row r of the tile is column k = 16 tile + r of the down matrix: position r
+                    // of its sub-block j = tile % 16 in block tile / 16
+                    const int blk = tile >> 4, j = tile & 15;
+                    float hs = 0.f;
+                    if (c < n) {
+                        const int e2 = 2 * q2_p(r, j >> 3);
+                        const float hp = hv * (1.0f / (float)(1 << e2)); // exact: power of two
+                        const uint32_t h1 = f32_to_bf16_bits(hp);
+                        const float h1f = __uint_as_float(h1 << 16);
+                        const uint32_t h2 = f32_to_bf16_bits(hp - h1f);
+                        const float h2f = __uint_as_float(h2 << 16);
+                        const int64_t o = (int64_t)(p0 + c) * a.I + q2_act_index(tile * 16 + r);
+                        a.hq_hi[o] = (uint16_t)h1;
+                        a.hq_lo[o] = (uint16_t)h2;
+                        hs = (h1f + h2f) * (float)(1 << e2); // the value the down product sees
+                    }
+#pragma unroll
+                    for (int o = 8; o > 0; o >>= 1) // over the 16 rows: one sub-block of the down columns
+                        hs += __shfl_xor_sync(0xFFFFFFFFu, hs, o);
+                    if (c < n && r == 0) {
+                        const uint32_t h1 = f32_to_bf16_bits(hs);
+                        const uint32_t h2 = f32_to_bf16_bits(hs - __uint_as_float(h1 << 16));
+                        uint16_t *so = a.hsums + (int64_t)(p0 + c) * (a.I / 8);
+                        so[q2_sum_index(blk, j, 0)] = (uint16_t)h1;
+                        so[q2_sum_index(blk, j, 1)] = (uint16_t)h2;
+                    }
+                }
+              }
+            }
+            __syncwarp();
+            if (lane == 0)
+                batch_arrive(part_empty);
+        }
+        return;
+    }
+
+    // compute warps
+    const int g = lane >> 2, tig = lane & 3;
+    const int grp = warp >> 3, wl = warp & 7; // down products: tile pair, warp within it
+    int cur_v = -1, k = -1, n = 0;
+    int v = v0, tile = t0;
+    for (int li = 0; li < cnt; li++) {
+        if (v != cur_v) {
+            int p0;
+            slot_cols(v, p0, n);
+            cur_v = v;
+            k++;
+            if (!batch_wait(act_full, (unsigned)k & 1u, abort, a.status))
+                return;
         }
         const int col = g < n ? g : 0; // this lane's MMA column (a repeated row is discarded)
         const uint8_t *xrow = sm + pl.oact + col * pl.act_pitch;
         const uint8_t *lrow = sm + pl.olo + col * pl.act_pitch;
         const uint8_t *srow = sm + pl.osum + col * pl.sum_pitch;
-        const int grp = warp >> 3, wl = warp & 7; // down products: tile pair, warp within it
         float out[2][2][2] = {};
         for (int sub = 0; sub < nsub; sub++) {
             const int q = li * nsub + sub;
-            const bool ok = batch_wait(bars + q % ns, (unsigned)(q / ns) & 1u);
-            if (__syncthreads_or(!ok)) {
-                fail(q, false, 0);
+            if (!batch_wait(full + q % ns, (unsigned)(q / ns) & 1u, abort, a.status))
                 return;
-            }
             const uint8_t *stage = sm + (q % ns) * pl.stage_bytes;
             const int nblk = pl.nblk;
             if constexpr (MODE == kBq2GateUp) {
                 const uint8_t *rec[2] = {stage, stage + pl.mat_bytes};
-                q2_gemv<2, false>(rec, xrow, xrow, srow, nblk * warp / kBatchWarps, nblk * (warp + 1) / kBatchWarps,
-                                  lane, out);
+                q2_gemv<2, false>(rec, xrow, xrow, srow, nblk * warp / kBatchComputeWarps,
+                                  nblk * (warp + 1) / kBatchComputeWarps, lane, out);
             } else if constexpr (MODE == kBq2Down) {
                 const uint8_t *rec[2] = {stage + (2 * grp) * pl.mat_bytes, stage + (2 * grp + 1) * pl.mat_bytes};
                 q2_gemv<2, true>(rec, xrow, lrow, srow, nblk * wl / 8, nblk * (wl + 1) / 8, lane, out);
             } else if constexpr (MODE == kBq8GateUp) {
                 const uint8_t *rec[2] = {stage, stage + pl.mat_bytes};
                 const uint8_t *xs = xrow + 2 * sub * pl.chunk;
-                q8_gemv<2, false, true>(rec, xs, xs, nblk * warp / kBatchWarps, nblk * (warp + 1) / kBatchWarps, lane,
-                                        out);
+                q8_gemv<2, false, true>(rec, xs, xs, nblk * warp / kBatchComputeWarps,
+                                        nblk * (warp + 1) / kBatchComputeWarps, lane, out);
             } else {
                 const uint8_t *rec[2] = {stage + (2 * grp) * pl.mat_bytes, stage + (2 * grp + 1) * pl.mat_bytes};
                 q8_gemv<2, true, false>(rec, xrow + 2 * sub * pl.chunk, lrow + 2 * sub * pl.chunk, nblk * wl / 8,
                                         nblk * (wl + 1) / 8, lane, out);
             }
-            __syncthreads(); // every warp is done with ring slot q % ns
-            if (tid == 0 && q + ns < nq)
-                issue(q + ns);
+            __syncwarp();
+            if (lane == 0)
+                batch_arrive(empty + q % ns);
         }
+        step(v, tile);
+        if (li + 1 < cnt && v != cur_v) { // done with this slot's activation rows
+            __syncwarp();
+            if (lane == 0)
+                batch_arrive(act_empty);
+        }
+        if (li > 0 && !batch_wait(part_empty, (unsigned)(li - 1) & 1u, abort, a.status))
+            return;
 #pragma unroll
         for (int m = 0; m < 2; m++)
 #pragma unroll
             for (int cc = 0; cc < 2; cc++) {
                 const int c = 2 * tig + cc;
-                part[((warp * 2 + m) * 16 + g) * kBatchCols + c] = out[m][0][cc];
-                part[((warp * 2 + m) * 16 + g + 8) * kBatchCols + c] = out[m][1][cc];
+                part[((warp * 2 + m) * kBatchCols + c) * kPartPitch + g] = out[m][0][cc];
+                part[((warp * 2 + m) * kBatchCols + c) * kPartPitch + g + 8] = out[m][1][cc];
             }
-        __syncthreads(); // the partial sums are complete
-        if constexpr (DOWN) {
-            // thread (c, m, r): row 64 tile + 16 m + r of column c, summed over its group's warps
-            const int c = tid >> 6, m = (tid >> 4) & 3, r = tid & 15;
-            if (c < n) {
-                float acc = 0.f;
-                for (int w = 8 * (m >> 1); w < 8 * (m >> 1) + 8; w++)
-                    acc += part[((w * 2 + (m & 1)) * 16 + r) * kBatchCols + c];
-                if (MODE == kBq2Down)
-                    a.ye[(int64_t)(p0 + c) * a.H + 64 * tile + 16 * m + r] = acc;
-                else
-                    a.ysh[(int64_t)(p0 + c) * a.H + 64 * tile + 16 * m + r] = acc;
-            }
-        } else if (tid < 16 * kBatchCols) {
-            const int c = tid >> 4, r = tid & 15;
-            float hv = 0.f;
-            if (c < n) {
-                float gs = 0.f, us = 0.f;
-                for (int w = 0; w < kBatchWarps; w++) {
-                    gs += part[((w * 2) * 16 + r) * kBatchCols + c];
-                    us += part[((w * 2 + 1) * 16 + r) * kBatchCols + c];
-                }
-                hv = silu(gs) * us;
-            }
-            if constexpr (MODE == kBq8GateUp) {
-                if (c < n) {
-                    const __half hi = __float2half_rn(hv);
-                    const __half lo = __float2half_rn(hv - __half2float(hi));
-                    const int64_t o = (int64_t)(p0 + c) * a.Ish + 16 * tile + r;
-                    a.hs_hi[o] = __half_as_ushort(hi);
-                    a.hs_lo[o] = __half_as_ushort(lo);
-                }
-            } else {
-                // row r of the tile is column k = 16 tile + r of the down matrix: position r of
-                // its sub-block j = tile % 16 in block tile / 16
-                const int blk = tile >> 4, j = tile & 15;
-                float hs = 0.f;
-                if (c < n) {
-                    const int e2 = 2 * q2_p(r, j >> 3);
-                    const float hp = hv * (1.0f / (float)(1 << e2)); // exact: power of two
-                    const uint32_t h1 = f32_to_bf16_bits(hp);
-                    const float h1f = __uint_as_float(h1 << 16);
-                    const uint32_t h2 = f32_to_bf16_bits(hp - h1f);
-                    const float h2f = __uint_as_float(h2 << 16);
-                    const int64_t o = (int64_t)(p0 + c) * a.I + q2_act_index(tile * 16 + r);
-                    a.hq_hi[o] = (uint16_t)h1;
-                    a.hq_lo[o] = (uint16_t)h2;
-                    hs = (h1f + h2f) * (float)(1 << e2); // the value the down product sees
-                }
-#pragma unroll
-                for (int o = 8; o > 0; o >>= 1) // over the 16 rows: one sub-block of the down columns
-                    hs += __shfl_xor_sync(0xFFFFFFFFu, hs, o);
-                if (c < n && r == 0) {
-                    const uint32_t h1 = f32_to_bf16_bits(hs);
-                    const uint32_t h2 = f32_to_bf16_bits(hs - __uint_as_float(h1 << 16));
-                    uint16_t *so = a.hsums + (int64_t)(p0 + c) * (a.I / 8);
-                    so[q2_sum_index(blk, j, 0)] = (uint16_t)h1;
-                    so[q2_sum_index(blk, j, 1)] = (uint16_t)h2;
-                }
-            }
-        }
-        __syncthreads(); // the partial sums and the activation rows may be reused
+        __syncwarp();
+        if (lane == 0)
+            batch_arrive(part_full);
     }
 }
 

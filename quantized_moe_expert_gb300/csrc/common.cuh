@@ -80,6 +80,15 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
+// Programmatic dependent launch. A kernel launched with the programmatic
+// stream-serialization attribute may be scheduled while its predecessor in
+// the stream still runs: pdl_wait() blocks until that grid has completed and
+// its writes are visible (a no-op after an ordinary launch), so it comes before
+// the kernel's first global access; pdl_launch_next() lets the next such
+// kernel be scheduled early. Only the launch and the prologue overlap.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_next() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
 
 __device__ __forceinline__ float sigmoid(float z) { return 1.0f / (1.0f + expf(-z)); }
@@ -132,8 +141,6 @@ __device__ __forceinline__ float down_gain(const uint8_t *blk, int c) {
 // Scratch owned by a handle, sized for max_tokens at create time.
 // Pair index p = t * K + k names the k-th routed choice of token t.
 struct Scratch {
-    float *x32;        // [Tmax][H] activations widened to fp32
-    float *xsum;       // [Tmax][H/16] sums of x over each 16-wide sub-block
     float *logits;     // [Tmax][E]
     int32_t *idx;      // [Tmax][K] routed experts
     float *w;          // [Tmax][K] mixing weights

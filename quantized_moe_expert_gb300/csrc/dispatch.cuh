@@ -101,6 +101,8 @@ __global__ void combine_kernel(const float *__restrict__ ye, const float *__rest
                                const float *__restrict__ w, const int32_t *__restrict__ inv,
                                const int32_t *__restrict__ idx, const float *__restrict__ g, int T, int H, int K,
                                float *__restrict__ y) {
+    pdl_launch_next();
+    pdl_wait();
     const int64_t i4 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int64_t n4 = (int64_t)T * H / 4;
     if (i4 >= n4)

@@ -371,8 +371,6 @@ void layout_scratch(ds4moe *h, Carver &c) {
     Scratch &S = h->S;
     const int64_t T = L.Tmax, P = (int64_t)L.Tmax * L.K;
     const int64_t U = P < L.E ? P : L.E;
-    S.x32 = c.take<float>(T * L.H);
-    S.xsum = c.take<float>(T * (L.H / 16));
     // the router GEMM may write up to (SM count * 128 / m-tiles) rows of K-split partial logits
     S.logits = c.take<float>((T > kLogitRowsSplit ? T : kLogitRowsSplit) * L.E);
     S.idx = c.take<int32_t>(P);
@@ -446,6 +444,24 @@ int launch_rc() { return cuda_rc(cudaGetLastError()); }
 
 unsigned blocks_for(int64_t n, int per) { return (unsigned)((n + per - 1) / per); }
 
+// A launch with programmatic stream serialization: the kernel (which calls
+// pdl_wait() before its first global access) may be scheduled while its
+// predecessor in the stream finishes.
+template <typename... KArgs, typename... Args>
+void launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 // Launch `body` (a kernel launch on h->stream), bracketed by timing events when
 // profiling is on, and count it.
 template <class F> void launch(ds4moe *h, const char *name, F &&body) {
@@ -516,28 +532,18 @@ int x_maps(ds4moe *h, const void *x, int T) {
 
 // ---- the launch sequence ----------------------------------------------------
 
-int run_prep(ds4moe *h, const void *x, int T) {
-    const LayerDev &L = h->L;
-    Scratch &S = h->S;
-    cudaStream_t st = h->stream;
-    launch(h, "prep_x", [&] {
-        prep_x_kernel<<<blocks_for((int64_t)T * (L.H / 16), 256), 256, 0, st>>>(
-            static_cast<const uint16_t *>(x), T, L.H, S.x32, S.xsum);
-    });
-    return launch_rc();
-}
-
-// From this many tokens on, the router logits are a tensor-core GEMM over the
-// three bf16 parts of the router rows (K = 3 H, x repeated per part);
-// below it, a warp-per-expert fp32 dot product.
-constexpr int kRouterGemmMinT = 16;
-
-int run_router(ds4moe *h, const void *x, int T, float *sel_out) {
+// Router logits. Up to kRtMaxT tokens: fp32 dot products on CUDA cores in
+// 256-column slices (router_tile_kernel; with xq/xsums given it also writes x
+// in the 2-bit GEMV's activation layout for the batch path). More tokens: a
+// tensor-core GEMM over the three bf16 parts of the router rows (K = 3 H, x
+// repeated per part) whose near-boundary scores the selection recomputes.
+int run_router(ds4moe *h, const void *x, int T, float *sel_out, uint16_t *xq = nullptr, uint16_t *xsums = nullptr) {
     const LayerDev &L = h->L;
     Scratch &S = h->S;
     cudaStream_t st = h->stream;
     int nsplit = 1;
-    if (T >= kRouterGemmMinT) {
+    const bool tiled = T <= kRtMaxT;
+    if (!tiled) {
         int rc = x_maps(h, x, T);
         if (rc)
             return rc;
@@ -564,20 +570,25 @@ int run_router(ds4moe *h, const void *x, int T, float *sel_out) {
         nsplit = split;
         launch_gemm<pf::kFmtBF16, 1, pf::kEpiF32>(h, "router_logits_tc", h->map_x, a);
     } else {
-        int rc = run_prep(h, x, T);
-        if (rc)
-            return rc;
+        nsplit = L.H / kRtSlice;
         launch(h, "router_logits", [&] {
-            dim3 lg(blocks_for(L.E, 8), blocks_for(T, kRouterTok));
-            router_logits_kernel<<<lg, 256, 0, st>>>(S.x32, T, L.H, L.router_w, L.E, S.logits);
+            const dim3 grid((L.E + kRtExperts - 1) / kRtExperts, nsplit);
+            const uint16_t *xb = static_cast<const uint16_t *>(x);
+            if (T <= 16)
+                launch_pdl(router_tile_kernel<16>, grid, dim3(kRtThreads), router_tile_smem(16), st, xb, T, L.H,
+                           L.router_w, L.E, S.logits, xq, xsums, h->status);
+            else
+                launch_pdl(router_tile_kernel<64>, grid, dim3(kRtThreads), router_tile_smem(64), st, xb, T, L.H,
+                           L.router_w, L.E, S.logits, xq, xsums, h->status);
         });
     }
     launch(h, "router_select", [&] {
         const size_t smem = (size_t)kSelectSmemPerExpert * L.E;
-        router_select_kernel<<<T, kSelectThreads, smem, st>>>(
-            S.logits, L.router_bias, T, L.E, L.K, S.idx, S.w, S.gap, sel_out,
-            T >= kRouterGemmMinT ? static_cast<const uint16_t *>(x) : nullptr, L.router_w, L.H, nsplit,
-            (int64_t)T * L.E);
+        // one thread per expert (at least kSelectThreads, at most 1024)
+        const int threads = L.E < kSelectThreads ? kSelectThreads : L.E > 1024 ? 1024 : (L.E + 31) / 32 * 32;
+        launch_pdl(router_select_kernel, dim3(T), dim3(threads), smem, st, S.logits, L.router_bias, T, L.E, L.K,
+                   S.idx, S.w, S.gap, sel_out, tiled ? nullptr : static_cast<const uint16_t *>(x), L.router_w, L.H,
+                   nsplit, (int64_t)T * L.E);
     });
     return launch_rc();
 }
@@ -680,24 +691,23 @@ int run_experts_prefill(ds4moe *h, const void *x, int T, float *y) {
 }
 
 // Experts and combine for the routing already in S.idx / S.w, T <= B.tmax:
-// the grouping, x in the 2-bit tile GEMV's layout, the virtual slots, the four
-// persistent products (routed gate/up and down, 2-bit; shared gate/up and down,
-// 8-bit), the combine.
-int run_experts_batch(ds4moe *h, const void *x, int T, float *y) {
+// x in the 2-bit tile GEMV's layout (unless the router wrote it), the grouping
+// with the virtual slots, the four persistent products (routed gate/up and
+// down, 2-bit; shared gate/up and down, 8-bit), the combine.
+int run_experts_batch(ds4moe *h, const void *x, int T, float *y, bool x_prepared) {
     const LayerDev &L = h->L;
     Scratch &S = h->S;
     BatchState &B = h->B;
     DecodeState &D = h->D;
     cudaStream_t st = h->stream;
-    int rc = run_dispatch(h, T);
-    if (rc)
-        return rc;
-    launch(h, "batch_prep_x", [&] {
-        batch_prep_x_kernel<<<blocks_for((int64_t)T * L.H / 16, 256), 256, 0, st>>>(static_cast<const uint16_t *>(x),
-                                                                                    T, L.H, B.xq, B.xsums);
-    });
-    launch(h, "batch_plan", [&] {
-        batch_plan_kernel<<<1, 1024, 0, st>>>(S.uexp, S.uoff, S.nuniq, B.vslot, B.nvslot);
+    if (!x_prepared)
+        launch(h, "batch_prep_x", [&] {
+            launch_pdl(batch_prep_x_kernel, dim3(blocks_for((int64_t)T * L.H / 16, 256)), dim3(256), 0, st,
+                       static_cast<const uint16_t *>(x), T, L.H, B.xq, B.xsums);
+        });
+    launch(h, "batch_group", [&] {
+        launch_pdl(batch_group_kernel, dim3(1), dim3(1024), 0, st, S.idx, T * L.K, L.E, S.counts, S.offsets, S.uexp,
+                   S.uoff, S.nuniq, S.perm, S.inv, B.vslot, B.nvslot, h->status);
     });
     BatchArgs a;
     a.H = L.H;
@@ -725,21 +735,20 @@ int run_experts_batch(ds4moe *h, const void *x, int T, float *y) {
     a.nvslot = B.nvslot;
     a.perm = S.perm;
     a.status = h->status;
-    auto product = [&](int mode, const char *name, const void *fn) {
+    auto product = [&](int mode, const char *name, void (*fn)(BatchArgs)) {
         a.nstage = B.nstage[mode];
         a.chunk = B.chunk[mode];
-        void *args[] = {&a};
-        launch(h, name, [&] { cudaLaunchKernel(fn, dim3(B.grid), dim3(kBatchThreads), args, B.smem[mode], st); });
+        launch(h, name, [&] { launch_pdl(fn, dim3(B.grid), dim3(kBatchThreads), B.smem[mode], st, a); });
     };
-    product(kBq2GateUp, "batch_gateup_q2", (const void *)batch_product_kernel<kBq2GateUp>);
-    product(kBq2Down, "batch_down_q2", (const void *)batch_product_kernel<kBq2Down>);
+    product(kBq2GateUp, "batch_gateup_q2", batch_product_kernel<kBq2GateUp>);
+    product(kBq2Down, "batch_down_q2", batch_product_kernel<kBq2Down>);
     if (L.Ish > 0) {
-        product(kBq8GateUp, "batch_gateup_q8", (const void *)batch_product_kernel<kBq8GateUp>);
-        product(kBq8Down, "batch_down_q8", (const void *)batch_product_kernel<kBq8Down>);
+        product(kBq8GateUp, "batch_gateup_q8", batch_product_kernel<kBq8GateUp>);
+        product(kBq8Down, "batch_down_q8", batch_product_kernel<kBq8Down>);
     }
     launch(h, "combine", [&] {
-        combine_kernel<<<blocks_for((int64_t)T * L.H / 4, 256), 256, 0, st>>>(
-            S.ye, L.Ish > 0 ? S.ysh : nullptr, S.w, S.inv, S.idx, L.gain, T, L.H, L.K, y);
+        launch_pdl(combine_kernel, dim3(blocks_for((int64_t)T * L.H / 4, 256)), dim3(256), 0, st, S.ye,
+                   L.Ish > 0 ? S.ysh : nullptr, S.w, S.inv, S.idx, L.gain, T, L.H, L.K, y);
     });
     return launch_rc();
 }
@@ -950,10 +959,14 @@ int forward_impl(ds4moe *h, const void *x, int T, int path, float *y) {
     }
     if (path == DS4MOE_PATH_DECODE)
         return run_decode(h, x, T, y, nullptr, nullptr);
+    if (path == DS4MOE_PATH_BATCH) {
+        int rc = run_router(h, x, T, nullptr, h->B.xq, h->B.xsums);
+        return rc ? rc : run_experts_batch(h, x, T, y, true);
+    }
     int rc = run_router(h, x, T, nullptr);
     if (rc)
         return rc;
-    return path == DS4MOE_PATH_BATCH ? run_experts_batch(h, x, T, y) : run_experts_prefill(h, x, T, y);
+    return run_experts_prefill(h, x, T, y);
 }
 
 } // namespace
@@ -1210,6 +1223,8 @@ int ds4moe_create(const ds4moe_layer_desc *desc, const ds4moe_weights *w, ds4moe
                 cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
         }
     }
+    cudaFuncSetAttribute(router_tile_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, router_tile_smem(16));
+    cudaFuncSetAttribute(router_tile_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, router_tile_smem(64));
     rc = setup_gemm<pf::kFmtQ2, 2, pf::kEpiSwiGLU>();
     if (!rc)
         rc = setup_gemm<pf::kFmtQ2, 1, pf::kEpiF32>();
@@ -1333,7 +1348,7 @@ int ds4moe_forward_routed(ds4moe_t *h, const void *x, int32_t T, const int32_t *
         return run_experts_vq(h, x, T, y);
     if (L.mx4)
         return run_experts_mx4(h, x, T, y);
-    return path == DS4MOE_PATH_BATCH ? run_experts_batch(h, x, T, y) : run_experts_prefill(h, x, T, y);
+    return path == DS4MOE_PATH_BATCH ? run_experts_batch(h, x, T, y, false) : run_experts_prefill(h, x, T, y);
 }
 
 int ds4moe_forward_host(ds4moe_t *h, const void *x_host, int32_t T, float *y_host) {

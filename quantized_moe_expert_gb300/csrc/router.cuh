@@ -9,6 +9,8 @@
 #pragma once
 
 #include "common.cuh"
+#include "frag_layout.cuh"
+#include "tile_gemv.cuh"
 
 namespace ds4 {
 
@@ -79,6 +81,160 @@ __global__ void router_logits_kernel(const float *__restrict__ x32, int T, int H
     }
 }
 
+// Router logits for up to 64 tokens as column-slice partials on CUDA cores:
+// part[s][t][e] = sum over the 256 columns k of slice s of x[t][k] Wr[e][k],
+// plain fp32 FMAs in ascending k (the selection kernel adds the slices in
+// order, so the logits do not depend on the schedule). Block (expert tile of
+// 32, slice s): the slice's 32 router rows and TT token rows (bf16 -> fp32)
+// in shared memory; thread (ex, tk) accumulates experts ex + 8 i, tokens
+// tk + 16 j over 16-byte loads. With xq given, the blocks of expert tile 0
+// also write the slice's tokens in the 2-bit GEMV's activation layout (x 4^-p,
+// permuted) and their 16-column sums (bf16 hi + lo), as the batch path needs.
+constexpr int kRtExperts = 32, kRtSlice = 256, kRtThreads = 128, kRtPitch = kRtSlice + 4;
+constexpr int kRtMaxT = 64;
+
+__host__ __device__ constexpr int router_tile_smem(int TT) { return (kRtExperts + TT) * kRtPitch * 4; }
+
+template <int TT>
+__global__ void __launch_bounds__(kRtThreads) router_tile_kernel(const uint16_t *__restrict__ x, int T, int H,
+                                                                 const float *__restrict__ wr, int E,
+                                                                 float *__restrict__ part, uint16_t *__restrict__ xq,
+                                                                 uint16_t *__restrict__ xsums, unsigned *status) {
+    pdl_launch_next();
+    pdl_wait();
+    extern __shared__ __align__(16) float rt_sm[];
+    __shared__ alignas(8) uint64_t wbar;
+    float *Ws = rt_sm;                          // [32][kRtPitch]
+    float *Xs = rt_sm + kRtExperts * kRtPitch;  // [TT][kRtPitch]
+    const int tid = threadIdx.x;
+    const int e0 = blockIdx.x * kRtExperts, s = blockIdx.y, k0 = s * kRtSlice;
+    const int nrows = min(kRtExperts, E - e0);
+    const uint32_t bar = static_cast<uint32_t>(__cvta_generic_to_shared(&wbar));
+    // the router rows' slice: one 1 KB bulk copy per row (warp 0), rows beyond E zeroed
+    if (tid < 32) {
+        if (tid == 0) {
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar) : "memory");
+            asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+            asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
+                         "r"((unsigned)nrows * kRtSlice * 4u)
+                         : "memory");
+        }
+        __syncwarp();
+        if (tid < nrows)
+            asm volatile(
+                "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                    static_cast<uint32_t>(__cvta_generic_to_shared(Ws + tid * kRtPitch))),
+                "l"(wr + (int64_t)(e0 + tid) * H + k0), "r"((unsigned)kRtSlice * 4u), "r"(bar)
+                : "memory");
+    }
+    for (int f = nrows * (kRtSlice / 4) + tid; f < kRtExperts * (kRtSlice / 4); f += kRtThreads)
+        *reinterpret_cast<float4 *>(Ws + (f / (kRtSlice / 4)) * kRtPitch + 4 * (f % (kRtSlice / 4))) =
+            make_float4(0.f, 0.f, 0.f, 0.f);
+    // the token rows' slice, bf16 -> fp32 (every load of a thread in flight at once)
+    constexpr int NX = TT * (kRtSlice / 8) / kRtThreads;
+    uint4 xv[NX];
+#pragma unroll
+    for (int i = 0; i < NX; i++) {
+        const int f = tid + i * kRtThreads, t = f / (kRtSlice / 8), c8 = f % (kRtSlice / 8);
+        xv[i] = t < T ? __ldg(reinterpret_cast<const uint4 *>(x + (int64_t)t * H + k0) + c8) : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int i = 0; i < NX; i++) {
+        const int f = tid + i * kRtThreads, t = f / (kRtSlice / 8), c8 = f % (kRtSlice / 8);
+        const uint4 v = xv[i];
+        float *d = Xs + t * kRtPitch + 8 * c8;
+        *reinterpret_cast<float4 *>(d) = make_float4(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xFFFF0000u),
+                                                     __uint_as_float(v.y << 16), __uint_as_float(v.y & 0xFFFF0000u));
+        *reinterpret_cast<float4 *>(d + 4) =
+            make_float4(__uint_as_float(v.z << 16), __uint_as_float(v.z & 0xFFFF0000u), __uint_as_float(v.w << 16),
+                        __uint_as_float(v.w & 0xFFFF0000u));
+    }
+    __syncthreads();
+    {
+        // bounded wait for the rows (1 s; on time-out the logits of this block are garbage and the
+        // status word says so)
+        uint64_t t0 = 0;
+        for (unsigned it = 0;; it++) {
+            uint32_t done;
+            asm volatile("{\n\t.reg .pred p;\n\t"
+                         "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], 0;\n\t"
+                         "selp.u32 %0, 1, 0, p;\n\t}"
+                         : "=r"(done)
+                         : "r"(bar)
+                         : "memory");
+            if (done)
+                break;
+            uint64_t now;
+            asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(now));
+            if (it == 0) {
+                t0 = now;
+            } else if (now - t0 > 1000000000ull) {
+                if (tid == 0)
+                    atomicOr(status, kErrTimeout);
+                break;
+            }
+        }
+    }
+    if (xq && blockIdx.x == 0) {
+        // one thread per (token, 16-column sub-block j) of this 256-column block s
+        for (int f = tid; f < T * 16; f += kRtThreads) {
+            const int t = f >> 4, j = f & 15, kappa = j >> 3;
+            const float *v = Xs + t * kRtPitch + 16 * j;
+            uint16_t *xt = xq + (int64_t)t * H;
+            float sum = 0.f;
+#pragma unroll
+            for (int c = 0; c < 16; c++) {
+                sum += v[c];
+                const float sv = v[c] * (1.0f / (float)(1 << (2 * q2_p(c, kappa)))); // exact: power of two
+                xt[q2_act_index(k0 + 16 * j + c)] = (uint16_t)f32_to_bf16_bits(sv);
+            }
+            const uint32_t hi = f32_to_bf16_bits(sum);
+            const uint32_t lo = f32_to_bf16_bits(sum - __uint_as_float(hi << 16));
+            uint16_t *st = xsums + (int64_t)t * (H / 8);
+            st[q2_sum_index(s, j, 0)] = (uint16_t)hi;
+            st[q2_sum_index(s, j, 1)] = (uint16_t)lo;
+        }
+    }
+    constexpr int NJ = TT / 16;
+    const int ex = tid & 7, tk = tid >> 3;
+    float acc[4][NJ];
+#pragma unroll
+    for (int i = 0; i < 4; i++)
+#pragma unroll
+        for (int j = 0; j < NJ; j++)
+            acc[i][j] = 0.f;
+    for (int k = 0; k < kRtSlice; k += 4) {
+        float4 w4[4], x4[NJ];
+#pragma unroll
+        for (int i = 0; i < 4; i++)
+            w4[i] = *reinterpret_cast<const float4 *>(Ws + (ex + 8 * i) * kRtPitch + k);
+#pragma unroll
+        for (int j = 0; j < NJ; j++)
+            x4[j] = *reinterpret_cast<const float4 *>(Xs + (tk + 16 * j) * kRtPitch + k);
+#pragma unroll
+        for (int i = 0; i < 4; i++)
+#pragma unroll
+            for (int j = 0; j < NJ; j++) {
+                acc[i][j] = fmaf(w4[i].x, x4[j].x, acc[i][j]);
+                acc[i][j] = fmaf(w4[i].y, x4[j].y, acc[i][j]);
+                acc[i][j] = fmaf(w4[i].z, x4[j].z, acc[i][j]);
+                acc[i][j] = fmaf(w4[i].w, x4[j].w, acc[i][j]);
+            }
+    }
+#pragma unroll
+    for (int j = 0; j < NJ; j++) {
+        const int t = tk + 16 * j;
+        if (t >= T)
+            continue;
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            const int e = e0 + ex + 8 * i;
+            if (e < E)
+                part[((int64_t)s * T + t) * E + e] = acc[i][j];
+        }
+    }
+}
+
 // One warp per token: selection scores into shared memory, then K+1 rounds of
 // a warp-wide arg-max ordered by (score desc, index asc). Round K+1 only
 // yields the runner-up score for the near-tie gap.
@@ -140,6 +296,8 @@ __global__ void router_select_kernel(const float *__restrict__ logits, const flo
                                      float *__restrict__ gap, float *__restrict__ sel_out,
                                      const uint16_t *__restrict__ x_refine, const float *__restrict__ wr, int H,
                                      int nsplit, int64_t split_stride) {
+    pdl_launch_next();
+    pdl_wait();
     extern __shared__ float smem[];
     __shared__ int ncand;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -151,9 +309,21 @@ __global__ void router_select_kernel(const float *__restrict__ logits, const flo
     int *cand = reinterpret_cast<int *>(score + E);
     unsigned *keys = reinterpret_cast<unsigned *>(cand + E);
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
-        float l = logits[(int64_t)t * E + e];
-        for (int q = 1; q < nsplit; q++) // partial logits of a K-split GEMM, added in order
-            l += logits[q * split_stride + (int64_t)t * E + e];
+        const float *lp = logits + (int64_t)t * E + e;
+        float l = lp[0];
+        // partial logits of a K split, added in order (eight loads in flight at a time)
+        int q = 1;
+        for (; q + 8 <= nsplit; q += 8) {
+            float v[8];
+#pragma unroll
+            for (int i = 0; i < 8; i++)
+                v[i] = lp[(q + i) * split_stride];
+#pragma unroll
+            for (int i = 0; i < 8; i++)
+                l += v[i];
+        }
+        for (; q < nsplit; q++)
+            l += lp[q * split_stride];
         float s = sigmoid(l);
         score[e] = s;
         sel[e] = bias ? s + bias[e] : s;
@@ -181,7 +351,7 @@ __global__ void router_select_kernel(const float *__restrict__ logits, const flo
         }
         __syncthreads();
         const uint2 *xr = reinterpret_cast<const uint2 *>(x_refine + (int64_t)t * H);
-        for (int c = warp; c < ncand; c += kSelectThreads / 32) {
+        for (int c = warp; c < ncand; c += blockDim.x / 32) {
             const int e = cand[c];
             const float4 *row = reinterpret_cast<const float4 *>(wr + (int64_t)e * H);
             float acc = 0.f;

@@ -137,6 +137,14 @@ WORKLOADS = {
                                     tuple(SEED_BASE + 4 + 0x100 * l for l in range(4)),
                                     "long prefill with skew: 4 independent H=4096 E=384 layers, "
                                     "T=4096, Zipf(1.1) router bias (hottest ~20x mean load)"),
+    # The decode <-> prefill crossover: the full layer with 64 tokens, each from its
+    # own N(0,1) draw (~246 distinct experts, one to a few pairs each).
+    "batch_t64": Workload("batch_t64", V4F_SHAPE, 64, 1, False, (SEED_BASE + 1,),
+                          "verify/multi-session batch: the H=4096 E=384 layer, T=64 tokens"),
+    # The same token count on 48 experts (~8 pairs per expert, <1 GB on the device)
+    # for profiler captures of the batch kernels.
+    "batch_profile": Workload("batch_profile", Shape(4096, 2048, 48, 6, 2048), 64, 1, False, (SEED_BASE + 9,),
+                              "profiling case: H=4096 I=2048 E=48 top-6 I_sh=2048, T=64"),
     # A reduced copy of the prefill layer for profiler captures: the same expert
     # matrices (H=4096, I=2048) but 48 experts (~400 MB of 2-bit rows, above the
     # L2 size) and 128 tokens, so one launch is short.
@@ -338,6 +346,10 @@ def make_tokens(workload: str, T: int | None = None, first: int = 0) -> np.ndarr
         return normal_bf16(T * H, SEED_BASE + 5 + 0x10000, S_X).reshape(T, H)
     if workload == "decode_profile":
         return normal_bf16(T * H, SEED_BASE + 7 + 0x10000, S_X).reshape(T, H)
+    if workload == "batch_t64":
+        return normal_bf16(T * H, SEED_BASE + 0x100 + T, S_X).reshape(T, H)
+    if workload == "batch_profile":
+        return normal_bf16(T * H, SEED_BASE + 9 + 0x10000, S_X).reshape(T, H)
     if workload == "prefill_hot_profile":
         return normal_bf16(T * H, SEED_BASE + 8 + 0x10000, S_X).reshape(T, H)
     raise KeyError(workload)
