@@ -66,6 +66,7 @@ Q8_BPW = 34 / 32
 
 
 GAIN_BPC = 17 / 32  # bytes per output channel of one down-gain table
+BATCH_MERGE_MAX_T = 4  # the batch kernels run the shared expert's items in the same launch up to this T
 MX4_BPW = 17 / 32  # bytes per MXFP4 weight
 VQ_BITS = {"vq12": 12, "vq13": 13}  # index bits per 8 weights
 
@@ -96,11 +97,14 @@ def kernel_bytes(name, shape, T, U, gains=0, fmt="q2"):
         "prefill_gateup_q8": 2 * Ish * H * Q8_BPW + 2 * T * H + 2 * T * Ish,
         "prefill_down_q8": H * Ish * Q8_BPW + 2 * T * Ish + 4 * T * H,
         "combine": 4 * P * H + 4 * T * H + 4 * T * H + gains * U * H * GAIN_BPC,
-        # batch path: the distinct experts' 2-bit rows, the shared expert's 8-bit rows, activations in and out
-        "batch_gateup_q2": U * 2 * I * H * Q2_BPW + 2 * T * H + 4 * P * I,
-        "batch_down_q2": U * H * I * Q2_BPW + 4 * P * I + 4 * P * H,
-        "batch_gateup_q8": 2 * Ish * H * Q8_BPW + 2 * T * H + 4 * T * Ish,
-        "batch_down_q8": H * Ish * Q8_BPW + 4 * T * Ish + 4 * T * H,
+        # batch path (each product over the distinct experts' 2-bit rows and the shared expert's
+        # 8-bit rows): weights, activation rows in, results out
+        "batch_gateup": U * 2 * I * H * Q2_BPW + 2 * T * H + 4 * P * I
+        + (2 * Ish * H * Q8_BPW + 4 * T * Ish if T <= BATCH_MERGE_MAX_T else 0),
+        "batch_down": U * H * I * Q2_BPW + 4 * P * I + 4 * P * H
+        + (H * Ish * Q8_BPW + 4 * T * Ish + 4 * T * H if T <= BATCH_MERGE_MAX_T else 0),
+        "batch_gateup_shared": 2 * Ish * H * Q8_BPW + 2 * T * H + 4 * T * Ish,
+        "batch_down_shared": H * Ish * Q8_BPW + 4 * T * Ish + 4 * T * H,
         # one launch of the fused decode kernel does the whole layer for up to 8 tokens
         "decode_fused": layer_bytes(shape, T, U, gains),
         # MXFP4 experts: weights of the distinct experts, fp32 activation rows in, results out

@@ -128,7 +128,7 @@ enum {
  * and the prefill path above: the measured crossovers on a GB300 at H=4096,
  * I=2048, E=384, top-6.
  */
-#define DS4MOE_AUTO_DECODE_MAX_T 12
+#define DS4MOE_AUTO_DECODE_MAX_T 1
 #define DS4MOE_AUTO_BATCH_MAX_T 64
 
 /* Most tokens one call of the batch path takes. */

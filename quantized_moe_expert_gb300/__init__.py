@@ -22,7 +22,7 @@ DS4MOE_OK, DS4MOE_EINVAL, DS4MOE_ENOMEM, DS4MOE_ECUDA, DS4MOE_EUNSUPPORTED, DS4M
 DS4MOE_ESCRATCH = -7
 DS4MOE_NOALLOC_SCRATCH = 4 << 20
 PATH_AUTO, PATH_DECODE, PATH_PREFILL, PATH_BATCH = 0, 1, 2, 3
-AUTO_DECODE_MAX_T = 12
+AUTO_DECODE_MAX_T = 1
 AUTO_BATCH_MAX_T = 64
 BATCH_MAX_T = 64
 FLAG_MXFP4 = 1

@@ -33,14 +33,19 @@ constexpr int kBatchThreads = 32 * (kBatchComputeWarps + 1 + kBatchEpiWarps);
 constexpr int kPartPitch = 20; // floats per (warp, matrix, column) run of 16 row sums: 20 avoids bank conflicts
 constexpr uint64_t kBatchWaitNs = 1000000000ull; // 1 s: far beyond any legitimate wait
 constexpr int kBatchStageCap = 48 << 10; // most bytes of one 8-bit stage
+// Relative cost of a routed and a shared item (a 16-row tile pair over all
+// columns, or four 16-row tiles), for splitting the items over the CTAs.
+constexpr int kBatchCostRouted = 2, kBatchCostShared = 3;
+// Up to this many tokens one launch per product runs both kinds of items.
+constexpr int kBatchMergeMaxT = 4;
 
-// The four products, one kernel instantiation each.
-enum BatchMode : int {
-    kBq2GateUp = 0, // routed gate and up: a 16-row tile of each per item, SwiGLU into hq
-    kBq2Down = 1,   // routed down: four 16-row tiles per item, into ye
-    kBq8GateUp = 2, // shared gate and up (8-bit), SwiGLU into hs
-    kBq8Down = 3    // shared down (8-bit), into ysh
-};
+// Each product kernel (gate/up, down) runs two kinds of items: first the
+// routed experts' (2-bit; a slot is a distinct expert with up to kBatchCols
+// of its pairs), then the shared expert's (8-bit; a slot is a group of up to
+// kBatchCols tokens).
+enum BatchKind : int { kRouted = 0, kShared = 1 };
+// Which kinds a product kernel runs (KINDS): bit 0 routed, bit 1 shared.
+constexpr int kBatchRouted = 1, kBatchShared = 2, kBatchBoth = 3;
 
 struct BatchArgs {
     int H, I, K, Ish, T;
@@ -201,28 +206,37 @@ __global__ void __launch_bounds__(1024) batch_group_kernel(int32_t *__restrict__
         *nvslot = sc[1023];
 }
 
-// Shared memory of a batch CTA for product MODE: the ring of stages (2-bit:
-// an item's whole records; 8-bit: `chunk` columns of them), the slot's
-// activation rows (hi, and lo for the down products) and, for 2-bit, their
-// sub-block sums, each row padded by 32 bytes, the compute warps' partial sums
-// of one item, the barriers (full and empty per stage; activations full and
-// empty; partial sums full and empty) and the abort flag.
+// Shared memory of a batch CTA for one product (gate/up or DOWN): the ring of
+// stages (routed: an item's whole 2-bit records; shared: `chunk` columns of an
+// item's 8-bit records), the slot's activation rows (hi, and lo for down) and,
+// for routed slots, their sub-block sums, each row padded by 32 bytes, the
+// compute warps' partial sums of one item, the barriers (full and empty per
+// stage; activations full and empty; partial sums full and empty) and the
+// abort flag.
 struct BatchPlan {
-    int K, chunk, nsub, nblk, mat_bytes, stage_bytes, nstage;
+    int K2, nb2, mat2, stage2;                  // routed: columns, 256-blocks, a tile's records, an item's stage
+    int K8, chunk8, nsub8, nblk8, mat8, stage8; // shared: columns, per stage, stages per item, 32-blocks per stage,
+                                                // a tile's records in a stage, a stage
+    int stage_bytes, nstage;
     int act_pitch, sum_pitch;
     int oact, olo, osum, opart, obar, oflag, total;
-    __host__ __device__ BatchPlan(int mode, int H, int I, int Ish, int chunk8, int ns) {
-        const bool q2 = mode == kBq2GateUp || mode == kBq2Down;
-        const bool down = mode == kBq2Down || mode == kBq8Down;
-        K = mode == kBq2Down ? I : mode == kBq8Down ? Ish : H;
-        chunk = q2 ? K : chunk8;
-        nsub = K / chunk;
-        nblk = q2 ? chunk / 256 : chunk / 32; // blocks of one tile in a stage
-        mat_bytes = nblk * (q2 ? kQ2Rec : kQ8Rec);
-        stage_bytes = (down ? 4 : 2) * mat_bytes;
+    __host__ __device__ BatchPlan(bool down, int H, int I, int Ish, int chunk, int ns) {
+        const int tiles = down ? 4 : 2;
+        K2 = down ? I : H;
+        nb2 = K2 / 256;
+        mat2 = nb2 * kQ2Rec;
+        stage2 = tiles * mat2;
+        K8 = Ish > 0 ? (down ? Ish : H) : 0;
+        chunk8 = Ish > 0 ? chunk : 32;
+        nsub8 = K8 / chunk8;
+        nblk8 = chunk8 / 32;
+        mat8 = nblk8 * kQ8Rec;
+        stage8 = Ish > 0 ? tiles * mat8 : 0;
+        stage_bytes = stage2 > stage8 ? stage2 : stage8;
         nstage = ns;
-        act_pitch = 2 * K + 32; // 32: the 8-byte loads of rows g = 0..3 (one half-warp) hit distinct banks
-        sum_pitch = q2 ? K / 4 + 32 : 0;
+        const int kmax = K2 > K8 ? K2 : K8;
+        act_pitch = 2 * kmax + 32; // 32: the 8-byte loads of rows g = 0..3 (one half-warp) hit distinct banks
+        sum_pitch = K2 / 4 + 32;
         oact = ns * stage_bytes;
         olo = oact + kBatchCols * act_pitch;
         osum = olo + (down ? kBatchCols * act_pitch : 0);
@@ -231,6 +245,11 @@ struct BatchPlan {
         oflag = obar + 8 * (2 * ns + 4);
         total = oflag + 16;
     }
+};
+
+// Position in a CTA's item range: kind, slot within the kind, row tile.
+struct BatchCursor {
+    int kind, v, tile;
 };
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
@@ -309,27 +328,28 @@ __device__ __forceinline__ void batch_copy(uint8_t *dst, const void *src, unsign
                  : "memory");
 }
 
-// One product over the items of this CTA (see BatchMode). Gate/up items: rows
-// 16 tile .. 16 tile + 15 of gate and up; the SwiGLU rows go to the down
-// product's activation layout (routed: by grouped position, permuted, bf16
-// hi + lo and sums; shared: by token, binary16 hi + lo). Down items: rows
-// 64 tile .. 64 tile + 63 (compute warps 0-7 the first two 16-row tiles,
-// warps 8-15 the other two).
+// One product over the items of this CTA. Gate/up items: rows 16 tile ..
+// 16 tile + 15 of gate and up; the SwiGLU rows go to the down product's
+// activation layout (routed: by grouped position, permuted, bf16 hi + lo and
+// sums; shared: by token, binary16 hi + lo). Down items: rows 64 tile ..
+// 64 tile + 63 (compute warps 0-7 the first two 16-row tiles, warps 8-15 the
+// other two), into ye (routed, by grouped position) or ysh (shared, by token).
 //
-// Roles: the producer streams the stages of the CTA's items through the ring
-// (waiting for a slot's release by all compute warps) and loads a slot's
-// activation rows once every compute warp is done with the previous slot's;
-// each compute warp runs its share of every stage as soon as it lands and
-// leaves its partial sums of an item for the epilogue warps, which reduce
-// them and write the results while the next item computes.
-template <int MODE> __global__ void __launch_bounds__(kBatchThreads, 1) batch_product_kernel(const BatchArgs a) {
+// The items are split over the CTAs in contiguous ranges of equal cost.
+// Roles: the producer streams the
+// stages of the CTA's items through the ring (waiting for a slot's release by
+// all compute warps) and loads a slot's activation rows once every compute
+// warp is done with the previous slot's; each compute warp runs its share of
+// every stage as soon as it lands and leaves its partial sums of an item for
+// the epilogue warps, which reduce them and write the results while the next
+// item computes.
+template <bool DOWN, int KINDS>
+__global__ void __launch_bounds__(kBatchThreads, 1) batch_product_kernel(const BatchArgs a) {
     pdl_launch_next();
     pdl_wait();
-    constexpr bool Q2 = MODE == kBq2GateUp || MODE == kBq2Down;
-    constexpr bool DOWN = MODE == kBq2Down || MODE == kBq8Down;
     extern __shared__ __align__(128) uint8_t sm[];
-    const BatchPlan pl(MODE, a.H, a.I, a.Ish, a.chunk, a.nstage);
-    const int ns = pl.nstage, nsub = pl.nsub, K = pl.K;
+    const BatchPlan pl(DOWN, a.H, a.I, a.Ish, a.chunk, a.nstage);
+    const int ns = pl.nstage;
     uint64_t *const full = reinterpret_cast<uint64_t *>(sm + pl.obar); // [ns]
     uint64_t *const empty = full + ns;                                 // [ns]
     uint64_t *const act_full = empty + ns;
@@ -339,33 +359,55 @@ template <int MODE> __global__ void __launch_bounds__(kBatchThreads, 1) batch_pr
     volatile int *const abort = reinterpret_cast<volatile int *>(sm + pl.oflag);
     float *const part = reinterpret_cast<float *>(sm + pl.opart); // [warp][matrix][column][kPartPitch]
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int rows_out = MODE == kBq2GateUp ? a.I : MODE == kBq8GateUp ? a.Ish : a.H;
-    const int ntiles = DOWN ? rows_out / 64 : rows_out / 16; // items per slot
-    const int nslots = Q2 ? *a.nvslot : (a.T + kBatchCols - 1) / kBatchCols;
-    const int64_t nitems = (int64_t)nslots * ntiles;
-    const int64_t i0 = nitems * blockIdx.x / gridDim.x;
-    const int cnt = (int)(nitems * (blockIdx.x + 1) / gridDim.x - i0);
+    // items: routed (nslot2 slots x ntiles2), then shared (nslot8 token groups x ntiles8)
+    const int ntiles2 = DOWN ? a.H / 64 : a.I / 16;
+    const int ntiles8 = DOWN ? a.H / 64 : a.Ish / 16;
+    const int nslot2 = (KINDS & kBatchRouted) ? *a.nvslot : 0;
+    const int nslot8 = (KINDS & kBatchShared) && a.Ish > 0 ? (a.T + kBatchCols - 1) / kBatchCols : 0;
+    // the item kind at a cursor (known at compile time unless the kernel runs both)
+    auto routed = [&](const BatchCursor &c) {
+        return KINDS == kBatchRouted ? true : KINDS == kBatchShared ? false : c.kind == kRouted;
+    };
+    const int nsub8 = pl.nsub8;
+    const int64_t R = (int64_t)nslot2 * ntiles2, S8 = (int64_t)nslot8 * ntiles8;
+    // cost units of the product: a routed item kBatchCostRouted, a shared item kBatchCostShared
+    // (their measured times: both are bound by the tile GEMV's instruction issue)
+    const int64_t R2 = R * kBatchCostRouted, U = R2 + S8 * kBatchCostShared;
+    // the first item that starts at or after unit u
+    auto item_at = [&](int64_t u) {
+        return u <= R2 ? (u + kBatchCostRouted - 1) / kBatchCostRouted
+                       : R + (u - R2 + kBatchCostShared - 1) / kBatchCostShared;
+    };
+    const int64_t i0 = item_at(U * blockIdx.x / gridDim.x);
+    const int cnt = (int)(item_at(U * (blockIdx.x + 1) / gridDim.x) - i0);
     if (cnt <= 0)
         return;
-    const int nq = cnt * nsub; // stages this CTA streams
-    const int64_t tile_bytes = (int64_t)(K / 256) * kQ2Rec; // a 2-bit tile's records over all K
-    // items run slot-major: item i0 + li is (slot, tile) = ((i0 + li) / ntiles, (i0 + li) % ntiles);
-    // every role steps through them with one division at the start
-    const int v0 = (int)(i0 / ntiles), t0 = (int)(i0 % ntiles);
-    auto step = [&](int &v, int &tile) {
-        if (++tile == ntiles) {
-            tile = 0;
-            v++;
+    const int64_t tile_bytes2 = (int64_t)pl.nb2 * kQ2Rec; // a 2-bit tile's records over all K2
+    const BatchCursor c0 = i0 < R ? BatchCursor{kRouted, (int)(i0 / ntiles2), (int)(i0 % ntiles2)}
+                                  : BatchCursor{kShared, (int)((i0 - R) / ntiles8), (int)((i0 - R) % ntiles8)};
+    auto step = [&](BatchCursor &c) {
+        if (routed(c)) {
+            if (++c.tile == ntiles2) {
+                c.tile = 0;
+                if (++c.v == nslot2 && KINDS == kBatchBoth) {
+                    c.kind = kShared;
+                    c.v = 0;
+                }
+            }
+        } else if (++c.tile == ntiles8) {
+            c.tile = 0;
+            c.v++;
         }
     };
-    // first grouped position (routed) or token (shared) of slot v, and its columns
-    auto slot_cols = [&](int v, int &p0, int &n) {
-        if constexpr (Q2) {
-            const int4 vs = a.vslot[v];
+    auto slot_id = [&](const BatchCursor &c) { return routed(c) ? c.v : nslot2 + c.v; };
+    // first grouped position (routed) or token (shared) of the cursor's slot, and its columns
+    auto slot_cols = [&](const BatchCursor &c, int &p0, int &n) {
+        if (routed(c)) {
+            const int4 vs = a.vslot[c.v];
             p0 = vs.y;
             n = vs.z;
         } else {
-            p0 = kBatchCols * v;
+            p0 = kBatchCols * c.v;
             n = min(kBatchCols, a.T - p0);
         }
     };
@@ -392,71 +434,79 @@ template <int MODE> __global__ void __launch_bounds__(kBatchThreads, 1) batch_pr
     if (warp == kBatchProducerWarp) {
         if (lane != 0)
             return;
-        int issued = 0, k = -1, cur_v = -1;
-        int v = v0, tile = t0, sub = 0;
-        for (int q = 0; q < nq; q++) {
-            if (q > 0 && ++sub == nsub) {
-                sub = 0;
-                step(v, tile);
-            }
-            if (q >= ns && !batch_wait(empty + q % ns, (unsigned)(q / ns - 1) & 1u, abort, a.status))
-                break;
-            uint64_t *bar = full + q % ns;
-            uint8_t *dst = sm + (q % ns) * pl.stage_bytes;
-            batch_expect(bar, (unsigned)pl.stage_bytes);
-            if constexpr (MODE == kBq2GateUp) {
-                const int64_t gt = (int64_t)a.vslot[v].x * (a.I / 16) + tile;
-                batch_copy(dst, a.gate.rec + gt * tile_bytes, (unsigned)pl.mat_bytes, bar);
-                batch_copy(dst + pl.mat_bytes, a.up.rec + gt * tile_bytes, (unsigned)pl.mat_bytes, bar);
-            } else if constexpr (MODE == kBq2Down) {
-                const int64_t gt = (int64_t)a.vslot[v].x * (a.H / 16) + 4 * tile;
-                batch_copy(dst, a.down.rec + gt * tile_bytes, (unsigned)pl.stage_bytes, bar);
-            } else {
-                const int64_t nbq = K / 32, b0 = (int64_t)sub * pl.nblk;
-                if constexpr (MODE == kBq8GateUp) {
-                    batch_copy(dst, a.sh_gate.rec + (tile * nbq + b0) * kQ8Rec, (unsigned)pl.mat_bytes, bar);
-                    batch_copy(dst + pl.mat_bytes, a.sh_up.rec + (tile * nbq + b0) * kQ8Rec, (unsigned)pl.mat_bytes,
-                               bar);
-                } else {
-                    for (int m = 0; m < 4; m++)
-                        batch_copy(dst + m * pl.mat_bytes, a.sh_down.rec + ((4 * tile + m) * nbq + b0) * kQ8Rec,
-                                   (unsigned)pl.mat_bytes, bar);
-                }
-            }
-            issued = q + 1;
-            if (sub == 0 && v != cur_v) { // the first stage of a new slot: its activation rows
-                k++;
-                cur_v = v;
-                if (k > 0 && !batch_wait(act_empty, (unsigned)(k - 1) & 1u, abort, a.status)) {
-                    k--; // not issued
+        int issued = 0, k = -1, cur = -1;
+        BatchCursor c = c0;
+        bool ok = true;
+        for (int li = 0; li < cnt && ok; li++, step(c)) {
+            const int nsub = routed(c) ? 1 : nsub8;
+            for (int sub = 0; sub < nsub; sub++) {
+                const int q = issued;
+                if (q >= ns && !batch_wait(empty + q % ns, (unsigned)(q / ns - 1) & 1u, abort, a.status)) {
+                    ok = false;
                     break;
                 }
-                int p0, n;
-                slot_cols(v, p0, n);
-                const unsigned row_bytes = (DOWN ? 4u : 2u) * K + (Q2 ? K / 4 : 0);
-                batch_expect(act_full, (unsigned)n * row_bytes);
-                for (int c = 0; c < n; c++) {
-                    const int64_t pos = p0 + c;
-                    const uint16_t *hi, *lo = nullptr, *sums = nullptr;
-                    if constexpr (MODE == kBq2GateUp) {
-                        const int t = __ldg(a.perm + pos) / a.K;
-                        hi = a.xq + (int64_t)t * K;
-                        sums = a.xsums + (int64_t)t * (K / 8);
-                    } else if constexpr (MODE == kBq2Down) {
-                        hi = a.hq_hi + pos * K;
-                        lo = a.hq_lo + pos * K;
-                        sums = a.hsums + pos * (K / 8);
-                    } else if constexpr (MODE == kBq8GateUp) {
-                        hi = a.x + pos * K;
+                uint64_t *bar = full + q % ns;
+                uint8_t *dst = sm + (q % ns) * pl.stage_bytes;
+                if (routed(c)) {
+                    const int64_t e = a.vslot[c.v].x;
+                    batch_expect(bar, (unsigned)(DOWN ? 4 : 2) * pl.mat2);
+                    if (DOWN) {
+                        batch_copy(dst, a.down.rec + (e * (a.H / 16) + 4 * c.tile) * tile_bytes2,
+                                   (unsigned)(4 * pl.mat2), bar);
                     } else {
-                        hi = a.hs_hi + pos * K;
-                        lo = a.hs_lo + pos * K;
+                        const int64_t gt = e * (a.I / 16) + c.tile;
+                        batch_copy(dst, a.gate.rec + gt * tile_bytes2, (unsigned)pl.mat2, bar);
+                        batch_copy(dst + pl.mat2, a.up.rec + gt * tile_bytes2, (unsigned)pl.mat2, bar);
                     }
-                    batch_copy(sm + pl.oact + c * pl.act_pitch, hi, 2 * K, act_full);
-                    if (DOWN)
-                        batch_copy(sm + pl.olo + c * pl.act_pitch, lo, 2 * K, act_full);
-                    if (Q2)
-                        batch_copy(sm + pl.osum + c * pl.sum_pitch, sums, K / 4, act_full);
+                } else {
+                    const int64_t nbq = pl.K8 / 32, b0 = (int64_t)sub * pl.nblk8;
+                    batch_expect(bar, (unsigned)(DOWN ? 4 : 2) * pl.mat8);
+                    if (DOWN) {
+                        for (int m = 0; m < 4; m++)
+                            batch_copy(dst + m * pl.mat8, a.sh_down.rec + ((4 * c.tile + m) * nbq + b0) * kQ8Rec,
+                                       (unsigned)pl.mat8, bar);
+                    } else {
+                        batch_copy(dst, a.sh_gate.rec + (c.tile * nbq + b0) * kQ8Rec, (unsigned)pl.mat8, bar);
+                        batch_copy(dst + pl.mat8, a.sh_up.rec + (c.tile * nbq + b0) * kQ8Rec, (unsigned)pl.mat8, bar);
+                    }
+                }
+                issued = q + 1;
+                if (sub == 0 && slot_id(c) != cur) { // the first stage of a new slot: its activation rows
+                    cur = slot_id(c);
+                    if (k >= 0 && !batch_wait(act_empty, (unsigned)k & 1u, abort, a.status)) {
+                        ok = false;
+                        break;
+                    }
+                    k++;
+                    int p0, n;
+                    slot_cols(c, p0, n);
+                    const bool rt = routed(c);
+                    const int K = rt ? pl.K2 : pl.K8;
+                    const unsigned row_bytes = (DOWN ? 4u : 2u) * K + (rt ? K / 4 : 0);
+                    batch_expect(act_full, (unsigned)n * row_bytes);
+                    for (int col = 0; col < n; col++) {
+                        const int64_t pos = p0 + col;
+                        const uint16_t *hi, *lo = nullptr, *sums = nullptr;
+                        if (rt && !DOWN) {
+                            const int t = __ldg(a.perm + pos) / a.K;
+                            hi = a.xq + (int64_t)t * K;
+                            sums = a.xsums + (int64_t)t * (K / 8);
+                        } else if (rt) {
+                            hi = a.hq_hi + pos * K;
+                            lo = a.hq_lo + pos * K;
+                            sums = a.hsums + pos * (K / 8);
+                        } else if (!DOWN) {
+                            hi = a.x + pos * K;
+                        } else {
+                            hi = a.hs_hi + pos * K;
+                            lo = a.hs_lo + pos * K;
+                        }
+                        batch_copy(sm + pl.oact + col * pl.act_pitch, hi, 2 * K, act_full);
+                        if (DOWN)
+                            batch_copy(sm + pl.olo + col * pl.act_pitch, lo, 2 * K, act_full);
+                        if (rt)
+                            batch_copy(sm + pl.osum + col * pl.sum_pitch, sums, K / 4, act_full);
+                    }
                 }
             }
         }
@@ -470,83 +520,82 @@ template <int MODE> __global__ void __launch_bounds__(kBatchThreads, 1) batch_pr
 
     if (warp > kBatchProducerWarp) { // epilogue warps: thread et of kBatchEpiThreads
         const int et = (warp - kBatchProducerWarp - 1) * 32 + lane;
-        int cur_v = -1, p0 = 0, n = 0;
-        int v = v0, tile = t0;
-        for (int li = 0; li < cnt; li++, step(v, tile)) {
-            if (v != cur_v) {
-                slot_cols(v, p0, n);
-                cur_v = v;
+        int cur = -1, p0 = 0, n = 0;
+        BatchCursor c = c0;
+        for (int li = 0; li < cnt; li++, step(c)) {
+            if (slot_id(c) != cur) {
+                slot_cols(c, p0, n);
+                cur = slot_id(c);
             }
             if (!batch_wait(part_full, (unsigned)li & 1u, abort, a.status))
                 return;
-            if constexpr (DOWN) {
-                // output o = (c, m, r): row 64 tile + 16 m + r of column c, summed over its group's warps
+            const int tile = c.tile;
+            if (DOWN) {
+                // output o = (col, m, r): row 64 tile + 16 m + r of column col, summed over its group's warps
+                float *dst = routed(c) ? a.ye : a.ysh;
 #pragma unroll
                 for (int k4 = 0; k4 < 16 * 4 * kBatchCols / kBatchEpiThreads; k4++) {
                     const int o = et + kBatchEpiThreads * k4;
-                    const int c = o >> 6, m = (o >> 4) & 3, r = o & 15;
-                    if (c < n) {
+                    const int col = o >> 6, m = (o >> 4) & 3, r = o & 15;
+                    if (col < n) {
                         float acc = 0.f;
 #pragma unroll
                         for (int w = 8 * (m >> 1); w < 8 * (m >> 1) + 8; w++)
-                            acc += part[((w * 2 + (m & 1)) * kBatchCols + c) * kPartPitch + r];
-                        if (MODE == kBq2Down)
-                            a.ye[(int64_t)(p0 + c) * a.H + 64 * tile + 16 * m + r] = acc;
-                        else
-                            a.ysh[(int64_t)(p0 + c) * a.H + 64 * tile + 16 * m + r] = acc;
+                            acc += part[((w * 2 + (m & 1)) * kBatchCols + col) * kPartPitch + r];
+                        dst[(int64_t)(p0 + col) * a.H + 64 * tile + 16 * m + r] = acc;
                     }
                 }
             } else {
 #pragma unroll
-              for (int k2 = 0; k2 < 16 * kBatchCols / kBatchEpiThreads; k2++) {
-                const int c = (et >> 4) + (kBatchEpiThreads / 16) * k2, r = et & 15;
-                float hv = 0.f;
-                if (c < n) {
-                    float gs = 0.f, us = 0.f;
+                for (int k2 = 0; k2 < 16 * kBatchCols / kBatchEpiThreads; k2++) {
+                    const int col = (et >> 4) + (kBatchEpiThreads / 16) * k2, r = et & 15;
+                    float hv = 0.f;
+                    if (col < n) {
+                        float gs = 0.f, us = 0.f;
 #pragma unroll
-                    for (int w = 0; w < kBatchComputeWarps; w++) {
-                        gs += part[((w * 2) * kBatchCols + c) * kPartPitch + r];
-                        us += part[((w * 2 + 1) * kBatchCols + c) * kPartPitch + r];
+                        for (int w = 0; w < kBatchComputeWarps; w++) {
+                            gs += part[((w * 2) * kBatchCols + col) * kPartPitch + r];
+                            us += part[((w * 2 + 1) * kBatchCols + col) * kPartPitch + r];
+                        }
+                        hv = silu(gs) * us;
                     }
-                    hv = silu(gs) * us;
-                }
-                if constexpr (MODE == kBq8GateUp) {
-                    if (c < n) {
-                        const __half hi = __float2half_rn(hv);
-                        const __half lo = __float2half_rn(hv - __half2float(hi));
-                        const int64_t o = (int64_t)(p0 + c) * a.Ish + 16 * tile + r;
-                        a.hs_hi[o] = __half_as_ushort(hi);
-                        a.hs_lo[o] = __half_as_ushort(lo);
-                    }
-                } else {
-                    // row r of the tile is column k = 16 tile + r of the down matrix: position r
-                    // of its sub-block j = tile % 16 in block tile / 16
-                    const int blk = tile >> 4, j = tile & 15;
-                    float hs = 0.f;
-                    if (c < n) {
-                        const int e2 = 2 * q2_p(r, j >> 3);
-                        const float hp = hv * (1.0f / (float)(1 << e2)); // exact: power of two
-                        const uint32_t h1 = f32_to_bf16_bits(hp);
-                        const float h1f = __uint_as_float(h1 << 16);
-                        const uint32_t h2 = f32_to_bf16_bits(hp - h1f);
-                        const float h2f = __uint_as_float(h2 << 16);
-                        const int64_t o = (int64_t)(p0 + c) * a.I + q2_act_index(tile * 16 + r);
-                        a.hq_hi[o] = (uint16_t)h1;
-                        a.hq_lo[o] = (uint16_t)h2;
-                        hs = (h1f + h2f) * (float)(1 << e2); // the value the down product sees
-                    }
+                    if (!routed(c)) {
+                        if (col < n) {
+                            const __half hi = __float2half_rn(hv);
+                            const __half lo = __float2half_rn(hv - __half2float(hi));
+                            const int64_t o = (int64_t)(p0 + col) * a.Ish + 16 * tile + r;
+                            a.hs_hi[o] = __half_as_ushort(hi);
+                            a.hs_lo[o] = __half_as_ushort(lo);
+                        }
+                    } else {
+                        // row r of the tile is column k = 16 tile + r of the down matrix: position r
+                        // of its sub-block j = tile % 16 in block tile / 16
+                        const int blk = tile >> 4, j = tile & 15;
+                        float hs = 0.f;
+                        if (col < n) {
+                            const int e2 = 2 * q2_p(r, j >> 3);
+                            const float hp = hv * (1.0f / (float)(1 << e2)); // exact: power of two
+                            const uint32_t h1 = f32_to_bf16_bits(hp);
+                            const float h1f = __uint_as_float(h1 << 16);
+                            const uint32_t h2 = f32_to_bf16_bits(hp - h1f);
+                            const float h2f = __uint_as_float(h2 << 16);
+                            const int64_t o = (int64_t)(p0 + col) * a.I + q2_act_index(tile * 16 + r);
+                            a.hq_hi[o] = (uint16_t)h1;
+                            a.hq_lo[o] = (uint16_t)h2;
+                            hs = (h1f + h2f) * (float)(1 << e2); // the value the down product sees
+                        }
 #pragma unroll
-                    for (int o = 8; o > 0; o >>= 1) // over the 16 rows: one sub-block of the down columns
-                        hs += __shfl_xor_sync(0xFFFFFFFFu, hs, o);
-                    if (c < n && r == 0) {
-                        const uint32_t h1 = f32_to_bf16_bits(hs);
-                        const uint32_t h2 = f32_to_bf16_bits(hs - __uint_as_float(h1 << 16));
-                        uint16_t *so = a.hsums + (int64_t)(p0 + c) * (a.I / 8);
-                        so[q2_sum_index(blk, j, 0)] = (uint16_t)h1;
-                        so[q2_sum_index(blk, j, 1)] = (uint16_t)h2;
+                        for (int o = 8; o > 0; o >>= 1) // over the 16 rows: one sub-block of the down columns
+                            hs += __shfl_xor_sync(0xFFFFFFFFu, hs, o);
+                        if (col < n && r == 0) {
+                            const uint32_t h1 = f32_to_bf16_bits(hs);
+                            const uint32_t h2 = f32_to_bf16_bits(hs - __uint_as_float(h1 << 16));
+                            uint16_t *so = a.hsums + (int64_t)(p0 + col) * (a.I / 8);
+                            so[q2_sum_index(blk, j, 0)] = (uint16_t)h1;
+                            so[q2_sum_index(blk, j, 1)] = (uint16_t)h2;
+                        }
                     }
                 }
-              }
             }
             __syncwarp();
             if (lane == 0)
@@ -558,13 +607,13 @@ template <int MODE> __global__ void __launch_bounds__(kBatchThreads, 1) batch_pr
     // compute warps
     const int g = lane >> 2, tig = lane & 3;
     const int grp = warp >> 3, wl = warp & 7; // down products: tile pair, warp within it
-    int cur_v = -1, k = -1, n = 0;
-    int v = v0, tile = t0;
+    int cur = -1, k = -1, n = 0, q = 0;
+    BatchCursor c = c0;
     for (int li = 0; li < cnt; li++) {
-        if (v != cur_v) {
+        if (slot_id(c) != cur) {
             int p0;
-            slot_cols(v, p0, n);
-            cur_v = v;
+            slot_cols(c, p0, n);
+            cur = slot_id(c);
             k++;
             if (!batch_wait(act_full, (unsigned)k & 1u, abort, a.status))
                 return;
@@ -574,35 +623,39 @@ template <int MODE> __global__ void __launch_bounds__(kBatchThreads, 1) batch_pr
         const uint8_t *lrow = sm + pl.olo + col * pl.act_pitch;
         const uint8_t *srow = sm + pl.osum + col * pl.sum_pitch;
         float out[2][2][2] = {};
-        for (int sub = 0; sub < nsub; sub++) {
-            const int q = li * nsub + sub;
+        const int nsub = routed(c) ? 1 : nsub8;
+        for (int sub = 0; sub < nsub; sub++, q++) {
             if (!batch_wait(full + q % ns, (unsigned)(q / ns) & 1u, abort, a.status))
                 return;
             const uint8_t *stage = sm + (q % ns) * pl.stage_bytes;
-            const int nblk = pl.nblk;
-            if constexpr (MODE == kBq2GateUp) {
-                const uint8_t *rec[2] = {stage, stage + pl.mat_bytes};
-                q2_gemv<2, false>(rec, xrow, xrow, srow, nblk * warp / kBatchComputeWarps,
-                                  nblk * (warp + 1) / kBatchComputeWarps, lane, out);
-            } else if constexpr (MODE == kBq2Down) {
-                const uint8_t *rec[2] = {stage + (2 * grp) * pl.mat_bytes, stage + (2 * grp + 1) * pl.mat_bytes};
-                q2_gemv<2, true>(rec, xrow, lrow, srow, nblk * wl / 8, nblk * (wl + 1) / 8, lane, out);
-            } else if constexpr (MODE == kBq8GateUp) {
-                const uint8_t *rec[2] = {stage, stage + pl.mat_bytes};
-                const uint8_t *xs = xrow + 2 * sub * pl.chunk;
-                q8_gemv<2, false, true>(rec, xs, xs, nblk * warp / kBatchComputeWarps,
-                                        nblk * (warp + 1) / kBatchComputeWarps, lane, out);
+            if (routed(c)) {
+                const int nb = pl.nb2;
+                if (DOWN) {
+                    const uint8_t *rec[2] = {stage + (2 * grp) * pl.mat2, stage + (2 * grp + 1) * pl.mat2};
+                    q2_gemv<2, true>(rec, xrow, lrow, srow, nb * wl / 8, nb * (wl + 1) / 8, lane, out);
+                } else {
+                    const uint8_t *rec[2] = {stage, stage + pl.mat2};
+                    q2_gemv<2, false>(rec, xrow, xrow, srow, nb * warp / kBatchComputeWarps,
+                                      nb * (warp + 1) / kBatchComputeWarps, lane, out);
+                }
             } else {
-                const uint8_t *rec[2] = {stage + (2 * grp) * pl.mat_bytes, stage + (2 * grp + 1) * pl.mat_bytes};
-                q8_gemv<2, true, false>(rec, xrow + 2 * sub * pl.chunk, lrow + 2 * sub * pl.chunk, nblk * wl / 8,
-                                        nblk * (wl + 1) / 8, lane, out);
+                const int nb = pl.nblk8;
+                const int off = 2 * sub * pl.chunk8;
+                if (DOWN) {
+                    const uint8_t *rec[2] = {stage + (2 * grp) * pl.mat8, stage + (2 * grp + 1) * pl.mat8};
+                    q8_gemv<2, true, false>(rec, xrow + off, lrow + off, nb * wl / 8, nb * (wl + 1) / 8, lane, out);
+                } else {
+                    const uint8_t *rec[2] = {stage, stage + pl.mat8};
+                    q8_gemv<2, false, true>(rec, xrow + off, xrow + off, nb * warp / kBatchComputeWarps,
+                                            nb * (warp + 1) / kBatchComputeWarps, lane, out);
+                }
             }
             __syncwarp();
             if (lane == 0)
                 batch_arrive(empty + q % ns);
         }
-        step(v, tile);
-        if (li + 1 < cnt && v != cur_v) { // done with this slot's activation rows
+        step(c);
+        if (li + 1 < cnt && slot_id(c) != cur) { // done with this slot's activation rows
             __syncwarp();
             if (lane == 0)
                 batch_arrive(act_empty);
@@ -613,9 +666,9 @@ template <int MODE> __global__ void __launch_bounds__(kBatchThreads, 1) batch_pr
         for (int m = 0; m < 2; m++)
 #pragma unroll
             for (int cc = 0; cc < 2; cc++) {
-                const int c = 2 * tig + cc;
-                part[((warp * 2 + m) * kBatchCols + c) * kPartPitch + g] = out[m][0][cc];
-                part[((warp * 2 + m) * kBatchCols + c) * kPartPitch + g + 8] = out[m][1][cc];
+                const int cl = 2 * tig + cc;
+                part[((warp * 2 + m) * kBatchCols + cl) * kPartPitch + g] = out[m][0][cc];
+                part[((warp * 2 + m) * kBatchCols + cl) * kPartPitch + g + 8] = out[m][1][cc];
             }
         __syncwarp();
         if (lane == 0)

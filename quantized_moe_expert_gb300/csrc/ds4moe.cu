@@ -112,9 +112,9 @@ struct BatchState {
     int4 *vslot = nullptr;                                         // [Pb] virtual slots
     int32_t *nvslot = nullptr;
     int tmax = 0;                 // tokens per call; 0: the path is unavailable for this layer
-    int nstage[4] = {0, 0, 0, 0}; // ring depth of each product (BatchMode)
-    int smem[4] = {0, 0, 0, 0};   // its dynamic shared memory
-    int chunk[4] = {0, 0, 0, 0};  // columns per stage of the 8-bit products
+    int nstage[2] = {0, 0}; // ring depth of the gate/up and the down product kernel
+    int smem[2] = {0, 0};   // their dynamic shared memory
+    int chunk[2] = {0, 0};  // columns per stage of their shared-expert (8-bit) items
     int grid = 0;
 };
 
@@ -692,8 +692,9 @@ int run_experts_prefill(ds4moe *h, const void *x, int T, float *y) {
 
 // Experts and combine for the routing already in S.idx / S.w, T <= B.tmax:
 // x in the 2-bit tile GEMV's layout (unless the router wrote it), the grouping
-// with the virtual slots, the four persistent products (routed gate/up and
-// down, 2-bit; shared gate/up and down, 8-bit), the combine.
+// with the virtual slots, the two persistent products (gate/up, then down;
+// each over the routed experts' 2-bit items and the shared expert's 8-bit
+// items), the combine.
 int run_experts_batch(ds4moe *h, const void *x, int T, float *y, bool x_prepared) {
     const LayerDev &L = h->L;
     Scratch &S = h->S;
@@ -740,11 +741,16 @@ int run_experts_batch(ds4moe *h, const void *x, int T, float *y, bool x_prepared
         a.chunk = B.chunk[mode];
         launch(h, name, [&] { launch_pdl(fn, dim3(B.grid), dim3(kBatchThreads), B.smem[mode], st, a); });
     };
-    product(kBq2GateUp, "batch_gateup_q2", batch_product_kernel<kBq2GateUp>);
-    product(kBq2Down, "batch_down_q2", batch_product_kernel<kBq2Down>);
-    if (L.Ish > 0) {
-        product(kBq8GateUp, "batch_gateup_q8", batch_product_kernel<kBq8GateUp>);
-        product(kBq8Down, "batch_down_q8", batch_product_kernel<kBq8Down>);
+    // few tokens: one launch per product over both kinds of items (the shared expert fills the
+    // routed items' tail); more: separate launches, each split evenly over the SMs
+    if (T <= kBatchMergeMaxT || L.Ish == 0) {
+        product(0, "batch_gateup", batch_product_kernel<false, kBatchBoth>);
+        product(1, "batch_down", batch_product_kernel<true, kBatchBoth>);
+    } else {
+        product(0, "batch_gateup", batch_product_kernel<false, kBatchRouted>);
+        product(0, "batch_gateup_shared", batch_product_kernel<false, kBatchShared>);
+        product(1, "batch_down", batch_product_kernel<true, kBatchRouted>);
+        product(1, "batch_down_shared", batch_product_kernel<true, kBatchShared>);
     }
     launch(h, "combine", [&] {
         launch_pdl(combine_kernel, dim3(blocks_for((int64_t)T * L.H / 4, 256)), dim3(256), 0, st, S.ye,
@@ -1195,31 +1201,33 @@ int ds4moe_create(const ds4moe_layer_desc *desc, const ds4moe_weights *w, ds4moe
         BatchState &B = h->B;
         const int optin = (int)prop.sharedMemPerBlockOptin;
         bool fits = true;
-        for (int mode = 0; mode < 4; mode++) {
-            if (mode >= kBq8GateUp && L.Ish == 0)
-                continue;
-            int chunk = 0;
-            if (mode >= kBq8GateUp) {
-                const int K = mode == kBq8Down ? L.Ish : L.H, tiles = mode == kBq8Down ? 4 : 2;
-                for (int c = K; c >= 32 && !chunk; c -= 32)
-                    if (K % c == 0 && tiles * (c / 32) * kQ8Rec <= kBatchStageCap)
+        for (int down = 0; down < 2; down++) {
+            int chunk = 32;
+            if (L.Ish > 0) {
+                const int K = down ? L.Ish : L.H, tiles = down ? 4 : 2;
+                for (int c = K; c >= 32; c -= 32)
+                    if (K % c == 0 && tiles * (c / 32) * kQ8Rec <= kBatchStageCap) {
                         chunk = c;
+                        break;
+                    }
             }
             int ns = 3;
-            while (ns >= 2 && BatchPlan(mode, L.H, L.I, L.Ish, chunk, ns).total > optin)
+            while (ns >= 2 && BatchPlan(down, L.H, L.I, L.Ish, chunk, ns).total > optin)
                 ns--;
             fits = fits && ns >= 2;
-            B.nstage[mode] = ns;
-            B.chunk[mode] = chunk;
-            B.smem[mode] = BatchPlan(mode, L.H, L.I, L.Ish, chunk, ns).total;
+            B.nstage[down] = ns;
+            B.chunk[down] = chunk;
+            B.smem[down] = BatchPlan(down, L.H, L.I, L.Ish, chunk, ns).total;
         }
         if (fits) {
             B.tmax = L.Tmax < kBatchMaxT ? L.Tmax : kBatchMaxT;
             B.grid = nsm;
-            for (const void *fn : {(const void *)batch_product_kernel<kBq2GateUp>,
-                                   (const void *)batch_product_kernel<kBq2Down>,
-                                   (const void *)batch_product_kernel<kBq8GateUp>,
-                                   (const void *)batch_product_kernel<kBq8Down>})
+            for (const void *fn :
+                 {(const void *)batch_product_kernel<false, kBatchBoth>, (const void *)batch_product_kernel<true, kBatchBoth>,
+                  (const void *)batch_product_kernel<false, kBatchRouted>,
+                  (const void *)batch_product_kernel<true, kBatchRouted>,
+                  (const void *)batch_product_kernel<false, kBatchShared>,
+                  (const void *)batch_product_kernel<true, kBatchShared>})
                 cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
         }
     }

@@ -1,4 +1,5 @@
-"""GPU parity at the full H=4096, E=384 layer (decode T=1, T=8; prefill T=1024).
+"""GPU parity at the full H=4096, E=384 layer (decode T=1; T=8 on the batch and
+the decode path; prefill T=1024).
 
 The oracle computes every decode token and a sample of prefill rows one by
 one; routing is compared on every token. Runs in the launch configuration
@@ -52,13 +53,17 @@ def test_decode_t8(big):
     shape, layer, moe = big
     x = synth.make_tokens("decode_t8")
     xd = x_to_dev(x)
-    y = moe.forward(xd).cpu().numpy()
+    y = moe.forward(xd).cpu().numpy()  # the automatic path: the batch kernels
     s = moe.stats()  # statistics of the forward call (route() below replaces them)
+    yd = moe.forward(xd, path=ds4.PATH_DECODE).cpu().numpy()  # the fused decode kernel
+    sd = moe.stats()
     idx, w, gap, _ = moe.route(xd)
     y_ref, r = oracle.forward(shape, layer, x)
     check_routing(idx.cpu().numpy(), w.cpu().numpy(), gap.cpu().numpy(), r, shape.top_k)
-    assert s.path == ds4.PATH_DECODE and s.n_unique == len(np.unique(r["idx"]))
+    assert s.path == ds4.PATH_BATCH and s.n_unique == len(np.unique(r["idx"]))
+    assert sd.path == ds4.PATH_DECODE and sd.n_unique == s.n_unique
     assert_close(y, y_ref, TOL_DECODE)
+    assert_close(yd, y_ref, TOL_DECODE)
     assert moe.status() == 0
 
 

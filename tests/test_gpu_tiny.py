@@ -64,7 +64,7 @@ def test_auto_path_and_stats(tiny):
     x = tokens(shape, ds4.AUTO_BATCH_MAX_T + 1, 401)
     moe.forward(x_to_dev(x[:4]))
     s = moe.stats()
-    assert s.path == ds4.PATH_DECODE and s.tokens == 4 and s.kernel_count > 0
+    assert s.path == ds4.PATH_BATCH and s.tokens == 4 and s.kernel_count > 0
     r = oracle.route(shape, layer["router_w"], None, x[:4])
     assert s.n_unique == len(np.unique(r["idx"]))
     assert s.max_load == np.bincount(r["idx"].ravel()).max()
