@@ -127,6 +127,7 @@ TRAFFIC = {
     ("decode_fused", "decode_t1"): (83687424, "decode_fused.cuh", "706623878407df8cb54985e1f126854688daed79"),
     # mean of two batches of the pool (43-47 distinct experts each; the traffic follows the batch's experts)
     ("decode_fused", "decode_t8"): (404592256, "decode_fused.cuh", "706623878407df8cb54985e1f126854688daed79"),
+    ("batch_gateup", "batch_t64"): (1363576064, "batch_experts.cuh", "66928072388d47a3c2c96500e68f480a0891b70e"),
 }
 
 
