@@ -110,6 +110,9 @@ def kernel_bytes(name, shape, T, U, gains=0, fmt="q2"):
         # MXFP4 experts: weights of the distinct experts, fp32 activation rows in, results out
         "mx4_gateup": U * 2 * I * H * MX4_BPW + 4 * T * H + 4 * P * I,
         "mx4_down": U * H * I * MX4_BPW + 4 * P * I + 4 * P * H,
+        # MXFP4 prefill form: grouped GEMMs on the MXFP4 tile records, binary16 activation rows
+        "prefill_gateup_mx4": U * 2 * I * H * MX4_BPW + 2 * T * H + 2 * P * I,
+        "prefill_down_mx4": U * H * I * MX4_BPW + 2 * P * I + 4 * P * H,
         # VQ experts: index streams (+ bit planes) and row gains of the distinct experts
         "vq_gateup": U * 2 * I * H * VQ_BITS.get(fmt, 12) / 64 + U * 2 * I * 2 + 4 * T * H + 4 * P * I,
         "vq_down": U * H * I * VQ_BITS.get(fmt, 12) / 64 + U * H * 2 + 4 * P * I + 4 * P * H,
@@ -154,6 +157,8 @@ def kernel_flops(name, shape, T):
         "router_logits_tc": 2 * T * E * 3 * H,
         "prefill_gateup_q2": 2 * P * 2 * I * H,
         "prefill_down_q2": 2 * P * H * I,
+        "prefill_gateup_mx4": 2 * P * 2 * I * H,
+        "prefill_down_mx4": 2 * P * H * I,
         "prefill_gateup_q8": 2 * T * 2 * Ish * H,
         "prefill_down_q8": 2 * T * H * Ish,
     }
@@ -314,8 +319,7 @@ def cpu_oracle_rate(name, layers, batches, budget_tokens=None, min_seconds=0.0):
     passes = 0
     while True:
         for layer in layers:
-            oracle.forward(wl.shape, layer, np.ascontiguousarray(flat),
-                           act="q8" if layer.get("routed_format") == "mx4" else None)
+            oracle.forward(wl.shape, layer, np.ascontiguousarray(flat), act=mx4_act(layer, wl.tokens))
         passes += 1
         dt = time.perf_counter() - t0
         if dt >= min_seconds:
@@ -323,6 +327,16 @@ def cpu_oracle_rate(name, layers, batches, budget_tokens=None, min_seconds=0.0):
     if passes > 1:
         sample += f", {passes} passes"
     return passes * len(flat) / dt, cores, sample, dt
+
+
+def mx4_act(layer, T):
+    """The activation arithmetic of an MXFP4 layer's expert products at T tokens
+    (the library's automatic form: Q8 for decode, FP4 for prefill); None for
+    other layers."""
+    if layer.get("routed_format") != "mx4":
+        return None
+    import quantized_moe_expert_gb300 as ds4
+    return "mx4" if T >= ds4.AUTO_MX4_PREFILL_MIN_T else "q8"
 
 
 def dist_setup(args):
@@ -385,7 +399,8 @@ def workload_config(wl, name, l2_note, gains=0, fmt="q2"):
     cfg = {"workload": name, "description": wl.description, "hidden": s.hidden, "inter": s.inter,
            "n_experts": s.n_experts, "top_k": s.top_k, "shared_inter": s.shared_inter,
            "tokens_per_step": wl.tokens, "layers_per_step": wl.n_layers,
-           "weights": {"mx4": "routed MXFP4 17B/32 blocks on Q8 activations",
+           "weights": {"mx4": "routed MXFP4 17B/32 blocks on " + (
+                           "FP4 activations (tensor cores)" if wl.tokens >= 64 else "Q8 activations"),
                        "vq12": "routed VQ, 12-bit indices per 8 weights into a 4096 x 8 E4M3 codebook, f16 row gains",
                        "vq13": "routed VQ, 13-bit indices per 8 weights into an 8192 x 8 E4M3 codebook, f16 row gains"
                        }.get(fmt, "routed 2-bit 84B/256 blocks") + ", shared 8-bit 34B/32 blocks, router fp32"}

@@ -98,10 +98,16 @@ enum {
  *   gate, up [E][I][H/32] blocks; down [E][H][I/32] blocks (router, shared
  *   expert and down gains unchanged).
  * Each routed-expert product quantises its input per 32 values first (x, and
- * the SwiGLU rows before the down product): d = amax / 127, q = x / d rounded
- * to the nearest integer (ties to even), both in binary32; the product uses
- * d * q. Such a layer runs one path for every T (the path argument and
- * DS4MOE_AUTO_DECODE_MAX_T do not apply).
+ * the SwiGLU rows, rounded to binary32, before the down product). Decode form:
+ * d = amax / 127, q = x / d rounded to the nearest integer (ties to even), both
+ * in binary32; the product uses d * q. Prefill form ("Blackwell CUDA devices use
+ * native FP4 matrix instructions and FP4 activations for batched expert work"):
+ * the OCP MX conversion, X = 2^(floor(log2 amax) - 2) and the E2M1 value nearest
+ * to x / X (ties to even, saturating at 6); the product uses X * e2m1. The
+ * prefill form runs on the tensor cores with both operands in binary16, exact
+ * for weight scale bytes 104..141 and activation blocks with amax in
+ * [2^-21, 2^16). The path argument picks the form (see
+ * DS4MOE_AUTO_MX4_PREFILL_MIN_T); DS4MOE_AUTO_DECODE_MAX_T does not apply.
  */
 #define DS4MOE_FLAG_MXFP4 1u
 
@@ -130,6 +136,15 @@ enum {
  */
 #define DS4MOE_AUTO_DECODE_MAX_T 1
 #define DS4MOE_AUTO_BATCH_MAX_T 64
+
+/*
+ * Layers with MXFP4 routed experts (DS4MOE_FLAG_MXFP4) have two forms: decode
+ * (Q8 activations, CUDA-core integer products; DS4MOE_PATH_DECODE and _BATCH)
+ * and prefill (FP4 activations, grouped GEMMs on the tensor cores;
+ * DS4MOE_PATH_PREFILL). DS4MOE_PATH_AUTO takes the prefill form from this many
+ * tokens on.
+ */
+#define DS4MOE_AUTO_MX4_PREFILL_MIN_T 64
 
 /* Most tokens one call of the batch path takes. */
 #define DS4MOE_BATCH_MAX_T 64

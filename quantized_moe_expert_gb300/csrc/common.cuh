@@ -163,6 +163,7 @@ struct Scratch {
     uint16_t *xstage;  // [Tmax][H] bf16 staging for host-memory calls
     float *ystage;     // [Tmax][H]
     float *ax;         // VQ layers: [Tmax][H] x in fp32
+    uint16_t *x4;      // MXFP4 layers: [Tmax][H] the token rows on the FP4 grid, as binary16
     int8_t *xq;        // MXFP4 layers: [Tmax][H] Q8 codes of the token rows
     float *xd;         // MXFP4 layers: [Tmax][H/32] their block scales
     float *hf;         // MXFP4 and VQ layers: [Tmax*K][I] fp32 SwiGLU rows, expert-grouped order
@@ -177,6 +178,17 @@ struct Mx4Mat {
     const uint8_t *scale; // [rows][nb]
     int64_t rows;
     int32_t nb; // 32-weight blocks per row
+};
+
+// MXFP4 weights in the prefill GEMM's tile order: one kMx4TileRec-byte record
+// per (128-row tile, 64-column step): the 16 code bytes of each row's two
+// 32-weight blocks ([block][row][16 B]), then the rows' two E8M0 bytes
+// ([row][block]). A loader moves one step of a tile with one bulk copy.
+constexpr int kMx4TileRec = 2 * 128 * 16 + 128 * 2;
+struct Mx4Tile {
+    const uint8_t *rec; // [rows / 128][nks] records
+    int64_t rows;
+    int32_t nks; // K / 64
 };
 
 // VQ weights of one matrix: per expert the index stream, the bit plane
@@ -199,6 +211,7 @@ struct LayerDev {
     const float *gain; // [E][H] per-expert down gains s1 * s2 expanded from the tables, or nullptr
     bool mx4;          // routed experts in MXFP4 (mgate, mup, mdown) instead of 2-bit
     Mx4Mat mgate, mup, mdown;
+    Mx4Tile tgate, tup, tdown; // the same weights in the prefill GEMM's tile order
     int vq;            // 12 or 13: routed experts vector-quantised (vgate, vup, vdown, codebook); 0: not
     VqMat vgate, vup, vdown;
     const uint8_t *codebook; // [2^vq][8] E4M3

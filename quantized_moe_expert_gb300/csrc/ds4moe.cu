@@ -328,6 +328,14 @@ void layout_weights(ds4moe *h, Carver &c) {
         m4(L.mgate, (int64_t)L.E * L.I, L.H);
         m4(L.mup, (int64_t)L.E * L.I, L.H);
         m4(L.mdown, (int64_t)L.E * L.H, L.I);
+        auto t4 = [&](Mx4Tile &m, int64_t rows, int k) {
+            m.rows = rows;
+            m.nks = k / 64;
+            m.rec = c.take<uint8_t>((uint64_t)(rows / 128) * m.nks * kMx4TileRec);
+        };
+        t4(L.tgate, (int64_t)L.E * L.I, L.H);
+        t4(L.tup, (int64_t)L.E * L.I, L.H);
+        t4(L.tdown, (int64_t)L.E * L.H, L.I);
     } else {
         q2(L.gate, (int64_t)L.E * L.I, L.H);
         q2(L.up, (int64_t)L.E * L.I, L.H);
@@ -395,6 +403,7 @@ void layout_scratch(ds4moe *h, Carver &c) {
     S.ystage = c.take<float>(T * L.H);
     S.ax = L.vq ? c.take<float>(T * L.H) : nullptr;
     S.xq = L.mx4 ? c.take<int8_t>(T * L.H) : nullptr;
+    S.x4 = L.mx4 ? c.take<uint16_t>(T * L.H) : nullptr;
     S.xd = L.mx4 ? c.take<float>(T * (L.H / 32)) : nullptr;
     S.hf = L.mx4 || L.vq ? c.take<float>(P * L.I) : nullptr;
     S.hq = L.mx4 ? c.take<int8_t>(P * L.I) : nullptr;
@@ -807,6 +816,61 @@ int run_experts_mx4(ds4moe *h, const void *x, int T, float *y) {
     return launch_rc();
 }
 
+// MXFP4 routed experts on the tensor cores (the prefill form) for the routing
+// already in S.idx / S.w: the grouping and the tile groups, x on the FP4 grid
+// (binary16) gathered into expert-grouped order, the grouped GEMMs on the MXFP4
+// tile records (weights expanded exactly to binary16 in TMEM; the gate/up
+// epilogue puts the SwiGLU rows on the FP4 grid), the shared expert, the combine.
+int run_experts_mx4_tc(ds4moe *h, const void *x, int T, float *y) {
+    const LayerDev &L = h->L;
+    Scratch &S = h->S;
+    cudaStream_t st = h->stream;
+    int rc = run_dispatch(h, T);
+    if (rc)
+        return rc;
+    launch(h, "plan_groups", [&] {
+        pf::plan_groups_kernel<<<1, 1024, 0, st>>>(S.uexp, S.uoff, S.nuniq, pf::Cfg<pf::kFmtMx4, 2>::kNMax, S.grp_gu,
+                                                     S.ngrp, pf::Cfg<pf::kFmtMx4, 1>::kNMax, S.grp_dn, S.ngrp + 1);
+    });
+    launch(h, "mx4_act_fp4", [&] {
+        act_fp4_kernel<<<blocks_for((int64_t)T * L.H, 256), 256, 0, st>>>(static_cast<const uint16_t *>(x),
+                                                                          (int64_t)T * L.H, S.x4);
+    });
+    launch(h, "gather_rows", [&] {
+        pf::gather_rows_kernel<<<T * L.K, 256, 0, st>>>(S.x4, S.perm, L.K, L.H, S.xp);
+    });
+    pf::Args a{};
+    a.status = h->status;
+    a.mx4[0] = L.tgate;
+    a.mx4[1] = L.tup;
+    a.M = L.I;
+    a.Kd = L.H;
+    a.groups = S.grp_gu;
+    a.ngroups = S.ngrp;
+    a.dense_n = 0;
+    a.out = S.h;
+    a.ldo = L.I;
+    launch_gemm<pf::kFmtMx4, 2, pf::kEpiSwiGLUFp4>(h, "prefill_gateup_mx4", h->map_xp, a);
+    a.mx4[0] = L.tdown;
+    a.M = L.H;
+    a.Kd = L.I;
+    a.groups = S.grp_dn;
+    a.ngroups = S.ngrp + 1;
+    a.out = S.ye;
+    a.ldo = L.H;
+    launch_gemm<pf::kFmtMx4, 1, pf::kEpiF32>(h, "prefill_down_mx4", h->map_h, a);
+    if (L.Ish > 0) {
+        rc = run_shared_gemms(h, x, T);
+        if (rc)
+            return rc;
+    }
+    launch(h, "combine", [&] {
+        combine_kernel<<<blocks_for((int64_t)T * L.H / 4, 256), 256, 0, st>>>(
+            S.ye, L.Ish > 0 ? S.ysh : nullptr, S.w, S.inv, S.idx, L.gain, T, L.H, L.K, y);
+    });
+    return launch_rc();
+}
+
 // VQ routed experts for the routing already in S.idx / S.w, every T: x in fp32,
 // the gate/up product with SwiGLU, the down product, the shared expert, the
 // combine. The product kernels are persistent (two CTAs per SM) and load the
@@ -945,6 +1009,11 @@ int check_call(ds4moe *h, const void *x, int T) {
 // batch path cannot take the call (more than B.tmax tokens, or no batch path
 // for this layer). MXFP4 and VQ layers run one pipeline whatever the path.
 int resolve_path(const ds4moe *h, int T, int path) {
+    if (h->L.mx4) { // two forms: decode (Q8 activations, CUDA cores), prefill (FP4 activations, tensor cores)
+        if (path == DS4MOE_PATH_AUTO)
+            return T >= DS4MOE_AUTO_MX4_PREFILL_MIN_T ? DS4MOE_PATH_PREFILL : DS4MOE_PATH_DECODE;
+        return path == DS4MOE_PATH_PREFILL ? DS4MOE_PATH_PREFILL : DS4MOE_PATH_DECODE;
+    }
     if (path == DS4MOE_PATH_AUTO) {
         if (T <= DS4MOE_AUTO_DECODE_MAX_T)
             return DS4MOE_PATH_DECODE;
@@ -959,9 +1028,13 @@ int forward_impl(ds4moe *h, const void *x, int T, int path, float *y) {
     h->stats = ds4moe_stats{};
     h->stats.tokens = T;
     h->stats.path = path;
-    if (h->L.mx4 || h->L.vq) { // one path for every T
+    if (h->L.mx4 || h->L.vq) {
         int rc = run_router(h, x, T, nullptr);
-        return rc ? rc : h->L.vq ? run_experts_vq(h, x, T, y) : run_experts_mx4(h, x, T, y);
+        if (rc)
+            return rc;
+        if (h->L.vq) // one path for every T
+            return run_experts_vq(h, x, T, y);
+        return path == DS4MOE_PATH_PREFILL ? run_experts_mx4_tc(h, x, T, y) : run_experts_mx4(h, x, T, y);
     }
     if (path == DS4MOE_PATH_DECODE)
         return run_decode(h, x, T, y, nullptr, nullptr);
@@ -1129,6 +1202,11 @@ int ds4moe_create(const ds4moe_layer_desc *desc, const ds4moe_weights *w, ds4moe
         cudaMemcpyAsync(const_cast<uint16_t *>(m.gain), rowgain, (uint64_t)L.E * m.rows * 2, cudaMemcpyDeviceToDevice,
                         st);
     };
+    auto rm4t = [&](const void *src, Mx4Tile &m) {
+        const int nb = m.nks * 2;
+        repack_mx4_tile_kernel<<<blocks_for(m.rows * nb, 256), 256, 0, st>>>(static_cast<const uint8_t *>(src),
+                                                                           m.rows, nb, const_cast<uint8_t *>(m.rec));
+    };
     if (L.vq) {
         cvq(w->gate, w->gate_plane, w->gate_rowgain, L.vgate);
         cvq(w->up, w->up_plane, w->up_rowgain, L.vup);
@@ -1139,6 +1217,9 @@ int ds4moe_create(const ds4moe_layer_desc *desc, const ds4moe_weights *w, ds4moe
         rm4(w->gate, L.mgate);
         rm4(w->up, L.mup);
         rm4(w->down, L.mdown);
+        rm4t(w->gate, L.tgate);
+        rm4t(w->up, L.tup);
+        rm4t(w->down, L.tdown);
     } else {
         rq2(w->gate, L.gate);
         rq2(w->up, L.up);
@@ -1242,6 +1323,10 @@ int ds4moe_create(const ds4moe_layer_desc *desc, const ds4moe_weights *w, ds4moe
         rc = setup_gemm<pf::kFmtQ8, 1, pf::kEpiF32>();
     if (!rc)
         rc = setup_gemm<pf::kFmtBF16, 1, pf::kEpiF32>();
+    if (!rc)
+        rc = setup_gemm<pf::kFmtMx4, 2, pf::kEpiSwiGLUFp4>();
+    if (!rc)
+        rc = setup_gemm<pf::kFmtMx4, 1, pf::kEpiF32>();
     if (rc || D.grid <= 0) {
         ds4moe_destroy(h);
         return DS4MOE_ECUDA;
@@ -1355,7 +1440,7 @@ int ds4moe_forward_routed(ds4moe_t *h, const void *x, int32_t T, const int32_t *
     if (L.vq)
         return run_experts_vq(h, x, T, y);
     if (L.mx4)
-        return run_experts_mx4(h, x, T, y);
+        return path == DS4MOE_PATH_PREFILL ? run_experts_mx4_tc(h, x, T, y) : run_experts_mx4(h, x, T, y);
     return path == DS4MOE_PATH_BATCH ? run_experts_batch(h, x, T, y, false) : run_experts_prefill(h, x, T, y);
 }
 

@@ -47,6 +47,67 @@ __global__ void repack_mx4_kernel(const uint8_t *__restrict__ src, int64_t nbloc
     scale[i] = b[16];
 }
 
+// Canonical 17-byte blocks [rows][K/32] -> the prefill GEMM's tile records
+// (Mx4Tile). One thread per (row, 32-weight block).
+__global__ void repack_mx4_tile_kernel(const uint8_t *__restrict__ src, int64_t rows, int nb,
+                                       uint8_t *__restrict__ rec) {
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= rows * nb)
+        return;
+    const int64_t row = i / nb;
+    const int kb = (int)(i % nb);
+    const int64_t rt = row >> 7;
+    const int r = (int)(row & 127), ks = kb >> 1, half = kb & 1;
+    const uint8_t *b = src + i * kMx4Bytes;
+    uint8_t *dst = rec + (rt * (nb / 2) + ks) * kMx4TileRec;
+    uint32_t w[4];
+#pragma unroll
+    for (int k = 0; k < 4; k++)
+        w[k] = (uint32_t)b[4 * k] | (uint32_t)b[4 * k + 1] << 8 | (uint32_t)b[4 * k + 2] << 16 |
+               (uint32_t)b[4 * k + 3] << 24;
+    reinterpret_cast<uint4 *>(dst)[half * 128 + r] = make_uint4(w[0], w[1], w[2], w[3]);
+    dst[2 * 128 * 16 + 2 * r + half] = b[16];
+}
+
+// The OCP MX conversion of one value v of a 32-value block whose largest
+// magnitude is amax: X = 2^(floor(log2 amax) - 2), clamped to the E8M0 range
+// (amax = 0 or subnormal: 2^-127), and the E2M1 value nearest to v / X (ties to
+// the even code, magnitude saturating at 6, sign kept: -0 for small negatives).
+// Returns X * e2m1 as binary16 bits: exact while X lies in [2^-23, 2^13] (every
+// block whose amax is in [2^-21, 2^16)); beyond that the binary16 value
+// underflows or overflows.
+__device__ __forceinline__ uint16_t fp4_grid_f16(float v, float amax) {
+    const int ef = (int)(__float_as_uint(amax) >> 23); // biased exponent of amax >= 0
+    const int sb = ef == 0 ? 0 : min(254, max(0, ef - 2));
+    const float inv = sb == 254 ? __uint_as_float(0x00400000u) : __uint_as_float((uint32_t)(254 - sb) << 23);
+    const float X = sb == 0 ? __uint_as_float(0x00400000u) : __uint_as_float((uint32_t)sb << 23);
+    const float r = fabsf(v) * inv; // exact: a power of two (r < 8)
+    const float m = r <= 0.25f  ? 0.f
+                    : r < 0.75f ? 0.5f
+                    : r <= 1.25f ? 1.f
+                    : r < 1.75f ? 1.5f
+                    : r <= 2.5f ? 2.f
+                    : r < 3.5f  ? 3.f
+                    : r <= 5.f  ? 4.f
+                                : 6.f;
+    return __half_as_ushort(__float2half_rn(copysignf(m * X, v)));
+}
+
+// FP4 activation rows for the MXFP4 prefill: bf16 x [n] -> binary16 values on
+// the FP4 grid (fp4_grid_f16 per 32-value block). One thread per value, a warp
+// per block (n is a multiple of 32).
+__global__ void act_fp4_kernel(const uint16_t *__restrict__ x, int64_t n, uint16_t *__restrict__ out) {
+    pdl_launch_next();
+    pdl_wait();
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i - (threadIdx.x & 31) >= n) // whole warps past the end
+        return;
+    const float v = i < n ? bf16_to_f32(x[i]) : 0.f;
+    const float amax = __uint_as_float(__reduce_max_sync(0xFFFFFFFFu, __float_as_uint(fabsf(v))));
+    if (i < n)
+        out[i] = fp4_grid_f16(v, amax);
+}
+
 // Q8 activation blocks: per 32 values d = amax / 127 and q_i = x_i / d
 // rounded to the nearest integer (ties to even), both IEEE binary32 (the build
 // has no fast-math flags). One thread per value, a warp per block (n is a

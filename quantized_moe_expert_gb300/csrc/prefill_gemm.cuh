@@ -58,6 +58,7 @@
 #include <cuda.h>
 
 #include "common.cuh"
+#include "mx4_experts.cuh"
 #include "umma.cuh"
 
 namespace ds4 {
@@ -69,8 +70,11 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kWaitNs = 1000000000ull; // 1 s: far beyond any legitimate wait
 constexpr int kBoxes = 4;                   // B box heights 16, 32, 64, 128 rows
 
-enum { kFmtQ2 = 0, kFmtQ8 = 1, kFmtBF16 = 2 };
-enum { kEpiSwiGLU = 0, kEpiF32 = 1 };
+enum { kFmtQ2 = 0, kFmtQ8 = 1, kFmtBF16 = 2, kFmtMx4 = 3 };
+// Epilogues: SwiGLU -> bf16 rows; fp32 rows; SwiGLU -> binary16 rows on the FP4
+// grid (each 32-row block of a token column is one MX block: the epilogue
+// warp's 32 lanes).
+enum { kEpiSwiGLU = 0, kEpiF32 = 1, kEpiSwiGLUFp4 = 2 };
 
 // Tensor maps of one B matrix (bf16 rows, 128-byte swizzle, box 64 columns x
 // 16 << i rows); passed by value as a grid constant.
@@ -83,6 +87,7 @@ struct Args {
     Q2Mat q2[2];
     Q8Mat q8[2];
     BfMat bf[1];
+    Mx4Tile mx4[2];
     int M;                 // rows of one expert's matrix (output features)
     int Kd;                // reduction length
     const int4 *groups;    // routed groups (ignored when dense_n > 0)
@@ -113,7 +118,10 @@ template <int FMT, int NA> struct Cfg {
     static constexpr int kStages = NA == 2 ? 4 : 8;        // A (TMEM) and B (smem) ring depth
     static constexpr int kACols = NA * kTileK / 2;         // TMEM columns of one A stage
     static constexpr int kSPB = FMT == kFmtQ2 ? 4 : 1;     // K steps per raw block
-    static constexpr int kRawMat = FMT == kFmtQ2 ? 8192 + 2048 + 512 : (FMT == kFmtQ8 ? 8192 + 512 : 16384);
+    static constexpr int kRawMat = FMT == kFmtQ2   ? 8192 + 2048 + 512
+                                   : FMT == kFmtQ8 ? 8192 + 512
+                                   : FMT == kFmtMx4 ? kMx4TileRec
+                                                    : 16384;
     static constexpr int kRaw = 4;                         // raw ring depth (blocks)
     static constexpr int kBBytes = kNMax * kTileK * 2;     // one B stage
     static constexpr int kRawOffset = kStages * kBBytes;
@@ -285,6 +293,11 @@ template <int P> struct RawBF { // one 64-column K step: P bf16 of the row
     uint4 c[P / 8];
 };
 
+template <int P> struct RawMx4 { // one 64-column K step: P of the row's weights (P / 32 MX blocks)
+    uint4 c[P / 32];
+    uint32_t sc[P / 32]; // their E8M0 bytes
+};
+
 // part: first 16-column quarter of the step owned (P = 64: 0, P = 32: 2 * half).
 template <int P> __device__ __forceinline__ void read_raw(uint32_t slot, int r, int part, RawQ2<P> &x) {
 #pragma unroll
@@ -323,6 +336,16 @@ template <int P> __device__ __forceinline__ void read_raw(uint32_t slot, int r, 
 #pragma unroll
     for (int i = 0; i < P / 8; i++)
         x.c[i] = lds128(slot + ((2 * part + i) * 128 + r) * 16);
+}
+
+template <int P> __device__ __forceinline__ void read_raw(uint32_t slot, int r, int part, RawMx4<P> &x) {
+    const uint32_t sw = lds32(slot + 2 * 128 * 16 + (r & ~1) * 2) >> (16 * (r & 1)); // the row's two scale bytes
+#pragma unroll
+    for (int i = 0; i < P / 32; i++) {
+        const int half = part / 2 + i;
+        x.c[i] = lds128(slot + (half * 128 + r) * 16);
+        x.sc[i] = (sw >> (8 * half)) & 0xFFu;
+    }
 }
 
 // Expand one sub-block word (16 weights, pair p of codes at bits 2p and
@@ -395,6 +418,39 @@ template <int P> __device__ __forceinline__ void expand_step(const RawBF<P> &r, 
     }
 }
 
+// MXFP4 block -> binary16 pairs X * e2m1: the hardware E2M1-pair conversion
+// (byte j = weights 2j, 2j+1, the even one in the low nibble and the low half)
+// and one packed multiply by X (exact while X * 6 and X / 2 are normal or
+// subnormal binary16 values: scale bytes 104..141).
+__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte) {
+    uint32_t r;
+    asm("{ .reg .b8 t;\n\t"
+        "cvt.u8.u32 t, %1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %0, t; }"
+        : "=r"(r)
+        : "r"(byte));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t hmul2_f16(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
+template <int P> __device__ __forceinline__ void expand_step(const RawMx4<P> &r, int /*s*/, uint32_t (&o)[P / 2]) {
+#pragma unroll
+    for (int i = 0; i < P / 32; i++) {
+        const float X = r.sc[i] == 0 ? __uint_as_float(0x00400000u) : __uint_as_float(r.sc[i] << 23);
+        const uint32_t xh = __half_as_ushort(__float2half_rn(X));
+        const uint32_t X2 = xh | xh << 16;
+        const uint32_t w[4] = {r.c[i].x, r.c[i].y, r.c[i].z, r.c[i].w};
+#pragma unroll
+        for (int j = 0; j < 16; j++)
+            o[16 * i + j] = hmul2_f16(e2m1x2_to_f16x2(w[j >> 2] >> (8 * (j & 3))), X2);
+    }
+}
+
 template <int FMT> struct FmtTraits;
 template <> struct FmtTraits<kFmtQ2> {
     template <int P> using Raw = RawQ2<P>;
@@ -404,6 +460,9 @@ template <> struct FmtTraits<kFmtQ8> {
 };
 template <> struct FmtTraits<kFmtBF16> {
     template <int P> using Raw = RawBF<P>;
+};
+template <> struct FmtTraits<kFmtMx4> {
+    template <int P> using Raw = RawMx4<P>;
 };
 
 // The loader's bulk copies of raw block kb of 128-row tile rt of matrix m
@@ -423,6 +482,11 @@ __device__ __forceinline__ unsigned copy_raw(const Q8Mat &m, int64_t rt, int ks,
     return 8192 + 512;
 }
 
+__device__ __forceinline__ unsigned copy_raw(const Mx4Tile &m, int64_t rt, int ks, uint32_t dst, uint64_t *bar) {
+    bulk_g2s(dst, m.rec + (rt * m.nks + ks) * kMx4TileRec, kMx4TileRec, bar);
+    return kMx4TileRec;
+}
+
 __device__ __forceinline__ unsigned copy_raw(const BfMat &m, int64_t rt, int ks, uint32_t dst, uint64_t *bar) {
     bulk_g2s(dst, m.p + (rt * m.nks + ks) * 1024, 16384, bar);
     return 16384;
@@ -437,6 +501,9 @@ template <> struct MatOf<kFmtQ8> {
 };
 template <> struct MatOf<kFmtBF16> {
     __device__ static const BfMat &get(const Args &a, int i) { return a.bf[0]; }
+};
+template <> struct MatOf<kFmtMx4> {
+    __device__ static const Mx4Tile &get(const Args &a, int i) { return a.mx4[i]; }
 };
 
 // ---- tiles ------------------------------------------------------------------------
@@ -670,7 +737,9 @@ __global__ void __launch_bounds__(Cfg<FMT, NA>::kThreads, 1)
                 if (wide && !mbar_wait(acce + 1, ((use >> 1) & 1u) ^ 1u, abort, a.status))
                     break;
                 umma::fence_after_sync();
-                const uint32_t idesc = umma::idesc_bf16_f32(kTileM, n_mma);
+                // MXFP4: both operands binary16 (the expanded weights and the FP4-grid activations)
+                const uint32_t idesc =
+                    FMT == kFmtMx4 ? umma::idesc_f16_f32(kTileM, n_mma) : umma::idesc_bf16_f32(kTileM, n_mma);
                 const uint32_t dacc = tmem + pl.col + iss * pl.stride;
                 const uint32_t a_off = NA == 2 ? iss * (kTileK / 2) : 0;
                 for (int ks = 0; ks < nk; ks++) {
@@ -751,7 +820,19 @@ __global__ void __launch_bounds__(Cfg<FMT, NA>::kThreads, 1)
                     for (int jj = 0; jj < 8; jj++)
                         v[0][jj] += v[1][jj];
                 }
-                if (mrow >= a.M) {
+                if (EPI == kEpiSwiGLUFp4) {
+                    // one MX block per token column: this warp's 32 rows (M is a multiple of 128)
+                    uint16_t *out = static_cast<uint16_t *>(a.out);
+#pragma unroll
+                    for (int jj = 0; jj < 8; jj++) {
+                        const float h = silu(v[0][jj]) * v[1][jj];
+                        const float amax =
+                            __uint_as_float(__reduce_max_sync(0xFFFFFFFFu, __float_as_uint(fabsf(h))));
+                        const uint16_t q = fp4_grid_f16(h, amax);
+                        if (c0 + jj < g.z)
+                            out[(int64_t)(g.y + c0 + jj) * a.ldo + mrow] = q;
+                    }
+                } else if (mrow >= a.M) {
                     // rows past a partial last m-tile
                 } else if (EPI == kEpiSwiGLU) {
                     uint16_t *out = static_cast<uint16_t *>(a.out);
