@@ -400,7 +400,8 @@ def workload_config(wl, name, l2_note, gains=0, fmt="q2"):
            "n_experts": s.n_experts, "top_k": s.top_k, "shared_inter": s.shared_inter,
            "tokens_per_step": wl.tokens, "layers_per_step": wl.n_layers,
            "weights": {"mx4": "routed MXFP4 17B/32 blocks on " + (
-                           "FP4 activations (tensor cores)" if wl.tokens >= 64 else "Q8 activations"),
+                           "FP4 activations (tensor cores)" if mx4_act({"routed_format": "mx4"}, wl.tokens) == "mx4"
+                           else "Q8 activations"),
                        "vq12": "routed VQ, 12-bit indices per 8 weights into a 4096 x 8 E4M3 codebook, f16 row gains",
                        "vq13": "routed VQ, 13-bit indices per 8 weights into an 8192 x 8 E4M3 codebook, f16 row gains"
                        }.get(fmt, "routed 2-bit 84B/256 blocks") + ", shared 8-bit 34B/32 blocks, router fp32"}
@@ -427,27 +428,25 @@ def run_crossover(args):
 
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
-    wl, layers = workload_layers("decode_t1", args.gains)
+    fmt = args.routed_format
+    wl, layers = workload_layers("decode_t1", args.gains, fmt)
     shape = wl.shape
-    w = {k: (None if v is None else torch.from_numpy(np.ascontiguousarray(v)).to(dev)) for k, v in layers[0].items()}
-    moe = ds4.MoELayer(shape, w, max_tokens=max(CROSSOVER_T))
-    del w
-    torch.cuda.empty_cache()
     stream = torch.cuda.current_stream(dev)
-    moe.set_stream(stream)
+    T_list = CROSSOVER_T if fmt == "q2" else CROSSOVER_T + (128, 256)
+    moe = make_handles(layers[:1], shape, dev, max(T_list), fmt, stream)[0]
     flush = torch.empty(2 * torch.cuda.get_device_properties(dev).L2_cache_size, dtype=torch.uint8, device=dev)
     gpu_id = getattr(torch.cuda.get_device_properties(dev), "uuid", None)
     gpu_id = ("GPU-" + str(gpu_id)) if gpu_id is not None and not str(gpu_id).startswith("GPU-") else gpu_id
     rows = {}
     with ClockSampler(gpu_id) as clk:
-        for T in CROSSOVER_T:
+        for T in T_list:
             xb = synth.normal_bf16(T * shape.hidden, synth.SEED_BASE + 0x100 + T, synth.S_X)
             x = torch.from_numpy(xb.reshape(T, shape.hidden).view(np.int16)).to(dev)
             y = torch.empty((T, shape.hidden), dtype=torch.float32, device=dev)
             idx, _, _, _ = moe.route(x)
             row = {"unique_experts": int(torch.unique(idx).numel())}
             paths = [("decode_us", ds4.PATH_DECODE), ("prefill_us", ds4.PATH_PREFILL)]
-            if T <= ds4.BATCH_MAX_T:
+            if T <= ds4.BATCH_MAX_T and fmt == "q2":
                 paths.append(("batch_us", ds4.PATH_BATCH))
             for name, path in paths:
                 ts = []
@@ -467,8 +466,8 @@ def run_crossover(args):
     if moe.status() != 0:
         raise RuntimeError("device error during the crossover sweep")
     moe.close()
-    print(json.dumps({"crossover": rows, "auto_decode_max_t": ds4.AUTO_DECODE_MAX_T,
-                      "auto_batch_max_t": ds4.AUTO_BATCH_MAX_T,
+    print(json.dumps({"crossover": rows, "routed_format": fmt, "auto_decode_max_t": ds4.AUTO_DECODE_MAX_T,
+                      "auto_batch_max_t": ds4.AUTO_BATCH_MAX_T, "auto_mx4_prefill_min_t": ds4.AUTO_MX4_PREFILL_MIN_T,
                       "config": workload_config(wl, "decode_t1", "flushed before every call", args.gains),
                       "clocks": clk.summary()}))
 

@@ -142,9 +142,12 @@ enum {
  * (Q8 activations, CUDA-core integer products; DS4MOE_PATH_DECODE and _BATCH)
  * and prefill (FP4 activations, grouped GEMMs on the tensor cores;
  * DS4MOE_PATH_PREFILL). DS4MOE_PATH_AUTO takes the prefill form from this many
- * tokens on.
+ * tokens on: the measured crossover on a GB300 at H=4096, I=2048, E=384, top-6
+ * (the pages pair Q8 activations with decode and FP4 activations with batched
+ * expert work; the boundary between the two sits where the tensor-core form
+ * becomes the faster one).
  */
-#define DS4MOE_AUTO_MX4_PREFILL_MIN_T 64
+#define DS4MOE_AUTO_MX4_PREFILL_MIN_T 6
 
 /* Most tokens one call of the batch path takes. */
 #define DS4MOE_BATCH_MAX_T 64

@@ -117,10 +117,11 @@ template <int FMT, int NA> struct Cfg {
     static constexpr int kPartsPerMat = 64 / kPart;
     static constexpr int kStages = NA == 2 ? 4 : 8;        // A (TMEM) and B (smem) ring depth
     static constexpr int kACols = NA * kTileK / 2;         // TMEM columns of one A stage
-    static constexpr int kSPB = FMT == kFmtQ2 ? 4 : 1;     // K steps per raw block
+    // K steps per raw block: a loader that issues a raw block every K step would bound the kernel
+    static constexpr int kSPB = FMT == kFmtQ2 || FMT == kFmtMx4 ? 4 : FMT == kFmtQ8 ? 2 : 1;
     static constexpr int kRawMat = FMT == kFmtQ2   ? 8192 + 2048 + 512
-                                   : FMT == kFmtQ8 ? 8192 + 512
-                                   : FMT == kFmtMx4 ? kMx4TileRec
+                                   : FMT == kFmtQ8 ? 2 * (8192 + 512)
+                                   : FMT == kFmtMx4 ? 4 * kMx4TileRec
                                                     : 16384;
     static constexpr int kRaw = 4;                         // raw ring depth (blocks)
     static constexpr int kBBytes = kNMax * kTileK * 2;     // one B stage
@@ -284,18 +285,18 @@ template <int P> struct RawQ2 { // one 256-weight block, P/16 quarters of 4 sub-
     uint32_t dm;
 };
 
-template <int P> struct RawQ8 { // one 64-column K step, P weights (one or two 32-weight blocks)
-    uint4 c[P / 16];
-    uint32_t d[P > 32 ? 2 : 1];
+template <int P> struct RawQ8 { // two 64-column K steps, per step P weights (one or two 32-weight blocks)
+    uint4 c[2][P / 16];
+    uint32_t d[2][P > 32 ? 2 : 1];
 };
 
 template <int P> struct RawBF { // one 64-column K step: P bf16 of the row
     uint4 c[P / 8];
 };
 
-template <int P> struct RawMx4 { // one 64-column K step: P of the row's weights (P / 32 MX blocks)
-    uint4 c[P / 32];
-    uint32_t sc[P / 32]; // their E8M0 bytes
+template <int P> struct RawMx4 { // four 64-column K steps: per step P of the row's weights (P / 32 MX blocks)
+    uint4 c[4][P / 32];
+    uint32_t sc[4][P / 32]; // their E8M0 bytes
 };
 
 // part: first 16-column quarter of the step owned (P = 64: 0, P = 32: 2 * half).
@@ -319,16 +320,20 @@ template <int P> __device__ __forceinline__ void read_raw(uint32_t slot, int r, 
     x.dm = lds32(slot + 10240 + r * 4);
 }
 
+// 8-bit raw block: the two steps' codes (8192 B each), then their scales (512 B each).
 template <int P> __device__ __forceinline__ void read_raw(uint32_t slot, int r, int part, RawQ8<P> &x) {
 #pragma unroll
-    for (int i = 0; i < P / 16; i++)
-        x.c[i] = lds128(slot + ((part + i) * 128 + r) * 16);
-    const uint32_t d = lds32(slot + 8192 + r * 4);
-    if (P > 32) {
-        x.d[0] = d & 0xFFFFu;
-        x.d[P > 32 ? 1 : 0] = d >> 16;
-    } else {
-        x.d[0] = (d >> (16 * (part / 2))) & 0xFFFFu;
+    for (int s = 0; s < 2; s++) {
+#pragma unroll
+        for (int i = 0; i < P / 16; i++)
+            x.c[s][i] = lds128(slot + s * 8192 + ((part + i) * 128 + r) * 16);
+        const uint32_t d = lds32(slot + 2 * 8192 + s * 512 + r * 4);
+        if (P > 32) {
+            x.d[s][0] = d & 0xFFFFu;
+            x.d[s][P > 32 ? 1 : 0] = d >> 16;
+        } else {
+            x.d[s][0] = (d >> (16 * (part / 2))) & 0xFFFFu;
+        }
     }
 }
 
@@ -339,12 +344,16 @@ template <int P> __device__ __forceinline__ void read_raw(uint32_t slot, int r, 
 }
 
 template <int P> __device__ __forceinline__ void read_raw(uint32_t slot, int r, int part, RawMx4<P> &x) {
-    const uint32_t sw = lds32(slot + 2 * 128 * 16 + (r & ~1) * 2) >> (16 * (r & 1)); // the row's two scale bytes
 #pragma unroll
-    for (int i = 0; i < P / 32; i++) {
-        const int half = part / 2 + i;
-        x.c[i] = lds128(slot + (half * 128 + r) * 16);
-        x.sc[i] = (sw >> (8 * half)) & 0xFFu;
+    for (int s = 0; s < 4; s++) {
+        const uint32_t st = slot + s * kMx4TileRec;
+        const uint32_t sw = lds32(st + 2 * 128 * 16 + (r & ~1) * 2) >> (16 * (r & 1)); // the row's two scale bytes
+#pragma unroll
+        for (int i = 0; i < P / 32; i++) {
+            const int half = part / 2 + i;
+            x.c[s][i] = lds128(st + (half * 128 + r) * 16);
+            x.sc[s][i] = (sw >> (8 * half)) & 0xFFu;
+        }
     }
 }
 
@@ -395,11 +404,11 @@ __device__ __forceinline__ uint32_t q8_pair(uint32_t w, int j, float d) {
     return pack_bf16x2(d * s8_to_f(w >> (16 * j)), d * s8_to_f(w >> (16 * j + 8)));
 }
 
-template <int P> __device__ __forceinline__ void expand_step(const RawQ8<P> &r, int /*s*/, uint32_t (&o)[P / 2]) {
+template <int P> __device__ __forceinline__ void expand_step(const RawQ8<P> &r, int s, uint32_t (&o)[P / 2]) {
 #pragma unroll
     for (int v = 0; v < P / 16; v++) {
-        const float d = f16_to_f32(r.d[P > 32 ? v >> 1 : 0]);
-        const uint32_t w[4] = {r.c[v].x, r.c[v].y, r.c[v].z, r.c[v].w};
+        const float d = f16_to_f32(r.d[s][P > 32 ? v >> 1 : 0]);
+        const uint32_t w[4] = {r.c[s][v].x, r.c[s][v].y, r.c[s][v].z, r.c[s][v].w};
 #pragma unroll
         for (int i = 0; i < 4; i++) {
             o[8 * v + 2 * i] = q8_pair(w[i], 0, d);
@@ -438,13 +447,13 @@ __device__ __forceinline__ uint32_t hmul2_f16(uint32_t a, uint32_t b) {
     return r;
 }
 
-template <int P> __device__ __forceinline__ void expand_step(const RawMx4<P> &r, int /*s*/, uint32_t (&o)[P / 2]) {
+template <int P> __device__ __forceinline__ void expand_step(const RawMx4<P> &r, int s, uint32_t (&o)[P / 2]) {
 #pragma unroll
     for (int i = 0; i < P / 32; i++) {
-        const float X = r.sc[i] == 0 ? __uint_as_float(0x00400000u) : __uint_as_float(r.sc[i] << 23);
+        const float X = r.sc[s][i] == 0 ? __uint_as_float(0x00400000u) : __uint_as_float(r.sc[s][i] << 23);
         const uint32_t xh = __half_as_ushort(__float2half_rn(X));
         const uint32_t X2 = xh | xh << 16;
-        const uint32_t w[4] = {r.c[i].x, r.c[i].y, r.c[i].z, r.c[i].w};
+        const uint32_t w[4] = {r.c[s][i].x, r.c[s][i].y, r.c[s][i].z, r.c[s][i].w};
 #pragma unroll
         for (int j = 0; j < 16; j++)
             o[16 * i + j] = hmul2_f16(e2m1x2_to_f16x2(w[j >> 2] >> (8 * (j & 3))), X2);
@@ -475,16 +484,18 @@ __device__ __forceinline__ unsigned copy_raw(const Q2Mat &m, int64_t rt, int kb,
     return 8192 + 2048 + 512;
 }
 
-__device__ __forceinline__ unsigned copy_raw(const Q8Mat &m, int64_t rt, int ks, uint32_t dst, uint64_t *bar) {
-    const int64_t ts = rt * m.nks + ks;
-    bulk_g2s(dst, m.qs + ts * 512, 8192, bar);
-    bulk_g2s(dst + 8192, m.d + ts * 128, 512, bar);
-    return 8192 + 512;
+// 8-bit: raw block kb is K steps 2 kb and 2 kb + 1 (consecutive in both streams).
+__device__ __forceinline__ unsigned copy_raw(const Q8Mat &m, int64_t rt, int kb, uint32_t dst, uint64_t *bar) {
+    const int64_t ts = rt * m.nks + 2 * kb;
+    bulk_g2s(dst, m.qs + ts * 512, 2 * 8192, bar);
+    bulk_g2s(dst + 2 * 8192, m.d + ts * 128, 2 * 512, bar);
+    return 2 * (8192 + 512);
 }
 
-__device__ __forceinline__ unsigned copy_raw(const Mx4Tile &m, int64_t rt, int ks, uint32_t dst, uint64_t *bar) {
-    bulk_g2s(dst, m.rec + (rt * m.nks + ks) * kMx4TileRec, kMx4TileRec, bar);
-    return kMx4TileRec;
+// MXFP4: raw block kb is K steps 4 kb .. 4 kb + 3, four consecutive records.
+__device__ __forceinline__ unsigned copy_raw(const Mx4Tile &m, int64_t rt, int kb, uint32_t dst, uint64_t *bar) {
+    bulk_g2s(dst, m.rec + (rt * m.nks + 4 * kb) * kMx4TileRec, 4 * kMx4TileRec, bar);
+    return 4 * kMx4TileRec;
 }
 
 __device__ __forceinline__ unsigned copy_raw(const BfMat &m, int64_t rt, int ks, uint32_t dst, uint64_t *bar) {

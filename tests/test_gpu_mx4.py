@@ -113,11 +113,16 @@ def test_forward_routed_and_gains(tiny):
         x = tokens(shape, T, 1301)
         idx = np.stack([rng.choice(shape.n_experts, shape.top_k, replace=False) for _ in range(T)]).astype(np.int32)
         w = rng.random((T, shape.top_k)).astype(np.float32)
-        y = moe.forward_routed(x_to_dev(x), torch.from_numpy(idx).cuda(), torch.from_numpy(w).cuda()).cpu().numpy()
+        y = moe.forward_routed(x_to_dev(x), torch.from_numpy(idx).cuda(), torch.from_numpy(w).cuda(),
+                               path=ds4.PATH_DECODE).cpu().numpy()
         y_ref = oracle.forward_routed(shape, L, x, idx, w.astype(np.float64), act="q8")
         y_plain = oracle.forward_routed(shape, layer, x, idx, w.astype(np.float64), act="q8")
         assert rel_l2(y_plain, y_ref) > 0.1
         assert_close(y, y_ref, TOL_DECODE)
+        # the prefill form applies the same gains in its combine
+        y4 = moe.forward_routed(x_to_dev(x), torch.from_numpy(idx).cuda(), torch.from_numpy(w).cuda(),
+                                path=ds4.PATH_PREFILL).cpu().numpy()
+        assert_close(y4, oracle.forward_routed(shape, L, x, idx, w.astype(np.float64), act="mx4"), TOL_PREFILL)
         assert moe.status() == 0
     finally:
         moe.close()
@@ -131,7 +136,8 @@ def test_q8_activations_are_what_the_layer_uses(tiny):
     x = tokens(shape, T, 1401)
     r = oracle.route(shape, layer["router_w"], None, x)
     w32 = r["weights"].astype(np.float32)
-    y = moe.forward_routed(x_to_dev(x), torch.from_numpy(r["idx"]).cuda(), torch.from_numpy(w32).cuda()).cpu().numpy()
+    y = moe.forward_routed(x_to_dev(x), torch.from_numpy(r["idx"]).cuda(), torch.from_numpy(w32).cuda(),
+                           path=ds4.PATH_DECODE).cpu().numpy()
     yq = oracle.forward_routed(shape, layer, x, r["idx"], w32.astype(np.float64), act="q8")
     ye = oracle.forward_routed(shape, layer, x, r["idx"], w32.astype(np.float64), act="exact")
     assert rel_l2(y, yq) <= TOL_DECODE < rel_l2(y, ye)
