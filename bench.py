@@ -116,6 +116,11 @@ def kernel_bytes(name, shape, T, U, gains=0, fmt="q2"):
         # VQ experts: index streams (+ bit planes) and row gains of the distinct experts
         "vq_gateup": U * 2 * I * H * VQ_BITS.get(fmt, 12) / 64 + U * 2 * I * 2 + 4 * T * H + 4 * P * I,
         "vq_down": U * H * I * VQ_BITS.get(fmt, 12) / 64 + U * H * 2 + 4 * P * I + 4 * P * H,
+        # VQ tensor-core form: index bits (and plane), row gains, codebook, binary16 activation rows
+        "prefill_gateup_vq": U * 2 * I * H * VQ_BITS.get(fmt, 12) / 64 + U * 2 * I * 2 + (8 << VQ_BITS.get(fmt, 12))
+        + 2 * T * H + 2 * P * I,
+        "prefill_down_vq": U * H * I * VQ_BITS.get(fmt, 12) / 64 + U * H * 2 + (8 << VQ_BITS.get(fmt, 12))
+        + 2 * P * I + 4 * P * H,
     }
     return table.get(name)
 
@@ -159,6 +164,8 @@ def kernel_flops(name, shape, T):
         "prefill_down_q2": 2 * P * H * I,
         "prefill_gateup_mx4": 2 * P * 2 * I * H,
         "prefill_down_mx4": 2 * P * H * I,
+        "prefill_gateup_vq": 2 * P * 2 * I * H,
+        "prefill_down_vq": 2 * P * H * I,
         "prefill_gateup_q8": 2 * T * 2 * Ish * H,
         "prefill_down_q8": 2 * T * H * Ish,
     }

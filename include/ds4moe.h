@@ -123,7 +123,8 @@ enum {
  *     per expert for gate and up, H*I*3/16 for down;
  *   *_plane: 13-bit layers, bit k (least significant first) = bit 12 of index k;
  *   *_rowgain: binary16 g_r per row; vq_codebook: entry n at bytes 8n .. 8n+7.
- * Activations are not quantised. Such a layer runs one path for every T.
+ * Activations are not quantised (the tensor-core form rounds x and the SwiGLU
+ * rows to binary16, see DS4MOE_AUTO_VQ_PREFILL_MIN_T).
  */
 #define DS4MOE_FLAG_VQ12 2u
 #define DS4MOE_FLAG_VQ13 4u
@@ -148,6 +149,16 @@ enum {
  * becomes the faster one).
  */
 #define DS4MOE_AUTO_MX4_PREFILL_MIN_T 6
+
+/*
+ * Layers with VQ routed experts (DS4MOE_FLAG_VQ12, _VQ13) have two forms of
+ * the same arithmetic: CUDA-core products (DS4MOE_PATH_DECODE and _BATCH) and
+ * grouped GEMMs on the tensor cores (DS4MOE_PATH_PREFILL: codewords exact in
+ * binary16, x and the SwiGLU rows rounded to binary16). DS4MOE_PATH_AUTO takes
+ * the tensor-core form from this many tokens on: measured on a GB300 at H=4096,
+ * I=2048, E=384, top-6, it is the faster form at every T (174 vs 226 us at T=1).
+ */
+#define DS4MOE_AUTO_VQ_PREFILL_MIN_T 1
 
 /* Most tokens one call of the batch path takes. */
 #define DS4MOE_BATCH_MAX_T 64

@@ -25,6 +25,7 @@ PATH_AUTO, PATH_DECODE, PATH_PREFILL, PATH_BATCH = 0, 1, 2, 3
 AUTO_DECODE_MAX_T = 1
 AUTO_BATCH_MAX_T = 64
 AUTO_MX4_PREFILL_MIN_T = 6
+AUTO_VQ_PREFILL_MIN_T = 1
 BATCH_MAX_T = 64
 FLAG_MXFP4 = 1
 FLAG_VQ12, FLAG_VQ13 = 2, 4

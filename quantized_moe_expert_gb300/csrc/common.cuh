@@ -163,7 +163,7 @@ struct Scratch {
     uint16_t *xstage;  // [Tmax][H] bf16 staging for host-memory calls
     float *ystage;     // [Tmax][H]
     float *ax;         // VQ layers: [Tmax][H] x in fp32
-    uint16_t *x4;      // MXFP4 layers: [Tmax][H] the token rows on the FP4 grid, as binary16
+    uint16_t *x4;      // MXFP4 layers: [Tmax][H] the token rows on the FP4 grid, as binary16; VQ layers: x as binary16
     int8_t *xq;        // MXFP4 layers: [Tmax][H] Q8 codes of the token rows
     float *xd;         // MXFP4 layers: [Tmax][H/32] their block scales
     float *hf;         // MXFP4 and VQ layers: [Tmax*K][I] fp32 SwiGLU rows, expert-grouped order
@@ -201,6 +201,19 @@ struct VqMat {
     int32_t k;              // weights per row
 };
 
+// VQ indices in the prefill GEMM's tile order: one kVqTileRec-byte record per
+// (128-row tile, 256-column block): each row's 32 indices (48 bytes: the index
+// stream's bytes for those columns, 12 bits per index, least significant bit
+// first) as three 16-byte chunks [chunk][row][16 B], then each row's 32 bit-plane
+// bits (13-bit layers) [row][4 B]. Rows run over all experts (expert e's rows at
+// e * rows_per_expert).
+constexpr int kVqTileRec = 3 * 128 * 16 + 128 * 4;
+struct VqTile {
+    const uint8_t *rec; // [E * rows / 128][k / 256] records
+    int64_t rows;       // rows of all experts
+    int32_t nkb;        // k / 256
+};
+
 struct LayerDev {
     int H, I, E, K, Ish, Tmax;
     const float *router_w;
@@ -214,6 +227,7 @@ struct LayerDev {
     Mx4Tile tgate, tup, tdown; // the same weights in the prefill GEMM's tile order
     int vq;            // 12 or 13: routed experts vector-quantised (vgate, vup, vdown, codebook); 0: not
     VqMat vgate, vup, vdown;
+    VqTile tvgate, tvup, tvdown; // the same indices in the prefill GEMM's tile order
     const uint8_t *codebook; // [2^vq][8] E4M3
 };
 

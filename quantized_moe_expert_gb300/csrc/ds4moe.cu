@@ -324,6 +324,14 @@ void layout_weights(ds4moe *h, Carver &c) {
         vqm(L.vup, L.I, L.H);
         vqm(L.vdown, L.H, L.I);
         L.codebook = c.take<uint8_t>((uint64_t)8 << L.vq);
+        auto tv = [&](VqTile &m, int64_t rows, int k) {
+            m.rows = rows;
+            m.nkb = k / 256;
+            m.rec = c.take<uint8_t>((uint64_t)(rows / 128) * m.nkb * kVqTileRec);
+        };
+        tv(L.tvgate, (int64_t)L.E * L.I, L.H);
+        tv(L.tvup, (int64_t)L.E * L.I, L.H);
+        tv(L.tvdown, (int64_t)L.E * L.H, L.I);
     } else if (L.mx4) {
         m4(L.mgate, (int64_t)L.E * L.I, L.H);
         m4(L.mup, (int64_t)L.E * L.I, L.H);
@@ -403,7 +411,7 @@ void layout_scratch(ds4moe *h, Carver &c) {
     S.ystage = c.take<float>(T * L.H);
     S.ax = L.vq ? c.take<float>(T * L.H) : nullptr;
     S.xq = L.mx4 ? c.take<int8_t>(T * L.H) : nullptr;
-    S.x4 = L.mx4 ? c.take<uint16_t>(T * L.H) : nullptr;
+    S.x4 = L.mx4 || L.vq ? c.take<uint16_t>(T * L.H) : nullptr;
     S.xd = L.mx4 ? c.take<float>(T * (L.H / 32)) : nullptr;
     S.hf = L.mx4 || L.vq ? c.take<float>(P * L.I) : nullptr;
     S.hq = L.mx4 ? c.take<int8_t>(P * L.I) : nullptr;
@@ -871,6 +879,66 @@ int run_experts_mx4_tc(ds4moe *h, const void *x, int T, float *y) {
     return launch_rc();
 }
 
+// VQ routed experts on the tensor cores (the prefill form) for the routing
+// already in S.idx / S.w: the grouping and the tile groups, x as binary16
+// gathered into expert-grouped order, the grouped GEMMs on the VQ tile records
+// (codewords from the codebook in shared memory, exact in binary16; row gains
+// in the epilogues; the SwiGLU rows as binary16), the shared expert, the combine.
+int run_experts_vq_tc(ds4moe *h, const void *x, int T, float *y) {
+    const LayerDev &L = h->L;
+    Scratch &S = h->S;
+    cudaStream_t st = h->stream;
+    int rc = run_dispatch(h, T);
+    if (rc)
+        return rc;
+    launch(h, "plan_groups", [&] {
+        pf::plan_groups_kernel<<<1, 1024, 0, st>>>(S.uexp, S.uoff, S.nuniq, pf::Cfg<pf::kFmtVq, 2>::kNMax, S.grp_gu,
+                                                     S.ngrp, pf::Cfg<pf::kFmtVq, 1>::kNMax, S.grp_dn, S.ngrp + 1);
+    });
+    launch(h, "vq_x_f16", [&] {
+        bf16_to_f16_kernel<<<blocks_for((int64_t)T * L.H, 256), 256, 0, st>>>(static_cast<const uint16_t *>(x),
+                                                                              (int64_t)T * L.H, S.x4);
+    });
+    launch(h, "gather_rows", [&] {
+        pf::gather_rows_kernel<<<T * L.K, 256, 0, st>>>(S.x4, S.perm, L.K, L.H, S.xp);
+    });
+    pf::Args a{};
+    a.status = h->status;
+    a.vq[0] = L.tvgate;
+    a.vq[1] = L.tvup;
+    a.rgain[0] = L.vgate.gain;
+    a.rgain[1] = L.vup.gain;
+    a.codebook = L.codebook;
+    a.vq_bits = L.vq;
+    a.M = L.I;
+    a.Kd = L.H;
+    a.groups = S.grp_gu;
+    a.ngroups = S.ngrp;
+    a.dense_n = 0;
+    a.out = S.h;
+    a.ldo = L.I;
+    launch_gemm<pf::kFmtVq, 2, pf::kEpiSwiGLUF16>(h, "prefill_gateup_vq", h->map_xp, a);
+    a.vq[0] = L.tvdown;
+    a.rgain[0] = L.vdown.gain;
+    a.M = L.H;
+    a.Kd = L.I;
+    a.groups = S.grp_dn;
+    a.ngroups = S.ngrp + 1;
+    a.out = S.ye;
+    a.ldo = L.H;
+    launch_gemm<pf::kFmtVq, 1, pf::kEpiF32>(h, "prefill_down_vq", h->map_h, a);
+    if (L.Ish > 0) {
+        rc = run_shared_gemms(h, x, T);
+        if (rc)
+            return rc;
+    }
+    launch(h, "combine", [&] {
+        combine_kernel<<<blocks_for((int64_t)T * L.H / 4, 256), 256, 0, st>>>(
+            S.ye, L.Ish > 0 ? S.ysh : nullptr, S.w, S.inv, S.idx, L.gain, T, L.H, L.K, y);
+    });
+    return launch_rc();
+}
+
 // VQ routed experts for the routing already in S.idx / S.w, every T: x in fp32,
 // the gate/up product with SwiGLU, the down product, the shared expert, the
 // combine. The product kernels are persistent (two CTAs per SM) and load the
@@ -1014,6 +1082,11 @@ int resolve_path(const ds4moe *h, int T, int path) {
             return T >= DS4MOE_AUTO_MX4_PREFILL_MIN_T ? DS4MOE_PATH_PREFILL : DS4MOE_PATH_DECODE;
         return path == DS4MOE_PATH_PREFILL ? DS4MOE_PATH_PREFILL : DS4MOE_PATH_DECODE;
     }
+    if (h->L.vq) { // CUDA-core products for decode sizes, tensor cores for prefill sizes
+        if (path == DS4MOE_PATH_AUTO)
+            return T >= DS4MOE_AUTO_VQ_PREFILL_MIN_T ? DS4MOE_PATH_PREFILL : DS4MOE_PATH_DECODE;
+        return path == DS4MOE_PATH_PREFILL ? DS4MOE_PATH_PREFILL : DS4MOE_PATH_DECODE;
+    }
     if (path == DS4MOE_PATH_AUTO) {
         if (T <= DS4MOE_AUTO_DECODE_MAX_T)
             return DS4MOE_PATH_DECODE;
@@ -1032,8 +1105,8 @@ int forward_impl(ds4moe *h, const void *x, int T, int path, float *y) {
         int rc = run_router(h, x, T, nullptr);
         if (rc)
             return rc;
-        if (h->L.vq) // one path for every T
-            return run_experts_vq(h, x, T, y);
+        if (h->L.vq)
+            return path == DS4MOE_PATH_PREFILL ? run_experts_vq_tc(h, x, T, y) : run_experts_vq(h, x, T, y);
         return path == DS4MOE_PATH_PREFILL ? run_experts_mx4_tc(h, x, T, y) : run_experts_mx4(h, x, T, y);
     }
     if (path == DS4MOE_PATH_DECODE)
@@ -1211,6 +1284,13 @@ int ds4moe_create(const ds4moe_layer_desc *desc, const ds4moe_weights *w, ds4moe
         cvq(w->gate, w->gate_plane, w->gate_rowgain, L.vgate);
         cvq(w->up, w->up_plane, w->up_rowgain, L.vup);
         cvq(w->down, w->down_plane, w->down_rowgain, L.vdown);
+        auto rvt = [&](const VqMat &m, VqTile &t) {
+            repack_vq_tile_kernel<<<blocks_for(t.rows * t.nkb, 256), 256, 0, st>>>(m.stream, m.plane, t.rows, m.k,
+                                                                                 const_cast<uint8_t *>(t.rec));
+        };
+        rvt(L.vgate, L.tvgate);
+        rvt(L.vup, L.tvup);
+        rvt(L.vdown, L.tvdown);
         cudaMemcpyAsync(const_cast<uint8_t *>(L.codebook), w->vq_codebook, (size_t)8 << L.vq, cudaMemcpyDeviceToDevice,
                         st);
     } else if (L.mx4) {
@@ -1327,6 +1407,10 @@ int ds4moe_create(const ds4moe_layer_desc *desc, const ds4moe_weights *w, ds4moe
         rc = setup_gemm<pf::kFmtMx4, 2, pf::kEpiSwiGLUFp4>();
     if (!rc)
         rc = setup_gemm<pf::kFmtMx4, 1, pf::kEpiF32>();
+    if (!rc)
+        rc = setup_gemm<pf::kFmtVq, 2, pf::kEpiSwiGLUF16>();
+    if (!rc)
+        rc = setup_gemm<pf::kFmtVq, 1, pf::kEpiF32>();
     if (rc || D.grid <= 0) {
         ds4moe_destroy(h);
         return DS4MOE_ECUDA;
@@ -1438,7 +1522,7 @@ int ds4moe_forward_routed(ds4moe_t *h, const void *x, int32_t T, const int32_t *
     if (rc)
         return rc;
     if (L.vq)
-        return run_experts_vq(h, x, T, y);
+        return path == DS4MOE_PATH_PREFILL ? run_experts_vq_tc(h, x, T, y) : run_experts_vq(h, x, T, y);
     if (L.mx4)
         return path == DS4MOE_PATH_PREFILL ? run_experts_mx4_tc(h, x, T, y) : run_experts_mx4(h, x, T, y);
     return path == DS4MOE_PATH_BATCH ? run_experts_batch(h, x, T, y, false) : run_experts_prefill(h, x, T, y);

@@ -70,11 +70,12 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kWaitNs = 1000000000ull; // 1 s: far beyond any legitimate wait
 constexpr int kBoxes = 4;                   // B box heights 16, 32, 64, 128 rows
 
-enum { kFmtQ2 = 0, kFmtQ8 = 1, kFmtBF16 = 2, kFmtMx4 = 3 };
+enum { kFmtQ2 = 0, kFmtQ8 = 1, kFmtBF16 = 2, kFmtMx4 = 3, kFmtVq = 4 };
 // Epilogues: SwiGLU -> bf16 rows; fp32 rows; SwiGLU -> binary16 rows on the FP4
 // grid (each 32-row block of a token column is one MX block: the epilogue
 // warp's 32 lanes).
-enum { kEpiSwiGLU = 0, kEpiF32 = 1, kEpiSwiGLUFp4 = 2 };
+// SwiGLU -> binary16 rows (the VQ form's down-product operand).
+enum { kEpiSwiGLU = 0, kEpiF32 = 1, kEpiSwiGLUFp4 = 2, kEpiSwiGLUF16 = 3 };
 
 // Tensor maps of one B matrix (bf16 rows, 128-byte swizzle, box 64 columns x
 // 16 << i rows); passed by value as a grid constant.
@@ -88,6 +89,10 @@ struct Args {
     Q8Mat q8[2];
     BfMat bf[1];
     Mx4Tile mx4[2];
+    VqTile vq[2];
+    const uint16_t *rgain[2]; // VQ: binary16 gain of every row (all experts) of the A matrices
+    const uint8_t *codebook;  // VQ: 2^vq_bits codewords of 8 E4M3 bytes
+    int vq_bits;
     int M;                 // rows of one expert's matrix (output features)
     int Kd;                // reduction length
     const int4 *groups;    // routed groups (ignored when dense_n > 0)
@@ -118,15 +123,18 @@ template <int FMT, int NA> struct Cfg {
     static constexpr int kStages = NA == 2 ? 4 : 8;        // A (TMEM) and B (smem) ring depth
     static constexpr int kACols = NA * kTileK / 2;         // TMEM columns of one A stage
     // K steps per raw block: a loader that issues a raw block every K step would bound the kernel
-    static constexpr int kSPB = FMT == kFmtQ2 || FMT == kFmtMx4 ? 4 : FMT == kFmtQ8 ? 2 : 1;
+    static constexpr int kSPB = FMT == kFmtQ2 || FMT == kFmtMx4 || FMT == kFmtVq ? 4 : FMT == kFmtQ8 ? 2 : 1;
     static constexpr int kRawMat = FMT == kFmtQ2   ? 8192 + 2048 + 512
                                    : FMT == kFmtQ8 ? 2 * (8192 + 512)
                                    : FMT == kFmtMx4 ? 4 * kMx4TileRec
+                                   : FMT == kFmtVq  ? kVqTileRec
                                                     : 16384;
     static constexpr int kRaw = 4;                         // raw ring depth (blocks)
     static constexpr int kBBytes = kNMax * kTileK * 2;     // one B stage
     static constexpr int kRawOffset = kStages * kBBytes;
-    static constexpr int kBarOffset = kRawOffset + kRaw * NA * kRawMat;
+    static constexpr int kCbOffset = kRawOffset + kRaw * NA * kRawMat; // VQ: the codebook (13-bit size)
+    static constexpr int kCbBytes = FMT == kFmtVq ? 8 << 13 : 0;
+    static constexpr int kBarOffset = kCbOffset + kCbBytes;
     static constexpr int kSmemBytes = kBarOffset + 512 + 1024; // + barriers + alignment slack
     static_assert(256 + kStages * kACols <= (int)kTmemCols, "TMEM budget");
     static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
@@ -294,6 +302,13 @@ template <int P> struct RawBF { // one 64-column K step: P bf16 of the row
     uint4 c[P / 8];
 };
 
+template <int P> struct RawVq { // one 256-column block of the row: 32 indices (48 bytes), plane bits
+    uint4 c[3];
+    uint32_t plane;
+    uint32_t cb;   // shared-memory address of the codebook
+    int part;      // first 16-column quarter of each K step owned
+};
+
 template <int P> struct RawMx4 { // four 64-column K steps: per step P of the row's weights (P / 32 MX blocks)
     uint4 c[4][P / 32];
     uint32_t sc[4][P / 32]; // their E8M0 bytes
@@ -355,6 +370,14 @@ template <int P> __device__ __forceinline__ void read_raw(uint32_t slot, int r, 
             x.sc[s][i] = (sw >> (8 * half)) & 0xFFu;
         }
     }
+}
+
+template <int P> __device__ __forceinline__ void read_raw(uint32_t slot, int r, int part, RawVq<P> &x) {
+#pragma unroll
+    for (int c = 0; c < 3; c++)
+        x.c[c] = lds128(slot + (c * 128 + r) * 16);
+    x.plane = lds32(slot + 3 * 128 * 16 + r * 4);
+    x.part = part;
 }
 
 // Expand one sub-block word (16 weights, pair p of codes at bits 2p and
@@ -460,6 +483,52 @@ template <int P> __device__ __forceinline__ void expand_step(const RawMx4<P> &r,
     }
 }
 
+// Index i (0..31) of a 48-byte index string (12 bits, least significant bit first).
+__device__ __forceinline__ uint32_t vq_index12(const uint32_t (&w)[12], int i) {
+    const int b = 12 * i, wd = b >> 5, sh = b & 31;
+    uint32_t v = w[wd] >> sh;
+    if (sh > 20)
+        v |= w[wd + 1] << (32 - sh);
+    return v & 0xFFFu;
+}
+
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
+    uint32_t r;
+    asm("{ .reg .b16 t;\n\t"
+        "cvt.u16.u32 t, %1;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, t; }"
+        : "=r"(r)
+        : "r"(two));
+    return r;
+}
+
+// VQ: K step s of the block -> the codewords of the owned indices as binary16
+// pairs (E4M3 is exact in binary16). P = 64: the step's 8 indices; P = 32: the
+// 4 of the owned half.
+template <int N> __device__ __forceinline__ void vq_expand(const uint32_t (&w)[12], uint32_t plane, uint32_t cb,
+                                                          int i0, uint32_t *o) {
+#pragma unroll
+    for (int q = 0; q < N; q++) {
+        const int i = i0 + q;
+        const uint32_t idx = vq_index12(w, i) | ((plane >> i) & 1u) << 12; // plane bits are 0 in 12-bit layers
+        const uint2 cw = lds64(cb + idx * 8);
+        o[4 * q] = e4m3x2_to_f16x2(cw.x);
+        o[4 * q + 1] = e4m3x2_to_f16x2(cw.x >> 16);
+        o[4 * q + 2] = e4m3x2_to_f16x2(cw.y);
+        o[4 * q + 3] = e4m3x2_to_f16x2(cw.y >> 16);
+    }
+}
+
+template <int P> __device__ __forceinline__ void expand_step(const RawVq<P> &r, int s, uint32_t (&o)[P / 2]) {
+    const uint32_t w[12] = {r.c[0].x, r.c[0].y, r.c[0].z, r.c[0].w, r.c[1].x, r.c[1].y,
+                            r.c[1].z, r.c[1].w, r.c[2].x, r.c[2].y, r.c[2].z, r.c[2].w};
+    // the index positions stay compile-time constants (the string is in registers)
+    if (P == 64 || r.part == 0)
+        vq_expand<P / 8>(w, r.plane, r.cb, 8 * s, o);
+    else // part 2: columns 32..63 of the step
+        vq_expand<P / 8>(w, r.plane, r.cb, 8 * s + 4, o);
+}
+
 template <int FMT> struct FmtTraits;
 template <> struct FmtTraits<kFmtQ2> {
     template <int P> using Raw = RawQ2<P>;
@@ -472,6 +541,9 @@ template <> struct FmtTraits<kFmtBF16> {
 };
 template <> struct FmtTraits<kFmtMx4> {
     template <int P> using Raw = RawMx4<P>;
+};
+template <> struct FmtTraits<kFmtVq> {
+    template <int P> using Raw = RawVq<P>;
 };
 
 // The loader's bulk copies of raw block kb of 128-row tile rt of matrix m
@@ -498,6 +570,12 @@ __device__ __forceinline__ unsigned copy_raw(const Mx4Tile &m, int64_t rt, int k
     return 4 * kMx4TileRec;
 }
 
+// VQ: raw block kb is the 256-column block kb of tile rt: one record.
+__device__ __forceinline__ unsigned copy_raw(const VqTile &m, int64_t rt, int kb, uint32_t dst, uint64_t *bar) {
+    bulk_g2s(dst, m.rec + (rt * m.nkb + kb) * kVqTileRec, kVqTileRec, bar);
+    return kVqTileRec;
+}
+
 __device__ __forceinline__ unsigned copy_raw(const BfMat &m, int64_t rt, int ks, uint32_t dst, uint64_t *bar) {
     bulk_g2s(dst, m.p + (rt * m.nks + ks) * 1024, 16384, bar);
     return 16384;
@@ -515,6 +593,9 @@ template <> struct MatOf<kFmtBF16> {
 };
 template <> struct MatOf<kFmtMx4> {
     __device__ static const Mx4Tile &get(const Args &a, int i) { return a.mx4[i]; }
+};
+template <> struct MatOf<kFmtVq> {
+    __device__ static const VqTile &get(const Args &a, int i) { return a.vq[i]; }
 };
 
 // ---- tiles ------------------------------------------------------------------------
@@ -593,6 +674,11 @@ __global__ void __launch_bounds__(Cfg<FMT, NA>::kThreads, 1)
     }
     if (warp == C::kMmaWarp)
         umma::tmem_alloc(tmem_slot, kTmemCols);
+    if constexpr (FMT == kFmtVq) { // the codebook, once per CTA
+        const int n16 = (8 << a.vq_bits) / 16;
+        for (int i = tid; i < n16; i += C::kThreads)
+            reinterpret_cast<uint4 *>(smem + C::kCbOffset)[i] = __ldg(reinterpret_cast<const uint4 *>(a.codebook) + i);
+    }
     umma::fence_before_sync();
     __syncthreads();
     umma::fence_after_sync();
@@ -624,6 +710,8 @@ __global__ void __launch_bounds__(Cfg<FMT, NA>::kThreads, 1)
                 break;
             Raw cur;
             read_raw(raw_base + (rs * NA + mat) * C::kRawMat, row, part, cur);
+            if constexpr (FMT == kFmtVq)
+                cur.cb = smem_base + C::kCbOffset;
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(rempty + rs);
@@ -749,8 +837,8 @@ __global__ void __launch_bounds__(Cfg<FMT, NA>::kThreads, 1)
                     break;
                 umma::fence_after_sync();
                 // MXFP4: both operands binary16 (the expanded weights and the FP4-grid activations)
-                const uint32_t idesc =
-                    FMT == kFmtMx4 ? umma::idesc_f16_f32(kTileM, n_mma) : umma::idesc_bf16_f32(kTileM, n_mma);
+                const uint32_t idesc = FMT == kFmtMx4 || FMT == kFmtVq ? umma::idesc_f16_f32(kTileM, n_mma)
+                                                                        : umma::idesc_bf16_f32(kTileM, n_mma);
                 const uint32_t dacc = tmem + pl.col + iss * pl.stride;
                 const uint32_t a_off = NA == 2 ? iss * (kTileK / 2) : 0;
                 for (int ks = 0; ks < nk; ks++) {
@@ -831,6 +919,15 @@ __global__ void __launch_bounds__(Cfg<FMT, NA>::kThreads, 1)
                     for (int jj = 0; jj < 8; jj++)
                         v[0][jj] += v[1][jj];
                 }
+                if constexpr (FMT == kFmtVq) { // the rows' gains (expert g.x, row mrow)
+#pragma unroll
+                    for (int m = 0; m < NA; m++) {
+                        const float gr = f16_to_f32(__ldg(a.rgain[m] + (int64_t)g.x * a.M + mrow));
+#pragma unroll
+                        for (int jj = 0; jj < 8; jj++)
+                            v[m][jj] *= gr;
+                    }
+                }
                 if (EPI == kEpiSwiGLUFp4) {
                     // one MX block per token column: this warp's 32 rows (M is a multiple of 128)
                     uint16_t *out = static_cast<uint16_t *>(a.out);
@@ -845,6 +942,13 @@ __global__ void __launch_bounds__(Cfg<FMT, NA>::kThreads, 1)
                     }
                 } else if (mrow >= a.M) {
                     // rows past a partial last m-tile
+                } else if (EPI == kEpiSwiGLUF16) {
+                    uint16_t *out = static_cast<uint16_t *>(a.out);
+#pragma unroll
+                    for (int jj = 0; jj < 8; jj++)
+                        if (c0 + jj < g.z)
+                            out[(int64_t)(g.y + c0 + jj) * a.ldo + mrow] =
+                                __half_as_ushort(__float2half_rn(silu(v[0][jj]) * v[1][jj]));
                 } else if (EPI == kEpiSwiGLU) {
                     uint16_t *out = static_cast<uint16_t *>(a.out);
 #pragma unroll

@@ -29,6 +29,37 @@ __device__ __forceinline__ float2 e4m3x2_to_float2(uint32_t two) {
     return __half22float2(*reinterpret_cast<const __half2 *>(&h2));
 }
 
+// The index stream of one matrix (all experts) -> the prefill GEMM's tile
+// records (VqTile). One thread per (row of all experts, 256-column block):
+// 48 bytes of indices and, for 13-bit layers, 4 bytes of bit plane.
+__global__ void repack_vq_tile_kernel(const uint32_t *__restrict__ stream, const uint8_t *__restrict__ plane,
+                                      int64_t rows, int k, uint8_t *__restrict__ rec) {
+    const int nkb = k / 256;
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= rows * nkb)
+        return;
+    const int64_t grow = i / nkb;
+    const int kb = (int)(i % nkb);
+    const int64_t g0 = grow * (k / 8) + 32 * kb; // first index of the piece (in the whole matrix's stream)
+    const uint4 *src = reinterpret_cast<const uint4 *>(reinterpret_cast<const uint8_t *>(stream) + g0 * 3 / 2);
+    uint8_t *dst = rec + ((grow >> 7) * nkb + kb) * kVqTileRec;
+    const int r = (int)(grow & 127);
+#pragma unroll
+    for (int c = 0; c < 3; c++)
+        reinterpret_cast<uint4 *>(dst)[c * 128 + r] = src[c];
+    reinterpret_cast<uint32_t *>(dst + 3 * 128 * 16)[r] =
+        plane ? *reinterpret_cast<const uint32_t *>(plane + g0 / 8) : 0u;
+}
+
+// bf16 -> binary16, round to nearest (x for the VQ tensor-core form).
+__global__ void bf16_to_f16_kernel(const uint16_t *__restrict__ x, int64_t n, uint16_t *__restrict__ out) {
+    pdl_launch_next();
+    pdl_wait();
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i < n)
+        out[i] = __half_as_ushort(__float2half_rn(bf16_to_f32(x[i])));
+}
+
 // bf16 rows -> fp32 (exact).
 __global__ void widen_bf16_kernel(const uint16_t *__restrict__ x, int64_t n, float *__restrict__ out) {
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;

@@ -40,6 +40,7 @@ def test_binding_constants_match_the_header():
     assert macro("DS4MOE_AUTO_BATCH_MAX_T") == ds4.AUTO_BATCH_MAX_T
     assert macro("DS4MOE_BATCH_MAX_T") == ds4.BATCH_MAX_T
     assert macro("DS4MOE_AUTO_MX4_PREFILL_MIN_T") == ds4.AUTO_MX4_PREFILL_MIN_T
+    assert macro("DS4MOE_AUTO_VQ_PREFILL_MIN_T") == ds4.AUTO_VQ_PREFILL_MIN_T
     paths = dict(re.findall(r"(DS4MOE_PATH_\w+)\s*=\s*(\d+)", text))
     assert {k: int(v) for k, v in paths.items()} == {
         "DS4MOE_PATH_AUTO": ds4.PATH_AUTO, "DS4MOE_PATH_DECODE": ds4.PATH_DECODE,

@@ -1,8 +1,10 @@
 """GPU parity of layers with VQ-12/13 routed experts (DS4MOE_FLAG_VQ12/VQ13).
 
 Every 8 weights of a row are a codeword of the layer's E4M3 codebook times a
-binary16 row gain; activations are not quantised, so the bound is the decode
-path's. Every compute call goes through the C ABI.
+binary16 row gain; activations are not quantised. Two forms: CUDA-core
+products (the decode bound) and the grouped GEMMs on the tensor cores, which
+round x and the SwiGLU rows to binary16 (the prefill bound). Every compute call
+goes through the C ABI.
 """
 import numpy as np
 import pytest
@@ -11,7 +13,7 @@ import torch
 import oracle
 import quantized_moe_expert_gb300 as ds4
 import synth
-from gpu_util import TOL_DECODE, assert_close, check_routing, to_dev, x_to_dev
+from gpu_util import TOL_DECODE, TOL_PREFILL, assert_close, check_routing, to_dev, x_to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -37,7 +39,7 @@ def test_forward_matches_oracle(tiny, T):
     shape, layer, moe = tiny
     x = tokens(shape, T, 1500 + T)
     xd = x_to_dev(x)
-    y = moe.forward(xd).cpu().numpy()
+    y = moe.forward(xd, path=ds4.PATH_DECODE).cpu().numpy()
     s = moe.stats()
     idx, w, gap, _ = moe.route(xd)
     assert s.tokens == T and s.n_unique == len(np.unique(idx.cpu().numpy()))
@@ -61,12 +63,39 @@ def test_forward_routed_with_gains(tiny):
         x = tokens(shape, T, 1601)
         idx = np.stack([rng.choice(shape.n_experts, shape.top_k, replace=False) for _ in range(T)]).astype(np.int32)
         w = rng.random((T, shape.top_k)).astype(np.float32)
-        y = moe.forward_routed(x_to_dev(x), torch.from_numpy(idx).cuda(), torch.from_numpy(w).cuda()).cpu().numpy()
         y_ref = oracle.forward_routed(shape, L, x, idx, w.astype(np.float64))
-        assert_close(y, y_ref, TOL_DECODE)
+        for path, tol in ((ds4.PATH_DECODE, TOL_DECODE), (ds4.PATH_PREFILL, TOL_PREFILL)):
+            y = moe.forward_routed(x_to_dev(x), torch.from_numpy(idx).cuda(), torch.from_numpy(w).cuda(),
+                                   path=path).cpu().numpy()
+            assert_close(y, y_ref, tol)
         assert moe.status() == 0
     finally:
         moe.close()
+
+
+@pytest.mark.parametrize("T", [1, 5, 16, 80])
+def test_tensor_form_matches_oracle(tiny, T):
+    shape, layer, moe = tiny
+    x = tokens(shape, T, 1700 + T)
+    y = moe.forward(x_to_dev(x), path=ds4.PATH_PREFILL).cpu().numpy()
+    assert moe.stats().path == ds4.PATH_PREFILL
+    r = moe.inspect(T, grouping=False)
+    y_ref, ref = oracle.forward(shape, layer, x)
+    near = check_routing(r["idx"], r["w"], r["gap"], ref, shape.top_k)
+    if near.any():
+        y_ref = oracle.forward_routed(shape, layer, x, r["idx"], r["w"].astype(np.float64))
+    assert_close(y, y_ref, TOL_PREFILL)
+    assert moe.status() == 0
+
+
+def test_automatic_form_by_token_count(tiny):
+    shape, layer, moe = tiny
+    x = x_to_dev(tokens(shape, ds4.AUTO_VQ_PREFILL_MIN_T, 1801))
+    moe.forward(x[:ds4.AUTO_VQ_PREFILL_MIN_T - 1])
+    assert moe.stats().path == ds4.PATH_DECODE
+    moe.forward(x)
+    assert moe.stats().path == ds4.PATH_PREFILL
+    assert moe.status() == 0
 
 
 def test_create_checks_the_vq_fields():
@@ -86,7 +115,7 @@ def big():
     wl = synth.WORKLOADS["decode_t1"]
     layer = synth.make_layer(wl.shape, wl.layer_seeds[0], routed_format="vq", vq_bits=12)
     dev = to_dev(layer)
-    moe = ds4.MoELayer(wl.shape, dev, max_tokens=8, flags=ds4.FLAG_VQ12)
+    moe = ds4.MoELayer(wl.shape, dev, max_tokens=256, flags=ds4.FLAG_VQ12)
     del dev
     torch.cuda.empty_cache()
     yield wl.shape, layer, moe
@@ -97,9 +126,28 @@ def test_full_size_t1_and_t8(big):
     shape, layer, moe = big
     for x in (synth.make_tokens("decode_t1", T=1), synth.make_tokens("decode_t8")):
         xd = x_to_dev(x)
-        y = moe.forward(xd).cpu().numpy()
+        y = moe.forward(xd, path=ds4.PATH_DECODE).cpu().numpy()
         idx, w, gap, _ = moe.route(xd)
         idx, w = idx.cpu().numpy(), w.cpu().numpy()
         y_ref = oracle.forward_routed(shape, layer, x, idx, w.astype(np.float64))
         assert_close(y, y_ref, TOL_DECODE)
+    assert moe.status() == 0
+
+
+def test_full_size_tensor_form(big):
+    """H=4096, E=384 VQ-12 layer, 256 tokens on the tensor-core form; sampled rows."""
+    shape, layer, moe = big
+    T = 256
+    x = synth.normal_bf16(T * shape.hidden, synth.SEED_BASE + 0x400, synth.S_X).reshape(T, shape.hidden)
+    y = moe.forward(x_to_dev(x)).cpu().numpy()
+    assert moe.stats().path == ds4.PATH_PREFILL
+    r = moe.inspect(T, grouping=False)
+    ref = oracle.route(shape, layer["router_w"], None, x)
+    near = check_routing(r["idx"], r["w"], r["gap"], ref, shape.top_k)
+    rows = np.array(sorted(set([0, 1, 127, 128, 255] + np.random.default_rng(8).choice(T, 5, replace=False).tolist())))
+    ridx = np.where(near[rows][:, None], r["idx"][rows], ref["idx"][rows])
+    rw = np.where(near[rows][:, None], r["w"][rows].astype(np.float64), ref["weights"][rows])
+    y_ref = oracle.forward_routed(shape, layer, np.ascontiguousarray(x[rows]), ridx, rw)
+    assert_close(y[rows], y_ref, TOL_PREFILL)
+    assert np.isfinite(y).all()
     assert moe.status() == 0
