@@ -100,9 +100,9 @@ enum {
  * Each routed-expert product quantises its input per 32 values first (x, and
  * the SwiGLU rows, rounded to binary32, before the down product). Decode form:
  * d = amax / 127, q = x / d rounded to the nearest integer (ties to even), both
- * in binary32; the product uses d * q. Prefill form ("Blackwell CUDA devices use
- * native FP4 matrix instructions and FP4 activations for batched expert work"):
- * the OCP MX conversion, X = 2^(floor(log2 amax) - 2) and the E2M1 value nearest
+ * in binary32; the product uses d * q. Prefill form (the model page's note on
+ * Blackwell: batched expert work runs on FP4 matrix instructions with FP4
+ * activations): the OCP MX conversion, X = 2^(floor(log2 amax) - 2) and the E2M1 value nearest
  * to x / X (ties to even, saturating at 6); the product uses X * e2m1. The
  * prefill form runs on the tensor cores with both operands in binary16, exact
  * for weight scale bytes 104..141 and activation blocks with amax in
