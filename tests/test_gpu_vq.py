@@ -90,11 +90,17 @@ def test_tensor_form_matches_oracle(tiny, T):
 
 def test_automatic_form_by_token_count(tiny):
     shape, layer, moe = tiny
-    x = x_to_dev(tokens(shape, ds4.AUTO_VQ_PREFILL_MIN_T, 1801))
-    moe.forward(x[:ds4.AUTO_VQ_PREFILL_MIN_T - 1])
-    assert moe.stats().path == ds4.PATH_DECODE
-    moe.forward(x)
+    T = max(ds4.AUTO_VQ_PREFILL_MIN_T, 2)
+    x = x_to_dev(tokens(shape, T, 1801))
+    if ds4.AUTO_VQ_PREFILL_MIN_T > 1:
+        moe.forward(x[:ds4.AUTO_VQ_PREFILL_MIN_T - 1])
+        assert moe.stats().path == ds4.PATH_DECODE
+    moe.forward(x[:ds4.AUTO_VQ_PREFILL_MIN_T])
     assert moe.stats().path == ds4.PATH_PREFILL
+    moe.forward(x, path=ds4.PATH_DECODE)  # the CUDA-core form on request
+    assert moe.stats().path == ds4.PATH_DECODE
+    moe.forward(x, path=ds4.PATH_BATCH)
+    assert moe.stats().path == ds4.PATH_DECODE
     assert moe.status() == 0
 
 
