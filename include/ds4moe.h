@@ -160,7 +160,12 @@ enum {
  */
 #define DS4MOE_AUTO_VQ_PREFILL_MIN_T 1
 
-/* Most tokens one call of the batch path takes. */
+/*
+ * Most tokens one call of the batch path takes. The shared expert takes the
+ * batch path's 8-bit tile GEMV (exact products, fp32 sums) in every path and
+ * format up to this many tokens (and max_tokens); the fused decode kernel
+ * holds its own, and larger calls take the tensor-core GEMMs.
+ */
 #define DS4MOE_BATCH_MAX_T 64
 
 /* Execution paths for ds4moe_forward_path. */

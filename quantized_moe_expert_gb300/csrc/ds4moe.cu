@@ -104,7 +104,8 @@ struct DecodeState {
 static_assert(kBatchMaxT == DS4MOE_BATCH_MAX_T, "batch path token limit");
 
 // Buffers and launch shape of the batch path (2-bit layers, up to kBatchMaxT
-// tokens per call).
+// tokens per call) and of its shared-expert items, which every layer's
+// shared expert takes for calls of up to sh_tmax tokens.
 struct BatchState {
     uint16_t *xq = nullptr, *xsums = nullptr;                      // [Tb][H], [Tb][H/8]
     uint16_t *hq_hi = nullptr, *hq_lo = nullptr, *hsums = nullptr; // [Pb][I], [Pb][I], [Pb][I/8]
@@ -112,6 +113,7 @@ struct BatchState {
     int4 *vslot = nullptr;                                         // [Pb] virtual slots
     int32_t *nvslot = nullptr;
     int tmax = 0;                 // tokens per call; 0: the path is unavailable for this layer
+    int sh_tmax = 0;              // tokens per call of the shared expert on the 8-bit tile GEMV; 0: never
     int nstage[2] = {0, 0}; // ring depth of the gate/up and the down product kernel
     int smem[2] = {0, 0};   // their dynamic shared memory
     int chunk[2] = {0, 0};  // columns per stage of their shared-expert (8-bit) items
@@ -366,16 +368,18 @@ void layout_weights(ds4moe *h, Carver &c) {
         m.nbq = k / 32;
         m.rec = c.take<uint8_t>((uint64_t)(rows / 16) * m.nbq * kQ8Rec);
     };
-    if (L.mx4 || L.vq)
-        return; // MXFP4 and VQ layers do not use the fused decode kernel or its layouts
-    f2(D.gate, (int64_t)L.E * L.I, L.H);
-    f2(D.up, (int64_t)L.E * L.I, L.H);
-    f2(D.down, (int64_t)L.E * L.H, L.I);
+    // the shared expert's 8-bit tile GEMV layout serves every layer (the batch kernel's shared
+    // items); the 2-bit one only 2-bit layers (MXFP4 and VQ layers do not use the fused decode kernel)
     if (L.Ish > 0) {
         f8(D.sh_gate, L.Ish, L.H);
         f8(D.sh_up, L.Ish, L.H);
         f8(D.sh_down, L.H, L.Ish);
     }
+    if (L.mx4 || L.vq)
+        return;
+    f2(D.gate, (int64_t)L.E * L.I, L.H);
+    f2(D.up, (int64_t)L.E * L.I, L.H);
+    f2(D.down, (int64_t)L.E * L.H, L.I);
 }
 
 // Logits rows reserved for the router GEMM's K-split partials: tiles * split <=
@@ -435,16 +439,16 @@ void layout_scratch(ds4moe *h, Carver &c) {
     D.ysh = c.take<float>(Td * L.H);
     D.ctl_words = kCtlTileCnt + L.H / 32;
     D.ctl = c.take<unsigned>(D.ctl_words);
+    BatchState &B = h->B;
+    const int64_t Tb = T < kBatchMaxT ? T : kBatchMaxT, Pb = Tb * L.K;
+    B.hs_hi = c.take<uint16_t>(Tb * (L.Ish > 0 ? L.Ish : 2));
+    B.hs_lo = c.take<uint16_t>(Tb * (L.Ish > 0 ? L.Ish : 2));
     if (!L.mx4 && !L.vq) {
-        BatchState &B = h->B;
-        const int64_t Tb = T < kBatchMaxT ? T : kBatchMaxT, Pb = Tb * L.K;
         B.xq = c.take<uint16_t>(Tb * L.H);
         B.xsums = c.take<uint16_t>(Tb * (L.H / 8));
         B.hq_hi = c.take<uint16_t>(Pb * L.I);
         B.hq_lo = c.take<uint16_t>(Pb * L.I);
         B.hsums = c.take<uint16_t>(Pb * (L.I / 8));
-        B.hs_hi = c.take<uint16_t>(Tb * (L.Ish > 0 ? L.Ish : 2));
-        B.hs_lo = c.take<uint16_t>(Tb * (L.Ish > 0 ? L.Ish : 2));
         B.vslot = c.take<int4>(Pb);
         B.nvslot = c.take<int32_t>(1);
     }
@@ -657,6 +661,45 @@ int run_shared_gemms(ds4moe *h, const void *x, int T) {
     return launch_rc();
 }
 
+// The shared expert on the batch kernel's 8-bit items (token groups of up to
+// 8 columns over the exact tile GEMV; SwiGLU rows as a binary16 hi + lo pair):
+// gate/up, then down into S.ysh.
+int run_shared_batch(ds4moe *h, const void *x, int T) {
+    const LayerDev &L = h->L;
+    BatchState &B = h->B;
+    DecodeState &D = h->D;
+    BatchArgs a{};
+    a.H = L.H;
+    a.I = L.I;
+    a.K = L.K;
+    a.Ish = L.Ish;
+    a.T = T;
+    a.sh_gate = D.sh_gate;
+    a.sh_up = D.sh_up;
+    a.sh_down = D.sh_down;
+    a.x = static_cast<const uint16_t *>(x);
+    a.hs_hi = B.hs_hi;
+    a.hs_lo = B.hs_lo;
+    a.ysh = h->S.ysh;
+    a.status = h->status;
+    for (int down = 0; down < 2; down++) {
+        a.nstage = B.nstage[down];
+        a.chunk = B.chunk[down];
+        auto fn = down ? batch_product_kernel<true, kBatchShared> : batch_product_kernel<false, kBatchShared>;
+        launch(h, down ? "batch_down_shared" : "batch_gateup_shared", [&] {
+            launch_pdl(fn, dim3(B.grid), dim3(kBatchThreads), B.smem[down], h->stream, a);
+        });
+    }
+    return launch_rc();
+}
+
+// The shared expert of a call: the tile GEMV for up to B.sh_tmax tokens (a
+// tensor-core tile of 128 rows would leave most SMs idle there), else the
+// tensor-core GEMMs.
+int run_shared(ds4moe *h, const void *x, int T) {
+    return T <= h->B.sh_tmax ? run_shared_batch(h, x, T) : run_shared_gemms(h, x, T);
+}
+
 // Experts and combine for the routing already in S.idx / S.w: grouped
 // tensor-core GEMMs over the expert-grouped rows.
 int run_experts_prefill(ds4moe *h, const void *x, int T, float *y) {
@@ -696,7 +739,7 @@ int run_experts_prefill(ds4moe *h, const void *x, int T, float *y) {
     a.ldo = L.H;
     launch_gemm<pf::kFmtQ2, 1, pf::kEpiF32>(h, "prefill_down_q2", h->map_h, a);
     if (L.Ish > 0) {
-        rc = run_shared_gemms(h, x, T);
+        rc = run_shared(h, x, T);
         if (rc)
             return rc;
     }
@@ -813,7 +856,7 @@ int run_experts_mx4(ds4moe *h, const void *x, int T, float *y) {
         k<<<grid, 256, 0, st>>>(L.mdown, L.mdown, S.hq, S.hd, S.uexp, S.uoff, S.nuniq, S.perm, L.K, L.H, L.I, S.ye);
     });
     if (L.Ish > 0) {
-        rc = run_shared_gemms(h, x, T);
+        rc = run_shared(h, x, T);
         if (rc)
             return rc;
     }
@@ -868,7 +911,7 @@ int run_experts_mx4_tc(ds4moe *h, const void *x, int T, float *y) {
     a.ldo = L.H;
     launch_gemm<pf::kFmtMx4, 1, pf::kEpiF32>(h, "prefill_down_mx4", h->map_h, a);
     if (L.Ish > 0) {
-        rc = run_shared_gemms(h, x, T);
+        rc = run_shared(h, x, T);
         if (rc)
             return rc;
     }
@@ -928,7 +971,7 @@ int run_experts_vq_tc(ds4moe *h, const void *x, int T, float *y) {
     a.ldo = L.H;
     launch_gemm<pf::kFmtVq, 1, pf::kEpiF32>(h, "prefill_down_vq", h->map_h, a);
     if (L.Ish > 0) {
-        rc = run_shared_gemms(h, x, T);
+        rc = run_shared(h, x, T);
         if (rc)
             return rc;
     }
@@ -980,7 +1023,7 @@ int run_experts_vq(ds4moe *h, const void *x, int T, float *y) {
                                    L.H, L.I, U, S.ye);
     });
     if (L.Ish > 0) {
-        rc = run_shared_gemms(h, x, T);
+        rc = run_shared(h, x, T);
         if (rc)
             return rc;
     }
@@ -1329,11 +1372,11 @@ int ds4moe_create(const ds4moe_layer_desc *desc, const ds4moe_weights *w, ds4moe
         rf2(w->gate, D.gate);
         rf2(w->up, D.up);
         rf2(w->down, D.down);
-        if (has_shared) {
-            rf8(w->sh_gate, D.sh_gate);
-            rf8(w->sh_up, D.sh_up);
-            rf8(w->sh_down, D.sh_down);
-        }
+    }
+    if (has_shared) {
+        rf8(w->sh_gate, D.sh_gate);
+        rf8(w->sh_up, D.sh_up);
+        rf8(w->sh_down, D.sh_down);
     }
     cudaMemsetAsync(D.ctl, 0, sizeof(unsigned) * D.ctl_words, st);
     // no stale word may carry a future launch's epoch (epochs start at 1)
@@ -1355,10 +1398,11 @@ int ds4moe_create(const ds4moe_layer_desc *desc, const ds4moe_weights *w, ds4moe
     cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
     D.grid = per_sm * nsm;
     g_pf_grid = nsm;
-    if (!L.mx4 && !L.vq) {
+    {
         // the batch path where its shared memory fits: three stages per ring, else two (the
         // attribute belongs to the kernel, not to the layer: it allows the device maximum).
         // An 8-bit stage holds the widest column range that divides K within kBatchStageCap.
+        // Its routed items serve 2-bit layers only, its shared items every layer.
         BatchState &B = h->B;
         const int optin = (int)prop.sharedMemPerBlockOptin;
         bool fits = true;
@@ -1381,7 +1425,9 @@ int ds4moe_create(const ds4moe_layer_desc *desc, const ds4moe_weights *w, ds4moe
             B.smem[down] = BatchPlan(down, L.H, L.I, L.Ish, chunk, ns).total;
         }
         if (fits) {
-            B.tmax = L.Tmax < kBatchMaxT ? L.Tmax : kBatchMaxT;
+            const int tb = L.Tmax < kBatchMaxT ? L.Tmax : kBatchMaxT;
+            B.tmax = L.mx4 || L.vq ? 0 : tb;
+            B.sh_tmax = L.Ish > 0 ? tb : 0;
             B.grid = nsm;
             for (const void *fn :
                  {(const void *)batch_product_kernel<false, kBatchBoth>, (const void *)batch_product_kernel<true, kBatchBoth>,
