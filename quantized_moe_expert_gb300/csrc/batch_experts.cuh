@@ -70,8 +70,8 @@ struct BatchArgs {
 // x bf16 [T][H] -> the 2-bit GEMV's activation layout (x 4^-p, permuted) and
 // the 16-column sums (bf16 hi + lo), for calls whose router did not write them.
 // One thread per 16-column sub-block.
-__global__ void batch_prep_x_kernel(const uint16_t *__restrict__ x, int T, int H, uint16_t *__restrict__ xq,
-                                    uint16_t *__restrict__ xsums) {
+__global__ void batch_prep_x_kernel(const uint16_t *x, int T, int H, uint16_t *xq,
+                                    uint16_t *xsums) {
     pdl_launch_next();
     pdl_wait();
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -107,12 +107,12 @@ __global__ void batch_prep_x_kernel(const uint16_t *__restrict__ x, int T, int H
 // consecutive grouped positions). Out-of-range indices are clamped and
 // reported (kErrIndex). The same results as the three grouping kernels of the
 // prefill path, in one launch.
-__global__ void __launch_bounds__(1024) batch_group_kernel(int32_t *__restrict__ idx, int P, int E,
-                                                           int32_t *__restrict__ counts, int32_t *__restrict__ offsets,
-                                                           int32_t *__restrict__ uexp, int32_t *__restrict__ uoff,
-                                                           int32_t *__restrict__ nuniq, int32_t *__restrict__ perm,
-                                                           int32_t *__restrict__ inv, int4 *__restrict__ vslot,
-                                                           int32_t *__restrict__ nvslot, unsigned *__restrict__ status) {
+__global__ void __launch_bounds__(1024) batch_group_kernel(int32_t *idx, int P, int E,
+                                                           int32_t *counts, int32_t *offsets,
+                                                           int32_t *uexp, int32_t *uoff,
+                                                           int32_t *nuniq, int32_t *perm,
+                                                           int32_t *inv, int4 *vslot,
+                                                           int32_t *nvslot, unsigned *status) {
     pdl_launch_next();
     pdl_wait();
     __shared__ int32_t cnt[1024], sc[1024], sf[1024], cur[1024], ue[1024], uo[1025];
@@ -488,7 +488,7 @@ __global__ void __launch_bounds__(kBatchThreads, 1) batch_product_kernel(const B
                         const int64_t pos = p0 + col;
                         const uint16_t *hi, *lo = nullptr, *sums = nullptr;
                         if (rt && !DOWN) {
-                            const int t = __ldg(a.perm + pos) / a.K;
+                            const int t = a.perm[pos] / a.K;
                             hi = a.xq + (int64_t)t * K;
                             sums = a.xsums + (int64_t)t * (K / 8);
                         } else if (rt) {

@@ -86,6 +86,12 @@ __device__ __forceinline__ float warp_sum(float v) {
 // its writes are visible (a no-op after an ordinary launch), so it comes before
 // the kernel's first global access; pdl_launch_next() lets the next such
 // kernel be scheduled early. Only the launch and the prologue overlap.
+// Because such a kernel can be resident while every earlier grid of the chain
+// still runs, it reaches the data those grids write through pointers without
+// __restrict__ (a noalias pointer lets the compiler move a load or a store
+// across the wait) and with ordinary loads: the non-coherent path (__ldg, or
+// what the compiler makes of a const __restrict__ pointer) is only for data no
+// grid writes while the kernel is resident, such as the layer's weights.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_launch_next() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 

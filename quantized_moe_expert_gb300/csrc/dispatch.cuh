@@ -97,10 +97,10 @@ __global__ void dispatch_place_kernel(const int32_t *__restrict__ idx, int npair
 // y[t][j] = sum_k w[t][k] * (g[e][j] * ye[inv[t*K+k]][j]) + ysh[t][j], e =
 // idx[t*K+k], summed in k order and then the shared term, so the result does
 // not depend on the schedule. g: [E][H] per-expert down gains, or nullptr (1).
-__global__ void combine_kernel(const float *__restrict__ ye, const float *__restrict__ ysh,
-                               const float *__restrict__ w, const int32_t *__restrict__ inv,
-                               const int32_t *__restrict__ idx, const float *__restrict__ g, int T, int H, int K,
-                               float *__restrict__ y) {
+__global__ void combine_kernel(const float *ye, const float *ysh,
+                               const float *w, const int32_t *inv,
+                               const int32_t *idx, const float *g, int T, int H, int K,
+                               float *y) {
     pdl_launch_next();
     pdl_wait();
     const int64_t i4 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;

@@ -443,14 +443,14 @@ void layout_scratch(ds4moe *h, Carver &c) {
     const int64_t Tb = T < kBatchMaxT ? T : kBatchMaxT, Pb = Tb * L.K;
     B.hs_hi = c.take<uint16_t>(Tb * (L.Ish > 0 ? L.Ish : 2));
     B.hs_lo = c.take<uint16_t>(Tb * (L.Ish > 0 ? L.Ish : 2));
+    B.vslot = c.take<int4>(Pb); // the one-launch grouping writes them for every layer
+    B.nvslot = c.take<int32_t>(1);
     if (!L.mx4 && !L.vq) {
         B.xq = c.take<uint16_t>(Tb * L.H);
         B.xsums = c.take<uint16_t>(Tb * (L.H / 8));
         B.hq_hi = c.take<uint16_t>(Pb * L.I);
         B.hq_lo = c.take<uint16_t>(Pb * L.I);
         B.hsums = c.take<uint16_t>(Pb * (L.I / 8));
-        B.vslot = c.take<int4>(Pb);
-        B.nvslot = c.take<int32_t>(1);
     }
 }
 
@@ -633,6 +633,21 @@ int run_dispatch(ds4moe *h, int T) {
     return launch_rc();
 }
 
+// Expert grouping for the routing in S.idx: for up to kBatchMaxT tokens the
+// batch path's one-launch grouping (which also writes its virtual slots), else
+// the three grouping kernels.
+int run_group(ds4moe *h, int T) {
+    if (T > kBatchMaxT)
+        return run_dispatch(h, T);
+    const LayerDev &L = h->L;
+    Scratch &S = h->S;
+    launch(h, "batch_group", [&] {
+        launch_pdl(batch_group_kernel, dim3(1), dim3(1024), 0, h->stream, S.idx, T * L.K, L.E, S.counts, S.offsets,
+                   S.uexp, S.uoff, S.nuniq, S.perm, S.inv, h->B.vslot, h->B.nvslot, h->status);
+    });
+    return launch_rc();
+}
+
 // The shared expert on tensor cores (dense over the T token rows of x): SwiGLU
 // rows into S.hsh, then the down product into S.ysh.
 int run_shared_gemms(ds4moe *h, const void *x, int T) {
@@ -706,15 +721,17 @@ int run_experts_prefill(ds4moe *h, const void *x, int T, float *y) {
     const LayerDev &L = h->L;
     Scratch &S = h->S;
     cudaStream_t st = h->stream;
-    int rc = run_dispatch(h, T);
+    int rc = run_group(h, T);
     if (rc)
         return rc;
     launch(h, "plan_groups", [&] {
-        pf::plan_groups_kernel<<<1, 1024, 0, st>>>(S.uexp, S.uoff, S.nuniq, pf::Cfg<pf::kFmtQ2, 2>::kNMax, S.grp_gu, S.ngrp,
+        launch_pdl(pf::plan_groups_kernel, dim3(1), dim3(1024), 0, st, S.uexp, S.uoff, S.nuniq, pf::Cfg<pf::kFmtQ2,
+                   2>::kNMax, S.grp_gu, S.ngrp,
                                                      pf::Cfg<pf::kFmtQ2, 1>::kNMax, S.grp_dn, S.ngrp + 1);
     });
     launch(h, "gather_rows", [&] {
-        pf::gather_rows_kernel<<<T * L.K, 256, 0, st>>>(static_cast<const uint16_t *>(x), S.perm, L.K, L.H, S.xp);
+        launch_pdl(pf::gather_rows_kernel, dim3(T * L.K), dim3(256), 0, st, static_cast<const uint16_t *>(x), S.perm,
+                   L.K, L.H, S.xp);
     });
     pf::Args a{};
     a.status = h->status;
@@ -744,8 +761,8 @@ int run_experts_prefill(ds4moe *h, const void *x, int T, float *y) {
             return rc;
     }
     launch(h, "combine", [&] {
-        combine_kernel<<<blocks_for((int64_t)T * L.H / 4, 256), 256, 0, st>>>(
-            S.ye, L.Ish > 0 ? S.ysh : nullptr, S.w, S.inv, S.idx, L.gain, T, L.H, L.K, y);
+        launch_pdl(combine_kernel, dim3(blocks_for((int64_t)T * L.H / 4, 256)), dim3(256), 0, st, S.ye,
+                   L.Ish > 0 ? S.ysh : nullptr, S.w, S.inv, S.idx, L.gain, T, L.H, L.K, y);
     });
     return launch_rc();
 }
@@ -766,10 +783,9 @@ int run_experts_batch(ds4moe *h, const void *x, int T, float *y, bool x_prepared
             launch_pdl(batch_prep_x_kernel, dim3(blocks_for((int64_t)T * L.H / 16, 256)), dim3(256), 0, st,
                        static_cast<const uint16_t *>(x), T, L.H, B.xq, B.xsums);
         });
-    launch(h, "batch_group", [&] {
-        launch_pdl(batch_group_kernel, dim3(1), dim3(1024), 0, st, S.idx, T * L.K, L.E, S.counts, S.offsets, S.uexp,
-                   S.uoff, S.nuniq, S.perm, S.inv, B.vslot, B.nvslot, h->status);
-    });
+    int rc = run_group(h, T);
+    if (rc)
+        return rc;
     BatchArgs a;
     a.H = L.H;
     a.I = L.I;
@@ -826,13 +842,14 @@ int run_experts_mx4(ds4moe *h, const void *x, int T, float *y) {
     const LayerDev &L = h->L;
     Scratch &S = h->S;
     cudaStream_t st = h->stream;
-    int rc = run_dispatch(h, T);
+    int rc = run_group(h, T);
     if (rc)
         return rc;
     const int P = T * L.K;
     const int U = P < L.E ? P : L.E; // bound on the distinct experts
     launch(h, "mx4_act_x", [&] {
-        act_q8_kernel<<<blocks_for((int64_t)T * L.H, 256), 256, 0, st>>>(x, 1, (int64_t)T * L.H, S.xq, S.xd);
+        launch_pdl(act_q8_kernel, dim3(blocks_for((int64_t)T * L.H, 256)), dim3(256), 0, st, x, 1, (int64_t)T * L.H,
+                   S.xq, S.xd);
     });
     // an expert holds at most T rows when a token's experts are distinct; more come in chunks
     const int nt = T <= 1 ? 1 : T <= 2 ? 2 : T <= 4 ? 4 : 8;
@@ -842,10 +859,12 @@ int run_experts_mx4(ds4moe *h, const void *x, int T, float *y) {
                  : nt == 2 ? mx4_product_kernel<true, 2>
                  : nt == 4 ? mx4_product_kernel<true, 4>
                            : mx4_product_kernel<true, 8>;
-        k<<<grid, 256, 0, st>>>(L.mgate, L.mup, S.xq, S.xd, S.uexp, S.uoff, S.nuniq, S.perm, L.K, L.I, L.H, S.hf);
+        launch_pdl(k, grid, dim3(256), 0, st, L.mgate, L.mup, S.xq, S.xd, S.uexp, S.uoff, S.nuniq, S.perm, L.K, L.I,
+                   L.H, S.hf);
     });
     launch(h, "mx4_act_h", [&] {
-        act_q8_kernel<<<blocks_for((int64_t)P * L.I, 256), 256, 0, st>>>(S.hf, 0, (int64_t)P * L.I, S.hq, S.hd);
+        launch_pdl(act_q8_kernel, dim3(blocks_for((int64_t)P * L.I, 256)), dim3(256), 0, st, S.hf, 0,
+                   (int64_t)P * L.I, S.hq, S.hd);
     });
     launch(h, "mx4_down", [&] {
         const dim3 grid((L.H + 7) / 8, U);
@@ -853,7 +872,8 @@ int run_experts_mx4(ds4moe *h, const void *x, int T, float *y) {
                  : nt == 2 ? mx4_product_kernel<false, 2>
                  : nt == 4 ? mx4_product_kernel<false, 4>
                            : mx4_product_kernel<false, 8>;
-        k<<<grid, 256, 0, st>>>(L.mdown, L.mdown, S.hq, S.hd, S.uexp, S.uoff, S.nuniq, S.perm, L.K, L.H, L.I, S.ye);
+        launch_pdl(k, grid, dim3(256), 0, st, L.mdown, L.mdown, S.hq, S.hd, S.uexp, S.uoff, S.nuniq, S.perm, L.K, L.H,
+                   L.I, S.ye);
     });
     if (L.Ish > 0) {
         rc = run_shared(h, x, T);
@@ -861,8 +881,8 @@ int run_experts_mx4(ds4moe *h, const void *x, int T, float *y) {
             return rc;
     }
     launch(h, "combine", [&] {
-        combine_kernel<<<blocks_for((int64_t)T * L.H / 4, 256), 256, 0, st>>>(
-            S.ye, L.Ish > 0 ? S.ysh : nullptr, S.w, S.inv, S.idx, L.gain, T, L.H, L.K, y);
+        launch_pdl(combine_kernel, dim3(blocks_for((int64_t)T * L.H / 4, 256)), dim3(256), 0, st, S.ye,
+                   L.Ish > 0 ? S.ysh : nullptr, S.w, S.inv, S.idx, L.gain, T, L.H, L.K, y);
     });
     return launch_rc();
 }
@@ -876,19 +896,21 @@ int run_experts_mx4_tc(ds4moe *h, const void *x, int T, float *y) {
     const LayerDev &L = h->L;
     Scratch &S = h->S;
     cudaStream_t st = h->stream;
-    int rc = run_dispatch(h, T);
+    int rc = run_group(h, T);
     if (rc)
         return rc;
     launch(h, "plan_groups", [&] {
-        pf::plan_groups_kernel<<<1, 1024, 0, st>>>(S.uexp, S.uoff, S.nuniq, pf::Cfg<pf::kFmtMx4, 2>::kNMax, S.grp_gu,
+        launch_pdl(pf::plan_groups_kernel, dim3(1), dim3(1024), 0, st, S.uexp, S.uoff, S.nuniq, pf::Cfg<pf::kFmtMx4,
+                   2>::kNMax, S.grp_gu,
                                                      S.ngrp, pf::Cfg<pf::kFmtMx4, 1>::kNMax, S.grp_dn, S.ngrp + 1);
     });
     launch(h, "mx4_act_fp4", [&] {
-        act_fp4_kernel<<<blocks_for((int64_t)T * L.H, 256), 256, 0, st>>>(static_cast<const uint16_t *>(x),
+        launch_pdl(act_fp4_kernel, dim3(blocks_for((int64_t)T * L.H, 256)), dim3(256), 0, st,
+                   static_cast<const uint16_t *>(x),
                                                                           (int64_t)T * L.H, S.x4);
     });
     launch(h, "gather_rows", [&] {
-        pf::gather_rows_kernel<<<T * L.K, 256, 0, st>>>(S.x4, S.perm, L.K, L.H, S.xp);
+        launch_pdl(pf::gather_rows_kernel, dim3(T * L.K), dim3(256), 0, st, S.x4, S.perm, L.K, L.H, S.xp);
     });
     pf::Args a{};
     a.status = h->status;
@@ -916,8 +938,8 @@ int run_experts_mx4_tc(ds4moe *h, const void *x, int T, float *y) {
             return rc;
     }
     launch(h, "combine", [&] {
-        combine_kernel<<<blocks_for((int64_t)T * L.H / 4, 256), 256, 0, st>>>(
-            S.ye, L.Ish > 0 ? S.ysh : nullptr, S.w, S.inv, S.idx, L.gain, T, L.H, L.K, y);
+        launch_pdl(combine_kernel, dim3(blocks_for((int64_t)T * L.H / 4, 256)), dim3(256), 0, st, S.ye,
+                   L.Ish > 0 ? S.ysh : nullptr, S.w, S.inv, S.idx, L.gain, T, L.H, L.K, y);
     });
     return launch_rc();
 }
@@ -931,19 +953,21 @@ int run_experts_vq_tc(ds4moe *h, const void *x, int T, float *y) {
     const LayerDev &L = h->L;
     Scratch &S = h->S;
     cudaStream_t st = h->stream;
-    int rc = run_dispatch(h, T);
+    int rc = run_group(h, T);
     if (rc)
         return rc;
     launch(h, "plan_groups", [&] {
-        pf::plan_groups_kernel<<<1, 1024, 0, st>>>(S.uexp, S.uoff, S.nuniq, pf::Cfg<pf::kFmtVq, 2>::kNMax, S.grp_gu,
+        launch_pdl(pf::plan_groups_kernel, dim3(1), dim3(1024), 0, st, S.uexp, S.uoff, S.nuniq, pf::Cfg<pf::kFmtVq,
+                   2>::kNMax, S.grp_gu,
                                                      S.ngrp, pf::Cfg<pf::kFmtVq, 1>::kNMax, S.grp_dn, S.ngrp + 1);
     });
     launch(h, "vq_x_f16", [&] {
-        bf16_to_f16_kernel<<<blocks_for((int64_t)T * L.H, 256), 256, 0, st>>>(static_cast<const uint16_t *>(x),
+        launch_pdl(bf16_to_f16_kernel, dim3(blocks_for((int64_t)T * L.H, 256)), dim3(256), 0, st,
+                   static_cast<const uint16_t *>(x),
                                                                               (int64_t)T * L.H, S.x4);
     });
     launch(h, "gather_rows", [&] {
-        pf::gather_rows_kernel<<<T * L.K, 256, 0, st>>>(S.x4, S.perm, L.K, L.H, S.xp);
+        launch_pdl(pf::gather_rows_kernel, dim3(T * L.K), dim3(256), 0, st, S.x4, S.perm, L.K, L.H, S.xp);
     });
     pf::Args a{};
     a.status = h->status;
@@ -976,8 +1000,8 @@ int run_experts_vq_tc(ds4moe *h, const void *x, int T, float *y) {
             return rc;
     }
     launch(h, "combine", [&] {
-        combine_kernel<<<blocks_for((int64_t)T * L.H / 4, 256), 256, 0, st>>>(
-            S.ye, L.Ish > 0 ? S.ysh : nullptr, S.w, S.inv, S.idx, L.gain, T, L.H, L.K, y);
+        launch_pdl(combine_kernel, dim3(blocks_for((int64_t)T * L.H / 4, 256)), dim3(256), 0, st, S.ye,
+                   L.Ish > 0 ? S.ysh : nullptr, S.w, S.inv, S.idx, L.gain, T, L.H, L.K, y);
     });
     return launch_rc();
 }
@@ -990,7 +1014,7 @@ int run_experts_vq(ds4moe *h, const void *x, int T, float *y) {
     const LayerDev &L = h->L;
     Scratch &S = h->S;
     cudaStream_t st = h->stream;
-    int rc = run_dispatch(h, T);
+    int rc = run_group(h, T);
     if (rc)
         return rc;
     const int P = T * L.K;
@@ -999,7 +1023,8 @@ int run_experts_vq(ds4moe *h, const void *x, int T, float *y) {
     const int entries = 1 << L.vq;
     const size_t smem = (size_t)8 << L.vq;
     launch(h, "vq_widen_x", [&] {
-        widen_bf16_kernel<<<blocks_for((int64_t)T * L.H, 256), 256, 0, st>>>(static_cast<const uint16_t *>(x),
+        launch_pdl(widen_bf16_kernel, dim3(blocks_for((int64_t)T * L.H, 256)), dim3(256), 0, st,
+                   static_cast<const uint16_t *>(x),
                                                                               (int64_t)T * L.H, S.ax);
     });
     launch(h, "vq_gateup", [&] {
@@ -1009,7 +1034,8 @@ int run_experts_vq(ds4moe *h, const void *x, int T, float *y) {
                  : nt == 2 ? vq_product_kernel<true, 2>
                  : nt == 4 ? vq_product_kernel<true, 4>
                            : vq_product_kernel<true, 8>;
-        k<<<grid, 256, smem, st>>>(L.vgate, L.vup, L.codebook, entries, S.ax, S.uexp, S.uoff, S.nuniq, S.perm, L.K,
+        launch_pdl(k, dim3(grid), dim3(256), smem, st, L.vgate, L.vup, L.codebook, entries, S.ax, S.uexp, S.uoff,
+                   S.nuniq, S.perm, L.K,
                                    L.I, L.H, U, S.hf);
     });
     launch(h, "vq_down", [&] {
@@ -1019,7 +1045,8 @@ int run_experts_vq(ds4moe *h, const void *x, int T, float *y) {
                  : nt == 2 ? vq_product_kernel<false, 2>
                  : nt == 4 ? vq_product_kernel<false, 4>
                            : vq_product_kernel<false, 8>;
-        k<<<grid, 256, smem, st>>>(L.vdown, L.vdown, L.codebook, entries, S.hf, S.uexp, S.uoff, S.nuniq, S.perm, L.K,
+        launch_pdl(k, dim3(grid), dim3(256), smem, st, L.vdown, L.vdown, L.codebook, entries, S.hf, S.uexp, S.uoff,
+                   S.nuniq, S.perm, L.K,
                                    L.H, L.I, U, S.ye);
     });
     if (L.Ish > 0) {
@@ -1028,8 +1055,8 @@ int run_experts_vq(ds4moe *h, const void *x, int T, float *y) {
             return rc;
     }
     launch(h, "combine", [&] {
-        combine_kernel<<<blocks_for((int64_t)T * L.H / 4, 256), 256, 0, st>>>(
-            S.ye, L.Ish > 0 ? S.ysh : nullptr, S.w, S.inv, S.idx, L.gain, T, L.H, L.K, y);
+        launch_pdl(combine_kernel, dim3(blocks_for((int64_t)T * L.H / 4, 256)), dim3(256), 0, st, S.ye,
+                   L.Ish > 0 ? S.ysh : nullptr, S.w, S.inv, S.idx, L.gain, T, L.H, L.K, y);
     });
     return launch_rc();
 }
@@ -1430,7 +1457,8 @@ int ds4moe_create(const ds4moe_layer_desc *desc, const ds4moe_weights *w, ds4moe
             B.sh_tmax = L.Ish > 0 ? tb : 0;
             B.grid = nsm;
             for (const void *fn :
-                 {(const void *)batch_product_kernel<false, kBatchBoth>, (const void *)batch_product_kernel<true, kBatchBoth>,
+                 {(const void *)batch_product_kernel<false, kBatchBoth>,
+                  (const void *)batch_product_kernel<true, kBatchBoth>,
                   (const void *)batch_product_kernel<false, kBatchRouted>,
                   (const void *)batch_product_kernel<true, kBatchRouted>,
                   (const void *)batch_product_kernel<false, kBatchShared>,

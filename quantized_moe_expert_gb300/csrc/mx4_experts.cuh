@@ -96,7 +96,7 @@ __device__ __forceinline__ uint16_t fp4_grid_f16(float v, float amax) {
 // FP4 activation rows for the MXFP4 prefill: bf16 x [n] -> binary16 values on
 // the FP4 grid (fp4_grid_f16 per 32-value block). One thread per value, a warp
 // per block (n is a multiple of 32).
-__global__ void act_fp4_kernel(const uint16_t *__restrict__ x, int64_t n, uint16_t *__restrict__ out) {
+__global__ void act_fp4_kernel(const uint16_t *x, int64_t n, uint16_t *out) {
     pdl_launch_next();
     pdl_wait();
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -112,8 +112,10 @@ __global__ void act_fp4_kernel(const uint16_t *__restrict__ x, int64_t n, uint16
 // rounded to the nearest integer (ties to even), both IEEE binary32 (the build
 // has no fast-math flags). One thread per value, a warp per block (n is a
 // multiple of 32); codes to q, block scales to d. src is bf16 (src_bf16) or fp32.
-__global__ void act_q8_kernel(const void *__restrict__ src, int src_bf16, int64_t n, int8_t *__restrict__ q,
-                              float *__restrict__ d) {
+__global__ void act_q8_kernel(const void *src, int src_bf16, int64_t n, int8_t *q,
+                              float *d) {
+    pdl_launch_next();
+    pdl_wait();
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (i - (threadIdx.x & 31) >= n) // whole warps past the end
         return;
@@ -158,22 +160,24 @@ __device__ __forceinline__ uint32_t e2m1x4_twice(uint32_t h, uint32_t *neg) {
 constexpr int kMx4LaneBlocks = 4;
 
 template <bool GATEUP, int NT>
-__global__ void __launch_bounds__(256) mx4_product_kernel(Mx4Mat A, Mx4Mat B, const int8_t *__restrict__ aq,
-                                                          const float *__restrict__ ad,
-                                                          const int32_t *__restrict__ uexp,
-                                                          const int32_t *__restrict__ uoff,
-                                                          const int32_t *__restrict__ nuniq,
-                                                          const int32_t *__restrict__ perm, int K, int M, int Kd,
-                                                          float *__restrict__ out) {
+__global__ void __launch_bounds__(256) mx4_product_kernel(Mx4Mat A, Mx4Mat B, const int8_t *aq,
+                                                          const float *ad,
+                                                          const int32_t *uexp,
+                                                          const int32_t *uoff,
+                                                          const int32_t *nuniq,
+                                                          const int32_t *perm, int K, int M, int Kd,
+                                                          float *out) {
+    pdl_launch_next();
+    pdl_wait();
     const int u = blockIdx.y;
-    if (u >= __ldg(nuniq))
+    if (u >= *nuniq)
         return;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int r = blockIdx.x * 8 + warp;
     if (r >= M)
         return;
-    const int e = __ldg(uexp + u);
-    const int p0 = __ldg(uoff + u), p1 = __ldg(uoff + u + 1);
+    const int e = uexp[u];
+    const int p0 = uoff[u], p1 = uoff[u + 1];
     const int nb = Kd / 32;
     const int64_t row = ((int64_t)e * M + r) * nb;
     for (int c0 = p0; c0 < p1; c0 += NT) {
@@ -182,7 +186,7 @@ __global__ void __launch_bounds__(256) mx4_product_kernel(Mx4Mat A, Mx4Mat B, co
 #pragma unroll
         for (int t = 0; t < NT; t++) {
             const int pos = c0 + (t < n ? t : 0);
-            arow[t] = GATEUP ? __ldg(perm + pos) / K : pos;
+            arow[t] = GATEUP ? perm[pos] / K : pos;
         }
         float ga[NT], ua[NT];
 #pragma unroll
@@ -229,7 +233,7 @@ __global__ void __launch_bounds__(256) mx4_product_kernel(Mx4Mat A, Mx4Mat B, co
                     for (int t = 0; t < NT; t++) {
                         if (t < n) {
                             const int4 *qp = reinterpret_cast<const int4 *>(aq + arow[t] * Kd + b * 32);
-                            const int4 q0 = __ldg(qp), q1 = __ldg(qp + 1);
+                            const int4 q0 = qp[0], q1 = qp[1];
                             const int qw[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
                             int sa_ = 0, sn = 0, sbm = 0, snb = 0;
 #pragma unroll
@@ -241,7 +245,7 @@ __global__ void __launch_bounds__(256) mx4_product_kernel(Mx4Mat A, Mx4Mat B, co
                                     snb = __dp4a((int)nbm[m], qw[m], snb);
                                 }
                             }
-                            const float dt = __ldg(ad + arow[t] * (Kd / 32) + b);
+                            const float dt = ad[arow[t] * (Kd / 32) + b];
                             ga[t] = fmaf(Xa * dt, (float)(sa_ - 2 * sn), ga[t]);
                             if (GATEUP)
                                 ua[t] = fmaf(Xb * dt, (float)(sbm - 2 * snb), ua[t]);

@@ -991,14 +991,16 @@ __global__ void __launch_bounds__(Cfg<FMT, NA>::kThreads, 1)
 
 // B rows of the routed gate/up in expert-grouped order: xp[pos] = x[perm[pos] / K];
 // one CTA per row.
-__global__ void gather_rows_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict__ perm, int K, int H,
-                                   uint16_t *__restrict__ xp) {
+__global__ void gather_rows_kernel(const uint16_t *x, const int32_t *perm, int K, int H,
+                                   uint16_t *xp) {
+    pdl_launch_next();
+    pdl_wait();
     const int pos = blockIdx.x;
     const int t = perm[pos] / K;
     const uint4 *src = reinterpret_cast<const uint4 *>(x + (int64_t)t * H);
     uint4 *dst = reinterpret_cast<uint4 *>(xp + (int64_t)pos * H);
     for (int c = threadIdx.x; c < H / 8; c += blockDim.x)
-        dst[c] = __ldg(src + c);
+        dst[c] = src[c];
 }
 
 // ---- routed tile groups -------------------------------------------------------------
@@ -1006,10 +1008,12 @@ __global__ void gather_rows_kernel(const uint16_t *__restrict__ x, const int32_t
 // One block of 1024 threads (distinct experts <= 1024). For each distinct
 // expert u with rows [uoff[u], uoff[u+1]) emit ceil(rows / nmax) groups of at
 // most nmax rows, for two group sizes at once.
-__global__ void plan_groups_kernel(const int32_t *__restrict__ uexp, const int32_t *__restrict__ uoff,
-                                   const int32_t *__restrict__ nuniq, int nmax_a, int4 *__restrict__ ga,
-                                   int32_t *__restrict__ na, int nmax_b, int4 *__restrict__ gb,
-                                   int32_t *__restrict__ nb) {
+__global__ void plan_groups_kernel(const int32_t *uexp, const int32_t *uoff,
+                                   const int32_t *nuniq, int nmax_a, int4 *ga,
+                                   int32_t *na, int nmax_b, int4 *gb,
+                                   int32_t *nb) {
+    pdl_launch_next();
+    pdl_wait();
     __shared__ int32_t sa[1024], sb[1024];
     const int u = threadIdx.x;
     const int U = *nuniq;

@@ -96,10 +96,10 @@ constexpr int kRtMaxT = 64;
 __host__ __device__ constexpr int router_tile_smem(int TT) { return (kRtExperts + TT) * kRtPitch * 4; }
 
 template <int TT>
-__global__ void __launch_bounds__(kRtThreads) router_tile_kernel(const uint16_t *__restrict__ x, int T, int H,
-                                                                 const float *__restrict__ wr, int E,
-                                                                 float *__restrict__ part, uint16_t *__restrict__ xq,
-                                                                 uint16_t *__restrict__ xsums, unsigned *status) {
+__global__ void __launch_bounds__(kRtThreads) router_tile_kernel(const uint16_t *x, int T, int H,
+                                                                 const float *wr, int E,
+                                                                 float *part, uint16_t *xq,
+                                                                 uint16_t *xsums, unsigned *status) {
     pdl_launch_next();
     pdl_wait();
     extern __shared__ __align__(16) float rt_sm[];
@@ -136,7 +136,7 @@ __global__ void __launch_bounds__(kRtThreads) router_tile_kernel(const uint16_t 
 #pragma unroll
     for (int i = 0; i < NX; i++) {
         const int f = tid + i * kRtThreads, t = f / (kRtSlice / 8), c8 = f % (kRtSlice / 8);
-        xv[i] = t < T ? __ldg(reinterpret_cast<const uint4 *>(x + (int64_t)t * H + k0) + c8) : make_uint4(0u, 0u, 0u, 0u);
+        xv[i] = t < T ? reinterpret_cast<const uint4 *>(x + (int64_t)t * H + k0)[c8] : make_uint4(0u, 0u, 0u, 0u);
     }
 #pragma unroll
     for (int i = 0; i < NX; i++) {
@@ -291,10 +291,10 @@ __device__ __forceinline__ void select_rounds(unsigned *keys, const float *score
 // fp32 dot product of x (bf16) and its router row (the block's warps share
 // the candidates) before the final decision.
 // Shared memory: 2 * E floats + 2 * E ints (kSelectSmemPerExpert bytes per expert).
-__global__ void router_select_kernel(const float *__restrict__ logits, const float *__restrict__ bias, int T,
-                                     int E, int K, int32_t *__restrict__ idx, float *__restrict__ w,
-                                     float *__restrict__ gap, float *__restrict__ sel_out,
-                                     const uint16_t *__restrict__ x_refine, const float *__restrict__ wr, int H,
+__global__ void router_select_kernel(const float *logits, const float *bias, int T,
+                                     int E, int K, int32_t *idx, float *w,
+                                     float *gap, float *sel_out,
+                                     const uint16_t *x_refine, const float *wr, int H,
                                      int nsplit, int64_t split_stride) {
     pdl_launch_next();
     pdl_wait();

@@ -52,7 +52,7 @@ __global__ void repack_vq_tile_kernel(const uint32_t *__restrict__ stream, const
 }
 
 // bf16 -> binary16, round to nearest (x for the VQ tensor-core form).
-__global__ void bf16_to_f16_kernel(const uint16_t *__restrict__ x, int64_t n, uint16_t *__restrict__ out) {
+__global__ void bf16_to_f16_kernel(const uint16_t *x, int64_t n, uint16_t *out) {
     pdl_launch_next();
     pdl_wait();
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -61,7 +61,9 @@ __global__ void bf16_to_f16_kernel(const uint16_t *__restrict__ x, int64_t n, ui
 }
 
 // bf16 rows -> fp32 (exact).
-__global__ void widen_bf16_kernel(const uint16_t *__restrict__ x, int64_t n, float *__restrict__ out) {
+__global__ void widen_bf16_kernel(const uint16_t *x, int64_t n, float *out) {
+    pdl_launch_next();
+    pdl_wait();
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (i < n)
         out[i] = bf16_to_f32(x[i]);
@@ -73,24 +75,26 @@ __global__ void widen_bf16_kernel(const uint16_t *__restrict__ x, int64_t n, flo
 // perm[pos] / K; else grouped positions. The launch's dynamic shared memory
 // holds the codebook (entries << 3 bytes).
 template <bool GATEUP, int NT>
-__global__ void __launch_bounds__(256) vq_product_kernel(VqMat A, VqMat B, const uint8_t *__restrict__ codebook,
-                                                         int entries, const float *__restrict__ act,
-                                                         const int32_t *__restrict__ uexp,
-                                                         const int32_t *__restrict__ uoff,
-                                                         const int32_t *__restrict__ nuniq,
-                                                         const int32_t *__restrict__ perm, int K, int M, int Kd,
-                                                         int ubound, float *__restrict__ out) {
+__global__ void __launch_bounds__(256) vq_product_kernel(VqMat A, VqMat B, const uint8_t *codebook,
+                                                         int entries, const float *act,
+                                                         const int32_t *uexp,
+                                                         const int32_t *uoff,
+                                                         const int32_t *nuniq,
+                                                         const int32_t *perm, int K, int M, int Kd,
+                                                         int ubound, float *out) {
     extern __shared__ __align__(16) uint8_t cb_smem[];
-    {
+    pdl_launch_next();
+    { // the codebook is the layer's own: loaded while the predecessor in the stream finishes
         const uint4 *src = reinterpret_cast<const uint4 *>(codebook);
         uint4 *dst = reinterpret_cast<uint4 *>(cb_smem);
         for (int i = threadIdx.x; i < entries / 2; i += blockDim.x)
             dst[i] = __ldg(src + i);
     }
+    pdl_wait();
     __syncthreads();
     const uint2 *cb = reinterpret_cast<const uint2 *>(cb_smem);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int nu = __ldg(nuniq);
+    const int nu = *nuniq;
     const int groups = (M + 7) / 8;
     const int ngrp = Kd / 64; // 8-index groups per row
     const int64_t row_words = (int64_t)Kd * 3 / 64;
@@ -101,8 +105,8 @@ __global__ void __launch_bounds__(256) vq_product_kernel(VqMat A, VqMat B, const
         const int r = (w - u * groups) * 8 + warp;
         if (r >= M)
             continue;
-        const int e = __ldg(uexp + u);
-        const int p0 = __ldg(uoff + u), p1 = __ldg(uoff + u + 1);
+        const int e = uexp[u];
+        const int p0 = uoff[u], p1 = uoff[u + 1];
         const int64_t er = (int64_t)e * M + r; // row within the whole matrix
         const uint32_t *sa = A.stream + er * row_words;
         const uint32_t *sb = B.stream + er * row_words;
@@ -116,7 +120,7 @@ __global__ void __launch_bounds__(256) vq_product_kernel(VqMat A, VqMat B, const
 #pragma unroll
             for (int t = 0; t < NT; t++) {
                 const int pos = c0 + (t < n ? t : 0);
-                const int64_t ar = GATEUP ? __ldg(perm + pos) / K : pos;
+                const int64_t ar = GATEUP ? perm[pos] / K : pos;
                 arow[t] = act + ar * Kd;
             }
             float acc_a[NT], acc_b[NT];
@@ -159,8 +163,8 @@ __global__ void __launch_bounds__(256) vq_product_kernel(VqMat A, VqMat B, const
 #pragma unroll
                     for (int t = 0; t < NT; t++) {
                         if (t < n) {
-                            const float4 x0 = __ldg(reinterpret_cast<const float4 *>(arow[t] + col));
-                            const float4 x1 = __ldg(reinterpret_cast<const float4 *>(arow[t] + col + 4));
+                            const float4 x0 = *reinterpret_cast<const float4 *>(arow[t] + col);
+                            const float4 x1 = *reinterpret_cast<const float4 *>(arow[t] + col + 4);
                             const float xv[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
 #pragma unroll
                             for (int m = 0; m < 8; m++) {

@@ -48,6 +48,25 @@ def test_prefill_token_counts(mid, T):
     run_and_check(moe, shape, layer, tokens(shape, T, 5000 + T), ds4.PATH_PREFILL, TOL_PREFILL)
 
 
+def test_paths_in_rotation(mid):
+    """Each path's call right after another path's, over token counts around the
+    group boundaries: every call's kernels chain on the stream behind the
+    previous call's (programmatic dependent launches), so a kernel that read
+    its inputs before its predecessors finished would see the previous call's
+    routing or rows here. Each output is held to the routing the library took."""
+    shape, layer, moe = mid
+    paths = ((ds4.PATH_PREFILL, TOL_PREFILL), (ds4.PATH_BATCH, TOL_DECODE), (ds4.PATH_DECODE, TOL_DECODE))
+    for T in (9, 16, 17, 18, 24, 33):
+        x = tokens(shape, T, 5000 + T)
+        xd = x_to_dev(x)
+        for path, tol in paths:
+            y = moe.forward(xd, path=path).cpu().numpy()
+            r = moe.inspect(T, grouping=False)
+            y_ref = oracle.forward_routed(shape, layer, x, r["idx"], r["w"].astype(np.float64))
+            assert_close(y, y_ref, tol)
+            assert moe.status() == 0
+
+
 def test_largest_expert_count_and_top_k():
     shape = synth.Shape(256, 256, 1024, 8, 256)
     layer = synth.make_layer(shape, 4242)
