@@ -69,6 +69,14 @@ __device__ __forceinline__ float f16_to_f32(uint32_t bits) {
     return __half2float(__ushort_as_half(static_cast<unsigned short>(bits & 0xFFFFu)));
 }
 
+// fp32 -> binary16 bits, round to nearest, magnitudes beyond the largest
+// finite binary16 saturating to it.
+__device__ __forceinline__ uint16_t f32_to_f16_sat(float v) {
+    uint16_t h;
+    asm("cvt.rn.satfinite.f16.f32 %0, %1;" : "=h"(h) : "f"(v));
+    return h;
+}
+
 __device__ __forceinline__ float bf16_to_f32(uint32_t bits) {
     return __uint_as_float((bits & 0xFFFFu) << 16);
 }
@@ -160,7 +168,7 @@ struct Scratch {
     int32_t *inv;      // [Tmax*K] expert-grouped position of each pair
     uint16_t *h;       // [Tmax*K][I] bf16 routed SwiGLU activations, expert-grouped order
     float *ye;         // [Tmax*K][H] routed expert outputs, expert-grouped order
-    uint16_t *hsh;     // [Tmax][I_sh] bf16 shared-expert SwiGLU activations
+    uint16_t *hsh;     // [Tmax][I_sh] binary16 shared-expert SwiGLU activations
     uint16_t *xp;      // [Tmax*K][H] bf16 token rows in expert-grouped order (routed gate/up B)
     int4 *grp_gu;      // routed tile groups of at most 128 rows (gate/up)
     int4 *grp_dn;      // routed tile groups of at most 256 rows (down)
@@ -169,7 +177,8 @@ struct Scratch {
     uint16_t *xstage;  // [Tmax][H] bf16 staging for host-memory calls
     float *ystage;     // [Tmax][H]
     float *ax;         // VQ layers: [Tmax][H] x in fp32
-    uint16_t *x4;      // MXFP4 layers: [Tmax][H] the token rows on the FP4 grid, as binary16; VQ layers: x as binary16
+    uint16_t *x4;      // [Tmax][H] binary16 token rows: on the FP4 grid (MXFP4 routed GEMMs) or x itself (VQ routed
+                       // GEMMs, then the shared expert's GEMMs of every layer)
     int8_t *xq;        // MXFP4 layers: [Tmax][H] Q8 codes of the token rows
     float *xd;         // MXFP4 layers: [Tmax][H/32] their block scales
     float *hf;         // MXFP4 and VQ layers: [Tmax*K][I] fp32 SwiGLU rows, expert-grouped order

@@ -122,7 +122,7 @@ struct BatchState {
 
 struct ds4moe {
     Profiler prof;
-    pf::BMaps map_xp, map_h, map_hsh; // B tensor maps over scratch (fixed addresses)
+    pf::BMaps map_xp, map_h, map_hsh, map_x4; // B tensor maps over scratch (fixed addresses)
     pf::BMaps map_x;                  // over the caller's x of the last call
     const void *map_x_ptr = nullptr;
     int map_x_rows = -1;
@@ -415,7 +415,7 @@ void layout_scratch(ds4moe *h, Carver &c) {
     S.ystage = c.take<float>(T * L.H);
     S.ax = L.vq ? c.take<float>(T * L.H) : nullptr;
     S.xq = L.mx4 ? c.take<int8_t>(T * L.H) : nullptr;
-    S.x4 = L.mx4 || L.vq ? c.take<uint16_t>(T * L.H) : nullptr;
+    S.x4 = c.take<uint16_t>(T * L.H); // binary16 x: MXFP4 and VQ forms, the shared expert's GEMMs
     S.xd = L.mx4 ? c.take<float>(T * (L.H / 32)) : nullptr;
     S.hf = L.mx4 || L.vq ? c.take<float>(P * L.I) : nullptr;
     S.hq = L.mx4 ? c.take<int8_t>(P * L.I) : nullptr;
@@ -648,15 +648,16 @@ int run_group(ds4moe *h, int T) {
     return launch_rc();
 }
 
-// The shared expert on tensor cores (dense over the T token rows of x): SwiGLU
-// rows into S.hsh, then the down product into S.ysh.
+// The shared expert on tensor cores (dense over the T token rows of x, in
+// binary16 like the expanded 8-bit weights): SwiGLU rows (binary16) into
+// S.hsh, then the down product into S.ysh.
 int run_shared_gemms(ds4moe *h, const void *x, int T) {
     const LayerDev &L = h->L;
     Scratch &S = h->S;
-    int rc;
-    rc = x_maps(h, x, T);
-    if (rc)
-        return rc;
+    launch(h, "shared_x_f16", [&] {
+        launch_pdl(bf16_to_f16_kernel, dim3(blocks_for((int64_t)T * L.H / 8, 256)), dim3(256), 0, h->stream,
+                   static_cast<const uint16_t *>(x), (int64_t)T * L.H, S.x4);
+    });
     pf::Args s{};
     s.status = h->status;
     s.q8[0] = L.sh_gate;
@@ -666,7 +667,7 @@ int run_shared_gemms(ds4moe *h, const void *x, int T) {
     s.dense_n = T;
     s.out = S.hsh;
     s.ldo = L.Ish;
-    launch_gemm<pf::kFmtQ8, 2, pf::kEpiSwiGLU>(h, "prefill_gateup_q8", h->map_x, s);
+    launch_gemm<pf::kFmtQ8, 2, pf::kEpiSwiGLUF16>(h, "prefill_gateup_q8", h->map_x4, s);
     s.q8[0] = L.sh_down;
     s.M = L.H;
     s.Kd = L.Ish;
@@ -905,7 +906,7 @@ int run_experts_mx4_tc(ds4moe *h, const void *x, int T, float *y) {
                                                      S.ngrp, pf::Cfg<pf::kFmtMx4, 1>::kNMax, S.grp_dn, S.ngrp + 1);
     });
     launch(h, "mx4_act_fp4", [&] {
-        launch_pdl(act_fp4_kernel, dim3(blocks_for((int64_t)T * L.H, 256)), dim3(256), 0, st,
+        launch_pdl(act_fp4_kernel, dim3(blocks_for((int64_t)T * L.H / 8, 256)), dim3(256), 0, st,
                    static_cast<const uint16_t *>(x),
                                                                           (int64_t)T * L.H, S.x4);
     });
@@ -962,7 +963,7 @@ int run_experts_vq_tc(ds4moe *h, const void *x, int T, float *y) {
                                                      S.ngrp, pf::Cfg<pf::kFmtVq, 1>::kNMax, S.grp_dn, S.ngrp + 1);
     });
     launch(h, "vq_x_f16", [&] {
-        launch_pdl(bf16_to_f16_kernel, dim3(blocks_for((int64_t)T * L.H, 256)), dim3(256), 0, st,
+        launch_pdl(bf16_to_f16_kernel, dim3(blocks_for((int64_t)T * L.H / 8, 256)), dim3(256), 0, st,
                    static_cast<const uint16_t *>(x),
                                                                               (int64_t)T * L.H, S.x4);
     });
@@ -1023,7 +1024,7 @@ int run_experts_vq(ds4moe *h, const void *x, int T, float *y) {
     const int entries = 1 << L.vq;
     const size_t smem = (size_t)8 << L.vq;
     launch(h, "vq_widen_x", [&] {
-        launch_pdl(widen_bf16_kernel, dim3(blocks_for((int64_t)T * L.H, 256)), dim3(256), 0, st,
+        launch_pdl(widen_bf16_kernel, dim3(blocks_for((int64_t)T * L.H / 8, 256)), dim3(256), 0, st,
                    static_cast<const uint16_t *>(x),
                                                                               (int64_t)T * L.H, S.ax);
     });
@@ -1300,6 +1301,8 @@ int ds4moe_create(const ds4moe_layer_desc *desc, const ds4moe_weights *w, ds4moe
             rc = make_bmaps(h->S.h, P, L.I, &h->map_h);
         if (!rc && L.Ish > 0)
             rc = make_bmaps(h->S.hsh, L.Tmax, L.Ish, &h->map_hsh);
+        if (!rc && L.Ish > 0)
+            rc = make_bmaps(h->S.x4, L.Tmax, L.H, &h->map_x4);
         if (rc) {
             ds4moe_destroy(h);
             return rc;
@@ -1472,7 +1475,7 @@ int ds4moe_create(const ds4moe_layer_desc *desc, const ds4moe_weights *w, ds4moe
     if (!rc)
         rc = setup_gemm<pf::kFmtQ2, 1, pf::kEpiF32>();
     if (!rc)
-        rc = setup_gemm<pf::kFmtQ8, 2, pf::kEpiSwiGLU>();
+        rc = setup_gemm<pf::kFmtQ8, 2, pf::kEpiSwiGLUF16>();
     if (!rc)
         rc = setup_gemm<pf::kFmtQ8, 1, pf::kEpiF32>();
     if (!rc)

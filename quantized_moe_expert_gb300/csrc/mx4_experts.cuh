@@ -94,18 +94,40 @@ __device__ __forceinline__ uint16_t fp4_grid_f16(float v, float amax) {
 }
 
 // FP4 activation rows for the MXFP4 prefill: bf16 x [n] -> binary16 values on
-// the FP4 grid (fp4_grid_f16 per 32-value block). One thread per value, a warp
-// per block (n is a multiple of 32).
+// the FP4 grid (fp4_grid_f16 per 32-value block). A thread per 8 values, four
+// consecutive lanes per block (n is a multiple of 32, both arrays 16-byte
+// aligned).
 __global__ void act_fp4_kernel(const uint16_t *x, int64_t n, uint16_t *out) {
     pdl_launch_next();
     pdl_wait();
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (i - (threadIdx.x & 31) >= n) // whole warps past the end
+    if (i - (threadIdx.x & 31) >= n / 8) // whole warps past the end
         return;
-    const float v = i < n ? bf16_to_f32(x[i]) : 0.f;
-    const float amax = __uint_as_float(__reduce_max_sync(0xFFFFFFFFu, __float_as_uint(fabsf(v))));
-    if (i < n)
-        out[i] = fp4_grid_f16(v, amax);
+    float v[8];
+    uint32_t mb = 0u; // the largest magnitude's bits (a NaN ranks above every number)
+    if (i < n / 8) {
+        const uint4 w = reinterpret_cast<const uint4 *>(x)[i];
+        const uint32_t p[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int j = 0; j < 4; j++) {
+            v[2 * j] = bf16_to_f32(p[j] & 0xFFFFu);
+            v[2 * j + 1] = bf16_to_f32(p[j] >> 16);
+        }
+#pragma unroll
+        for (int j = 0; j < 8; j++)
+            mb = max(mb, __float_as_uint(fabsf(v[j])));
+    }
+    // the block's four lanes (a block never straddles lanes of two warps)
+    mb = max(mb, __shfl_xor_sync(0xFFFFFFFFu, mb, 1));
+    mb = max(mb, __shfl_xor_sync(0xFFFFFFFFu, mb, 2));
+    const float m = __uint_as_float(mb);
+    if (i < n / 8) {
+        uint32_t o[4];
+#pragma unroll
+        for (int j = 0; j < 4; j++)
+            o[j] = (uint32_t)fp4_grid_f16(v[2 * j], m) | ((uint32_t)fp4_grid_f16(v[2 * j + 1], m) << 16);
+        reinterpret_cast<uint4 *>(out)[i] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
 }
 
 // Q8 activation blocks: per 32 values d = amax / 127 and q_i = x_i / d

@@ -12,8 +12,9 @@
 //                    out = bf16 silu(g) * u in expert-grouped order
 //   routed down      A = 2-bit down rows of e,         B = those bf16 rows,
 //                    out = fp32 expert outputs in expert-grouped order
-//   shared gate/up   A = 8-bit shared gate and up,     B = every x row
-//   shared down      A = 8-bit shared down,            B = the shared SwiGLU rows
+//   shared gate/up   A = 8-bit shared gate and up,     B = every x row (binary16),
+//                    out = binary16 silu(g) * u
+//   shared down      A = 8-bit shared down,            B = those binary16 rows
 //   router logits    A = bf16 parts of the router,     B = every x row (K = 3H)
 //
 // A tile is (group of <= 128 B rows, 128-row m-tile of the expert's matrix):
@@ -51,8 +52,12 @@
 // block's d, dmin: w = (d sc) q - (dmin m). S = d sc and C = dmin m are exact
 // in fp32 and rounded once to bf16; each pair of codes becomes an exact bf16
 // pair q through a magic-number OR and one packed fma, and a second packed
-// fma gives round_bf16(q S - C). 8-bit expansion: w = round_bf16(d q), d q
-// exact in fp32.
+// fma gives round_bf16(q S - C). 8-bit expansion (binary16 operands: the
+// MMA takes both operands in one type, so the shared expert's x and SwiGLU
+// rows are binary16 too): each pair of codes becomes the exact binary16 pair q
+// through a byte permute under a magic exponent and one packed subtraction,
+// and one packed multiply by the block's binary16 scale d gives
+// round_f16(d q).
 #pragma once
 
 #include <cuda.h>
@@ -74,7 +79,8 @@ enum { kFmtQ2 = 0, kFmtQ8 = 1, kFmtBF16 = 2, kFmtMx4 = 3, kFmtVq = 4 };
 // Epilogues: SwiGLU -> bf16 rows; fp32 rows; SwiGLU -> binary16 rows on the FP4
 // grid (each 32-row block of a token column is one MX block: the epilogue
 // warp's 32 lanes).
-// SwiGLU -> binary16 rows (the VQ form's down-product operand).
+// SwiGLU -> binary16 rows, saturating (the down-product operand of the VQ form
+// and of the 8-bit shared expert).
 enum { kEpiSwiGLU = 0, kEpiF32 = 1, kEpiSwiGLUFp4 = 2, kEpiSwiGLUF16 = 3 };
 
 // Tensor maps of one B matrix (bf16 rows, 128-byte swizzle, box 64 columns x
@@ -418,24 +424,30 @@ template <int P> __device__ __forceinline__ void expand_step(const RawQ2<P> &r, 
     }
 }
 
-__device__ __forceinline__ float s8_to_f(uint32_t byte) {
-    // (byte ^ 0x80) is the code + 128; 2^23 + that, minus 2^23 + 128, is exact.
-    return __uint_as_float(0x4B000000u | ((byte ^ 0x80u) & 0xFFu)) - 8388736.0f;
-}
-
-__device__ __forceinline__ uint32_t q8_pair(uint32_t w, int j, float d) {
-    return pack_bf16x2(d * s8_to_f(w >> (16 * j)), d * s8_to_f(w >> (16 * j + 8)));
+// Two int8 codes -> the binary16 pair d * q, rounded once. u is the code word
+// with every byte's top bit flipped (code + 128); sel picks its bytes j, j + 1
+// under the byte 0x64, giving the exact binary16 pair 1152 + q; minus 1152 is
+// the exact q, and one packed multiply by the block's binary16 scale d2 (both
+// halves) rounds d * q.
+__device__ __forceinline__ uint32_t q8_pair_f16(uint32_t u, uint32_t sel, uint32_t d2) {
+    uint32_t p, q, r;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(p) : "r"(u), "r"(0x64646464u), "r"(sel));
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(q) : "r"(p), "r"(0x64806480u)); // 1152 in both halves
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(q), "r"(d2));
+    return r;
 }
 
 template <int P> __device__ __forceinline__ void expand_step(const RawQ8<P> &r, int s, uint32_t (&o)[P / 2]) {
 #pragma unroll
     for (int v = 0; v < P / 16; v++) {
-        const float d = f16_to_f32(r.d[s][P > 32 ? v >> 1 : 0]);
+        const uint32_t d = r.d[s][P > 32 ? v >> 1 : 0] & 0xFFFFu;
+        const uint32_t d2 = d | (d << 16);
         const uint32_t w[4] = {r.c[s][v].x, r.c[s][v].y, r.c[s][v].z, r.c[s][v].w};
 #pragma unroll
         for (int i = 0; i < 4; i++) {
-            o[8 * v + 2 * i] = q8_pair(w[i], 0, d);
-            o[8 * v + 2 * i + 1] = q8_pair(w[i], 1, d);
+            const uint32_t u = w[i] ^ 0x80808080u;
+            o[8 * v + 2 * i] = q8_pair_f16(u, 0x4140u, d2);     // bytes 0, 1
+            o[8 * v + 2 * i + 1] = q8_pair_f16(u, 0x4342u, d2); // bytes 2, 3
         }
     }
 }
@@ -836,9 +848,10 @@ __global__ void __launch_bounds__(Cfg<FMT, NA>::kThreads, 1)
                 if (wide && !mbar_wait(acce + 1, ((use >> 1) & 1u) ^ 1u, abort, a.status))
                     break;
                 umma::fence_after_sync();
-                // MXFP4: both operands binary16 (the expanded weights and the FP4-grid activations)
-                const uint32_t idesc = FMT == kFmtMx4 || FMT == kFmtVq ? umma::idesc_f16_f32(kTileM, n_mma)
-                                                                        : umma::idesc_bf16_f32(kTileM, n_mma);
+                // MXFP4, VQ and 8-bit: both operands binary16 (the expanded weights and the activations)
+                const uint32_t idesc = FMT == kFmtMx4 || FMT == kFmtVq || FMT == kFmtQ8
+                                           ? umma::idesc_f16_f32(kTileM, n_mma)
+                                           : umma::idesc_bf16_f32(kTileM, n_mma);
                 const uint32_t dacc = tmem + pl.col + iss * pl.stride;
                 const uint32_t a_off = NA == 2 ? iss * (kTileK / 2) : 0;
                 for (int ks = 0; ks < nk; ks++) {
@@ -947,8 +960,7 @@ __global__ void __launch_bounds__(Cfg<FMT, NA>::kThreads, 1)
 #pragma unroll
                     for (int jj = 0; jj < 8; jj++)
                         if (c0 + jj < g.z)
-                            out[(int64_t)(g.y + c0 + jj) * a.ldo + mrow] =
-                                __half_as_ushort(__float2half_rn(silu(v[0][jj]) * v[1][jj]));
+                            out[(int64_t)(g.y + c0 + jj) * a.ldo + mrow] = f32_to_f16_sat(silu(v[0][jj]) * v[1][jj]);
                 } else if (EPI == kEpiSwiGLU) {
                     uint16_t *out = static_cast<uint16_t *>(a.out);
 #pragma unroll

@@ -51,22 +51,44 @@ __global__ void repack_vq_tile_kernel(const uint32_t *__restrict__ stream, const
         plane ? *reinterpret_cast<const uint32_t *>(plane + g0 / 8) : 0u;
 }
 
-// bf16 -> binary16, round to nearest (x for the VQ tensor-core form).
+// A bf16 pair -> the binary16 pair, round to nearest, magnitudes beyond the
+// largest finite binary16 saturating to it.
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2_sat(uint32_t v) {
+    uint32_t r;
+    asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;"
+        : "=r"(r)
+        : "f"(__uint_as_float(v & 0xFFFF0000u)), "f"(__uint_as_float(v << 16)));
+    return r;
+}
+
+// bf16 -> binary16 (bf16x2_to_f16x2_sat; x for the VQ tensor-core form and for
+// the shared expert's tensor-core GEMMs). A thread per 8 values: n is a
+// multiple of 8 and both arrays 16-byte aligned.
 __global__ void bf16_to_f16_kernel(const uint16_t *x, int64_t n, uint16_t *out) {
     pdl_launch_next();
     pdl_wait();
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (i < n)
-        out[i] = __half_as_ushort(__float2half_rn(bf16_to_f32(x[i])));
+    if (i < n / 8) {
+        const uint4 v = reinterpret_cast<const uint4 *>(x)[i];
+        reinterpret_cast<uint4 *>(out)[i] = make_uint4(bf16x2_to_f16x2_sat(v.x), bf16x2_to_f16x2_sat(v.y),
+                                                       bf16x2_to_f16x2_sat(v.z), bf16x2_to_f16x2_sat(v.w));
+    }
 }
 
-// bf16 rows -> fp32 (exact).
+// bf16 rows -> fp32 (exact). A thread per 8 values: n is a multiple of 8 and
+// both arrays 16-byte aligned.
 __global__ void widen_bf16_kernel(const uint16_t *x, int64_t n, float *out) {
     pdl_launch_next();
     pdl_wait();
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (i < n)
-        out[i] = bf16_to_f32(x[i]);
+    if (i < n / 8) {
+        const uint4 v = reinterpret_cast<const uint4 *>(x)[i];
+        float4 *o = reinterpret_cast<float4 *>(out) + 2 * i;
+        o[0] = make_float4(bf16_to_f32(v.x & 0xFFFFu), bf16_to_f32(v.x >> 16), bf16_to_f32(v.y & 0xFFFFu),
+                           bf16_to_f32(v.y >> 16));
+        o[1] = make_float4(bf16_to_f32(v.z & 0xFFFFu), bf16_to_f32(v.z >> 16), bf16_to_f32(v.w & 0xFFFFu),
+                           bf16_to_f32(v.w >> 16));
+    }
 }
 
 // out[pos][r] for the expert-grouped rows pos of each distinct expert and r in
