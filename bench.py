@@ -439,7 +439,7 @@ def run_crossover(args):
     wl, layers = workload_layers("decode_t1", args.gains, fmt)
     shape = wl.shape
     stream = torch.cuda.current_stream(dev)
-    T_list = CROSSOVER_T if fmt == "q2" else CROSSOVER_T + (128, 256)
+    T_list = CROSSOVER_T if fmt == "q2" else tuple(sorted(set(CROSSOVER_T + (3, 5, 128, 256))))
     moe = make_handles(layers[:1], shape, dev, max(T_list), fmt, stream)[0]
     flush = torch.empty(2 * torch.cuda.get_device_properties(dev).L2_cache_size, dtype=torch.uint8, device=dev)
     gpu_id = getattr(torch.cuda.get_device_properties(dev), "uuid", None)

@@ -148,7 +148,7 @@ enum {
  * expert work; the boundary between the two sits where the tensor-core form
  * becomes the faster one).
  */
-#define DS4MOE_AUTO_MX4_PREFILL_MIN_T 6
+#define DS4MOE_AUTO_MX4_PREFILL_MIN_T 3
 
 /*
  * Layers with VQ routed experts (DS4MOE_FLAG_VQ12, _VQ13) have two forms of

@@ -24,7 +24,7 @@ DS4MOE_NOALLOC_SCRATCH = 4 << 20
 PATH_AUTO, PATH_DECODE, PATH_PREFILL, PATH_BATCH = 0, 1, 2, 3
 AUTO_DECODE_MAX_T = 1
 AUTO_BATCH_MAX_T = 64
-AUTO_MX4_PREFILL_MIN_T = 6
+AUTO_MX4_PREFILL_MIN_T = 3
 AUTO_VQ_PREFILL_MIN_T = 1
 BATCH_MAX_T = 64
 FLAG_MXFP4 = 1
