@@ -319,7 +319,13 @@ int ds4moe_get_stats(ds4moe_t *h, ds4moe_stats *out);
 int ds4moe_inspect(ds4moe_t *h, int32_t T, int32_t *idx, float *w, float *gap, int32_t *counts, int32_t *inv,
                    int32_t *uexp, int32_t *ustart, int32_t *n_unique);
 
-/* Device bytes the handle owns: repacked weights and scratch. */
+/*
+ * Device bytes the handle owns: repacked weights and scratch. The weights
+ * count every resident layout: the routed experts twice (the tensor-core
+ * tile layout and the layout of the CUDA-core products: 2 x 3.17 GB for a
+ * 2-bit layer at H=4096, I=2048, E=384) and the 8-bit shared expert twice
+ * (tile layout and the tile GEMV's fragment layout), besides the router.
+ */
 int ds4moe_memory(ds4moe_t *h, uint64_t *weight_bytes, uint64_t *scratch_bytes);
 
 /*
