@@ -105,8 +105,8 @@ __global__ void batch_prep_x_kernel(const uint16_t *x, int T, int H, uint16_t *x
 // inverse: pairs of one expert keep ascending pair index) and the virtual
 // slots (distinct expert u with n pairs gives ceil(n / kBatchCols) slots of
 // consecutive grouped positions). Out-of-range indices are clamped and
-// reported (kErrIndex). The same results as the three grouping kernels of the
-// prefill path, in one launch.
+// reported (kErrIndex). The same results as group_kernel, the grouping of
+// larger calls.
 __global__ void __launch_bounds__(1024) batch_group_kernel(int32_t *idx, int P, int E,
                                                            int32_t *counts, int32_t *offsets,
                                                            int32_t *uexp, int32_t *uoff,

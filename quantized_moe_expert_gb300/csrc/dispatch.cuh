@@ -12,84 +12,112 @@
 
 namespace ds4 {
 
-__global__ void dispatch_count_kernel(int32_t *__restrict__ idx, int npairs, int E, int32_t *__restrict__ counts,
-                                      unsigned *__restrict__ status) {
-    const int p = blockIdx.x * blockDim.x + threadIdx.x;
-    if (p >= npairs)
-        return;
-    int e = idx[p];
-    if (e < 0 || e >= E) {
-        atomicOr(status, kErrIndex);
-        e = e < 0 ? 0 : E - 1;
-        idx[p] = e;
+// The grouping in one block of 1024 threads for any number of pairs P (E <= 1024):
+// warp w owns the w-th of 32 contiguous chunks of the pairs.
+//   0. with stage_idx, the block first copies idx into shared memory (every
+//      thread's loads in flight at once), so the two walks below do not wait
+//      on a global load per step;
+//   1. each warp counts its chunk's pairs per expert in its own row of a
+//      shared-memory histogram [32][E] (dynamic shared memory: 128 E bytes,
+//      then 4 P bytes of staged indices);
+//   2. per expert: the total over the rows, the exclusive scan over experts
+//      (offsets), the distinct experts, and per row the first grouped position
+//      of that warp's pairs of the expert (the expert's offset plus the counts
+//      of the lower rows), written over the histogram;
+//   3. each warp walks its chunk again, 32 pairs at a time in pair order: the
+//      lanes of one expert (match_any) take consecutive positions in lane
+//      order from the warp's cursor, which the lowest of them then advances.
+// Pairs of one expert keep ascending pair index (chunks, steps and lanes in
+// order). Out-of-range indices are clamped and reported (kErrIndex).
+__global__ void __launch_bounds__(1024) group_kernel(int32_t *idx, int P, int E, bool stage_idx, int32_t *counts,
+                                                     int32_t *offsets, int32_t *uexp, int32_t *uoff, int32_t *nuniq,
+                                                     int32_t *perm, int32_t *inv, unsigned *status) {
+    pdl_launch_next();
+    pdl_wait();
+    extern __shared__ int32_t hist[]; // [32][E], then (stage_idx) the P indices
+    __shared__ int32_t sc[1024], sf[1024];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    for (int i = tid; i < 32 * E; i += 1024)
+        hist[i] = 0;
+    int32_t *ix = idx; // where the walks read the (clamped) indices
+    if (stage_idx) {
+        ix = hist + 32 * E;
+        for (int p = tid; p < P; p += 1024) {
+            int e = idx[p];
+            if (e < 0 || e >= E) {
+                atomicOr(status, kErrIndex);
+                e = e < 0 ? 0 : E - 1;
+                idx[p] = e;
+            }
+            ix[p] = e;
+        }
     }
-    atomicAdd(counts + e, 1);
-}
-
-// One block of 1024 threads; E <= 1024.
-__global__ void dispatch_scan_kernel(const int32_t *__restrict__ counts, int E, int npairs,
-                                     int32_t *__restrict__ offsets, int32_t *__restrict__ uexp,
-                                     int32_t *__restrict__ uoff, int32_t *__restrict__ nuniq) {
-    __shared__ int32_t sc[1024];
-    __shared__ int32_t sf[1024];
-    const int e = threadIdx.x;
-    const int c = e < E ? counts[e] : 0;
-    sc[e] = c;
-    sf[e] = c > 0;
+    __syncthreads();
+    const int chunk = (P + 31) / 32;
+    const int p_begin = min(P, warp * chunk), p_end = min(P, p_begin + chunk);
+    int32_t *row = hist + warp * E;
+    for (int p = p_begin + lane; p < p_end; p += 32) {
+        int e = ix[p];
+        if (e < 0 || e >= E) { // unstaged indices only: the staging clamped its copies
+            atomicOr(status, kErrIndex);
+            e = e < 0 ? 0 : E - 1;
+            idx[p] = e;
+        }
+        atomicAdd(row + e, 1);
+    }
+    __syncthreads();
+    int c = 0;
+    if (tid < E)
+        for (int w = 0; w < 32; w++)
+            c += hist[w * E + tid];
+    sc[tid] = c;
+    sf[tid] = c > 0;
     __syncthreads();
     for (int o = 1; o < 1024; o <<= 1) { // inclusive Hillis-Steele scans
-        int a = e >= o ? sc[e - o] : 0;
-        int b = e >= o ? sf[e - o] : 0;
+        const int a = tid >= o ? sc[tid - o] : 0;
+        const int b = tid >= o ? sf[tid - o] : 0;
         __syncthreads();
-        sc[e] += a;
-        sf[e] += b;
+        sc[tid] += a;
+        sf[tid] += b;
         __syncthreads();
     }
-    if (e < E) {
-        offsets[e] = sc[e] - c;
+    const int nu = sf[1023];
+    if (tid < E) {
+        const int off = sc[tid] - c;
+        counts[tid] = c;
+        offsets[tid] = off;
         if (c > 0) {
-            uexp[sf[e] - 1] = e;
-            uoff[sf[e] - 1] = sc[e] - c;
+            uexp[sf[tid] - 1] = tid;
+            uoff[sf[tid] - 1] = off;
+        }
+        int run = off;
+        for (int w = 0; w < 32; w++) {
+            const int n = hist[w * E + tid];
+            hist[w * E + tid] = run;
+            run += n;
         }
     }
-    if (e == 0) {
-        int n = sf[1023];
-        *nuniq = n;
-        uoff[n] = npairs;
-        offsets[E] = npairs;
+    if (tid == 0) {
+        *nuniq = nu;
+        uoff[nu] = P;
+        offsets[E] = P;
     }
-}
-
-// One block of 256 threads per expert: walk the pairs in order and give each
-// pair routed to this expert its stable rank.
-__global__ void dispatch_place_kernel(const int32_t *__restrict__ idx, int npairs, const int32_t *__restrict__ counts,
-                                      const int32_t *__restrict__ offsets, int32_t *__restrict__ perm,
-                                      int32_t *__restrict__ inv) {
-    const int e = blockIdx.x;
-    if (counts[e] == 0)
-        return;
-    __shared__ int32_t warp_tot[8];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    int base = offsets[e];
-    for (int p0 = 0; p0 < npairs; p0 += 256) {
-        const int p = p0 + threadIdx.x;
-        const bool hit = p < npairs && idx[p] == e;
-        const unsigned m = __ballot_sync(0xFFFFFFFFu, hit);
-        if (lane == 0)
-            warp_tot[warp] = __popc(m);
-        __syncthreads();
-        int before = 0, total = 0;
-        for (int w = 0; w < 8; w++) {
-            before += w < warp ? warp_tot[w] : 0;
-            total += warp_tot[w];
-        }
-        if (hit) {
-            const int pos = base + before + __popc(m & ((1u << lane) - 1u));
+    __syncthreads();
+    for (int p0 = p_begin; p0 < p_end; p0 += 32) { // warp-uniform bounds
+        const int p = p0 + lane;
+        const int e = p < p_end ? ix[p] : -1; // clamped in step 0 or 1 (by this lane, unstaged)
+        const unsigned m = __match_any_sync(0xFFFFFFFFu, e);
+        const int leader = __ffs(m) - 1;
+        const int base = __shfl_sync(0xFFFFFFFFu, e >= 0 && lane == leader ? row[e] : 0, leader);
+        if (e >= 0) {
+            const int pos = base + __popc(m & ((1u << lane) - 1u));
             perm[pos] = p;
             inv[p] = pos;
         }
-        base += total;
-        __syncthreads();
+        __syncwarp();
+        if (e >= 0 && lane == leader)
+            row[e] = base + __popc(m);
+        __syncwarp();
     }
 }
 

@@ -614,33 +614,26 @@ int run_router(ds4moe *h, const void *x, int T, float *sel_out, uint16_t *xq = n
     return launch_rc();
 }
 
-// Expert grouping for the routing in S.idx.
-int run_dispatch(ds4moe *h, int T) {
-    const LayerDev &L = h->L;
-    Scratch &S = h->S;
-    cudaStream_t st = h->stream;
-    const int P = T * L.K;
-    cudaMemsetAsync(S.counts, 0, sizeof(int32_t) * L.E, st);
-    launch(h, "dispatch_count", [&] {
-        dispatch_count_kernel<<<blocks_for(P, 256), 256, 0, st>>>(S.idx, P, L.E, S.counts, h->status);
-    });
-    launch(h, "dispatch_scan", [&] {
-        dispatch_scan_kernel<<<1, 1024, 0, st>>>(S.counts, L.E, P, S.offsets, S.uexp, S.uoff, S.nuniq);
-    });
-    launch(h, "dispatch_place", [&] {
-        dispatch_place_kernel<<<L.E, 256, 0, st>>>(S.idx, P, S.counts, S.offsets, S.perm, S.inv);
-    });
-    return launch_rc();
-}
+// Dynamic shared memory of the one-block grouping: the histograms (128 E bytes,
+// at most 128 KB) and, where they fit beside them, the staged indices.
+constexpr size_t kGroupSmemMax = 200 * 1024;
 
-// Expert grouping for the routing in S.idx: for up to kBatchMaxT tokens the
-// batch path's one-launch grouping (which also writes its virtual slots), else
-// the three grouping kernels.
+// Expert grouping for the routing in S.idx, one launch: for up to kBatchMaxT
+// tokens the batch path's grouping (which also writes its virtual slots),
+// else the one-block grouping over per-warp histograms.
 int run_group(ds4moe *h, int T) {
-    if (T > kBatchMaxT)
-        return run_dispatch(h, T);
     const LayerDev &L = h->L;
     Scratch &S = h->S;
+    if (T > kBatchMaxT) {
+        const int P = T * L.K;
+        const size_t hist = (size_t)128 * L.E, staged = hist + (size_t)4 * P;
+        const bool stage = staged <= kGroupSmemMax;
+        launch(h, "group", [&] {
+            launch_pdl(group_kernel, dim3(1), dim3(1024), stage ? staged : hist, h->stream, S.idx, P, L.E, stage,
+                       S.counts, S.offsets, S.uexp, S.uoff, S.nuniq, S.perm, S.inv, h->status);
+        });
+        return launch_rc();
+    }
     launch(h, "batch_group", [&] {
         launch_pdl(batch_group_kernel, dim3(1), dim3(1024), 0, h->stream, S.idx, T * L.K, L.E, S.counts, S.offsets,
                    S.uexp, S.uoff, S.nuniq, S.perm, S.inv, h->B.vslot, h->B.nvslot, h->status);
@@ -1469,6 +1462,7 @@ int ds4moe_create(const ds4moe_layer_desc *desc, const ds4moe_weights *w, ds4moe
                 cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
         }
     }
+    cudaFuncSetAttribute(group_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGroupSmemMax);
     cudaFuncSetAttribute(router_tile_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, router_tile_smem(16));
     cudaFuncSetAttribute(router_tile_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, router_tile_smem(64));
     rc = setup_gemm<pf::kFmtQ2, 2, pf::kEpiSwiGLU>();

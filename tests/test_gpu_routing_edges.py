@@ -165,6 +165,24 @@ def test_all_nan_token_takes_the_lowest_indices(how, T):
         moe.close()
 
 
+@pytest.mark.parametrize("T", [40, 130, 2400])
+def test_grouping_at_the_largest_expert_count(T):
+    """E = 1024 and top-8: the widest per-warp histograms (128 KB of shared
+    memory) and the scans at their full width; at T=2400 (19200 pairs) the
+    indices no longer fit beside the histograms and the walks read them from
+    global memory."""
+    shape = synth.Shape(256, 256, 1024, 8, 256)
+    layer = synth.make_layer(shape, 4242)
+    moe = ds4.MoELayer(shape, to_dev(layer), max_tokens=T)
+    try:
+        moe.forward(x_to_dev(synth.normal_bf16(T * shape.hidden, 1900 + T, synth.S_X).reshape(T, shape.hidden)),
+                    path=ds4.PATH_PREFILL)
+        check_grouping(moe, T, shape.n_experts)
+        assert moe.status() == 0
+    finally:
+        moe.close()
+
+
 def counting_sort(idx, E):
     """Stable counting sort of the (token, k) pairs by expert: counts, the
     grouped position of every pair, the distinct experts and their starts."""
@@ -190,11 +208,14 @@ def check_grouping(moe, T, E):
 
 @pytest.mark.parametrize("path,T", [(ds4.PATH_DECODE, 1), (ds4.PATH_DECODE, 3), (ds4.PATH_DECODE, 8),
                                     (ds4.PATH_PREFILL, 16), (ds4.PATH_PREFILL, 64), (ds4.PATH_BATCH, 9),
-                                    (ds4.PATH_BATCH, 64)])
+                                    (ds4.PATH_BATCH, 64), (ds4.PATH_PREFILL, 65), (ds4.PATH_PREFILL, 1000)])
 def test_grouping_is_a_stable_counting_sort(path, T):
+    """Up to 64 tokens the one-launch grouping of the batch path (or the decode
+    kernel's own), above it the one-block grouping over per-warp histograms
+    (T=1000: 6000 pairs, about 190 per expert, chunks of 188 pairs per warp)."""
     shape = synth.TINY_SHAPE
     layer = synth.make_layer(shape, synth.SEED_BASE)
-    moe = ds4.MoELayer(shape, to_dev(layer), max_tokens=64)
+    moe = ds4.MoELayer(shape, to_dev(layer), max_tokens=max(64, T))
     try:
         moe.forward(x_to_dev(tokens(T, 1700 + T)), path=path)
         check_grouping(moe, T, shape.n_experts)
