@@ -130,12 +130,13 @@ def kernel_bytes(name, shape, T, U, gains=0, fmt="q2"):
 # with the SHA-1 of the kernel's source file at capture time: the figure is
 # reported only while that source is unchanged.
 TRAFFIC = {
-    ("prefill_gateup_q2", "prefill_t1024"): (2188538368, "prefill_gemm.cuh", "d7c7eaefd5d9bbc2898ca2a38b0ed443da38ec51"),
-    ("prefill_down_q2", "prefill_t1024"): (1174258176, "prefill_gemm.cuh", "d7c7eaefd5d9bbc2898ca2a38b0ed443da38ec51"),
-    ("decode_fused", "decode_t1"): (83687424, "decode_fused.cuh", "706623878407df8cb54985e1f126854688daed79"),
-    # mean of two batches of the pool (43-47 distinct experts each; the traffic follows the batch's experts)
-    ("decode_fused", "decode_t8"): (404592256, "decode_fused.cuh", "706623878407df8cb54985e1f126854688daed79"),
-    ("batch_gateup", "batch_t64"): (1363576064, "batch_experts.cuh", "66928072388d47a3c2c96500e68f480a0891b70e"),
+    ("prefill_gateup_q2", "prefill_t1024"): (2188350208, "prefill_gemm.cuh", "c4d8d4b85ae902ac97cf5595672432168c7c5ec7"),
+    ("prefill_down_q2", "prefill_t1024"): (1174632192, "prefill_gemm.cuh", "c4d8d4b85ae902ac97cf5595672432168c7c5ec7"),
+    # mean of two launches
+    ("decode_fused", "decode_t1"): (83569152, "decode_fused.cuh", "e72c292f502930ae0475e19e48ff689409d3a399"),
+    # one launch, a batch of the pool with about 46 distinct experts (the traffic follows the batch's experts)
+    ("batch_gateup", "decode_t8"): (256792064, "batch_experts.cuh", "1a43797efb490c1ae6771547950806630f0c4bda"),
+    ("batch_gateup", "batch_t64"): (1363536896, "batch_experts.cuh", "1a43797efb490c1ae6771547950806630f0c4bda"),
 }
 
 
