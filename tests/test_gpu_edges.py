@@ -67,6 +67,25 @@ def test_paths_in_rotation(mid):
             assert moe.status() == 0
 
 
+def test_binary16_saturation_in_the_shared_gemms(mid):
+    """Above 64 tokens the shared expert's tensor-core GEMMs take x as binary16,
+    saturating at +-65504: a token with bf16 values beyond that range gets a
+    finite output, and every other token of the call still matches the oracle."""
+    shape, layer, moe = mid
+    T = 80
+    x = tokens(shape, T, 5900).copy()
+    x[7, :64] = np.uint16(0x4980) # bf16 bits of 2^20, far beyond binary16's range
+    xd = x_to_dev(x)
+    y = moe.forward(xd, path=ds4.PATH_PREFILL).cpu().numpy()
+    assert np.isfinite(y).all()
+    r = moe.inspect(T, grouping=False)
+    others = np.array([t for t in range(T) if t != 7])
+    y_ref = oracle.forward_routed(shape, layer, np.ascontiguousarray(x[others]), r["idx"][others],
+                                  r["w"][others].astype(np.float64))
+    assert_close(y[others], y_ref, TOL_PREFILL)
+    assert moe.status() == 0
+
+
 def test_largest_expert_count_and_top_k():
     shape = synth.Shape(256, 256, 1024, 8, 256)
     layer = synth.make_layer(shape, 4242)

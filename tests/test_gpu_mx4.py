@@ -191,3 +191,21 @@ def test_full_size_prefill_form(big):
     assert_close(y[rows], y_ref, TOL_PREFILL)
     assert np.isfinite(y).all()
     assert moe.status() == 0
+
+
+def test_full_size_automatic_form(big):
+    """H=4096, E=384 MXFP4 layer on the automatic path: 2 tokens on the decode
+    form (Q8 activations) and the eight-token batch on the prefill form (FP4
+    activations, tensor cores), each against the oracle's arithmetic of that
+    form on the library's routing."""
+    shape, layer, moe = big
+    pool = synth.make_tokens("decode_t8")
+    for T, path, act, tol in ((2, ds4.PATH_DECODE, "q8", TOL_DECODE), (8, ds4.PATH_PREFILL, "mx4", TOL_PREFILL)):
+        x = np.ascontiguousarray(pool[:T])
+        y = moe.forward(x_to_dev(x)).cpu().numpy()
+        assert moe.stats().path == path
+        r = moe.inspect(T, grouping=False)
+        check_routing(r["idx"], r["w"], r["gap"], oracle.route(shape, layer["router_w"], None, x), shape.top_k)
+        y_ref = oracle.forward_routed(shape, layer, x, r["idx"], r["w"].astype(np.float64), act=act)
+        assert_close(y, y_ref, tol)
+    assert moe.status() == 0

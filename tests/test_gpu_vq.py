@@ -157,3 +157,19 @@ def test_full_size_tensor_form(big):
     assert_close(y[rows], y_ref, TOL_PREFILL)
     assert np.isfinite(y).all()
     assert moe.status() == 0
+
+
+def test_full_size_automatic_form_t1_and_t8(big):
+    """H=4096, E=384 VQ-12 layer on the automatic path (the tensor-core form at
+    every T): the decode pool's first token and the eight-token batch, on the
+    library's routing, at the tensor-core form's bound."""
+    shape, layer, moe = big
+    for x in (synth.make_tokens("decode_t1", T=1), synth.make_tokens("decode_t8")):
+        T = x.shape[0]
+        y = moe.forward(x_to_dev(x)).cpu().numpy()
+        assert moe.stats().path == ds4.PATH_PREFILL
+        r = moe.inspect(T, grouping=False)
+        check_routing(r["idx"], r["w"], r["gap"], oracle.route(shape, layer["router_w"], None, x), shape.top_k)
+        y_ref = oracle.forward_routed(shape, layer, x, r["idx"], r["w"].astype(np.float64))
+        assert_close(y, y_ref, TOL_PREFILL)
+    assert moe.status() == 0
