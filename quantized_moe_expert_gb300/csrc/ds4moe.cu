@@ -577,15 +577,23 @@ int run_router(ds4moe *h, const void *x, int T, float *sel_out, uint16_t *xq = n
         a.b_kwrap = L.H;
         a.out = S.logits;
         a.ldo = L.E;
-        // split K so that the tiles fill the GPU: the largest divisor of the K steps
-        // with tiles * split <= grid and at least 4 K steps per partial tile
-        const int tiles = ((L.E + 127) / 128) * ((T + 127) / 128);
+        // split K so that the partial tiles fill the GPU: the divisor of the K steps
+        // with the fewest K steps on the busiest CTA (rounds of partial tiles times
+        // K steps per partial tile; the smaller split on a tie), at least 4 K steps
+        // per partial tile, within the partial-logit rows
+        const int64_t tiles = ((L.E + 127) / 128) * ((T + 127) / 128);
         const int nk = 3 * L.H / 64;
         int split = 1;
-        for (int d = 1; d <= nk; d++)
-            if (nk % d == 0 && nk / d >= 4 && (int64_t)tiles * d <= g_pf_grid &&
-                (int64_t)d * T <= (T > kLogitRowsSplit ? T : kLogitRowsSplit))
+        int64_t best = -1;
+        for (int d = 1; d <= nk; d++) {
+            if (nk % d != 0 || nk / d < 4 || (int64_t)d * T > (T > kLogitRowsSplit ? T : kLogitRowsSplit))
+                continue;
+            const int64_t steps = (tiles * d + g_pf_grid - 1) / g_pf_grid * (nk / d);
+            if (best < 0 || steps < best) {
+                best = steps;
                 split = d;
+            }
+        }
         a.ksplit = split;
         a.out_kstride = (int64_t)T * L.E;
         nsplit = split;
