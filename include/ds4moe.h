@@ -285,6 +285,17 @@ int ds4moe_route_detail(ds4moe_t *h, const void *x_bf16, int32_t T, int32_t *idx
 /* Synchronise the handle's stream; return and clear the sticky device error. */
 int ds4moe_status(ds4moe_t *h);
 
+/*
+ * Test hook for the failure detection of the persistent kernels: in each of
+ * the next `launches` product launches of the batch path (DS4MOE_PATH_BATCH),
+ * CTA 0 issues nothing for its first ring stage, so the bounded waits on that
+ * stage run out (about a second), the CTA's roles stop and drain their own
+ * copies, and ds4moe_status then returns DS4MOE_ETIMEOUT; the device and the
+ * handle stay usable, the outputs of those calls are undefined. 0 turns it off.
+ * Errors: EINVAL (NULL handle, launches < 0).
+ */
+int ds4moe_debug_skip_signal(ds4moe_t *h, int32_t launches);
+
 /* Statistics of the last forward call (read after ds4moe_status). */
 typedef struct {
     int32_t tokens;        /* T of the last call */

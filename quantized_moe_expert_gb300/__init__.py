@@ -68,6 +68,7 @@ SIGNATURES = {
     "ds4moe_forward_routed": (ctypes.c_int, [_vp, _vp, _i32, _vp, _vp, _i32, _vp]),
     "ds4moe_route_detail": (ctypes.c_int, [_vp, _vp, _i32, _vp, _vp, _vp, _vp]),
     "ds4moe_status": (ctypes.c_int, [_vp]),
+    "ds4moe_debug_skip_signal": (ctypes.c_int, [_vp, _i32]),
     "ds4moe_get_stats": (ctypes.c_int, [_vp, ctypes.POINTER(Stats)]),
     "ds4moe_inspect": (ctypes.c_int, [_vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.POINTER(_i32)]),
     "ds4moe_memory": (ctypes.c_int, [_vp, ctypes.POINTER(ctypes.c_uint64), ctypes.POINTER(ctypes.c_uint64)]),
@@ -156,6 +157,10 @@ def ds4moe_forward_host(h: int, x_host, T: int, y_host):
 
 def ds4moe_status(h: int) -> int:
     return int(_lib.ds4moe_status(h))
+
+
+def ds4moe_debug_skip_signal(h: int, launches: int):
+    _check(_lib.ds4moe_debug_skip_signal(h, launches), "ds4moe_debug_skip_signal")
 
 
 def ds4moe_get_stats(h: int) -> Stats:

@@ -64,6 +64,8 @@ struct BatchArgs {
     const int32_t *perm;     // grouped position -> pair t * K + k
     int nstage;              // stages in each CTA's ring
     int chunk;               // columns per stage of the 8-bit products
+    int skip_signal;         // test hook: CTA 0's producer issues nothing for its first stage, so that
+                             // stage's bounded waits run out (kErrTimeout) and every role stops
     unsigned *status;
 };
 
@@ -447,7 +449,9 @@ __global__ void __launch_bounds__(kBatchThreads, 1) batch_product_kernel(const B
                 }
                 uint64_t *bar = full + q % ns;
                 uint8_t *dst = sm + (q % ns) * pl.stage_bytes;
-                if (routed(c)) {
+                if (a.skip_signal && blockIdx.x == 0 && q == 0) {
+                    // nothing arrives on this stage's barrier
+                } else if (routed(c)) {
                     const int64_t e = a.vslot[c.v].x;
                     batch_expect(bar, (unsigned)(DOWN ? 4 : 2) * pl.mat2);
                     if (DOWN) {

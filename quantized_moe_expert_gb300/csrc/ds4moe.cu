@@ -139,6 +139,7 @@ struct ds4moe {
     uint64_t scratch_bytes = 0;
     ds4moe_stats stats{};
     bool has_gain[2] = {false, false};
+    int skip_signal = 0; // test hook: batch product launches still to skip one stage's signal
 };
 
 namespace {
@@ -817,6 +818,9 @@ int run_experts_batch(ds4moe *h, const void *x, int T, float *y, bool x_prepared
     auto product = [&](int mode, const char *name, void (*fn)(BatchArgs)) {
         a.nstage = B.nstage[mode];
         a.chunk = B.chunk[mode];
+        a.skip_signal = h->skip_signal > 0;
+        if (h->skip_signal > 0)
+            h->skip_signal--;
         launch(h, name, [&] { launch_pdl(fn, dim3(B.grid), dim3(kBatchThreads), B.smem[mode], st, a); });
     };
     // few tokens: one launch per product over both kinds of items (the shared expert fills the
@@ -1626,6 +1630,13 @@ int ds4moe_forward_host(ds4moe_t *h, const void *x_host, int32_t T, float *y_hos
     if (rc)
         return rc;
     return cuda_rc(cudaStreamSynchronize(st));
+}
+
+int ds4moe_debug_skip_signal(ds4moe_t *h, int32_t launches) {
+    if (!h || launches < 0)
+        return DS4MOE_EINVAL;
+    h->skip_signal = launches;
+    return DS4MOE_OK;
 }
 
 int ds4moe_status(ds4moe_t *h) {

@@ -177,3 +177,24 @@ def test_batch_full_layer(big, T):
     assert np.isfinite(y).all()
     assert s.n_unique == len(np.unique(r["idx"]))
     assert moe.status() == 0
+
+
+def test_a_bounded_wait_that_runs_out_is_reported(tiny):
+    """Failure detection without a GPU fault: a test hook makes CTA 0 of the next
+    batch product launch issue nothing for its first stage. Its waits give up
+    after about a second, every role of the CTA stops and drains its own copies,
+    ds4moe_status returns DS4MOE_ETIMEOUT, and the next call on the same handle
+    is right again."""
+    shape, layer, moe = tiny
+    x = tokens(shape, 8, 3700)
+    xd = x_to_dev(x)
+    ds4.ds4moe_debug_skip_signal(moe.handle, 1)
+    moe.forward(xd, path=ds4.PATH_BATCH)
+    assert moe.status() == ds4.DS4MOE_ETIMEOUT
+    y = moe.forward(xd, path=ds4.PATH_BATCH).cpu().numpy()
+    r = moe.inspect(8, grouping=False)
+    y_ref = oracle.forward_routed(shape, layer, x, r["idx"], r["w"].astype(np.float64))
+    assert_close(y, y_ref, TOL_DECODE)
+    assert moe.status() == 0
+    with pytest.raises(ds4.DS4MoEError):
+        ds4.ds4moe_debug_skip_signal(moe.handle, -1)
