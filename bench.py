@@ -135,8 +135,8 @@ TRAFFIC = {
     # mean of two launches
     ("decode_fused", "decode_t1"): (83569152, "decode_fused.cuh", "e72c292f502930ae0475e19e48ff689409d3a399"),
     # one launch, a batch of the pool with about 46 distinct experts (the traffic follows the batch's experts)
-    ("batch_gateup", "decode_t8"): (256792064, "batch_experts.cuh", "1a43797efb490c1ae6771547950806630f0c4bda"),
-    ("batch_gateup", "batch_t64"): (1363536896, "batch_experts.cuh", "1a43797efb490c1ae6771547950806630f0c4bda"),
+    ("batch_gateup", "decode_t8"): (256490752, "batch_experts.cuh", "03b7b0fabb2eb84ea263c524d2264b2f9fa4a45c"),
+    ("batch_gateup", "batch_t64"): (1363641344, "batch_experts.cuh", "03b7b0fabb2eb84ea263c524d2264b2f9fa4a45c"),
 }
 
 
