@@ -137,21 +137,38 @@ __global__ void combine_kernel(const float *ye, const float *ysh,
         return;
     const int t = (int)((i4 * 4) / H);
     const int j = (int)((i4 * 4) % H);
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int k = 0; k < K; k++) {
-        const float wk = w[(int64_t)t * K + k];
-        float4 v = *reinterpret_cast<const float4 *>(ye + (int64_t)inv[(int64_t)t * K + k] * H + j);
-        if (g) {
-            const float4 s = __ldg(reinterpret_cast<const float4 *>(g + (int64_t)idx[(int64_t)t * K + k] * H + j));
-            v.x *= s.x;
-            v.y *= s.y;
-            v.z *= s.z;
-            v.w *= s.w;
+    // every pair's row loaded first (up to kMaxTopK loads in flight), then summed in k order
+    float wk[kMaxTopK];
+    float4 v[kMaxTopK];
+#pragma unroll
+    for (int k = 0; k < kMaxTopK; k++) {
+        if (k < K) {
+            wk[k] = w[(int64_t)t * K + k];
+            v[k] = *reinterpret_cast<const float4 *>(ye + (int64_t)inv[(int64_t)t * K + k] * H + j);
         }
-        acc.x = fmaf(wk, v.x, acc.x);
-        acc.y = fmaf(wk, v.y, acc.y);
-        acc.z = fmaf(wk, v.z, acc.z);
-        acc.w = fmaf(wk, v.w, acc.w);
+    }
+    if (g) {
+#pragma unroll
+        for (int k = 0; k < kMaxTopK; k++) {
+            if (k < K) {
+                const float4 s =
+                    __ldg(reinterpret_cast<const float4 *>(g + (int64_t)idx[(int64_t)t * K + k] * H + j));
+                v[k].x *= s.x;
+                v[k].y *= s.y;
+                v[k].z *= s.z;
+                v[k].w *= s.w;
+            }
+        }
+    }
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int k = 0; k < kMaxTopK; k++) {
+        if (k < K) {
+            acc.x = fmaf(wk[k], v[k].x, acc.x);
+            acc.y = fmaf(wk[k], v[k].y, acc.y);
+            acc.z = fmaf(wk[k], v[k].z, acc.z);
+            acc.w = fmaf(wk[k], v[k].w, acc.w);
+        }
     }
     if (ysh) {
         const float4 s = *reinterpret_cast<const float4 *>(ysh + (int64_t)t * H + j);
