@@ -19,11 +19,6 @@
 namespace ds4 {
 namespace umma {
 
-// Byte offset of (row r, 16-byte chunk c) in a K-major 128-byte-swizzled tile.
-__host__ __device__ __forceinline__ uint32_t sw128_offset(uint32_t r, uint32_t c) {
-    return r * 128u + ((c ^ (r & 7u)) << 4);
-}
-
 // Shared-memory matrix descriptor (64 bits):
 //   [0,14)  start address >> 4      [16,30) leading-dimension byte offset >> 4
 //   [32,46) stride-dimension byte offset >> 4   [46,48) version = 1
@@ -72,21 +67,6 @@ __device__ __forceinline__ void fence_after_sync() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// Generic-proxy shared-memory writes made visible to the tensor core (async proxy).
-__device__ __forceinline__ void fence_smem_to_async() {
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
-// One thread: D[tmem] (+)= A * B^T for one K=16 step.
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                         bool accumulate) {
-    asm volatile("{\n\t.reg .pred p;\n\t"
-                 "setp.ne.b32 p, %4, 0;\n\t"
-                 "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-                 "l"(a_desc), "l"(b_desc), "r"(idesc), "r"((uint32_t)accumulate)
-                 : "memory");
-}
-
 // One thread: the mbarrier gets one arrival when all MMAs issued so far by
 // this thread have completed.
 __device__ __forceinline__ void commit(uint64_t *bar) {
@@ -95,18 +75,8 @@ __device__ __forceinline__ void commit(uint64_t *bar) {
                  : "memory");
 }
 
-// Warp-wide: 32 lanes x 16 columns of 32-bit TMEM starting at taddr (lane
+// Warp-wide: 32 lanes x 8 columns of 32-bit TMEM starting at taddr (lane
 // field = the warp's lane quarter base). Thread i receives lane base + i.
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
-    asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, "
-                 "[%16];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-                   "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
-                   "=r"(r[15])
-                 : "r"(taddr));
-}
-
-// Warp-wide: 32 lanes x 8 columns.
 __device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
     asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
                  : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
