@@ -1,7 +1,7 @@
 // tcgen05 (5th-generation tensor core) building blocks for sm_100-family GPUs,
 // written from the PTX ISA: shared-memory matrix descriptors, the instruction
-// descriptor of kind::f16, TMEM allocation, MMA issue, commit to an mbarrier
-// and TMEM loads.
+// descriptors of kind::f16, TMEM allocation, the tcgen05 fences, commit to an
+// mbarrier and TMEM loads (the grouped GEMM issues its MMAs with A in TMEM).
 //
 // Operand layout used everywhere here: K-major tiles with the 128-byte
 // swizzle. A tile of R rows x 64 bf16 columns occupies R * 128 bytes; row r
