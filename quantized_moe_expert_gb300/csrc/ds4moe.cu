@@ -728,9 +728,9 @@ int run_experts_prefill(ds4moe *h, const void *x, int T, float *y) {
     if (rc)
         return rc;
     launch(h, "plan_groups", [&] {
-        launch_pdl(pf::plan_groups_kernel, dim3(1), dim3(1024), 0, st, S.uexp, S.uoff, S.nuniq, pf::Cfg<pf::kFmtQ2,
-                   2>::kNMax, S.grp_gu, S.ngrp,
-                                                     pf::Cfg<pf::kFmtQ2, 1>::kNMax, S.grp_dn, S.ngrp + 1);
+        launch_pdl(pf::plan_groups_kernel, dim3(1), dim3(1024), 0, st, S.uexp, S.uoff, S.nuniq,
+                   pf::Cfg<pf::kFmtQ2, 2>::kNMax, S.grp_gu, S.ngrp, pf::Cfg<pf::kFmtQ2, 1>::kNMax, S.grp_dn,
+                   S.ngrp + 1);
     });
     launch(h, "gather_rows", [&] {
         launch_pdl(pf::gather_rows_kernel, dim3(T * L.K), dim3(256), 0, st, static_cast<const uint16_t *>(x), S.perm,
@@ -906,14 +906,13 @@ int run_experts_mx4_tc(ds4moe *h, const void *x, int T, float *y) {
     if (rc)
         return rc;
     launch(h, "plan_groups", [&] {
-        launch_pdl(pf::plan_groups_kernel, dim3(1), dim3(1024), 0, st, S.uexp, S.uoff, S.nuniq, pf::Cfg<pf::kFmtMx4,
-                   2>::kNMax, S.grp_gu,
-                                                     S.ngrp, pf::Cfg<pf::kFmtMx4, 1>::kNMax, S.grp_dn, S.ngrp + 1);
+        launch_pdl(pf::plan_groups_kernel, dim3(1), dim3(1024), 0, st, S.uexp, S.uoff, S.nuniq,
+                   pf::Cfg<pf::kFmtMx4, 2>::kNMax, S.grp_gu, S.ngrp, pf::Cfg<pf::kFmtMx4, 1>::kNMax, S.grp_dn,
+                   S.ngrp + 1);
     });
     launch(h, "mx4_act_fp4", [&] {
         launch_pdl(act_fp4_kernel, dim3(blocks_for((int64_t)T * L.H / 8, 256)), dim3(256), 0, st,
-                   static_cast<const uint16_t *>(x),
-                                                                          (int64_t)T * L.H, S.x4);
+                   static_cast<const uint16_t *>(x), (int64_t)T * L.H, S.x4);
     });
     launch(h, "gather_rows", [&] {
         launch_pdl(pf::gather_rows_kernel, dim3(T * L.K), dim3(256), 0, st, S.x4, S.perm, L.K, L.H, S.xp);
@@ -963,17 +962,13 @@ int run_experts_vq_tc(ds4moe *h, const void *x, int T, float *y) {
     if (rc)
         return rc;
     launch(h, "plan_groups", [&] {
-        launch_pdl(pf::plan_groups_kernel, dim3(1), dim3(1024), 0, st, S.uexp, S.uoff, S.nuniq, pf::Cfg<pf::kFmtVq,
-                   2>::kNMax, S.grp_gu,
-                                                     S.ngrp, pf::Cfg<pf::kFmtVq, 1>::kNMax, S.grp_dn, S.ngrp + 1);
+        launch_pdl(pf::plan_groups_kernel, dim3(1), dim3(1024), 0, st, S.uexp, S.uoff, S.nuniq,
+                   pf::Cfg<pf::kFmtVq, 2>::kNMax, S.grp_gu, S.ngrp, pf::Cfg<pf::kFmtVq, 1>::kNMax, S.grp_dn,
+                   S.ngrp + 1);
     });
-    launch(h, "vq_x_f16", [&] {
-        launch_pdl(bf16_to_f16_kernel, dim3(blocks_for((int64_t)T * L.H / 8, 256)), dim3(256), 0, st,
-                   static_cast<const uint16_t *>(x),
-                                                                              (int64_t)T * L.H, S.x4);
-    });
-    launch(h, "gather_rows", [&] {
-        launch_pdl(pf::gather_rows_kernel, dim3(T * L.K), dim3(256), 0, st, S.x4, S.perm, L.K, L.H, S.xp);
+    launch(h, "gather_rows_f16", [&] {
+        launch_pdl(gather_rows_f16_kernel, dim3(T * L.K), dim3(256), 0, st, static_cast<const uint16_t *>(x), S.perm,
+                   L.K, L.H, S.xp);
     });
     pf::Args a{};
     a.status = h->status;
@@ -1030,8 +1025,7 @@ int run_experts_vq(ds4moe *h, const void *x, int T, float *y) {
     const size_t smem = (size_t)8 << L.vq;
     launch(h, "vq_widen_x", [&] {
         launch_pdl(widen_bf16_kernel, dim3(blocks_for((int64_t)T * L.H / 8, 256)), dim3(256), 0, st,
-                   static_cast<const uint16_t *>(x),
-                                                                              (int64_t)T * L.H, S.ax);
+                   static_cast<const uint16_t *>(x), (int64_t)T * L.H, S.ax);
     });
     launch(h, "vq_gateup", [&] {
         const int work = U * ((L.I + 7) / 8);

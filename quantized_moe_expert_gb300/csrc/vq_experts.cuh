@@ -75,6 +75,23 @@ __global__ void bf16_to_f16_kernel(const uint16_t *x, int64_t n, uint16_t *out) 
     }
 }
 
+// B rows of the VQ tensor-core form's routed gate/up in expert-grouped order,
+// as binary16: xp[pos] = bf16x2_to_f16x2_sat(x[perm[pos] / K]); one CTA per row,
+// 8 values per thread (H a multiple of 8, both arrays 16-byte aligned).
+__global__ void gather_rows_f16_kernel(const uint16_t *x, const int32_t *perm, int K, int H, uint16_t *xp) {
+    pdl_launch_next();
+    pdl_wait();
+    const int pos = blockIdx.x;
+    const int t = perm[pos] / K;
+    const uint4 *src = reinterpret_cast<const uint4 *>(x + (int64_t)t * H);
+    uint4 *dst = reinterpret_cast<uint4 *>(xp + (int64_t)pos * H);
+    for (int c = threadIdx.x; c < H / 8; c += blockDim.x) {
+        const uint4 v = src[c];
+        dst[c] = make_uint4(bf16x2_to_f16x2_sat(v.x), bf16x2_to_f16x2_sat(v.y), bf16x2_to_f16x2_sat(v.z),
+                            bf16x2_to_f16x2_sat(v.w));
+    }
+}
+
 // bf16 rows -> fp32 (exact). A thread per 8 values: n is a multiple of 8 and
 // both arrays 16-byte aligned.
 __global__ void widen_bf16_kernel(const uint16_t *x, int64_t n, float *out) {
