@@ -226,3 +226,19 @@ def test_router_bias_changes_selection_only():
     y_ref = oracle.forward_routed(shape, layer, x, ref["idx"], ref["weights"])
     assert_close(y, y_ref, TOL_DECODE)
     moe.close()
+
+
+def test_memory_counts_every_resident_layout(tiny):
+    """ds4moe_memory's weight bytes: the router (fp32 rows, their three bf16 parts
+    padded to 128 rows, the bias), the routed experts in both resident layouts
+    (84 B per 256 weights each) and the shared expert in both (34 B per 32
+    weights each), plus at most the pieces' 256-byte alignment."""
+    shape, layer, moe = tiny
+    H, I, E, Ish = shape.hidden, shape.inter, shape.n_experts, shape.shared_inter
+    router = E * H * 4 + -(-E // 128) * 128 * 3 * H * 2 + E * 4
+    routed = 3 * E * I * H * 84 // 256
+    shared = 3 * Ish * H * 34 // 32
+    expected = router + 2 * routed + 2 * shared
+    wb, sb = ds4.ds4moe_memory(moe.handle)
+    assert expected <= wb <= expected + 64 * 1024, (wb, expected)
+    assert sb > 0
