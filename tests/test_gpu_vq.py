@@ -173,3 +173,27 @@ def test_full_size_automatic_form_t1_and_t8(big):
         y_ref = oracle.forward_routed(shape, layer, x, r["idx"], r["w"].astype(np.float64))
         assert_close(y, y_ref, TOL_PREFILL)
     assert moe.status() == 0
+
+
+def test_full_size_vq13_both_forms():
+    """H=4096, E=384 VQ-13 layer (the 12-bit stream plus the bit plane): the
+    eight-token batch on the tensor-core form (the automatic one) and on the
+    CUDA-core form, each at its bound, on the library's routing."""
+    wl = synth.WORKLOADS["decode_t1"]
+    layer = synth.make_layer(wl.shape, wl.layer_seeds[0], routed_format="vq", vq_bits=13)
+    dev = to_dev(layer)
+    moe = ds4.MoELayer(wl.shape, dev, max_tokens=8, flags=ds4.FLAG_VQ13)
+    del dev
+    torch.cuda.empty_cache()
+    try:
+        shape = wl.shape
+        x = synth.make_tokens("decode_t8")
+        for path, tol in ((ds4.PATH_AUTO, TOL_PREFILL), (ds4.PATH_DECODE, TOL_DECODE)):
+            y = moe.forward(x_to_dev(x), path=path).cpu().numpy()
+            r = moe.inspect(8, grouping=False)
+            check_routing(r["idx"], r["w"], r["gap"], oracle.route(shape, layer["router_w"], None, x), shape.top_k)
+            y_ref = oracle.forward_routed(shape, layer, x, r["idx"], r["w"].astype(np.float64))
+            assert_close(y, y_ref, tol)
+        assert moe.status() == 0
+    finally:
+        moe.close()
