@@ -17,7 +17,7 @@ import torch
 import oracle
 import quantized_moe_expert_gb300 as ds4
 import synth
-from gpu_util import TOL_DECODE, assert_close, check_routing, to_dev, x_to_dev
+from gpu_util import TOL_DECODE, TOL_PREFILL, assert_close, check_routing, to_dev, x_to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -198,3 +198,32 @@ def test_a_bounded_wait_that_runs_out_is_reported(tiny):
     assert moe.status() == 0
     with pytest.raises(ds4.DS4MoEError):
         ds4.ds4moe_debug_skip_signal(moe.handle, -1)
+
+
+def test_wide_layer_without_a_batch_plan():
+    """H=8192: a 2-bit stage of the batch kernel (two 16-row tiles over the whole
+    row) does not fit its shared memory, so the layer has no batch path: an
+    explicit batch call is refused, the automatic path takes the prefill path
+    (shared expert on its GEMMs), and the decode kernel streams the wide rows in
+    K chunks; both match the oracle."""
+    shape = synth.Shape(8192, 256, 8, 2, 256)
+    layer = synth.make_layer(shape, synth.SEED_BASE + 50)
+    moe = ds4.MoELayer(shape, to_dev(layer), max_tokens=16)
+    try:
+        T = 9
+        x = tokens(shape, T, 3800)
+        xd = x_to_dev(x)
+        y = torch.empty((T, shape.hidden), dtype=torch.float32, device="cuda")
+        with pytest.raises(ds4.DS4MoEError) as e:
+            ds4.ds4moe_forward_path(moe.handle, xd, T, ds4.PATH_BATCH, y)
+        assert e.value.code == ds4.DS4MOE_EINVAL
+        for path, want, tol in ((ds4.PATH_AUTO, ds4.PATH_PREFILL, TOL_PREFILL),
+                                (ds4.PATH_DECODE, ds4.PATH_DECODE, TOL_DECODE)):
+            yy = moe.forward(xd, path=path).cpu().numpy()
+            assert moe.stats().path == want
+            r = moe.inspect(T, grouping=False)
+            y_ref = oracle.forward_routed(shape, layer, x, r["idx"], r["w"].astype(np.float64))
+            assert_close(yy, y_ref, tol)
+        assert moe.status() == 0
+    finally:
+        moe.close()
