@@ -132,6 +132,9 @@ def kernel_bytes(name, shape, T, U, gains=0, fmt="q2"):
 TRAFFIC = {
     ("prefill_gateup_q2", "prefill_t1024"): (2188350208, "prefill_gemm.cuh", "c4d8d4b85ae902ac97cf5595672432168c7c5ec7"),
     ("prefill_down_q2", "prefill_t1024"): (1174632192, "prefill_gemm.cuh", "c4d8d4b85ae902ac97cf5595672432168c7c5ec7"),
+    # mean of the four Zipf layers' launches
+    ("prefill_gateup_q2", "prefill_t4096_zipf4"): (2425953536, "prefill_gemm.cuh",
+                                                   "c4d8d4b85ae902ac97cf5595672432168c7c5ec7"),
     # mean of two launches
     ("decode_fused", "decode_t1"): (83569152, "decode_fused.cuh", "e72c292f502930ae0475e19e48ff689409d3a399"),
     # one launch, a batch of the pool with about 46 distinct experts (the traffic follows the batch's experts)
